@@ -1,0 +1,356 @@
+"""fp64 CPU oracle for paged GQA decode, block scoring, tiering, selection,
+gather and identity-keyed re-admission.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  It shares no code with
+the CUDA library (it never imports it, nor its header) and reads its inputs
+from the seeded generators in ``workloads``.
+
+Attention and block mass are the plain definitions in ``kvs_oracle.c``.  The
+scoring, tiering, selection, page assembly and demote/readmit bookkeeping are
+written here with numpy, in fp64, each operation in the order stated in its
+docstring.
+
+Sources (page titles and sections):
+  [VA]  "KV-Cache Offloading for LLM Inference -- Visual Reference" (v6.0):
+        s.3 KV-cache size formula; s.11 EMA update rule, Diagram 11.2 worked
+        example and half-life; s.12 priority P and tier thresholds.
+  [GQA] "GQA per-head attention as scoring streams" figure page: 640
+        streams aggregated into one score per (sequence, 16-token block);
+        64-byte per-block record; identity key and score persist across
+        eviction and are restored on re-admission.
+  [ARCH] "LLM KV cache offload" architecture page: block manager, block
+        tables, reference counts for shared blocks, pinned-host staging.
+  [RETR] "RETRACTIONS": s.3 brute-force argmin audit of victim selection.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_BUILD = _HERE / "_build"
+_SO = _BUILD / "liboracle.so"
+_lib = None
+
+# ---------------------------------------------------------------------------
+# build / load
+# ---------------------------------------------------------------------------
+
+
+def build(force: bool = False) -> Path:
+    """Compile kvs_oracle.c into a shared library (gcc, IEEE fp64 order)."""
+    src = _HERE / "kvs_oracle.c"
+    _BUILD.mkdir(exist_ok=True)
+    if force or not _SO.exists() or _SO.stat().st_mtime < src.stat().st_mtime:
+        tmp = _SO.with_suffix(f".tmp{os.getpid()}.so")
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-pthread", str(src), "-o", str(tmp), "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(str(_SO))
+        P = ctypes.c_void_p
+        lib.orc_decode_heads.argtypes = [
+            P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, P, P, P]
+        lib.orc_decode_heads.restype = ctypes.c_int
+        lib.orc_aggregate_mass.argtypes = [P, ctypes.c_int64, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, P]
+        lib.orc_aggregate_mass.restype = None
+        lib.orc_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.orc_bf16_to_f64.restype = ctypes.c_double
+        _lib = lib
+    return _lib
+
+
+def _u16(x) -> np.ndarray:
+    """bf16 tensor (torch) or uint16 bit array (numpy) -> contiguous uint16."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16
+        return np.ascontiguousarray(x)
+    import torch  # plain CPU conversion of the bit pattern only
+    assert x.dtype == torch.bfloat16
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else None
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float64."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# attention and block mass (C)
+# ---------------------------------------------------------------------------
+
+
+def decode(q, K, V, *, L, Hq, Hkv, d, block_tokens=16, heads=None,
+           threads=None, want_out=True, want_head_mass=True):
+    """Decode attention of one sequence.
+
+    q: [L][Hq][d] bf16; K, V: [n][L][Hkv][d] bf16 in logical token order.
+    heads: iterable of flat l*Hq+h indices (None = all, in order).
+    Returns dict(out [nh][d], lse [nh], head_mass [nh][nb] or None).
+    """
+    lib = _load()
+    qb, kb, vb = _u16(q), _u16(K), _u16(V)
+    n = kb.shape[0]
+    assert qb.shape == (L, Hq, d) and kb.shape == (n, L, Hkv, d) and vb.shape == kb.shape
+    nb = (n + block_tokens - 1) // block_tokens
+    hl = None if heads is None else np.ascontiguousarray(np.asarray(heads, dtype=np.int32))
+    nh = L * Hq if hl is None else len(hl)
+    out = np.zeros((nh, d), np.float64) if want_out else None
+    lse = np.zeros(nh, np.float64)
+    hm = np.zeros((nh, nb), np.float64) if want_head_mass else None
+    rc = lib.orc_decode_heads(_ptr(qb), _ptr(kb), _ptr(vb), n, L, Hq, Hkv, d,
+                              block_tokens, _ptr(hl) if hl is not None else None,
+                              nh, int(threads or os.cpu_count() or 1),
+                              _ptr(out), _ptr(lse), _ptr(hm))
+    if rc != 0:
+        raise RuntimeError("oracle decode failed (bad argument or out of memory)")
+    return {"out": out, "lse": lse, "head_mass": hm}
+
+
+def aggregate_mass(head_mass: np.ndarray, *, L, Hq, Hkv) -> np.ndarray:
+    """M(b) from all L*Hq per-head block masses [L*Hq][nb] ([GQA] s.2)."""
+    lib = _load()
+    hm = np.ascontiguousarray(head_mass, dtype=np.float64)
+    assert hm.shape[0] == L * Hq
+    nb = hm.shape[1]
+    mass = np.zeros(nb, np.float64)
+    lib.orc_aggregate_mass(_ptr(hm), nb, L, Hq, Hkv, _ptr(mass))
+    return mass
+
+
+def decode_with_mass(q, K, V, *, L, Hq, Hkv, d, block_tokens=16, threads=None,
+                     want_out=True):
+    """All heads of one sequence: out [L][Hq][d], lse [L][Hq], mass [nb]."""
+    r = decode(q, K, V, L=L, Hq=Hq, Hkv=Hkv, d=d, block_tokens=block_tokens,
+               threads=threads, want_out=want_out, want_head_mass=True)
+    mass = aggregate_mass(r["head_mass"], L=L, Hq=Hq, Hkv=Hkv)
+    return {
+        "out": None if r["out"] is None else r["out"].reshape(L, Hq, d),
+        "lse": r["lse"].reshape(L, Hq),
+        "head_mass": r["head_mass"],
+        "mass": mass,
+    }
+
+
+# ---------------------------------------------------------------------------
+# 64-byte per-block record ([GQA]: 16 B identity key, 8 B score, 8 B touch
+# timestamp, 4 B touch count, reserved).  The reserved bytes carry the tier,
+# the last priority and the last mass so that every step can be compared.
+# ---------------------------------------------------------------------------
+
+REC_DTYPE = np.dtype({
+    "names": ["seq_id", "block_idx", "score", "last_touch", "count", "tier",
+              "flags", "pad0", "prio", "mass", "rsv"],
+    "formats": ["<u8", "<u8", "<f8", "<u8", "<u4", "u1", "u1", "<u2", "<f8",
+                "<f4", ("u1", 12)],
+    "offsets": [0, 8, 16, 24, 32, 36, 37, 38, 40, 48, 52],
+    "itemsize": 64,
+})
+TIER_UNSCORED = 255
+
+
+def new_records(seq_id: int, first_block: int, count: int, t_create: int) -> np.ndarray:
+    """Records of freshly opened blocks: score 0 (the worked example of [VA]
+    Diagram 11.2 starts from 0), last touch = creation step, count 0."""
+    r = np.zeros(count, REC_DTYPE)
+    r["seq_id"] = seq_id
+    r["block_idx"] = np.arange(first_block, first_block + count, dtype=np.uint64)
+    r["last_touch"] = t_create
+    r["tier"] = TIER_UNSCORED
+    return r
+
+
+def ema(prev: np.ndarray, attn: np.ndarray, alpha: float) -> np.ndarray:
+    """[VA] s.11: score_t = alpha*attention_t + (1-alpha)*score_{t-1}.
+    Evaluated as (alpha*attn) + ((1.0-alpha)*prev) in fp64."""
+    a = np.float64(alpha)
+    return a * np.asarray(attn, np.float64) + (np.float64(1.0) - a) * np.asarray(prev, np.float64)
+
+
+def recency(t: int, last_touch: np.ndarray, W: int) -> np.ndarray:
+    """R = 1 - (t - last_touch)/W, clipped to [0, 1]: 1.0 - (age / W)."""
+    age = (np.int64(t) - np.asarray(last_touch, np.int64)).astype(np.float64)
+    r = np.float64(1.0) - age / np.float64(W)
+    return np.minimum(np.maximum(r, 0.0), 1.0)
+
+
+def priority(R, E, N, weights=(0.25, 0.55, 0.20)) -> np.ndarray:
+    """[VA] s.12: P = 0.25*R + 0.55*E + 0.20*N, summed left to right."""
+    wR, wE, wN = (np.float64(w) for w in weights)
+    return (wR * np.asarray(R, np.float64) + wE * np.asarray(E, np.float64)) + wN * np.asarray(N, np.float64)
+
+
+def tier_of(P, cuts=(0.3, 0.6)) -> np.ndarray:
+    """[VA] Diagram 12.2, boundaries half-open: P < 0.3 -> 2 (lowest tier),
+    0.3 <= P < 0.6 -> 1, P >= 0.6 -> 0 (pinned)."""
+    lo, hi = np.float64(cuts[0]), np.float64(cuts[1])
+    P = np.asarray(P, np.float64)
+    return np.where(P >= hi, 0, np.where(P >= lo, 1, 2)).astype(np.uint8)
+
+
+def score_update(rec: np.ndarray, mass: np.ndarray, t: int, alpha: float,
+                 W: int = 64, weights=(0.25, 0.55, 0.20), cuts=(0.3, 0.6)) -> np.ndarray:
+    """One scoring step over the nb records (block order) of one sequence.
+
+    mass: the step's M(b), float64 (or float32, widened exactly).
+    Order: EMA -> touch (mass >= 1/num_blocks: M*nb >= 1, count += 1,
+    last_touch = t) -> recency R -> anchor N (block 0 and the newest block)
+    -> P -> tier.  Returns a new record array.
+    """
+    r = rec.copy()
+    nb = len(r)
+    M = np.asarray(mass, dtype=np.float64)
+    assert M.shape == (nb,)
+    r["score"] = ema(r["score"], M, alpha)
+    touched = M * np.float64(nb) >= 1.0
+    r["count"] = r["count"] + touched.astype(np.uint32)
+    r["last_touch"] = np.where(touched, np.uint64(t), r["last_touch"])
+    R = recency(t, r["last_touch"], W)
+    N = np.zeros(nb, np.float64)
+    if nb:
+        N[0] = 1.0
+        N[nb - 1] = 1.0
+    P = priority(R, r["score"], N, weights)
+    r["prio"] = P
+    r["tier"] = tier_of(P, cuts)
+    r["mass"] = M.astype(np.float32)
+    return r
+
+
+# ---------------------------------------------------------------------------
+# selection ([VA] s.12 tiers; [RETR] s.3 brute-force audit)
+# ---------------------------------------------------------------------------
+
+
+def _ordered(recs_by_seq: dict) -> np.ndarray:
+    """All records in ascending (seq_id, block_idx) order."""
+    parts = [recs_by_seq[s] for s in sorted(recs_by_seq)]
+    return np.concatenate(parts) if parts else np.zeros(0, REC_DTYPE)
+
+
+def select_thresh(recs_by_seq: dict) -> list:
+    """Every record in the lowest tier (P < 0.3), ascending (seq_id, block_idx)."""
+    allr = _ordered(recs_by_seq)
+    pick = allr["tier"] == 2
+    return [(int(a), int(b)) for a, b in zip(allr["seq_id"][pick], allr["block_idx"][pick])]
+
+
+def lowfrac_k(n_records: int, frac: float) -> int:
+    return int(math.floor(np.float64(frac) * np.float64(n_records)))
+
+
+def select_lowfrac(recs_by_seq: dict, frac: float) -> list:
+    """The k = floor(frac*N) records of smallest P, ties broken by
+    (seq_id, block_idx); returned in ascending (seq_id, block_idx) order.
+    Plain full sort of every record."""
+    allr = _ordered(recs_by_seq)
+    k = lowfrac_k(len(allr), frac)
+    order = sorted(range(len(allr)), key=lambda i: (float(allr["prio"][i]), i))
+    chosen = sorted(order[:k])
+    return [(int(allr["seq_id"][i]), int(allr["block_idx"][i])) for i in chosen]
+
+
+# ---------------------------------------------------------------------------
+# page assembly and gather ([ARCH]: one block = one page of all layers and
+# KV heads, laid out contiguously for coalesced transfer)
+# ---------------------------------------------------------------------------
+
+
+def assemble_page(K_blk, V_blk, block_tokens: int = 16) -> bytes:
+    """Bytes of one page from the logical K, V of its t <= block_tokens
+    tokens ([t][L][Hkv][d] bf16 each).
+
+    Layout, outermost first: layer, {K, V}, KV head, token slot, head dim;
+    bf16 little-endian; slots past the last token are zero.
+    """
+    kb, vb = _u16(K_blk), _u16(V_blk)
+    t, L, Hkv, d = kb.shape
+    assert t <= block_tokens and vb.shape == kb.shape
+    page = np.zeros((L, 2, Hkv, block_tokens, d), np.uint16)
+    page[:, 0, :, :t, :] = kb.transpose(1, 2, 0, 3)
+    page[:, 1, :, :t, :] = vb.transpose(1, 2, 0, 3)
+    return page.tobytes()
+
+
+def gather_plan(selected: list, page_of: dict, refs_of: dict) -> list:
+    """Pages to gather for a selected list of (seq_id, block_idx) keys.
+
+    page_of[key] -> page identity; refs_of[page] -> set of keys referencing
+    it.  A page is gathered when every record referencing it is selected
+    (a shared block is released only by its last user, [ARCH] reference
+    counts), once, at the position of its first selected record.
+    Returns the page identities in gather order.
+    """
+    sel = set(selected)
+    seen, plan = set(), []
+    for key in selected:
+        p = page_of[key]
+        if p in seen:
+            continue
+        if refs_of[p] <= sel:
+            plan.append(p)
+            seen.add(p)
+    return plan
+
+
+# ---------------------------------------------------------------------------
+# identity-keyed demote / readmit ([GQA]: identity key and score persist and
+# are restored on re-admission rather than reset)
+# ---------------------------------------------------------------------------
+
+
+class IdentityStore:
+    """Key (seq_id, block_idx) -> (64-byte record, page bytes)."""
+
+    def __init__(self):
+        self._m = {}
+
+    def demote(self, key, record: np.ndarray, page: bytes):
+        if key in self._m:
+            raise KeyError(f"{key} already demoted")
+        self._m[key] = (record.copy(), bytes(page))
+
+    def readmit(self, key):
+        if key not in self._m:
+            raise KeyError(f"{key} not demoted")
+        return self._m.pop(key)
+
+    def __contains__(self, key):
+        return key in self._m
+
+    def __len__(self):
+        return len(self._m)
+
+
+# ---------------------------------------------------------------------------
+# capacity arithmetic ([VA] s.3; [GQA] 64 B x blocks)
+# ---------------------------------------------------------------------------
+
+
+def kv_bytes_per_token(L, Hkv, d, elem_bytes=2) -> int:
+    """2 (K and V) x layers x KV heads x head dim x bytes per element."""
+    return 2 * L * Hkv * d * elem_bytes
+
+
+def metadata_bytes(num_blocks: int, record_bytes: int = 64) -> int:
+    return num_blocks * record_bytes

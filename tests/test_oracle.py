@@ -1,0 +1,330 @@
+"""Pins of the fp64 CPU oracle against things other than itself: a library
+attention routine, closed forms, the pages' printed numbers, invariants and
+brute force.  CPU only."""
+import math
+from pathlib import Path
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle as O
+import workloads as W
+
+GOLDEN = Path(__file__).parent / "golden"
+
+
+def _read_golden(name):
+    rows = []
+    for line in (GOLDEN / name).read_text().splitlines():
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(line.split())
+    return rows
+
+
+def _sdpa(q, K, V, L, Hq, Hkv, d):
+    """Contiguous attention through torch's fp64 SDPA, K/V repeated per group."""
+    G = Hq // Hkv
+    qd = q.double().unsqueeze(2)                                  # [L][Hq][1][d]
+    Kr = K.double().permute(1, 2, 0, 3).repeat_interleave(G, dim=1)  # [L][Hq][n][d]
+    Vr = V.double().permute(1, 2, 0, 3).repeat_interleave(G, dim=1)
+    out = F.scaled_dot_product_attention(qd, Kr, Vr).squeeze(2)
+    logits = (qd @ Kr.transpose(-1, -2)).squeeze(2) / math.sqrt(d)  # [L][Hq][n]
+    return out, torch.logsumexp(logits, -1), torch.softmax(logits, -1)
+
+
+def _case(name, n=None, **kw):
+    wl = W.workload(name, **kw)
+    n = n or wl.prefill_lens[0]
+    K, V = W.kv_tokens(wl, 0, 0, n, "cpu")
+    q = W.queries(wl, 0, 1, "cpu")
+    return wl, q, K, V
+
+
+# ----------------------------------------------------------------- capacity
+
+
+def test_capacity_arithmetic_matches_pages():
+    g = {r[0]: int(r[1]) for r in _read_golden("capacity.txt")}
+    bpt = O.kv_bytes_per_token(80, 8, 128)
+    assert bpt == g["bytes_per_token_70b"]
+    assert bpt * 16 == g["bytes_per_block_70b"] == 5 * 2**20
+    assert 131072 // 16 == g["blocks_at_128k"]
+    assert bpt * 131072 == g["kv_bytes_at_128k"] == 40 * 2**30
+    assert bpt * 8192 == g["kv_bytes_at_8k"] == int(2.5 * 2**30)
+    assert O.metadata_bytes(8192) == g["metadata_bytes_at_128k"] == 512 * 1024
+    assert O.REC_DTYPE.itemsize == g["record_bytes"]
+    cross = 130.4 * 2**30 / bpt
+    assert abs(cross - g["crossover_tokens_approx"]) / 427000 < 0.001
+    # generator geometry agrees with the formula
+    assert W.workload("l70b_128k").token_bytes == bpt
+    assert W.workload("tiny").page_bytes == 16 * 1024
+
+
+def test_record_layout_is_64_bytes_with_key_first():
+    r = O.new_records(7, 3, 2, 5)
+    raw = r.tobytes()
+    assert len(raw) == 128
+    assert int.from_bytes(raw[0:8], "little") == 7
+    assert int.from_bytes(raw[8:16], "little") == 3
+    assert int.from_bytes(raw[24:32], "little") == 5
+    assert int.from_bytes(raw[64 + 8:64 + 16], "little") == 4
+
+
+# ---------------------------------------------------------------- attention
+
+
+@pytest.mark.parametrize("name,n,kw", [
+    ("tiny", 256, {}),
+    ("tiny", 37, {}),                       # ragged: 2 full blocks + 5 tokens
+    ("l70b_8k", 1024, {"L": 2}),            # 2-layer, 1,024-token cut of the 70B shape
+])
+def test_attention_matches_library_sdpa(name, n, kw):
+    wl, q, K, V = _case(name, n, **kw)
+    r = O.decode_with_mass(q, K, V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d)
+    out, lse, p = _sdpa(q, K, V, wl.L, wl.Hq, wl.Hkv, wl.d)
+    np.testing.assert_allclose(r["out"], out.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["lse"], lse.numpy(), rtol=0, atol=1e-12)
+    # per-head block mass = block sums of the library softmax
+    nb = (n + 15) // 16
+    pad = torch.zeros(p.shape[:-1] + (nb * 16 - n,), dtype=p.dtype)
+    blk = torch.cat([p, pad], -1).reshape(wl.L * wl.Hq, nb, 16).sum(-1)
+    np.testing.assert_allclose(r["head_mass"], blk.numpy(), rtol=0, atol=1e-13)
+    # per-head masses sum to one; the aggregate sums to one
+    np.testing.assert_allclose(r["head_mass"].sum(1), 1.0, rtol=0, atol=1e-12)
+    assert abs(r["mass"].sum() - 1.0) < 1e-12
+    # aggregate = mean over all heads (equal group sizes), brute force
+    np.testing.assert_allclose(r["mass"], blk.mean(0).numpy(), rtol=0, atol=1e-14)
+
+
+def test_attention_head_subset_and_threads_are_bit_identical():
+    wl, q, K, V = _case("tiny", 200)
+    a = O.decode(q, K, V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, threads=1)
+    b = O.decode(q, K, V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, threads=5)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["head_mass"], b["head_mass"])
+    heads = [13, 2, 9]
+    c = O.decode(q, K, V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, heads=heads, threads=2)
+    assert np.array_equal(c["out"], a["out"][heads])
+    assert np.array_equal(c["lse"], a["lse"][heads])
+
+
+def test_gqa_head_to_kv_head_mapping():
+    """Query head h must read KV head h // G: zero every KV head but one and
+    only that group's heads may see non-uniform attention."""
+    wl, q, K, V = _case("tiny", 64)
+    K = K.clone()
+    V = V.clone()
+    K[:, :, 0, :] = 0            # KV head 0 keys all zero -> uniform weights
+    r = O.decode(q, K, V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d)
+    hm = r["head_mass"].reshape(wl.L, wl.Hq, -1)
+    G = wl.G
+    assert np.allclose(hm[:, :G, :], 0.25, atol=1e-15)          # 4 blocks, uniform
+    assert not np.allclose(hm[:, G:, :], 0.25, atol=1e-3)
+
+
+def test_single_token_and_partial_block():
+    wl, q, K, V = _case("tiny", 1)
+    r = O.decode_with_mass(q, K, V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d)
+    # one token: output equals its value vector, all mass on block 0
+    v = O.bf16_to_f64(O._u16(V))[0]                              # [L][Hkv][d]
+    exp = np.repeat(v, wl.G, axis=1)
+    np.testing.assert_array_equal(r["out"], exp)
+    assert r["mass"].tolist() == [1.0]
+
+
+def test_skewed_inputs_put_most_mass_on_recent_tenth():
+    """The generator's recency boost (input shaping) does what it says."""
+    wl, q, K, V = _case("l70b_8k", 2048, L=2, prefill_lens=(2048,))
+    r = O.decode_with_mass(q, K, V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, want_out=False)
+    nb = len(r["mass"])
+    recent = r["mass"][int(0.9 * nb):].sum()
+    assert 0.65 < recent < 0.92
+
+
+# ----------------------------------------------------------------- scoring
+
+
+def test_ema_worked_example_from_pages():
+    rows = _read_golden("ema_worked_example.txt")
+    alpha = float(rows[0][1])
+    traces = {}
+    for name, step, attn, printed, dec in rows[1:]:
+        traces.setdefault(name, []).append((float(attn), float(printed), int(dec)))
+    exact = {"anchor": [0.008, 0.0124, 0.01992], "middle": [0.0002, 0.00016, 0.000528]}
+    for name, steps in traces.items():
+        s = np.zeros(1)
+        for i, (attn, printed, dec) in enumerate(steps):
+            s = O.ema(s, np.array([attn]), alpha)
+            assert round(float(s[0]), dec) == pytest.approx(printed, abs=10 ** -(dec + 3))
+            assert float(s[0]) == pytest.approx(exact[name][i], rel=1e-14)
+
+
+def test_ema_special_cases():
+    rng = np.random.default_rng(1)
+    prev, m = rng.random(50), rng.random(50)
+    assert np.array_equal(O.ema(prev, m, 1.0), m)           # alpha = 1: current mass
+    assert np.array_equal(O.ema(prev, m, 0.0), prev)        # alpha = 0: unchanged
+
+
+def test_ema_half_life_closed_form():
+    """[VA] s.11: half-life ln 0.5 / ln 0.95 = 13.5 steps at alpha = 0.05."""
+    s = np.ones(1)
+    hist = []
+    for _ in range(20):
+        s = O.ema(s, np.zeros(1), 0.05)
+        hist.append(float(s[0]))
+    hl = math.log(0.5) / math.log(0.95)
+    assert 13.5 < hl < 13.52
+    assert hist[12] > 0.5 > hist[13]                        # after 13 steps > 1/2 > after 14
+    assert hist[12] == pytest.approx(0.95 ** 13, rel=1e-14)
+
+
+def test_recency_clip_and_window():
+    t = 100
+    lt = np.array([100, 99, 37, 36, 35, 0], dtype=np.uint64)
+    R = O.recency(t, lt, 64)
+    assert R.tolist() == [1.0, 63 / 64, 1 / 64, 0.0, 0.0, 0.0]
+
+
+def test_tier_boundaries_half_open():
+    lo = 0.3
+    below = np.nextafter(lo, 0)
+    P = np.array([0.0, below, 0.3, np.nextafter(0.6, 0), 0.6, 1.0])
+    assert O.tier_of(P).tolist() == [2, 2, 1, 1, 0, 0]
+
+
+def test_priority_weights_and_range():
+    assert O.priority(1.0, 0.0, 0.0).item() == 0.25
+    assert O.priority(0.0, 1.0, 0.0).item() == 0.55
+    assert O.priority(0.0, 0.0, 1.0).item() == pytest.approx(0.20, abs=0)
+    assert O.priority(1.0, 1.0, 1.0).item() == pytest.approx(1.0, abs=1e-15)
+    rng = np.random.default_rng(2)
+    P = O.priority(rng.random(1000), rng.random(1000), rng.integers(0, 2, 1000))
+    assert P.min() >= 0.0 and P.max() <= 1.0 + 1e-15
+    # an anchor with E = 0.3 touched now is pinned (0.25 + 0.165 + 0.2 >= 0.6)
+    assert O.tier_of(O.priority(1.0, 0.3, 1.0)).item() == 0
+
+
+def test_score_update_touch_anchor_and_order():
+    nb = 5
+    rec = O.new_records(9, 0, nb, t_create=0)
+    mass = np.array([0.5, 0.2, 0.2, 0.05, 0.05])       # touch iff M*nb >= 1
+    r = O.score_update(rec, mass, t=1, alpha=0.15)
+    assert r["count"].tolist() == [1, 1, 1, 0, 0]
+    assert r["last_touch"].tolist() == [1, 1, 1, 0, 0]
+    R = np.array([1, 1, 1, 63 / 64, 63 / 64])
+    E = 0.15 * mass
+    N = np.array([1, 0, 0, 0, 1.0])
+    np.testing.assert_allclose(r["prio"], 0.25 * R + 0.55 * E + 0.2 * N, rtol=0, atol=1e-15)
+    assert r["tier"].tolist() == [1, 2, 2, 2, 1]
+    assert np.array_equal(r["score"], 0.15 * mass)
+    assert r["mass"].dtype == np.float32
+
+
+def test_touch_at_exact_uniform_share():
+    nb = 8
+    rec = O.new_records(1, 0, nb, 0)
+    r = O.score_update(rec, np.full(nb, 1 / nb), t=3, alpha=0.5)
+    assert r["count"].tolist() == [1] * nb
+
+
+# --------------------------------------------------------------- selection
+
+
+def _random_recs(rng, nseq, nb, ties=False):
+    out = {}
+    for s in range(nseq):
+        r = O.new_records(100 + 3 * s, 0, nb, 0)
+        p = rng.integers(0, 4, nb) / 10.0 if ties else rng.random(nb)
+        r["prio"] = p
+        r["tier"] = O.tier_of(p)
+        out[100 + 3 * s] = r
+    return out
+
+
+def test_select_thresh_brute_force():
+    rng = np.random.default_rng(3)
+    recs = _random_recs(rng, 3, 7)
+    got = O.select_thresh(recs)
+    exp = [(s, b) for s in sorted(recs) for b in range(7) if recs[s]["prio"][b] < 0.3]
+    assert got == exp
+
+
+@pytest.mark.parametrize("ties", [False, True])
+def test_select_lowfrac_brute_force(ties):
+    """[RETR] s.3 audit: every chosen record beats every other one under
+    (P, seq_id, block_idx); k = floor(frac*N)."""
+    rng = np.random.default_rng(4)
+    recs = _random_recs(rng, 4, 9, ties)
+    got = O.select_lowfrac(recs, 0.25)
+    keys = [(s, b) for s in sorted(recs) for b in range(9)]
+    assert len(got) == math.floor(0.25 * len(keys))
+    assert got == sorted(got)
+    rank = {k: i for i, k in enumerate(keys)}
+    P = {(s, b): recs[s]["prio"][b] for s, b in keys}
+    for a in got:
+        for b in set(keys) - set(got):
+            assert (P[a], rank[a]) < (P[b], rank[b])
+
+
+def test_lowfrac_k_matches_pages_fraction():
+    assert O.lowfrac_k(20000, 0.10) == 2000
+    assert O.lowfrac_k(9, 0.10) == 0
+    assert O.lowfrac_k(10, 0.10) == 1
+
+
+def test_gather_plan_refcount_rule():
+    page_of = {(1, 0): "P0", (2, 0): "P0", (1, 1): "A", (2, 1): "B"}
+    refs = {"P0": {(1, 0), (2, 0)}, "A": {(1, 1)}, "B": {(2, 1)}}
+    assert O.gather_plan([(1, 0), (1, 1), (2, 1)], page_of, refs) == ["A", "B"]
+    assert O.gather_plan([(1, 0), (1, 1), (2, 0)], page_of, refs) == ["P0", "A"]
+
+
+# ------------------------------------------------------------------ pages
+
+
+def test_page_layout_hand_offsets():
+    L, Hkv, d, t = 2, 2, 4, 3
+    K = np.arange(t * L * Hkv * d, dtype=np.uint16).reshape(t, L, Hkv, d)
+    V = (K + 1000).astype(np.uint16)
+    page = np.frombuffer(O.assemble_page(K, V, 16), np.uint16)
+    assert page.size == L * 2 * Hkv * 16 * d
+    # element (layer l, K/V kv, head g, slot s, dim i) at ((((l*2+kv)*Hkv+g)*16+s)*d+i)
+    def at(l, kv, g, s, i):
+        return page[(((l * 2 + kv) * Hkv + g) * 16 + s) * d + i]
+    assert at(0, 0, 0, 0, 0) == K[0, 0, 0, 0]
+    assert at(1, 1, 1, 2, 3) == V[2, 1, 1, 3]
+    assert at(1, 0, 1, 1, 2) == K[1, 1, 1, 2]
+    assert at(0, 1, 0, 5, 0) == 0                       # slot past the last token
+
+
+def test_identity_store_round_trip():
+    st = O.IdentityStore()
+    rec = O.new_records(5, 2, 1, 7)
+    st.demote((5, 2), rec, b"abc")
+    with pytest.raises(KeyError):
+        st.demote((5, 2), rec, b"abc")
+    r, p = st.readmit((5, 2))
+    assert r.tobytes() == rec.tobytes() and p == b"abc"
+    with pytest.raises(KeyError):
+        st.readmit((5, 2))
+
+
+# --------------------------------------------------------- planted mistakes
+
+
+def test_pins_catch_planted_mistakes(monkeypatch):
+    """Each plausible slip in the scoring formulas fails one of the pins."""
+    good_ema, good_prio = O.ema, O.priority
+    # swapped EMA operands -> the worked example fails
+    monkeypatch.setattr(O, "ema", lambda p, a, al: good_ema(a, p, al))
+    with pytest.raises(AssertionError):
+        test_ema_worked_example_from_pages()
+    monkeypatch.setattr(O, "ema", good_ema)
+    # dropped anchor term -> the hand case fails
+    monkeypatch.setattr(O, "priority", lambda R, E, N, w=(0.25, 0.55, 0.2): good_prio(R, E, 0 * np.asarray(N), w))
+    with pytest.raises(AssertionError):
+        test_score_update_touch_anchor_and_order()
+    monkeypatch.setattr(O, "priority", good_prio)
