@@ -1,0 +1,317 @@
+/*
+ * kvs.h -- C ABI of the paged KV-cache decode and block-scoring library
+ * (one GPU, sm_103a).
+ *
+ * The library runs one hot path:
+ *   append token K/V into 16-token pages reached through a per-sequence block
+ *   table -> grouped-query decode attention over every cached token ->
+ *   attention mass per (sequence, block), aggregated over all (layer, KV head)
+ *   streams -> EMA/LRFU score, touch count and touch time in a 64-byte record
+ *   per block -> priority P and tier -> selection of low-priority blocks ->
+ *   gather of their pages into a pinned-host staging buffer -> identity-keyed
+ *   re-admission that restores the record instead of resetting it.
+ *
+ * Sources, cited by page title and section:
+ *   [VA]   "KV-Cache Offloading for LLM Inference -- Visual Reference" (v6.0):
+ *          s.1 model geometry, s.3 KV size formula, s.4 decode reads the whole
+ *          KV cache, s.11 EMA update rule, s.12 priority formula and tier
+ *          thresholds (Diagrams 12.1, 12.2).
+ *   [GQA]  "GQA per-head attention as scoring streams" figure page: 64 query
+ *          heads grouped 8:1 onto 8 KV heads, 640 (layer, KV head) streams
+ *          aggregated into one score per (sequence, 16-token block), the
+ *          64-byte per-block state, identity-keyed persistence across
+ *          eviction.
+ *   [ARCH] "LLM KV cache offload" architecture page: block manager with
+ *          fixed-size blocks and per-sequence block tables, reference counts
+ *          for shared prefixes, eviction by demotion through pinned host
+ *          staging on the copy engines, contiguous block layout.
+ *   [RETR] "RETRACTIONS" page, s.2: blocks are write-once.
+ *
+ * Conventions for every call:
+ *   - Status: every function returns KVS_OK (0) or a kvs_status code;
+ *     kvs_last_error() then describes the failure.  On failure no state of
+ *     the context has changed unless the description says so.
+ *   - Memory: the library allocates no device memory.  The caller allocates
+ *     every device buffer (sizes from kvs_required_sizes) and keeps it alive
+ *     until kvs_destroy.  Host buffers passed to the gather/readmit calls are
+ *     caller-owned pinned memory (cudaHostAlloc).  The context itself owns
+ *     only host bookkeeping, CUDA events and a small pinned upload ring.
+ *   - Streams: `stream` arguments are cudaStream_t values passed as void*.
+ *     Calls are stream-ordered and asynchronous unless documented as
+ *     synchronising: device outputs are valid once the stream has reached
+ *     the call.  Calls on one context must be ordered by the caller (one
+ *     stream, or events between streams).
+ *   - Layouts (bf16 = IEEE bfloat16, little-endian):
+ *       page   : [L][2 (K, V)][Hkv][16 token slots][d] bf16, page_bytes =
+ *                2*L*Hkv*16*d*2 (5,242,880 B for 80/8/128); slots past the
+ *                last token of a partial block are zero.
+ *       pool   : [pool_blocks] pages.
+ *       q      : [nseq][L][Hq][d] bf16; out: [nseq][L][Hq][d] float32.
+ *       K, V   : token-major [n][L][Hkv][d] bf16 (as produced by a layer's
+ *                projections for n consecutive tokens).
+ *       record : 64 bytes, see kvs_record.
+ *       mass   : float32 [max_seqs][max_blocks_per_seq], row = sequence slot.
+ */
+#ifndef KVS_H
+#define KVS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVS_BLOCK_TOKENS 16u
+#define KVS_RECORD_BYTES 64u
+#define KVS_MAX_CALL_SEQS 256u   /* sequences in one decode call */
+
+/* Opaque context: host bookkeeping of one pool (free list, reference counts,
+ * block tables, identity store), its events and its upload ring. */
+typedef struct kvs_ctx kvs_ctx_t;
+
+typedef enum kvs_status {
+    KVS_OK = 0,
+    KVS_EINVAL = 1,     /* bad argument or call in the wrong state */
+    KVS_ENOMEM = 2,     /* pool pages, sequence slots or staging exhausted */
+    KVS_ECUDA = 3,      /* a CUDA runtime call failed */
+    KVS_ENOTFOUND = 4,  /* unknown sequence or identity key */
+    KVS_EEXIST = 5,     /* sequence or key already present / resident */
+    KVS_ETRUNC = 6,     /* output buffer too small: partial result written */
+    KVS_ETIMEOUT = 7,   /* a bounded wait ran out (device or host) */
+    KVS_EDEVICE = 8     /* a kernel reported an inconsistency (see error text) */
+} kvs_status;
+
+typedef enum kvs_select_mode {
+    KVS_SELECT_THRESH = 0,   /* every record with P < cut_lo (tier 2) */
+    KVS_SELECT_LOWFRAC = 1   /* the floor(frac*N) records with smallest P */
+} kvs_select_mode;
+
+/* kvs_gather_args.flags */
+#define KVS_GATHER_DEMOTE 1u  /* free the gathered pages, keep records by key */
+#define KVS_GATHER_MIRROR 2u  /* host_dst mirrors the pool (page p at p*page_bytes);
+                                 pages whose host copy is current are not re-sent */
+
+typedef struct kvs_config {
+    uint32_t num_layers;          /* L                                        */
+    uint32_t num_q_heads;         /* Hq                                       */
+    uint32_t num_kv_heads;        /* Hkv; Hq % Hkv == 0, Hq/Hkv <= 8          */
+    uint32_t head_dim;            /* d: 64 or 128                             */
+    uint32_t block_tokens;        /* must be 16                               */
+    uint32_t pool_blocks;         /* physical pages in the pool               */
+    uint32_t max_seqs;            /* sequence slots                           */
+    uint32_t max_blocks_per_seq;  /* block-table row length                   */
+    uint32_t max_call_blocks;     /* max sum of blocks over one decode call;
+                                     0 = max_seqs * max_blocks_per_seq       */
+    uint32_t staging_pages;       /* device staging ring, pages (>= 1)        */
+    double alpha;                 /* EMA weight of the current mass [VA] s.11 */
+    uint32_t recency_window;      /* W: R = clip(1 - (t - last_touch)/W, 0, 1) */
+    uint32_t reserved0;
+    double w_recency, w_ema, w_anchor;   /* [VA] s.12: 0.25, 0.55, 0.20      */
+    double cut_lo, cut_hi;               /* [VA] Diagram 12.2: 0.3, 0.6      */
+    uint64_t pool_seed;           /* seeds the free-list order of the pool    */
+} kvs_config;
+
+/* Byte sizes of the caller-allocated device buffers.  Every buffer must be
+ * 256-byte aligned (cudaMalloc and the PyTorch caching allocator are). */
+typedef struct kvs_sizes {
+    size_t page_bytes;
+    size_t pool_bytes;        /* pool_blocks * page_bytes                     */
+    size_t table_bytes;       /* int32 [max_seqs][max_blocks_per_seq]         */
+    size_t records_bytes;     /* kvs_record [max_seqs][max_blocks_per_seq]    */
+    size_t mass_bytes;        /* float [max_seqs][max_blocks_per_seq]         */
+    size_t workspace_bytes;   /* decode partials, per-block LSE, select state */
+    size_t staging_bytes;     /* staging_pages * page_bytes                   */
+} kvs_sizes;
+
+typedef struct kvs_buffers {
+    void *pool, *block_table, *records, *mass, *workspace, *staging;
+} kvs_buffers;
+
+/* Identity key of a block [GQA]: the sequence it belongs to and its logical
+ * block index.  16 bytes. */
+typedef struct kvs_key {
+    uint64_t seq_id;
+    uint64_t block_idx;
+} kvs_key;
+
+/* The 64-byte per-block state [GQA]: 16 B identity key, 8 B score, 8 B touch
+ * timestamp, 4 B touch count, then reserved bytes, which hold the tier, the
+ * last priority and the last mass. */
+typedef struct kvs_record {
+    kvs_key key;          /*  0 */
+    double score;         /* 16  EMA of the block mass, 0 at creation        */
+    uint64_t last_touch;  /* 24  step of the last touch (creation step first) */
+    uint32_t count;       /* 32  touches so far                              */
+    uint8_t tier;         /* 36  0, 1, 2; 255 = not scored yet               */
+    uint8_t flags;        /* 37  bit 0: demoted (not resident)               */
+    uint16_t pad0;        /* 38                                              */
+    double prio;          /* 40  last P                                      */
+    float mass;           /* 48  last block mass M                           */
+    uint8_t reserved[12]; /* 52                                              */
+} kvs_record;
+
+typedef struct kvs_gather_args {
+    int32_t mode;            /* kvs_select_mode                                */
+    uint32_t flags;          /* KVS_GATHER_*                                   */
+    double frac;             /* LOWFRAC fraction of all records (e.g. 0.10)    */
+    void *host_dst;          /* pinned host buffer, caller-owned               */
+    size_t host_dst_bytes;
+    kvs_key *ids_dev;        /* device out [ids_capacity]: selected keys in list
+                                order (may be NULL)                            */
+    int32_t *slot_dev;       /* device out [ids_capacity]: page index in host_dst
+                                holding each id's bytes, -1 if not gathered
+                                (may be NULL)                                  */
+    uint32_t ids_capacity;
+    uint32_t reserved0;
+    void *stream;            /* main stream (selection, gather kernels)       */
+    void *side_stream;       /* copy stream for device->host (may == stream)  */
+} kvs_gather_args;
+
+typedef struct kvs_gather_result {
+    uint32_t n_selected;     /* records in the list                           */
+    uint32_t n_pages;        /* pages the list makes eligible (deduplicated)  */
+    uint32_t n_staged;       /* pages written to host_dst by this call        */
+    uint32_t n_demoted;      /* records demoted (KVS_GATHER_DEMOTE)           */
+    uint64_t bytes_to_host;  /* bytes copied device -> host by this call      */
+} kvs_gather_result;
+
+/* Sizes of every caller-allocated device buffer for `cfg`.
+ * Returns KVS_EINVAL (with no sizes) if cfg is not supported. */
+int kvs_required_sizes(const kvs_config *cfg, kvs_sizes *out);
+
+/* Creates a context over caller-allocated device buffers (sizes from
+ * kvs_required_sizes, all on the current device).  Zeroes the block table,
+ * records and mass (synchronously) and builds the pool's TMA descriptor.
+ * The free list holds every pool page in an order seeded by cfg->pool_seed. */
+int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out);
+
+/* Destroys host state and events; does not touch caller buffers.  Waits for
+ * work the context enqueued. */
+void kvs_destroy(kvs_ctx_t *ctx);
+
+/* Text of the last failure on this context (owned by the context). */
+const char *kvs_last_error(const kvs_ctx_t *ctx);
+
+/* Adds a sequence with no tokens.  With parent_seq_id >= 0, the first
+ * shared_prefix_blocks (full) blocks of the parent are shared read-only:
+ * the new table points at the same pages and their reference counts rise
+ * [ARCH]; the new sequence gets its own records for those blocks (score 0,
+ * count 0, last_touch = current step), written on `stream`.  Appending
+ * never writes a shared page.  KVS_EEXIST if seq_id is
+ * present, KVS_ENOTFOUND if the parent is not, KVS_ENOMEM if no slot is
+ * free, KVS_EINVAL if the parent has fewer full blocks. */
+int kvs_seq_add(kvs_ctx_t *ctx, uint64_t seq_id, int64_t parent_seq_id,
+                uint32_t shared_prefix_blocks, void *stream);
+
+/* Removes a sequence: its pages lose one reference each and return to the
+ * free list at zero; its demoted keys are dropped.  Stream-ordered after
+ * `stream` (page reuse waits for work enqueued before). */
+int kvs_seq_remove(kvs_ctx_t *ctx, uint64_t seq_id, void *stream);
+
+/* Appends n tokens to a sequence [ARCH]: K and V are device, token-major
+ * [n][L][Hkv][d] bf16.  A page is taken from the free list whenever a token
+ * opens a new block; the page's later slots are zero-filled and the block's
+ * record is created with score 0, count 0, last_touch = the current step
+ * counter (decode steps completed so far), tier 255.  KVS_ENOMEM if the free
+ * list runs out (nothing appended), KVS_EINVAL for n == 0 or a table row
+ * overflow. */
+int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n,
+                      const void *k_dev, const void *v_dev, void *stream);
+int kvs_append_token(kvs_ctx_t *ctx, uint64_t seq_id, const void *k_dev,
+                     const void *v_dev, void *stream);
+
+/* One decode step for nseq sequences [VA] s.4, [GQA]: advances the step
+ * counter t by one, then for every (sequence, layer, query head) computes
+ *   out = sum_t softmax_t(q.k_t / sqrt(d)) v_t   over all cached tokens,
+ * (query head h reads KV head h / (Hq/Hkv)), and for every block b of each
+ * sequence the aggregated mass
+ *   M(b) = 1/(L*Hq) * sum_{l,h} sum_{t in b} softmax weight,
+ * written to mass[slot][b].  q [nseq][L][Hq][d] bf16 and out [nseq][L][Hq][d]
+ * float32 are device, in the order of seq_ids.  The set of sequences becomes
+ * the one kvs_score_update and kvs_select_and_gather work on.
+ * KVS_EINVAL: nseq == 0 or > KVS_MAX_CALL_SEQS, duplicates, an empty
+ * sequence or one with a demoted block; KVS_ENOTFOUND: unknown id. */
+int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
+                    const void *q_dev, float *out_dev, void *stream);
+
+/* Scores every block of the last decode set [VA] s.11, s.12, [GQA]:
+ *   E <- alpha*M + (1-alpha)*E;  if M*num_blocks >= 1: count += 1,
+ *   last_touch = t;  R = clip(1 - (t - last_touch)/W, 0, 1);
+ *   N = 1 for block 0 and the newest block, else 0;
+ *   P = w_recency*R + w_ema*E + w_anchor*N;
+ *   tier = 0 if P >= cut_hi, 1 if cut_lo <= P < cut_hi, 2 if P < cut_lo.
+ * fp64 with no fused multiply-add, in that order. */
+int kvs_score_update(kvs_ctx_t *ctx, void *stream);
+
+/* Changes alpha for later score updates. */
+int kvs_set_alpha(kvs_ctx_t *ctx, double alpha);
+
+/* Selects records of the last decode set and gathers their pages
+ * [VA] s.12, [ARCH].  Synchronising: returns after the list is known and
+ * every copy is enqueued; host_dst is complete once args->side_stream has
+ * reached this call.
+ *   THRESH : every record with tier 2, ascending (seq_id, block_idx).
+ *   LOWFRAC: the floor(frac*N) records of smallest (P, seq_id, block_idx)
+ *            over all N records of the set, listed ascending (seq_id,
+ *            block_idx).
+ * A page is eligible when every record that references it is in the list
+ * (a shared page is released only by its last user); each eligible page is
+ * gathered once, at the position of its first record.  Default: eligible
+ * pages go into host_dst in list order through the device staging ring;
+ * if host_dst is too small a prefix is written and KVS_ETRUNC returned with
+ * the full counts.  KVS_GATHER_MIRROR: host_dst holds pool_blocks pages and
+ * page p goes to offset p*page_bytes; a page whose host copy is still
+ * current (written whole and unchanged since, [RETR] s.2) is not copied
+ * again.  KVS_GATHER_DEMOTE (list mode only): eligible records are demoted:
+ * their 64-byte record and the offset of their page in host_dst are kept
+ * under their key, the table entry is cleared and the page freed.  The
+ * caller keeps host_dst alive until kvs_readmit. */
+int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args,
+                          kvs_gather_result *res);
+
+/* Re-admits demoted blocks [GQA]: for each key, takes a page from the free
+ * list, copies the page bytes from host_src (the buffer given to the demoting
+ * gather) and restores the 64-byte record bit for bit.  KVS_ENOTFOUND for a
+ * key that is not demoted, KVS_EEXIST for a duplicate key in `keys`,
+ * KVS_ENOMEM if the free list runs out (nothing re-admitted). */
+int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n,
+                const void *host_src, size_t host_src_bytes, void *stream);
+
+/* Test hook: makes seq_ids the current set and copies mass_dev (float32
+ * [nseq][max_blocks_per_seq], row i for seq_ids[i], device) into the mass
+ * rows, without decoding and without advancing t.  Lets the scoring,
+ * tiering and selection steps be driven from given masses. */
+int kvs_debug_set_mass(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
+                       const float *mass_dev, void *stream);
+
+/* Test hook: advances the step counter without decoding. */
+int kvs_debug_advance(kvs_ctx_t *ctx, uint64_t steps);
+
+/* Copies the records of one sequence (block order, 64 B each) to host_dst.
+ * Synchronising.  KVS_ETRUNC if host_bytes holds fewer than all blocks. */
+int kvs_export_records(kvs_ctx_t *ctx, uint64_t seq_id, void *host_dst,
+                       size_t host_bytes, void *stream);
+
+/* Host view of a sequence: its slot (row of the table, records and mass
+ * buffers), token count, block count, and (if table_out is not NULL) up to
+ * table_cap page ids (-1 = demoted).  Any output pointer may be NULL. */
+int kvs_seq_info(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t *slot,
+                 uint32_t *n_tokens, uint32_t *n_blocks, int32_t *table_out,
+                 uint32_t table_cap);
+
+/* Decode steps completed so far (the step counter t). */
+uint64_t kvs_step_count(const kvs_ctx_t *ctx);
+
+/* Free pages left in the pool. */
+uint32_t kvs_free_pages(const kvs_ctx_t *ctx);
+
+/* Reads and clears the device error word (synchronising on `stream`).
+ * KVS_OK if no kernel reported a problem, else KVS_EDEVICE / KVS_ETIMEOUT
+ * with the description in kvs_last_error. */
+int kvs_check_device(kvs_ctx_t *ctx, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVS_H */

@@ -152,7 +152,8 @@ int orc_decode_heads(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      const int32_t *heads, int nheads, int nthreads,
                      double *out, double *lse, double *head_mass)
 {
-    if (n < 1 || L < 1 || Hkv < 1 || Hq % Hkv || d < 1 || block_tokens < 1)
+    if (n < 1 || L < 1 || Hkv < 1 || Hq % Hkv || d < 1 || block_tokens < 1 ||
+        (heads && nheads < 1))
         return -1;
     int32_t *all = NULL;
     if (!heads) {
@@ -169,10 +170,14 @@ int orc_decode_heads(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             free(all);
             return -1;
         }
-    if (nthreads < 1)
-        nthreads = 1;
+    if (nheads < 1 || nheads > (1 << 30)) {
+        free(all);
+        return -1;
+    }
     if (nthreads > nheads)
         nthreads = nheads;
+    if (nthreads < 1)
+        nthreads = 1;
     job_t *jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
     pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     int rc = 0;

@@ -1,0 +1,418 @@
+// Block-level kernels: append into pages, EMA/priority/tier scoring,
+// selection (threshold compaction and lowest-fraction radix select), page
+// gather into the staging ring, and table/record patches for demote/readmit.
+//
+// Sources: "KV-Cache Offloading for LLM Inference -- Visual Reference" s.11
+// (EMA rule), s.12 (priority P, tier thresholds 0.3 / 0.6); "GQA per-head
+// attention as scoring streams" (64-byte per-block state, identity key kept
+// across eviction); "LLM KV cache offload" (block tables, pinned-host
+// staging); "RETRACTIONS" s.3 (exact victim selection, audited by brute force).
+#include <algorithm>
+
+#include <cuda_bf16.h>
+
+#include "kvs_internal.h"
+
+namespace kvs {
+namespace {
+
+// ----------------------------------------------------------------- append
+// One thread moves 16 bytes.  Rows are (token slot, layer, K/V, KV head) of
+// d bf16 values; slots of the last touched block past the appended tokens
+// are zero-filled.  Thread-blocks past the row range initialise the records
+// of newly opened blocks and their table entries.
+__global__ void append_kernel(const Geo g, const AppendArgs a, uint64_t rows_total,
+                              uint32_t vec_per_row)
+{
+    const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const uint64_t nvec = rows_total * vec_per_row;
+    if (tid < nvec) {
+        const uint64_t row = tid / vec_per_row;
+        const uint32_t v16 = static_cast<uint32_t>(tid % vec_per_row);
+        // row = ((slot_pos * L + l) * 2 + kv) * Hkv + h, slot_pos from p0
+        const uint32_t h = row % g.Hkv;
+        uint64_t r2 = row / g.Hkv;
+        const uint32_t kv = r2 % 2;
+        r2 /= 2;
+        const uint32_t l = r2 % g.L;
+        const uint64_t rel = r2 / g.L;                  // token position - p0
+        const uint64_t pos = a.p0 + rel;
+        const uint32_t blk = static_cast<uint32_t>(pos / kBlockTokens);
+        const uint32_t slot_in = static_cast<uint32_t>(pos % kBlockTokens);
+        const int32_t page = a.pages[blk - a.first_blk];
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (rel < a.n) {
+            const uint16_t *src = (kv == 0 ? a.k : a.v) + ((rel * g.L + l) * g.Hkv + h) * g.d;
+            val = __ldg(reinterpret_cast<const uint4 *>(src) + v16);
+        }
+        uint16_t *dst = a.pool + static_cast<uint64_t>(page) * (g.page_bytes / 2) +
+                        ((((static_cast<uint64_t>(l) * 2 + kv) * g.Hkv + h) * kBlockTokens + slot_in) * g.d);
+        reinterpret_cast<uint4 *>(dst)[v16] = val;
+    } else {
+        const uint64_t j = tid - nvec;                  // new-block index
+        const uint32_t nnew = a.first_blk + a.nblk - a.first_new;
+        if (j < nnew) {
+            const uint32_t b = a.first_new + static_cast<uint32_t>(j);
+            const size_t idx = static_cast<size_t>(a.slot) * g.mb + b;
+            kvs_record r;
+            r.key.seq_id = a.seq_id;
+            r.key.block_idx = b;
+            r.score = 0.0;
+            r.last_touch = a.t_create;
+            r.count = 0;
+            r.tier = 255;
+            r.flags = 0;
+            r.pad0 = 0;
+            r.prio = 0.0;
+            r.mass = 0.f;
+            for (int q = 0; q < 12; ++q)
+                r.reserved[q] = 0;
+            a.records[idx] = r;
+            a.table[idx] = a.pages[b - a.first_blk];
+        }
+    }
+}
+
+// ----------------------------------------------------------------- scoring
+__device__ __forceinline__ uint32_t find_sorted(const DSet *ds, uint32_t r)
+{
+    uint32_t lo = 0, hi = ds->nseq;
+    while (hi - lo > 1) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (ds->srt_off[mid] <= r)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+struct ScoreArgs {
+    double alpha, wR, wE, wN, lo, hi;
+    uint32_t W;
+};
+
+// One thread per record of the decode set (record order: ascending seq_id,
+// then block).  fp64, every operation rounded on its own (no fused
+// multiply-add), in the order: EMA, touch, recency, anchor, P, tier.
+__global__ void score_kernel(const Geo g, const Work w, kvs_record *recs, const float *mass,
+                             const ScoreArgs sa, uint32_t nb_total)
+{
+    const uint32_t r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= nb_total)
+        return;
+    const DSet *ds = w.dset;
+    const uint32_t si = find_sorted(ds, r);
+    const DSeq sq = ds->seq[ds->sorted[si]];
+    const uint32_t b = r - ds->srt_off[si];
+    const size_t idx = static_cast<size_t>(sq.slot) * g.mb + b;
+    kvs_record rec = recs[idx];
+    const uint64_t t = ds->t;
+    if (rec.key.block_idx != b || rec.key.seq_id != sq.seq_id || rec.last_touch > t) {
+        atomicOr(w.err, kErrBadRecord);
+        return;
+    }
+    const double M = static_cast<double>(mass[idx]);
+    // E <- alpha*M + (1 - alpha)*E
+    const double E = __dadd_rn(__dmul_rn(sa.alpha, M), __dmul_rn(__dsub_rn(1.0, sa.alpha), rec.score));
+    // touch: mass at or above the uniform share 1/num_blocks
+    if (__dmul_rn(M, static_cast<double>(sq.nb)) >= 1.0) {
+        rec.count += 1;
+        rec.last_touch = t;
+    }
+    const double age = static_cast<double>(t - rec.last_touch);
+    double R = __dsub_rn(1.0, __ddiv_rn(age, static_cast<double>(sa.W)));
+    R = fmin(fmax(R, 0.0), 1.0);
+    const double N = (b == 0 || b + 1 == sq.nb) ? 1.0 : 0.0;
+    const double P = __dadd_rn(__dadd_rn(__dmul_rn(sa.wR, R), __dmul_rn(sa.wE, E)), __dmul_rn(sa.wN, N));
+    rec.score = E;
+    rec.prio = P;
+    rec.tier = P >= sa.hi ? 0 : (P >= sa.lo ? 1 : 2);
+    rec.mass = static_cast<float>(M);
+    recs[idx] = rec;
+}
+
+// ---------------------------------------------------------------- selection
+constexpr int kSelThreads = 256;
+constexpr int kSelPerThread = 4;
+constexpr int kSelTile = kSelThreads * kSelPerThread;
+
+__device__ __forceinline__ const kvs_record &rec_at(const Geo &g, const DSet *ds,
+                                                    const kvs_record *recs, uint32_t r,
+                                                    uint32_t *slot_out, uint32_t *b_out)
+{
+    const uint32_t si = find_sorted(ds, r);
+    const DSeq &sq = ds->seq[ds->sorted[si]];
+    const uint32_t b = r - ds->srt_off[si];
+    *slot_out = sq.slot;
+    *b_out = b;
+    return recs[static_cast<size_t>(sq.slot) * g.mb + b];
+}
+
+__device__ __forceinline__ bool picked(int mode, const kvs_record &rec, uint32_t r,
+                                       const uint64_t *thr)
+{
+    if (mode == KVS_SELECT_THRESH)
+        return rec.tier == 2;
+    // composite key (P bits, record index); P >= 0 so its bits order like P
+    const uint64_t pb = static_cast<uint64_t>(__double_as_longlong(rec.prio));
+    return pb < thr[0] || (pb == thr[0] && r <= thr[1]);
+}
+
+// Counts picked records per tile of kSelTile records.
+__global__ void __launch_bounds__(kSelThreads)
+    select_count_kernel(const Geo g, const Work w, const kvs_record *recs, int mode,
+                        uint32_t nb_total)
+{
+    __shared__ uint32_t wsum[kSelThreads / 32];
+    const DSet *ds = w.dset;
+    uint32_t c = 0;
+    for (int q = 0; q < kSelPerThread; ++q) {
+        const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
+        if (r < nb_total) {
+            uint32_t slot, b;
+            c += picked(mode, rec_at(g, ds, recs, r, &slot, &b), r, w.sel_thr) ? 1u : 0u;
+        }
+    }
+    for (int x = 16; x > 0; x >>= 1)
+        c += __shfl_xor_sync(0xffffffffu, c, x);
+    if ((threadIdx.x & 31) == 0)
+        wsum[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t t = 0;
+        for (int q = 0; q < kSelThreads / 32; ++q)
+            t += wsum[q];
+        w.tile_cnt[blockIdx.x] = t;
+    }
+}
+
+// Writes picked records in record order: key, page and record index.
+__global__ void __launch_bounds__(kSelThreads)
+    select_scatter_kernel(const Geo g, const Work w, const kvs_record *recs, const int32_t *table,
+                          int mode, uint32_t nb_total, uint32_t ntiles)
+{
+    __shared__ uint32_t wpre[kSelThreads / 32];
+    __shared__ uint32_t base_sh;
+    const DSet *ds = w.dset;
+    if (threadIdx.x == 0) {
+        uint32_t base = 0;
+        for (uint32_t q = 0; q < blockIdx.x; ++q)
+            base += w.tile_cnt[q];
+        base_sh = base;
+        if (blockIdx.x == ntiles - 1)
+            *w.sel_count = base + w.tile_cnt[blockIdx.x];
+    }
+    bool pk[kSelPerThread];
+    uint32_t slots[kSelPerThread], bs[kSelPerThread];
+    kvs_key keys[kSelPerThread];
+    uint32_t c = 0;
+    for (int q = 0; q < kSelPerThread; ++q) {
+        const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
+        pk[q] = false;
+        if (r < nb_total) {
+            const kvs_record &rec = rec_at(g, ds, recs, r, &slots[q], &bs[q]);
+            pk[q] = picked(mode, rec, r, w.sel_thr);
+            keys[q] = rec.key;
+        }
+        c += pk[q] ? 1u : 0u;
+    }
+    // exclusive scan of c over the block
+    const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint32_t inc = c;
+    for (int x = 1; x < 32; x <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, x);
+        if (lane >= static_cast<uint32_t>(x))
+            inc += y;
+    }
+    if (lane == 31)
+        wpre[wid] = inc;
+    __syncthreads();
+    uint32_t wbase = 0;
+    for (uint32_t q = 0; q < wid; ++q)
+        wbase += wpre[q];
+    uint32_t pos = base_sh + wbase + inc - c;
+    for (int q = 0; q < kSelPerThread; ++q) {
+        if (!pk[q])
+            continue;
+        const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
+        w.sel_ids[pos] = keys[q];
+        w.sel_recs[pos] = recs[static_cast<size_t>(slots[q]) * g.mb + bs[q]];
+        w.sel_pages[pos] = table[static_cast<size_t>(slots[q]) * g.mb + bs[q]];
+        w.sel_recidx[pos] = r;
+        ++pos;
+    }
+}
+
+// k-th smallest composite key (prio bits, record index), k >= 1, by an 8-bit
+// radix descent over the 96-bit key.  One block of 1024 threads.
+__global__ void __launch_bounds__(1024)
+    radix_select_kernel(const Geo g, const Work w, const kvs_record *recs, uint32_t nb_total,
+                        uint32_t k)
+{
+    __shared__ uint32_t hist[256];
+    __shared__ uint64_t pre_p;
+    __shared__ uint32_t pre_r;
+    __shared__ uint32_t remaining;
+    const DSet *ds = w.dset;
+    if (threadIdx.x == 0) {
+        pre_p = 0;
+        pre_r = 0;
+        remaining = k;
+    }
+    // 8 passes over the prio bits, then 4 over the record index
+    for (int pass = 0; pass < 12; ++pass) {
+        for (uint32_t q = threadIdx.x; q < 256; q += blockDim.x)
+            hist[q] = 0;
+        __syncthreads();
+        const uint64_t pp = pre_p;
+        const uint32_t pr = pre_r;
+        for (uint32_t r = threadIdx.x; r < nb_total; r += blockDim.x) {
+            uint32_t slot, b;
+            const kvs_record &rec = rec_at(g, ds, recs, r, &slot, &b);
+            const uint64_t pbits = static_cast<uint64_t>(__double_as_longlong(rec.prio));
+            uint32_t digit;
+            bool match;
+            if (pass < 8) {
+                const int sh = 56 - 8 * pass;
+                const uint64_t mask = pass == 0 ? 0ull : (~0ull << (sh + 8));
+                match = (pbits & mask) == pp;
+                digit = static_cast<uint32_t>(pbits >> sh) & 0xffu;
+            } else {
+                const int sh = 24 - 8 * (pass - 8);
+                const uint32_t mask = pass == 8 ? 0u : (~0u << (sh + 8));
+                match = pbits == pp && (r & mask) == pr;
+                digit = (r >> sh) & 0xffu;
+            }
+            if (match)
+                atomicAdd(&hist[digit], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t rem = remaining, dsel = 255;
+            for (uint32_t q = 0; q < 256; ++q) {
+                if (hist[q] >= rem) {
+                    dsel = q;
+                    break;
+                }
+                rem -= hist[q];
+            }
+            remaining = rem;
+            if (pass < 8)
+                pre_p |= static_cast<uint64_t>(dsel) << (56 - 8 * pass);
+            else
+                pre_r |= dsel << (24 - 8 * (pass - 8));
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        w.sel_thr[0] = pre_p;
+        w.sel_thr[1] = pre_r;
+    }
+}
+
+// ------------------------------------------------------------------- gather
+// grid.x = pages, grid.y = parts of a page; 16-byte vector copies.
+__global__ void __launch_bounds__(256)
+    gather_kernel(const uint4 *pool, const int32_t *pages, uint4 *staging, uint64_t page_vec)
+{
+    const int32_t page = pages[blockIdx.x];
+    const uint4 *src = pool + static_cast<uint64_t>(page) * page_vec;
+    uint4 *dst = staging + static_cast<uint64_t>(blockIdx.x) * page_vec;
+    const uint64_t per = (page_vec + gridDim.y - 1) / gridDim.y;
+    const uint64_t a = blockIdx.y * per;
+    const uint64_t e = min(page_vec, a + per);
+    for (uint64_t i = a + threadIdx.x; i < e; i += blockDim.x)
+        dst[i] = __ldcs(src + i);
+}
+
+__global__ void patch_kernel(const Geo g, int32_t *table, kvs_record *recs, const Patch *p,
+                             uint32_t n)
+{
+    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n)
+        return;
+    const Patch q = p[i];
+    const size_t idx = static_cast<size_t>(q.slot) * g.mb + q.block;
+    table[idx] = q.page;
+    if (q.has_record)
+        recs[idx] = q.rec;
+}
+
+__global__ void copy_mass_kernel(const Geo g, const Work w, const float *src, float *mass)
+{
+    const DSet *ds = w.dset;
+    const uint32_t ci = blockIdx.y;
+    const DSeq sq = ds->seq[ci];
+    for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < sq.nb; b += gridDim.x * blockDim.x)
+        mass[static_cast<size_t>(sq.slot) * g.mb + b] = src[static_cast<size_t>(ci) * g.mb + b];
+}
+
+}  // namespace
+
+cudaError_t launch_append(const Geo &g, const AppendArgs &a, cudaStream_t s)
+{
+    const uint32_t vec_per_row = g.d * 2 / 16;
+    // rows cover every slot from p0 to the end of the last touched block
+    const uint64_t slots = static_cast<uint64_t>(a.first_blk + a.nblk) * kBlockTokens - a.p0;
+    const uint64_t rows = slots * g.L * 2 * g.Hkv;
+    const uint64_t nnew = a.first_blk + a.nblk - a.first_new;
+    const uint64_t threads = rows * vec_per_row + nnew;
+    const uint32_t bs = 256;
+    const uint64_t grid = (threads + bs - 1) / bs;
+    if (grid > 0x7fffffffull)
+        return cudaErrorInvalidValue;
+    append_kernel<<<static_cast<uint32_t>(grid), bs, 0, s>>>(g, a, rows, vec_per_row);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const float *mass,
+                         double alpha, uint32_t W, double wR, double wE, double wN, double lo,
+                         double hi, uint32_t nb_total, cudaStream_t s)
+{
+    ScoreArgs sa{alpha, wR, wE, wN, lo, hi, W};
+    score_kernel<<<(nb_total + 127) / 128, 128, 0, s>>>(g, w, rec, mass, sa, nb_total);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *rec,
+                                uint32_t nb_total, uint32_t k, cudaStream_t s)
+{
+    radix_select_kernel<<<1, 1024, 0, s>>>(g, w, rec, nb_total, k);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table,
+                          int mode, uint32_t nb_total, cudaStream_t s)
+{
+    const uint32_t ntiles = (nb_total + kSelTile - 1) / kSelTile;
+    select_count_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, mode, nb_total);
+    select_scatter_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, table, mode, nb_total, ntiles);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pages, uint32_t npages,
+                          uint8_t *staging, cudaStream_t s)
+{
+    const uint64_t page_vec = g.page_bytes / 16;
+    const uint32_t parts = static_cast<uint32_t>(std::max<uint64_t>(1, std::min<uint64_t>(64, page_vec / 4096)));
+    gather_kernel<<<dim3(npages, parts), 256, 0, s>>>(reinterpret_cast<const uint4 *>(pool), pages,
+                                                     reinterpret_cast<uint4 *>(staging), page_vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, const Patch *p, uint32_t n,
+                         cudaStream_t s)
+{
+    patch_kernel<<<(n + 127) / 128, 128, 0, s>>>(g, table, rec, p, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_mass(const Geo &g, const Work &w, const float *src, float *mass,
+                             uint32_t nseq, cudaStream_t s)
+{
+    copy_mass_kernel<<<dim3(std::max<uint32_t>(1, (g.mb + 255) / 256), nseq), 256, 0, s>>>(g, w, src, mass);
+    return cudaGetLastError();
+}
+
+}  // namespace kvs

@@ -1,0 +1,505 @@
+// Paged GQA decode with per-block attention mass (sm_103a).
+//
+// Sources: "KV-Cache Offloading for LLM Inference -- Visual Reference" s.4
+// (a decode step reads every cached token of the sequence) and the "GQA
+// per-head attention as scoring streams" page (query heads grouped 8:1 onto
+// a KV head; every (layer, KV head) stream contributes to one mass per
+// (sequence, 16-token block)).
+//
+// Structure of one step:
+//   decode_kernel  -- persistent CTAs pull work items (sequence, layer, group
+//                     of KV heads, chunk of 64 blocks).  Each warp owns one KV
+//                     head: a TMA ring streams the head's 4 KiB K and V
+//                     sub-pages of each block into shared memory (128-byte
+//                     swizzle), and warp-level tensor-core MMAs compute
+//                       S^T[16 tokens][8 heads] = K . Q^T
+//                       O^T[d][8 heads]        += V^T . P^T
+//                     with an online softmax in registers.  Per block it writes
+//                     the block's log2-sum-exp for each query head; per chunk
+//                     the running max, sum and unnormalised output.
+//   combine_kernel -- merges a stream's chunks: per head log2-sum-exp LSE_h and
+//                     the normalised output.
+//   mass_kernel    -- M(b) = 1/(L*Hq) * sum_{l,h} 2^(lse_blk(l,h,b) - LSE_h),
+//                     summed in a fixed order (deterministic).
+#include <cuda_bf16.h>
+
+#include "kvs_internal.h"
+
+namespace kvs {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float fast_log2(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after `limit` polls and reports it.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, uint32_t *err)
+{
+    for (uint32_t i = 0; i < (1u << 22); ++i)
+        if (mbar_try_wait(bar, phase))
+            return true;
+    atomicOr(err, kErrTmaTimeout);
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &a0, uint32_t &a1, uint32_t &a2,
+                                        uint32_t &a3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &a0, uint32_t &a1, uint32_t &a2,
+                                          uint32_t &a3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr));
+}
+
+// D (16x8 f32) += A (16x16 bf16, row) * B (16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t find_seq(const uint32_t *off_base, size_t stride_words,
+                                             uint32_t nseq, uint32_t x)
+{
+    // largest i with off(i) <= x; off() read with a stride (fields of DSeq)
+    uint32_t lo = 0, hi = nseq;
+    while (hi - lo > 1) {
+        uint32_t mid = (lo + hi) >> 1;
+        if (off_base[mid * stride_words] <= x)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+struct DecodeArgs {
+    Geo g;
+    Work w;
+    const uint16_t *q;
+    const int32_t *table;
+    uint32_t n_items;
+    uint32_t wg;
+};
+
+// Bytes of one block's K and V sub-pages for one KV head.
+template <int D>
+struct Tile {
+    static constexpr int kHalf = D / 64;                 // 64-wide TMA boxes
+    static constexpr int kBoxBytes = 2 * 16 * 64 * 2;    // [K,V][16 tok][64 dims] bf16
+    static constexpr int kStageBytes = kHalf * kBoxBytes;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a)
+{
+    using T = Tile<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[8][kStages];
+    __shared__ uint32_t item_sh;
+
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // 1024-byte alignment for the 128-byte swizzle atoms
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *ring = smem + warp * kStages * T::kStageBytes;
+    const uint32_t ring_u32 = smem_u32(ring);
+
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(smem_u32(&bars[warp][s]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+
+    const Geo &g = a.g;
+    const DSet *ds = a.w.dset;
+    const uint32_t G = g.G;
+    const uint32_t gq = lane >> 2;          // row group id in MMA fragments
+    const uint32_t tq = lane & 3;           // thread in group
+    const uint32_t h0 = 2 * tq, h1 = 2 * tq + 1;   // heads of this lane's S/O columns
+    const float scale_log2 = rsqrtf(static_cast<float>(D)) * kLog2e;
+    uint32_t kload = 0;                     // blocks this warp has consumed so far
+
+    for (;;) {
+        __syncthreads();
+        if (threadIdx.x == 0)
+            item_sh = atomicAdd(a.w.counter, 1u);
+        __syncthreads();
+        const uint32_t item = item_sh;
+        if (item >= a.n_items)
+            break;
+
+        // ---- decode the work item -------------------------------------
+        const uint32_t ci = find_seq(&ds->seq[0].item_off, sizeof(DSeq) / 4, ds->nseq, item);
+        const DSeq sq = ds->seq[ci];
+        uint32_t local = item - sq.item_off;
+        const uint32_t chunk = local % sq.nchunk;
+        local /= sq.nchunk;
+        const uint32_t ngg = g.Hkv / a.wg;
+        const uint32_t l = local / ngg, gg = local % ngg;
+        const uint32_t kvh = gg * a.wg + warp;
+        const uint32_t b0 = chunk * kChunkBlocks;
+        const uint32_t nblk = min(static_cast<uint32_t>(kChunkBlocks), sq.nb - b0);
+
+        // page ids of the chunk's blocks (lane j holds blocks j and 32 + j)
+        const int32_t *trow = a.table + static_cast<size_t>(sq.slot) * g.mb + b0;
+        int32_t pg_lo = lane < nblk ? __ldg(trow + lane) : 0;
+        int32_t pg_hi = lane + 32 < nblk ? __ldg(trow + lane + 32) : 0;
+        if (pg_lo < 0 || pg_lo >= static_cast<int32_t>(g.pool_blocks)) {
+            if (lane < nblk) {
+                atomicOr(a.w.err, kErrBadPage);
+                atomicCAS(a.w.err_info, 0u, static_cast<uint32_t>(pg_lo) | 0x80000000u);
+            }
+            pg_lo = 0;
+        }
+        if (pg_hi < 0 || pg_hi >= static_cast<int32_t>(g.pool_blocks)) {
+            if (lane + 32 < nblk) {
+                atomicOr(a.w.err, kErrBadPage);
+                atomicCAS(a.w.err_info, 0u, static_cast<uint32_t>(pg_hi) | 0x80000000u);
+            }
+            pg_hi = 0;
+        }
+
+        // query fragments (B operand of S^T = K Q^T): head gq, dims 16ks+2tq(+1), +8
+        uint32_t qf[D / 16][2];
+        {
+            const bool valid = gq < G;
+            const uint16_t *qh =
+                a.q + ((static_cast<size_t>(ci) * g.L + l) * g.Hq + kvh * G + (valid ? gq : 0)) * D;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                qf[ks][0] = valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 2 * tq)) : 0u;
+                qf[ks][1] =
+                    valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 8 + 2 * tq)) : 0u;
+            }
+        }
+
+        // ---- prologue: fill the ring ------------------------------------
+        auto issue = [&](uint32_t i) {
+            const int32_t page = __shfl_sync(0xffffffffu, i < 32 ? pg_lo : pg_hi, i & 31);
+            if (lane == 0) {
+                const uint32_t st = (kload + i) % kStages;
+                const uint32_t bar = smem_u32(&bars[warp][st]);
+                mbar_expect_tx(bar, T::kStageBytes);
+                const int c4 = page * static_cast<int>(g.L) + static_cast<int>(l);
+#pragma unroll
+                for (int h = 0; h < T::kHalf; ++h)
+                    tma_load_5d(ring_u32 + st * T::kStageBytes + h * T::kBoxBytes, &tmap, bar, h * 64,
+                                0, static_cast<int>(kvh), 0, c4);
+            }
+        };
+        const uint32_t npre = min(nblk, static_cast<uint32_t>(kStages));
+        for (uint32_t i = 0; i < npre; ++i)
+            issue(i);
+
+        float o[D / 16][4];
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+            o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+        const uint32_t jm = lane >> 3, i8 = lane & 7;
+        float *lse_row0 = a.w.lse_blk + (static_cast<size_t>(l) * g.Hq + kvh * G + h0) * ds->nb_total +
+                          sq.blk_off + b0;
+        const size_t lse_head_stride = ds->nb_total;
+
+        for (uint32_t i = 0; i < nblk; ++i) {
+            const uint32_t k = kload + i;
+            const uint32_t st = k % kStages;
+            mbar_wait(smem_u32(&bars[warp][st]), (k / kStages) & 1u, a.w.err);
+            const uint32_t base = ring_u32 + st * T::kStageBytes;
+
+            // S^T = K . Q^T  (rows: 16 tokens, cols: 8 heads)
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t h = ks >> 2, c0 = (ks & 3) * 2;
+                const uint32_t row = i8 + 8 * (jm & 1);          // token, K half
+                const uint32_t chunk16 = c0 + (jm >> 1);
+                const uint32_t addr = base + h * T::kBoxBytes + row * 128 + ((chunk16 ^ (row & 7)) << 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(addr, a0, a1, a2, a3);
+                mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            }
+            const uint32_t blk = b0 + i;
+            const uint32_t tok0 = blk * kBlockTokens + gq, tok1 = tok0 + 8;
+            s[0] = tok0 < sq.ntok ? s[0] * scale_log2 : -INFINITY;
+            s[1] = tok0 < sq.ntok ? s[1] * scale_log2 : -INFINITY;
+            s[2] = tok1 < sq.ntok ? s[2] * scale_log2 : -INFINITY;
+            s[3] = tok1 < sq.ntok ? s[3] * scale_log2 : -INFINITY;
+
+            float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
+            const float p0 = fast_exp2(s[0] - mn0), p1 = fast_exp2(s[1] - mn1);
+            const float p2 = fast_exp2(s[2] - mn0), p3 = fast_exp2(s[3] - mn1);
+            float w0 = p0 + p2, w1 = p1 + p3;
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                w0 += __shfl_xor_sync(0xffffffffu, w0, x);
+                w1 += __shfl_xor_sync(0xffffffffu, w1, x);
+            }
+            l0 = l0 * sc0 + w0;
+            l1 = l1 * sc1 + w1;
+            m0 = mn0;
+            m1 = mn1;
+            if (gq == 0) {
+                if (h0 < G)
+                    lse_row0[i] = mn0 + fast_log2(w0);
+                if (h1 < G)
+                    lse_row0[lse_head_stride + i] = mn1 + fast_log2(w1);
+            }
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                o[mt][0] *= sc0;
+                o[mt][1] *= sc1;
+                o[mt][2] *= sc0;
+                o[mt][3] *= sc1;
+            }
+            // P^T as the B operand: transpose the two 8x8 bf16 tiles in registers
+            const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
+            const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
+            // O^T += V^T . P^T  (rows: d, cols: 8 heads)
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const uint32_t h = mt >> 2, c0 = (mt & 3) * 2;
+                const uint32_t row = 16 + i8 + 8 * (jm >> 1);    // V half, token
+                const uint32_t chunk16 = c0 + (jm & 1);
+                const uint32_t addr = base + h * T::kBoxBytes + row * 128 + ((chunk16 ^ (row & 7)) << 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(addr, a0, a1, a2, a3);
+                mma_bf16(o[mt], a0, a1, a2, a3, pb0, pb1);
+            }
+            __syncwarp();
+            if (i + kStages < nblk)
+                issue(i + kStages);
+        }
+        kload += nblk;
+
+        // ---- chunk partials ----------------------------------------------
+        const uint32_t part = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk + chunk;
+        if (gq == 0) {
+            a.w.part_ml[part * kMaxGroup + h0] = make_float2(m0, l0);
+            a.w.part_ml[part * kMaxGroup + h1] = make_float2(m1, l1);
+        }
+        float *po = a.w.part_o + static_cast<size_t>(part) * kMaxGroup * D;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            po[h0 * D + mt * 16 + gq] = o[mt][0];
+            po[h1 * D + mt * 16 + gq] = o[mt][1];
+            po[h0 * D + mt * 16 + gq + 8] = o[mt][2];
+            po[h1 * D + mt * 16 + gq + 8] = o[mt][3];
+        }
+    }
+}
+
+// One CTA per (sequence, layer, KV head); warp h merges query head h's chunks.
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w, float *out)
+{
+    const DSet *ds = w.dset;
+    const uint32_t lane = threadIdx.x & 31, h = threadIdx.x >> 5;
+    const uint32_t ci = blockIdx.x / (g.L * g.Hkv);
+    const uint32_t rest = blockIdx.x % (g.L * g.Hkv);
+    const uint32_t l = rest / g.Hkv, kvh = rest % g.Hkv;
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *w.counter = 0;            // ready for the next decode launch
+    if (h >= g.G)
+        return;
+    const DSeq sq = ds->seq[ci];
+    const uint32_t pb = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk;
+    float mmax = -INFINITY;
+    for (uint32_t c = 0; c < sq.nchunk; ++c)
+        mmax = fmaxf(mmax, w.part_ml[(pb + c) * kMaxGroup + h].x);
+    constexpr int E = D / 32;
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        acc[e] = 0.f;
+    float lsum = 0.f;
+    for (uint32_t c = 0; c < sq.nchunk; ++c) {
+        const float2 ml = w.part_ml[(pb + c) * kMaxGroup + h];
+        const float f = fast_exp2(ml.x - mmax);
+        lsum += ml.y * f;
+        const float *po = w.part_o + (static_cast<size_t>(pb + c) * kMaxGroup + h) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            acc[e] += po[e] * f;
+    }
+    const float inv = 1.f / lsum;
+    const uint32_t hq = kvh * g.G + h;
+    float *dst = out + ((static_cast<size_t>(ci) * g.L + l) * g.Hq + hq) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        dst[e] = acc[e] * inv;
+    if (lane == 0)
+        w.lse_head[static_cast<size_t>(ci) * g.L * g.Hq + l * g.Hq + hq] = mmax + fast_log2(lsum);
+}
+
+// 32 consecutive blocks per CTA x 8 partial sums over (layer, head) pairs.
+__global__ void __launch_bounds__(256) mass_kernel(const Geo g, const Work w, float *mass,
+                                                   uint32_t nb_total)
+{
+    __shared__ float part[8][33];
+    const DSet *ds = w.dset;
+    const uint32_t i = threadIdx.x & 31, j = threadIdx.x >> 5;
+    const uint32_t r = blockIdx.x * 32 + i;
+    const uint32_t LH = g.L * g.Hq;
+    float acc = 0.f;
+    uint32_t ci = 0;
+    if (r < nb_total) {
+        ci = find_seq(&ds->seq[0].blk_off, sizeof(DSeq) / 4, ds->nseq, r);
+        const float *lh_row = w.lse_head + static_cast<size_t>(ci) * LH;
+        for (uint32_t lh = j; lh < LH; lh += 8)
+            acc += fast_exp2(w.lse_blk[static_cast<size_t>(lh) * nb_total + r] - lh_row[lh]);
+    }
+    part[j][i] = acc;
+    __syncthreads();
+    if (j == 0 && r < nb_total) {
+        float t = part[0][i];
+#pragma unroll
+        for (int q = 1; q < 8; ++q)
+            t += part[q][i];
+        const DSeq sq = ds->seq[ci];
+        mass[static_cast<size_t>(sq.slot) * g.mb + (r - sq.blk_off)] = t / static_cast<float>(LH);
+    }
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(const Geo &g, uint32_t wg)
+{
+    const size_t stage = g.d == 128 ? Tile<128>::kStageBytes : Tile<64>::kStageBytes;
+    return wg * kStages * stage + 1024;   // + alignment slack
+}
+
+int decode_blocks_per_sm(const Geo &g, uint32_t wg)
+{
+    int n = 0;
+    const size_t smem = decode_smem_bytes(g, wg);
+    if (g.d == 128) {
+        cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<128>, 32 * wg, smem);
+    } else {
+        cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<64>, 32 * wg, smem);
+    }
+    return n;
+}
+
+cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w, const uint16_t *q,
+                          const int32_t *table, uint32_t n_items, uint32_t wg, int grid,
+                          cudaStream_t s)
+{
+    DecodeArgs a{g, w, q, table, n_items, wg};
+    const size_t smem = decode_smem_bytes(g, wg);
+    if (g.d == 128)
+        decode_kernel<128><<<grid, 32 * wg, smem, s>>>(tmap, a);
+    else
+        decode_kernel<64><<<grid, 32 * wg, smem, s>>>(tmap, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq, cudaStream_t s)
+{
+    const dim3 grid(nseq * g.L * g.Hkv);
+    if (g.d == 128)
+        combine_kernel<128><<<grid, 32 * kMaxGroup, 0, s>>>(g, w, out);
+    else
+        combine_kernel<64><<<grid, 32 * kMaxGroup, 0, s>>>(g, w, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total, cudaStream_t s)
+{
+    mass_kernel<<<(nb_total + 31) / 32, 256, 0, s>>>(g, w, mass, nb_total);
+    return cudaGetLastError();
+}
+
+}  // namespace kvs

@@ -1,0 +1,1183 @@
+// Host layer of the C ABI: configuration checks, free list and reference
+// counts of the page pool, per-sequence block tables, the identity-keyed
+// store of demoted blocks, the pinned upload ring and the launch sequence of
+// every call.
+//
+// Sources: "LLM KV cache offload" (block manager, block tables, reference
+// counts freeing a shared block only with its last user, demotion through
+// pinned host staging on the copy engines); "GQA per-head attention as
+// scoring streams" (identity key and score persist across eviction and are
+// restored on re-admission); "RETRACTIONS" s.2 (blocks are write-once).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <map>
+#include <memory>
+#include <string>
+#include <unordered_map>
+#include <utility>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "kvs_internal.h"
+
+using namespace kvs;
+
+namespace {
+
+constexpr uint32_t kRingSlots = 8;
+constexpr size_t kRingSlotBytes = size_t(1) << 20;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+uint64_t splitmix64(uint64_t &s)
+{
+    uint64_t z = (s += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+struct SeqState {
+    uint64_t id = 0;
+    bool live = false;
+    uint32_t ntok = 0;
+    uint32_t shared_blocks = 0;      // leading blocks shared read-only
+    std::vector<int32_t> table;      // page per block, -1 = demoted
+};
+
+struct Demoted {
+    kvs_record rec;
+    uint64_t host_off;
+};
+
+}  // namespace
+
+struct kvs_ctx {
+    kvs_config cfg{};
+    Geo geo{};
+    Layout lay{};
+    Work work{};
+    kvs_buffers buf{};
+    kvs_sizes sz{};
+    int device = 0;
+    int sm_count = 0;
+    int decode_grid = 0;
+    uint32_t wg = 1;
+    alignas(64) CUtensorMap tmap;
+
+    std::vector<SeqState> seqs;                     // by slot
+    std::unordered_map<uint64_t, uint32_t> slot_of;
+    std::vector<uint32_t> free_slots;
+    std::deque<int32_t> free_pages;
+    std::vector<uint32_t> refcnt;
+    std::vector<uint8_t> mirror_clean;              // host mirror copy is current
+    std::map<std::pair<uint64_t, uint64_t>, Demoted> store;
+    uint64_t t = 0;
+
+    std::unique_ptr<DSet> dset;                     // host copy of the current set
+    bool have_set = false;
+
+    uint8_t *ring_host = nullptr;                   // pinned upload ring
+    cudaEvent_t ring_ev[kRingSlots]{};
+    bool ring_used[kRingSlots]{};
+    uint32_t ring_next = 0;
+    uint32_t *pinned_small = nullptr;               // readbacks
+
+    cudaEvent_t ev_ready[2]{}, ev_free[2]{}, ev_side_done{}, ev_pool_release{};
+    bool side_pending = false, release_pending = false;
+
+    std::string err;
+};
+
+namespace {
+
+int fail(kvs_ctx *c, int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (c)
+        c->err = buf;
+    return code;
+}
+
+#define CU(call)                                                                         \
+    do {                                                                                 \
+        cudaError_t e_ = (call);                                                         \
+        if (e_ != cudaSuccess)                                                           \
+            return fail(ctx, KVS_ECUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                        __FILE__, __LINE__);                                             \
+    } while (0)
+
+cudaStream_t S(void *s) { return static_cast<cudaStream_t>(s); }
+
+struct RingSlot {
+    uint32_t idx;
+    uint8_t *host;
+    uint8_t *dev;
+};
+
+// Takes the next ring slot (waiting for its previous user to finish).
+int ring_acquire(kvs_ctx *ctx, size_t bytes, RingSlot *out)
+{
+    if (bytes > kRingSlotBytes)
+        return fail(ctx, KVS_EINVAL, "upload of %zu bytes exceeds the ring slot (%zu)", bytes,
+                    kRingSlotBytes);
+    const uint32_t i = ctx->ring_next;
+    ctx->ring_next = (i + 1) % kRingSlots;
+    if (ctx->ring_used[i])
+        CU(cudaEventSynchronize(ctx->ring_ev[i]));
+    out->idx = i;
+    out->host = ctx->ring_host + i * kRingSlotBytes;
+    out->dev = ctx->work.ring + i * kRingSlotBytes;
+    return KVS_OK;
+}
+
+// Copies the slot's bytes to its device side on `s` (after the host filled it).
+int ring_push(kvs_ctx *ctx, const RingSlot &r, size_t bytes, cudaStream_t s)
+{
+    CU(cudaMemcpyAsync(r.dev, r.host, bytes, cudaMemcpyHostToDevice, s));
+    return KVS_OK;
+}
+
+// Marks the slot busy until `s` passes this point (after its consumers).
+int ring_release(kvs_ctx *ctx, const RingSlot &r, cudaStream_t s)
+{
+    CU(cudaEventRecord(ctx->ring_ev[r.idx], s));
+    ctx->ring_used[r.idx] = true;
+    return KVS_OK;
+}
+
+// Orders page writes on `s` after device->host copies still reading pages
+// and after the release of pages by kvs_seq_remove.
+int order_pool_writes(kvs_ctx *ctx, cudaStream_t s)
+{
+    if (ctx->side_pending)
+        CU(cudaStreamWaitEvent(s, ctx->ev_side_done, 0));
+    if (ctx->release_pending)
+        CU(cudaStreamWaitEvent(s, ctx->ev_pool_release, 0));
+    return KVS_OK;
+}
+
+int check_cfg(const kvs_config *c, kvs_ctx *ctx)
+{
+    if (!c)
+        return fail(ctx, KVS_EINVAL, "null config");
+    if (c->block_tokens != KVS_BLOCK_TOKENS)
+        return fail(ctx, KVS_EINVAL, "block_tokens must be 16");
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return fail(ctx, KVS_EINVAL, "head_dim must be 64 or 128");
+    if (!c->num_layers || !c->num_kv_heads || !c->num_q_heads ||
+        c->num_q_heads % c->num_kv_heads)
+        return fail(ctx, KVS_EINVAL, "head counts: Hq must be a positive multiple of Hkv");
+    if (c->num_q_heads / c->num_kv_heads > static_cast<uint32_t>(kMaxGroup))
+        return fail(ctx, KVS_EINVAL, "at most 8 query heads per KV head");
+    if (!c->pool_blocks || !c->max_seqs || !c->max_blocks_per_seq || !c->staging_pages)
+        return fail(ctx, KVS_EINVAL, "pool_blocks, max_seqs, max_blocks_per_seq, staging_pages must be > 0");
+    if (static_cast<uint64_t>(c->num_layers) * c->pool_blocks >= (1ull << 31))
+        return fail(ctx, KVS_EINVAL, "layers * pool_blocks must stay below 2^31");
+    if (!(c->alpha >= 0.0 && c->alpha <= 1.0) || !c->recency_window)
+        return fail(ctx, KVS_EINVAL, "alpha must be in [0, 1] and recency_window > 0");
+    if (!(c->cut_lo <= c->cut_hi))
+        return fail(ctx, KVS_EINVAL, "cut_lo must not exceed cut_hi");
+    return KVS_OK;
+}
+
+uint32_t pick_wg(uint32_t hkv)
+{
+    for (uint32_t w : {4u, 2u, 1u})
+        if (hkv % w == 0)
+            return w;
+    return 1;
+}
+
+SeqState *find_seq(kvs_ctx *ctx, uint64_t id, uint32_t *slot = nullptr)
+{
+    auto it = ctx->slot_of.find(id);
+    if (it == ctx->slot_of.end())
+        return nullptr;
+    if (slot)
+        *slot = it->second;
+    return &ctx->seqs[it->second];
+}
+
+// Builds the decode set for seq_ids (call order); validates residency.
+int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
+{
+    if (!ids || nseq == 0 || nseq > kMaxCallSeqs)
+        return fail(ctx, KVS_EINVAL, "nseq must be in [1, %u]", kMaxCallSeqs);
+    std::memset(ds, 0, sizeof(DSet));
+    const Geo &g = ctx->geo;
+    const uint32_t ngg = g.Hkv / ctx->wg;
+    uint32_t blk = 0, items = 0, parts = 0;
+    std::vector<std::pair<uint64_t, uint32_t>> order;
+    order.reserve(nseq);
+    for (uint32_t i = 0; i < nseq; ++i) {
+        uint32_t slot;
+        SeqState *s = find_seq(ctx, ids[i], &slot);
+        if (!s)
+            return fail(ctx, KVS_ENOTFOUND, "unknown sequence %llu", (unsigned long long)ids[i]);
+        if (s->ntok == 0)
+            return fail(ctx, KVS_EINVAL, "sequence %llu has no tokens", (unsigned long long)ids[i]);
+        for (int32_t p : s->table)
+            if (p < 0)
+                return fail(ctx, KVS_EINVAL, "sequence %llu has a demoted block; re-admit it first",
+                            (unsigned long long)ids[i]);
+        DSeq &q = ds->seq[i];
+        q.slot = slot;
+        q.ntok = s->ntok;
+        q.nb = (s->ntok + kBlockTokens - 1) / kBlockTokens;
+        q.nchunk = (q.nb + kChunkBlocks - 1) / kChunkBlocks;
+        q.blk_off = blk;
+        q.item_off = items;
+        q.part_off = parts;
+        q.seq_id = ids[i];
+        blk += q.nb;
+        items += g.L * ngg * q.nchunk;
+        parts += g.L * g.Hkv * q.nchunk;
+        order.emplace_back(ids[i], i);
+    }
+    std::sort(order.begin(), order.end());
+    for (uint32_t i = 1; i < nseq; ++i)
+        if (order[i].first == order[i - 1].first)
+            return fail(ctx, KVS_EINVAL, "sequence %llu listed twice",
+                        (unsigned long long)order[i].first);
+    if (blk > ctx->lay.nb_max)
+        return fail(ctx, KVS_EINVAL, "%u blocks in one call exceed max_call_blocks %u", blk,
+                    ctx->lay.nb_max);
+    if (parts > ctx->lay.parts_max)
+        return fail(ctx, KVS_EINVAL, "too many decode partials (%u > %u)", parts, ctx->lay.parts_max);
+    uint32_t off = 0;
+    for (uint32_t i = 0; i < nseq; ++i) {
+        ds->sorted[i] = order[i].second;
+        ds->srt_off[i] = off;
+        off += ds->seq[order[i].second].nb;
+    }
+    ds->srt_off[nseq] = off;
+    ds->nseq = nseq;
+    ds->nb_total = blk;
+    ds->n_items = items;
+    ds->n_parts = parts;
+    ds->wg = ctx->wg;
+    ds->t = ctx->t;
+    return KVS_OK;
+}
+
+int upload_set(kvs_ctx *ctx, const DSet &ds, cudaStream_t s)
+{
+    RingSlot r;
+    int rc = ring_acquire(ctx, sizeof(DSet), &r);
+    if (rc)
+        return rc;
+    std::memcpy(r.host, &ds, sizeof(DSet));
+    CU(cudaMemcpyAsync(ctx->work.dset, r.host, sizeof(DSet), cudaMemcpyHostToDevice, s));
+    return ring_release(ctx, r, s);
+}
+
+int launch_rc(kvs_ctx *ctx, cudaError_t e, const char *what)
+{
+    if (e != cudaSuccess)
+        return fail(ctx, KVS_ECUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+    return KVS_OK;
+}
+
+// Patch list upload + kernel (table entries and records).
+int apply_patches(kvs_ctx *ctx, const std::vector<Patch> &p, cudaStream_t s)
+{
+    const size_t per = kRingSlotBytes / sizeof(Patch);
+    for (size_t a = 0; a < p.size(); a += per) {
+        const size_t n = std::min(per, p.size() - a);
+        RingSlot r;
+        int rc = ring_acquire(ctx, n * sizeof(Patch), &r);
+        if (rc)
+            return rc;
+        std::memcpy(r.host, p.data() + a, n * sizeof(Patch));
+        if ((rc = ring_push(ctx, r, n * sizeof(Patch), s)))
+            return rc;
+        if ((rc = launch_rc(ctx,
+                            launch_patch(ctx->geo, static_cast<int32_t *>(ctx->buf.block_table),
+                                         static_cast<kvs_record *>(ctx->buf.records),
+                                         reinterpret_cast<const Patch *>(r.dev),
+                                         static_cast<uint32_t>(n), s),
+                            "patch")))
+            return rc;
+        if ((rc = ring_release(ctx, r, s)))
+            return rc;
+    }
+    return KVS_OK;
+}
+
+kvs_record fresh_record(uint64_t seq_id, uint64_t b, uint64_t t)
+{
+    kvs_record r;
+    std::memset(&r, 0, sizeof r);
+    r.key.seq_id = seq_id;
+    r.key.block_idx = b;
+    r.last_touch = t;
+    r.tier = 255;
+    return r;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- layout
+
+namespace kvs {
+
+Layout workspace_layout(const kvs_config &c)
+{
+    Layout L{};
+    const size_t nb_max = c.max_call_blocks ? c.max_call_blocks
+                                            : static_cast<size_t>(c.max_seqs) * c.max_blocks_per_seq;
+    const size_t seqs = std::min<size_t>(c.max_seqs, kMaxCallSeqs);
+    const size_t LH = static_cast<size_t>(c.num_layers) * c.num_q_heads;
+    L.nb_max = static_cast<uint32_t>(nb_max);
+    L.parts_max = static_cast<uint32_t>(static_cast<size_t>(c.num_layers) * c.num_kv_heads *
+                                        ((nb_max + kChunkBlocks - 1) / kChunkBlocks + seqs));
+    L.tiles_max = static_cast<uint32_t>((nb_max + 1023) / 1024 + 1);
+    L.ring_slots = kRingSlots;
+    L.ring_slot_bytes = kRingSlotBytes;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.err = take(64);
+    L.counter = take(64);
+    L.sel_count = take(64);
+    L.sel_thr = take(64);
+    L.dset = take(sizeof(DSet));
+    L.part_ml = take(static_cast<size_t>(L.parts_max) * kMaxGroup * sizeof(float2));
+    L.part_o = take(static_cast<size_t>(L.parts_max) * kMaxGroup * c.head_dim * sizeof(float));
+    L.lse_blk = take(LH * nb_max * sizeof(float));
+    L.lse_head = take(seqs * LH * sizeof(float));
+    L.tile_cnt = take(L.tiles_max * sizeof(uint32_t));
+    L.sel_ids = take(nb_max * sizeof(kvs_key));
+    L.sel_pages = take(nb_max * sizeof(int32_t));
+    L.sel_recidx = take(nb_max * sizeof(uint32_t));
+    L.sel_recs = take(nb_max * sizeof(kvs_record));
+    L.ring = take(kRingSlots * kRingSlotBytes);
+    L.total = o;
+    return L;
+}
+
+Work carve(const Layout &L, void *ws)
+{
+    uint8_t *b = static_cast<uint8_t *>(ws);
+    Work w{};
+    w.err = reinterpret_cast<uint32_t *>(b + L.err);
+    w.err_info = w.err + 1;
+    w.counter = reinterpret_cast<uint32_t *>(b + L.counter);
+    w.sel_count = reinterpret_cast<uint32_t *>(b + L.sel_count);
+    w.sel_thr = reinterpret_cast<uint64_t *>(b + L.sel_thr);
+    w.dset = reinterpret_cast<DSet *>(b + L.dset);
+    w.part_ml = reinterpret_cast<float2 *>(b + L.part_ml);
+    w.part_o = reinterpret_cast<float *>(b + L.part_o);
+    w.lse_blk = reinterpret_cast<float *>(b + L.lse_blk);
+    w.lse_head = reinterpret_cast<float *>(b + L.lse_head);
+    w.tile_cnt = reinterpret_cast<uint32_t *>(b + L.tile_cnt);
+    w.sel_ids = reinterpret_cast<kvs_key *>(b + L.sel_ids);
+    w.sel_pages = reinterpret_cast<int32_t *>(b + L.sel_pages);
+    w.sel_recidx = reinterpret_cast<uint32_t *>(b + L.sel_recidx);
+    w.sel_recs = reinterpret_cast<kvs_record *>(b + L.sel_recs);
+    w.ring = b + L.ring;
+    return w;
+}
+
+}  // namespace kvs
+
+// ------------------------------------------------------------------ ABI
+
+extern "C" {
+
+int kvs_required_sizes(const kvs_config *cfg, kvs_sizes *out)
+{
+    kvs_ctx *ctx = nullptr;
+    int rc = check_cfg(cfg, ctx);
+    if (rc)
+        return rc;
+    if (!out)
+        return KVS_EINVAL;
+    const kvs_config &c = *cfg;
+    const size_t rows = static_cast<size_t>(c.max_seqs) * c.max_blocks_per_seq;
+    out->page_bytes = static_cast<size_t>(2) * c.num_layers * c.num_kv_heads * KVS_BLOCK_TOKENS *
+                      c.head_dim * 2;
+    out->pool_bytes = out->page_bytes * c.pool_blocks;
+    out->table_bytes = rows * sizeof(int32_t);
+    out->records_bytes = rows * sizeof(kvs_record);
+    out->mass_bytes = rows * sizeof(float);
+    out->workspace_bytes = workspace_layout(c).total;
+    out->staging_bytes = out->page_bytes * c.staging_pages;
+    return KVS_OK;
+}
+
+int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
+{
+    if (!out)
+        return KVS_EINVAL;
+    *out = nullptr;
+    std::unique_ptr<kvs_ctx> holder(new kvs_ctx());
+    kvs_ctx *ctx = holder.get();
+    int rc = check_cfg(cfg, ctx);
+    if (rc)
+        return rc;
+    if (!buf || !buf->pool || !buf->block_table || !buf->records || !buf->mass || !buf->workspace ||
+        !buf->staging)
+        return fail(ctx, KVS_EINVAL, "every device buffer must be given");
+    for (void *p : {buf->pool, buf->block_table, buf->records, buf->mass, buf->workspace, buf->staging})
+        if (reinterpret_cast<uintptr_t>(p) % 256)
+            return fail(ctx, KVS_EINVAL, "device buffers must be 256-byte aligned");
+    static_assert(sizeof(kvs_record) == KVS_RECORD_BYTES, "record must be 64 bytes");
+    static_assert(sizeof(kvs_key) == 16, "key must be 16 bytes");
+    ctx->cfg = *cfg;
+    ctx->buf = *buf;
+    kvs_required_sizes(cfg, &ctx->sz);
+    ctx->lay = workspace_layout(*cfg);
+    ctx->work = carve(ctx->lay, buf->workspace);
+    Geo &g = ctx->geo;
+    g.L = cfg->num_layers;
+    g.Hq = cfg->num_q_heads;
+    g.Hkv = cfg->num_kv_heads;
+    g.d = cfg->head_dim;
+    g.G = g.Hq / g.Hkv;
+    g.pool_blocks = cfg->pool_blocks;
+    g.max_seqs = cfg->max_seqs;
+    g.mb = cfg->max_blocks_per_seq;
+    g.page_bytes = ctx->sz.page_bytes;
+    ctx->wg = pick_wg(g.Hkv);
+    ctx->dset.reset(new DSet());
+
+    CU(cudaGetDevice(&ctx->device));
+    CU(cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device));
+    const int per_sm = decode_blocks_per_sm(g, ctx->wg);
+    if (per_sm < 1)
+        return fail(ctx, KVS_ECUDA, "decode kernel does not fit on an SM (%zu B shared memory)",
+                    decode_smem_bytes(g, ctx->wg));
+    ctx->decode_grid = per_sm * ctx->sm_count;
+
+    // TMA descriptor of the pool: dims (d, token slot, KV head, K/V, layer*page)
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    CU(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void **>(&encode),
+                                        12000, cudaEnableDefault, &qres));
+    if (qres != cudaDriverEntryPointSuccess || !encode)
+        return fail(ctx, KVS_ECUDA, "cuTensorMapEncodeTiled not available");
+    const cuuint64_t d = g.d;
+    cuuint64_t dims[5] = {d, KVS_BLOCK_TOKENS, g.Hkv, 2, static_cast<cuuint64_t>(g.L) * g.pool_blocks};
+    cuuint64_t strides[4] = {d * 2, KVS_BLOCK_TOKENS * d * 2, g.Hkv * KVS_BLOCK_TOKENS * d * 2,
+                             2ull * g.Hkv * KVS_BLOCK_TOKENS * d * 2};
+    cuuint32_t box[5] = {64, KVS_BLOCK_TOKENS, 1, 2, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult cr = encode(&ctx->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, buf->pool, dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS)
+        return fail(ctx, KVS_ECUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(cr));
+
+    CU(cudaMemset(buf->block_table, 0xff, ctx->sz.table_bytes));
+    CU(cudaMemset(buf->records, 0, ctx->sz.records_bytes));
+    CU(cudaMemset(buf->mass, 0, ctx->sz.mass_bytes));
+    CU(cudaMemset(buf->workspace, 0, ctx->lay.dset));   // error word, counters
+    CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->ring_host), kRingSlots * kRingSlotBytes,
+                     cudaHostAllocDefault));
+    CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->pinned_small), 256, cudaHostAllocDefault));
+    for (auto &e : ctx->ring_ev)
+        CU(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    for (int i = 0; i < 2; ++i) {
+        CU(cudaEventCreateWithFlags(&ctx->ev_ready[i], cudaEventDisableTiming));
+        CU(cudaEventCreateWithFlags(&ctx->ev_free[i], cudaEventDisableTiming));
+    }
+    CU(cudaEventCreateWithFlags(&ctx->ev_side_done, cudaEventDisableTiming));
+    CU(cudaEventCreateWithFlags(&ctx->ev_pool_release, cudaEventDisableTiming));
+    CU(cudaDeviceSynchronize());
+
+    ctx->seqs.resize(cfg->max_seqs);
+    for (uint32_t i = cfg->max_seqs; i > 0; --i)
+        ctx->free_slots.push_back(i - 1);
+    std::vector<int32_t> perm(cfg->pool_blocks);
+    for (uint32_t i = 0; i < cfg->pool_blocks; ++i)
+        perm[i] = static_cast<int32_t>(i);
+    uint64_t st = cfg->pool_seed;
+    for (uint32_t i = cfg->pool_blocks; i > 1; --i) {   // Fisher-Yates
+        const uint32_t j = static_cast<uint32_t>(splitmix64(st) % i);
+        std::swap(perm[i - 1], perm[j]);
+    }
+    ctx->free_pages.assign(perm.begin(), perm.end());
+    ctx->refcnt.assign(cfg->pool_blocks, 0);
+    ctx->mirror_clean.assign(cfg->pool_blocks, 0);
+    *out = holder.release();
+    return KVS_OK;
+}
+
+void kvs_destroy(kvs_ctx_t *ctx)
+{
+    if (!ctx)
+        return;
+    cudaDeviceSynchronize();
+    for (auto &e : ctx->ring_ev)
+        if (e)
+            cudaEventDestroy(e);
+    for (int i = 0; i < 2; ++i) {
+        if (ctx->ev_ready[i])
+            cudaEventDestroy(ctx->ev_ready[i]);
+        if (ctx->ev_free[i])
+            cudaEventDestroy(ctx->ev_free[i]);
+    }
+    if (ctx->ev_side_done)
+        cudaEventDestroy(ctx->ev_side_done);
+    if (ctx->ev_pool_release)
+        cudaEventDestroy(ctx->ev_pool_release);
+    if (ctx->ring_host)
+        cudaFreeHost(ctx->ring_host);
+    if (ctx->pinned_small)
+        cudaFreeHost(ctx->pinned_small);
+    delete ctx;
+}
+
+const char *kvs_last_error(const kvs_ctx_t *ctx) { return ctx ? ctx->err.c_str() : "null context"; }
+
+int kvs_seq_add(kvs_ctx_t *ctx, uint64_t seq_id, int64_t parent, uint32_t shared_blocks, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (ctx->slot_of.count(seq_id))
+        return fail(ctx, KVS_EEXIST, "sequence %llu exists", (unsigned long long)seq_id);
+    if (ctx->free_slots.empty())
+        return fail(ctx, KVS_ENOMEM, "no free sequence slot (max_seqs %u)", ctx->cfg.max_seqs);
+    SeqState *par = nullptr;
+    if (parent >= 0) {
+        par = find_seq(ctx, static_cast<uint64_t>(parent));
+        if (!par)
+            return fail(ctx, KVS_ENOTFOUND, "parent %lld not found", (long long)parent);
+        if (par->ntok / kBlockTokens < shared_blocks)
+            return fail(ctx, KVS_EINVAL, "parent has %u full blocks, %u requested",
+                        par->ntok / kBlockTokens, shared_blocks);
+        for (uint32_t b = 0; b < shared_blocks; ++b)
+            if (par->table[b] < 0)
+                return fail(ctx, KVS_EINVAL, "parent block %u is demoted", b);
+    } else if (shared_blocks) {
+        return fail(ctx, KVS_EINVAL, "shared blocks need a parent");
+    }
+    if (shared_blocks > ctx->cfg.max_blocks_per_seq)
+        return fail(ctx, KVS_EINVAL, "shared prefix longer than a table row");
+    const uint32_t slot = ctx->free_slots.back();
+    std::vector<Patch> patches;
+    for (uint32_t b = 0; b < shared_blocks; ++b) {
+        Patch p{};
+        p.slot = slot;
+        p.block = b;
+        p.page = par->table[b];
+        p.has_record = 1;
+        p.rec = fresh_record(seq_id, b, ctx->t);
+        patches.push_back(p);
+    }
+    if (!patches.empty()) {
+        int rc = apply_patches(ctx, patches, S(stream));
+        if (rc)
+            return rc;
+    }
+    ctx->free_slots.pop_back();
+    SeqState &s = ctx->seqs[slot];
+    s = SeqState();
+    s.id = seq_id;
+    s.live = true;
+    s.shared_blocks = shared_blocks;
+    for (uint32_t b = 0; b < shared_blocks; ++b) {
+        s.table.push_back(par->table[b]);
+        ctx->refcnt[par->table[b]] += 1;
+    }
+    s.ntok = shared_blocks * kBlockTokens;
+    ctx->slot_of[seq_id] = slot;
+    return KVS_OK;
+}
+
+int kvs_seq_remove(kvs_ctx_t *ctx, uint64_t seq_id, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    uint32_t slot;
+    SeqState *s = find_seq(ctx, seq_id, &slot);
+    if (!s)
+        return fail(ctx, KVS_ENOTFOUND, "unknown sequence %llu", (unsigned long long)seq_id);
+    CU(cudaEventRecord(ctx->ev_pool_release, S(stream)));
+    ctx->release_pending = true;
+    for (int32_t p : s->table) {
+        if (p < 0)
+            continue;
+        if (--ctx->refcnt[p] == 0) {
+            ctx->free_pages.push_back(p);
+            ctx->mirror_clean[p] = 0;
+        }
+    }
+    for (auto it = ctx->store.begin(); it != ctx->store.end();)
+        it = it->first.first == seq_id ? ctx->store.erase(it) : std::next(it);
+    *s = SeqState();
+    ctx->slot_of.erase(seq_id);
+    ctx->free_slots.push_back(slot);
+    if (ctx->have_set)
+        for (uint32_t i = 0; i < ctx->dset->nseq; ++i)
+            if (ctx->dset->seq[i].seq_id == seq_id)
+                ctx->have_set = false;
+    return KVS_OK;
+}
+
+int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n, const void *k_dev,
+                      const void *v_dev, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    uint32_t slot;
+    SeqState *s = find_seq(ctx, seq_id, &slot);
+    if (!s)
+        return fail(ctx, KVS_ENOTFOUND, "unknown sequence %llu", (unsigned long long)seq_id);
+    if (n == 0 || !k_dev || !v_dev)
+        return fail(ctx, KVS_EINVAL, "append needs n > 0 and K/V pointers");
+    if ((reinterpret_cast<uintptr_t>(k_dev) | reinterpret_cast<uintptr_t>(v_dev)) % 16)
+        return fail(ctx, KVS_EINVAL, "K/V must be 16-byte aligned");
+    const uint64_t p0 = s->ntok, p1 = p0 + n;
+    const uint32_t first_blk = static_cast<uint32_t>(p0 / kBlockTokens);
+    const uint64_t last_blk = (p1 - 1) / kBlockTokens;
+    if (last_blk >= ctx->cfg.max_blocks_per_seq)
+        return fail(ctx, KVS_EINVAL, "sequence would need %llu blocks (table row holds %u)",
+                    (unsigned long long)(last_blk + 1), ctx->cfg.max_blocks_per_seq);
+    const uint32_t nb_old = static_cast<uint32_t>((p0 + kBlockTokens - 1) / kBlockTokens);
+    const uint32_t nblk = static_cast<uint32_t>(last_blk) - first_blk + 1;
+    if (first_blk < nb_old) {
+        if (first_blk < s->shared_blocks)
+            return fail(ctx, KVS_EINVAL, "block %u is shared read-only", first_blk);
+        if (s->table[first_blk] < 0)
+            return fail(ctx, KVS_EINVAL, "block %u is demoted", first_blk);
+    }
+    const uint32_t need = static_cast<uint32_t>(last_blk + 1) - nb_old;
+    if (ctx->free_pages.size() < need)
+        return fail(ctx, KVS_ENOMEM, "pool exhausted: %u pages needed, %zu free", need,
+                    ctx->free_pages.size());
+    int rc = order_pool_writes(ctx, S(stream));
+    if (rc)
+        return rc;
+    RingSlot r;
+    if ((rc = ring_acquire(ctx, nblk * sizeof(int32_t), &r)))
+        return rc;
+    int32_t *pages = reinterpret_cast<int32_t *>(r.host);
+    std::vector<int32_t> fresh;
+    for (uint32_t b = first_blk; b <= last_blk; ++b) {
+        if (b < nb_old) {
+            pages[b - first_blk] = s->table[b];
+        } else {
+            pages[b - first_blk] = ctx->free_pages.front();
+            fresh.push_back(ctx->free_pages.front());
+            ctx->free_pages.pop_front();
+        }
+    }
+    auto undo = [&]() {
+        for (auto it = fresh.rbegin(); it != fresh.rend(); ++it)
+            ctx->free_pages.push_front(*it);
+    };
+    if ((rc = ring_push(ctx, r, nblk * sizeof(int32_t), S(stream)))) {
+        undo();
+        return rc;
+    }
+    AppendArgs a{};
+    a.k = static_cast<const uint16_t *>(k_dev);
+    a.v = static_cast<const uint16_t *>(v_dev);
+    a.pool = static_cast<uint16_t *>(ctx->buf.pool);
+    a.table = static_cast<int32_t *>(ctx->buf.block_table);
+    a.records = static_cast<kvs_record *>(ctx->buf.records);
+    a.pages = reinterpret_cast<const int32_t *>(r.dev);
+    a.slot = slot;
+    a.p0 = static_cast<uint32_t>(p0);
+    a.n = n;
+    a.first_blk = first_blk;
+    a.nblk = nblk;
+    a.first_new = nb_old;
+    a.seq_id = seq_id;
+    a.t_create = ctx->t;
+    if ((rc = launch_rc(ctx, launch_append(ctx->geo, a, S(stream)), "append"))) {
+        undo();
+        return rc;
+    }
+    if ((rc = ring_release(ctx, r, S(stream))))
+        return rc;
+    for (uint32_t b = first_blk; b <= last_blk; ++b) {
+        const int32_t p = pages[b - first_blk];
+        if (b >= nb_old) {
+            s->table.push_back(p);
+            ctx->refcnt[p] = 1;
+        }
+        ctx->mirror_clean[p] = 0;
+    }
+    s->ntok = static_cast<uint32_t>(p1);
+    return KVS_OK;
+}
+
+int kvs_append_token(kvs_ctx_t *ctx, uint64_t seq_id, const void *k_dev, const void *v_dev,
+                     void *stream)
+{
+    return kvs_append_tokens(ctx, seq_id, 1, k_dev, v_dev, stream);
+}
+
+int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const void *q_dev,
+                    float *out_dev, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (!q_dev || !out_dev)
+        return fail(ctx, KVS_EINVAL, "q and out must be given");
+    if ((reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(out_dev)) % 16)
+        return fail(ctx, KVS_EINVAL, "q and out must be 16-byte aligned");
+    DSet *ds = ctx->dset.get();
+    int rc = build_set(ctx, seq_ids, nseq, ds);
+    if (rc) {
+        ctx->have_set = false;
+        return rc;
+    }
+    ctx->t += 1;
+    ds->t = ctx->t;
+    cudaStream_t s = S(stream);
+    if ((rc = upload_set(ctx, *ds, s)))
+        return rc;
+    ctx->have_set = true;
+    const int grid = static_cast<int>(std::min<uint32_t>(ds->n_items, ctx->decode_grid));
+    if ((rc = launch_rc(ctx,
+                        launch_decode(ctx->geo, ctx->tmap, ctx->work, static_cast<const uint16_t *>(q_dev),
+                                      static_cast<const int32_t *>(ctx->buf.block_table), ds->n_items,
+                                      ctx->wg, grid, s),
+                        "decode")))
+        return rc;
+    if ((rc = launch_rc(ctx, launch_combine(ctx->geo, ctx->work, out_dev, ds->nseq, s), "combine")))
+        return rc;
+    return launch_rc(ctx, launch_mass(ctx->geo, ctx->work, static_cast<float *>(ctx->buf.mass),
+                                      ds->nb_total, s),
+                     "mass");
+}
+
+int kvs_score_update(kvs_ctx_t *ctx, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (!ctx->have_set)
+        return fail(ctx, KVS_EINVAL, "no decode set: call kvs_decode_step first");
+    const kvs_config &c = ctx->cfg;
+    return launch_rc(ctx,
+                     launch_score(ctx->geo, ctx->work, static_cast<kvs_record *>(ctx->buf.records),
+                                  static_cast<const float *>(ctx->buf.mass), c.alpha, c.recency_window,
+                                  c.w_recency, c.w_ema, c.w_anchor, c.cut_lo, c.cut_hi,
+                                  ctx->dset->nb_total, S(stream)),
+                     "score");
+}
+
+int kvs_set_alpha(kvs_ctx_t *ctx, double alpha)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (!(alpha >= 0.0 && alpha <= 1.0))
+        return fail(ctx, KVS_EINVAL, "alpha must be in [0, 1]");
+    ctx->cfg.alpha = alpha;
+    return KVS_OK;
+}
+
+int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gather_result *res)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (!args || !res)
+        return fail(ctx, KVS_EINVAL, "args and result must be given");
+    std::memset(res, 0, sizeof *res);
+    if (!ctx->have_set)
+        return fail(ctx, KVS_EINVAL, "no decode set: call kvs_decode_step first");
+    const bool mirror = args->flags & KVS_GATHER_MIRROR, demote = args->flags & KVS_GATHER_DEMOTE;
+    if (mirror && demote)
+        return fail(ctx, KVS_EINVAL, "DEMOTE works in list mode only");
+    if (args->mode != KVS_SELECT_THRESH && args->mode != KVS_SELECT_LOWFRAC)
+        return fail(ctx, KVS_EINVAL, "unknown selection mode %d", args->mode);
+    const size_t pb = ctx->sz.page_bytes;
+    if (mirror && (!args->host_dst || args->host_dst_bytes < pb * ctx->cfg.pool_blocks))
+        return fail(ctx, KVS_EINVAL, "MIRROR needs host_dst of pool_blocks pages");
+    cudaStream_t s = S(args->stream);
+    cudaStream_t side = args->side_stream ? S(args->side_stream) : s;
+    const DSet &ds = *ctx->dset;
+    const uint32_t N = ds.nb_total;
+    int rc;
+
+    // ---- selection on the device --------------------------------------
+    uint32_t nsel = 0;
+    bool run = true;
+    if (args->mode == KVS_SELECT_LOWFRAC) {
+        if (!(args->frac >= 0.0 && args->frac <= 1.0))
+            return fail(ctx, KVS_EINVAL, "frac must be in [0, 1]");
+        const double kf = std::floor(args->frac * static_cast<double>(N));
+        const uint32_t k = static_cast<uint32_t>(kf);
+        if (k == 0)
+            run = false;
+        else if ((rc = launch_rc(ctx,
+                                 launch_radix_select(ctx->geo, ctx->work,
+                                                     static_cast<const kvs_record *>(ctx->buf.records),
+                                                     N, k, s),
+                                 "radix select")))
+            return rc;
+    }
+    if (run) {
+        if ((rc = launch_rc(ctx,
+                            launch_select(ctx->geo, ctx->work, static_cast<const kvs_record *>(ctx->buf.records),
+                                          static_cast<const int32_t *>(ctx->buf.block_table), args->mode, N, s),
+                            "select")))
+            return rc;
+        CU(cudaMemcpyAsync(ctx->pinned_small, ctx->work.sel_count, 4, cudaMemcpyDeviceToHost, s));
+        CU(cudaStreamSynchronize(s));
+        nsel = ctx->pinned_small[0];
+    }
+    std::vector<kvs_key> ids(nsel);
+    std::vector<int32_t> pages(nsel);
+    std::vector<kvs_record> recs(demote ? nsel : 0);
+    if (nsel) {
+        CU(cudaMemcpyAsync(ids.data(), ctx->work.sel_ids, nsel * sizeof(kvs_key), cudaMemcpyDeviceToHost, s));
+        CU(cudaMemcpyAsync(pages.data(), ctx->work.sel_pages, nsel * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+        if (demote)
+            CU(cudaMemcpyAsync(recs.data(), ctx->work.sel_recs, nsel * sizeof(kvs_record),
+                               cudaMemcpyDeviceToHost, s));
+        CU(cudaStreamSynchronize(s));
+    }
+    res->n_selected = nsel;
+    if (args->ids_dev && nsel)
+        CU(cudaMemcpyAsync(args->ids_dev, ctx->work.sel_ids,
+                           std::min(nsel, args->ids_capacity) * sizeof(kvs_key), cudaMemcpyDeviceToDevice, s));
+
+    // ---- gather plan: eligible pages, first occurrence ----------------
+    std::unordered_map<int32_t, uint32_t> listed;     // page -> selected references
+    for (uint32_t i = 0; i < nsel; ++i) {
+        if (pages[i] < 0 || pages[i] >= static_cast<int32_t>(ctx->cfg.pool_blocks))
+            return fail(ctx, KVS_EDEVICE, "selected record has no resident page");
+        listed[pages[i]] += 1;
+    }
+    std::vector<int32_t> slot_of_id(nsel, -1);
+    std::vector<int32_t> plan;                         // pages in gather order
+    std::unordered_map<int32_t, int32_t> plan_pos;
+    for (uint32_t i = 0; i < nsel; ++i) {
+        const int32_t p = pages[i];
+        if (listed[p] != ctx->refcnt[p])
+            continue;                                  // another user keeps it
+        auto it = plan_pos.find(p);
+        if (it == plan_pos.end()) {
+            it = plan_pos.emplace(p, static_cast<int32_t>(plan.size())).first;
+            plan.push_back(p);
+        }
+        slot_of_id[i] = mirror ? p : it->second;
+    }
+    res->n_pages = static_cast<uint32_t>(plan.size());
+
+    // ---- copies ------------------------------------------------------
+    uint32_t nstage = res->n_pages;
+    bool trunc = false;
+    if (!mirror) {
+        const size_t cap = args->host_dst ? args->host_dst_bytes / pb : 0;
+        if (nstage > cap) {
+            nstage = static_cast<uint32_t>(cap);
+            trunc = true;
+            for (auto &x : slot_of_id)
+                if (x >= static_cast<int32_t>(nstage))
+                    x = -1;
+        }
+    }
+    if (args->slot_dev && nsel) {
+        const uint32_t n = std::min(nsel, args->ids_capacity);
+        RingSlot r;
+        if ((rc = ring_acquire(ctx, n * sizeof(int32_t), &r)))
+            return rc;
+        std::memcpy(r.host, slot_of_id.data(), n * sizeof(int32_t));
+        CU(cudaMemcpyAsync(args->slot_dev, r.host, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+        if ((rc = ring_release(ctx, r, s)))
+            return rc;
+    }
+    uint8_t *host = static_cast<uint8_t *>(args->host_dst);
+    if (mirror) {
+        CU(cudaEventRecord(ctx->ev_ready[0], s));
+        CU(cudaStreamWaitEvent(side, ctx->ev_ready[0], 0));
+        // owner sequence of each page decides whether the page is full
+        std::unordered_map<int32_t, bool> full;
+        for (uint32_t i = 0; i < nsel; ++i) {
+            if (full.count(pages[i]))
+                continue;
+            SeqState *sq = find_seq(ctx, ids[i].seq_id);
+            full[pages[i]] = sq && static_cast<uint64_t>(sq->ntok) >= (ids[i].block_idx + 1) * kBlockTokens;
+        }
+        for (int32_t p : plan) {
+            if (ctx->mirror_clean[p])
+                continue;
+            CU(cudaMemcpyAsync(host + static_cast<size_t>(p) * pb,
+                               static_cast<uint8_t *>(ctx->buf.pool) + static_cast<size_t>(p) * pb, pb,
+                               cudaMemcpyDeviceToHost, side));
+            ctx->mirror_clean[p] = full[p] ? 1 : 0;
+            res->n_staged += 1;
+            res->bytes_to_host += pb;
+        }
+        CU(cudaEventRecord(ctx->ev_side_done, side));
+        ctx->side_pending = true;
+    } else if (nstage) {
+        RingSlot r;
+        if ((rc = ring_acquire(ctx, nstage * sizeof(int32_t), &r)))
+            return rc;
+        std::memcpy(r.host, plan.data(), nstage * sizeof(int32_t));
+        if ((rc = ring_push(ctx, r, nstage * sizeof(int32_t), s)))
+            return rc;
+        const uint32_t C = ctx->cfg.staging_pages;
+        const uint32_t H = C >= 2 ? C / 2 : 1;
+        const int nbuf = C >= 2 ? 2 : 1;
+        uint8_t *staging = static_cast<uint8_t *>(ctx->buf.staging);
+        for (int hb = 0; hb < nbuf; ++hb)
+            CU(cudaStreamWaitEvent(s, ctx->ev_free[hb], 0));
+        for (uint32_t c0 = 0, ci = 0; c0 < nstage; c0 += H, ++ci) {
+            const uint32_t cnt = std::min(H, nstage - c0);
+            const int hb = static_cast<int>(ci % nbuf);
+            if (ci >= static_cast<uint32_t>(nbuf))
+                CU(cudaStreamWaitEvent(s, ctx->ev_free[hb], 0));
+            uint8_t *dst = staging + static_cast<size_t>(hb) * H * pb;
+            if ((rc = launch_rc(ctx,
+                                launch_gather(ctx->geo, static_cast<const uint16_t *>(ctx->buf.pool),
+                                              reinterpret_cast<const int32_t *>(r.dev) + c0, cnt, dst, s),
+                                "gather")))
+                return rc;
+            CU(cudaEventRecord(ctx->ev_ready[hb], s));
+            CU(cudaStreamWaitEvent(side, ctx->ev_ready[hb], 0));
+            CU(cudaMemcpyAsync(host + static_cast<size_t>(c0) * pb, dst, static_cast<size_t>(cnt) * pb,
+                               cudaMemcpyDeviceToHost, side));
+            CU(cudaEventRecord(ctx->ev_free[hb], side));
+        }
+        if ((rc = ring_release(ctx, r, s)))
+            return rc;
+        CU(cudaEventRecord(ctx->ev_side_done, side));
+        ctx->side_pending = true;
+        res->n_staged = nstage;
+        res->bytes_to_host = static_cast<uint64_t>(nstage) * pb;
+    }
+
+    // ---- demotion: keep records by key, clear table entries, free pages --
+    if (demote && nstage) {
+        std::vector<Patch> patches;
+        for (uint32_t i = 0; i < nsel; ++i) {
+            if (slot_of_id[i] < 0)
+                continue;
+            const std::pair<uint64_t, uint64_t> key(ids[i].seq_id, ids[i].block_idx);
+            if (ctx->store.count(key))
+                return fail(ctx, KVS_EEXIST, "key (%llu, %llu) already demoted",
+                            (unsigned long long)key.first, (unsigned long long)key.second);
+        }
+        for (uint32_t i = 0; i < nsel; ++i) {
+            if (slot_of_id[i] < 0)
+                continue;
+            const std::pair<uint64_t, uint64_t> key(ids[i].seq_id, ids[i].block_idx);
+            ctx->store[key] = Demoted{recs[i], static_cast<uint64_t>(slot_of_id[i]) * pb};
+            uint32_t slot;
+            SeqState *sq = find_seq(ctx, ids[i].seq_id, &slot);
+            const int32_t p = pages[i];
+            sq->table[ids[i].block_idx] = -1;
+            Patch q{};
+            q.slot = slot;
+            q.block = static_cast<uint32_t>(ids[i].block_idx);
+            q.page = -1;
+            q.has_record = 1;
+            q.rec = recs[i];
+            q.rec.flags |= 1;
+            patches.push_back(q);
+            if (--ctx->refcnt[p] == 0) {
+                ctx->free_pages.push_back(p);
+                ctx->mirror_clean[p] = 0;
+            }
+            res->n_demoted += 1;
+        }
+        if ((rc = apply_patches(ctx, patches, s)))
+            return rc;
+        ctx->have_set = false;   // the set now has holes
+    }
+    if (trunc)
+        return fail(ctx, KVS_ETRUNC, "host_dst holds %u of %u pages", nstage, res->n_pages);
+    return KVS_OK;
+}
+
+int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n, const void *host_src,
+                size_t host_src_bytes, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (n == 0)
+        return KVS_OK;
+    if (!keys || !host_src)
+        return fail(ctx, KVS_EINVAL, "keys and host_src must be given");
+    const size_t pb = ctx->sz.page_bytes;
+    std::vector<std::pair<uint64_t, uint64_t>> ks(n);
+    for (uint32_t i = 0; i < n; ++i)
+        ks[i] = {keys[i].seq_id, keys[i].block_idx};
+    {
+        auto sorted = ks;
+        std::sort(sorted.begin(), sorted.end());
+        for (uint32_t i = 1; i < n; ++i)
+            if (sorted[i] == sorted[i - 1])
+                return fail(ctx, KVS_EEXIST, "key (%llu, %llu) listed twice",
+                            (unsigned long long)sorted[i].first, (unsigned long long)sorted[i].second);
+    }
+    for (auto &k : ks) {
+        auto it = ctx->store.find(k);
+        if (it == ctx->store.end()) {
+            SeqState *sq = find_seq(ctx, k.first);
+            if (sq && k.second < sq->table.size() && sq->table[k.second] >= 0)
+                return fail(ctx, KVS_EEXIST, "key (%llu, %llu) is resident",
+                            (unsigned long long)k.first, (unsigned long long)k.second);
+            return fail(ctx, KVS_ENOTFOUND, "key (%llu, %llu) is not demoted",
+                        (unsigned long long)k.first, (unsigned long long)k.second);
+        }
+        if (it->second.host_off + pb > host_src_bytes)
+            return fail(ctx, KVS_EINVAL, "host_src too small for key (%llu, %llu)",
+                        (unsigned long long)k.first, (unsigned long long)k.second);
+    }
+    if (ctx->free_pages.size() < n)
+        return fail(ctx, KVS_ENOMEM, "pool exhausted: %u pages needed, %zu free", n,
+                    ctx->free_pages.size());
+    cudaStream_t s = S(stream);
+    int rc = order_pool_writes(ctx, s);
+    if (rc)
+        return rc;
+    std::vector<Patch> patches;
+    std::vector<int32_t> taken;
+    const uint8_t *src = static_cast<const uint8_t *>(host_src);
+    for (auto &k : ks) {
+        const Demoted &dm = ctx->store[k];
+        const int32_t p = ctx->free_pages.front();
+        ctx->free_pages.pop_front();
+        taken.push_back(p);
+        cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t *>(ctx->buf.pool) + static_cast<size_t>(p) * pb,
+                                        src + dm.host_off, pb, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) {
+            for (auto it = taken.rbegin(); it != taken.rend(); ++it)
+                ctx->free_pages.push_front(*it);
+            return fail(ctx, KVS_ECUDA, "readmit copy: %s", cudaGetErrorString(e));
+        }
+        uint32_t slot;
+        find_seq(ctx, k.first, &slot);
+        Patch q{};
+        q.slot = slot;
+        q.block = static_cast<uint32_t>(k.second);
+        q.page = p;
+        q.has_record = 1;
+        q.rec = dm.rec;
+        patches.push_back(q);
+    }
+    if ((rc = apply_patches(ctx, patches, s)))
+        return rc;
+    for (size_t i = 0; i < ks.size(); ++i) {
+        uint32_t slot;
+        SeqState *sq = find_seq(ctx, ks[i].first, &slot);
+        sq->table[ks[i].second] = taken[i];
+        ctx->refcnt[taken[i]] = 1;
+        ctx->mirror_clean[taken[i]] = 0;
+        ctx->store.erase(ks[i]);
+    }
+    return KVS_OK;
+}
+
+int kvs_debug_set_mass(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const float *mass_dev,
+                       void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (!mass_dev)
+        return fail(ctx, KVS_EINVAL, "mass must be given");
+    DSet *ds = ctx->dset.get();
+    int rc = build_set(ctx, seq_ids, nseq, ds);
+    if (rc) {
+        ctx->have_set = false;
+        return rc;
+    }
+    ds->t = ctx->t;
+    cudaStream_t s = S(stream);
+    if ((rc = upload_set(ctx, *ds, s)))
+        return rc;
+    ctx->have_set = true;
+    return launch_rc(ctx,
+                     launch_copy_mass(ctx->geo, ctx->work, mass_dev, static_cast<float *>(ctx->buf.mass),
+                                      nseq, s),
+                     "copy mass");
+}
+
+int kvs_debug_advance(kvs_ctx_t *ctx, uint64_t steps)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    ctx->t += steps;
+    return KVS_OK;
+}
+
+int kvs_export_records(kvs_ctx_t *ctx, uint64_t seq_id, void *host_dst, size_t host_bytes, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    uint32_t slot;
+    SeqState *s = find_seq(ctx, seq_id, &slot);
+    if (!s)
+        return fail(ctx, KVS_ENOTFOUND, "unknown sequence %llu", (unsigned long long)seq_id);
+    const size_t nb = s->table.size();
+    const size_t want = nb * sizeof(kvs_record);
+    const size_t n = std::min(want, host_bytes / sizeof(kvs_record) * sizeof(kvs_record));
+    if (n) {
+        CU(cudaMemcpyAsync(host_dst, static_cast<kvs_record *>(ctx->buf.records) + static_cast<size_t>(slot) * ctx->cfg.max_blocks_per_seq,
+                           n, cudaMemcpyDeviceToHost, S(stream)));
+        CU(cudaStreamSynchronize(S(stream)));
+    }
+    if (n < want)
+        return fail(ctx, KVS_ETRUNC, "host buffer holds %zu of %zu records", n / 64, nb);
+    return KVS_OK;
+}
+
+int kvs_seq_info(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t *slot, uint32_t *n_tokens,
+                 uint32_t *n_blocks, int32_t *table_out, uint32_t table_cap)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    uint32_t sl;
+    SeqState *s = find_seq(ctx, seq_id, &sl);
+    if (!s)
+        return fail(ctx, KVS_ENOTFOUND, "unknown sequence %llu", (unsigned long long)seq_id);
+    if (slot)
+        *slot = sl;
+    if (n_tokens)
+        *n_tokens = s->ntok;
+    if (n_blocks)
+        *n_blocks = static_cast<uint32_t>(s->table.size());
+    if (table_out)
+        for (uint32_t i = 0; i < table_cap && i < s->table.size(); ++i)
+            table_out[i] = s->table[i];
+    return KVS_OK;
+}
+
+uint64_t kvs_step_count(const kvs_ctx_t *ctx) { return ctx ? ctx->t : 0; }
+
+uint32_t kvs_free_pages(const kvs_ctx_t *ctx)
+{
+    return ctx ? static_cast<uint32_t>(ctx->free_pages.size()) : 0;
+}
+
+int kvs_check_device(kvs_ctx_t *ctx, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    cudaStream_t s = S(stream);
+    CU(cudaMemcpyAsync(ctx->pinned_small, ctx->work.err, 8, cudaMemcpyDeviceToHost, s));
+    CU(cudaStreamSynchronize(s));
+    const uint32_t e = ctx->pinned_small[0], info = ctx->pinned_small[1];
+    if (!e)
+        return KVS_OK;
+    CU(cudaMemsetAsync(ctx->work.err, 0, 8, s));
+    CU(cudaStreamSynchronize(s));
+    if (e & kErrTmaTimeout)
+        return fail(ctx, KVS_ETIMEOUT, "a decode kernel gave up waiting for a TMA copy (error word 0x%x)", e);
+    return fail(ctx, KVS_EDEVICE, "device error word 0x%x (bad page %d, bad record %d), info 0x%x", e,
+                !!(e & kErrBadPage), !!(e & kErrBadRecord), info);
+}
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+"""Runs a workload through the C ABI (CUDA path) and, beside it, through the
+oracle, step by step, and compares them.  Inputs for both sides come from
+the seeded generators in ``workloads`` (generated on the GPU, copied to the
+host for the oracle); no expected value comes from the CUDA path."""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import oracle as O
+import paged_kv_cache_flash_gb300 as K
+import workloads as W
+
+OUT_TOL = 2e-2      # attention output, max abs (bf16 in, fp32 accumulate)
+MASS_TOL = 1e-4     # block mass, abs
+SCORE_TOL = 1e-5    # EMA score and priority, abs
+CUT_MARGIN = 1e-5   # blocks with oracle P this close to a cut are excluded
+TOUCH_MARGIN = 1e-5 # blocks with oracle M*nb this close to 1 are excluded
+
+
+def seq_ids_for(wl):
+    # descending ids: call order differs from the ascending-id record order
+    return [5000 - 17 * s for s in range(wl.nseq)]
+
+
+@dataclass
+class OracleSeq:
+    seq_id: int
+    K: torch.Tensor               # host bf16 [n][L][Hkv][d]
+    V: torch.Tensor
+    rec: np.ndarray               # oracle records, block order
+    ambiguous: np.ndarray         # touch decision within TOUCH_MARGIN at some step
+    page_of: list = field(default_factory=list)   # page identity per block
+
+
+class Run:
+    def __init__(self, wl, alpha, *, staging_pages=8, chunk=4096, oracle_on=True,
+                 pool_pages=None, device="cuda"):
+        self.wl, self.alpha = wl, alpha
+        self.dev = device
+        self.ids = seq_ids_for(wl)
+        self.mb = wl.max_blocks_per_seq()
+        cfg = K.make_config(wl.L, wl.Hq, wl.Hkv, wl.d, pool_pages or wl.pool_pages, max_seqs=wl.nseq,
+                            max_blocks_per_seq=self.mb, alpha=alpha,
+                            recency_window=wl.recency_window, weights=wl.weights, cuts=wl.cuts,
+                            pool_seed=wl.seed, staging_pages=staging_pages)
+        self.ctx = K.Context(cfg)
+        self.oracle_on = oracle_on
+        self.t = 0
+        self.ntok = list(wl.prefill_lens)
+        self.orc = {}
+        B = wl.block_tokens
+        pre_blocks = wl.shared_prefix_tokens // B
+        for s, sid in enumerate(self.ids):
+            n = wl.prefill_lens[s]
+            if s > 0 and pre_blocks:
+                self.ctx.seq_add(sid, self.ids[0], pre_blocks)
+                start = wl.shared_prefix_tokens
+            else:
+                self.ctx.seq_add(sid)
+                start = 0
+            for a in range(start, n, chunk):
+                b = min(n, a + chunk)
+                Kt, Vt = W.kv_tokens(wl, s, a, b, device)
+                self.ctx.append_tokens(sid, Kt, Vt)
+            if oracle_on:
+                Kh, Vh = W.kv_tokens(wl, s, 0, n, device)
+                nb = (n + B - 1) // B
+                page_of = [((0, b) if b < pre_blocks else (s, b)) for b in range(nb)]
+                self.orc[sid] = OracleSeq(sid, Kh.cpu(), Vh.cpu(), O.new_records(sid, 0, nb, 0),
+                                          np.zeros(nb, bool), page_of)
+        torch.cuda.synchronize()
+
+    # ------------------------------------------------------------------
+    def step(self, gather_host=None, mode=K.KVS_SELECT_THRESH, flags=0, frac=0.0):
+        """One decode step over every sequence; returns a dict of GPU results
+        and, if the oracle is on, the oracle's."""
+        wl = self.wl
+        B = wl.block_tokens
+        self.t += 1
+        t = self.t
+        for s, sid in enumerate(self.ids):
+            n = self.ntok[s]
+            Kt, Vt = W.kv_tokens(wl, s, n, n + 1, self.dev)
+            self.ctx.append_tokens(sid, Kt, Vt)
+            if self.oracle_on:
+                o = self.orc[sid]
+                if n % B == 0:      # a new block opens at the step counter t-1
+                    o.rec = np.concatenate([o.rec, O.new_records(sid, n // B, 1, t - 1)])
+                    o.ambiguous = np.append(o.ambiguous, False)
+                    o.page_of.append((s, n // B))
+                o.K = torch.cat([o.K, Kt.cpu()])
+                o.V = torch.cat([o.V, Vt.cpu()])
+            self.ntok[s] = n + 1
+        q = torch.stack([W.queries(wl, s, t, self.dev) for s in range(wl.nseq)]).contiguous()
+        out = torch.empty((wl.nseq, wl.L, wl.Hq, wl.d), dtype=torch.float32, device=self.dev)
+        self.ctx.decode_step(self.ids, q, out)
+        self.ctx.score_update()
+        res = {"out": out, "q": q}
+        nrec = sum((n + B - 1) // B for n in self.ntok)
+        ids = torch.zeros(nrec * 2, dtype=torch.int64, device=self.dev)
+        slots = torch.full((nrec,), -2, dtype=torch.int32, device=self.dev)
+        side = torch.cuda.Stream()
+        rc, r = self.ctx.select_and_gather(mode, gather_host, frac=frac, flags=flags, ids=ids,
+                                           slots=slots, side_stream=side)
+        side.synchronize()
+        torch.cuda.synchronize()
+        res["rc"], res["gather"] = rc, r
+        res["ids"] = [tuple(x) for x in ids.view(-1, 2)[: r.n_selected].cpu().tolist()]
+        res["slots"] = slots[: r.n_selected].cpu().tolist()
+        res["records"] = {sid: self.ctx.export_records(sid) for sid in self.ids
+                          if not (flags & K.KVS_GATHER_DEMOTE)}
+        if self.oracle_on:
+            res["oracle"] = self._oracle_step(q.cpu(), t)
+        return res
+
+    def _oracle_step(self, q, t):
+        wl = self.wl
+        outs, masses = {}, {}
+        for s, sid in enumerate(self.ids):
+            o = self.orc[sid]
+            r = O.decode_with_mass(q[s], o.K, o.V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d)
+            nb = len(o.rec)
+            M = r["mass"]
+            o.ambiguous |= np.abs(M * nb - 1.0) < TOUCH_MARGIN
+            o.rec = O.score_update(o.rec, M, t, self.alpha, wl.recency_window, wl.weights, wl.cuts)
+            outs[sid], masses[sid] = r["out"], M
+        return {"out": outs, "mass": masses}
+
+    # ------------------------------------------------------------------
+    def excluded(self, sid):
+        o = self.orc[sid]
+        lo, hi = self.wl.cuts
+        nearcut = (np.abs(o.rec["prio"] - lo) < CUT_MARGIN) | (np.abs(o.rec["prio"] - hi) < CUT_MARGIN)
+        return nearcut | o.ambiguous
+
+    def compare(self, res, check_records=True):
+        """Asserts parity of one step; returns the error summary."""
+        wl = self.wl
+        summ = {"out_max_abs": 0.0, "mass_max_abs": 0.0, "score_max_abs": 0.0,
+                "prio_max_abs": 0.0, "excluded": 0}
+        orc = res["oracle"]
+        out = res["out"].cpu().numpy()
+        for s, sid in enumerate(self.ids):
+            e = np.abs(out[s] - orc["out"][sid]).max()
+            summ["out_max_abs"] = max(summ["out_max_abs"], float(e))
+            slot = self.ctx.seq_info(sid)[0]
+            nb = len(self.orc[sid].rec)
+            gm = self.ctx.mass()[slot, :nb].cpu().numpy().astype(np.float64)
+            summ["mass_max_abs"] = max(summ["mass_max_abs"], float(np.abs(gm - orc["mass"][sid]).max()))
+            if not check_records:
+                continue
+            g = res["records"][sid]
+            o = self.orc[sid].rec
+            assert len(g) == len(o)
+            assert np.array_equal(g["seq_id"], o["seq_id"]) and np.array_equal(g["block_idx"], o["block_idx"])
+            summ["score_max_abs"] = max(summ["score_max_abs"], float(np.abs(g["score"] - o["score"]).max()))
+            ex = self.excluded(sid)
+            keep = ~ex
+            summ["excluded"] += int(ex.sum())
+            summ["prio_max_abs"] = max(summ["prio_max_abs"],
+                                       float(np.abs(g["prio"][keep] - o["prio"][keep]).max(initial=0)))
+            assert np.array_equal(g["tier"][keep], o["tier"][keep]), f"tier mismatch seq {sid}"
+            assert np.array_equal(g["count"][keep], o["count"][keep]), f"count mismatch seq {sid}"
+            assert np.array_equal(g["last_touch"][keep], o["last_touch"][keep])
+        assert summ["out_max_abs"] <= OUT_TOL, summ
+        assert summ["mass_max_abs"] <= MASS_TOL, summ
+        if check_records:
+            assert summ["score_max_abs"] <= SCORE_TOL, summ
+            assert summ["prio_max_abs"] <= SCORE_TOL, summ
+        return summ
+
+    def excluded_keys(self):
+        out = set()
+        for sid in self.ids:
+            ex = self.excluded(sid)
+            out |= {(sid, int(b)) for b in np.nonzero(ex)[0]}
+        return out
+
+    def oracle_page(self, sid, b):
+        o = self.orc[sid]
+        B = self.wl.block_tokens
+        return O.assemble_page(o.K[b * B:(b + 1) * B], o.V[b * B:(b + 1) * B], B)
+
+    def close(self):
+        self.ctx.close()

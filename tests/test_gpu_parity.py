@@ -1,0 +1,277 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import paged_kv_cache_flash_gb300 as K
+import workloads as W
+from gpu_harness import Run, seq_ids_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_flash_gb300 import build
+    build.build()
+
+
+def _pinned(nbytes):
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8).pin_memory()
+
+
+def _check_gather(run, res, host):
+    """Listed ids equal the oracle's (outside the exclusion); a listed page is
+    gathered exactly when the oracle's reference-count rule makes it
+    eligible, and its bytes equal the oracle's page assembly."""
+    excl = run.excluded_keys()
+    orc_ids = O.select_thresh({sid: run.orc[sid].rec for sid in run.ids})
+    assert [k for k in res["ids"] if k not in excl] == [k for k in orc_ids if k not in excl]
+    assert res["ids"] == sorted(res["ids"])
+    page_of, refs = {}, {}
+    for sid in run.ids:
+        for b, pid in enumerate(run.orc[sid].page_of):
+            page_of[(sid, b)] = pid
+            refs.setdefault(pid, set()).add((sid, b))
+    eligible = set(O.gather_plan(res["ids"], page_of, refs))
+    pb = run.ctx.page_bytes
+    hb = host.numpy()
+    for (sid, b), slot in zip(res["ids"], res["slots"]):
+        if page_of[(sid, b)] not in eligible:
+            assert slot == -1, (sid, b)
+            continue
+        assert slot >= 0
+        assert hb[slot * pb:(slot + 1) * pb].tobytes() == run.oracle_page(sid, b), (sid, b)
+    return len(excl)
+
+
+def test_tiny_end_to_end():
+    """Tiny workload: 2 layers, 4:1 GQA, d=64, 1 x 256 tokens, 4 steps."""
+    wl = W.workload("tiny")
+    run = Run(wl, wl.alphas[0])
+    host = _pinned(wl.pool_pages * wl.page_bytes)
+    for _ in range(wl.steps):
+        res = run.step(host)
+        summ = run.compare(res)
+        _check_gather(run, res, host)
+        assert res["rc"] == K.KVS_OK
+    run.ctx.check_device()
+    print("tiny", summ)
+    run.close()
+
+
+def test_ragged_multi_sequence_and_shared_prefix():
+    """Three sequences of ragged lengths (1 token .. 9 blocks + tail), two of
+    them sharing the first 2 blocks of the first (refcounted pages)."""
+    wl = W.workload("tiny", prefill_lens=(40, 33, 150), shared_prefix_tokens=32,
+                    pool_pages=40, steps=20, skew=True)
+    run = Run(wl, 0.3)
+    host = _pinned(wl.pool_pages * wl.page_bytes)
+    for _ in range(wl.steps):
+        res = run.step(host)
+        run.compare(res)
+        _check_gather(run, res, host)
+    # the shared pages are gathered only when all three users list them
+    run.close()
+
+
+def test_single_token_sequence_and_large_group():
+    """One-token sequences (nothing but block 0) and the full 8:1 group at d=128."""
+    wl = W.workload("l70b_8k", L=3, prefill_lens=(1, 17), pool_pages=8, steps=3)
+    run = Run(wl, 0.15)
+    for _ in range(wl.steps):
+        res = run.step(None)
+        run.compare(res)
+    run.close()
+
+
+def test_llama70b_shape_cut():
+    """All 80 layers, 64/8 heads, d=128, one ragged 1,000-token sequence."""
+    wl = W.workload("l70b_8k", prefill_lens=(1000,), pool_pages=70, steps=2)
+    run = Run(wl, 0.15)
+    host = _pinned(64 * wl.page_bytes)
+    for _ in range(wl.steps):
+        res = run.step(host)
+        summ = run.compare(res)
+        _check_gather(run, res, host)
+    print("l70b cut", summ)
+    run.close()
+
+
+@pytest.mark.slow
+def test_llama70b_8k_full_size():
+    """The 8K single-sequence workload at full size (512 blocks, 2.50 GiB), 2 steps."""
+    wl = W.workload("l70b_8k", steps=2)
+    run = Run(wl, 0.15)
+    host = _pinned((wl.pool_pages) * wl.page_bytes)
+    for _ in range(wl.steps):
+        res = run.step(host)
+        summ = run.compare(res)
+        _check_gather(run, res, host)
+    print("l70b 8k", summ)
+    run.close()
+
+
+# --------------------------------------------------------------- scoring
+
+
+def _mass_tensor(run, masses):
+    m = torch.zeros((len(run.ids), run.mb), dtype=torch.float32)
+    for i, sid in enumerate(run.ids):
+        m[i, :len(masses[sid])] = torch.from_numpy(masses[sid])
+    return m.cuda()
+
+
+@pytest.mark.parametrize("alpha,cuts", [(0.15, (0.3, 0.6)), (1.0, (0.3, 0.6)),
+                                        (0.0, (0.25, 0.25 + 0.2))])
+def test_scoring_bit_exact_on_injected_mass(alpha, cuts):
+    """Scoring, tiers and both selections driven from the same seeded masses
+    on both sides must agree bit for bit in all 64 record bytes.  With
+    alpha = 0 and cuts (0.25, 0.25+0.2) every touched interior block sits
+    exactly on cut_lo and every touched anchor exactly on cut_hi."""
+    cuts = (cuts[0], float(np.float64(0.25) + np.float64(0.2))) if alpha == 0.0 else cuts
+    wl = W.workload("tiny", prefill_lens=(37, 300, 1), pool_pages=40, cuts=cuts, steps=0)
+    run = Run(wl, alpha)
+    rng = np.random.default_rng(7)
+    seen = set()
+    for t in range(1, 90):
+        masses = {}
+        for sid in run.ids:
+            nb = len(run.orc[sid].rec)
+            m = W.synthetic_masses(1000 * t + sid, nb)
+            m[rng.random(nb) < (0.6 if t < 70 else 1.0)] = 0.0   # long silences: R clips
+            masses[sid] = m
+        run.ctx.debug_advance(1)
+        run.ctx.debug_set_mass(run.ids, _mass_tensor(run, masses))
+        run.ctx.score_update()
+        for sid in run.ids:
+            o = run.orc[sid]
+            o.rec = O.score_update(o.rec, masses[sid].astype(np.float64), t, alpha,
+                                   wl.recency_window, wl.weights, wl.cuts)
+            g = run.ctx.export_records(sid)
+            assert g.tobytes() == o.rec.tobytes(), f"t={t} seq={sid}"
+            seen |= set(o.rec["tier"].tolist())
+        if t % 10 == 0:
+            recs = {sid: run.orc[sid].rec for sid in run.ids}
+            _, r = run.ctx.select_and_gather(K.KVS_SELECT_THRESH)
+            assert r.n_selected == len(O.select_thresh(recs))
+            ids = torch.zeros(2 * 400, dtype=torch.int64, device="cuda")
+            _, r = run.ctx.select_and_gather(K.KVS_SELECT_LOWFRAC, frac=0.25, ids=ids)
+            got = [tuple(x) for x in ids.view(-1, 2)[: r.n_selected].cpu().tolist()]
+            assert got == O.select_lowfrac(recs, 0.25)
+    if alpha == 0.0:     # blocks sat exactly on both cuts at some step
+        assert {0, 1, 2} <= seen
+    run.close()
+
+
+# ------------------------------------------------------ demote / readmit
+
+
+def test_demote_readmit_round_trip():
+    """LOWFRAC 10 % demotion to pinned host, then re-admission into other
+    pages: pages byte-equal, records restored bit for bit, decoding after
+    the round trip still matches the oracle."""
+    wl = W.workload("tiny", prefill_lens=(200, 333, 97, 150), pool_pages=60, steps=6, skew=True)
+    run = Run(wl, 0.05)
+    for _ in range(3):
+        run.compare(run.step(None))
+    before = {sid: run.ctx.export_records(sid) for sid in run.ids}
+    tables = {sid: run.ctx.seq_info(sid)[3] for sid in run.ids}
+    pages_before = {}
+    for sid in run.ids:
+        for b, p in enumerate(tables[sid]):
+            pages_before[(sid, b)] = run.ctx.page_bytes_of(p).cpu().numpy().tobytes()
+    nrec = sum(len(v) for v in before.values())
+    host = _pinned(nrec * run.ctx.page_bytes)
+    ids = torch.zeros(2 * nrec, dtype=torch.int64, device="cuda")
+    free0 = run.ctx.free_pages()
+    rc, r = run.ctx.select_and_gather(K.KVS_SELECT_LOWFRAC, host, frac=0.10,
+                                      flags=K.KVS_GATHER_DEMOTE, ids=ids)
+    torch.cuda.synchronize()
+    assert rc == K.KVS_OK
+    k = int(np.floor(0.10 * nrec))
+    assert r.n_selected == k == r.n_demoted
+    got = [tuple(x) for x in ids.view(-1, 2)[:k].cpu().tolist()]
+    assert got == O.select_lowfrac(before, 0.10)
+    assert run.ctx.free_pages() == free0 + k
+    hb = host.numpy()
+    pb = run.ctx.page_bytes
+    for i, key in enumerate(got):
+        assert hb[i * pb:(i + 1) * pb].tobytes() == pages_before[key]
+        assert run.ctx.seq_info(key[0])[3][key[1]] == -1
+    q = torch.zeros((wl.nseq, wl.L, wl.Hq, wl.d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((wl.nseq, wl.L, wl.Hq, wl.d), device="cuda")
+    with pytest.raises(K.KvsError) as e:       # blocks are missing: refused
+        run.ctx.decode_step(run.ids, q, out)
+    assert e.value.code == K.KVS_EINVAL
+    run.ctx.readmit(got, host)
+    torch.cuda.synchronize()
+    for sid in run.ids:
+        assert run.ctx.export_records(sid).tobytes() == before[sid].tobytes()
+        for b, p in enumerate(run.ctx.seq_info(sid)[3]):
+            assert run.ctx.page_bytes_of(p).cpu().numpy().tobytes() == pages_before[(sid, b)]
+    with pytest.raises(K.KvsError) as e:
+        run.ctx.readmit(got[:1], host)
+    assert e.value.code == K.KVS_EEXIST
+    for _ in range(2):                          # decoding resumes in parity
+        run.compare(run.step(None))
+    run.close()
+
+
+def test_error_paths():
+    wl = W.workload("tiny", prefill_lens=(32,), pool_pages=3, steps=0)
+    run = Run(wl, 0.1)
+    ctx = run.ctx
+    sid = run.ids[0]
+    with pytest.raises(K.KvsError) as e:
+        ctx.seq_add(sid)
+    assert e.value.code == K.KVS_EEXIST
+    Kt, Vt = W.kv_tokens(wl, 0, 32, 32 + 40, "cuda")
+    with pytest.raises(K.KvsError) as e:           # needs 3 new pages, 1 free
+        ctx.append_tokens(sid, Kt, Vt)
+    assert e.value.code == K.KVS_ENOMEM
+    assert ctx.seq_info(sid)[1] == 32               # nothing appended
+    with pytest.raises(K.KvsError) as e:
+        ctx.decode_step([12345], torch.zeros((1, wl.L, wl.Hq, wl.d), dtype=torch.bfloat16,
+                                             device="cuda"),
+                        torch.zeros((1, wl.L, wl.Hq, wl.d), device="cuda"))
+    assert e.value.code == K.KVS_ENOTFOUND
+    with pytest.raises(K.KvsError) as e:
+        ctx.readmit([(sid, 0)], _pinned(wl.page_bytes))
+    assert e.value.code == K.KVS_EEXIST
+    with pytest.raises(K.KvsError) as e:
+        ctx.readmit([(sid, 7)], _pinned(wl.page_bytes))
+    assert e.value.code == K.KVS_ENOTFOUND
+    with pytest.raises(K.KvsError) as e:
+        ctx.score_update()
+    assert e.value.code == K.KVS_EINVAL
+    # truncation: a host buffer of one page for a longer list
+    q = W.queries(wl, 0, 1, "cuda").unsqueeze(0).contiguous()
+    out = torch.empty((1, wl.L, wl.Hq, wl.d), device="cuda")
+    ctx.decode_step([sid], q, out)
+    ctx.debug_set_mass([sid], torch.zeros((1, run.mb), device="cuda"))
+    ctx.debug_advance(100)
+    ctx.debug_set_mass([sid], torch.zeros((1, run.mb), device="cuda"))
+    ctx.score_update()
+    rc, r = ctx.select_and_gather(K.KVS_SELECT_LOWFRAC, _pinned(wl.page_bytes), frac=1.0)
+    assert rc == K.KVS_ETRUNC and r.n_pages == 2 and r.n_staged == 1
+    ctx.check_device()
+    run.close()
+
+
+def test_mirror_mode_sends_each_full_page_once():
+    wl = W.workload("tiny", prefill_lens=(100, 64), pool_pages=20, steps=5, skew=True)
+    run = Run(wl, 0.15)
+    mirror = _pinned(wl.pool_pages * wl.page_bytes)
+    staged = []
+    for _ in range(wl.steps):
+        res = run.step(mirror, flags=K.KVS_GATHER_MIRROR)
+        run.compare(res)
+        staged.append(res["gather"].n_staged)
+        pb = run.ctx.page_bytes
+        hb = mirror.numpy()
+        for (sid, b), slot in zip(res["ids"], res["slots"]):
+            assert hb[slot * pb:(slot + 1) * pb].tobytes() == run.oracle_page(sid, b)
+    assert staged[0] > 0 and max(staged[1:]) <= 2
+    run.close()
