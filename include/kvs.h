@@ -300,6 +300,13 @@ int kvs_seq_info(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t *slot,
                  uint32_t *n_tokens, uint32_t *n_blocks, int32_t *table_out,
                  uint32_t table_cap);
 
+/* Measurement hook: when ev_start/ev_stop (cudaEvent_t as void*) are not
+ * NULL, every later kvs_decode_step records ev_start on its stream right
+ * before the split-K decode kernel and ev_stop right after it, so the kernel
+ * can be timed on the stream it runs on.  NULL, NULL turns it off.  The
+ * events stay owned by the caller. */
+int kvs_set_decode_events(kvs_ctx_t *ctx, void *ev_start, void *ev_stop);
+
 /* Decode steps completed so far (the step counter t). */
 uint64_t kvs_step_count(const kvs_ctx_t *ctx);
 

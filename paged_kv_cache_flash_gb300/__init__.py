@@ -100,6 +100,7 @@ _SIGS = {
     "kvs_export_records": (ctypes.c_int, [c_vp, c_u64, c_vp, c_sz, c_vp]),
     "kvs_seq_info": (ctypes.c_int, [c_vp, c_u64, ctypes.POINTER(c_u32), ctypes.POINTER(c_u32),
                                     ctypes.POINTER(c_u32), ctypes.POINTER(c_i32), c_u32]),
+    "kvs_set_decode_events": (ctypes.c_int, [c_vp, c_vp, c_vp]),
     "kvs_step_count": (c_u64, [c_vp]),
     "kvs_free_pages": (c_u32, [c_vp]),
     "kvs_check_device": (ctypes.c_int, [c_vp, c_vp]),
@@ -312,6 +313,12 @@ class Context:
         table = (c_i32 * max(nb.value, 1))()
         _check(self.h, lib().kvs_seq_info(self.h, seq_id, None, None, None, table, nb.value))
         return sl.value, nt.value, nb.value, list(table)[:nb.value]
+
+    def set_decode_events(self, start=None, stop=None):
+        """torch.cuda.Event pair recorded around the decode kernel (None: off)."""
+        a = start.cuda_event if start is not None else None
+        b = stop.cuda_event if stop is not None else None
+        _check(self.h, lib().kvs_set_decode_events(self.h, a, b))
 
     def step_count(self) -> int:
         return lib().kvs_step_count(self.h)

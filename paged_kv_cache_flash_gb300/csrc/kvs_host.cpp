@@ -89,6 +89,7 @@ struct kvs_ctx {
     uint32_t *pinned_small = nullptr;               // readbacks
 
     cudaEvent_t ev_ready[2]{}, ev_free[2]{}, ev_side_done{}, ev_pool_release{};
+    cudaEvent_t ev_dec_start = nullptr, ev_dec_stop = nullptr;   // caller's timing events
     bool side_pending = false, release_pending = false;
 
     std::string err;
@@ -746,12 +747,16 @@ int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
         return rc;
     ctx->have_set = true;
     const int grid = static_cast<int>(std::min<uint32_t>(ds->n_items, ctx->decode_grid));
+    if (ctx->ev_dec_start)
+        CU(cudaEventRecord(ctx->ev_dec_start, s));
     if ((rc = launch_rc(ctx,
                         launch_decode(ctx->geo, ctx->tmap, ctx->work, static_cast<const uint16_t *>(q_dev),
                                       static_cast<const int32_t *>(ctx->buf.block_table), ds->n_items,
                                       ctx->wg, grid, s),
                         "decode")))
         return rc;
+    if (ctx->ev_dec_stop)
+        CU(cudaEventRecord(ctx->ev_dec_stop, s));
     if ((rc = launch_rc(ctx, launch_combine(ctx->geo, ctx->work, out_dev, ds->nseq, s), "combine")))
         return rc;
     return launch_rc(ctx, launch_mass(ctx->geo, ctx->work, static_cast<float *>(ctx->buf.mass),
@@ -1152,6 +1157,17 @@ int kvs_seq_info(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t *slot, uint32_t *n_to
     if (table_out)
         for (uint32_t i = 0; i < table_cap && i < s->table.size(); ++i)
             table_out[i] = s->table[i];
+    return KVS_OK;
+}
+
+int kvs_set_decode_events(kvs_ctx_t *ctx, void *ev_start, void *ev_stop)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if ((ev_start == nullptr) != (ev_stop == nullptr))
+        return fail(ctx, KVS_EINVAL, "give both events or neither");
+    ctx->ev_dec_start = static_cast<cudaEvent_t>(ev_start);
+    ctx->ev_dec_stop = static_cast<cudaEvent_t>(ev_stop);
     return KVS_OK;
 }
 
