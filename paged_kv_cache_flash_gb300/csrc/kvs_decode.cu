@@ -459,15 +459,17 @@ size_t decode_smem_bytes(const Geo &g, uint32_t wg)
 
 int decode_blocks_per_sm(const Geo &g, uint32_t wg)
 {
+    // The attribute is per kernel, shared by every context in the process:
+    // always allow the largest configuration (4 warps) so that no context
+    // lowers it below what another one launches with.
     int n = 0;
     const size_t smem = decode_smem_bytes(g, wg);
+    const int smem_max = static_cast<int>(decode_smem_bytes(g, 4));
     if (g.d == 128) {
-        cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+        cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<128>, 32 * wg, smem);
     } else {
-        cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+        cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<64>, 32 * wg, smem);
     }
     return n;
