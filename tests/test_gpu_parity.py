@@ -220,7 +220,9 @@ def test_demote_readmit_round_trip():
 
 
 def test_error_paths():
-    wl = W.workload("tiny", prefill_lens=(32,), pool_pages=3, steps=0)
+    # steps only sizes the table row (7 blocks) so the append below fails on
+    # the pool (1 free page), not on the row length
+    wl = W.workload("tiny", prefill_lens=(32,), pool_pages=3, steps=60)
     run = Run(wl, 0.1)
     ctx = run.ctx
     sid = run.ids[0]
@@ -231,6 +233,10 @@ def test_error_paths():
     with pytest.raises(K.KvsError) as e:           # needs 3 new pages, 1 free
         ctx.append_tokens(sid, Kt, Vt)
     assert e.value.code == K.KVS_ENOMEM
+    Kt, Vt = W.kv_tokens(wl, 0, 32, 32 + 200, "cuda")
+    with pytest.raises(K.KvsError) as e:           # would need 15 blocks in a 7-block row
+        ctx.append_tokens(sid, Kt, Vt)
+    assert e.value.code == K.KVS_EINVAL
     assert ctx.seq_info(sid)[1] == 32               # nothing appended
     with pytest.raises(K.KvsError) as e:
         ctx.decode_step([12345], torch.zeros((1, wl.L, wl.Hq, wl.d), dtype=torch.bfloat16,
