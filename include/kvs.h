@@ -307,6 +307,35 @@ int kvs_seq_info(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t *slot,
  * events stay owned by the caller. */
 int kvs_set_decode_events(kvs_ctx_t *ctx, void *ev_start, void *ev_stop);
 
+/* Decode attention and per-block mass of ONE sequence, for callers that
+ * cannot allocate device memory.  The pages have no counterpart for this
+ * call: it exists for programs that are handed only their input and output
+ * buffers -- a plugin or custom operator running inside another framework's
+ * memory budget, or a serving loop that forbids allocation after start-up.
+ *
+ * Same arithmetic as kvs_decode_step (same kernels) for one sequence, with no
+ * context: pool ([pool_blocks] pages, layout as above), block_table (int32,
+ * ceil(n_tokens/16) page ids), q [L][Hq][d] bf16 and outputs out [L][Hq][d]
+ * float32 and mass [ceil(n_tokens/16)] float32, all device memory owned by
+ * the caller.  The decode scratch lives in a fixed 48 MiB array compiled into
+ * the library (held by every GPU that loads it, until exit); a call needing
+ * more returns KVS_EINVAL with the required size in msg (for the 80-layer,
+ * 8-KV-head, d=128 shape the limit is 12,288 tokens).  Nothing is allocated:
+ * no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * The first call on a device (with that device current) looks up the array's
+ * device address and the decode kernel's occupancy; make that first call
+ * before any stream capture.  Every call shares the array: calls that overlap
+ * on the GPU race, so order them (one stream).  The array keeps the last
+ * call's contents; what must start at zero is cleared by each call.
+ * msg (optional, msg_bytes long) receives a description of a failure. */
+int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads,
+                       uint32_t num_kv_heads, uint32_t head_dim,
+                       const void *pool, uint32_t pool_blocks,
+                       const int32_t *block_table, uint32_t n_tokens,
+                       const void *q, float *out, float *mass, void *stream,
+                       char *msg, size_t msg_bytes);
+
 /* Decode steps completed so far (the step counter t). */
 uint64_t kvs_step_count(const kvs_ctx_t *ctx);
 

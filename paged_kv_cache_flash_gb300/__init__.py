@@ -101,6 +101,8 @@ _SIGS = {
     "kvs_seq_info": (ctypes.c_int, [c_vp, c_u64, ctypes.POINTER(c_u32), ctypes.POINTER(c_u32),
                                     ctypes.POINTER(c_u32), ctypes.POINTER(c_i32), c_u32]),
     "kvs_set_decode_events": (ctypes.c_int, [c_vp, c_vp, c_vp]),
+    "kvs_decode_noalloc": (ctypes.c_int, [c_u32, c_u32, c_u32, c_u32, c_vp, c_u32, c_vp, c_u32,
+                                          c_vp, c_vp, c_vp, c_vp, ctypes.c_char_p, c_sz]),
     "kvs_step_count": (c_u64, [c_vp]),
     "kvs_free_pages": (c_u32, [c_vp]),
     "kvs_check_device": (ctypes.c_int, [c_vp, c_vp]),
