@@ -51,6 +51,8 @@ __global__ void append_kernel(const Geo g, const AppendArgs a, uint64_t rows_tot
     } else {
         const uint64_t j = tid - nvec;                  // new-block index
         const uint32_t nnew = a.first_blk + a.nblk - a.first_new;
+        if (j < a.nblk)
+            a.page_clean[a.pages[j]] = 0;               // page bytes change
         if (j < nnew) {
             const uint32_t b = a.first_new + static_cast<uint32_t>(j);
             const size_t idx = static_cast<size_t>(a.slot) * g.mb + b;
@@ -139,13 +141,16 @@ constexpr int kSelTile = kSelThreads * kSelPerThread;
 
 __device__ __forceinline__ const kvs_record &rec_at(const Geo &g, const DSet *ds,
                                                     const kvs_record *recs, uint32_t r,
-                                                    uint32_t *slot_out, uint32_t *b_out)
+                                                    uint32_t *slot_out, uint32_t *b_out,
+                                                    uint32_t *ntok_out = nullptr)
 {
     const uint32_t si = find_sorted(ds, r);
     const DSeq &sq = ds->seq[ds->sorted[si]];
     const uint32_t b = r - ds->srt_off[si];
     *slot_out = sq.slot;
     *b_out = b;
+    if (ntok_out)
+        *ntok_out = sq.ntok;
     return recs[static_cast<size_t>(sq.slot) * g.mb + b];
 }
 
@@ -204,14 +209,14 @@ __global__ void __launch_bounds__(kSelThreads)
             *w.sel_count = base + w.tile_cnt[blockIdx.x];
     }
     bool pk[kSelPerThread];
-    uint32_t slots[kSelPerThread], bs[kSelPerThread];
+    uint32_t slots[kSelPerThread], bs[kSelPerThread], nts[kSelPerThread];
     kvs_key keys[kSelPerThread];
     uint32_t c = 0;
     for (int q = 0; q < kSelPerThread; ++q) {
         const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
         pk[q] = false;
         if (r < nb_total) {
-            const kvs_record &rec = rec_at(g, ds, recs, r, &slots[q], &bs[q]);
+            const kvs_record &rec = rec_at(g, ds, recs, r, &slots[q], &bs[q], &nts[q]);
             pk[q] = picked(mode, rec, r, w.sel_thr);
             keys[q] = rec.key;
         }
@@ -240,6 +245,7 @@ __global__ void __launch_bounds__(kSelThreads)
         w.sel_recs[pos] = recs[static_cast<size_t>(slots[q]) * g.mb + bs[q]];
         w.sel_pages[pos] = table[static_cast<size_t>(slots[q]) * g.mb + bs[q]];
         w.sel_recidx[pos] = r;
+        w.sel_full[pos] = (bs[q] + 1) * kBlockTokens <= nts[q] ? 1 : 0;
         ++pos;
     }
 }
@@ -311,6 +317,103 @@ __global__ void __launch_bounds__(1024)
     }
 }
 
+// --------------------------------------------------------------- gather plan
+// Exclusive scan of one flag per thread over a 1024-thread block; returns the
+// thread's position and writes the block total to *total.
+__device__ __forceinline__ uint32_t block_scan_1024(uint32_t f, uint32_t *wsum, uint32_t *total)
+{
+    const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint32_t inc = f;
+    for (int x = 1; x < 32; x <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, x);
+        if (lane >= static_cast<uint32_t>(x))
+            inc += y;
+    }
+    if (lane == 31)
+        wsum[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        uint32_t v = wsum[lane], vi = v;
+        for (int x = 1; x < 32; x <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, vi, x);
+            if (lane >= static_cast<uint32_t>(x))
+                vi += y;
+        }
+        wsum[lane] = vi - v;            // exclusive warp offsets
+        if (lane == 31)
+            wsum[32] = vi;
+    }
+    __syncthreads();
+    const uint32_t pos = wsum[wid] + inc - f;
+    *total = wsum[32];
+    __syncthreads();
+    return pos;
+}
+
+// Gather plan of the selected list, one block of 1024 threads:
+//  - a page is eligible when every reference to it is selected (selected
+//    references == reference count), and is planned once, at its first
+//    selected position;
+//  - mirror mode: eligible pages whose host copy is stale form the copy
+//    list, and are marked current (full pages only) for the copy about to be
+//    issued;
+//  - per selected key: its slot (plan position, or page id in mirror mode),
+//    -1 when its page is not eligible.
+// page_cnt / page_first are restored to 0 / ~0 before returning.
+__global__ void __launch_bounds__(1024) plan_kernel(const Work w, uint32_t mirror)
+{
+    __shared__ uint32_t wsum[33];
+    const uint32_t n = *w.sel_count;
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int32_t p = w.sel_pages[i];
+        atomicAdd(&w.page_cnt[p], 1u);
+        atomicMin(&w.page_first[p], i);
+    }
+    __syncthreads();
+    uint32_t npages = 0, ncopy = 0;
+    for (uint32_t t0 = 0; t0 < n; t0 += blockDim.x) {
+        const uint32_t i = t0 + threadIdx.x;
+        uint32_t lead = 0, dirty = 0;
+        int32_t p = 0;
+        if (i < n) {
+            p = w.sel_pages[i];
+            lead = (w.page_cnt[p] == w.dev_refcnt[p] && w.page_first[p] == i) ? 1u : 0u;
+            dirty = (lead && mirror && !w.page_clean[p]) ? 1u : 0u;
+        }
+        uint32_t tot;
+        const uint32_t pos = npages + block_scan_1024(lead, wsum, &tot);
+        if (lead) {
+            w.plan_pages[pos] = p;
+            w.page_pos[p] = static_cast<int32_t>(pos);
+        }
+        npages += tot;
+        const uint32_t cpos = ncopy + block_scan_1024(dirty, wsum, &tot);
+        if (dirty) {
+            w.readback[4 + cpos] = static_cast<uint32_t>(p);
+            w.page_clean[p] = w.sel_full[i];
+        }
+        ncopy += tot;
+    }
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int32_t p = w.sel_pages[i];
+        const bool elig = w.page_cnt[p] == w.dev_refcnt[p];
+        w.plan_slot[i] = elig ? (mirror ? p : w.page_pos[p]) : -1;
+    }
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int32_t p = w.sel_pages[i];
+        w.page_cnt[p] = 0;
+        w.page_first[p] = 0xffffffffu;
+    }
+    if (threadIdx.x == 0) {
+        w.readback[0] = n;
+        w.readback[1] = npages;
+        w.readback[2] = ncopy;
+        w.readback[3] = 0;
+    }
+}
+
 // ------------------------------------------------------------------- gather
 // grid.x = pages, grid.y = parts of a page; 16-byte vector copies.
 __global__ void __launch_bounds__(256)
@@ -326,8 +429,8 @@ __global__ void __launch_bounds__(256)
         dst[i] = __ldcs(src + i);
 }
 
-__global__ void patch_kernel(const Geo g, int32_t *table, kvs_record *recs, const Patch *p,
-                             uint32_t n)
+__global__ void patch_kernel(const Geo g, int32_t *table, kvs_record *recs, uint8_t *page_clean,
+                             const Patch *p, uint32_t n)
 {
     const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n)
@@ -335,7 +438,9 @@ __global__ void patch_kernel(const Geo g, int32_t *table, kvs_record *recs, cons
     const Patch q = p[i];
     const size_t idx = static_cast<size_t>(q.slot) * g.mb + q.block;
     table[idx] = q.page;
-    if (q.has_record)
+    if (q.page >= 0 && (q.what & kPatchPageWritten))
+        page_clean[q.page] = 0;          // page bytes were rewritten (readmit)
+    if (q.what & kPatchRecord)
         recs[idx] = q.rec;
 }
 
@@ -356,8 +461,7 @@ cudaError_t launch_append(const Geo &g, const AppendArgs &a, cudaStream_t s)
     // rows cover every slot from p0 to the end of the last touched block
     const uint64_t slots = static_cast<uint64_t>(a.first_blk + a.nblk) * kBlockTokens - a.p0;
     const uint64_t rows = slots * g.L * 2 * g.Hkv;
-    const uint64_t nnew = a.first_blk + a.nblk - a.first_new;
-    const uint64_t threads = rows * vec_per_row + nnew;
+    const uint64_t threads = rows * vec_per_row + a.nblk;   // nblk >= new blocks
     const uint32_t bs = 256;
     const uint64_t grid = (threads + bs - 1) / bs;
     if (grid > 0x7fffffffull)
@@ -401,10 +505,16 @@ cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pag
     return cudaGetLastError();
 }
 
-cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, const Patch *p, uint32_t n,
-                         cudaStream_t s)
+cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, uint8_t *page_clean,
+                         const Patch *p, uint32_t n, cudaStream_t s)
 {
-    patch_kernel<<<(n + 127) / 128, 128, 0, s>>>(g, table, rec, p, n);
+    patch_kernel<<<(n + 127) / 128, 128, 0, s>>>(g, table, rec, page_clean, p, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const Work &w, uint32_t mirror, cudaStream_t s)
+{
+    plan_kernel<<<1, 1024, 0, s>>>(w, mirror);
     return cudaGetLastError();
 }
 

@@ -99,7 +99,8 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &a0, uint32_t &a
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                 : "r"(addr));
+                 : "r"(addr)
+                 : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &a0, uint32_t &a1, uint32_t &a2,
@@ -107,7 +108,8 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &a0, uint32_t 
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                 : "r"(addr));
+                 : "r"(addr)
+                 : "memory");
 }
 
 // D (16x8 f32) += A (16x16 bf16, row) * B (16x8 bf16, col)
@@ -166,6 +168,122 @@ struct Tile {
     static constexpr int kStageBytes = kHalf * kBoxBytes;
 };
 
+// A claimed work item: one chunk of blocks of one (sequence, layer, KV head)
+// stream, decoded by one warp.
+struct Item {
+    uint32_t valid;
+    uint32_t ci;        // sequence (call order)
+    uint32_t l;         // layer
+    uint32_t kvh;       // KV head
+    uint32_t b0;        // first block
+    uint32_t nblk;      // blocks in the chunk
+    uint32_t ntok;      // tokens of the sequence
+    uint32_t part;      // partial index
+    uint32_t lse0;      // blk_off + b0: column of the chunk's first block in lse_blk
+};
+
+// An item with its page ids: lane j holds those of blocks j, j+32, j+64, j+96.
+struct Prep {
+    Item it;
+    int32_t pg[kMaxChunk / 32];
+};
+
+__device__ __forceinline__ Prep prepare_item(const DecodeArgs &a, uint32_t id, uint32_t lane)
+{
+    Prep p;
+    p.it.valid = 0;
+    p.it.nblk = 0;
+    if (id >= a.n_items)
+        return p;
+    const DSet *ds = a.w.dset;
+    const Geo &g = a.g;
+    const uint32_t ci = find_seq(&ds->seq[0].item_off, sizeof(DSeq) / 4, ds->nseq, id);
+    const DSeq &sq = ds->seq[ci];
+    // KV head fastest: warps that claim consecutive items read adjacent
+    // sub-pages of the same pages at about the same time (DRAM locality)
+    uint32_t local = id - sq.item_off;
+    const uint32_t kvh = local % g.Hkv;
+    local /= g.Hkv;
+    const uint32_t chunk = local % sq.nchunk;
+    const uint32_t l = local / sq.nchunk;
+    const uint32_t b0 = chunk * ds->chunk;
+    const uint32_t nblk = min(ds->chunk, sq.nb - b0);
+    p.it.valid = 1;
+    p.it.ci = ci;
+    p.it.l = l;
+    p.it.kvh = kvh;
+    p.it.b0 = b0;
+    p.it.nblk = nblk;
+    p.it.ntok = sq.ntok;
+    p.it.part = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk + chunk;
+    p.it.lse0 = sq.blk_off + b0;
+    const int32_t *trow = a.table + static_cast<size_t>(sq.slot) * g.mb + b0;
+#pragma unroll
+    for (int q = 0; q < static_cast<int>(kMaxChunk / 32); ++q) {
+        const uint32_t j = lane + 32 * q;
+        int32_t pgid = j < nblk ? __ldg(trow + j) : 0;
+        if (pgid < 0 || pgid >= static_cast<int32_t>(g.pool_blocks)) {
+            atomicOr(a.w.err, kErrBadPage);
+            atomicCAS(a.w.err_info, 0u, static_cast<uint32_t>(pgid) | 0x80000000u);
+            pgid = 0;
+        }
+        p.pg[q] = pgid;
+    }
+    return p;
+}
+
+__device__ __forceinline__ int32_t page_of(const Prep &p, uint32_t j)
+{
+    // a select chain, not an indexed load: the page ids stay in registers
+    static_assert(kMaxChunk == 32 || kMaxChunk == 64 || kMaxChunk == 128, "chunk cap");
+    const uint32_t q = j >> 5;
+    int32_t page = p.pg[0];
+    if constexpr (kMaxChunk >= 64)
+        page = q == 1 ? p.pg[1] : page;
+    if constexpr (kMaxChunk >= 128)
+        page = q == 2 ? p.pg[2] : (q == 3 ? p.pg[3] : page);
+    return __shfl_sync(0xffffffffu, page, j & 31);
+}
+
+// Issues the next block of a warp's stream (items cur, then nxt) into its TMA
+// ring; false when the stream position is not known yet.  Warp-uniform.
+template <int D>
+__device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g, const Prep &cur,
+                                           const Prep &nxt, bool have_nxt, bool &c_in_nxt,
+                                           uint32_t &c_blk, uint32_t &k_issue, uint32_t ring_u32,
+                                           uint64_t *bars, uint32_t lane)
+{
+    using T = Tile<D>;
+    if (!c_in_nxt && c_blk >= cur.it.nblk) {
+        if (!have_nxt || !nxt.it.valid)
+            return false;
+        c_in_nxt = true;
+        c_blk = 0;
+    }
+    if (c_in_nxt && c_blk >= nxt.it.nblk)
+        return false;
+    const uint32_t l = c_in_nxt ? nxt.it.l : cur.it.l;
+    const uint32_t kv = c_in_nxt ? nxt.it.kvh : cur.it.kvh;
+    const int32_t page = c_in_nxt ? page_of(nxt, c_blk) : page_of(cur, c_blk);
+    if (lane == 0) {
+        const uint32_t st = k_issue % kStages;
+        const uint32_t bar = smem_u32(&bars[st]);
+        mbar_expect_tx(bar, T::kStageBytes);
+        const int c4 = page * static_cast<int>(g.L) + static_cast<int>(l);
+#pragma unroll
+        for (int h = 0; h < T::kHalf; ++h)
+            tma_load_5d(ring_u32 + st * T::kStageBytes + h * T::kBoxBytes, tmap, bar, h * 64, 0,
+                        static_cast<int>(kv), 0, c4);
+    }
+    ++c_blk;
+    ++k_issue;
+    return true;
+}
+
+// Persistent kernel of fully independent warps.  Each warp claims work items
+// (one KV-head stream chunk each) from a global counter, prepares the next
+// item while it computes the current one, and keeps its own TMA ring of
+// kStages blocks in flight across item boundaries.  No CTA-wide barrier.
 template <int D>
 __global__ void __launch_bounds__(256, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a)
@@ -173,15 +291,11 @@ __global__ void __launch_bounds__(256, 1)
     using T = Tile<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[8][kStages];
-    __shared__ uint32_t item_sh;
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // 1024-byte alignment for the 128-byte swizzle atoms
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *ring = smem + warp * kStages * T::kStageBytes;
-    const uint32_t ring_u32 = smem_u32(ring);
-
+    const uint32_t ring_u32 = smem_u32(smem + warp * kStages * T::kStageBytes);
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s)
             mbar_init(smem_u32(&bars[warp][s]), 1);
@@ -191,60 +305,42 @@ __global__ void __launch_bounds__(256, 1)
     __syncwarp();
 
     const Geo &g = a.g;
-    const DSet *ds = a.w.dset;
     const uint32_t G = g.G;
     const uint32_t gq = lane >> 2;          // row group id in MMA fragments
     const uint32_t tq = lane & 3;           // thread in group
     const uint32_t h0 = 2 * tq, h1 = 2 * tq + 1;   // heads of this lane's S/O columns
     const float scale_log2 = rsqrtf(static_cast<float>(D)) * kLog2e;
-    uint32_t kload = 0;                     // blocks this warp has consumed so far
+    const uint32_t nb_total = a.w.dset->nb_total;
+    const uint32_t jm = lane >> 3, i8 = lane & 7;
 
-    for (;;) {
-        __syncthreads();
-        if (threadIdx.x == 0)
-            item_sh = atomicAdd(a.w.counter, 1u);
-        __syncthreads();
-        const uint32_t item = item_sh;
-        if (item >= a.n_items)
-            break;
+    uint32_t claimed = 0;
+    if (lane == 0)
+        claimed = atomicAdd(a.w.counter, 1u);
+    Prep cur = prepare_item(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+    if (lane == 0)
+        claimed = atomicAdd(a.w.counter, 1u);   // id of the item after cur
+    Prep nxt;
+    nxt.it.valid = 0;
+    nxt.it.nblk = 0;
+    bool have_nxt = false;
 
-        // ---- decode the work item -------------------------------------
-        const uint32_t ci = find_seq(&ds->seq[0].item_off, sizeof(DSeq) / 4, ds->nseq, item);
-        const DSeq sq = ds->seq[ci];
-        uint32_t local = item - sq.item_off;
-        const uint32_t chunk = local % sq.nchunk;
-        local /= sq.nchunk;
-        const uint32_t ngg = g.Hkv / a.wg;
-        const uint32_t l = local / ngg, gg = local % ngg;
-        const uint32_t kvh = gg * a.wg + warp;
-        const uint32_t b0 = chunk * kChunkBlocks;
-        const uint32_t nblk = min(static_cast<uint32_t>(kChunkBlocks), sq.nb - b0);
-
-        // page ids of the chunk's blocks (lane j holds blocks j and 32 + j)
-        const int32_t *trow = a.table + static_cast<size_t>(sq.slot) * g.mb + b0;
-        int32_t pg_lo = lane < nblk ? __ldg(trow + lane) : 0;
-        int32_t pg_hi = lane + 32 < nblk ? __ldg(trow + lane + 32) : 0;
-        if (pg_lo < 0 || pg_lo >= static_cast<int32_t>(g.pool_blocks)) {
-            if (lane < nblk) {
-                atomicOr(a.w.err, kErrBadPage);
-                atomicCAS(a.w.err_info, 0u, static_cast<uint32_t>(pg_lo) | 0x80000000u);
-            }
-            pg_lo = 0;
+    uint32_t k_issue = 0, k_cons = 0;       // blocks issued / consumed by this warp
+    bool c_in_nxt = false;                  // issue cursor: item (cur / nxt) and block
+    uint32_t c_blk = 0;
+    if (cur.it.valid)
+        while (k_issue - k_cons < kStages && issue_next<D>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
         }
-        if (pg_hi < 0 || pg_hi >= static_cast<int32_t>(g.pool_blocks)) {
-            if (lane + 32 < nblk) {
-                atomicOr(a.w.err, kErrBadPage);
-                atomicCAS(a.w.err_info, 0u, static_cast<uint32_t>(pg_hi) | 0x80000000u);
-            }
-            pg_hi = 0;
-        }
+
+    while (cur.it.valid) {
+        const Item it = cur.it;
+        const uint32_t kvh = it.kvh;
 
         // query fragments (B operand of S^T = K Q^T): head gq, dims 16ks+2tq(+1), +8
         uint32_t qf[D / 16][2];
         {
             const bool valid = gq < G;
-            const uint16_t *qh =
-                a.q + ((static_cast<size_t>(ci) * g.L + l) * g.Hq + kvh * G + (valid ? gq : 0)) * D;
+            const uint16_t *qh = a.q + ((static_cast<size_t>(it.ci) * g.L + it.l) * g.Hq + kvh * G +
+                                        (valid ? gq : 0)) * D;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 qf[ks][0] = valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 2 * tq)) : 0u;
@@ -252,40 +348,16 @@ __global__ void __launch_bounds__(256, 1)
                     valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 8 + 2 * tq)) : 0u;
             }
         }
-
-        // ---- prologue: fill the ring ------------------------------------
-        auto issue = [&](uint32_t i) {
-            const int32_t page = __shfl_sync(0xffffffffu, i < 32 ? pg_lo : pg_hi, i & 31);
-            if (lane == 0) {
-                const uint32_t st = (kload + i) % kStages;
-                const uint32_t bar = smem_u32(&bars[warp][st]);
-                mbar_expect_tx(bar, T::kStageBytes);
-                const int c4 = page * static_cast<int>(g.L) + static_cast<int>(l);
-#pragma unroll
-                for (int h = 0; h < T::kHalf; ++h)
-                    tma_load_5d(ring_u32 + st * T::kStageBytes + h * T::kBoxBytes, &tmap, bar, h * 64,
-                                0, static_cast<int>(kvh), 0, c4);
-            }
-        };
-        const uint32_t npre = min(nblk, static_cast<uint32_t>(kStages));
-        for (uint32_t i = 0; i < npre; ++i)
-            issue(i);
-
         float o[D / 16][4];
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt)
             o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float *lse_row0 = a.w.lse_blk + (static_cast<size_t>(it.l) * g.Hq + kvh * G + h0) * nb_total + it.lse0;
 
-        const uint32_t jm = lane >> 3, i8 = lane & 7;
-        float *lse_row0 = a.w.lse_blk + (static_cast<size_t>(l) * g.Hq + kvh * G + h0) * ds->nb_total +
-                          sq.blk_off + b0;
-        const size_t lse_head_stride = ds->nb_total;
-
-        for (uint32_t i = 0; i < nblk; ++i) {
-            const uint32_t k = kload + i;
-            const uint32_t st = k % kStages;
-            mbar_wait(smem_u32(&bars[warp][st]), (k / kStages) & 1u, a.w.err);
+        for (uint32_t i = 0; i < it.nblk; ++i) {
+            const uint32_t st = k_cons % kStages;
+            mbar_wait(smem_u32(&bars[warp][st]), (k_cons / kStages) & 1u, a.w.err);
             const uint32_t base = ring_u32 + st * T::kStageBytes;
 
             // S^T = K . Q^T  (rows: 16 tokens, cols: 8 heads)
@@ -300,12 +372,21 @@ __global__ void __launch_bounds__(256, 1)
                 ldsm_x4(addr, a0, a1, a2, a3);
                 mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
             }
-            const uint32_t blk = b0 + i;
-            const uint32_t tok0 = blk * kBlockTokens + gq, tok1 = tok0 + 8;
-            s[0] = tok0 < sq.ntok ? s[0] * scale_log2 : -INFINITY;
-            s[1] = tok0 < sq.ntok ? s[1] * scale_log2 : -INFINITY;
-            s[2] = tok1 < sq.ntok ? s[2] * scale_log2 : -INFINITY;
-            s[3] = tok1 < sq.ntok ? s[3] * scale_log2 : -INFINITY;
+            // V fragments (A operand of O^T = V^T P^T): read before the stage is refilled
+            uint32_t va[D / 16][4];
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const uint32_t h = mt >> 2, c0 = (mt & 3) * 2;
+                const uint32_t row = 16 + i8 + 8 * (jm >> 1);    // V half, token
+                const uint32_t chunk16 = c0 + (jm & 1);
+                const uint32_t addr = base + h * T::kBoxBytes + row * 128 + ((chunk16 ^ (row & 7)) << 4);
+                ldsm_x4_t(addr, va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+            }
+            const uint32_t tok0 = (it.b0 + i) * kBlockTokens + gq, tok1 = tok0 + 8;
+            s[0] = tok0 < it.ntok ? s[0] * scale_log2 : -INFINITY;
+            s[1] = tok0 < it.ntok ? s[1] * scale_log2 : -INFINITY;
+            s[2] = tok1 < it.ntok ? s[2] * scale_log2 : -INFINITY;
+            s[3] = tok1 < it.ntok ? s[3] * scale_log2 : -INFINITY;
 
             float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
 #pragma unroll
@@ -313,6 +394,12 @@ __global__ void __launch_bounds__(256, 1)
                 bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
                 bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
             }
+            // every lane has its K and V fragments: refill the stage
+            __syncwarp();
+            ++k_cons;
+            if (k_issue - k_cons < kStages)
+                issue_next<D>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane);
+
             const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
             const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
             const float p0 = fast_exp2(s[0] - mn0), p1 = fast_exp2(s[1] - mn1);
@@ -331,7 +418,7 @@ __global__ void __launch_bounds__(256, 1)
                 if (h0 < G)
                     lse_row0[i] = mn0 + fast_log2(w0);
                 if (h1 < G)
-                    lse_row0[lse_head_stride + i] = mn1 + fast_log2(w1);
+                    lse_row0[nb_total + i] = mn1 + fast_log2(w1);
             }
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
@@ -345,23 +432,22 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
             // O^T += V^T . P^T  (rows: d, cols: 8 heads)
 #pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                const uint32_t h = mt >> 2, c0 = (mt & 3) * 2;
-                const uint32_t row = 16 + i8 + 8 * (jm >> 1);    // V half, token
-                const uint32_t chunk16 = c0 + (jm & 1);
-                const uint32_t addr = base + h * T::kBoxBytes + row * 128 + ((chunk16 ^ (row & 7)) << 4);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(addr, a0, a1, a2, a3);
-                mma_bf16(o[mt], a0, a1, a2, a3, pb0, pb1);
+            for (int mt = 0; mt < D / 16; ++mt)
+                mma_bf16(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pb0, pb1);
+
+            if (i == 0 && !have_nxt) {
+                // while the ring streams: the next item and the claim after it
+                nxt = prepare_item(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+                have_nxt = true;
+                if (lane == 0 && nxt.it.valid)
+                    claimed = atomicAdd(a.w.counter, 1u);
+                while (k_issue - k_cons < kStages && issue_next<D>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
+                }
             }
-            __syncwarp();
-            if (i + kStages < nblk)
-                issue(i + kStages);
         }
-        kload += nblk;
 
         // ---- chunk partials ----------------------------------------------
-        const uint32_t part = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk + chunk;
+        const uint32_t part = it.part;
         if (gq == 0) {
             a.w.part_ml[part * kMaxGroup + h0] = make_float2(m0, l0);
             a.w.part_ml[part * kMaxGroup + h1] = make_float2(m1, l1);
@@ -374,13 +460,35 @@ __global__ void __launch_bounds__(256, 1)
             po[h0 * D + mt * 16 + gq + 8] = o[mt][2];
             po[h1 * D + mt * 16 + gq + 8] = o[mt][3];
         }
+
+        // ---- the next item becomes current ----------------------------------
+        if (!have_nxt) {                    // a one-block item: prepare now
+            nxt = prepare_item(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+            if (lane == 0 && nxt.it.valid)
+                claimed = atomicAdd(a.w.counter, 1u);
+        }
+        if (c_in_nxt) {
+            c_in_nxt = false;               // cursor already inside the new item
+        } else {
+            c_blk = 0;
+        }
+        cur = nxt;
+        have_nxt = false;
+        nxt.it.valid = 0;
+        nxt.it.nblk = 0;
+        while (cur.it.valid && k_issue - k_cons < kStages && issue_next<D>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
+        }
     }
 }
 
-// One CTA per (sequence, layer, KV head); warp h merges query head h's chunks.
+// One CTA per (sequence, layer, KV head).  Warp h merges query head h's
+// chunks into its log2-sum-exp and output; then the CTA turns the per-block
+// log2-sum-exps of its G heads into the stream's block masses
+//   stream_mass(b) = sum_h 2^(lse_blk(h, b) - LSE_h).
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w, float *out)
 {
+    __shared__ float lse_sh[kMaxGroup];
     const DSet *ds = w.dset;
     const uint32_t lane = threadIdx.x & 31, h = threadIdx.x >> 5;
     const uint32_t ci = blockIdx.x / (g.L * g.Hkv);
@@ -388,39 +496,51 @@ __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w,
     const uint32_t l = rest / g.Hkv, kvh = rest % g.Hkv;
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *w.counter = 0;            // ready for the next decode launch
-    if (h >= g.G)
-        return;
     const DSeq sq = ds->seq[ci];
-    const uint32_t pb = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk;
-    float mmax = -INFINITY;
-    for (uint32_t c = 0; c < sq.nchunk; ++c)
-        mmax = fmaxf(mmax, w.part_ml[(pb + c) * kMaxGroup + h].x);
-    constexpr int E = D / 32;
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e)
-        acc[e] = 0.f;
-    float lsum = 0.f;
-    for (uint32_t c = 0; c < sq.nchunk; ++c) {
-        const float2 ml = w.part_ml[(pb + c) * kMaxGroup + h];
-        const float f = fast_exp2(ml.x - mmax);
-        lsum += ml.y * f;
-        const float *po = w.part_o + (static_cast<size_t>(pb + c) * kMaxGroup + h) * D + lane * E;
+    if (h < g.G) {
+        const uint32_t pb = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk;
+        float mmax = -INFINITY;
+        for (uint32_t c = 0; c < sq.nchunk; ++c)
+            mmax = fmaxf(mmax, w.part_ml[(pb + c) * kMaxGroup + h].x);
+        constexpr int E = D / 32;
+        float acc[E];
 #pragma unroll
         for (int e = 0; e < E; ++e)
-            acc[e] += po[e] * f;
-    }
-    const float inv = 1.f / lsum;
-    const uint32_t hq = kvh * g.G + h;
-    float *dst = out + ((static_cast<size_t>(ci) * g.L + l) * g.Hq + hq) * D + lane * E;
+            acc[e] = 0.f;
+        float lsum = 0.f;
+        for (uint32_t c = 0; c < sq.nchunk; ++c) {
+            const float2 ml = w.part_ml[(pb + c) * kMaxGroup + h];
+            const float f = fast_exp2(ml.x - mmax);
+            lsum += ml.y * f;
+            const float *po = w.part_o + (static_cast<size_t>(pb + c) * kMaxGroup + h) * D + lane * E;
 #pragma unroll
-    for (int e = 0; e < E; ++e)
-        dst[e] = acc[e] * inv;
-    if (lane == 0)
-        w.lse_head[static_cast<size_t>(ci) * g.L * g.Hq + l * g.Hq + hq] = mmax + fast_log2(lsum);
+            for (int e = 0; e < E; ++e)
+                acc[e] += po[e] * f;
+        }
+        const float inv = 1.f / lsum;
+        const uint32_t hq = kvh * g.G + h;
+        float *dst = out + ((static_cast<size_t>(ci) * g.L + l) * g.Hq + hq) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            dst[e] = acc[e] * inv;
+        if (lane == 0)
+            lse_sh[h] = mmax + fast_log2(lsum);
+    }
+    __syncthreads();
+    const uint32_t nbt = ds->nb_total;
+    const float *lb = w.lse_blk + (static_cast<size_t>(l) * g.Hq + kvh * g.G) * nbt + sq.blk_off;
+    float *sm = w.stream_mass + (static_cast<size_t>(l) * g.Hkv + kvh) * nbt + sq.blk_off;
+    for (uint32_t b = threadIdx.x; b < sq.nb; b += blockDim.x) {
+        float acc = 0.f;
+        for (uint32_t j = 0; j < g.G; ++j)
+            acc += fast_exp2(lb[static_cast<size_t>(j) * nbt + b] - lse_sh[j]);
+        sm[b] = acc;
+    }
 }
 
-// 32 consecutive blocks per CTA x 8 partial sums over (layer, head) pairs.
+// M(b) = 1/(L*Hq) * sum over the L*Hkv streams of stream_mass(b): 32
+// consecutive blocks per CTA x 8 interleaved partial sums, added in a fixed
+// order (deterministic).
 __global__ void __launch_bounds__(256) mass_kernel(const Geo g, const Work w, float *mass,
                                                    uint32_t nb_total)
 {
@@ -428,15 +548,11 @@ __global__ void __launch_bounds__(256) mass_kernel(const Geo g, const Work w, fl
     const DSet *ds = w.dset;
     const uint32_t i = threadIdx.x & 31, j = threadIdx.x >> 5;
     const uint32_t r = blockIdx.x * 32 + i;
-    const uint32_t LH = g.L * g.Hq;
+    const uint32_t LS = g.L * g.Hkv;
     float acc = 0.f;
-    uint32_t ci = 0;
-    if (r < nb_total) {
-        ci = find_seq(&ds->seq[0].blk_off, sizeof(DSeq) / 4, ds->nseq, r);
-        const float *lh_row = w.lse_head + static_cast<size_t>(ci) * LH;
-        for (uint32_t lh = j; lh < LH; lh += 8)
-            acc += fast_exp2(w.lse_blk[static_cast<size_t>(lh) * nb_total + r] - lh_row[lh]);
-    }
+    if (r < nb_total)
+        for (uint32_t s = j; s < LS; s += 8)
+            acc += w.stream_mass[static_cast<size_t>(s) * nb_total + r];
     part[j][i] = acc;
     __syncthreads();
     if (j == 0 && r < nb_total) {
@@ -444,11 +560,12 @@ __global__ void __launch_bounds__(256) mass_kernel(const Geo g, const Work w, fl
 #pragma unroll
         for (int q = 1; q < 8; ++q)
             t += part[q][i];
+        const uint32_t ci = find_seq(&ds->seq[0].blk_off, sizeof(DSeq) / 4, ds->nseq, r);
         const DSeq sq = ds->seq[ci];
-        mass[static_cast<size_t>(sq.slot) * g.mb + (r - sq.blk_off)] = t / static_cast<float>(LH);
+        mass[static_cast<size_t>(sq.slot) * g.mb + (r - sq.blk_off)] =
+            t / static_cast<float>(g.L * g.Hq);
     }
 }
-
 }  // namespace
 
 size_t decode_smem_bytes(const Geo &g, uint32_t wg)

@@ -31,6 +31,7 @@ namespace {
 
 constexpr uint32_t kRingSlots = 8;
 constexpr size_t kRingSlotBytes = size_t(1) << 20;
+constexpr size_t kReadbackBytes = 16384;            // header + first copy-list entries
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -75,7 +76,7 @@ struct kvs_ctx {
     std::vector<uint32_t> free_slots;
     std::deque<int32_t> free_pages;
     std::vector<uint32_t> refcnt;
-    std::vector<uint8_t> mirror_clean;              // host mirror copy is current
+    bool refcnt_dirty = true;                       // device mirror needs an upload
     std::map<std::pair<uint64_t, uint64_t>, Demoted> store;
     uint64_t t = 0;
 
@@ -216,10 +217,17 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
         return fail(ctx, KVS_EINVAL, "nseq must be in [1, %u]", kMaxCallSeqs);
     std::memset(ds, 0, sizeof(DSet));
     const Geo &g = ctx->geo;
-    const uint32_t ngg = g.Hkv / ctx->wg;
     uint32_t blk = 0, items = 0, parts = 0;
     std::vector<std::pair<uint64_t, uint32_t>> order;
     order.reserve(nseq);
+    uint32_t nbs[kMaxCallSeqs];
+    for (uint32_t i = 0; i < nseq; ++i) {
+        SeqState *s = find_seq(ctx, ids[i]);
+        nbs[i] = s ? (s->ntok + kBlockTokens - 1) / kBlockTokens : 1;
+    }
+    const uint32_t chunk = pick_chunk(nbs, nseq, g.L, g.Hkv, ctx->decode_grid * ctx->wg, ctx->lay.parts_max);
+    if (chunk == 0)
+        return fail(ctx, KVS_EINVAL, "too many blocks in one call for the workspace partials");
     for (uint32_t i = 0; i < nseq; ++i) {
         uint32_t slot;
         SeqState *s = find_seq(ctx, ids[i], &slot);
@@ -235,13 +243,13 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
         q.slot = slot;
         q.ntok = s->ntok;
         q.nb = (s->ntok + kBlockTokens - 1) / kBlockTokens;
-        q.nchunk = (q.nb + kChunkBlocks - 1) / kChunkBlocks;
+        q.nchunk = (q.nb + chunk - 1) / chunk;
         q.blk_off = blk;
         q.item_off = items;
         q.part_off = parts;
         q.seq_id = ids[i];
         blk += q.nb;
-        items += g.L * ngg * q.nchunk;
+        items += g.L * g.Hkv * q.nchunk;      // one item per KV head and chunk
         parts += g.L * g.Hkv * q.nchunk;
         order.emplace_back(ids[i], i);
     }
@@ -267,6 +275,7 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
     ds->n_items = items;
     ds->n_parts = parts;
     ds->wg = ctx->wg;
+    ds->chunk = chunk;
     ds->t = ctx->t;
     return KVS_OK;
 }
@@ -305,7 +314,7 @@ int apply_patches(kvs_ctx *ctx, const std::vector<Patch> &p, cudaStream_t s)
         if ((rc = launch_rc(ctx,
                             launch_patch(ctx->geo, static_cast<int32_t *>(ctx->buf.block_table),
                                          static_cast<kvs_record *>(ctx->buf.records),
-                                         reinterpret_cast<const Patch *>(r.dev),
+                                         ctx->work.page_clean, reinterpret_cast<const Patch *>(r.dev),
                                          static_cast<uint32_t>(n), s),
                             "patch")))
             return rc;
@@ -340,8 +349,9 @@ Layout workspace_layout(const kvs_config &c)
     const size_t seqs = std::min<size_t>(c.max_seqs, kMaxCallSeqs);
     const size_t LH = static_cast<size_t>(c.num_layers) * c.num_q_heads;
     L.nb_max = static_cast<uint32_t>(nb_max);
+    // partials for chunks of 32 blocks (the decode picks 16 only when they fit)
     L.parts_max = static_cast<uint32_t>(static_cast<size_t>(c.num_layers) * c.num_kv_heads *
-                                        ((nb_max + kChunkBlocks - 1) / kChunkBlocks + seqs));
+                                        ((nb_max + 31) / 32 + seqs));
     L.tiles_max = static_cast<uint32_t>((nb_max + 1023) / 1024 + 1);
     L.ring_slots = kRingSlots;
     L.ring_slot_bytes = kRingSlotBytes;
@@ -359,12 +369,21 @@ Layout workspace_layout(const kvs_config &c)
     L.part_ml = take(static_cast<size_t>(L.parts_max) * kMaxGroup * sizeof(float2));
     L.part_o = take(static_cast<size_t>(L.parts_max) * kMaxGroup * c.head_dim * sizeof(float));
     L.lse_blk = take(LH * nb_max * sizeof(float));
-    L.lse_head = take(seqs * LH * sizeof(float));
+    L.stream_mass = take(static_cast<size_t>(c.num_layers) * c.num_kv_heads * nb_max * sizeof(float));
     L.tile_cnt = take(L.tiles_max * sizeof(uint32_t));
     L.sel_ids = take(nb_max * sizeof(kvs_key));
     L.sel_pages = take(nb_max * sizeof(int32_t));
     L.sel_recidx = take(nb_max * sizeof(uint32_t));
     L.sel_recs = take(nb_max * sizeof(kvs_record));
+    L.sel_full = take(nb_max);
+    L.dev_refcnt = take(static_cast<size_t>(c.pool_blocks) * 4);
+    L.page_cnt = take(static_cast<size_t>(c.pool_blocks) * 4);
+    L.page_first = take(static_cast<size_t>(c.pool_blocks) * 4);
+    L.page_pos = take(static_cast<size_t>(c.pool_blocks) * 4);
+    L.page_clean = take(c.pool_blocks);
+    L.plan_pages = take(nb_max * 4);
+    L.plan_slot = take(nb_max * 4);
+    L.readback = take((4 + nb_max) * 4);
     L.ring = take(kRingSlots * kRingSlotBytes);
     L.total = o;
     return L;
@@ -383,12 +402,21 @@ Work carve(const Layout &L, void *ws)
     w.part_ml = reinterpret_cast<float2 *>(b + L.part_ml);
     w.part_o = reinterpret_cast<float *>(b + L.part_o);
     w.lse_blk = reinterpret_cast<float *>(b + L.lse_blk);
-    w.lse_head = reinterpret_cast<float *>(b + L.lse_head);
+    w.stream_mass = reinterpret_cast<float *>(b + L.stream_mass);
     w.tile_cnt = reinterpret_cast<uint32_t *>(b + L.tile_cnt);
     w.sel_ids = reinterpret_cast<kvs_key *>(b + L.sel_ids);
     w.sel_pages = reinterpret_cast<int32_t *>(b + L.sel_pages);
     w.sel_recidx = reinterpret_cast<uint32_t *>(b + L.sel_recidx);
     w.sel_recs = reinterpret_cast<kvs_record *>(b + L.sel_recs);
+    w.sel_full = b + L.sel_full;
+    w.dev_refcnt = reinterpret_cast<uint32_t *>(b + L.dev_refcnt);
+    w.page_cnt = reinterpret_cast<uint32_t *>(b + L.page_cnt);
+    w.page_first = reinterpret_cast<uint32_t *>(b + L.page_first);
+    w.page_pos = reinterpret_cast<int32_t *>(b + L.page_pos);
+    w.page_clean = b + L.page_clean;
+    w.plan_pages = reinterpret_cast<int32_t *>(b + L.plan_pages);
+    w.plan_slot = reinterpret_cast<int32_t *>(b + L.plan_slot);
+    w.readback = reinterpret_cast<uint32_t *>(b + L.readback);
     w.ring = b + L.ring;
     return w;
 }
@@ -487,9 +515,13 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
     CU(cudaMemset(buf->records, 0, ctx->sz.records_bytes));
     CU(cudaMemset(buf->mass, 0, ctx->sz.mass_bytes));
     CU(cudaMemset(buf->workspace, 0, ctx->lay.dset));   // error word, counters
+    CU(cudaMemset(ctx->work.page_cnt, 0, static_cast<size_t>(cfg->pool_blocks) * 4));
+    CU(cudaMemset(ctx->work.page_first, 0xff, static_cast<size_t>(cfg->pool_blocks) * 4));
+    CU(cudaMemset(ctx->work.page_clean, 0, cfg->pool_blocks));
+    CU(cudaMemset(ctx->work.dev_refcnt, 0, static_cast<size_t>(cfg->pool_blocks) * 4));
     CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->ring_host), kRingSlots * kRingSlotBytes,
                      cudaHostAllocDefault));
-    CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->pinned_small), 256, cudaHostAllocDefault));
+    CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->pinned_small), kReadbackBytes, cudaHostAllocDefault));
     for (auto &e : ctx->ring_ev)
         CU(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     for (int i = 0; i < 2; ++i) {
@@ -513,7 +545,6 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
     }
     ctx->free_pages.assign(perm.begin(), perm.end());
     ctx->refcnt.assign(cfg->pool_blocks, 0);
-    ctx->mirror_clean.assign(cfg->pool_blocks, 0);
     *out = holder.release();
     return KVS_OK;
 }
@@ -576,7 +607,7 @@ int kvs_seq_add(kvs_ctx_t *ctx, uint64_t seq_id, int64_t parent, uint32_t shared
         p.slot = slot;
         p.block = b;
         p.page = par->table[b];
-        p.has_record = 1;
+        p.what = kPatchRecord;
         p.rec = fresh_record(seq_id, b, ctx->t);
         patches.push_back(p);
     }
@@ -595,6 +626,7 @@ int kvs_seq_add(kvs_ctx_t *ctx, uint64_t seq_id, int64_t parent, uint32_t shared
         s.table.push_back(par->table[b]);
         ctx->refcnt[par->table[b]] += 1;
     }
+    ctx->refcnt_dirty = true;
     s.ntok = shared_blocks * kBlockTokens;
     ctx->slot_of[seq_id] = slot;
     return KVS_OK;
@@ -613,11 +645,10 @@ int kvs_seq_remove(kvs_ctx_t *ctx, uint64_t seq_id, void *stream)
     for (int32_t p : s->table) {
         if (p < 0)
             continue;
-        if (--ctx->refcnt[p] == 0) {
+        if (--ctx->refcnt[p] == 0)
             ctx->free_pages.push_back(p);
-            ctx->mirror_clean[p] = 0;
-        }
     }
+    ctx->refcnt_dirty = true;
     for (auto it = ctx->store.begin(); it != ctx->store.end();)
         it = it->first.first == seq_id ? ctx->store.erase(it) : std::next(it);
     *s = SeqState();
@@ -690,6 +721,7 @@ int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n, const void *k
     a.k = static_cast<const uint16_t *>(k_dev);
     a.v = static_cast<const uint16_t *>(v_dev);
     a.pool = static_cast<uint16_t *>(ctx->buf.pool);
+    a.page_clean = ctx->work.page_clean;
     a.table = static_cast<int32_t *>(ctx->buf.block_table);
     a.records = static_cast<kvs_record *>(ctx->buf.records);
     a.pages = reinterpret_cast<const int32_t *>(r.dev);
@@ -712,8 +744,8 @@ int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n, const void *k
         if (b >= nb_old) {
             s->table.push_back(p);
             ctx->refcnt[p] = 1;
+            ctx->refcnt_dirty = true;
         }
-        ctx->mirror_clean[p] = 0;
     }
     s->ntok = static_cast<uint32_t>(p1);
     return KVS_OK;
@@ -746,7 +778,8 @@ int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
     if ((rc = upload_set(ctx, *ds, s)))
         return rc;
     ctx->have_set = true;
-    const int grid = static_cast<int>(std::min<uint32_t>(ds->n_items, ctx->decode_grid));
+    const int grid = static_cast<int>(std::min<uint32_t>((ds->n_items + ctx->wg - 1) / ctx->wg,
+                                                         ctx->decode_grid));
     if (ctx->ev_dec_start)
         CU(cudaEventRecord(ctx->ev_dec_start, s));
     if ((rc = launch_rc(ctx,
@@ -806,132 +839,116 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
     const size_t pb = ctx->sz.page_bytes;
     if (mirror && (!args->host_dst || args->host_dst_bytes < pb * ctx->cfg.pool_blocks))
         return fail(ctx, KVS_EINVAL, "MIRROR needs host_dst of pool_blocks pages");
+    if (args->mode == KVS_SELECT_LOWFRAC && !(args->frac >= 0.0 && args->frac <= 1.0))
+        return fail(ctx, KVS_EINVAL, "frac must be in [0, 1]");
     cudaStream_t s = S(args->stream);
     cudaStream_t side = args->side_stream ? S(args->side_stream) : s;
-    const DSet &ds = *ctx->dset;
-    const uint32_t N = ds.nb_total;
+    const uint32_t N = ctx->dset->nb_total;
+    const Work &w = ctx->work;
     int rc;
 
-    // ---- selection on the device --------------------------------------
-    uint32_t nsel = 0;
+    // ---- device: reference counts, selection, gather plan ---------------
+    if (ctx->refcnt_dirty) {
+        RingSlot r;
+        const size_t bytes = ctx->refcnt.size() * sizeof(uint32_t);
+        if ((rc = ring_acquire(ctx, bytes, &r)))
+            return rc;
+        std::memcpy(r.host, ctx->refcnt.data(), bytes);
+        CU(cudaMemcpyAsync(w.dev_refcnt, r.host, bytes, cudaMemcpyHostToDevice, s));
+        if ((rc = ring_release(ctx, r, s)))
+            return rc;
+        ctx->refcnt_dirty = false;
+    }
     bool run = true;
     if (args->mode == KVS_SELECT_LOWFRAC) {
-        if (!(args->frac >= 0.0 && args->frac <= 1.0))
-            return fail(ctx, KVS_EINVAL, "frac must be in [0, 1]");
-        const double kf = std::floor(args->frac * static_cast<double>(N));
-        const uint32_t k = static_cast<uint32_t>(kf);
+        const uint32_t k = static_cast<uint32_t>(std::floor(args->frac * static_cast<double>(N)));
         if (k == 0)
             run = false;
         else if ((rc = launch_rc(ctx,
-                                 launch_radix_select(ctx->geo, ctx->work,
-                                                     static_cast<const kvs_record *>(ctx->buf.records),
+                                 launch_radix_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
                                                      N, k, s),
                                  "radix select")))
             return rc;
     }
+    uint32_t nsel = 0, npages = 0, ncopy = 0;
+    std::vector<uint32_t> copy_list;
     if (run) {
         if ((rc = launch_rc(ctx,
-                            launch_select(ctx->geo, ctx->work, static_cast<const kvs_record *>(ctx->buf.records),
+                            launch_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
                                           static_cast<const int32_t *>(ctx->buf.block_table), args->mode, N, s),
                             "select")))
             return rc;
-        CU(cudaMemcpyAsync(ctx->pinned_small, ctx->work.sel_count, 4, cudaMemcpyDeviceToHost, s));
+        if ((rc = launch_rc(ctx, launch_plan(w, mirror ? 1u : 0u, s), "plan")))
+            return rc;
+        // one readback: counts and the head of the copy list
+        CU(cudaMemcpyAsync(ctx->pinned_small, w.readback, kReadbackBytes, cudaMemcpyDeviceToHost, s));
         CU(cudaStreamSynchronize(s));
         nsel = ctx->pinned_small[0];
-    }
-    std::vector<kvs_key> ids(nsel);
-    std::vector<int32_t> pages(nsel);
-    std::vector<kvs_record> recs(demote ? nsel : 0);
-    if (nsel) {
-        CU(cudaMemcpyAsync(ids.data(), ctx->work.sel_ids, nsel * sizeof(kvs_key), cudaMemcpyDeviceToHost, s));
-        CU(cudaMemcpyAsync(pages.data(), ctx->work.sel_pages, nsel * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
-        if (demote)
-            CU(cudaMemcpyAsync(recs.data(), ctx->work.sel_recs, nsel * sizeof(kvs_record),
-                               cudaMemcpyDeviceToHost, s));
-        CU(cudaStreamSynchronize(s));
+        npages = ctx->pinned_small[1];
+        ncopy = ctx->pinned_small[2];
+        const uint32_t head = static_cast<uint32_t>(kReadbackBytes / 4 - 4);
+        copy_list.assign(ctx->pinned_small + 4, ctx->pinned_small + 4 + std::min(ncopy, head));
+        if (ncopy > head) {
+            copy_list.resize(ncopy);
+            CU(cudaMemcpy(copy_list.data() + head, w.readback + 4 + head, (ncopy - head) * 4,
+                          cudaMemcpyDeviceToHost));
+        }
     }
     res->n_selected = nsel;
-    if (args->ids_dev && nsel)
-        CU(cudaMemcpyAsync(args->ids_dev, ctx->work.sel_ids,
-                           std::min(nsel, args->ids_capacity) * sizeof(kvs_key), cudaMemcpyDeviceToDevice, s));
+    res->n_pages = npages;
+    if (nsel && args->ids_dev)
+        CU(cudaMemcpyAsync(args->ids_dev, w.sel_ids, std::min(nsel, args->ids_capacity) * sizeof(kvs_key),
+                           cudaMemcpyDeviceToDevice, s));
+    if (nsel && args->slot_dev && !demote && !(!mirror && npages > (args->host_dst ? args->host_dst_bytes / pb : 0)))
+        CU(cudaMemcpyAsync(args->slot_dev, w.plan_slot, std::min(nsel, args->ids_capacity) * sizeof(int32_t),
+                           cudaMemcpyDeviceToDevice, s));
 
-    // ---- gather plan: eligible pages, first occurrence ----------------
-    std::unordered_map<int32_t, uint32_t> listed;     // page -> selected references
-    for (uint32_t i = 0; i < nsel; ++i) {
-        if (pages[i] < 0 || pages[i] >= static_cast<int32_t>(ctx->cfg.pool_blocks))
-            return fail(ctx, KVS_EDEVICE, "selected record has no resident page");
-        listed[pages[i]] += 1;
-    }
-    std::vector<int32_t> slot_of_id(nsel, -1);
-    std::vector<int32_t> plan;                         // pages in gather order
-    std::unordered_map<int32_t, int32_t> plan_pos;
-    for (uint32_t i = 0; i < nsel; ++i) {
-        const int32_t p = pages[i];
-        if (listed[p] != ctx->refcnt[p])
-            continue;                                  // another user keeps it
-        auto it = plan_pos.find(p);
-        if (it == plan_pos.end()) {
-            it = plan_pos.emplace(p, static_cast<int32_t>(plan.size())).first;
-            plan.push_back(p);
-        }
-        slot_of_id[i] = mirror ? p : it->second;
-    }
-    res->n_pages = static_cast<uint32_t>(plan.size());
-
-    // ---- copies ------------------------------------------------------
-    uint32_t nstage = res->n_pages;
+    uint8_t *host = static_cast<uint8_t *>(args->host_dst);
+    uint32_t nstage = npages;
     bool trunc = false;
-    if (!mirror) {
-        const size_t cap = args->host_dst ? args->host_dst_bytes / pb : 0;
-        if (nstage > cap) {
-            nstage = static_cast<uint32_t>(cap);
-            trunc = true;
-            for (auto &x : slot_of_id)
+    if (mirror) {
+        // ---- mirror: copy the stale pages straight from the pool ----------
+        if (ncopy) {
+            CU(cudaEventRecord(ctx->ev_ready[0], s));
+            CU(cudaStreamWaitEvent(side, ctx->ev_ready[0], 0));
+            const uint8_t *pool = static_cast<const uint8_t *>(ctx->buf.pool);
+            for (uint32_t p : copy_list)
+                CU(cudaMemcpyAsync(host + static_cast<size_t>(p) * pb, pool + static_cast<size_t>(p) * pb, pb,
+                                   cudaMemcpyDeviceToHost, side));
+            CU(cudaEventRecord(ctx->ev_side_done, side));
+            ctx->side_pending = true;
+        }
+        res->n_staged = ncopy;
+        res->bytes_to_host = static_cast<uint64_t>(ncopy) * pb;
+        return KVS_OK;
+    }
+
+    // ---- list mode: plan pages through the staging ring, in order --------
+    const size_t cap = args->host_dst ? args->host_dst_bytes / pb : 0;
+    if (nstage > cap) {
+        nstage = static_cast<uint32_t>(cap);
+        trunc = true;
+    }
+    std::vector<int32_t> slots;
+    if ((trunc || demote) && nsel) {
+        slots.resize(nsel);
+        CU(cudaMemcpy(slots.data(), w.plan_slot, nsel * sizeof(int32_t), cudaMemcpyDeviceToHost));
+        if (trunc)
+            for (auto &x : slots)
                 if (x >= static_cast<int32_t>(nstage))
                     x = -1;
+        if (args->slot_dev) {
+            const uint32_t n = std::min(nsel, args->ids_capacity);
+            RingSlot r;
+            if ((rc = ring_acquire(ctx, n * sizeof(int32_t), &r)))
+                return rc;
+            std::memcpy(r.host, slots.data(), n * sizeof(int32_t));
+            CU(cudaMemcpyAsync(args->slot_dev, r.host, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+            if ((rc = ring_release(ctx, r, s)))
+                return rc;
         }
     }
-    if (args->slot_dev && nsel) {
-        const uint32_t n = std::min(nsel, args->ids_capacity);
-        RingSlot r;
-        if ((rc = ring_acquire(ctx, n * sizeof(int32_t), &r)))
-            return rc;
-        std::memcpy(r.host, slot_of_id.data(), n * sizeof(int32_t));
-        CU(cudaMemcpyAsync(args->slot_dev, r.host, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
-        if ((rc = ring_release(ctx, r, s)))
-            return rc;
-    }
-    uint8_t *host = static_cast<uint8_t *>(args->host_dst);
-    if (mirror) {
-        CU(cudaEventRecord(ctx->ev_ready[0], s));
-        CU(cudaStreamWaitEvent(side, ctx->ev_ready[0], 0));
-        // owner sequence of each page decides whether the page is full
-        std::unordered_map<int32_t, bool> full;
-        for (uint32_t i = 0; i < nsel; ++i) {
-            if (full.count(pages[i]))
-                continue;
-            SeqState *sq = find_seq(ctx, ids[i].seq_id);
-            full[pages[i]] = sq && static_cast<uint64_t>(sq->ntok) >= (ids[i].block_idx + 1) * kBlockTokens;
-        }
-        for (int32_t p : plan) {
-            if (ctx->mirror_clean[p])
-                continue;
-            CU(cudaMemcpyAsync(host + static_cast<size_t>(p) * pb,
-                               static_cast<uint8_t *>(ctx->buf.pool) + static_cast<size_t>(p) * pb, pb,
-                               cudaMemcpyDeviceToHost, side));
-            ctx->mirror_clean[p] = full[p] ? 1 : 0;
-            res->n_staged += 1;
-            res->bytes_to_host += pb;
-        }
-        CU(cudaEventRecord(ctx->ev_side_done, side));
-        ctx->side_pending = true;
-    } else if (nstage) {
-        RingSlot r;
-        if ((rc = ring_acquire(ctx, nstage * sizeof(int32_t), &r)))
-            return rc;
-        std::memcpy(r.host, plan.data(), nstage * sizeof(int32_t));
-        if ((rc = ring_push(ctx, r, nstage * sizeof(int32_t), s)))
-            return rc;
+    if (nstage) {
         const uint32_t C = ctx->cfg.staging_pages;
         const uint32_t H = C >= 2 ? C / 2 : 1;
         const int nbuf = C >= 2 ? 2 : 1;
@@ -946,7 +963,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             uint8_t *dst = staging + static_cast<size_t>(hb) * H * pb;
             if ((rc = launch_rc(ctx,
                                 launch_gather(ctx->geo, static_cast<const uint16_t *>(ctx->buf.pool),
-                                              reinterpret_cast<const int32_t *>(r.dev) + c0, cnt, dst, s),
+                                              w.plan_pages + c0, cnt, dst, s),
                                 "gather")))
                 return rc;
             CU(cudaEventRecord(ctx->ev_ready[hb], s));
@@ -955,30 +972,34 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
                                cudaMemcpyDeviceToHost, side));
             CU(cudaEventRecord(ctx->ev_free[hb], side));
         }
-        if ((rc = ring_release(ctx, r, s)))
-            return rc;
         CU(cudaEventRecord(ctx->ev_side_done, side));
         ctx->side_pending = true;
         res->n_staged = nstage;
         res->bytes_to_host = static_cast<uint64_t>(nstage) * pb;
     }
 
-    // ---- demotion: keep records by key, clear table entries, free pages --
+    // ---- demotion: keep records by key, clear table entries, free pages ---
     if (demote && nstage) {
-        std::vector<Patch> patches;
+        std::vector<kvs_key> ids(nsel);
+        std::vector<int32_t> pages(nsel);
+        std::vector<kvs_record> recs(nsel);
+        CU(cudaMemcpy(ids.data(), w.sel_ids, nsel * sizeof(kvs_key), cudaMemcpyDeviceToHost));
+        CU(cudaMemcpy(pages.data(), w.sel_pages, nsel * sizeof(int32_t), cudaMemcpyDeviceToHost));
+        CU(cudaMemcpy(recs.data(), w.sel_recs, nsel * sizeof(kvs_record), cudaMemcpyDeviceToHost));
         for (uint32_t i = 0; i < nsel; ++i) {
-            if (slot_of_id[i] < 0)
+            if (slots[i] < 0)
                 continue;
             const std::pair<uint64_t, uint64_t> key(ids[i].seq_id, ids[i].block_idx);
             if (ctx->store.count(key))
                 return fail(ctx, KVS_EEXIST, "key (%llu, %llu) already demoted",
                             (unsigned long long)key.first, (unsigned long long)key.second);
         }
+        std::vector<Patch> patches;
         for (uint32_t i = 0; i < nsel; ++i) {
-            if (slot_of_id[i] < 0)
+            if (slots[i] < 0)
                 continue;
             const std::pair<uint64_t, uint64_t> key(ids[i].seq_id, ids[i].block_idx);
-            ctx->store[key] = Demoted{recs[i], static_cast<uint64_t>(slot_of_id[i]) * pb};
+            ctx->store[key] = Demoted{recs[i], static_cast<uint64_t>(slots[i]) * pb};
             uint32_t slot;
             SeqState *sq = find_seq(ctx, ids[i].seq_id, &slot);
             const int32_t p = pages[i];
@@ -987,22 +1008,21 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             q.slot = slot;
             q.block = static_cast<uint32_t>(ids[i].block_idx);
             q.page = -1;
-            q.has_record = 1;
+            q.what = kPatchRecord;
             q.rec = recs[i];
             q.rec.flags |= 1;
             patches.push_back(q);
-            if (--ctx->refcnt[p] == 0) {
+            if (--ctx->refcnt[p] == 0)
                 ctx->free_pages.push_back(p);
-                ctx->mirror_clean[p] = 0;
-            }
             res->n_demoted += 1;
         }
+        ctx->refcnt_dirty = true;
         if ((rc = apply_patches(ctx, patches, s)))
             return rc;
         ctx->have_set = false;   // the set now has holes
     }
     if (trunc)
-        return fail(ctx, KVS_ETRUNC, "host_dst holds %u of %u pages", nstage, res->n_pages);
+        return fail(ctx, KVS_ETRUNC, "host_dst holds %u of %u pages", nstage, npages);
     return KVS_OK;
 }
 
@@ -1069,7 +1089,7 @@ int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n, const void *hos
         q.slot = slot;
         q.block = static_cast<uint32_t>(k.second);
         q.page = p;
-        q.has_record = 1;
+        q.what = kPatchRecord | kPatchPageWritten;
         q.rec = dm.rec;
         patches.push_back(q);
     }
@@ -1080,9 +1100,9 @@ int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n, const void *hos
         SeqState *sq = find_seq(ctx, ks[i].first, &slot);
         sq->table[ks[i].second] = taken[i];
         ctx->refcnt[taken[i]] = 1;
-        ctx->mirror_clean[taken[i]] = 0;
         ctx->store.erase(ks[i]);
     }
+    ctx->refcnt_dirty = true;
     return KVS_OK;
 }
 

@@ -13,9 +13,10 @@
 namespace kvs {
 
 constexpr int kBlockTokens = 16;
-constexpr int kChunkBlocks = 64;      // blocks per decode work item (split-K chunk)
+constexpr uint32_t kMaxChunk = 128;   // blocks per decode work item (split-K chunk): at most
+constexpr uint32_t kMinChunk = 16;    //   ... and at least
 constexpr int kMaxGroup = 8;          // query heads per KV head handled by one warp
-constexpr int kStages = 4;            // TMA ring depth per warp
+constexpr int kStages = 6;            // TMA ring depth per warp (6 x 8 KiB)
 constexpr int kMaxCallSeqs = KVS_MAX_CALL_SEQS;
 
 // Device error word bits (set by kernels, read by kvs_check_device).
@@ -33,7 +34,7 @@ struct DSeq {
     uint32_t blk_off;   // prefix of nb over call order (per-block LSE index)
     uint32_t item_off;  // prefix of CTA work items over call order
     uint32_t part_off;  // prefix of per-warp partials over call order
-    uint32_t nchunk;    // ceil(nb / kChunkBlocks)
+    uint32_t nchunk;    // ceil(nb / chunk)
     uint32_t pad;
     uint64_t seq_id;
 };
@@ -46,7 +47,7 @@ struct DSet {
     uint32_t n_parts;
     uint64_t t;                       // step counter after the decode
     uint32_t wg;                      // KV heads (warps) per work item
-    uint32_t pad;
+    uint32_t chunk;                   // blocks per work item in this call
     DSeq seq[kMaxCallSeqs];
     uint32_t sorted[kMaxCallSeqs];    // call indices, ascending seq_id
     uint32_t srt_off[kMaxCallSeqs + 1];  // record-order prefix of nb over `sorted`
@@ -69,18 +70,28 @@ struct Work {             // carved out of the caller's workspace buffer
     float2 *part_ml;      // [n_parts][8] (running max in log2 units, sum)
     float *part_o;        // [n_parts][8][d] unnormalised output
     float *lse_blk;       // [L*Hq][nb_total] per-block log2-sum-exp
-    float *lse_head;      // [nseq][L*Hq] log2-sum-exp per head
+    float *stream_mass;   // [L*Hkv][nb_total] block mass of each (layer, KV head) stream
     uint32_t *tile_cnt;   // [tiles] selection counts
     kvs_key *sel_ids;     // [nb_max] selected keys
     int32_t *sel_pages;   // [nb_max] page of each selected key
     uint32_t *sel_recidx; // [nb_max] record-order index of each selected key
     kvs_record *sel_recs; // [nb_max] record of each selected key
+    uint8_t *sel_full;    // [nb_max] 1 if the selected key's block holds 16 tokens
+    uint32_t *dev_refcnt; // [pool_blocks] references per page (host-maintained mirror)
+    uint32_t *page_cnt;   // [pool_blocks] selected references (zero between calls)
+    uint32_t *page_first; // [pool_blocks] first selected position (~0 between calls)
+    int32_t *page_pos;    // [pool_blocks] position of a page in the gather plan
+    uint8_t *page_clean;  // [pool_blocks] 1: the host mirror holds the page's bytes
+    int32_t *plan_pages;  // [nb_max] eligible pages, first-occurrence order
+    int32_t *plan_slot;   // [nb_max] per selected key: host page index, -1 if none
+    uint32_t *readback;   // [4 + nb_max]: n_selected, n_pages, n_copy, -, copy list
     uint8_t *ring;        // device side of the upload ring
 };
 
 struct Layout {           // byte offsets inside the workspace
     size_t err, counter, sel_count, sel_thr, dset, part_ml, part_o, lse_blk,
-        lse_head, tile_cnt, sel_ids, sel_pages, sel_recidx, sel_recs, ring, total;
+        stream_mass, tile_cnt, sel_ids, sel_pages, sel_recidx, sel_recs, sel_full, dev_refcnt,
+        page_cnt, page_first, page_pos, page_clean, plan_pages, plan_slot, readback, ring, total;
     size_t ring_slot_bytes;
     uint32_t ring_slots;
     uint32_t nb_max, parts_max, tiles_max;
@@ -94,14 +105,19 @@ struct Patch {
     uint32_t slot;
     uint32_t block;
     int32_t page;         // new table entry (-1 = none)
-    uint32_t has_record;  // 1: write `rec` into the record slot
+    uint32_t what;        // kPatchRecord | kPatchPageWritten
     kvs_record rec;
+};
+enum : uint32_t {
+    kPatchRecord = 1u,      // write `rec` into the record slot
+    kPatchPageWritten = 2u, // the page's bytes were rewritten: host mirror is stale
 };
 
 // Append of n tokens to one sequence.
 struct AppendArgs {
     const uint16_t *k, *v;     // [n][L][Hkv][d]
     uint16_t *pool;
+    uint8_t *page_clean;       // cleared for every page written
     int32_t *table;
     kvs_record *records;
     const int32_t *pages;      // page of each touched block, from block first_blk
@@ -128,14 +144,37 @@ cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *r
 cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec,
                           const int32_t *table, int mode, uint32_t nb_total,
                           cudaStream_t s);
+cudaError_t launch_plan(const Work &w, uint32_t mirror, cudaStream_t s);
 cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pages,
                           uint32_t npages, uint8_t *staging, cudaStream_t s);
-cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec,
+cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, uint8_t *page_clean,
                          const Patch *p, uint32_t n, cudaStream_t s);
 cudaError_t launch_copy_mass(const Geo &g, const Work &w, const float *src, float *mass,
                              uint32_t nseq, cudaStream_t s);
 
 int decode_blocks_per_sm(const Geo &g, uint32_t wg);
+
+// Blocks per decode work item (one KV-head stream chunk) for one call: the
+// largest of 128, 64, 32, 16 that still gives each of the `workers` warps of
+// the persistent grid at least 8 items (a short tail without many partials),
+// as long as the chunk partials fit in parts_cap; if no size gives that many
+// items, the smallest that fits.  0 if not even 128 fits.
+inline uint32_t pick_chunk(const uint32_t *nb, uint32_t n, uint32_t L, uint32_t Hkv,
+                           uint32_t workers, uint64_t parts_cap)
+{
+    uint32_t best = 0;
+    for (uint32_t c = kMaxChunk; c >= kMinChunk; c >>= 1) {
+        uint64_t parts = 0;
+        for (uint32_t i = 0; i < n; ++i)
+            parts += static_cast<uint64_t>(L) * Hkv * ((nb[i] + c - 1) / c);
+        if (parts > parts_cap)
+            break;
+        best = c;
+        if (parts >= 8ull * workers)        // one item per partial
+            break;
+    }
+    return best;
+}
 size_t decode_smem_bytes(const Geo &g, uint32_t wg);
 
 }  // namespace kvs

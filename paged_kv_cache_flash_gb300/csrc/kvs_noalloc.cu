@@ -83,7 +83,8 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
     g.mb = nb;
     g.page_bytes = static_cast<uint64_t>(2) * g.L * g.Hkv * kBlockTokens * g.d * 2;
     const uint32_t wg = g.Hkv % 4 == 0 ? 4 : (g.Hkv % 2 == 0 ? 2 : 1);
-    const uint32_t nchunk = (nb + kChunkBlocks - 1) / kChunkBlocks;
+    const uint32_t chunk = 64;
+    const uint32_t nchunk = (nb + chunk - 1) / chunk;
     const size_t LH = static_cast<size_t>(g.L) * g.Hq;
     const size_t parts = static_cast<size_t>(g.L) * g.Hkv * nchunk;
 
@@ -94,7 +95,7 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
     const size_t off_ml = o;    o = up256(o + parts * kMaxGroup * sizeof(float2));
     const size_t off_po = o;    o = up256(o + parts * kMaxGroup * g.d * sizeof(float));
     const size_t off_lb = o;    o = up256(o + LH * nb * sizeof(float));
-    const size_t off_lh = o;    o = up256(o + LH * sizeof(float));
+    const size_t off_sm = o;    o = up256(o + static_cast<size_t>(g.L) * g.Hkv * nb * sizeof(float));
     if (o > kScratchBytes) {
         std::snprintf(buf, sizeof buf,
                       "this call needs %zu bytes of scratch; the built-in maximum is %zu bytes "
@@ -141,16 +142,17 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
     w.part_ml = reinterpret_cast<float2 *>(base + off_ml);
     w.part_o = reinterpret_cast<float *>(base + off_po);
     w.lse_blk = reinterpret_cast<float *>(base + off_lb);
-    w.lse_head = reinterpret_cast<float *>(base + off_lh);
+    w.stream_mass = reinterpret_cast<float *>(base + off_sm);
 
     // the one-sequence decode set
     DSet ds;
     std::memset(&ds, 0, sizeof ds);
     ds.nseq = 1;
     ds.nb_total = nb;
-    ds.n_items = g.L * (g.Hkv / wg) * nchunk;
+    ds.n_items = g.L * g.Hkv * nchunk;
     ds.n_parts = static_cast<uint32_t>(parts);
     ds.wg = wg;
+    ds.chunk = chunk;
     ds.seq[0].ntok = n_tokens;
     ds.seq[0].nb = nb;
     ds.seq[0].nchunk = nchunk;
@@ -186,7 +188,8 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
     } while (0)
     NA_CHECK(cudaMemsetAsync(base + off_hdr, 0, 256, s));
     NA_CHECK(cudaMemcpyAsync(w.dset, &ds, sizeof ds, cudaMemcpyHostToDevice, s));
-    const int grid = static_cast<int>(std::min<uint32_t>(ds.n_items, static_cast<uint32_t>(grid_per_sm)));
+    const int grid = static_cast<int>(std::min<uint32_t>((ds.n_items + wg - 1) / wg,
+                                                         static_cast<uint32_t>(grid_per_sm)));
     NA_CHECK(launch_decode(g, tmap, w, static_cast<const uint16_t *>(q), block_table, ds.n_items, wg,
                            grid, s));
     NA_CHECK(launch_combine(g, w, out, 1, s));
