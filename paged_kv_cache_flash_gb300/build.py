@@ -17,7 +17,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 OUT_DIR = PKG / "_build"
 LIB = OUT_DIR / "libkvs.so"
-SOURCES = ["kvs_decode.cu", "kvs_blocks.cu", "kvs_host.cpp", "kvs_noalloc.cu"]
+SOURCES = ["kvs_decode.cu", "kvs_combine.cu", "kvs_blocks.cu", "kvs_host.cpp", "kvs_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -40,8 +40,8 @@ def _stale() -> bool:
     if not LIB.exists():
         return True
     t = LIB.stat().st_mtime
-    deps = [CSRC / s for s in SOURCES] + [CSRC / "kvs_internal.h", ROOT / "include" / "kvs.h",
-                                         Path(__file__)]
+    deps = [CSRC / s for s in SOURCES] + [CSRC / "kvs_internal.h", CSRC / "kvs_ptx.h",
+                                         ROOT / "include" / "kvs.h", Path(__file__)]
     return any(p.stat().st_mtime > t for p in deps)
 
 

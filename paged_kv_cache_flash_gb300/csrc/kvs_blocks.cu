@@ -370,29 +370,43 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Work w, uint32_t mirro
         atomicMin(&w.page_first[p], i);
     }
     __syncthreads();
+    // leaders in list order: 4 consecutive entries per thread per tile
     uint32_t npages = 0, ncopy = 0;
-    for (uint32_t t0 = 0; t0 < n; t0 += blockDim.x) {
-        const uint32_t i = t0 + threadIdx.x;
-        uint32_t lead = 0, dirty = 0;
-        int32_t p = 0;
-        if (i < n) {
-            p = w.sel_pages[i];
-            lead = (w.page_cnt[p] == w.dev_refcnt[p] && w.page_first[p] == i) ? 1u : 0u;
-            dirty = (lead && mirror && !w.page_clean[p]) ? 1u : 0u;
+    for (uint32_t t0 = 0; t0 < n; t0 += 4 * blockDim.x) {
+        const uint32_t i0 = t0 + 4 * threadIdx.x;
+        int32_t p[4];
+        uint32_t lead[4], dirty[4], nl = 0, nd = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t i = i0 + q;
+            lead[q] = dirty[q] = 0;
+            p[q] = 0;
+            if (i < n) {
+                p[q] = w.sel_pages[i];
+                lead[q] = (w.page_cnt[p[q]] == w.dev_refcnt[p[q]] && w.page_first[p[q]] == i) ? 1u : 0u;
+                dirty[q] = (lead[q] && mirror && !w.page_clean[p[q]]) ? 1u : 0u;
+            }
+            nl += lead[q];
+            nd += dirty[q];
         }
         uint32_t tot;
-        const uint32_t pos = npages + block_scan_1024(lead, wsum, &tot);
-        if (lead) {
-            w.plan_pages[pos] = p;
-            w.page_pos[p] = static_cast<int32_t>(pos);
-        }
+        uint32_t pos = npages + block_scan_1024(nl, wsum, &tot);
         npages += tot;
-        const uint32_t cpos = ncopy + block_scan_1024(dirty, wsum, &tot);
-        if (dirty) {
-            w.readback[4 + cpos] = static_cast<uint32_t>(p);
-            w.page_clean[p] = w.sel_full[i];
-        }
+        uint32_t cpos = ncopy + block_scan_1024(nd, wsum, &tot);
         ncopy += tot;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (lead[q]) {
+                w.plan_pages[pos] = p[q];
+                w.page_pos[p[q]] = static_cast<int32_t>(pos);
+                ++pos;
+            }
+            if (dirty[q]) {
+                w.readback[4 + cpos] = static_cast<uint32_t>(p[q]);
+                w.page_clean[p[q]] = w.sel_full[i0 + q];
+                ++cpos;
+            }
+        }
     }
     __syncthreads();
     for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {

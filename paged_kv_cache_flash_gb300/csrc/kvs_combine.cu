@@ -1,0 +1,141 @@
+// Split-K combine and block mass (sm_103a).
+//
+// Sources: "GQA per-head attention as scoring streams" (every (layer, KV head)
+// stream contributes to one mass per (sequence, 16-token block)); "KV-Cache
+// Offloading for LLM Inference -- Visual Reference" s.4 (the decode output
+// over every cached token).
+//
+//   combine_kernel -- per (sequence, layer, KV head) and range of blocks: each
+//                     head's log2-sum-exp LSE_h from the chunk partials; the
+//                     first range's CTA also merges the output; every CTA
+//                     turns the per-block log2-sum-exps of its range into the
+//                     stream's block masses  sum_h 2^(lse_blk(h, b) - LSE_h).
+//   mass_kernel    -- M(b) = 1/(L*Hq) * sum over the L*Hkv streams, in a fixed
+//                     order (deterministic).
+#include "kvs_internal.h"
+#include "kvs_ptx.h"
+
+namespace kvs {
+namespace {
+
+using namespace ptx;
+
+constexpr uint32_t kMassRange = 1024;   // blocks per combine CTA (stream-mass part)
+
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w, float *out)
+{
+    __shared__ float lse_sh[kMaxGroup];
+    const DSet *ds = w.dset;
+    const uint32_t lane = threadIdx.x & 31, h = threadIdx.x >> 5;
+    const uint32_t ci = blockIdx.x / (g.L * g.Hkv);
+    const uint32_t rest = blockIdx.x % (g.L * g.Hkv);
+    const uint32_t l = rest / g.Hkv, kvh = rest % g.Hkv;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        *w.counter = 0;            // ready for the next decode launch
+    const DSeq sq = ds->seq[ci];
+    const uint32_t r0 = blockIdx.y * kMassRange;
+    if (r0 >= sq.nb)
+        return;                    // uniform over the CTA
+    const uint32_t pb = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk;
+    if (h < g.G) {
+        float mmax = -INFINITY;
+        for (uint32_t c = lane; c < sq.nchunk; c += 32)
+            mmax = fmaxf(mmax, w.part_ml[(pb + c) * kMaxGroup + h].x);
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1)
+            mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, x));
+        float lsum = 0.f;
+        for (uint32_t c = lane; c < sq.nchunk; c += 32) {
+            const float2 ml = w.part_ml[(pb + c) * kMaxGroup + h];
+            lsum += ml.y * fast_exp2(ml.x - mmax);
+        }
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1)
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, x);
+        if (blockIdx.y == 0) {
+            constexpr int E = D / 32;
+            float acc[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                acc[e] = 0.f;
+#pragma unroll 4
+            for (uint32_t c = 0; c < sq.nchunk; ++c) {
+                const float f = fast_exp2(w.part_ml[(pb + c) * kMaxGroup + h].x - mmax);
+                const float *po = w.part_o + (static_cast<size_t>(pb + c) * kMaxGroup + h) * D + lane * E;
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    acc[e] += po[e] * f;
+            }
+            const float inv = 1.f / lsum;
+            const uint32_t hq = kvh * g.G + h;
+            float *dst = out + ((static_cast<size_t>(ci) * g.L + l) * g.Hq + hq) * D + lane * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                dst[e] = acc[e] * inv;
+        }
+        if (lane == 0)
+            lse_sh[h] = mmax + fast_log2(lsum);
+    }
+    __syncthreads();
+    const uint32_t nbt = ds->nb_total;
+    const float *lb = w.lse_blk + (static_cast<size_t>(l) * g.Hq + kvh * g.G) * nbt + sq.blk_off;
+    float *sm = w.stream_mass + (static_cast<size_t>(l) * g.Hkv + kvh) * nbt + sq.blk_off;
+    const uint32_t r1 = min(sq.nb, r0 + kMassRange);
+    for (uint32_t b = r0 + threadIdx.x; b < r1; b += blockDim.x) {
+        float acc = 0.f;
+        for (uint32_t j = 0; j < g.G; ++j)
+            acc += fast_exp2(lb[static_cast<size_t>(j) * nbt + b] - lse_sh[j]);
+        sm[b] = acc;
+    }
+}
+
+// M(b) = 1/(L*Hq) * sum over the L*Hkv streams of stream_mass(b): 32
+// consecutive blocks per CTA x 8 interleaved partial sums, added in a fixed
+// order (deterministic).
+__global__ void __launch_bounds__(256) mass_kernel(const Geo g, const Work w, float *mass,
+                                                   uint32_t nb_total)
+{
+    __shared__ float part[8][33];
+    const DSet *ds = w.dset;
+    const uint32_t i = threadIdx.x & 31, j = threadIdx.x >> 5;
+    const uint32_t r = blockIdx.x * 32 + i;
+    const uint32_t LS = g.L * g.Hkv;
+    float acc = 0.f;
+    if (r < nb_total)
+        for (uint32_t s = j; s < LS; s += 8)
+            acc += w.stream_mass[static_cast<size_t>(s) * nb_total + r];
+    part[j][i] = acc;
+    __syncthreads();
+    if (j == 0 && r < nb_total) {
+        float t = part[0][i];
+#pragma unroll
+        for (int q = 1; q < 8; ++q)
+            t += part[q][i];
+        const uint32_t ci = find_seq(&ds->seq[0].blk_off, sizeof(DSeq) / 4, ds->nseq, r);
+        const DSeq sq = ds->seq[ci];
+        mass[static_cast<size_t>(sq.slot) * g.mb + (r - sq.blk_off)] =
+            t / static_cast<float>(g.L * g.Hq);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq, uint32_t max_nb,
+                           cudaStream_t s)
+{
+    const dim3 grid(nseq * g.L * g.Hkv, (max_nb + kMassRange - 1) / kMassRange);
+    if (g.d == 128)
+        combine_kernel<128><<<grid, 32 * kMaxGroup, 0, s>>>(g, w, out);
+    else
+        combine_kernel<64><<<grid, 32 * kMaxGroup, 0, s>>>(g, w, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total, cudaStream_t s)
+{
+    mass_kernel<<<(nb_total + 31) / 32, 256, 0, s>>>(g, w, mass, nb_total);
+    return cudaGetLastError();
+}
+
+}  // namespace kvs

@@ -24,132 +24,12 @@
 #include <cuda_bf16.h>
 
 #include "kvs_internal.h"
+#include "kvs_ptx.h"
 
 namespace kvs {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ float fast_exp2(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float fast_log2(float x)
-{
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(phase)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: gives up after `limit` polls and reports it.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, uint32_t *err)
-{
-    for (uint32_t i = 0; i < (1u << 22); ++i)
-        if (mbar_try_wait(bar, phase))
-            return true;
-    atomicOr(err, kErrTmaTimeout);
-    return false;
-}
-
-__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3, int c4)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-        "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &a0, uint32_t &a1, uint32_t &a2,
-                                        uint32_t &a3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                 : "r"(addr)
-                 : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &a0, uint32_t &a1, uint32_t &a2,
-                                          uint32_t &a3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                 : "r"(addr)
-                 : "memory");
-}
-
-// D (16x8 f32) += A (16x16 bf16, row) * B (16x8 bf16, col)
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
-{
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
-{
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-__device__ __forceinline__ uint32_t find_seq(const uint32_t *off_base, size_t stride_words,
-                                             uint32_t nseq, uint32_t x)
-{
-    // largest i with off(i) <= x; off() read with a stride (fields of DSeq)
-    uint32_t lo = 0, hi = nseq;
-    while (hi - lo > 1) {
-        uint32_t mid = (lo + hi) >> 1;
-        if (off_base[mid * stride_words] <= x)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    return lo;
-}
+using namespace ptx;
 
 struct DecodeArgs {
     Geo g;
@@ -481,91 +361,6 @@ __global__ void __launch_bounds__(256, 1)
     }
 }
 
-// One CTA per (sequence, layer, KV head).  Warp h merges query head h's
-// chunks into its log2-sum-exp and output; then the CTA turns the per-block
-// log2-sum-exps of its G heads into the stream's block masses
-//   stream_mass(b) = sum_h 2^(lse_blk(h, b) - LSE_h).
-template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w, float *out)
-{
-    __shared__ float lse_sh[kMaxGroup];
-    const DSet *ds = w.dset;
-    const uint32_t lane = threadIdx.x & 31, h = threadIdx.x >> 5;
-    const uint32_t ci = blockIdx.x / (g.L * g.Hkv);
-    const uint32_t rest = blockIdx.x % (g.L * g.Hkv);
-    const uint32_t l = rest / g.Hkv, kvh = rest % g.Hkv;
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-        *w.counter = 0;            // ready for the next decode launch
-    const DSeq sq = ds->seq[ci];
-    if (h < g.G) {
-        const uint32_t pb = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk;
-        float mmax = -INFINITY;
-        for (uint32_t c = 0; c < sq.nchunk; ++c)
-            mmax = fmaxf(mmax, w.part_ml[(pb + c) * kMaxGroup + h].x);
-        constexpr int E = D / 32;
-        float acc[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-            acc[e] = 0.f;
-        float lsum = 0.f;
-        for (uint32_t c = 0; c < sq.nchunk; ++c) {
-            const float2 ml = w.part_ml[(pb + c) * kMaxGroup + h];
-            const float f = fast_exp2(ml.x - mmax);
-            lsum += ml.y * f;
-            const float *po = w.part_o + (static_cast<size_t>(pb + c) * kMaxGroup + h) * D + lane * E;
-#pragma unroll
-            for (int e = 0; e < E; ++e)
-                acc[e] += po[e] * f;
-        }
-        const float inv = 1.f / lsum;
-        const uint32_t hq = kvh * g.G + h;
-        float *dst = out + ((static_cast<size_t>(ci) * g.L + l) * g.Hq + hq) * D + lane * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-            dst[e] = acc[e] * inv;
-        if (lane == 0)
-            lse_sh[h] = mmax + fast_log2(lsum);
-    }
-    __syncthreads();
-    const uint32_t nbt = ds->nb_total;
-    const float *lb = w.lse_blk + (static_cast<size_t>(l) * g.Hq + kvh * g.G) * nbt + sq.blk_off;
-    float *sm = w.stream_mass + (static_cast<size_t>(l) * g.Hkv + kvh) * nbt + sq.blk_off;
-    for (uint32_t b = threadIdx.x; b < sq.nb; b += blockDim.x) {
-        float acc = 0.f;
-        for (uint32_t j = 0; j < g.G; ++j)
-            acc += fast_exp2(lb[static_cast<size_t>(j) * nbt + b] - lse_sh[j]);
-        sm[b] = acc;
-    }
-}
-
-// M(b) = 1/(L*Hq) * sum over the L*Hkv streams of stream_mass(b): 32
-// consecutive blocks per CTA x 8 interleaved partial sums, added in a fixed
-// order (deterministic).
-__global__ void __launch_bounds__(256) mass_kernel(const Geo g, const Work w, float *mass,
-                                                   uint32_t nb_total)
-{
-    __shared__ float part[8][33];
-    const DSet *ds = w.dset;
-    const uint32_t i = threadIdx.x & 31, j = threadIdx.x >> 5;
-    const uint32_t r = blockIdx.x * 32 + i;
-    const uint32_t LS = g.L * g.Hkv;
-    float acc = 0.f;
-    if (r < nb_total)
-        for (uint32_t s = j; s < LS; s += 8)
-            acc += w.stream_mass[static_cast<size_t>(s) * nb_total + r];
-    part[j][i] = acc;
-    __syncthreads();
-    if (j == 0 && r < nb_total) {
-        float t = part[0][i];
-#pragma unroll
-        for (int q = 1; q < 8; ++q)
-            t += part[q][i];
-        const uint32_t ci = find_seq(&ds->seq[0].blk_off, sizeof(DSeq) / 4, ds->nseq, r);
-        const DSeq sq = ds->seq[ci];
-        mass[static_cast<size_t>(sq.slot) * g.mb + (r - sq.blk_off)] =
-            t / static_cast<float>(g.L * g.Hq);
-    }
-}
 }  // namespace
 
 size_t decode_smem_bytes(const Geo &g, uint32_t wg)
@@ -602,22 +397,6 @@ cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w, 
         decode_kernel<128><<<grid, 32 * wg, smem, s>>>(tmap, a);
     else
         decode_kernel<64><<<grid, 32 * wg, smem, s>>>(tmap, a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq, cudaStream_t s)
-{
-    const dim3 grid(nseq * g.L * g.Hkv);
-    if (g.d == 128)
-        combine_kernel<128><<<grid, 32 * kMaxGroup, 0, s>>>(g, w, out);
-    else
-        combine_kernel<64><<<grid, 32 * kMaxGroup, 0, s>>>(g, w, out);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total, cudaStream_t s)
-{
-    mass_kernel<<<(nb_total + 31) / 32, 256, 0, s>>>(g, w, mass, nb_total);
     return cudaGetLastError();
 }
 

@@ -790,7 +790,10 @@ int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
         return rc;
     if (ctx->ev_dec_stop)
         CU(cudaEventRecord(ctx->ev_dec_stop, s));
-    if ((rc = launch_rc(ctx, launch_combine(ctx->geo, ctx->work, out_dev, ds->nseq, s), "combine")))
+    uint32_t max_nb = 0;
+    for (uint32_t i = 0; i < ds->nseq; ++i)
+        max_nb = std::max(max_nb, ds->seq[i].nb);
+    if ((rc = launch_rc(ctx, launch_combine(ctx->geo, ctx->work, out_dev, ds->nseq, max_nb, s), "combine")))
         return rc;
     return launch_rc(ctx, launch_mass(ctx->geo, ctx->work, static_cast<float *>(ctx->buf.mass),
                                       ds->nb_total, s),

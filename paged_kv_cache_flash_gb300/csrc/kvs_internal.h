@@ -133,7 +133,7 @@ cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w,
                           const uint16_t *q, const int32_t *table,
                           uint32_t n_items, uint32_t wg, int grid, cudaStream_t s);
 cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq,
-                           cudaStream_t s);
+                           uint32_t max_nb, cudaStream_t s);
 cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total,
                         cudaStream_t s);
 cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const float *mass,
