@@ -28,31 +28,46 @@ def seq_ids_for(wl):
 @dataclass
 class OracleSeq:
     seq_id: int
-    K: torch.Tensor               # host bf16 [n][L][Hkv][d]
-    V: torch.Tensor
+    Kbuf: torch.Tensor            # host bf16 [capacity][L][Hkv][d]
+    Vbuf: torch.Tensor
+    n: int                        # tokens so far
     rec: np.ndarray               # oracle records, block order
     ambiguous: np.ndarray         # touch decision within TOUCH_MARGIN at some step
     page_of: list = field(default_factory=list)   # page identity per block
 
+    @property
+    def K(self):
+        return self.Kbuf[: self.n]
+
+    @property
+    def V(self):
+        return self.Vbuf[: self.n]
+
 
 class Run:
+    """oracle_seqs: indices of the sequences the oracle follows (None = all);
+    each sequence's attention, mass and records depend on it alone."""
+
     def __init__(self, wl, alpha, *, staging_pages=8, chunk=4096, oracle_on=True,
-                 pool_pages=None, device="cuda"):
+                 oracle_seqs=None, pool_pages=None, extra_steps=0, device="cuda"):
         self.wl, self.alpha = wl, alpha
         self.dev = device
         self.ids = seq_ids_for(wl)
-        self.mb = wl.max_blocks_per_seq()
+        self.mb = wl.max_blocks_per_seq() + (extra_steps + 15) // 16
         cfg = K.make_config(wl.L, wl.Hq, wl.Hkv, wl.d, pool_pages or wl.pool_pages, max_seqs=wl.nseq,
                             max_blocks_per_seq=self.mb, alpha=alpha,
                             recency_window=wl.recency_window, weights=wl.weights, cuts=wl.cuts,
                             pool_seed=wl.seed, staging_pages=staging_pages)
         self.ctx = K.Context(cfg)
         self.oracle_on = oracle_on
+        track = set(range(wl.nseq)) if oracle_seqs is None else set(oracle_seqs)
+        self.tracked = [sid for s, sid in enumerate(self.ids) if oracle_on and s in track]
         self.t = 0
         self.ntok = list(wl.prefill_lens)
         self.orc = {}
         B = wl.block_tokens
         pre_blocks = wl.shared_prefix_tokens // B
+        cap_steps = wl.steps + extra_steps + 1
         for s, sid in enumerate(self.ids):
             n = wl.prefill_lens[s]
             if s > 0 and pre_blocks:
@@ -61,16 +76,27 @@ class Run:
             else:
                 self.ctx.seq_add(sid)
                 start = 0
-            for a in range(start, n, chunk):
-                b = min(n, a + chunk)
-                Kt, Vt = W.kv_tokens(wl, s, a, b, device)
-                self.ctx.append_tokens(sid, Kt, Vt)
-            if oracle_on:
-                Kh, Vh = W.kv_tokens(wl, s, 0, n, device)
+            o = None
+            if sid in self.tracked:
+                shape = (n + cap_steps, wl.L, wl.Hkv, wl.d)
                 nb = (n + B - 1) // B
                 page_of = [((0, b) if b < pre_blocks else (s, b)) for b in range(nb)]
-                self.orc[sid] = OracleSeq(sid, Kh.cpu(), Vh.cpu(), O.new_records(sid, 0, nb, 0),
-                                          np.zeros(nb, bool), page_of)
+                o = OracleSeq(sid, torch.empty(shape, dtype=torch.bfloat16),
+                              torch.empty(shape, dtype=torch.bfloat16), n,
+                              O.new_records(sid, 0, nb, 0), np.zeros(nb, bool), page_of)
+                self.orc[sid] = o
+            for a in range(0, n, chunk):
+                b = min(n, a + chunk)
+                if b <= start and o is None:
+                    continue
+                Kt, Vt = W.kv_tokens(wl, s, a, b, device)
+                if o is not None:
+                    o.Kbuf[a:b].copy_(Kt.cpu())
+                    o.Vbuf[a:b].copy_(Vt.cpu())
+                if b > start:
+                    lo = max(a, start) - a
+                    self.ctx.append_tokens(sid, Kt[lo:].contiguous(), Vt[lo:].contiguous())
+                del Kt, Vt
         torch.cuda.synchronize()
 
     # ------------------------------------------------------------------
@@ -85,14 +111,15 @@ class Run:
             n = self.ntok[s]
             Kt, Vt = W.kv_tokens(wl, s, n, n + 1, self.dev)
             self.ctx.append_tokens(sid, Kt, Vt)
-            if self.oracle_on:
+            if sid in self.orc:
                 o = self.orc[sid]
                 if n % B == 0:      # a new block opens at the step counter t-1
                     o.rec = np.concatenate([o.rec, O.new_records(sid, n // B, 1, t - 1)])
                     o.ambiguous = np.append(o.ambiguous, False)
                     o.page_of.append((s, n // B))
-                o.K = torch.cat([o.K, Kt.cpu()])
-                o.V = torch.cat([o.V, Vt.cpu()])
+                o.Kbuf[n:n + 1].copy_(Kt.cpu())
+                o.Vbuf[n:n + 1].copy_(Vt.cpu())
+                o.n = n + 1
             self.ntok[s] = n + 1
         q = torch.stack([W.queries(wl, s, t, self.dev) for s in range(wl.nseq)]).contiguous()
         out = torch.empty((wl.nseq, wl.L, wl.Hq, wl.d), dtype=torch.float32, device=self.dev)
@@ -112,7 +139,7 @@ class Run:
         res["slots"] = slots[: r.n_selected].cpu().tolist()
         res["records"] = {sid: self.ctx.export_records(sid) for sid in self.ids
                           if not (flags & K.KVS_GATHER_DEMOTE)}
-        if self.oracle_on:
+        if self.orc:
             res["oracle"] = self._oracle_step(q.cpu(), t)
         return res
 
@@ -120,6 +147,8 @@ class Run:
         wl = self.wl
         outs, masses = {}, {}
         for s, sid in enumerate(self.ids):
+            if sid not in self.orc:
+                continue
             o = self.orc[sid]
             r = O.decode_with_mass(q[s], o.K, o.V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d)
             nb = len(o.rec)
@@ -144,6 +173,8 @@ class Run:
         orc = res["oracle"]
         out = res["out"].cpu().numpy()
         for s, sid in enumerate(self.ids):
+            if sid not in self.orc:
+                continue
             e = np.abs(out[s] - orc["out"][sid]).max()
             summ["out_max_abs"] = max(summ["out_max_abs"], float(e))
             slot = self.ctx.seq_info(sid)[0]
@@ -174,7 +205,7 @@ class Run:
 
     def excluded_keys(self):
         out = set()
-        for sid in self.ids:
+        for sid in self.tracked:
             ex = self.excluded(sid)
             out |= {(sid, int(b)) for b in np.nonzero(ex)[0]}
         return out
