@@ -33,7 +33,6 @@ sys.path.insert(0, ROOT)
 METRIC = "KV GB/s streamed (% of GB300 HBM peak) + decode tok/s, paged GQA decode+scoring"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 7   # append, decode, combine, mass, score, select count, select scatter
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_dram_traffic.txt")
 
 
@@ -45,7 +44,8 @@ def parse():
     ap.add_argument("--impl", choices=["kvs", "reference"], default="kvs")
     ap.add_argument("--workload", default="l70b_128k")
     ap.add_argument("--alpha", type=float, default=None)
-    ap.add_argument("--gather", choices=["mirror", "list", "none"], default="mirror")
+    ap.add_argument("--gather", choices=["auto", "mirror", "list", "demote", "none"], default="auto",
+                    help="auto: demote for workloads with periodic demotion, else mirror")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-literal", action="store_true")
@@ -180,9 +180,18 @@ class Pipeline:
         self.side = torch.cuda.Stream(device)
         self.out = torch.empty((wl.nseq, wl.L, wl.Hq, wl.d), dtype=torch.float32, device=device)
         self.host = None
-        if gather != "none":
+        self.demote_every = wl.demote_every if gather == "demote" else 0
+        self.steps_done = 0
+        self.demoted_pages = 0
+        self.launches = 0                   # kernels of this library launched
+        self.half = 16                      # staging half-ring (32 staging pages)
+        if gather in ("mirror", "list"):
             self.host = torch.empty(self.pool_pages * self.ctx.page_bytes, dtype=torch.uint8,
                                     pin_memory=True)
+        elif gather == "demote":
+            k_max = int(math.floor(wl.demote_frac * (need + wl.nseq))) + 1
+            self.host = torch.empty(k_max * self.ctx.page_bytes, dtype=torch.uint8, pin_memory=True)
+            self.ids_dev = torch.zeros(2 * (need + wl.nseq), dtype=torch.int64, device=device)
 
     def prefill(self, chunk=4096):
         wl, W = self.wl, self.W
@@ -202,16 +211,19 @@ class Pipeline:
         self.torch.cuda.synchronize()
 
     def inputs(self, step0, nsteps):
-        """Per-step new-token K/V and queries, generated on the device."""
+        """Per-step new-token K/V ([nseq][L][Hkv][d] each) and queries, generated
+        on the device."""
         wl, W, torch = self.wl, self.W, self.torch
         kv, qs = [], []
         for i in range(nsteps):
             t = step0 + i
-            row = []
+            ks, vs = [], []
             for s in range(wl.nseq):
                 n = wl.prefill_lens[s] + t - 1
-                row.append(W.kv_tokens(wl, s, n, n + 1, self.dev))
-            kv.append(row)
+                k, v = W.kv_tokens(wl, s, n, n + 1, self.dev)
+                ks.append(k)
+                vs.append(v)
+            kv.append((torch.cat(ks).contiguous(), torch.cat(vs).contiguous()))
             qs.append(torch.stack([W.queries(wl, s, t, self.dev) for s in range(wl.nseq)]).contiguous())
         return kv, qs
 
@@ -223,9 +235,10 @@ class Pipeline:
         main = self.torch.cuda.current_stream()
         if ev:
             ev[0].record(main)
-        for s, sid in enumerate(self.ids):
-            ctx.append_tokens(sid, kv_row[s][0], kv_row[s][1])
+        ctx.append_step(self.ids, kv_row[0], kv_row[1])
+        for s in range(len(self.ids)):
             self.ntok[s] += 1
+        self.launches += 5                  # append_step, decode, combine, mass, score
         if ev:
             ev[1].record(main)
         ctx.decode_step(self.ids, q, self.out)
@@ -235,13 +248,26 @@ class Pipeline:
         if ev:
             ev[3].record(main)
         r = None
-        if self.gather != "none":
+        self.steps_done += 1
+        if self.gather in ("mirror", "list"):
             flags = K.KVS_GATHER_MIRROR if self.gather == "mirror" else 0
             if mode_flags is not None:
                 flags = mode_flags
             rc, r = ctx.select_and_gather(K.KVS_SELECT_THRESH, self.host, flags=flags,
                                           side_stream=self.side)
             main.wait_stream(self.side)
+            self.launches += 3 + (0 if flags & K.KVS_GATHER_MIRROR else -(-r.n_staged // self.half))
+        elif self.demote_every and self.steps_done % self.demote_every == 0:
+            # the lowest-P fraction goes to pinned host and comes back with its record
+            rc, r = ctx.select_and_gather(K.KVS_SELECT_LOWFRAC, self.host, frac=self.wl.demote_frac,
+                                          flags=K.KVS_GATHER_DEMOTE, ids=self.ids_dev,
+                                          side_stream=self.side)
+            keys = [tuple(x) for x in self.ids_dev.view(-1, 2)[: r.n_demoted].cpu().tolist()]
+            self.side.synchronize()
+            ctx.readmit(keys, self.host)
+            self.demoted_pages += r.n_demoted
+            # radix select, count, scatter, plan, gather chunks, demote + readmit patches
+            self.launches += 4 + -(-r.n_staged // self.half) + 2
         if ev:
             ev[4].record(main)
         return r
@@ -284,9 +310,11 @@ def run_kvs(args):
         dist.init_process_group("nccl", device_id=dev)
     wl = W.workload(args.workload)
     alpha = args.alpha if args.alpha is not None else wl.alphas[-1]
+    if args.gather == "auto":
+        args.gather = "demote" if wl.demote_every else "mirror"
     K_, W_ = args.steps, args.warmup
     e2e_steps = 0 if args.no_e2e else K_
-    lit_steps = 0 if (args.no_literal or args.gather == "none") else 2
+    lit_steps = 0 if (args.no_literal or args.gather not in ("mirror", "list")) else 2
     total = W_ + K_ + e2e_steps + lit_steps
     pipe = Pipeline(wl, alpha, total, dev, args.gather)
     pipe.prefill()
@@ -305,21 +333,27 @@ def run_kvs(args):
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     kv_bytes = 0
+    uniq_bytes = 0
     staged = 0
+    shared_extra = wl.shared_prefix_tokens * (wl.nseq - 1) * wl.token_bytes
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    launches0 = pipe.launches
     wall0 = time.perf_counter()
     t_start.record()
     for i in range(K_):
         pipe.ctx.set_decode_events(dec[i][0], dec[i][1])
         r = pipe.step(kv[W_ + i], qs[W_ + i], ev[i])
         kv_bytes += pipe.kv_bytes_this_step()
+        uniq_bytes += pipe.kv_bytes_this_step() - shared_extra
         staged += r.n_staged if r is not None else 0
+    demoted = pipe.demoted_pages
     t_stop.record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    launches = pipe.launches - launches0
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
@@ -354,21 +388,20 @@ def run_kvs(args):
     e2e = None
     if e2e_steps:
         kvh, qh = pipe.inputs(W_ + K_ + 1, e2e_steps)
-        kvh = [[(k.cpu().pin_memory(), v.cpu().pin_memory()) for k, v in row] for row in kvh]
+        kvh = [(k.cpu().pin_memory(), v.cpu().pin_memory()) for k, v in kvh]
         qh = [q.cpu().pin_memory() for q in qh]
-        dkv = [(torch.empty_like(kv[0][s][0]), torch.empty_like(kv[0][s][1])) for s in range(wl.nseq)]
+        dkv = (torch.empty_like(kv[0][0]), torch.empty_like(kv[0][1]))
         dq = torch.empty_like(qs[0])
         out_h = torch.empty(pipe.out.shape, dtype=torch.float32, pin_memory=True)
-        h2d = sum(k.numel() * 2 + v.numel() * 2 for k, v in kvh[0]) + qh[0].numel() * 2
+        h2d = kvh[0][0].numel() * 2 + kvh[0][1].numel() * 2 + qh[0].numel() * 2
         d2h = out_h.numel() * 4
         torch.cuda.synchronize()
         e_b = 0
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record()
         for i in range(e2e_steps):
-            for s in range(wl.nseq):
-                dkv[s][0].copy_(kvh[i][s][0], non_blocking=True)
-                dkv[s][1].copy_(kvh[i][s][1], non_blocking=True)
+            dkv[0].copy_(kvh[i][0], non_blocking=True)
+            dkv[1].copy_(kvh[i][1], non_blocking=True)
             dq.copy_(qh[i], non_blocking=True)
             pipe.step(dkv, dq)
             out_h.copy_(pipe.out, non_blocking=True)
@@ -424,13 +457,19 @@ def run_kvs(args):
             "steps": K_, "warmup": W_, "ms_per_step": round(ms_max / K_, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded generator; recency-skewed K/V)",
-            "config": {"workload": f"{wl.name}: {wl.nseq} seq x {wl.prefill_lens[0] if wl.nseq == 1 else 'mixed'} "
-                                   f"tokens, L={wl.L} Hq={wl.Hq} Hkv={wl.Hkv} d={wl.d}, 16-token pages",
+            "config": {"workload": f"{wl.name}: {wl.nseq} seq x "
+                                   f"{wl.prefill_lens[0] if wl.nseq == 1 else f'{min(wl.prefill_lens)}..{max(wl.prefill_lens)}'} "
+                                   f"tokens (+1 per step), L={wl.L} Hq={wl.Hq} Hkv={wl.Hkv} d={wl.d}, 16-token pages"
+                                   + (f", {wl.shared_prefix_tokens}-token shared prefix" if wl.shared_prefix_tokens else ""),
                        "global_batch": wl.nseq, "seq_len": max(wl.prefill_lens),
                        "alpha": alpha, "gather": args.gather,
                        "l2": "inputs larger than L2 (KV per step >> 129 MB), no flush",
                        "parallelism": f"replicas x{ws}"},
             "decode_tok_per_s": round(tok_s, 2),
+            "physical_bound": {
+                "unique_kv_gbps": round(uniq_bytes / (ms / 1e3) / 1e9, 2),
+                "logical_exceeds_measured_peak": bool(value > peak),
+                "note": "logical bytes count a shared prefix once per sequence; unique bytes once"},
             "kv_gbps_pct_of_hbm": round(100 * value / peak, 2),
             "roofline": {"bound": "hbm", "kernel": "decode_kernel (split-K paged GQA)",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -443,11 +482,12 @@ def run_kvs(args):
             "scoring_overhead_pct": round(100 * (part["score"] + part["select_gather"]) /
                                           max(part["decode_step"], 1e-9), 2),
             "gathered_pages_timed": staged,
+            "demoted_and_readmitted_pages_timed": demoted,
             "e2e": e2e,
             "literal_gather": literal,
             "cpu_baseline": cpu,
             "clocks": clk,
-            "gpu_launches": KERNELS_PER_STEP * K_,
+            "gpu_launches": launches,
             "wall_s_timed": round(wall, 3),
         }
         print(json.dumps(line))

@@ -221,6 +221,16 @@ int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n,
 int kvs_append_token(kvs_ctx_t *ctx, uint64_t seq_id, const void *k_dev,
                      const void *v_dev, void *stream);
 
+/* Appends one token to each of nseq sequences in one launch (the new K/V rows
+ * of a decode step) [ARCH]: k, v device [nseq][L][Hkv][d] bf16, row i for
+ * seq_ids[i].  Same effect as kvs_append_token for each sequence in turn:
+ * a token that opens a block takes a page from the free list (tail slots
+ * zeroed, record created with the current step counter).  KVS_ENOMEM if the
+ * free list cannot cover every new block (nothing appended); KVS_EINVAL for
+ * duplicates, a full table row, or a last block that is shared or demoted. */
+int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
+                    const void *k_dev, const void *v_dev, void *stream);
+
 /* One decode step for nseq sequences [VA] s.4, [GQA]: advances the step
  * counter t by one, then for every (sequence, layer, query head) computes
  *   out = sum_t softmax_t(q.k_t / sqrt(d)) v_t   over all cached tokens,

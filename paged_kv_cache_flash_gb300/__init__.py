@@ -89,6 +89,7 @@ _SIGS = {
     "kvs_seq_remove": (ctypes.c_int, [c_vp, c_u64, c_vp]),
     "kvs_append_tokens": (ctypes.c_int, [c_vp, c_u64, c_u32, c_vp, c_vp, c_vp]),
     "kvs_append_token": (ctypes.c_int, [c_vp, c_u64, c_vp, c_vp, c_vp]),
+    "kvs_append_step": (ctypes.c_int, [c_vp, ctypes.POINTER(c_u64), c_u32, c_vp, c_vp, c_vp]),
     "kvs_decode_step": (ctypes.c_int, [c_vp, ctypes.POINTER(c_u64), c_u32, c_vp, c_vp, c_vp]),
     "kvs_score_update": (ctypes.c_int, [c_vp, c_vp]),
     "kvs_set_alpha": (ctypes.c_int, [c_vp, c_dbl]),
@@ -234,6 +235,16 @@ class Context:
         assert k.is_contiguous() and v.is_contiguous() and k.shape == v.shape
         _check(self.h, lib().kvs_append_tokens(self.h, seq_id, k.shape[0], k.data_ptr(),
                                                v.data_ptr(), _stream_handle(stream)))
+
+    def append_step(self, seq_ids, k, v, stream=None):
+        """One token per sequence: k, v CUDA bf16 [nseq][L][Hkv][d]."""
+        t = self.torch
+        assert k.dtype == t.bfloat16 and v.dtype == t.bfloat16 and k.is_cuda and v.is_cuda
+        assert k.is_contiguous() and v.is_contiguous() and k.shape == v.shape
+        assert k.shape[0] == len(seq_ids)
+        ids = (c_u64 * len(seq_ids))(*seq_ids)
+        _check(self.h, lib().kvs_append_step(self.h, ids, len(seq_ids), k.data_ptr(), v.data_ptr(),
+                                             _stream_handle(stream)))
 
     def decode_step(self, seq_ids, q, out, stream=None):
         t = self.torch

@@ -75,6 +75,74 @@ __global__ void append_kernel(const Geo g, const AppendArgs a, uint64_t rows_tot
     }
 }
 
+// One token per sequence: thread -> (sequence by binary search on row_off,
+// row, 16-byte vector).  Row 0 of a sequence's rows holds the token; rows of
+// later slots (a freshly opened block) are zero-filled.  The first threads
+// past the row range write the records and table entries of fresh blocks.
+__global__ void append_step_kernel(const Geo g, const uint16_t *k, const uint16_t *v, uint16_t *pool,
+                                   int32_t *table, kvs_record *records, uint8_t *page_clean,
+                                   const StepAppend *sa, uint32_t nseq, uint32_t rows_total,
+                                   uint32_t vec_per_row, uint64_t t_create)
+{
+    const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const uint64_t nvec = static_cast<uint64_t>(rows_total) * vec_per_row;
+    if (tid < nvec) {
+        const uint32_t row = static_cast<uint32_t>(tid / vec_per_row);
+        const uint32_t v16 = static_cast<uint32_t>(tid % vec_per_row);
+        uint32_t lo = 0, hi = nseq;
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (sa[mid].row_off <= row)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const StepAppend a = sa[lo];
+        const uint32_t r = row - a.row_off;
+        // r = ((slot_rel * L + l) * 2 + kv) * Hkv + h
+        const uint32_t h = r % g.Hkv;
+        uint32_t r2 = r / g.Hkv;
+        const uint32_t kv = r2 % 2;
+        r2 /= 2;
+        const uint32_t l = r2 % g.L;
+        const uint32_t rel = r2 / g.L;
+        const uint32_t slot_in = a.pos % kBlockTokens + rel;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (rel == 0) {
+            const uint16_t *src = (kv == 0 ? k : v) + ((static_cast<size_t>(lo) * g.L + l) * g.Hkv + h) * g.d;
+            val = __ldg(reinterpret_cast<const uint4 *>(src) + v16);
+        }
+        uint16_t *dst = pool + static_cast<uint64_t>(a.page) * (g.page_bytes / 2) +
+                        ((((static_cast<uint64_t>(l) * 2 + kv) * g.Hkv + h) * kBlockTokens + slot_in) * g.d);
+        reinterpret_cast<uint4 *>(dst)[v16] = val;
+    } else {
+        const uint64_t i = tid - nvec;
+        if (i < nseq) {
+            const StepAppend a = sa[i];
+            page_clean[a.page] = 0;
+            if (a.fresh) {
+                const uint32_t b = a.pos / kBlockTokens;
+                const size_t idx = static_cast<size_t>(a.slot) * g.mb + b;
+                kvs_record rec;
+                rec.key.seq_id = a.seq_id;
+                rec.key.block_idx = b;
+                rec.score = 0.0;
+                rec.last_touch = t_create;
+                rec.count = 0;
+                rec.tier = 255;
+                rec.flags = 0;
+                rec.pad0 = 0;
+                rec.prio = 0.0;
+                rec.mass = 0.f;
+                for (int q = 0; q < 12; ++q)
+                    rec.reserved[q] = 0;
+                records[idx] = rec;
+                table[idx] = a.page;
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------- scoring
 __device__ __forceinline__ uint32_t find_sorted(const DSet *ds, uint32_t r)
 {
@@ -481,6 +549,19 @@ cudaError_t launch_append(const Geo &g, const AppendArgs &a, cudaStream_t s)
     if (grid > 0x7fffffffull)
         return cudaErrorInvalidValue;
     append_kernel<<<static_cast<uint32_t>(grid), bs, 0, s>>>(g, a, rows, vec_per_row);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append_step(const Geo &g, const uint16_t *k, const uint16_t *v, uint16_t *pool,
+                               int32_t *table, kvs_record *records, uint8_t *page_clean,
+                               const StepAppend *sa, uint32_t nseq, uint32_t rows_total,
+                               uint64_t t_create, cudaStream_t s)
+{
+    const uint32_t vec_per_row = g.d * 2 / 16;
+    const uint64_t threads = static_cast<uint64_t>(rows_total) * vec_per_row + nseq;
+    const uint32_t bs = 256;
+    append_step_kernel<<<static_cast<uint32_t>((threads + bs - 1) / bs), bs, 0, s>>>(
+        g, k, v, pool, table, records, page_clean, sa, nseq, rows_total, vec_per_row, t_create);
     return cudaGetLastError();
 }
 

@@ -757,6 +757,110 @@ int kvs_append_token(kvs_ctx_t *ctx, uint64_t seq_id, const void *k_dev, const v
     return kvs_append_tokens(ctx, seq_id, 1, k_dev, v_dev, stream);
 }
 
+int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const void *k_dev,
+                    const void *v_dev, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (!seq_ids || nseq == 0 || nseq > kMaxCallSeqs || !k_dev || !v_dev)
+        return fail(ctx, KVS_EINVAL, "append_step needs 1..%u sequences and K/V pointers", kMaxCallSeqs);
+    if ((reinterpret_cast<uintptr_t>(k_dev) | reinterpret_cast<uintptr_t>(v_dev)) % 16)
+        return fail(ctx, KVS_EINVAL, "K/V must be 16-byte aligned");
+    const Geo &g = ctx->geo;
+    std::vector<StepAppend> sa(nseq);
+    std::vector<SeqState *> seqs(nseq);
+    uint32_t fresh = 0;
+    {
+        std::vector<uint64_t> sorted(seq_ids, seq_ids + nseq);
+        std::sort(sorted.begin(), sorted.end());
+        for (uint32_t i = 1; i < nseq; ++i)
+            if (sorted[i] == sorted[i - 1])
+                return fail(ctx, KVS_EINVAL, "sequence %llu listed twice", (unsigned long long)sorted[i]);
+    }
+    for (uint32_t i = 0; i < nseq; ++i) {
+        uint32_t slot;
+        SeqState *s = find_seq(ctx, seq_ids[i], &slot);
+        if (!s)
+            return fail(ctx, KVS_ENOTFOUND, "unknown sequence %llu", (unsigned long long)seq_ids[i]);
+        const uint32_t pos = s->ntok, b = pos / kBlockTokens;
+        if (b >= ctx->cfg.max_blocks_per_seq)
+            return fail(ctx, KVS_EINVAL, "sequence %llu: table row full", (unsigned long long)seq_ids[i]);
+        if (pos % kBlockTokens) {
+            if (b < s->shared_blocks)
+                return fail(ctx, KVS_EINVAL, "block %u of %llu is shared read-only", b,
+                            (unsigned long long)seq_ids[i]);
+            if (s->table[b] < 0)
+                return fail(ctx, KVS_EINVAL, "block %u of %llu is demoted", b, (unsigned long long)seq_ids[i]);
+        } else {
+            ++fresh;
+        }
+        seqs[i] = s;
+        sa[i].slot = slot;
+        sa[i].pos = pos;
+        sa[i].seq_id = seq_ids[i];
+    }
+    if (ctx->free_pages.size() < fresh)
+        return fail(ctx, KVS_ENOMEM, "pool exhausted: %u pages needed, %zu free", fresh, ctx->free_pages.size());
+    int rc = order_pool_writes(ctx, S(stream));
+    if (rc)
+        return rc;
+    uint32_t rows = 0;
+    const uint32_t rows_per_slot = g.L * 2 * g.Hkv;
+    std::vector<int32_t> taken;
+    for (uint32_t i = 0; i < nseq; ++i) {
+        const uint32_t pos = sa[i].pos;
+        sa[i].fresh = pos % kBlockTokens == 0;
+        if (sa[i].fresh) {
+            sa[i].page = ctx->free_pages.front();
+            ctx->free_pages.pop_front();
+            taken.push_back(sa[i].page);
+            sa[i].nslots = kBlockTokens;
+        } else {
+            sa[i].page = seqs[i]->table[pos / kBlockTokens];
+            sa[i].nslots = 1;
+        }
+        sa[i].row_off = rows;
+        rows += sa[i].nslots * rows_per_slot;
+    }
+    auto undo = [&]() {
+        for (auto it = taken.rbegin(); it != taken.rend(); ++it)
+            ctx->free_pages.push_front(*it);
+    };
+    RingSlot r;
+    if ((rc = ring_acquire(ctx, nseq * sizeof(StepAppend), &r))) {
+        undo();
+        return rc;
+    }
+    std::memcpy(r.host, sa.data(), nseq * sizeof(StepAppend));
+    if ((rc = ring_push(ctx, r, nseq * sizeof(StepAppend), S(stream)))) {
+        undo();
+        return rc;
+    }
+    if ((rc = launch_rc(ctx,
+                        launch_append_step(g, static_cast<const uint16_t *>(k_dev),
+                                           static_cast<const uint16_t *>(v_dev),
+                                           static_cast<uint16_t *>(ctx->buf.pool),
+                                           static_cast<int32_t *>(ctx->buf.block_table),
+                                           static_cast<kvs_record *>(ctx->buf.records), ctx->work.page_clean,
+                                           reinterpret_cast<const StepAppend *>(r.dev), nseq, rows, ctx->t,
+                                           S(stream)),
+                        "append_step"))) {
+        undo();
+        return rc;
+    }
+    if ((rc = ring_release(ctx, r, S(stream))))
+        return rc;
+    for (uint32_t i = 0; i < nseq; ++i) {
+        if (sa[i].fresh) {
+            seqs[i]->table.push_back(sa[i].page);
+            ctx->refcnt[sa[i].page] = 1;
+            ctx->refcnt_dirty = true;
+        }
+        seqs[i]->ntok += 1;
+    }
+    return KVS_OK;
+}
+
 int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const void *q_dev,
                     float *out_dev, void *stream)
 {

@@ -127,7 +127,22 @@ struct AppendArgs {
     uint64_t seq_id, t_create;
 };
 
+// One sequence of a batched one-token append.
+struct StepAppend {
+    uint32_t slot;        // sequence slot
+    uint32_t pos;         // token position (block = pos / 16)
+    int32_t page;         // page of that block
+    uint32_t nslots;      // slots written: 1, or 16 - pos % 16 when the token opens the block
+    uint32_t row_off;     // prefix of nslots * L * 2 * Hkv over the call
+    uint32_t fresh;       // 1: the block is new (record + table entry written)
+    uint64_t seq_id;
+};
+
 // ---- launchers (each returns the cudaGetLastError() of its launch) -------
+cudaError_t launch_append_step(const Geo &g, const uint16_t *k, const uint16_t *v, uint16_t *pool,
+                               int32_t *table, kvs_record *records, uint8_t *page_clean,
+                               const StepAppend *sa, uint32_t nseq, uint32_t rows_total,
+                               uint64_t t_create, cudaStream_t s);
 cudaError_t launch_append(const Geo &g, const AppendArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w,
                           const uint16_t *q, const int32_t *table,

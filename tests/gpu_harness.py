@@ -100,17 +100,25 @@ class Run:
         torch.cuda.synchronize()
 
     # ------------------------------------------------------------------
-    def step(self, gather_host=None, mode=K.KVS_SELECT_THRESH, flags=0, frac=0.0):
+    def step(self, gather_host=None, mode=K.KVS_SELECT_THRESH, flags=0, frac=0.0,
+             batched_append=True):
         """One decode step over every sequence; returns a dict of GPU results
-        and, if the oracle is on, the oracle's."""
+        and, if the oracle is on, the oracle's.  batched_append: the new
+        tokens go in through kvs_append_step (one call), else through one
+        kvs_append_tokens call per sequence."""
         wl = self.wl
         B = wl.block_tokens
         self.t += 1
         t = self.t
+        new = [W.kv_tokens(wl, s, self.ntok[s], self.ntok[s] + 1, self.dev) for s in range(wl.nseq)]
+        if batched_append:
+            self.ctx.append_step(self.ids, torch.cat([k for k, _ in new]).contiguous(),
+                                 torch.cat([v for _, v in new]).contiguous())
         for s, sid in enumerate(self.ids):
             n = self.ntok[s]
-            Kt, Vt = W.kv_tokens(wl, s, n, n + 1, self.dev)
-            self.ctx.append_tokens(sid, Kt, Vt)
+            Kt, Vt = new[s]
+            if not batched_append:
+                self.ctx.append_tokens(sid, Kt, Vt)
             if sid in self.orc:
                 o = self.orc[sid]
                 if n % B == 0:      # a new block opens at the step counter t-1

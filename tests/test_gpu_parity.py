@@ -81,8 +81,9 @@ def test_ragged_multi_sequence_and_shared_prefix():
                     pool_pages=40, steps=20, skew=True)
     run = Run(wl, 0.3)
     host = _pinned(wl.pool_pages * wl.page_bytes)
-    for _ in range(wl.steps):
-        res = run.step(host)
+    for i in range(wl.steps):
+        # alternate the batched append and the per-sequence one
+        res = run.step(host, batched_append=bool(i % 2))
         run.compare(res)
         _check_gather(run, res, host)
     # the shared pages are gathered only when all three users list them
@@ -94,7 +95,7 @@ def test_single_token_sequence_and_large_group():
     wl = W.workload("l70b_8k", L=3, prefill_lens=(1, 17), pool_pages=8, steps=3)
     run = Run(wl, 0.15)
     for _ in range(wl.steps):
-        res = run.step(None)
+        res = run.step(None, batched_append=False)
         run.compare(res)
     run.close()
 
