@@ -154,6 +154,22 @@ class ClockSampler:
                                     if re.match(r"^[0-9.]+$", r[3])), default=None)}
 
 
+def reduce_over_ranks(ms: float, nbytes: float, device=None):
+    """Replicas: the job's time is the slowest rank's, its bytes the sum of
+    every rank's.  Returns (max ms, total bytes); identity without a process
+    group.  `device`: where the reduction tensors live (cuda for NCCL, cpu
+    for gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms), float(nbytes)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    b = torch.tensor([float(nbytes)], dtype=torch.float64, device=device)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
 # --------------------------------------------------------------- kvs arm
 
 
@@ -369,14 +385,7 @@ def run_kvs(args):
     pipe.ctx.check_device()
     ms = t_start.elapsed_time(t_stop)
 
-    ms_max, bytes_all = ms, kv_bytes
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
-        b = torch.tensor([float(kv_bytes)], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(b)
-        bytes_all = float(b.item())
+    ms_max, bytes_all = reduce_over_ranks(ms, kv_bytes, dev)
     value = bytes_all / (ms_max / 1e3) / 1e9
     tok_s = wl.nseq * K_ * ws / (ms_max / 1e3)
 
@@ -417,11 +426,8 @@ def run_kvs(args):
         s1.record()
         torch.cuda.synchronize()
         e_ms = s0.elapsed_time(s1)
-        e_val = e_b / (e_ms / 1e3) / 1e9
-        if ws > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_val = e_b * ws / (float(t.item()) / 1e3) / 1e9
+        e_ms_max, e_b_all = reduce_over_ranks(e_ms, e_b, dev)
+        e_val = e_b_all / (e_ms_max / 1e3) / 1e9
         e2e = {"value": round(e_val, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e_ms / e2e_steps, 4)}
 
