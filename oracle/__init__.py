@@ -66,6 +66,10 @@ def _load():
             P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, P, P, P]
         lib.orc_decode_heads.restype = ctypes.c_int
+        lib.orc_decode_heads_u8.argtypes = [
+            P, P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, P, P, P]
+        lib.orc_decode_heads_u8.restype = ctypes.c_int
         lib.orc_aggregate_mass.argtypes = [P, ctypes.c_int64, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, P]
         lib.orc_aggregate_mass.restype = None
@@ -101,15 +105,25 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def decode(q, K, V, *, L, Hq, Hkv, d, block_tokens=16, heads=None,
-           threads=None, want_out=True, want_head_mass=True):
+           threads=None, want_out=True, want_head_mass=True, k_lut=None, v_lut=None):
     """Decode attention of one sequence.
 
-    q: [L][Hq][d] bf16; K, V: [n][L][Hkv][d] bf16 in logical token order.
+    q: [L][Hq][d] bf16; K, V: [n][L][Hkv][d] bf16 in logical token order, or
+    uint8 codes with k_lut / v_lut (256 values each, e.g. e4m3_lut(scale)).
     heads: iterable of flat l*Hq+h indices (None = all, in order).
     Returns dict(out [nh][d], lse [nh], head_mass [nh][nb] or None).
     """
     lib = _load()
-    qb, kb, vb = _u16(q), _u16(K), _u16(V)
+    coded = k_lut is not None
+    qb = _u16(q)
+    if coded:
+        kb = np.ascontiguousarray(np.asarray(K, np.uint8))
+        vb = np.ascontiguousarray(np.asarray(V, np.uint8))
+        lk = np.ascontiguousarray(np.asarray(k_lut, np.float64))
+        lv = np.ascontiguousarray(np.asarray(v_lut, np.float64))
+        assert lk.shape == (256,) and lv.shape == (256,)
+    else:
+        kb, vb = _u16(K), _u16(V)
     n = kb.shape[0]
     assert qb.shape == (L, Hq, d) and kb.shape == (n, L, Hkv, d) and vb.shape == kb.shape
     nb = (n + block_tokens - 1) // block_tokens
@@ -118,10 +132,14 @@ def decode(q, K, V, *, L, Hq, Hkv, d, block_tokens=16, heads=None,
     out = np.zeros((nh, d), np.float64) if want_out else None
     lse = np.zeros(nh, np.float64)
     hm = np.zeros((nh, nb), np.float64) if want_head_mass else None
-    rc = lib.orc_decode_heads(_ptr(qb), _ptr(kb), _ptr(vb), n, L, Hq, Hkv, d,
-                              block_tokens, _ptr(hl) if hl is not None else None,
-                              nh, int(threads or os.cpu_count() or 1),
-                              _ptr(out), _ptr(lse), _ptr(hm))
+    hp = _ptr(hl) if hl is not None else None
+    nt = int(threads or os.cpu_count() or 1)
+    if coded:
+        rc = lib.orc_decode_heads_u8(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(lk), _ptr(lv), n, L, Hq,
+                                     Hkv, d, block_tokens, hp, nh, nt, _ptr(out), _ptr(lse), _ptr(hm))
+    else:
+        rc = lib.orc_decode_heads(_ptr(qb), _ptr(kb), _ptr(vb), n, L, Hq, Hkv, d,
+                                  block_tokens, hp, nh, nt, _ptr(out), _ptr(lse), _ptr(hm))
     if rc != 0:
         raise RuntimeError("oracle decode failed (bad argument or out of memory)")
     return {"out": out, "lse": lse, "head_mass": hm}
@@ -139,10 +157,10 @@ def aggregate_mass(head_mass: np.ndarray, *, L, Hq, Hkv) -> np.ndarray:
 
 
 def decode_with_mass(q, K, V, *, L, Hq, Hkv, d, block_tokens=16, threads=None,
-                     want_out=True):
+                     want_out=True, k_lut=None, v_lut=None):
     """All heads of one sequence: out [L][Hq][d], lse [L][Hq], mass [nb]."""
     r = decode(q, K, V, L=L, Hq=Hq, Hkv=Hkv, d=d, block_tokens=block_tokens,
-               threads=threads, want_out=want_out, want_head_mass=True)
+               threads=threads, want_out=want_out, want_head_mass=True, k_lut=k_lut, v_lut=v_lut)
     mass = aggregate_mass(r["head_mass"], L=L, Hq=Hq, Hkv=Hkv)
     return {
         "out": None if r["out"] is None else r["out"].reshape(L, Hq, d),
@@ -150,6 +168,59 @@ def decode_with_mass(q, K, V, *, L, Hq, Hkv, d, block_tokens=16, threads=None,
         "head_mass": r["head_mass"],
         "mass": mass,
     }
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 codes ("Fitting a Million Tokens", s.02: FP8 E4M3 KV halves the
+# bytes).  Format: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; no
+# infinities; S.1111.111 is NaN; largest finite 448, smallest subnormal 2^-9.
+# ---------------------------------------------------------------------------
+
+
+def e4m3_values() -> np.ndarray:
+    """Value of each of the 256 codes (NaN for the two NaN codes)."""
+    v = np.empty(256, np.float64)
+    for c in range(256):
+        sign = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 0x7
+        if e == 15 and m == 7:
+            v[c] = np.nan
+        elif e == 0:
+            v[c] = sign * 2.0 ** -6 * (m / 8.0)
+        else:
+            v[c] = sign * 2.0 ** (e - 7) * (1.0 + m / 8.0)
+    return v
+
+
+_E4M3 = e4m3_values()
+_E4M3_POS = _E4M3[:127]          # codes 0..126: 0 .. 448, increasing
+
+
+def e4m3_lut(scale: float) -> np.ndarray:
+    """Dequantised value of each code: code value x scale (float64)."""
+    return _E4M3 * np.float64(np.float32(scale))
+
+
+def quantize_e4m3(x, scale: float) -> np.ndarray:
+    """Codes of x / scale: the division in IEEE fp32, then the nearest code
+    (ties to the even mantissa), magnitudes beyond 448 saturating to 448,
+    the sign kept (also for results that round to zero)."""
+    xf = np.asarray(x, np.float32)
+    y = (xf / np.float32(scale)).astype(np.float64)
+    a = np.minimum(np.abs(y), 448.0)
+    hi = np.searchsorted(_E4M3_POS, a)                 # first value >= a
+    hi = np.minimum(hi, 126)
+    lo = np.maximum(hi - 1, 0)
+    dlo = a - _E4M3_POS[lo]
+    dhi = _E4M3_POS[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(y), code | 0x80, code).astype(np.uint8)
+
+
+def quantize_bf16_e4m3(bits, scale: float) -> np.ndarray:
+    """quantize_e4m3 of bf16 bit patterns (a torch bf16 tensor or uint16)."""
+    return quantize_e4m3(bf16_to_f64(_u16(bits)).astype(np.float32), scale)
 
 
 # ---------------------------------------------------------------------------
@@ -278,11 +349,19 @@ def select_lowfrac(recs_by_seq: dict, frac: float) -> list:
 
 def assemble_page(K_blk, V_blk, block_tokens: int = 16) -> bytes:
     """Bytes of one page from the logical K, V of its t <= block_tokens
-    tokens ([t][L][Hkv][d] bf16 each).
+    tokens ([t][L][Hkv][d] each: bf16, or uint8 codes for FP8 pages).
 
     Layout, outermost first: layer, {K, V}, KV head, token slot, head dim;
-    bf16 little-endian; slots past the last token are zero.
+    bf16 little-endian or one byte per code; slots past the last token are
+    zero.
     """
+    if isinstance(K_blk, np.ndarray) and K_blk.dtype == np.uint8:
+        kb, vb = K_blk, V_blk
+        t, L, Hkv, d = kb.shape
+        page = np.zeros((L, 2, Hkv, block_tokens, d), np.uint8)
+        page[:, 0, :, :t, :] = kb.transpose(1, 2, 0, 3)
+        page[:, 1, :, :t, :] = vb.transpose(1, 2, 0, 3)
+        return page.tobytes()
     kb, vb = _u16(K_blk), _u16(V_blk)
     t, L, Hkv, d = kb.shape
     assert t <= block_tokens and vb.shape == kb.shape

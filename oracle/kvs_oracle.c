@@ -56,17 +56,30 @@ double orc_bf16_to_f64(uint16_t h) { return bf16_to_f64(h); }
  *   bmass    : ceil(n / block_tokens) doubles, mu(b) (may be NULL)
  *   sbuf     : n doubles of scratch
  */
-static void attend_head(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+/* K and V elements: bf16 bit patterns, or 8-bit codes read through a
+ * 256-entry table of values (code value x scale), e.g. for FP8 pages. */
+typedef struct {
+    const uint16_t *p16;      /* bf16 elements, or NULL */
+    const uint8_t *p8;        /* 8-bit codes, or NULL   */
+    const double *lut;        /* value of each code     */
+} elems_t;
+
+static double elem_at(const elems_t *e, int64_t idx)
+{
+    return e->p16 ? bf16_to_f64(e->p16[idx]) : e->lut[e->p8[idx]];
+}
+
+static void attend_head(const uint16_t *q, const elems_t *k, const elems_t *v, int64_t off,
                         int64_t tok_stride, int64_t n, int d, int block_tokens,
                         double *sbuf, double *out, double *lse, double *bmass)
 {
     const double sigma = 1.0 / sqrt((double)d);
     double m = -INFINITY;
     for (int64_t t = 0; t < n; ++t) {
-        const uint16_t *kt = k + t * tok_stride;
+        const int64_t kt = off + t * tok_stride;
         double dot = 0.0;
         for (int i = 0; i < d; ++i)
-            dot += bf16_to_f64(q[i]) * bf16_to_f64(kt[i]);
+            dot += bf16_to_f64(q[i]) * elem_at(k, kt + i);
         sbuf[t] = sigma * dot;
         if (sbuf[t] > m)
             m = sbuf[t];
@@ -82,9 +95,9 @@ static void attend_head(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         for (int i = 0; i < d; ++i)
             out[i] = 0.0;
         for (int64_t t = 0; t < n; ++t) {
-            const uint16_t *vt = v + t * tok_stride;
+            const int64_t vt = off + t * tok_stride;
             for (int i = 0; i < d; ++i)
-                out[i] += sbuf[t] * bf16_to_f64(vt[i]);
+                out[i] += sbuf[t] * elem_at(v, vt + i);
         }
     }
     if (bmass) {
@@ -100,7 +113,8 @@ static void attend_head(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 }
 
 typedef struct {
-    const uint16_t *q, *k, *v;
+    const uint16_t *q;
+    elems_t k, v;
     int64_t n;
     int L, Hq, Hkv, d, block_tokens;
     const int32_t *heads;   /* flat (l*Hq + h) indices to compute */
@@ -127,7 +141,7 @@ static void *run_job(void *arg)
         const int l = lh / j->Hq, h = lh % j->Hq, g = h / G;
         const uint16_t *qh = j->q + ((int64_t)l * j->Hq + h) * j->d;
         const int64_t off = ((int64_t)l * j->Hkv + g) * j->d;
-        attend_head(qh, j->k + off, j->v + off, tok_stride, j->n, j->d,
+        attend_head(qh, &j->k, &j->v, off, tok_stride, j->n, j->d,
                     j->block_tokens, sbuf,
                     j->want_out ? j->out + (int64_t)idx * j->d : NULL,
                     j->lse + idx, j->head_mass ? j->head_mass + (int64_t)idx * nb : NULL);
@@ -147,10 +161,10 @@ static void *run_job(void *arg)
  * exactly one thread, so the result does not depend on the thread count.
  * Returns 0, or -1 on a bad argument or allocation failure.
  */
-int orc_decode_heads(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                     int64_t n, int L, int Hq, int Hkv, int d, int block_tokens,
-                     const int32_t *heads, int nheads, int nthreads,
-                     double *out, double *lse, double *head_mass)
+static int decode_heads(const uint16_t *q, elems_t k, elems_t v,
+                        int64_t n, int L, int Hq, int Hkv, int d, int block_tokens,
+                        const int32_t *heads, int nheads, int nthreads,
+                        double *out, double *lse, double *head_mass)
 {
     if (n < 1 || L < 1 || Hkv < 1 || Hq % Hkv || d < 1 || block_tokens < 1 ||
         (heads && nheads < 1))
@@ -208,6 +222,33 @@ done:
     free(th);
     free(all);
     return rc;
+}
+
+int orc_decode_heads(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     int64_t n, int L, int Hq, int Hkv, int d, int block_tokens,
+                     const int32_t *heads, int nheads, int nthreads,
+                     double *out, double *lse, double *head_mass)
+{
+    elems_t ek = {k, NULL, NULL}, ev = {v, NULL, NULL};
+    return decode_heads(q, ek, ev, n, L, Hq, Hkv, d, block_tokens, heads, nheads, nthreads,
+                        out, lse, head_mass);
+}
+
+/*
+ * Same, with K and V held as 8-bit codes [n][L][Hkv][d] whose values are
+ * lut_k[code] and lut_v[code] (256 entries each).
+ */
+int orc_decode_heads_u8(const uint16_t *q, const uint8_t *k, const uint8_t *v,
+                        const double *lut_k, const double *lut_v,
+                        int64_t n, int L, int Hq, int Hkv, int d, int block_tokens,
+                        const int32_t *heads, int nheads, int nthreads,
+                        double *out, double *lse, double *head_mass)
+{
+    if (!lut_k || !lut_v)
+        return -1;
+    elems_t ek = {NULL, k, lut_k}, ev = {NULL, v, lut_v};
+    return decode_heads(q, ek, ev, n, L, Hq, Hkv, d, block_tokens, heads, nheads, nthreads,
+                        out, lse, head_mass);
 }
 
 /*

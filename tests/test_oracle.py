@@ -328,3 +328,90 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_score_update_touch_anchor_and_order()
     monkeypatch.setattr(O, "priority", good_prio)
+
+
+# ------------------------------------------------------------ FP8 E4M3 codes
+
+
+def test_e4m3_table_closed_forms():
+    v = O.e4m3_values()
+    assert v[0x7E] == 448.0 and v[0x01] == 2.0 ** -9 and v[0x38] == 1.0
+    assert v[0x08] == 2.0 ** -6                     # smallest normal
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    pos = v[:127]
+    assert np.all(np.diff(pos) > 0)                  # 0 .. 448, increasing
+    assert np.array_equal(v[0x80:0xFF], -v[0x00:0x7F])
+
+
+def test_e4m3_quantize_matches_torch_in_range():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(3.0),
+        rng.uniform(-463.9, 463.9, 5000).astype(np.float32),
+        (O.e4m3_values()[1:126] + O.e4m3_values()[2:127]).astype(np.float32) / 2,   # exact ties
+        np.array([0.0, -0.0, 2 ** -10, -(2 ** -10), 1e-9, -1e-9, 464.0, -464.0], np.float32),
+    ])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.quantize_e4m3(x, 1.0), ref)
+
+
+def test_e4m3_saturation_and_scale():
+    big = np.array([465.0, 1e6, -470.0, -1e30], np.float32)
+    assert O.quantize_e4m3(big, 1.0).tolist() == [0x7E, 0x7E, 0xFE, 0xFE]
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal(1000).astype(np.float32)
+    for s in (0.25, 2.0, 8.0):               # a power-of-two scale shifts the exponent only
+        assert np.array_equal(O.quantize_e4m3(x, s), O.quantize_e4m3(x / np.float32(s), 1.0))
+    lut = O.e4m3_lut(0.5)
+    assert lut[0x38] == 0.5
+
+
+def test_e4m3_relative_error_bound():
+    rng = np.random.default_rng(7)
+    x = np.exp(rng.uniform(np.log(2.0 ** -6), np.log(448.0), 20000)).astype(np.float32)
+    x *= rng.choice([-1, 1], x.size).astype(np.float32)
+    back = O.e4m3_values()[O.quantize_e4m3(x, 1.0)]
+    assert np.all(np.abs(back - x) <= 2.0 ** -4 * np.abs(x))     # half an ulp of 3 mantissa bits
+
+
+def test_attention_on_fp8_codes_matches_library_sdpa():
+    wl, q, K, V = _case("l70b_8k", 300, L=2, prefill_lens=(300,))
+    sk, sv = 0.5, 0.25
+    kc, vc = O.quantize_bf16_e4m3(K, sk), O.quantize_bf16_e4m3(V, sv)
+    lk, lv = O.e4m3_lut(sk), O.e4m3_lut(sv)
+    r = O.decode_with_mass(q, kc, vc, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, k_lut=lk, v_lut=lv)
+    Kd = torch.from_numpy(lk[kc])
+    Vd = torch.from_numpy(lv[vc])
+    G = wl.Hq // wl.Hkv
+    qd = q.double().unsqueeze(2)
+    Kr = Kd.permute(1, 2, 0, 3).repeat_interleave(G, dim=1)
+    Vr = Vd.permute(1, 2, 0, 3).repeat_interleave(G, dim=1)
+    out = F.scaled_dot_product_attention(qd, Kr, Vr).squeeze(2)
+    np.testing.assert_allclose(r["out"], out.numpy(), rtol=0, atol=1e-12)
+    assert abs(r["mass"].sum() - 1.0) < 1e-12
+
+
+def test_fp8_page_assembly_is_bytes_of_codes():
+    codes = np.arange(2 * 2 * 2 * 4, dtype=np.uint8).reshape(2, 2, 2, 4)
+    page = np.frombuffer(O.assemble_page(codes, codes + 100, 16), np.uint8)
+    assert page.size == 2 * 2 * 2 * 16 * 4
+    assert page[((1 * 2 + 1) * 2 + 0) * 16 * 4 + 1 * 4 + 3] == codes[1, 1, 0, 3] + 100
+
+
+def test_quantizer_pin_catches_round_half_up(monkeypatch):
+    good = O.quantize_e4m3
+
+    def half_up(x, scale):
+        xf = np.asarray(x, np.float32)
+        y = (xf / np.float32(scale)).astype(np.float64)
+        a = np.minimum(np.abs(y), 448.0)
+        hi = np.minimum(np.searchsorted(O._E4M3_POS, a), 126)
+        lo = np.maximum(hi - 1, 0)
+        pick_hi = (O._E4M3_POS[hi] - a) <= (a - O._E4M3_POS[lo])
+        code = np.where(pick_hi, hi, lo).astype(np.uint8)
+        return np.where(np.signbit(y), code | 0x80, code).astype(np.uint8)
+
+    monkeypatch.setattr(O, "quantize_e4m3", half_up)
+    with pytest.raises(AssertionError):
+        test_e4m3_quantize_matches_torch_in_range()
+    monkeypatch.setattr(O, "quantize_e4m3", good)
