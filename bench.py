@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--alpha", type=float, default=None)
     ap.add_argument("--gather", choices=["auto", "mirror", "list", "demote", "none"], default="auto",
                     help="auto: demote for workloads with periodic demotion, else mirror")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="page element type: bf16, or FP8 E4M3 codes (per-tensor scale 1.0)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-literal", action="store_true")
@@ -176,7 +178,7 @@ def reduce_over_ranks(ms: float, nbytes: float, device=None):
 class Pipeline:
     """The hot path, driven through the public C ABI for a set of sequences."""
 
-    def __init__(self, wl, alpha, steps_total, device, gather):
+    def __init__(self, wl, alpha, steps_total, device, gather, kv_dtype="bf16"):
         import torch
         import paged_kv_cache_flash_gb300 as K
         import workloads as W
@@ -191,8 +193,10 @@ class Pipeline:
         self.pool_pages = max(wl.pool_pages, need + 8)
         cfg = K.make_config(wl.L, wl.Hq, wl.Hkv, wl.d, self.pool_pages, wl.nseq, mb, alpha=alpha,
                             recency_window=wl.recency_window, weights=wl.weights, cuts=wl.cuts,
-                            pool_seed=wl.seed, staging_pages=32)
+                            pool_seed=wl.seed, staging_pages=32,
+                            kv_dtype=K.KVS_KV_FP8_E4M3 if kv_dtype == "fp8" else K.KVS_KV_BF16)
         self.ctx = K.Context(cfg, device)
+        self.token_bytes = wl.token_bytes // (2 if kv_dtype == "fp8" else 1)
         self.side = torch.cuda.Stream(device)
         self.out = torch.empty((wl.nseq, wl.L, wl.Hq, wl.d), dtype=torch.float32, device=device)
         self.host = None
@@ -252,7 +256,7 @@ class Pipeline:
         return kv, qs
 
     def kv_bytes_this_step(self):
-        return sum(self.ntok) * self.wl.token_bytes   # tokens attended (after append)
+        return sum(self.ntok) * self.token_bytes   # tokens attended (after append)
 
     def step(self, kv_row, q, ev=None, mode_flags=None):
         K, ctx = self.K, self.ctx
@@ -340,7 +344,7 @@ def run_kvs(args):
     e2e_steps = 0 if args.no_e2e else K_
     lit_steps = 0 if (args.no_literal or args.gather not in ("mirror", "list")) else 2
     total = W_ + K_ + e2e_steps + lit_steps
-    pipe = Pipeline(wl, alpha, total, dev, args.gather)
+    pipe = Pipeline(wl, alpha, total, dev, args.gather, args.kv_dtype)
     pipe.prefill()
     kv, qs = pipe.inputs(1, W_ + K_)
 
@@ -359,7 +363,7 @@ def run_kvs(args):
     kv_bytes = 0
     uniq_bytes = 0
     staged = 0
-    shared_extra = wl.shared_prefix_tokens * (wl.nseq - 1) * wl.token_bytes
+    shared_extra = wl.shared_prefix_tokens * (wl.nseq - 1) * pipe.token_bytes
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -399,7 +403,7 @@ def run_kvs(args):
     algo = kv_bytes / K_ + wl.nseq * wl.L * wl.Hq * wl.d * 2 + sum(nb) * 4
     achieved = algo / (dec_avg / 1e3) / 1e9
     peak, peak_src = read_peaks()
-    traffic = read_traffic(args.workload)
+    traffic = read_traffic(args.workload) if args.kv_dtype == "bf16" else None
 
     # ---- end to end through host buffers --------------------------------
     e2e = None
@@ -469,7 +473,8 @@ def run_kvs(args):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
             "steps": K_, "warmup": W_, "ms_per_step": round(ms_max / K_, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if args.kv_dtype == "bf16" else "e4m3 KV, f16 MMA, fp32 accumulate",
             "data": "synthetic (seeded generator; recency-skewed K/V)",
             "config": {"workload": f"{wl.name}: {wl.nseq} seq x "
                                    f"{wl.prefill_lens[0] if wl.nseq == 1 else f'{min(wl.prefill_lens)}..{max(wl.prefill_lens)}'} "

@@ -42,9 +42,11 @@
  *     the call.  Calls on one context must be ordered by the caller (one
  *     stream, or events between streams).
  *   - Layouts (bf16 = IEEE bfloat16, little-endian):
- *       page   : [L][2 (K, V)][Hkv][16 token slots][d] bf16, page_bytes =
- *                2*L*Hkv*16*d*2 (5,242,880 B for 80/8/128); slots past the
- *                last token of a partial block are zero.
+ *       page   : [L][2 (K, V)][Hkv][16 token slots][d] elements, page_bytes =
+ *                2*L*Hkv*16*d*elem (5,242,880 B for 80/8/128 in bf16); slots
+ *                past the last token of a partial block are zero.  An element
+ *                is a bf16 value, or with kv_dtype KVS_KV_FP8_E4M3 one byte
+ *                holding an FP8 E4M3 code (page 2,621,440 B).
  *       pool   : [pool_blocks] pages.
  *       q      : [nseq][L][Hq][d] bf16; out: [nseq][L][Hq][d] float32.
  *       K, V   : token-major [n][L][Hkv][d] bf16 (as produced by a layer's
@@ -82,6 +84,14 @@ typedef enum kvs_status {
     KVS_EDEVICE = 8     /* a kernel reported an inconsistency (see error text) */
 } kvs_status;
 
+typedef enum kvs_kv_dtype {
+    KVS_KV_BF16 = 0,       /* pages hold bf16 K and V                          */
+    KVS_KV_FP8_E4M3 = 1    /* pages hold FP8 E4M3 codes: value = code * scale,
+                              appended bf16 values quantised as
+                              code = e4m3(x / scale) ("Fitting a Million
+                              Tokens", s.02: FP8 E4M3 KV halves the bytes)    */
+} kvs_kv_dtype;
+
 typedef enum kvs_select_mode {
     KVS_SELECT_THRESH = 0,   /* every record with P < cut_lo (tier 2) */
     KVS_SELECT_LOWFRAC = 1   /* the floor(frac*N) records with smallest P */
@@ -106,10 +116,14 @@ typedef struct kvs_config {
     uint32_t staging_pages;       /* device staging ring, pages (>= 1)        */
     double alpha;                 /* EMA weight of the current mass [VA] s.11 */
     uint32_t recency_window;      /* W: R = clip(1 - (t - last_touch)/W, 0, 1) */
-    uint32_t reserved0;
+    uint32_t kv_dtype;            /* kvs_kv_dtype; FP8 needs head_dim 128     */
     double w_recency, w_ema, w_anchor;   /* [VA] s.12: 0.25, 0.55, 0.20      */
     double cut_lo, cut_hi;               /* [VA] Diagram 12.2: 0.3, 0.6      */
     uint64_t pool_seed;           /* seeds the free-list order of the pool    */
+    float k_scale, v_scale;       /* FP8 only: per-tensor scales (> 0); the
+                                     quotient x / scale is an IEEE fp32
+                                     division, rounded to the nearest code
+                                     (ties to even), saturating at +-448   */
 } kvs_config;
 
 /* Byte sizes of the caller-allocated device buffers.  Every buffer must be

@@ -25,6 +25,7 @@ KVS_OK, KVS_EINVAL, KVS_ENOMEM, KVS_ECUDA, KVS_ENOTFOUND, KVS_EEXIST, KVS_ETRUNC
 STATUS_NAMES = ["OK", "EINVAL", "ENOMEM", "ECUDA", "ENOTFOUND", "EEXIST", "ETRUNC",
                 "ETIMEOUT", "EDEVICE"]
 KVS_SELECT_THRESH, KVS_SELECT_LOWFRAC = 0, 1
+KVS_KV_BF16, KVS_KV_FP8_E4M3 = 0, 1
 KVS_GATHER_DEMOTE, KVS_GATHER_MIRROR = 1, 2
 KVS_MAX_CALL_SEQS = 256
 BLOCK_TOKENS = 16
@@ -39,8 +40,9 @@ class kvs_config(ctypes.Structure):
                 ("head_dim", c_u32), ("block_tokens", c_u32), ("pool_blocks", c_u32),
                 ("max_seqs", c_u32), ("max_blocks_per_seq", c_u32), ("max_call_blocks", c_u32),
                 ("staging_pages", c_u32), ("alpha", c_dbl), ("recency_window", c_u32),
-                ("reserved0", c_u32), ("w_recency", c_dbl), ("w_ema", c_dbl), ("w_anchor", c_dbl),
-                ("cut_lo", c_dbl), ("cut_hi", c_dbl), ("pool_seed", c_u64)]
+                ("kv_dtype", c_u32), ("w_recency", c_dbl), ("w_ema", c_dbl), ("w_anchor", c_dbl),
+                ("cut_lo", c_dbl), ("cut_hi", c_dbl), ("pool_seed", c_u64),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class kvs_sizes(ctypes.Structure):
@@ -151,13 +153,15 @@ def _check(ctx, rc):
 
 def make_config(L, Hq, Hkv, d, pool_blocks, max_seqs, max_blocks_per_seq, *, alpha=0.15,
                 recency_window=64, weights=(0.25, 0.55, 0.20), cuts=(0.3, 0.6), pool_seed=0,
-                staging_pages=16, max_call_blocks=0) -> kvs_config:
+                staging_pages=16, max_call_blocks=0, kv_dtype=KVS_KV_BF16, k_scale=1.0,
+                v_scale=1.0) -> kvs_config:
     return kvs_config(num_layers=L, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
                       block_tokens=BLOCK_TOKENS, pool_blocks=pool_blocks, max_seqs=max_seqs,
                       max_blocks_per_seq=max_blocks_per_seq, max_call_blocks=max_call_blocks,
                       staging_pages=staging_pages, alpha=alpha, recency_window=recency_window,
-                      w_recency=weights[0], w_ema=weights[1], w_anchor=weights[2],
-                      cut_lo=cuts[0], cut_hi=cuts[1], pool_seed=pool_seed)
+                      kv_dtype=kv_dtype, w_recency=weights[0], w_ema=weights[1],
+                      w_anchor=weights[2], cut_lo=cuts[0], cut_hi=cuts[1], pool_seed=pool_seed,
+                      k_scale=k_scale, v_scale=v_scale)
 
 
 def kvs_required_sizes(cfg: kvs_config) -> kvs_sizes:

@@ -10,6 +10,7 @@
 #include <algorithm>
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "kvs_internal.h"
 
@@ -17,6 +18,43 @@ namespace kvs {
 namespace {
 
 // ----------------------------------------------------------------- append
+// One 16-byte vector of a page row from the token-major bf16 source row:
+// 8 bf16 values as they are, or (FP8 pages) 16 values quantised to E4M3 codes,
+// code = e4m3(x / scale) with an IEEE fp32 division, nearest code, saturating.
+__device__ __forceinline__ uint4 page_vec_from_bf16(const Geo &g, const uint16_t *src_row, uint32_t v16,
+                                                    float scale)
+{
+    if (!g.fp8)
+        return __ldg(reinterpret_cast<const uint4 *>(src_row) + v16);
+    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src_row) + 2 * v16);
+    const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src_row) + 2 * v16 + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const uint32_t word = w[2 * q + r];
+            const float x0 = __fdiv_rn(__uint_as_float(word << 16), scale);
+            const float x1 = __fdiv_rn(__uint_as_float(word & 0xffff0000u), scale);
+            const __nv_fp8x2_storage_t c =
+                __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+            packed |= static_cast<uint32_t>(c) << (16 * r);
+        }
+        out[q] = packed;
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__device__ __forceinline__ uint8_t *page_row(const Geo &g, uint8_t *pool, int32_t page, uint32_t l,
+                                             uint32_t kv, uint32_t h, uint32_t slot)
+{
+    const uint64_t elem = g.fp8 ? 1 : 2;
+    return pool + static_cast<uint64_t>(page) * g.page_bytes +
+           (((static_cast<uint64_t>(l) * 2 + kv) * g.Hkv + h) * kBlockTokens + slot) * g.d * elem;
+}
+
 // One thread moves 16 bytes.  Rows are (token slot, layer, K/V, KV head) of
 // d bf16 values; slots of the last touched block past the appended tokens
 // are zero-filled.  Thread-blocks past the row range initialise the records
@@ -43,10 +81,9 @@ __global__ void append_kernel(const Geo g, const AppendArgs a, uint64_t rows_tot
         uint4 val = make_uint4(0, 0, 0, 0);
         if (rel < a.n) {
             const uint16_t *src = (kv == 0 ? a.k : a.v) + ((rel * g.L + l) * g.Hkv + h) * g.d;
-            val = __ldg(reinterpret_cast<const uint4 *>(src) + v16);
+            val = page_vec_from_bf16(g, src, v16, kv == 0 ? g.k_scale : g.v_scale);
         }
-        uint16_t *dst = a.pool + static_cast<uint64_t>(page) * (g.page_bytes / 2) +
-                        ((((static_cast<uint64_t>(l) * 2 + kv) * g.Hkv + h) * kBlockTokens + slot_in) * g.d);
+        uint8_t *dst = page_row(g, reinterpret_cast<uint8_t *>(a.pool), page, l, kv, h, slot_in);
         reinterpret_cast<uint4 *>(dst)[v16] = val;
     } else {
         const uint64_t j = tid - nvec;                  // new-block index
@@ -110,10 +147,9 @@ __global__ void append_step_kernel(const Geo g, const uint16_t *k, const uint16_
         uint4 val = make_uint4(0, 0, 0, 0);
         if (rel == 0) {
             const uint16_t *src = (kv == 0 ? k : v) + ((static_cast<size_t>(lo) * g.L + l) * g.Hkv + h) * g.d;
-            val = __ldg(reinterpret_cast<const uint4 *>(src) + v16);
+            val = page_vec_from_bf16(g, src, v16, kv == 0 ? g.k_scale : g.v_scale);
         }
-        uint16_t *dst = pool + static_cast<uint64_t>(a.page) * (g.page_bytes / 2) +
-                        ((((static_cast<uint64_t>(l) * 2 + kv) * g.Hkv + h) * kBlockTokens + slot_in) * g.d);
+        uint8_t *dst = page_row(g, reinterpret_cast<uint8_t *>(pool), a.page, l, kv, h, slot_in);
         reinterpret_cast<uint4 *>(dst)[v16] = val;
     } else {
         const uint64_t i = tid - nvec;
@@ -553,7 +589,7 @@ __global__ void copy_mass_kernel(const Geo g, const Work w, const float *src, fl
 
 cudaError_t launch_append(const Geo &g, const AppendArgs &a, cudaStream_t s)
 {
-    const uint32_t vec_per_row = g.d * 2 / 16;
+    const uint32_t vec_per_row = g.d * (g.fp8 ? 1 : 2) / 16;   // 16-byte page vectors per row
     // rows cover every slot from p0 to the end of the last touched block
     const uint64_t slots = static_cast<uint64_t>(a.first_blk + a.nblk) * kBlockTokens - a.p0;
     const uint64_t rows = slots * g.L * 2 * g.Hkv;
@@ -571,7 +607,7 @@ cudaError_t launch_append_step(const Geo &g, const uint16_t *k, const uint16_t *
                                const StepAppend *sa, uint32_t nseq, uint32_t rows_total,
                                uint64_t t_create, cudaStream_t s)
 {
-    const uint32_t vec_per_row = g.d * 2 / 16;
+    const uint32_t vec_per_row = g.d * (g.fp8 ? 1 : 2) / 16;   // 16-byte page vectors per row
     const uint64_t threads = static_cast<uint64_t>(rows_total) * vec_per_row + nseq;
     const uint32_t bs = 256;
     append_step_kernel<<<static_cast<uint32_t>((threads + bs - 1) / bs), bs, 0, s>>>(

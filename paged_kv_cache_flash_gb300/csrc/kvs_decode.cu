@@ -40,13 +40,36 @@ struct DecodeArgs {
     uint32_t wg;
 };
 
-// Bytes of one block's K and V sub-pages for one KV head.
-template <int D>
+// Bytes of one block's K and V sub-pages for one KV head.  bf16: boxes of
+// [K,V][16 tok][64 dims]; FP8 codes: one box of [K,V][16 tok][128 dims].
+template <int D, bool FP8>
 struct Tile {
-    static constexpr int kHalf = D / 64;                 // 64-wide TMA boxes
-    static constexpr int kBoxBytes = 2 * 16 * 64 * 2;    // [K,V][16 tok][64 dims] bf16
+    static constexpr int kHalf = FP8 ? 1 : D / 64;       // TMA boxes per stage
+    static constexpr int kBoxBytes = 2 * 16 * 64 * 2;    // 4 KiB either way
     static constexpr int kStageBytes = kHalf * kBoxBytes;
+    static constexpr int kBoxElems = FP8 ? 128 : 64;     // box width in elements
+    static constexpr int kWarpBytes = kStages * kStageBytes;
 };
+
+// Two E4M3 codes (low 16 bits) -> two f16 (exact), low code in the low half.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu),
+                                                     __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Head dimension of row r (0..15) of O^T m-tile mt.  bf16: 16 mt + r.  FP8:
+// m-tiles come in pairs (even, odd dims) per 32-dim group, from the V
+// fragment load below: rows 0..7 -> dims 2r, rows 8..15 -> 16 + 2(r-8).
+template <bool FP8>
+__device__ __forceinline__ uint32_t o_dim(uint32_t mt, uint32_t r)
+{
+    if constexpr (FP8)
+        return 32 * (mt >> 1) + (r < 8 ? 2 * r : 16 + 2 * (r - 8)) + (mt & 1);
+    else
+        return 16 * mt + r;
+}
 
 // A claimed work item: one chunk of blocks of one (sequence, layer, KV head)
 // stream, decoded by one warp.
@@ -127,13 +150,13 @@ __device__ __forceinline__ int32_t page_of(const Prep &p, uint32_t j)
 
 // Issues the next block of a warp's stream (items cur, then nxt) into its TMA
 // ring; false when the stream position is not known yet.  Warp-uniform.
-template <int D>
+template <int D, bool FP8>
 __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g, const Prep &cur,
                                            const Prep &nxt, bool have_nxt, bool &c_in_nxt,
                                            uint32_t &c_blk, uint32_t &k_issue, uint32_t ring_u32,
                                            uint64_t *bars, uint32_t lane)
 {
-    using T = Tile<D>;
+    using T = Tile<D, FP8>;
     if (!c_in_nxt && c_blk >= cur.it.nblk) {
         if (!have_nxt || !nxt.it.valid)
             return false;
@@ -152,8 +175,8 @@ __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g
         const int c4 = page * static_cast<int>(g.L) + static_cast<int>(l);
 #pragma unroll
         for (int h = 0; h < T::kHalf; ++h)
-            tma_load_5d(ring_u32 + st * T::kStageBytes + h * T::kBoxBytes, tmap, bar, h * 64, 0,
-                        static_cast<int>(kv), 0, c4);
+            tma_load_5d(ring_u32 + st * T::kStageBytes + h * T::kBoxBytes, tmap, bar,
+                        h * T::kBoxElems, 0, static_cast<int>(kv), 0, c4);
     }
     ++c_blk;
     ++k_issue;
@@ -164,18 +187,18 @@ __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g
 // (one KV-head stream chunk each) from a global counter, prepares the next
 // item while it computes the current one, and keeps its own TMA ring of
 // kStages blocks in flight across item boundaries.  No CTA-wide barrier.
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(256, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a)
 {
-    using T = Tile<D>;
+    using T = Tile<D, FP8>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[8][kStages];
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t ring_u32 = smem_u32(smem + warp * kStages * T::kStageBytes);
+    const uint32_t ring_u32 = smem_u32(smem + warp * T::kWarpBytes);
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s)
             mbar_init(smem_u32(&bars[warp][s]), 1);
@@ -189,7 +212,7 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t gq = lane >> 2;          // row group id in MMA fragments
     const uint32_t tq = lane & 3;           // thread in group
     const uint32_t h0 = 2 * tq, h1 = 2 * tq + 1;   // heads of this lane's S/O columns
-    const float scale_log2 = rsqrtf(static_cast<float>(D)) * kLog2e;
+    const float scale_log2 = rsqrtf(static_cast<float>(D)) * kLog2e * g.k_scale;
     const uint32_t nb_total = a.w.dset->nb_total;
     const uint32_t jm = lane >> 3, i8 = lane & 7;
 
@@ -208,14 +231,17 @@ __global__ void __launch_bounds__(256, 1)
     bool c_in_nxt = false;                  // issue cursor: item (cur / nxt) and block
     uint32_t c_blk = 0;
     if (cur.it.valid)
-        while (k_issue - k_cons < kStages && issue_next<D>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
+        while (k_issue - k_cons < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
         }
 
     while (cur.it.valid) {
         const Item it = cur.it;
         const uint32_t kvh = it.kvh;
 
-        // query fragments (B operand of S^T = K Q^T): head gq, dims 16ks+2tq(+1), +8
+        // query fragments (B operand of S^T = K Q^T), head gq.  bf16: dims
+        // 16ks+2tq(+1) and +8.  FP8: the K fragments below hold dims
+        // 16ks+4tq..+3 of a token, so the same permutation of the contracted
+        // dimension is applied here: dims 16ks+4tq(+1) and 16ks+4tq+2(+3).
         uint32_t qf[D / 16][2];
         {
             const bool valid = gq < G;
@@ -223,9 +249,16 @@ __global__ void __launch_bounds__(256, 1)
                                         (valid ? gq : 0)) * D;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                qf[ks][0] = valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 2 * tq)) : 0u;
-                qf[ks][1] =
-                    valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 8 + 2 * tq)) : 0u;
+                if constexpr (FP8) {        // bf16 pairs -> f16 pairs (the MMA's operand type)
+                    const uint2 x = valid ? __ldg(reinterpret_cast<const uint2 *>(qh + ks * 16 + 4 * tq))
+                                          : make_uint2(0u, 0u);
+                    qf[ks][0] = pack_f16(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u));
+                    qf[ks][1] = pack_f16(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
+                } else {
+                    qf[ks][0] = valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 2 * tq)) : 0u;
+                    qf[ks][1] =
+                        valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 8 + 2 * tq)) : 0u;
+                }
             }
         }
         float o[D / 16][4];
@@ -242,25 +275,53 @@ __global__ void __launch_bounds__(256, 1)
 
             // S^T = K . Q^T  (rows: 16 tokens, cols: 8 heads)
             float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t h = ks >> 2, c0 = (ks & 3) * 2;
-                const uint32_t row = i8 + 8 * (jm & 1);          // token, K half
-                const uint32_t chunk16 = c0 + (jm >> 1);
-                const uint32_t addr = base + h * T::kBoxBytes + row * 128 + ((chunk16 ^ (row & 7)) << 4);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(addr, a0, a1, a2, a3);
-                mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-            }
-            // V fragments (A operand of O^T = V^T P^T): read before the stage is refilled
+            // V fragments (A operand of O^T = V^T P^T), read before the stage is
+            // refilled; FP8 keeps the raw codes and converts them at the MMA
             uint32_t va[D / 16][4];
+            if constexpr (FP8) {
+                // K: an x4 load of 8x8 16-bit tiles over the code bytes gives lane
+                // (gq, tq) codes of dims 4tq..4tq+3 (two k-steps per load) of
+                // tokens gq (tiles 0, 2) and gq+8 (tiles 1, 3)
 #pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                const uint32_t h = mt >> 2, c0 = (mt & 3) * 2;
-                const uint32_t row = 16 + i8 + 8 * (jm >> 1);    // V half, token
-                const uint32_t chunk16 = c0 + (jm & 1);
-                const uint32_t addr = base + h * T::kBoxBytes + row * 128 + ((chunk16 ^ (row & 7)) << 4);
-                ldsm_x4_t(addr, va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+                for (int kp = 0; kp < D / 32; ++kp) {
+                    const uint32_t row = i8 + 8 * (jm & 1);
+                    const uint32_t chunk16 = 2 * kp + (jm >> 1);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(base + row * 128 + ((chunk16 ^ (row & 7)) << 4), r0, r1, r2, r3);
+                    mma_f16(s, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
+                            e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0], qf[2 * kp][1]);
+                    mma_f16(s, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                            e4m3x2_to_f16x2(r3 >> 16), qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+                }
+                // V: a transposing x4 load of 16-bit units gives lane (gq, tq),
+                // per tile, tokens 2tq, 2tq+1 x dims 2gq, 2gq+1 of a 16-dim span;
+                // tiles: tokens 0-7 / 8-15 x spans 32p / 32p+16
+#pragma unroll
+                for (int p = 0; p < D / 32; ++p) {
+                    const uint32_t row = 16 + i8 + 8 * (jm & 1);
+                    const uint32_t chunk16 = 2 * p + (jm >> 1);
+                    ldsm_x4_t(base + row * 128 + ((chunk16 ^ (row & 7)) << 4), va[2 * p][0], va[2 * p][1],
+                              va[2 * p][2], va[2 * p][3]);
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t h = ks >> 2, c0 = (ks & 3) * 2;
+                    const uint32_t row = i8 + 8 * (jm & 1);          // token, K half
+                    const uint32_t chunk16 = c0 + (jm >> 1);
+                    const uint32_t addr = base + h * T::kBoxBytes + row * 128 + ((chunk16 ^ (row & 7)) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(addr, a0, a1, a2, a3);
+                    mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                }
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const uint32_t h = mt >> 2, c0 = (mt & 3) * 2;
+                    const uint32_t row = 16 + i8 + 8 * (jm >> 1);    // V half, token
+                    const uint32_t chunk16 = c0 + (jm & 1);
+                    const uint32_t addr = base + h * T::kBoxBytes + row * 128 + ((chunk16 ^ (row & 7)) << 4);
+                    ldsm_x4_t(addr, va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+                }
             }
             const uint32_t tok0 = (it.b0 + i) * kBlockTokens + gq, tok1 = tok0 + 8;
             s[0] = tok0 < it.ntok ? s[0] * scale_log2 : -INFINITY;
@@ -278,7 +339,7 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             ++k_cons;
             if (k_issue - k_cons < kStages)
-                issue_next<D>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane);
+                issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane);
 
             const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
             const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
@@ -307,13 +368,29 @@ __global__ void __launch_bounds__(256, 1)
                 o[mt][2] *= sc0;
                 o[mt][3] *= sc1;
             }
-            // P^T as the B operand: transpose the two 8x8 bf16 tiles in registers
-            const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
-            const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
+            // P^T as the B operand: transpose the two 8x8 16-bit tiles in registers
+            const uint32_t pb0 = movmatrix_t(FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1));
+            const uint32_t pb1 = movmatrix_t(FP8 ? pack_f16(p2, p3) : pack_bf16(p2, p3));
             // O^T += V^T . P^T  (rows: d, cols: 8 heads)
+            if constexpr (FP8) {
 #pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt)
-                mma_bf16(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pb0, pb1);
+                for (int p = 0; p < D / 32; ++p) {
+                    // byte regroup: low half = dim 2gq (tokens 2tq, 2tq+1), high
+                    // half = dim 2gq+1; tiles 0/2 feed rows gq/gq+8, 1/3 tokens 8-15
+                    const uint32_t t0 = __byte_perm(va[2 * p][0], 0u, 0x3120);
+                    const uint32_t t1 = __byte_perm(va[2 * p][1], 0u, 0x3120);
+                    const uint32_t t2 = __byte_perm(va[2 * p][2], 0u, 0x3120);
+                    const uint32_t t3 = __byte_perm(va[2 * p][3], 0u, 0x3120);
+                    mma_f16(o[2 * p], e4m3x2_to_f16x2(t0), e4m3x2_to_f16x2(t2), e4m3x2_to_f16x2(t1),
+                            e4m3x2_to_f16x2(t3), pb0, pb1);
+                    mma_f16(o[2 * p + 1], e4m3x2_to_f16x2(t0 >> 16), e4m3x2_to_f16x2(t2 >> 16),
+                            e4m3x2_to_f16x2(t1 >> 16), e4m3x2_to_f16x2(t3 >> 16), pb0, pb1);
+                }
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt)
+                    mma_bf16(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pb0, pb1);
+            }
 
             if (i == 0 && !have_nxt) {
                 // while the ring streams: the next item and the claim after it
@@ -321,7 +398,7 @@ __global__ void __launch_bounds__(256, 1)
                 have_nxt = true;
                 if (lane == 0 && nxt.it.valid)
                     claimed = atomicAdd(a.w.counter, 1u);
-                while (k_issue - k_cons < kStages && issue_next<D>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
+                while (k_issue - k_cons < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
                 }
             }
         }
@@ -333,12 +410,14 @@ __global__ void __launch_bounds__(256, 1)
             a.w.part_ml[part * kMaxGroup + h1] = make_float2(m1, l1);
         }
         float *po = a.w.part_o + static_cast<size_t>(part) * kMaxGroup * D;
+        const float vs = FP8 ? g.v_scale : 1.f;     // values = codes * v_scale
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-            po[h0 * D + mt * 16 + gq] = o[mt][0];
-            po[h1 * D + mt * 16 + gq] = o[mt][1];
-            po[h0 * D + mt * 16 + gq + 8] = o[mt][2];
-            po[h1 * D + mt * 16 + gq + 8] = o[mt][3];
+            const uint32_t d0 = o_dim<FP8>(mt, gq), d1 = o_dim<FP8>(mt, gq + 8);
+            po[h0 * D + d0] = o[mt][0] * vs;
+            po[h1 * D + d0] = o[mt][1] * vs;
+            po[h0 * D + d1] = o[mt][2] * vs;
+            po[h1 * D + d1] = o[mt][3] * vs;
         }
 
         // ---- the next item becomes current ----------------------------------
@@ -356,7 +435,7 @@ __global__ void __launch_bounds__(256, 1)
         have_nxt = false;
         nxt.it.valid = 0;
         nxt.it.nblk = 0;
-        while (cur.it.valid && k_issue - k_cons < kStages && issue_next<D>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
+        while (cur.it.valid && k_issue - k_cons < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
         }
     }
 }
@@ -365,26 +444,30 @@ __global__ void __launch_bounds__(256, 1)
 
 size_t decode_smem_bytes(const Geo &g, uint32_t wg)
 {
-    const size_t stage = g.d == 128 ? Tile<128>::kStageBytes : Tile<64>::kStageBytes;
-    return wg * kStages * stage + 1024;   // + alignment slack
+    const size_t per_warp = g.fp8 ? Tile<128, true>::kWarpBytes
+                                  : (g.d == 128 ? Tile<128, false>::kWarpBytes : Tile<64, false>::kWarpBytes);
+    return wg * per_warp + 1024;   // + alignment slack
 }
 
-int decode_blocks_per_sm(const Geo &g, uint32_t wg)
+template <int D, bool FP8>
+static int occupancy(const Geo &g, uint32_t wg)
 {
     // The attribute is per kernel, shared by every context in the process:
     // always allow the largest configuration (4 warps) so that no context
     // lowers it below what another one launches with.
     int n = 0;
-    const size_t smem = decode_smem_bytes(g, wg);
-    const int smem_max = static_cast<int>(decode_smem_bytes(g, 4));
-    if (g.d == 128) {
-        cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<128>, 32 * wg, smem);
-    } else {
-        cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<64>, 32 * wg, smem);
-    }
+    cudaFuncSetAttribute(decode_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(decode_smem_bytes(g, 4)));
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, FP8>, 32 * wg,
+                                                  decode_smem_bytes(g, wg));
     return n;
+}
+
+int decode_blocks_per_sm(const Geo &g, uint32_t wg)
+{
+    if (g.fp8)
+        return occupancy<128, true>(g, wg);
+    return g.d == 128 ? occupancy<128, false>(g, wg) : occupancy<64, false>(g, wg);
 }
 
 cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w, const uint16_t *q,
@@ -393,10 +476,12 @@ cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w, 
 {
     DecodeArgs a{g, w, q, table, n_items, wg};
     const size_t smem = decode_smem_bytes(g, wg);
-    if (g.d == 128)
-        decode_kernel<128><<<grid, 32 * wg, smem, s>>>(tmap, a);
+    if (g.fp8)
+        decode_kernel<128, true><<<grid, 32 * wg, smem, s>>>(tmap, a);
+    else if (g.d == 128)
+        decode_kernel<128, false><<<grid, 32 * wg, smem, s>>>(tmap, a);
     else
-        decode_kernel<64><<<grid, 32 * wg, smem, s>>>(tmap, a);
+        decode_kernel<64, false><<<grid, 32 * wg, smem, s>>>(tmap, a);
     return cudaGetLastError();
 }
 

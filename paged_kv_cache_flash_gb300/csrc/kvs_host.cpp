@@ -226,6 +226,14 @@ int check_cfg(const kvs_config *c, kvs_ctx *ctx)
         return fail(ctx, KVS_EINVAL, "alpha must be in [0, 1] and recency_window > 0");
     if (!(c->cut_lo <= c->cut_hi))
         return fail(ctx, KVS_EINVAL, "cut_lo must not exceed cut_hi");
+    if (c->kv_dtype != KVS_KV_BF16 && c->kv_dtype != KVS_KV_FP8_E4M3)
+        return fail(ctx, KVS_EINVAL, "unknown kv_dtype %u", c->kv_dtype);
+    if (c->kv_dtype == KVS_KV_FP8_E4M3) {
+        if (c->head_dim != 128)
+            return fail(ctx, KVS_EINVAL, "FP8 pages need head_dim 128");
+        if (!(c->k_scale > 0.f && c->k_scale < 1e30f && c->v_scale > 0.f && c->v_scale < 1e30f))
+            return fail(ctx, KVS_EINVAL, "FP8 scales must be positive and finite");
+    }
     return KVS_OK;
 }
 
@@ -493,8 +501,9 @@ int kvs_required_sizes(const kvs_config *cfg, kvs_sizes *out)
         return KVS_EINVAL;
     const kvs_config &c = *cfg;
     const size_t rows = static_cast<size_t>(c.max_seqs) * c.max_blocks_per_seq;
+    const size_t elem = c.kv_dtype == KVS_KV_FP8_E4M3 ? 1 : 2;
     out->page_bytes = static_cast<size_t>(2) * c.num_layers * c.num_kv_heads * KVS_BLOCK_TOKENS *
-                      c.head_dim * 2;
+                      c.head_dim * elem;
     out->pool_bytes = out->page_bytes * c.pool_blocks;
     out->table_bytes = rows * sizeof(int32_t);
     out->records_bytes = rows * sizeof(kvs_record);
@@ -537,6 +546,9 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
     g.max_seqs = cfg->max_seqs;
     g.mb = cfg->max_blocks_per_seq;
     g.page_bytes = ctx->sz.page_bytes;
+    g.fp8 = cfg->kv_dtype == KVS_KV_FP8_E4M3 ? 1 : 0;
+    g.k_scale = g.fp8 ? cfg->k_scale : 1.f;
+    g.v_scale = g.fp8 ? cfg->v_scale : 1.f;
     ctx->wg = pick_wg(g.Hkv);
     ctx->dset.reset(new DSet());
 
@@ -555,13 +567,15 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
                                         12000, cudaEnableDefault, &qres));
     if (qres != cudaDriverEntryPointSuccess || !encode)
         return fail(ctx, KVS_ECUDA, "cuTensorMapEncodeTiled not available");
-    const cuuint64_t d = g.d;
+    // bf16: 64-element (128-byte) boxes, two per row; FP8: one 128-byte box
+    const cuuint64_t d = g.d, el = g.fp8 ? 1 : 2;
     cuuint64_t dims[5] = {d, KVS_BLOCK_TOKENS, g.Hkv, 2, static_cast<cuuint64_t>(g.L) * g.pool_blocks};
-    cuuint64_t strides[4] = {d * 2, KVS_BLOCK_TOKENS * d * 2, g.Hkv * KVS_BLOCK_TOKENS * d * 2,
-                             2ull * g.Hkv * KVS_BLOCK_TOKENS * d * 2};
-    cuuint32_t box[5] = {64, KVS_BLOCK_TOKENS, 1, 2, 1};
+    cuuint64_t strides[4] = {d * el, KVS_BLOCK_TOKENS * d * el, g.Hkv * KVS_BLOCK_TOKENS * d * el,
+                             2ull * g.Hkv * KVS_BLOCK_TOKENS * d * el};
+    cuuint32_t box[5] = {g.fp8 ? 128u : 64u, KVS_BLOCK_TOKENS, 1, 2, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult cr = encode(&ctx->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, buf->pool, dims, strides, box,
+    CUresult cr = encode(&ctx->tmap, g.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         5, buf->pool, dims, strides, box,
                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS)

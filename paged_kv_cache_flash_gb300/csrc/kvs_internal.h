@@ -58,6 +58,8 @@ struct Geo {
     uint32_t L, Hq, Hkv, d, G;
     uint32_t pool_blocks, max_seqs, mb;  // mb = max_blocks_per_seq
     uint64_t page_bytes;
+    uint32_t fp8;                        // pages hold E4M3 codes (1 byte per element)
+    float k_scale, v_scale;              // FP8: value = code * scale
 };
 
 struct Work {             // carved out of the caller's workspace buffer

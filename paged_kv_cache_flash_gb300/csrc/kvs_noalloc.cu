@@ -82,6 +82,8 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
     const uint32_t nb = (n_tokens + kBlockTokens - 1) / kBlockTokens;
     g.mb = nb;
     g.page_bytes = static_cast<uint64_t>(2) * g.L * g.Hkv * kBlockTokens * g.d * 2;
+    g.fp8 = 0;            // bf16 pages only
+    g.k_scale = g.v_scale = 1.f;
     const uint32_t wg = g.Hkv % 4 == 0 ? 4 : (g.Hkv % 2 == 0 ? 2 : 1);
     const uint32_t chunk = 64;
     const uint32_t nchunk = (nb + chunk - 1) / chunk;

@@ -49,15 +49,19 @@ class Run:
     each sequence's attention, mass and records depend on it alone."""
 
     def __init__(self, wl, alpha, *, staging_pages=8, chunk=4096, oracle_on=True,
-                 oracle_seqs=None, pool_pages=None, extra_steps=0, device="cuda"):
+                 oracle_seqs=None, pool_pages=None, extra_steps=0, device="cuda",
+                 kv_dtype=K.KVS_KV_BF16, k_scale=1.0, v_scale=1.0):
         self.wl, self.alpha = wl, alpha
         self.dev = device
         self.ids = seq_ids_for(wl)
         self.mb = wl.max_blocks_per_seq() + (extra_steps + 15) // 16
+        self.fp8 = kv_dtype == K.KVS_KV_FP8_E4M3
+        self.k_scale, self.v_scale = k_scale, v_scale
         cfg = K.make_config(wl.L, wl.Hq, wl.Hkv, wl.d, pool_pages or wl.pool_pages, max_seqs=wl.nseq,
                             max_blocks_per_seq=self.mb, alpha=alpha,
                             recency_window=wl.recency_window, weights=wl.weights, cuts=wl.cuts,
-                            pool_seed=wl.seed, staging_pages=staging_pages)
+                            pool_seed=wl.seed, staging_pages=staging_pages, kv_dtype=kv_dtype,
+                            k_scale=k_scale, v_scale=v_scale)
         self.ctx = K.Context(cfg)
         self.oracle_on = oracle_on
         track = set(range(wl.nseq)) if oracle_seqs is None else set(oracle_seqs)
@@ -158,7 +162,12 @@ class Run:
             if sid not in self.orc:
                 continue
             o = self.orc[sid]
-            r = O.decode_with_mass(q[s], o.K, o.V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d)
+            if self.fp8:       # the pages hold codes of the bf16 inputs
+                kc, vc = self.codes(o.K, o.V)
+                r = O.decode_with_mass(q[s], kc, vc, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d,
+                                       k_lut=O.e4m3_lut(self.k_scale), v_lut=O.e4m3_lut(self.v_scale))
+            else:
+                r = O.decode_with_mass(q[s], o.K, o.V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d)
             nb = len(o.rec)
             M = r["mass"]
             o.ambiguous |= np.abs(M * nb - 1.0) < TOUCH_MARGIN
@@ -218,10 +227,16 @@ class Run:
             out |= {(sid, int(b)) for b in np.nonzero(ex)[0]}
         return out
 
+    def codes(self, Kb, Vb):
+        return (O.quantize_bf16_e4m3(Kb, self.k_scale), O.quantize_bf16_e4m3(Vb, self.v_scale))
+
     def oracle_page(self, sid, b):
         o = self.orc[sid]
         B = self.wl.block_tokens
-        return O.assemble_page(o.K[b * B:(b + 1) * B], o.V[b * B:(b + 1) * B], B)
+        Kb, Vb = o.K[b * B:(b + 1) * B], o.V[b * B:(b + 1) * B]
+        if self.fp8:
+            return O.assemble_page(*self.codes(Kb, Vb), B)
+        return O.assemble_page(Kb, Vb, B)
 
     def close(self):
         self.ctx.close()

@@ -62,6 +62,12 @@ def test_record_layout_agrees_with_oracle_restatement():
         assert K.RECORD_DTYPE.fields[name][0] == O.REC_DTYPE.fields[ofield][0]
 
 
+def test_fp8_pages_are_half_size(lib):
+    cfg = K.make_config(80, 64, 8, 128, pool_blocks=16, max_seqs=1, max_blocks_per_seq=16,
+                        kv_dtype=K.KVS_KV_FP8_E4M3)
+    assert K.kvs_required_sizes(cfg).page_bytes == 5 * 2**20 // 2
+
+
 def test_required_sizes_llama70b(lib):
     cfg = K.make_config(80, 64, 8, 128, pool_blocks=8200, max_seqs=1, max_blocks_per_seq=8197)
     sz = K.kvs_required_sizes(cfg)

@@ -48,6 +48,19 @@ def test_batch16_shared_prefix_full_size():
     run.close()
 
 
+def test_fp8_8k_full_size():
+    """The 8K workload with FP8 E4M3 pages (scales 1.0), 2 steps, full oracle."""
+    wl = W.workload("l70b_8k", steps=2)
+    run = Run(wl, 0.15, kv_dtype=K.KVS_KV_FP8_E4M3)
+    host = _pinned(wl.pool_pages * run.ctx.page_bytes)
+    for _ in range(wl.steps):
+        res = run.step(host)
+        summ = run.compare(res)
+        _check_gather(run, res, host, sample=32)
+    print("fp8 8k", summ)
+    run.close()
+
+
 def test_128k_full_size():
     """1 sequence of 131,072 tokens (8,192 blocks, 40 GiB), 2 steps: outputs,
     masses and records against the full oracle; the P < 0.3 list in full and

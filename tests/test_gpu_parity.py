@@ -127,6 +127,35 @@ def test_llama70b_8k_full_size():
     run.close()
 
 
+# ------------------------------------------------------------- FP8 pages
+
+
+@pytest.mark.parametrize("scales", [(1.0, 1.0), (0.5, 0.25)])
+def test_fp8_pages_parity(scales):
+    """FP8 E4M3 pages: codes quantised on append (bit-exact against the
+    oracle's quantiser, checked through the gathered page bytes), decode over
+    the codes within the bf16 tolerances, two append paths, ragged lengths."""
+    wl = W.workload("l70b_8k", L=4, prefill_lens=(300, 1000, 17), pool_pages=100, steps=4)
+    run = Run(wl, 0.15, kv_dtype=K.KVS_KV_FP8_E4M3, k_scale=scales[0], v_scale=scales[1])
+    assert run.ctx.page_bytes == wl.page_bytes // 2
+    host = _pinned(wl.pool_pages * run.ctx.page_bytes)
+    for i in range(wl.steps):
+        res = run.step(host, batched_append=bool(i % 2))
+        summ = run.compare(res)
+        _check_gather(run, res, host)
+    run.ctx.check_device()
+    print("fp8", scales, summ)
+    run.close()
+
+
+def test_fp8_config_checks():
+    with pytest.raises(K.KvsError):
+        K.kvs_required_sizes(K.make_config(2, 8, 2, 64, 17, 1, 18, kv_dtype=K.KVS_KV_FP8_E4M3))
+    with pytest.raises(K.KvsError):
+        K.kvs_required_sizes(K.make_config(2, 16, 2, 128, 17, 1, 18, kv_dtype=K.KVS_KV_FP8_E4M3,
+                                           k_scale=0.0))
+
+
 # --------------------------------------------------------------- scoring
 
 
