@@ -51,14 +51,6 @@ struct Tile {
     static constexpr int kWarpBytes = kStages * kStageBytes;
 };
 
-// Two E4M3 codes (low 16 bits) -> two f16 (exact), low code in the low half.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
-{
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu),
-                                                     __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
-
 // Head dimension of row r (0..15) of O^T m-tile mt.  bf16: 16 mt + r.  FP8:
 // m-tiles come in pairs (even, odd dims) per 32-dim group, from the V
 // fragment load below: rows 0..7 -> dims 2r, rows 8..15 -> 16 + 2(r-8).
@@ -70,6 +62,15 @@ __device__ __forceinline__ uint32_t o_dim(uint32_t mt, uint32_t r)
     else
         return 16 * mt + r;
 }
+
+// A warp's TMA ring: blocks in flight, the stage the next issue fills, the
+// stage the consumer waits on and that stage's mbarrier phase.
+struct Ring {
+    uint32_t inflight;
+    uint32_t st_issue;
+    uint32_t st_cons;
+    uint32_t ph_cons;
+};
 
 // A claimed work item: one chunk of blocks of one (sequence, layer, KV head)
 // stream, decoded by one warp.
@@ -153,7 +154,7 @@ __device__ __forceinline__ int32_t page_of(const Prep &p, uint32_t j)
 template <int D, bool FP8>
 __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g, const Prep &cur,
                                            const Prep &nxt, bool have_nxt, bool &c_in_nxt,
-                                           uint32_t &c_blk, uint32_t &k_issue, uint32_t ring_u32,
+                                           uint32_t &c_blk, Ring &rg, uint32_t ring_u32,
                                            uint64_t *bars, uint32_t lane)
 {
     using T = Tile<D, FP8>;
@@ -169,7 +170,7 @@ __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g
     const uint32_t kv = c_in_nxt ? nxt.it.kvh : cur.it.kvh;
     const int32_t page = c_in_nxt ? page_of(nxt, c_blk) : page_of(cur, c_blk);
     if (lane == 0) {
-        const uint32_t st = k_issue % kStages;
+        const uint32_t st = rg.st_issue;
         const uint32_t bar = smem_u32(&bars[st]);
         mbar_expect_tx(bar, T::kStageBytes);
         const int c4 = page * static_cast<int>(g.L) + static_cast<int>(l);
@@ -179,7 +180,8 @@ __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g
                         h * T::kBoxElems, 0, static_cast<int>(kv), 0, c4);
     }
     ++c_blk;
-    ++k_issue;
+    ++rg.inflight;
+    rg.st_issue = rg.st_issue + 1 == kStages ? 0 : rg.st_issue + 1;
     return true;
 }
 
@@ -227,34 +229,76 @@ __global__ void __launch_bounds__(256, 1)
     nxt.it.nblk = 0;
     bool have_nxt = false;
 
-    uint32_t k_issue = 0, k_cons = 0;       // blocks issued / consumed by this warp
+    Ring rg{0, 0, 0, 0};
     bool c_in_nxt = false;                  // issue cursor: item (cur / nxt) and block
     uint32_t c_blk = 0;
     if (cur.it.valid)
-        while (k_issue - k_cons < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
+        while (rg.inflight < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane)) {
         }
 
     while (cur.it.valid) {
         const Item it = cur.it;
         const uint32_t kvh = it.kvh;
 
-        // query fragments (B operand of S^T = K Q^T), head gq.  bf16: dims
-        // 16ks+2tq(+1) and +8.  FP8: the K fragments below hold dims
-        // 16ks+4tq..+3 of a token, so the same permutation of the contracted
-        // dimension is applied here: dims 16ks+4tq(+1) and 16ks+4tq+2(+3).
+        // query fragments (B operand of S^T = K Q^T), head gq, and the scale
+        // of the logits of this lane's heads h0, h1 (log2 domain)
         uint32_t qf[D / 16][2];
+        float sl0 = scale_log2, sl1 = scale_log2;
         {
             const bool valid = gq < G;
             const uint16_t *qh = a.q + ((static_cast<size_t>(it.ci) * g.L + it.l) * g.Hq + kvh * G +
                                         (valid ? gq : 0)) * D;
+            if constexpr (FP8) {
+                // E4M3 terms: q = (q1 + q2) 2^e, e chosen per head so that
+                // the largest |q| 2^-e is in [128, 256).  A bf16 value has 8
+                // significant bits; q1 takes the top 4 (rounded) and the
+                // remainder, a multiple of the value's last bit no larger
+                // than half q1's last bit, fits q2's 4 bits exactly while
+                // that last bit is at least E4M3's 2^-9: exact for |q| at
+                // least 2^-9 of the head's largest, absolute error below
+                // 2^-16 of it otherwise.
+                // Lane holds dims 32k + 16j + 4tq .. +3 (k32 B fragment).
+                float x[D / 32][2][4];
+                float amax = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                if constexpr (FP8) {        // bf16 pairs -> f16 pairs (the MMA's operand type)
-                    const uint2 x = valid ? __ldg(reinterpret_cast<const uint2 *>(qh + ks * 16 + 4 * tq))
-                                          : make_uint2(0u, 0u);
-                    qf[ks][0] = pack_f16(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u));
-                    qf[ks][1] = pack_f16(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
-                } else {
+                for (int k = 0; k < D / 32; ++k)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const uint2 r = valid ? __ldg(reinterpret_cast<const uint2 *>(qh + 32 * k + 16 * j + 4 * tq))
+                                              : make_uint2(0u, 0u);
+                        x[k][j][0] = __uint_as_float(r.x << 16);
+                        x[k][j][1] = __uint_as_float(r.x & 0xffff0000u);
+                        x[k][j][2] = __uint_as_float(r.y << 16);
+                        x[k][j][3] = __uint_as_float(r.y & 0xffff0000u);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            amax = fmaxf(amax, fabsf(x[k][j][e]));
+                    }
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const int ex = amax > 0.f ? max(static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 134, -100)
+                                          : 0;
+                const float down = __uint_as_float(static_cast<uint32_t>(127 - ex) << 23);
+                const float up = __uint_as_float(static_cast<uint32_t>(127 + ex) << 23);
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float y[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            y[e] = x[k][j][e] * down;
+                        const uint32_t c1 = f32x4_e4m3x4(y[0], y[1], y[2], y[3]);
+                        const uint32_t b01 = e4m3x2_lo_f16x2(c1), b23 = e4m3x2_hi_f16x2(c1);
+                        qf[2 * k][j] = c1;
+                        qf[2 * k + 1][j] = f32x4_e4m3x4(y[0] - f16_lo(b01), y[1] - f16_hi(b01),
+                                                        y[2] - f16_lo(b23), y[3] - f16_hi(b23));
+                    }
+                sl0 = scale_log2 * __shfl_sync(0xffffffffu, up, 4 * h0);
+                sl1 = scale_log2 * __shfl_sync(0xffffffffu, up, 4 * h1);
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
                     qf[ks][0] = valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 2 * tq)) : 0u;
                     qf[ks][1] =
                         valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 8 + 2 * tq)) : 0u;
@@ -269,9 +313,8 @@ __global__ void __launch_bounds__(256, 1)
         float *lse_row0 = a.w.lse_blk + (static_cast<size_t>(it.l) * g.Hq + kvh * G + h0) * nb_total + it.lse0;
 
         for (uint32_t i = 0; i < it.nblk; ++i) {
-            const uint32_t st = k_cons % kStages;
-            mbar_wait(smem_u32(&bars[warp][st]), (k_cons / kStages) & 1u, a.w.err);
-            const uint32_t base = ring_u32 + st * T::kStageBytes;
+            mbar_wait(smem_u32(&bars[warp][rg.st_cons]), rg.ph_cons, a.w.err);
+            const uint32_t base = ring_u32 + rg.st_cons * T::kStageBytes;
 
             // S^T = K . Q^T  (rows: 16 tokens, cols: 8 heads)
             float s[4] = {0.f, 0.f, 0.f, 0.f};
@@ -280,19 +323,22 @@ __global__ void __launch_bounds__(256, 1)
             uint32_t va[D / 16][4];
             if constexpr (FP8) {
                 // K: an x4 load of 8x8 16-bit tiles over the code bytes gives lane
-                // (gq, tq) codes of dims 4tq..4tq+3 (two k-steps per load) of
-                // tokens gq (tiles 0, 2) and gq+8 (tiles 1, 3)
+                // (gq, tq) codes of dims 32k + 4tq..+3 of tokens gq, gq+8 and of
+                // dims 32k + 16 + 4tq..+3: the k32 E4M3 A fragment as stored.
+                // One accumulator per Q term keeps the MMA chains short.
+                float s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int kp = 0; kp < D / 32; ++kp) {
+                for (int k = 0; k < D / 32; ++k) {
                     const uint32_t row = i8 + 8 * (jm & 1);
-                    const uint32_t chunk16 = 2 * kp + (jm >> 1);
+                    const uint32_t chunk16 = 2 * k + (jm >> 1);
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4(base + row * 128 + ((chunk16 ^ (row & 7)) << 4), r0, r1, r2, r3);
-                    mma_f16(s, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
-                            e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0], qf[2 * kp][1]);
-                    mma_f16(s, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
-                            e4m3x2_to_f16x2(r3 >> 16), qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+                    mma_e4m3(s, r0, r1, r2, r3, qf[2 * k][0], qf[2 * k][1]);
+                    mma_e4m3(s2, r0, r1, r2, r3, qf[2 * k + 1][0], qf[2 * k + 1][1]);
                 }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    s[e] += s2[e];
                 // V: a transposing x4 load of 16-bit units gives lane (gq, tq),
                 // per tile, tokens 2tq, 2tq+1 x dims 2gq, 2gq+1 of a 16-dim span;
                 // tiles: tokens 0-7 / 8-15 x spans 32p / 32p+16
@@ -323,11 +369,17 @@ __global__ void __launch_bounds__(256, 1)
                     ldsm_x4_t(addr, va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
                 }
             }
-            const uint32_t tok0 = (it.b0 + i) * kBlockTokens + gq, tok1 = tok0 + 8;
-            s[0] = tok0 < it.ntok ? s[0] * scale_log2 : -INFINITY;
-            s[1] = tok0 < it.ntok ? s[1] * scale_log2 : -INFINITY;
-            s[2] = tok1 < it.ntok ? s[2] * scale_log2 : -INFINITY;
-            s[3] = tok1 < it.ntok ? s[3] * scale_log2 : -INFINITY;
+            s[0] *= sl0;
+            s[1] *= sl1;
+            s[2] *= sl0;
+            s[3] *= sl1;
+            if ((it.b0 + i + 1) * kBlockTokens > it.ntok) {      // the sequence's last block
+                const uint32_t tok0 = (it.b0 + i) * kBlockTokens + gq, tok1 = tok0 + 8;
+                s[0] = tok0 < it.ntok ? s[0] : -INFINITY;
+                s[1] = tok0 < it.ntok ? s[1] : -INFINITY;
+                s[2] = tok1 < it.ntok ? s[2] : -INFINITY;
+                s[3] = tok1 < it.ntok ? s[3] : -INFINITY;
+            }
 
             float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
 #pragma unroll
@@ -337,9 +389,13 @@ __global__ void __launch_bounds__(256, 1)
             }
             // every lane has its K and V fragments: refill the stage
             __syncwarp();
-            ++k_cons;
-            if (k_issue - k_cons < kStages)
-                issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane);
+            --rg.inflight;
+            if (++rg.st_cons == kStages) {
+                rg.st_cons = 0;
+                rg.ph_cons ^= 1u;
+            }
+            if (rg.inflight < kStages)
+                issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane);
 
             const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
             const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
@@ -381,10 +437,10 @@ __global__ void __launch_bounds__(256, 1)
                     const uint32_t t1 = __byte_perm(va[2 * p][1], 0u, 0x3120);
                     const uint32_t t2 = __byte_perm(va[2 * p][2], 0u, 0x3120);
                     const uint32_t t3 = __byte_perm(va[2 * p][3], 0u, 0x3120);
-                    mma_f16(o[2 * p], e4m3x2_to_f16x2(t0), e4m3x2_to_f16x2(t2), e4m3x2_to_f16x2(t1),
-                            e4m3x2_to_f16x2(t3), pb0, pb1);
-                    mma_f16(o[2 * p + 1], e4m3x2_to_f16x2(t0 >> 16), e4m3x2_to_f16x2(t2 >> 16),
-                            e4m3x2_to_f16x2(t1 >> 16), e4m3x2_to_f16x2(t3 >> 16), pb0, pb1);
+                    mma_f16(o[2 * p], e4m3x2_lo_f16x2(t0), e4m3x2_lo_f16x2(t2), e4m3x2_lo_f16x2(t1),
+                            e4m3x2_lo_f16x2(t3), pb0, pb1);
+                    mma_f16(o[2 * p + 1], e4m3x2_hi_f16x2(t0), e4m3x2_hi_f16x2(t2), e4m3x2_hi_f16x2(t1),
+                            e4m3x2_hi_f16x2(t3), pb0, pb1);
                 }
             } else {
 #pragma unroll
@@ -398,7 +454,7 @@ __global__ void __launch_bounds__(256, 1)
                 have_nxt = true;
                 if (lane == 0 && nxt.it.valid)
                     claimed = atomicAdd(a.w.counter, 1u);
-                while (k_issue - k_cons < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
+                while (rg.inflight < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane)) {
                 }
             }
         }
@@ -435,7 +491,7 @@ __global__ void __launch_bounds__(256, 1)
         have_nxt = false;
         nxt.it.valid = 0;
         nxt.it.nblk = 0;
-        while (cur.it.valid && k_issue - k_cons < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, k_issue, ring_u32, bars[warp], lane)) {
+        while (cur.it.valid && rg.inflight < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane)) {
         }
     }
 }

@@ -119,6 +119,53 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A.B, m16n8k32, A and B E4M3 codes (4 per register, lowest k in the
+// low byte), fp32 accumulate.  Every product of two E4M3 values is exact in
+// fp32.
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The two E4M3 codes in the low (lo) or high (hi) 16 bits of x -> two f16
+// (exact), the lower byte's value in the low half.
+__device__ __forceinline__ uint32_t e4m3x2_lo_f16x2(uint32_t x)
+{
+    uint32_t h;
+    asm("{.reg .b16 l, u;\n\tmov.b32 {l, u}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;}" : "=r"(h) : "r"(x));
+    return h;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_hi_f16x2(uint32_t x)
+{
+    uint32_t h;
+    asm("{.reg .b16 l, u;\n\tmov.b32 {l, u}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, u;}" : "=r"(h) : "r"(x));
+    return h;
+}
+
+// Four floats -> four E4M3 codes (round to nearest even, saturating), a in
+// the low byte.
+__device__ __forceinline__ uint32_t f32x4_e4m3x4(float a, float b, float c, float d)
+{
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t h2)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+}
+
+__device__ __forceinline__ float f16_hi(uint32_t h2)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
 {
     __half2 v = __floats2half2_rn(lo, hi);
