@@ -48,7 +48,11 @@ struct Tile {
     static constexpr int kBoxBytes = 2 * 16 * 64 * 2;    // 4 KiB either way
     static constexpr int kStageBytes = kHalf * kBoxBytes;
     static constexpr int kBoxElems = FP8 ? 128 : 64;     // box width in elements
-    static constexpr int kWarpBytes = kStages * kStageBytes;
+    // FP8: a shallower ring (the same bytes in flight per SM) so that three
+    // CTAs of 4 warps fit on an SM, with registers capped to match
+    static constexpr int kRing = FP8 ? 4 : kStages;
+    static constexpr int kMinCtas = FP8 ? 3 : 1;
+    static constexpr int kWarpBytes = kRing * kStageBytes;
 };
 
 // Head dimension of row r (0..15) of O^T m-tile mt.  bf16: 16 mt + r.  FP8:
@@ -181,7 +185,7 @@ __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g
     }
     ++c_blk;
     ++rg.inflight;
-    rg.st_issue = rg.st_issue + 1 == kStages ? 0 : rg.st_issue + 1;
+    rg.st_issue = rg.st_issue + 1 == T::kRing ? 0 : rg.st_issue + 1;
     return true;
 }
 
@@ -190,7 +194,7 @@ __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g
 // item while it computes the current one, and keeps its own TMA ring of
 // kStages blocks in flight across item boundaries.  No CTA-wide barrier.
 template <int D, bool FP8>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(FP8 ? 128 : 256, Tile<D, FP8>::kMinCtas)
     decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a)
 {
     using T = Tile<D, FP8>;
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(256, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_u32 = smem_u32(smem + warp * T::kWarpBytes);
     if (lane == 0) {
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < T::kRing; ++s)
             mbar_init(smem_u32(&bars[warp][s]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(256, 1)
     bool c_in_nxt = false;                  // issue cursor: item (cur / nxt) and block
     uint32_t c_blk = 0;
     if (cur.it.valid)
-        while (rg.inflight < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane)) {
+        while (rg.inflight < T::kRing && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane)) {
         }
 
     while (cur.it.valid) {
@@ -390,11 +394,11 @@ __global__ void __launch_bounds__(256, 1)
             // every lane has its K and V fragments: refill the stage
             __syncwarp();
             --rg.inflight;
-            if (++rg.st_cons == kStages) {
+            if (++rg.st_cons == T::kRing) {
                 rg.st_cons = 0;
                 rg.ph_cons ^= 1u;
             }
-            if (rg.inflight < kStages)
+            if (rg.inflight < T::kRing)
                 issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane);
 
             const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(256, 1)
                 have_nxt = true;
                 if (lane == 0 && nxt.it.valid)
                     claimed = atomicAdd(a.w.counter, 1u);
-                while (rg.inflight < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane)) {
+                while (rg.inflight < T::kRing && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane)) {
                 }
             }
         }
@@ -491,7 +495,7 @@ __global__ void __launch_bounds__(256, 1)
         have_nxt = false;
         nxt.it.valid = 0;
         nxt.it.nblk = 0;
-        while (cur.it.valid && rg.inflight < kStages && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane)) {
+        while (cur.it.valid && rg.inflight < T::kRing && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane)) {
         }
     }
 }
