@@ -21,6 +21,10 @@ Sources (page titles and sections):
         eviction and are restored on re-admission.
   [ARCH] "LLM KV cache offload" architecture page: block manager, block
         tables, reference counts for shared blocks, pinned-host staging.
+  [VA]  s.14 "Prefetching Strategy", Diagram 14.1: the prefetch targets
+        (anchor zone, recent window, high EMA); s.12 notes beside the P
+        formula: prefetch priority 1/(1 + distance/100) and the fetch-order
+        blend 0.6 rope_factor + 0.4 ema_factor.
   [RETR] "RETRACTIONS": s.3 brute-force argmin audit of victim selection.
 """
 from __future__ import annotations
@@ -419,6 +423,56 @@ class IdentityStore:
 
     def __len__(self):
         return len(self._m)
+
+
+# ---------------------------------------------------------------------------
+# prefetch order of demoted blocks ([VA] s.14 Diagram 14.1; s.12 notes)
+# ---------------------------------------------------------------------------
+
+ANCHOR_LAST_POSITION = 100    # anchor zone: token positions 0..100
+RECENT_WINDOW = 200           # recent window: positions m-200..m-1
+
+
+def prefetch_class(block_idx: int, ntok: int, block_tokens: int = 16) -> int:
+    """0 if the block holds a position of the anchor zone [0, 100], else 1 if
+    it holds a position of the recent window [m - 200, m - 1] (m = the
+    sequence's token count), else 2: the order of the three target lists."""
+    first = block_idx * block_tokens
+    last = first + block_tokens - 1
+    if first <= ANCHOR_LAST_POSITION:
+        return 0
+    if last >= ntok - RECENT_WINDOW:
+        return 1
+    return 2
+
+
+def rope_factor(distance: int) -> float:
+    """1 / (1 + distance / 100), in fp64: division, addition, division."""
+    return 1.0 / (1.0 + float(distance) / 100.0)
+
+
+def prefetch_blend(block_idx: int, ntok: int, ema_score: float, block_tokens: int = 16) -> float:
+    """0.6 rope_factor + 0.4 ema_factor.  distance = tokens between the last
+    token (position m - 1) and the block's last position (0 when the block
+    holds the last token); ema_factor = the block's EMA score E as kept in
+    its record.  fp64: two products, then their sum."""
+    last = block_idx * block_tokens + block_tokens - 1
+    distance = max(0, (ntok - 1) - last)
+    return 0.6 * rope_factor(distance) + 0.4 * float(ema_score)
+
+
+def prefetch_order(cands, budget: int, block_tokens: int = 16) -> list:
+    """Fetch order of demoted blocks: class ascending, blend descending, then
+    (seq_id, block_idx) ascending; the first `budget` entries.
+
+    cands: iterable of (seq_id, block_idx, ntok, ema_score).
+    Returns [(seq_id, block_idx, class, blend)]."""
+    rows = []
+    for seq_id, b, m, e in cands:
+        blend = min(prefetch_blend(b, m, e, block_tokens), 1.0)
+        rows.append((prefetch_class(b, m, block_tokens), -blend, int(seq_id), int(b)))
+    rows.sort()
+    return [(sid, b, c, -nb) for c, nb, sid, b in rows[:budget]]
 
 
 # ---------------------------------------------------------------------------

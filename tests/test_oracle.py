@@ -415,3 +415,88 @@ def test_quantizer_pin_catches_round_half_up(monkeypatch):
     with pytest.raises(AssertionError):
         test_e4m3_quantize_matches_torch_in_range()
     monkeypatch.setattr(O, "quantize_e4m3", good)
+
+
+# ------------------------------------------------------------- prefetch order
+# [VA] s.14 Diagram 14.1 (targets: anchor zone 0..100, recent m-200..m-1, high
+# EMA) and the s.12 notes (priority 1/(1 + distance/100); fetch-order blend
+# 0.6 rope_factor + 0.4 ema_factor).  Expected blends below are exact
+# rationals, rounded once, independent of the oracle's floating-point steps.
+
+from fractions import Fraction as _Fr
+
+
+def _blend_exact(b, m, e):
+    last = 16 * b + 15
+    dist = max(0, (m - 1) - last)
+    return float(_Fr(3, 5) / (1 + _Fr(dist, 100)) + _Fr(2, 5) * _Fr(e))
+
+
+def test_rope_factor_closed_forms():
+    assert O.rope_factor(0) == 1.0
+    assert O.rope_factor(100) == 0.5
+    assert O.rope_factor(300) == 0.25
+    assert O.rope_factor(50) == 2.0 / 3.0
+
+
+def test_prefetch_class_boundaries():
+    # block 6 holds positions 96..111 (contains 100): anchor; block 7 does not
+    assert O.prefetch_class(6, 4000) == 0 and O.prefetch_class(7, 4000) == 2
+    # m = 1000: recent window 800..999; block 49 ends at 799, block 50 starts at 800
+    assert O.prefetch_class(49, 1000) == 2 and O.prefetch_class(50, 1000) == 1
+    # short sequence: anchor wins over recent
+    assert O.prefetch_class(0, 50) == 0 and O.prefetch_class(7, 150) == 1
+
+
+_PREFETCH_CASE = [          # (seq_id, block, ntok, E)
+    (7, 0, 4000, 0.0), (7, 6, 4000, 0.5), (7, 7, 4000, 0.9), (7, 237, 4000, 0.0),
+    (7, 249, 4000, 0.01), (3, 236, 4000, 0.2), (3, 100, 4000, 0.2),
+    (9, 150, 4000, 0.1), (8, 150, 4000, 0.1),
+]
+# by hand: class 0 = {(7,6) 0.2150, (7,0) 0.0147}; class 1 = {(7,249) 0.604,
+# (7,237) 0.2055}; class 2 = {(7,7) 0.3751, (3,236) 0.2748, (3,100) 0.1042,
+# (8,150) = (9,150) 0.0756: equal blends, seq_id order}
+_PREFETCH_EXPECTED = [(7, 6, 0), (7, 0, 0), (7, 249, 1), (7, 237, 1), (7, 7, 2), (3, 236, 2),
+                      (3, 100, 2), (8, 150, 2), (9, 150, 2)]
+
+
+def test_prefetch_order_worked_example():
+    got = O.prefetch_order(_PREFETCH_CASE, 100)
+    assert [(s, b, c) for s, b, c, _ in got] == _PREFETCH_EXPECTED
+    blends = {(s, b): x for s, b, _, x in got}
+    for s, b, m, e in _PREFETCH_CASE:
+        assert abs(blends[(s, b)] - _blend_exact(b, m, e)) <= 2e-16
+    assert O.prefetch_order(_PREFETCH_CASE, 3) == got[:3]
+    assert O.prefetch_order(_PREFETCH_CASE, 0) == []
+
+
+def test_prefetch_order_invariants():
+    rng = np.random.default_rng(12)
+    cands = [(int(s), int(b), 3000 + 37 * int(s), float(rng.uniform(0, 0.05)))
+             for s in range(6) for b in rng.choice(180, 25, replace=False)]
+    ref = O.prefetch_order(cands, len(cands))
+    perm = [cands[i] for i in rng.permutation(len(cands))]
+    assert O.prefetch_order(perm, len(cands)) == ref
+    classes = [c for _, _, c, _ in ref]
+    assert classes == sorted(classes)
+    # raising one class-2 block's E to 1 brings it to the front of class 2 only
+    i2 = next(i for i, (s, b, m, e) in enumerate(cands) if O.prefetch_class(b, m) == 2)
+    boosted = list(cands)
+    s, b, m, _ = boosted[i2]
+    boosted[i2] = (s, b, m, 1.0)
+    out = O.prefetch_order(boosted, len(cands))
+    first2 = next(k for k, r in enumerate(out) if r[2] == 2)
+    assert out[first2][:2] == (s, b)
+
+
+def test_prefetch_pin_catches_swapped_weights(monkeypatch):
+    good = O.prefetch_blend
+
+    def swapped(b, m, e, block_tokens=16):
+        last = b * block_tokens + block_tokens - 1
+        return 0.4 * O.rope_factor(max(0, (m - 1) - last)) + 0.6 * float(e)
+
+    monkeypatch.setattr(O, "prefetch_blend", swapped)
+    with pytest.raises(AssertionError):
+        test_prefetch_order_worked_example()
+    monkeypatch.setattr(O, "prefetch_blend", good)
