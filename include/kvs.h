@@ -67,6 +67,7 @@ extern "C" {
 #define KVS_BLOCK_TOKENS 16u
 #define KVS_RECORD_BYTES 64u
 #define KVS_MAX_CALL_SEQS 256u   /* sequences in one decode call */
+#define KVS_PREFETCH_MAX 4096u   /* blocks in one prefetch plan */
 
 /* Opaque context: host bookkeeping of one pool (free list, reference counts,
  * block tables, identity store), its events and its upload ring. */
@@ -301,6 +302,37 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args,
  * KVS_ENOMEM if the free list runs out (nothing re-admitted). */
 int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n,
                 const void *host_src, size_t host_src_bytes, void *stream);
+
+/* Fetch order of the demoted blocks, [VA] s.14 "Prefetching Strategy"
+ * (Diagram 14.1 targets, in order: the anchor zone, token positions 0..100;
+ * the recent window, positions m-200..m-1 where m is the sequence's token
+ * count; high-EMA blocks) with the fetch priority 1/(1 + distance/100) and
+ * the fetch-order blend 0.6 rope_factor + 0.4 ema_factor named beside the
+ * [VA] s.12 priority formula.  For every demoted block of a live sequence
+ * the device computes
+ *   class = 0 if the block holds a position <= 100, else 1 if it holds a
+ *           position >= m - 200, else 2;
+ *   distance = max(0, (m - 1) - (16*block_idx + 15));
+ *   blend = min(1, 0.6 * (1 / (1 + distance/100)) + 0.4 * E)
+ * (fp64, each operation rounded in that order, no fused multiply-add; E is
+ * the record's EMA score kept since demotion) and orders the blocks by
+ * (class ascending, blend descending, seq_id ascending, block_idx
+ * ascending).  The first n = min(budget, demoted) entries are written to
+ * keys_out[n] and, if given, blend_out[n] and class_out[n] (all host).
+ * Synchronising on `stream`.  KVS_EINVAL: budget > KVS_PREFETCH_MAX or a
+ * missing output.  n_out = 0 when nothing is demoted. */
+int kvs_prefetch_plan(kvs_ctx_t *ctx, uint32_t budget, kvs_key *keys_out,
+                      double *blend_out, uint8_t *class_out, uint32_t *n_out,
+                      void *stream);
+
+/* kvs_prefetch_plan, then kvs_readmit of those blocks with their
+ * host-to-device copies issued in plan order (highest priority first) on
+ * `stream`; pass a stream other than the one decoding so that the copies
+ * run on a copy engine beside the decode kernels.  host_src and the errors
+ * are those of kvs_readmit (nothing is re-admitted on an error). */
+int kvs_prefetch(kvs_ctx_t *ctx, uint32_t budget, const void *host_src,
+                 size_t host_src_bytes, kvs_key *keys_out, double *blend_out,
+                 uint8_t *class_out, uint32_t *n_out, void *stream);
 
 /* Test hook: makes seq_ids the current set and copies mass_dev (float32
  * [nseq][max_blocks_per_seq], row i for seq_ids[i], device) into the mass

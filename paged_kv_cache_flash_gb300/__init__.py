@@ -28,6 +28,7 @@ KVS_SELECT_THRESH, KVS_SELECT_LOWFRAC = 0, 1
 KVS_KV_BF16, KVS_KV_FP8_E4M3 = 0, 1
 KVS_GATHER_DEMOTE, KVS_GATHER_MIRROR = 1, 2
 KVS_MAX_CALL_SEQS = 256
+KVS_PREFETCH_MAX = 4096
 BLOCK_TOKENS = 16
 
 c_u32, c_u64, c_i32, c_i64, c_dbl, c_sz, c_vp = (
@@ -98,6 +99,10 @@ _SIGS = {
     "kvs_select_and_gather": (ctypes.c_int, [c_vp, ctypes.POINTER(kvs_gather_args),
                                              ctypes.POINTER(kvs_gather_result)]),
     "kvs_readmit": (ctypes.c_int, [c_vp, ctypes.POINTER(kvs_key), c_u32, c_vp, c_sz, c_vp]),
+    "kvs_prefetch_plan": (ctypes.c_int, [c_vp, c_u32, ctypes.POINTER(kvs_key), ctypes.POINTER(c_dbl),
+                                         ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(c_u32), c_vp]),
+    "kvs_prefetch": (ctypes.c_int, [c_vp, c_u32, c_vp, c_sz, ctypes.POINTER(kvs_key), ctypes.POINTER(c_dbl),
+                                    ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(c_u32), c_vp]),
     "kvs_debug_set_mass": (ctypes.c_int, [c_vp, ctypes.POINTER(c_u64), c_u32, c_vp, c_vp]),
     "kvs_debug_advance": (ctypes.c_int, [c_vp, c_u64]),
     "kvs_export_records": (ctypes.c_int, [c_vp, c_u64, c_vp, c_sz, c_vp]),
@@ -303,6 +308,32 @@ class Context:
         _check(self.h, lib().kvs_readmit(self.h, arr, n, host_src.data_ptr(),
                                          host_src.numel() * host_src.element_size(),
                                          _stream_handle(stream)))
+
+    @staticmethod
+    def _plan_out(budget):
+        cap = max(budget, 1)
+        return (kvs_key * cap)(), (c_dbl * cap)(), (ctypes.c_uint8 * cap)(), c_u32(0)
+
+    @staticmethod
+    def _plan_list(keys, blend, cls, n):
+        return [(keys[i].seq_id, keys[i].block_idx, int(cls[i]), blend[i]) for i in range(n.value)]
+
+    def prefetch_plan(self, budget, stream=None):
+        """[(seq_id, block_idx, class, blend)] of the demoted blocks in fetch
+        order, at most `budget`."""
+        keys, blend, cls, n = self._plan_out(budget)
+        _check(self.h, lib().kvs_prefetch_plan(self.h, budget, keys, blend, cls, ctypes.byref(n),
+                                               _stream_handle(stream)))
+        return self._plan_list(keys, blend, cls, n)
+
+    def prefetch(self, budget, host_src, stream=None):
+        """The plan of prefetch_plan, re-admitted with copies in plan order."""
+        assert host_src.is_pinned()
+        keys, blend, cls, n = self._plan_out(budget)
+        _check(self.h, lib().kvs_prefetch(self.h, budget, host_src.data_ptr(),
+                                          host_src.numel() * host_src.element_size(), keys, blend, cls,
+                                          ctypes.byref(n), _stream_handle(stream)))
+        return self._plan_list(keys, blend, cls, n)
 
     def debug_set_mass(self, seq_ids, mass, stream=None):
         t = self.torch

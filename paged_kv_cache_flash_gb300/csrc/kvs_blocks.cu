@@ -454,6 +454,155 @@ __device__ __forceinline__ uint32_t block_scan_1024(uint32_t f, uint32_t *wsum, 
     return pos;
 }
 
+// ------------------------------------------------------------- prefetch plan
+// Order key of a demoted block: class in the top two bits (0 anchor zone,
+// 1 recent window, 2 other), then the blend descending as 1.0's bits minus
+// the blend's bits (blend in [0, 1], so the difference fits 62 bits and
+// orders exactly like the blend, reversed).
+constexpr uint64_t kOneBits = 0x3FF0000000000000ull;
+constexpr int64_t kAnchorLastPos = 100;     // anchor zone: positions 0..100
+constexpr int64_t kRecentWindow = 200;      // recent window: m-200..m-1
+
+__device__ __forceinline__ uint64_t prefetch_key(const PrefCand &c)
+{
+    const int64_t first = static_cast<int64_t>(c.block) * kBlockTokens;
+    const int64_t last = first + kBlockTokens - 1;
+    const int64_t m = c.ntok;
+    const uint64_t cls = first <= kAnchorLastPos ? 0u : (last >= m - kRecentWindow ? 1u : 2u);
+    const int64_t dist = max(static_cast<int64_t>(0), (m - 1) - last);
+    const double rope = __ddiv_rn(1.0, __dadd_rn(1.0, __ddiv_rn(static_cast<double>(dist), 100.0)));
+    const double blend = __dadd_rn(__dmul_rn(0.6, rope), __dmul_rn(0.4, c.ema));
+    uint64_t bits = static_cast<uint64_t>(__double_as_longlong(blend));
+    bits = bits > kOneBits ? kOneBits : bits;
+    return (cls << 62) | (kOneBits - bits);
+}
+
+// One block of 1024 threads: keys of the n candidates, the k-th smallest
+// (key, index) by an 8-bit radix descent (when k < n), the k smallest
+// compacted in index order, then a bitonic sort of them in shared memory.
+__global__ void __launch_bounds__(1024)
+    prefetch_plan_kernel(const PrefCand *cand, uint32_t n, uint32_t k, uint64_t *keys,
+                         uint64_t *out_key, uint32_t *out_idx)
+{
+    extern __shared__ __align__(16) uint8_t psm[];
+    uint64_t *skey = reinterpret_cast<uint64_t *>(psm);
+    uint32_t *sidx = reinterpret_cast<uint32_t *>(psm + KVS_PREFETCH_MAX * sizeof(uint64_t));
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t wsum[33];
+    __shared__ uint64_t pre_k;
+    __shared__ uint32_t pre_i, remaining, base;
+
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x)
+        keys[i] = prefetch_key(cand[i]);
+    if (threadIdx.x == 0) {
+        pre_k = 0;
+        pre_i = 0;
+        remaining = k;
+        base = 0;
+    }
+    __syncthreads();
+    uint64_t tk = ~0ull;
+    uint32_t ti = ~0u;
+    if (k < n) {
+        // 8 passes over the key bits, then 4 over the candidate index
+        for (int pass = 0; pass < 12; ++pass) {
+            for (uint32_t q = threadIdx.x; q < 256; q += blockDim.x)
+                hist[q] = 0;
+            __syncthreads();
+            const uint64_t pk = pre_k;
+            const uint32_t pi = pre_i;
+            for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+                const uint64_t key = keys[i];
+                uint32_t digit;
+                bool match;
+                if (pass < 8) {
+                    const int sh = 56 - 8 * pass;
+                    const uint64_t mask = pass == 0 ? 0ull : (~0ull << (sh + 8));
+                    match = (key & mask) == pk;
+                    digit = static_cast<uint32_t>(key >> sh) & 0xffu;
+                } else {
+                    const int sh = 24 - 8 * (pass - 8);
+                    const uint32_t mask = pass == 8 ? 0u : (~0u << (sh + 8));
+                    match = key == pk && (i & mask) == pi;
+                    digit = (i >> sh) & 0xffu;
+                }
+                if (match)
+                    atomicAdd(&hist[digit], 1u);
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                uint32_t rem = remaining, dsel = 255;
+                for (uint32_t q = 0; q < 256; ++q) {
+                    if (hist[q] >= rem) {
+                        dsel = q;
+                        break;
+                    }
+                    rem -= hist[q];
+                }
+                remaining = rem;
+                if (pass < 8)
+                    pre_k |= static_cast<uint64_t>(dsel) << (56 - 8 * pass);
+                else
+                    pre_i |= dsel << (24 - 8 * (pass - 8));
+            }
+            __syncthreads();
+        }
+        tk = pre_k;
+        ti = pre_i;
+    }
+    // the k entries with (key, index) <= (tk, ti), in index order
+    for (uint32_t t0 = 0; t0 < n; t0 += blockDim.x) {
+        const uint32_t i = t0 + threadIdx.x;
+        uint64_t key = 0;
+        uint32_t f = 0;
+        if (i < n) {
+            key = keys[i];
+            f = (key < tk || (key == tk && i <= ti)) ? 1u : 0u;
+        }
+        uint32_t tot;
+        const uint32_t pos = base + block_scan_1024(f, wsum, &tot);
+        if (f && pos < KVS_PREFETCH_MAX) {
+            skey[pos] = key;
+            sidx[pos] = i;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0)
+            base += tot;
+        __syncthreads();
+    }
+    uint32_t P = 1;
+    while (P < k)
+        P <<= 1;
+    for (uint32_t i = k + threadIdx.x; i < P; i += blockDim.x) {
+        skey[i] = ~0ull;
+        sidx[i] = ~0u;
+    }
+    __syncthreads();
+    for (uint32_t size = 2; size <= P; size <<= 1)
+        for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+            for (uint32_t i = threadIdx.x; i < P; i += blockDim.x) {
+                const uint32_t j = i ^ stride;
+                if (j > i) {
+                    const bool up = (i & size) == 0;
+                    const uint64_t ki = skey[i], kj = skey[j];
+                    const uint32_t ii = sidx[i], ij = sidx[j];
+                    const bool gt = ki > kj || (ki == kj && ii > ij);
+                    if (gt == up) {
+                        skey[i] = kj;
+                        skey[j] = ki;
+                        sidx[i] = ij;
+                        sidx[j] = ii;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    for (uint32_t i = threadIdx.x; i < k; i += blockDim.x) {
+        out_key[i] = skey[i];
+        out_idx[i] = sidx[i];
+    }
+}
+
 // Gather plan of the selected list, one block of 1024 threads:
 //  - a page is eligible when every reference to it is selected (selected
 //    references == reference count), and is planned once, at its first
@@ -637,6 +786,19 @@ cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, co
     const uint32_t ntiles = (nb_total + kSelTile - 1) / kSelTile;
     select_count_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, mode, nb_total);
     select_scatter_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, table, mode, nb_total, ntiles);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefetch_plan(const PrefCand *cand, uint32_t n, uint32_t k, uint64_t *keys,
+                                 uint64_t *out_key, uint32_t *out_idx, cudaStream_t s)
+{
+    if (k == 0 || k > KVS_PREFETCH_MAX || k > n)
+        return cudaErrorInvalidValue;
+    const int smem = KVS_PREFETCH_MAX * (sizeof(uint64_t) + sizeof(uint32_t));
+    cudaError_t e = cudaFuncSetAttribute(prefetch_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return e;
+    prefetch_plan_kernel<<<1, 1024, smem, s>>>(cand, n, k, keys, out_key, out_idx);
     return cudaGetLastError();
 }
 

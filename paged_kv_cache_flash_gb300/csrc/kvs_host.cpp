@@ -1224,19 +1224,18 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
     return KVS_OK;
 }
 
-int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n, const void *host_src,
-                size_t host_src_bytes, void *stream)
+}  // extern "C"
+
+namespace {
+
+// Re-admission of the demoted keys ks: validation, pages from the free list,
+// host-to-device copies (in host order, or in the order of ks), records and
+// table entries restored.  Nothing changes on an error.
+int readmit_keys(kvs_ctx_t *ctx, std::vector<std::pair<uint64_t, uint64_t>> ks, bool host_order,
+                 const void *host_src, size_t host_src_bytes, cudaStream_t s)
 {
-    if (!ctx)
-        return KVS_EINVAL;
-    if (n == 0)
-        return KVS_OK;
-    if (!keys || !host_src)
-        return fail(ctx, KVS_EINVAL, "keys and host_src must be given");
+    const uint32_t n = static_cast<uint32_t>(ks.size());
     const size_t pb = ctx->sz.page_bytes;
-    std::vector<std::pair<uint64_t, uint64_t>> ks(n);
-    for (uint32_t i = 0; i < n; ++i)
-        ks[i] = {keys[i].seq_id, keys[i].block_idx};
     {
         auto sorted = ks;
         std::sort(sorted.begin(), sorted.end());
@@ -1262,16 +1261,17 @@ int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n, const void *hos
     if (pages_available(ctx) < n)
         return fail(ctx, KVS_ENOMEM, "pool exhausted: %u pages needed, %zu free", n,
                     pages_available(ctx));
-    cudaStream_t s = S(stream);
     int rc = order_pool_writes(ctx, s);
     if (rc || (rc = reclaim_pages(ctx, s, n)))
         return rc;
-    // copy in host order and wait only for the D2H chunks that hold each
-    // page, so re-admission overlaps the tail of a demotion still in flight
-    std::sort(ks.begin(), ks.end(), [&](const std::pair<uint64_t, uint64_t> &x,
-                                        const std::pair<uint64_t, uint64_t> &y) {
-        return ctx->store.at(x).host_off < ctx->store.at(y).host_off;
-    });
+    // copy in host order (or the given order) and wait only for the D2H
+    // chunks that hold each page, so re-admission overlaps the tail of a
+    // demotion still in flight
+    if (host_order)
+        std::sort(ks.begin(), ks.end(), [&](const std::pair<uint64_t, uint64_t> &x,
+                                            const std::pair<uint64_t, uint64_t> &y) {
+            return ctx->store.at(x).host_off < ctx->store.at(y).host_off;
+        });
     std::vector<Patch> patches;
     std::vector<int32_t> taken;
     const uint8_t *src = static_cast<const uint8_t *>(host_src);
@@ -1366,6 +1366,139 @@ int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n, const void *hos
     }
     ctx->refcnt_dirty = true;
     return KVS_OK;
+}
+
+// Plan of kvs_prefetch_plan: the first min(budget, demoted) keys in fetch
+// order and their order keys (class << 62 | (bits(1.0) - bits(blend))).
+int prefetch_plan(kvs_ctx_t *ctx, uint32_t budget, std::vector<std::pair<uint64_t, uint64_t>> &plan,
+                  std::vector<uint64_t> &pkeys, cudaStream_t s)
+{
+    plan.clear();
+    pkeys.clear();
+    std::vector<std::pair<uint64_t, uint64_t>> keys;
+    std::vector<PrefCand> cands;
+    for (const auto &e : ctx->store) {          // (seq_id, block_idx) order
+        const SeqState *sq = find_seq(ctx, e.first.first);
+        if (!sq)
+            continue;
+        cands.push_back(PrefCand{e.second.rec.score, sq->ntok, static_cast<uint32_t>(e.first.second)});
+        keys.push_back(e.first);
+    }
+    const uint32_t n = static_cast<uint32_t>(cands.size());
+    const uint32_t k = std::min(budget, n);
+    if (k == 0)
+        return KVS_OK;
+    if (n > ctx->lay.nb_max)
+        return fail(ctx, KVS_EINVAL, "%u demoted blocks exceed the plan workspace (%u)", n, ctx->lay.nb_max);
+    // candidates in ring-slot pieces straight into the selection scratch,
+    // idle outside kvs_select_and_gather
+    PrefCand *dcand = reinterpret_cast<PrefCand *>(ctx->work.sel_recs);
+    const uint32_t per_slot = static_cast<uint32_t>(kRingSlotBytes / sizeof(PrefCand));
+    for (uint32_t off = 0; off < n; off += per_slot) {
+        const uint32_t m = std::min(per_slot, n - off);
+        RingSlot r;
+        int rc = ring_acquire(ctx, m * sizeof(PrefCand), &r);
+        if (rc)
+            return rc;
+        std::memcpy(r.host, cands.data() + off, m * sizeof(PrefCand));
+        CU(cudaMemcpyAsync(dcand + off, r.host, m * sizeof(PrefCand), cudaMemcpyHostToDevice, s));
+        if ((rc = ring_release(ctx, r, s)))
+            return rc;
+    }
+    uint64_t *dkeys = reinterpret_cast<uint64_t *>(ctx->work.sel_ids);
+    uint64_t *dout_key = dkeys + ctx->lay.nb_max;
+    uint32_t *dout_idx = ctx->work.sel_recidx;
+    int rc = launch_rc(ctx, launch_prefetch_plan(dcand, n, k, dkeys, dout_key, dout_idx, s), "prefetch plan");
+    if (rc)
+        return rc;
+    std::vector<uint32_t> idx(k);
+    pkeys.resize(k);
+    CU(cudaMemcpyAsync(pkeys.data(), dout_key, k * sizeof(uint64_t), cudaMemcpyDeviceToHost, s));
+    CU(cudaMemcpyAsync(idx.data(), dout_idx, k * sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+    CU(cudaStreamSynchronize(s));
+    plan.resize(k);
+    for (uint32_t i = 0; i < k; ++i) {
+        if (idx[i] >= n)
+            return fail(ctx, KVS_ECUDA, "prefetch plan returned index %u of %u", idx[i], n);
+        plan[i] = keys[idx[i]];
+    }
+    return KVS_OK;
+}
+
+int write_plan(const std::vector<std::pair<uint64_t, uint64_t>> &plan, const std::vector<uint64_t> &pkeys,
+               kvs_key *keys_out, double *blend_out, uint8_t *class_out, uint32_t *n_out)
+{
+    for (size_t i = 0; i < plan.size(); ++i) {
+        keys_out[i].seq_id = plan[i].first;
+        keys_out[i].block_idx = plan[i].second;
+        const uint64_t low = pkeys[i] & ((uint64_t(1) << 62) - 1);
+        if (blend_out) {
+            const uint64_t bits = 0x3FF0000000000000ull - low;
+            std::memcpy(&blend_out[i], &bits, sizeof bits);
+        }
+        if (class_out)
+            class_out[i] = static_cast<uint8_t>(pkeys[i] >> 62);
+    }
+    *n_out = static_cast<uint32_t>(plan.size());
+    return KVS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n, const void *host_src,
+                size_t host_src_bytes, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (n == 0)
+        return KVS_OK;
+    if (!keys || !host_src)
+        return fail(ctx, KVS_EINVAL, "keys and host_src must be given");
+    std::vector<std::pair<uint64_t, uint64_t>> ks(n);
+    for (uint32_t i = 0; i < n; ++i)
+        ks[i] = {keys[i].seq_id, keys[i].block_idx};
+    return readmit_keys(ctx, std::move(ks), true, host_src, host_src_bytes, S(stream));
+}
+
+int kvs_prefetch_plan(kvs_ctx_t *ctx, uint32_t budget, kvs_key *keys_out, double *blend_out,
+                      uint8_t *class_out, uint32_t *n_out, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (!keys_out || !n_out)
+        return fail(ctx, KVS_EINVAL, "keys_out and n_out must be given");
+    if (budget > KVS_PREFETCH_MAX)
+        return fail(ctx, KVS_EINVAL, "budget %u exceeds %u", budget, KVS_PREFETCH_MAX);
+    *n_out = 0;
+    std::vector<std::pair<uint64_t, uint64_t>> plan;
+    std::vector<uint64_t> pkeys;
+    int rc = prefetch_plan(ctx, budget, plan, pkeys, S(stream));
+    if (rc)
+        return rc;
+    return write_plan(plan, pkeys, keys_out, blend_out, class_out, n_out);
+}
+
+int kvs_prefetch(kvs_ctx_t *ctx, uint32_t budget, const void *host_src, size_t host_src_bytes,
+                 kvs_key *keys_out, double *blend_out, uint8_t *class_out, uint32_t *n_out, void *stream)
+{
+    if (!ctx)
+        return KVS_EINVAL;
+    if (!keys_out || !n_out || !host_src)
+        return fail(ctx, KVS_EINVAL, "keys_out, n_out and host_src must be given");
+    if (budget > KVS_PREFETCH_MAX)
+        return fail(ctx, KVS_EINVAL, "budget %u exceeds %u", budget, KVS_PREFETCH_MAX);
+    *n_out = 0;
+    cudaStream_t s = S(stream);
+    std::vector<std::pair<uint64_t, uint64_t>> plan;
+    std::vector<uint64_t> pkeys;
+    int rc = prefetch_plan(ctx, budget, plan, pkeys, s);
+    if (rc || plan.empty())
+        return rc;
+    if ((rc = readmit_keys(ctx, plan, false, host_src, host_src_bytes, s)))
+        return rc;
+    return write_plan(plan, pkeys, keys_out, blend_out, class_out, n_out);
 }
 
 int kvs_debug_set_mass(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const float *mass_dev,

@@ -99,6 +99,14 @@ struct Layout {           // byte offsets inside the workspace
     uint32_t nb_max, parts_max, tiles_max;
 };
 
+// One demoted block as the prefetch plan sees it.
+struct PrefCand {
+    double ema;         // EMA score kept in the block's record
+    uint32_t ntok;      // tokens of its sequence
+    uint32_t block;     // block index
+};
+static_assert(sizeof(PrefCand) == 16, "PrefCand is 16 bytes");
+
 Layout workspace_layout(const kvs_config &cfg);
 Work carve(const Layout &lay, void *workspace);
 
@@ -168,6 +176,8 @@ cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pag
                           uint32_t npages, uint8_t *staging, cudaStream_t s);
 cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, uint8_t *page_clean,
                          const Patch *p, uint32_t n, cudaStream_t s);
+cudaError_t launch_prefetch_plan(const PrefCand *cand, uint32_t n, uint32_t k, uint64_t *keys,
+                                 uint64_t *out_key, uint32_t *out_idx, cudaStream_t s);
 cudaError_t launch_copy_mass(const Geo &g, const Work &w, const float *src, float *mass,
                              uint32_t nseq, cudaStream_t s);
 

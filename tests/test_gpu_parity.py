@@ -262,6 +262,64 @@ def test_demote_readmit_round_trip():
     run.close()
 
 
+def test_prefetch_order_and_readmission():
+    """Demote half of the blocks, then: the device fetch order equals the
+    oracle's (keys, classes, blends bit for bit) for several budgets; a
+    budgeted prefetch re-admits exactly the plan's head with pages and
+    records restored; the rest follows; decoding resumes in parity."""
+    wl = W.workload("tiny", prefill_lens=(700, 1333, 420, 950), pool_pages=240, steps=5, skew=True)
+    run = Run(wl, 0.05)
+    for _ in range(3):
+        run.compare(run.step(None))
+    before = {sid: run.ctx.export_records(sid) for sid in run.ids}
+    pages_before = {}
+    for sid in run.ids:
+        for b, p in enumerate(run.ctx.seq_info(sid)[3]):
+            pages_before[(sid, b)] = run.ctx.page_bytes_of(p).cpu().numpy().tobytes()
+    nrec = sum(len(v) for v in before.values())
+    host = _pinned(nrec * run.ctx.page_bytes)
+    ids = torch.zeros(2 * nrec, dtype=torch.int64, device="cuda")
+    rc, r = run.ctx.select_and_gather(K.KVS_SELECT_LOWFRAC, host, frac=0.5,
+                                      flags=K.KVS_GATHER_DEMOTE, ids=ids)
+    torch.cuda.synchronize()
+    assert rc == K.KVS_OK and r.n_demoted == r.n_selected
+    demoted = [tuple(x) for x in ids.view(-1, 2)[: r.n_demoted].cpu().tolist()]
+    ntok = {sid: run.ctx.seq_info(sid)[1] for sid in run.ids}
+    score = {(sid, int(b)): float(e) for sid in run.ids
+             for b, e in zip(before[sid]["block_idx"], before[sid]["score"])}
+
+    def oracle_plan(keys, budget):
+        return O.prefetch_order([(s, b, ntok[s], score[(s, b)]) for s, b in keys], budget)
+
+    full = oracle_plan(demoted, len(demoted))
+    assert {c for _, _, c, _ in full} == {0, 1, 2}, "the case must cover every class"
+    for budget in (1, 7, 64, len(demoted), K.KVS_PREFETCH_MAX):
+        assert run.ctx.prefetch_plan(budget) == oracle_plan(demoted, budget)
+    side = torch.cuda.Stream()
+    head = run.ctx.prefetch(20, host, stream=side)
+    side.synchronize()
+    assert head == full[:20]
+    for s, b, _, _ in head:
+        p = run.ctx.seq_info(s)[3][b]
+        assert p >= 0 and run.ctx.page_bytes_of(p).cpu().numpy().tobytes() == pages_before[(s, b)]
+    rest = [k for k in demoted if k not in {(s, b) for s, b, _, _ in head}]
+    assert run.ctx.prefetch_plan(K.KVS_PREFETCH_MAX) == oracle_plan(rest, len(rest))
+    tail = run.ctx.prefetch(K.KVS_PREFETCH_MAX, host, stream=side)
+    side.synchronize()
+    assert [(s, b) for s, b, _, _ in tail] == [(s, b) for s, b, _, _ in oracle_plan(rest, len(rest))]
+    assert run.ctx.prefetch_plan(8) == []
+    for sid in run.ids:
+        assert run.ctx.export_records(sid).tobytes() == before[sid].tobytes()
+        for b, p in enumerate(run.ctx.seq_info(sid)[3]):
+            assert run.ctx.page_bytes_of(p).cpu().numpy().tobytes() == pages_before[(sid, b)]
+    with pytest.raises(K.KvsError) as e:
+        run.ctx.prefetch_plan(K.KVS_PREFETCH_MAX + 1)
+    assert e.value.code == K.KVS_EINVAL
+    for _ in range(2):
+        run.compare(run.step(None))
+    run.close()
+
+
 def test_error_paths():
     # steps only sizes the table row (7 blocks) so the append below fails on
     # the pool (1 free page), not on the row length
