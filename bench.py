@@ -44,8 +44,13 @@ def parse():
     ap.add_argument("--impl", choices=["kvs", "reference"], default="kvs")
     ap.add_argument("--workload", default="l70b_128k")
     ap.add_argument("--alpha", type=float, default=None)
-    ap.add_argument("--gather", choices=["auto", "mirror", "list", "demote", "none"], default="auto",
-                    help="auto: demote for workloads with periodic demotion, else mirror")
+    ap.add_argument("--gather", choices=["auto", "mirror", "list", "demote", "prefetch", "none"],
+                    default="auto",
+                    help="auto: demote for workloads with periodic demotion, else mirror; prefetch: "
+                         "demoted blocks come back in fetch order, a budget per step, while the "
+                         "sequences without holes decode")
+    ap.add_argument("--prefetch-budget", type=int, default=512,
+                    help="blocks re-admitted per step in prefetch mode")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="page element type: bf16, or FP8 E4M3 codes (per-tensor scale 1.0)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -178,7 +183,7 @@ def reduce_over_ranks(ms: float, nbytes: float, device=None):
 class Pipeline:
     """The hot path, driven through the public C ABI for a set of sequences."""
 
-    def __init__(self, wl, alpha, steps_total, device, gather, kv_dtype="bf16"):
+    def __init__(self, wl, alpha, steps_total, device, gather, kv_dtype="bf16", prefetch_budget=512):
         import torch
         import paged_kv_cache_flash_gb300 as K
         import workloads as W
@@ -200,15 +205,20 @@ class Pipeline:
         self.side = torch.cuda.Stream(device)
         self.out = torch.empty((wl.nseq, wl.L, wl.Hq, wl.d), dtype=torch.float32, device=device)
         self.host = None
-        self.demote_every = wl.demote_every if gather == "demote" else 0
+        self.demote_every = wl.demote_every if gather in ("demote", "prefetch") else 0
         self.steps_done = 0
         self.demoted_pages = 0
-        self.launches = 0                   # kernels of this library launched
-        self.half = 16                      # staging half-ring (32 staging pages)
+        self.prefetched_pages = 0
+        self.holes = {}                     # prefetch: seq_id -> blocks still demoted
+        self.budget = prefetch_budget
+        self.pf_stream = torch.cuda.Stream(device) if gather == "prefetch" else None
+        self.pf_done = None
+        self.active = list(range(wl.nseq))  # sequences decoded by the last step
+        self._idx = {}
         if gather in ("mirror", "list"):
             self.host = torch.empty(self.pool_pages * self.ctx.page_bytes, dtype=torch.uint8,
                                     pin_memory=True)
-        elif gather == "demote":
+        elif gather in ("demote", "prefetch"):
             k_max = int(math.floor(wl.demote_frac * (need + wl.nseq))) + 1
             self.host = torch.empty(k_max * self.ctx.page_bytes, dtype=torch.uint8, pin_memory=True)
             self.ids_dev = torch.zeros(2 * (need + wl.nseq), dtype=torch.int64, device=device)
@@ -256,20 +266,48 @@ class Pipeline:
         return kv, qs
 
     def kv_bytes_this_step(self):
-        return sum(self.ntok) * self.token_bytes   # tokens attended (after append)
+        # tokens attended (after append) by the sequences decoded this step
+        return sum(self.ntok[i] for i in self.active) * self.token_bytes
+
+    def _rows(self, x, active):
+        if len(active) == len(self.ids):
+            return x
+        key = tuple(active)
+        if key not in self._idx:
+            self._idx[key] = self.torch.tensor(active, dtype=self.torch.int64, device=self.dev)
+        return x.index_select(0, self._idx[key])
 
     def step(self, kv_row, q, ev=None, mode_flags=None):
-        K, ctx = self.K, self.ctx
-        main = self.torch.cuda.current_stream()
+        K, ctx, torch = self.K, self.ctx, self.torch
+        main = torch.cuda.current_stream()
         if ev:
             ev[0].record(main)
-        ctx.append_step(self.ids, kv_row[0], kv_row[1])
-        for s in range(len(self.ids)):
-            self.ntok[s] += 1
-        self.launches += 5                  # append_step, decode, combine, mass, score
+        paused = set()
+        if self.gather == "prefetch":
+            # blocks re-admitted by the last step are in place before anything reads them
+            if self.pf_done is not None:
+                main.wait_event(self.pf_done)
+            paused = set(self.holes)
+            if self.holes:
+                # plan first (its kernel cannot share the SMs with the decode),
+                # then the copies run on their own stream beside this step's decode
+                plan = ctx.prefetch(self.budget, self.host, stream=self.pf_stream)
+                done = torch.cuda.Event()
+                done.record(self.pf_stream)
+                self.pf_done = done
+                for sid, _, _, _ in plan:
+                    self.holes[sid] -= 1
+                self.holes = {k: v for k, v in self.holes.items() if v > 0}
+                self.prefetched_pages += len(plan)
+        active = [i for i, sid in enumerate(self.ids) if sid not in paused]
+        self.active = active
+        ids = [self.ids[i] for i in active]
+        ctx.append_step(ids, self._rows(kv_row[0], active), self._rows(kv_row[1], active))
+        for i in active:
+            self.ntok[i] += 1
         if ev:
             ev[1].record(main)
-        ctx.decode_step(self.ids, q, self.out)
+        ctx.decode_step(ids, self._rows(q, active), self.out[:len(active)])
         if ev:
             ev[2].record(main)
         ctx.score_update()
@@ -284,18 +322,19 @@ class Pipeline:
             rc, r = ctx.select_and_gather(K.KVS_SELECT_THRESH, self.host, flags=flags,
                                           side_stream=self.side)
             main.wait_stream(self.side)
-            self.launches += 3 + (0 if flags & K.KVS_GATHER_MIRROR else -(-r.n_staged // self.half))
-        elif self.demote_every and self.steps_done % self.demote_every == 0:
+        elif self.demote_every and self.steps_done % self.demote_every == 0 and not self.holes:
             # the lowest-P fraction goes to pinned host and comes back with its record
             rc, r = ctx.select_and_gather(K.KVS_SELECT_LOWFRAC, self.host, frac=self.wl.demote_frac,
                                           flags=K.KVS_GATHER_DEMOTE, ids=self.ids_dev,
                                           side_stream=self.side)
             keys = [tuple(x) for x in self.ids_dev.view(-1, 2)[: r.n_demoted].cpu().tolist()]
-            ctx.readmit(keys, self.host)        # overlaps the demotion's copies
-            main.wait_stream(self.side)
             self.demoted_pages += r.n_demoted
-            # radix select, count, scatter, plan, gather chunks, demote + readmit patches
-            self.launches += 4 + -(-r.n_staged // self.half) + 2
+            if self.gather == "demote":
+                ctx.readmit(keys, self.host)        # overlaps the demotion's copies
+                main.wait_stream(self.side)
+            else:
+                for sid, _ in keys:
+                    self.holes[sid] = self.holes.get(sid, 0) + 1
         if ev:
             ev[4].record(main)
         return r
@@ -344,7 +383,7 @@ def run_kvs(args):
     e2e_steps = 0 if args.no_e2e else K_
     lit_steps = 0 if (args.no_literal or args.gather not in ("mirror", "list")) else 2
     total = W_ + K_ + e2e_steps + lit_steps
-    pipe = Pipeline(wl, alpha, total, dev, args.gather, args.kv_dtype)
+    pipe = Pipeline(wl, alpha, total, dev, args.gather, args.kv_dtype, args.prefetch_budget)
     pipe.prefill()
     kv, qs = pipe.inputs(1, W_ + K_)
 
@@ -361,6 +400,7 @@ def run_kvs(args):
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     kv_bytes = 0
+    decoded = 0                     # sequence-steps decoded (all, unless prefetch pauses some)
     uniq_bytes = 0
     staged = 0
     shared_extra = wl.shared_prefix_tokens * (wl.nseq - 1) * pipe.token_bytes
@@ -368,20 +408,24 @@ def run_kvs(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    launches0 = pipe.launches
+    launches0 = pipe.ctx.kernel_launches()
+    prefetched0 = pipe.prefetched_pages
+    demoted0 = pipe.demoted_pages
     wall0 = time.perf_counter()
     t_start.record()
     for i in range(K_):
         pipe.ctx.set_decode_events(dec[i][0], dec[i][1])
         r = pipe.step(kv[W_ + i], qs[W_ + i], ev[i])
         kv_bytes += pipe.kv_bytes_this_step()
+        decoded += len(pipe.active)
         uniq_bytes += pipe.kv_bytes_this_step() - shared_extra
         staged += r.n_staged if r is not None else 0
-    demoted = pipe.demoted_pages
+    demoted = pipe.demoted_pages - demoted0
     t_stop.record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    launches = pipe.launches - launches0
+    launches = pipe.ctx.kernel_launches() - launches0
+    prefetched = pipe.prefetched_pages - prefetched0
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
@@ -391,7 +435,7 @@ def run_kvs(args):
 
     ms_max, bytes_all = reduce_over_ranks(ms, kv_bytes, dev)
     value = bytes_all / (ms_max / 1e3) / 1e9
-    tok_s = wl.nseq * K_ * ws / (ms_max / 1e3)
+    tok_s = decoded * ws / (ms_max / 1e3)
 
     dec_ms = [dec[i][0].elapsed_time(dec[i][1]) for i in range(K_)]
     part = {name: statistics.median(ev[i][a].elapsed_time(ev[i][b]) for i in range(K_))
@@ -482,6 +526,7 @@ def run_kvs(args):
                                    + (f", {wl.shared_prefix_tokens}-token shared prefix" if wl.shared_prefix_tokens else ""),
                        "global_batch": wl.nseq, "seq_len": max(wl.prefill_lens),
                        "alpha": alpha, "gather": args.gather,
+                       **({"prefetch_budget": args.prefetch_budget} if args.gather == "prefetch" else {}),
                        "l2": "inputs larger than L2 (KV per step >> 129 MB), no flush",
                        "parallelism": f"replicas x{ws}"},
             "decode_tok_per_s": round(tok_s, 2),
@@ -502,6 +547,7 @@ def run_kvs(args):
                                           max(part["decode_step"], 1e-9), 2),
             "gathered_pages_timed": staged,
             "demoted_and_readmitted_pages_timed": demoted,
+            "prefetched_pages_timed": prefetched if args.gather == "prefetch" else None,
             "e2e": e2e,
             "literal_gather": literal,
             "cpu_baseline": cpu,

@@ -328,8 +328,11 @@ int kvs_prefetch_plan(kvs_ctx_t *ctx, uint32_t budget, kvs_key *keys_out,
 /* kvs_prefetch_plan, then kvs_readmit of those blocks with their
  * host-to-device copies issued in plan order (highest priority first) on
  * `stream`; pass a stream other than the one decoding so that the copies
- * run on a copy engine beside the decode kernels.  host_src and the errors
- * are those of kvs_readmit (nothing is re-admitted on an error). */
+ * run on a copy engine beside the decode kernels.  The re-admitted blocks
+ * are in place once `stream` reaches the end of this call: make the
+ * decoding stream wait for it (an event) before it decodes their
+ * sequences.  host_src and the errors are those of kvs_readmit (nothing is
+ * re-admitted on an error). */
 int kvs_prefetch(kvs_ctx_t *ctx, uint32_t budget, const void *host_src,
                  size_t host_src_bytes, kvs_key *keys_out, double *blend_out,
                  uint8_t *class_out, uint32_t *n_out, void *stream);
@@ -391,6 +394,10 @@ int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads,
                        const int32_t *block_table, uint32_t n_tokens,
                        const void *q, float *out, float *mass, void *stream,
                        char *msg, size_t msg_bytes);
+
+/* Kernels this context has launched so far (every kernel of the library,
+ * counted at launch). */
+uint64_t kvs_kernel_launches(const kvs_ctx_t *ctx);
 
 /* Decode steps completed so far (the step counter t). */
 uint64_t kvs_step_count(const kvs_ctx_t *ctx);

@@ -112,6 +112,7 @@ _SIGS = {
     "kvs_decode_noalloc": (ctypes.c_int, [c_u32, c_u32, c_u32, c_u32, c_vp, c_u32, c_vp, c_u32,
                                           c_vp, c_vp, c_vp, c_vp, ctypes.c_char_p, c_sz]),
     "kvs_step_count": (c_u64, [c_vp]),
+    "kvs_kernel_launches": (c_u64, [c_vp]),
     "kvs_free_pages": (c_u32, [c_vp]),
     "kvs_check_device": (ctypes.c_int, [c_vp, c_vp]),
 }
@@ -370,6 +371,9 @@ class Context:
 
     def step_count(self) -> int:
         return lib().kvs_step_count(self.h)
+
+    def kernel_launches(self) -> int:
+        return lib().kvs_kernel_launches(self.h)
 
     def free_pages(self) -> int:
         return lib().kvs_free_pages(self.h)

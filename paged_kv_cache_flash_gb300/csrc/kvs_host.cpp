@@ -97,6 +97,7 @@ struct kvs_ctx {
     cudaEvent_t ev_quarantine{};                    // after the gathers reading them
     bool side_pending = false, release_pending = false;
 
+    uint64_t kernel_launches = 0;                   // kernels launched by this context
     std::string err;
 };
 
@@ -336,10 +337,11 @@ int upload_set(kvs_ctx *ctx, const DSet &ds, cudaStream_t s)
     return ring_release(ctx, r, s);
 }
 
-int launch_rc(kvs_ctx *ctx, cudaError_t e, const char *what)
+int launch_rc(kvs_ctx *ctx, cudaError_t e, const char *what, uint32_t kernels = 1)
 {
     if (e != cudaSuccess)
         return fail(ctx, KVS_ECUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+    ctx->kernel_launches += kernels;
     return KVS_OK;
 }
 
@@ -1055,7 +1057,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         if ((rc = launch_rc(ctx,
                             launch_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
                                           static_cast<const int32_t *>(ctx->buf.block_table), args->mode, N, s),
-                            "select")))
+                            "select", 2)))
             return rc;
         if ((rc = launch_rc(ctx, launch_plan(w, mirror ? 1u : 0u, s), "plan")))
             return rc;
@@ -1324,6 +1326,21 @@ int readmit_keys(kvs_ctx_t *ctx, std::vector<std::pair<uint64_t, uint64_t>> ks, 
             while (j < ks.size() && j - i < R && ctx->store.at(ks[j]).host_off == off0 + (j - i) * pb)
                 ++j;
             const uint32_t n = static_cast<uint32_t>(j - i);
+            if (n == 1) {       // a lone page goes straight into its pool page
+                if ((rc = wait_chunks(ctx->store.at(ks[i]).chunk, ctx->store.at(ks[i]).chunk))) {
+                    undo();
+                    return rc;
+                }
+                const cudaError_t e = cudaMemcpyAsync(
+                    static_cast<uint8_t *>(ctx->buf.pool) + static_cast<size_t>(taken[i]) * pb, src + off0, pb,
+                    cudaMemcpyHostToDevice, s);
+                if (e != cudaSuccess) {
+                    undo();
+                    return fail(ctx, KVS_ECUDA, "readmit copy: %s", cudaGetErrorString(e));
+                }
+                i = j;
+                continue;
+            }
             if ((rc = wait_chunks(ctx->store.at(ks[i]).chunk, ctx->store.at(ks[j - 1]).chunk)) ||
                 (rc = [&]() -> int {
                     CU(cudaMemcpyAsync(buf, src + off0, static_cast<size_t>(n) * pb, cudaMemcpyHostToDevice, s));
@@ -1584,6 +1601,11 @@ int kvs_set_decode_events(kvs_ctx_t *ctx, void *ev_start, void *ev_stop)
     ctx->ev_dec_start = static_cast<cudaEvent_t>(ev_start);
     ctx->ev_dec_stop = static_cast<cudaEvent_t>(ev_stop);
     return KVS_OK;
+}
+
+uint64_t kvs_kernel_launches(const kvs_ctx_t *ctx)
+{
+    return ctx ? ctx->kernel_launches : 0;
 }
 
 uint64_t kvs_step_count(const kvs_ctx_t *ctx) { return ctx ? ctx->t : 0; }
