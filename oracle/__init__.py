@@ -25,7 +25,9 @@ Sources (page titles and sections):
         (anchor zone, recent window, high EMA); s.12 notes beside the P
         formula: prefetch priority 1/(1 + distance/100) and the fetch-order
         blend 0.6 rope_factor + 0.4 ema_factor.
-  [RETR] "RETRACTIONS": s.3 brute-force argmin audit of victim selection.
+  [RETR] "RETRACTIONS": s.3 brute-force argmin audit of victim selection;
+        the lazily decayed EMA and its order-preserving key
+        K = ln S_touch + t_touch*(-ln(1-alpha)).
 """
 from __future__ import annotations
 
@@ -230,15 +232,16 @@ def quantize_bf16_e4m3(bits, scale: float) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # 64-byte per-block record ([GQA]: 16 B identity key, 8 B score, 8 B touch
 # timestamp, 4 B touch count, reserved).  The reserved bytes carry the tier,
-# the last priority and the last mass so that every step can be compared.
+# the last priority, the last mass and the event-driven (LRFU) score at the
+# last touch, so that every step can be compared.
 # ---------------------------------------------------------------------------
 
 REC_DTYPE = np.dtype({
     "names": ["seq_id", "block_idx", "score", "last_touch", "count", "tier",
-              "flags", "pad0", "prio", "mass", "rsv"],
+              "flags", "pad0", "prio", "mass", "rsv", "lrfu"],
     "formats": ["<u8", "<u8", "<f8", "<u8", "<u4", "u1", "u1", "<u2", "<f8",
-                "<f4", ("u1", 12)],
-    "offsets": [0, 8, 16, 24, 32, 36, 37, 38, 40, 48, 52],
+                "<f4", ("u1", 4), "<f8"],
+    "offsets": [0, 8, 16, 24, 32, 36, 37, 38, 40, 48, 52, 56],
     "itemsize": 64,
 })
 TIER_UNSCORED = 255
@@ -260,6 +263,48 @@ def ema(prev: np.ndarray, attn: np.ndarray, alpha: float) -> np.ndarray:
     Evaluated as (alpha*attn) + ((1.0-alpha)*prev) in fp64."""
     a = np.float64(alpha)
     return a * np.asarray(attn, np.float64) + (np.float64(1.0) - a) * np.asarray(prev, np.float64)
+
+
+def lrfu_decay(alpha: float, dt) -> np.ndarray:
+    """(1 - alpha)^dt for integer dt >= 0 by binary exponentiation in fp64:
+    result = 1, base = 1 - alpha; for each bit of dt from the lowest: if set,
+    result = result * base; then base = base * base."""
+    dt = np.asarray(dt, np.int64).copy()
+    base = np.full(dt.shape, np.float64(1.0) - np.float64(alpha))
+    res = np.ones(dt.shape, np.float64)
+    while np.any(dt > 0):
+        odd = (dt & 1) == 1
+        res = np.where(odd, res * base, res)
+        base = base * base
+        dt >>= 1
+    return res
+
+
+def lrfu_touch(S_prev, t_prev, t: int, alpha: float) -> np.ndarray:
+    """Event-driven score of a block touched at step t ([RETR] s.3 lazy
+    decay; the [VA] s.11 EMA of the touch indicator x: score_t = alpha*x_t +
+    (1-alpha)*score_{t-1}, with x = 0 between touches).  S_prev is the score
+    right after the previous touch at t_prev (0 and the creation step for a
+    block never touched): S = alpha + (1-alpha)^(t - t_prev) * S_prev, the
+    product first."""
+    d = lrfu_decay(alpha, np.int64(t) - np.asarray(t_prev, np.int64))
+    return np.float64(alpha) + d * np.asarray(S_prev, np.float64)
+
+
+def lrfu_decayed(S_touch, t_touch, t: int, alpha: float) -> np.ndarray:
+    """The score at step t of a block last touched at t_touch: S_touch *
+    (1-alpha)^(t - t_touch)."""
+    return np.asarray(S_touch, np.float64) * lrfu_decay(alpha, np.int64(t) - np.asarray(t_touch, np.int64))
+
+
+def lrfu_key(S_touch, t_touch, alpha: float) -> np.ndarray:
+    """[RETR] s.3 order-preserving key K = ln S_touch + t_touch*(-ln(1-alpha)):
+    ln of the decayed score at any t is K + t*ln(1-alpha), so K orders the
+    blocks as the decayed score does, at every t (-inf for S_touch = 0)."""
+    S = np.asarray(S_touch, np.float64)
+    with np.errstate(divide="ignore"):
+        lnS = np.log(S)
+    return lnS + np.asarray(t_touch, np.float64) * -np.log1p(-np.float64(alpha))
 
 
 def recency(t: int, last_touch: np.ndarray, W: int) -> np.ndarray:
@@ -289,8 +334,9 @@ def score_update(rec: np.ndarray, mass: np.ndarray, t: int, alpha: float,
 
     mass: the step's M(b), float64 (or float32, widened exactly).
     Order: EMA -> touch (mass >= 1/num_blocks: M*nb >= 1, count += 1,
-    last_touch = t) -> recency R -> anchor N (block 0 and the newest block)
-    -> P -> tier.  Returns a new record array.
+    the event-driven score by lrfu_touch, last_touch = t) -> recency R ->
+    anchor N (block 0 and the newest block) -> P -> tier.  Returns a new
+    record array.
     """
     r = rec.copy()
     nb = len(r)
@@ -299,6 +345,7 @@ def score_update(rec: np.ndarray, mass: np.ndarray, t: int, alpha: float,
     r["score"] = ema(r["score"], M, alpha)
     touched = M * np.float64(nb) >= 1.0
     r["count"] = r["count"] + touched.astype(np.uint32)
+    r["lrfu"] = np.where(touched, lrfu_touch(r["lrfu"], r["last_touch"], t, alpha), r["lrfu"])
     r["last_touch"] = np.where(touched, np.uint64(t), r["last_touch"])
     R = recency(t, r["last_touch"], W)
     N = np.zeros(nb, np.float64)
@@ -341,6 +388,30 @@ def select_lowfrac(recs_by_seq: dict, frac: float) -> list:
     allr = _ordered(recs_by_seq)
     k = lowfrac_k(len(allr), frac)
     order = sorted(range(len(allr)), key=lambda i: (float(allr["prio"][i]), i))
+    chosen = sorted(order[:k])
+    return [(int(allr["seq_id"][i]), int(allr["block_idx"][i])) for i in chosen]
+
+
+def select_lrfu(recs_by_seq: dict, frac: float, alpha: float) -> list:
+    """The k = floor(frac*N) records of smallest LRFU key (lrfu_key of the
+    score at the last touch and last_touch), ties broken by (seq_id,
+    block_idx); returned in ascending (seq_id, block_idx) order."""
+    allr = _ordered(recs_by_seq)
+    k = lowfrac_k(len(allr), frac)
+    K = lrfu_key(allr["lrfu"], allr["last_touch"], alpha)
+    order = sorted(range(len(allr)), key=lambda i: (float(K[i]), i))
+    chosen = sorted(order[:k])
+    return [(int(allr["seq_id"][i]), int(allr["block_idx"][i])) for i in chosen]
+
+
+def lrfu_victims_brute_force(recs_by_seq: dict, frac: float, t: int, alpha: float) -> list:
+    """[RETR] s.3 audit: the k = floor(frac*N) records of smallest decayed
+    score at step t, each computed directly (lrfu_decayed), ties broken by
+    (seq_id, block_idx); ascending (seq_id, block_idx)."""
+    allr = _ordered(recs_by_seq)
+    k = lowfrac_k(len(allr), frac)
+    S = lrfu_decayed(allr["lrfu"], allr["last_touch"], t, alpha)
+    order = sorted(range(len(allr)), key=lambda i: (float(S[i]), i))
     chosen = sorted(order[:k])
     return [(int(allr["seq_id"][i]), int(allr["block_idx"][i])) for i in chosen]
 

@@ -500,3 +500,123 @@ def test_prefetch_pin_catches_swapped_weights(monkeypatch):
     with pytest.raises(AssertionError):
         test_prefetch_order_worked_example()
     monkeypatch.setattr(O, "prefetch_blend", good)
+
+
+# ------------------------------------------------------------ LRFU lazy decay
+# [RETR] s.3: event-driven EMA with lazy decay and the order-preserving key
+# K = ln S_touch + t_touch*(-ln(1-alpha)), audited against a brute-force
+# argmin of the decayed scores.
+
+import heapq as _heapq
+
+
+def test_lrfu_decay_closed_forms():
+    assert O.lrfu_decay(0.15, 0)[()] == 1.0
+    assert O.lrfu_decay(0.15, 1)[()] == 1.0 - 0.15
+    assert O.lrfu_decay(0.5, 10)[()] == 2.0 ** -10
+    dts = np.arange(0, 3000, 7)
+    # each squaring doubles the relative error: about 2^12 ulp at dt < 4096
+    np.testing.assert_allclose(O.lrfu_decay(0.05, dts), (1.0 - 0.05) ** dts.astype(np.float64), rtol=1e-12)
+
+
+def test_lrfu_lazy_equals_dense_ema_of_touches():
+    rng = np.random.default_rng(21)
+    nb, T, alpha = 40, 400, 0.05
+    x = rng.random((T + 1, nb)) < rng.uniform(0.01, 0.3, nb)   # sparse touch streams
+    dense = np.zeros(nb)
+    S = np.zeros(nb)
+    tt = np.zeros(nb, np.int64)
+    for t in range(1, T + 1):
+        dense = O.ema(dense, x[t].astype(np.float64), alpha)
+        hit = x[t]
+        S = np.where(hit, O.lrfu_touch(S, tt, t, alpha), S)
+        tt = np.where(hit, t, tt)
+        if t % 37 == 0:
+            np.testing.assert_allclose(O.lrfu_decayed(S, tt, t, alpha), dense, rtol=1e-11, atol=0)
+
+
+def test_lrfu_key_orders_like_decayed_score_at_every_time():
+    rng = np.random.default_rng(22)
+    alpha = 0.15
+    S = rng.uniform(0.01, 1.0, 500)
+    tt = rng.integers(0, 200, 500)
+    K = O.lrfu_key(S, tt, alpha)
+    for t in (200, 230, 400):
+        dec = O.lrfu_decayed(S, tt, t, alpha)
+        assert np.array_equal(np.argsort(K, kind="stable"), np.argsort(dec, kind="stable"))
+    assert O.lrfu_key(np.array([0.0]), np.array([5]), alpha)[0] == -np.inf
+
+
+def _lrfu_recs(rng, nseq=3, nb=60, T=120, alpha=0.15):
+    out = {}
+    for s in range(nseq):
+        r = O.new_records(10 + s, 0, nb, 0)
+        for t in range(1, T + 1):
+            M = rng.dirichlet(np.full(nb, 0.3))
+            r = O.score_update(r, M, t, alpha)
+        out[10 + s] = r
+    return out
+
+
+def test_lrfu_selection_matches_brute_force_audit():
+    rng = np.random.default_rng(23)
+    recs = _lrfu_recs(rng)
+    for frac in (0.02, 0.1, 0.5):
+        got = O.select_lrfu(recs, frac, 0.15)
+        assert got == O.lrfu_victims_brute_force(recs, frac, 120, 0.15)
+        assert got == O.lrfu_victims_brute_force(recs, frac, 500, 0.15)
+        assert len(got) == O.lowfrac_k(180, frac)
+
+
+def test_score_update_keeps_lrfu_score_of_touches():
+    a = 0.15
+    r = O.new_records(1, 0, 2, 0)
+    # block 0 touched at steps 1 and 4, block 1 never (M*nb >= 1 decides)
+    for t, M in ((1, [0.9, 0.1]), (2, [0.2, 0.8]), (3, [0.3, 0.7]), (4, [0.6, 0.4])):
+        r = O.score_update(r, np.array(M), t, a)
+    assert r["lrfu"][0] == a + (1 - a) ** 3 * a
+    assert r["lrfu"][1] == a + (1 - a) ** 1 * a      # touched at 2 and 3
+    assert r["last_touch"].tolist() == [4, 3]
+
+
+def _evict_all(S, tt, t, alpha, picker):
+    """Evicts every block one by one at step t; counts victims that are not
+    the brute-force argmin of the decayed score among those left."""
+    left = set(range(len(S)))
+    wrong = 0
+    dec = O.lrfu_decayed(S, tt, t, alpha)
+    for victim in picker(S, tt, t, alpha):
+        best = min(left, key=lambda i: (dec[i], i))
+        wrong += victim != best
+        left.discard(victim)
+    return wrong
+
+
+def _heap_stale_high(S, tt, t, alpha):
+    # the retracted revision-1 rule: entries keyed by the score when pushed;
+    # a popped entry is pushed back only if its recomputed score is higher
+    h = [(float(S[i]), i) for i in range(len(S))]
+    _heapq.heapify(h)
+    while h:
+        stored, i = _heapq.heappop(h)
+        now = float(O.lrfu_decayed(S[i:i + 1], tt[i:i + 1], t, alpha)[0])
+        if now > stored:
+            _heapq.heappush(h, (now, i))
+            continue
+        yield i
+
+
+def _heap_order_key(S, tt, t, alpha):
+    K = O.lrfu_key(S, tt, alpha)
+    h = [(float(K[i]), i) for i in range(len(S))]
+    _heapq.heapify(h)
+    while h:
+        yield _heapq.heappop(h)[1]
+
+
+def test_brute_force_audit_catches_the_stale_high_heap():
+    rng = np.random.default_rng(24)
+    S = rng.uniform(0.05, 1.0, 300)
+    tt = rng.integers(0, 400, 300)
+    assert _evict_all(S, tt, 400, 0.15, _heap_order_key) == 0
+    assert _evict_all(S, tt, 400, 0.15, _heap_stale_high) > 100
