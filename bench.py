@@ -51,6 +51,9 @@ def parse():
                          "sequences without holes decode")
     ap.add_argument("--prefetch-budget", type=int, default=512,
                     help="blocks re-admitted per step in prefetch mode")
+    ap.add_argument("--victims", choices=["lowfrac", "lrfu"], default="lowfrac",
+                    help="demotion victims: smallest P, or smallest LRFU key (lazily decayed "
+                         "EMA of touches)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="page element type: bf16, or FP8 E4M3 codes (per-tensor scale 1.0)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -183,7 +186,8 @@ def reduce_over_ranks(ms: float, nbytes: float, device=None):
 class Pipeline:
     """The hot path, driven through the public C ABI for a set of sequences."""
 
-    def __init__(self, wl, alpha, steps_total, device, gather, kv_dtype="bf16", prefetch_budget=512):
+    def __init__(self, wl, alpha, steps_total, device, gather, kv_dtype="bf16", prefetch_budget=512,
+                 victims="lowfrac"):
         import torch
         import paged_kv_cache_flash_gb300 as K
         import workloads as W
@@ -211,6 +215,7 @@ class Pipeline:
         self.prefetched_pages = 0
         self.holes = {}                     # prefetch: seq_id -> blocks still demoted
         self.budget = prefetch_budget
+        self.victim_mode = K.KVS_SELECT_LRFU if victims == "lrfu" else K.KVS_SELECT_LOWFRAC
         self.pf_stream = torch.cuda.Stream(device) if gather == "prefetch" else None
         self.pf_done = None
         self.active = list(range(wl.nseq))  # sequences decoded by the last step
@@ -324,7 +329,7 @@ class Pipeline:
             main.wait_stream(self.side)
         elif self.demote_every and self.steps_done % self.demote_every == 0 and not self.holes:
             # the lowest-P fraction goes to pinned host and comes back with its record
-            rc, r = ctx.select_and_gather(K.KVS_SELECT_LOWFRAC, self.host, frac=self.wl.demote_frac,
+            rc, r = ctx.select_and_gather(self.victim_mode, self.host, frac=self.wl.demote_frac,
                                           flags=K.KVS_GATHER_DEMOTE, ids=self.ids_dev,
                                           side_stream=self.side)
             keys = [tuple(x) for x in self.ids_dev.view(-1, 2)[: r.n_demoted].cpu().tolist()]
@@ -383,7 +388,7 @@ def run_kvs(args):
     e2e_steps = 0 if args.no_e2e else K_
     lit_steps = 0 if (args.no_literal or args.gather not in ("mirror", "list")) else 2
     total = W_ + K_ + e2e_steps + lit_steps
-    pipe = Pipeline(wl, alpha, total, dev, args.gather, args.kv_dtype, args.prefetch_budget)
+    pipe = Pipeline(wl, alpha, total, dev, args.gather, args.kv_dtype, args.prefetch_budget, args.victims)
     pipe.prefill()
     kv, qs = pipe.inputs(1, W_ + K_)
 
@@ -527,6 +532,7 @@ def run_kvs(args):
                        "global_batch": wl.nseq, "seq_len": max(wl.prefill_lens),
                        "alpha": alpha, "gather": args.gather,
                        **({"prefetch_budget": args.prefetch_budget} if args.gather == "prefetch" else {}),
+                       **({"victims": args.victims} if args.gather in ("demote", "prefetch") else {}),
                        "l2": "inputs larger than L2 (KV per step >> 129 MB), no flush",
                        "parallelism": f"replicas x{ws}"},
             "decode_tok_per_s": round(tok_s, 2),

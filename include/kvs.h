@@ -95,7 +95,8 @@ typedef enum kvs_kv_dtype {
 
 typedef enum kvs_select_mode {
     KVS_SELECT_THRESH = 0,   /* every record with P < cut_lo (tier 2) */
-    KVS_SELECT_LOWFRAC = 1   /* the floor(frac*N) records with smallest P */
+    KVS_SELECT_LOWFRAC = 1,  /* the floor(frac*N) records with smallest P */
+    KVS_SELECT_LRFU = 2      /* the floor(frac*N) records with smallest LRFU key */
 } kvs_select_mode;
 
 /* kvs_gather_args.flags */
@@ -152,7 +153,7 @@ typedef struct kvs_key {
 
 /* The 64-byte per-block state [GQA]: 16 B identity key, 8 B score, 8 B touch
  * timestamp, 4 B touch count, then reserved bytes, which hold the tier, the
- * last priority and the last mass. */
+ * last priority, the last mass and the event-driven (LRFU) score. */
 typedef struct kvs_record {
     kvs_key key;          /*  0 */
     double score;         /* 16  EMA of the block mass, 0 at creation        */
@@ -163,7 +164,9 @@ typedef struct kvs_record {
     uint16_t pad0;        /* 38                                              */
     double prio;          /* 40  last P                                      */
     float mass;           /* 48  last block mass M                           */
-    uint8_t reserved[12]; /* 52                                              */
+    uint8_t reserved[4];  /* 52                                              */
+    double lrfu;          /* 56  event-driven score right after the last
+                           *     touch (0 if never touched), [RETR] s.3      */
 } kvs_record;
 
 typedef struct kvs_gather_args {
@@ -261,12 +264,17 @@ int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
                     const void *q_dev, float *out_dev, void *stream);
 
 /* Scores every block of the last decode set [VA] s.11, s.12, [GQA]:
- *   E <- alpha*M + (1-alpha)*E;  if M*num_blocks >= 1: count += 1,
+ *   E <- alpha*M + (1-alpha)*E;  if M*num_blocks >= 1 (a touch):
+ *   count += 1, lrfu <- alpha + (1-alpha)^(t - last_touch) * lrfu,
  *   last_touch = t;  R = clip(1 - (t - last_touch)/W, 0, 1);
  *   N = 1 for block 0 and the newest block, else 0;
  *   P = w_recency*R + w_ema*E + w_anchor*N;
  *   tier = 0 if P >= cut_hi, 1 if cut_lo <= P < cut_hi, 2 if P < cut_lo.
- * fp64 with no fused multiply-add, in that order. */
+ * fp64 with no fused multiply-add, in that order.  lrfu is the EMA of the
+ * touch indicator, decayed lazily ([RETR] s.3): its value at any step t is
+ * lrfu * (1-alpha)^(t - last_touch); the power is taken by binary
+ * exponentiation (result = 1, base = 1-alpha; per bit of the exponent from
+ * the lowest: if set result *= base; base *= base). */
 int kvs_score_update(kvs_ctx_t *ctx, void *stream);
 
 /* Changes alpha for later score updates. */
@@ -280,6 +288,12 @@ int kvs_set_alpha(kvs_ctx_t *ctx, double alpha);
  *   LOWFRAC: the floor(frac*N) records of smallest (P, seq_id, block_idx)
  *            over all N records of the set, listed ascending (seq_id,
  *            block_idx).
+ *   LRFU   : as LOWFRAC with the order-preserving key of [RETR] s.3,
+ *            K = ln(lrfu) + last_touch * (-ln(1 - alpha)) (-inf when lrfu
+ *            is 0), in place of P: the records whose lazily decayed LRFU
+ *            score is smallest at any step (the device's log, so keys equal
+ *            to within an ulp may order either way).  KVS_EINVAL if
+ *            alpha >= 1.
  * A page is eligible when every record that references it is in the list
  * (a shared page is released only by its last user); each eligible page is
  * gathered once, at the position of its first record.  Default: eligible

@@ -25,6 +25,7 @@ KVS_OK, KVS_EINVAL, KVS_ENOMEM, KVS_ECUDA, KVS_ENOTFOUND, KVS_EEXIST, KVS_ETRUNC
 STATUS_NAMES = ["OK", "EINVAL", "ENOMEM", "ECUDA", "ENOTFOUND", "EEXIST", "ETRUNC",
                 "ETIMEOUT", "EDEVICE"]
 KVS_SELECT_THRESH, KVS_SELECT_LOWFRAC = 0, 1
+KVS_SELECT_LRFU = 2
 KVS_KV_BF16, KVS_KV_FP8_E4M3 = 0, 1
 KVS_GATHER_DEMOTE, KVS_GATHER_MIRROR = 1, 2
 KVS_MAX_CALL_SEQS = 256
@@ -76,9 +77,9 @@ class kvs_gather_result(ctypes.Structure):
 # The 64-byte record of include/kvs.h (kvs_record), as a numpy dtype.
 RECORD_DTYPE = np.dtype({
     "names": ["seq_id", "block_idx", "score", "last_touch", "count", "tier", "flags", "pad0",
-              "prio", "mass", "reserved"],
-    "formats": ["<u8", "<u8", "<f8", "<u8", "<u4", "u1", "u1", "<u2", "<f8", "<f4", ("u1", 12)],
-    "offsets": [0, 8, 16, 24, 32, 36, 37, 38, 40, 48, 52],
+              "prio", "mass", "reserved", "lrfu"],
+    "formats": ["<u8", "<u8", "<f8", "<u8", "<u4", "u1", "u1", "<u2", "<f8", "<f4", ("u1", 4), "<f8"],
+    "offsets": [0, 8, 16, 24, 32, 36, 37, 38, 40, 48, 52, 56],
     "itemsize": 64,
 })
 

@@ -198,6 +198,19 @@ struct ScoreArgs {
     uint32_t W;
 };
 
+// (1 - alpha)^dt by binary exponentiation: result = 1, base = 1 - alpha; per
+// bit of dt from the lowest, if set result *= base; then base *= base.
+__device__ __forceinline__ double lrfu_decay(double alpha, uint64_t dt)
+{
+    double base = __dsub_rn(1.0, alpha), res = 1.0;
+    for (; dt; dt >>= 1) {
+        if (dt & 1u)
+            res = __dmul_rn(res, base);
+        base = __dmul_rn(base, base);
+    }
+    return res;
+}
+
 // One thread per record of the decode set (record order: ascending seq_id,
 // then block).  fp64, every operation rounded on its own (no fused
 // multiply-add), in the order: EMA, touch, recency, anchor, P, tier.
@@ -221,9 +234,11 @@ __global__ void score_kernel(const Geo g, const Work w, kvs_record *recs, const 
     const double M = static_cast<double>(mass[idx]);
     // E <- alpha*M + (1 - alpha)*E
     const double E = __dadd_rn(__dmul_rn(sa.alpha, M), __dmul_rn(__dsub_rn(1.0, sa.alpha), rec.score));
-    // touch: mass at or above the uniform share 1/num_blocks
+    // touch: mass at or above the uniform share 1/num_blocks; the
+    // event-driven score decays lazily from the previous touch
     if (__dmul_rn(M, static_cast<double>(sq.nb)) >= 1.0) {
         rec.count += 1;
+        rec.lrfu = __dadd_rn(sa.alpha, __dmul_rn(lrfu_decay(sa.alpha, t - rec.last_touch), rec.lrfu));
         rec.last_touch = t;
     }
     const double age = static_cast<double>(t - rec.last_touch);
@@ -258,19 +273,32 @@ __device__ __forceinline__ const kvs_record &rec_at(const Geo &g, const DSet *ds
     return recs[static_cast<size_t>(sq.slot) * g.mb + b];
 }
 
+// 64-bit order key of a record for LOWFRAC (P >= 0: its bits order like P)
+// and LRFU (K = ln lrfu + last_touch * c with c = -ln(1 - alpha), mapped to
+// bits that order like K: negative values complemented, others with the
+// top bit set).
+__device__ __forceinline__ uint64_t sel_key(int mode, const kvs_record &rec, double c)
+{
+    if (mode != KVS_SELECT_LRFU)
+        return static_cast<uint64_t>(__double_as_longlong(rec.prio));
+    const double K = __dadd_rn(log(rec.lrfu), __dmul_rn(static_cast<double>(rec.last_touch), c));
+    const uint64_t u = static_cast<uint64_t>(__double_as_longlong(K));
+    return (u >> 63) ? ~u : (u | (uint64_t(1) << 63));
+}
+
 __device__ __forceinline__ bool picked(int mode, const kvs_record &rec, uint32_t r,
-                                       const uint64_t *thr)
+                                       const uint64_t *thr, double c)
 {
     if (mode == KVS_SELECT_THRESH)
         return rec.tier == 2;
-    // composite key (P bits, record index); P >= 0 so its bits order like P
-    const uint64_t pb = static_cast<uint64_t>(__double_as_longlong(rec.prio));
+    // composite key (order key, record index)
+    const uint64_t pb = sel_key(mode, rec, c);
     return pb < thr[0] || (pb == thr[0] && r <= thr[1]);
 }
 
 // Counts picked records per tile of kSelTile records.
 __global__ void __launch_bounds__(kSelThreads)
-    select_count_kernel(const Geo g, const Work w, const kvs_record *recs, int mode,
+    select_count_kernel(const Geo g, const Work w, const kvs_record *recs, int mode, double lrfu_c,
                         uint32_t nb_total)
 {
     __shared__ uint32_t wsum[kSelThreads / 32];
@@ -280,7 +308,7 @@ __global__ void __launch_bounds__(kSelThreads)
         const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
         if (r < nb_total) {
             uint32_t slot, b;
-            c += picked(mode, rec_at(g, ds, recs, r, &slot, &b), r, w.sel_thr) ? 1u : 0u;
+            c += picked(mode, rec_at(g, ds, recs, r, &slot, &b), r, w.sel_thr, lrfu_c) ? 1u : 0u;
         }
     }
     for (int x = 16; x > 0; x >>= 1)
@@ -299,7 +327,7 @@ __global__ void __launch_bounds__(kSelThreads)
 // Writes picked records in record order: key, page and record index.
 __global__ void __launch_bounds__(kSelThreads)
     select_scatter_kernel(const Geo g, const Work w, const kvs_record *recs, const int32_t *table,
-                          int mode, uint32_t nb_total, uint32_t ntiles)
+                          int mode, double lrfu_c, uint32_t nb_total, uint32_t ntiles)
 {
     __shared__ uint32_t wpre[kSelThreads / 32];
     __shared__ uint32_t base_sh;
@@ -321,7 +349,7 @@ __global__ void __launch_bounds__(kSelThreads)
         pk[q] = false;
         if (r < nb_total) {
             const kvs_record &rec = rec_at(g, ds, recs, r, &slots[q], &bs[q], &nts[q]);
-            pk[q] = picked(mode, rec, r, w.sel_thr);
+            pk[q] = picked(mode, rec, r, w.sel_thr, lrfu_c);
             keys[q] = rec.key;
         }
         c += pk[q] ? 1u : 0u;
@@ -354,11 +382,11 @@ __global__ void __launch_bounds__(kSelThreads)
     }
 }
 
-// k-th smallest composite key (prio bits, record index), k >= 1, by an 8-bit
-// radix descent over the 96-bit key.  One block of 1024 threads.
+// k-th smallest composite key (order key of the mode, record index), k >= 1,
+// by an 8-bit radix descent over the 96-bit key.  One block of 1024 threads.
 __global__ void __launch_bounds__(1024)
     radix_select_kernel(const Geo g, const Work w, const kvs_record *recs, uint32_t nb_total,
-                        uint32_t k)
+                        uint32_t k, int mode, double c)
 {
     __shared__ uint32_t hist[256];
     __shared__ uint64_t pre_p;
@@ -380,7 +408,7 @@ __global__ void __launch_bounds__(1024)
         for (uint32_t r = threadIdx.x; r < nb_total; r += blockDim.x) {
             uint32_t slot, b;
             const kvs_record &rec = rec_at(g, ds, recs, r, &slot, &b);
-            const uint64_t pbits = static_cast<uint64_t>(__double_as_longlong(rec.prio));
+            const uint64_t pbits = sel_key(mode, rec, c);
             uint32_t digit;
             bool match;
             if (pass < 8) {
@@ -774,18 +802,18 @@ cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const flo
 }
 
 cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *rec,
-                                uint32_t nb_total, uint32_t k, cudaStream_t s)
+                                uint32_t nb_total, uint32_t k, int mode, double c, cudaStream_t s)
 {
-    radix_select_kernel<<<1, 1024, 0, s>>>(g, w, rec, nb_total, k);
+    radix_select_kernel<<<1, 1024, 0, s>>>(g, w, rec, nb_total, k, mode, c);
     return cudaGetLastError();
 }
 
 cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table,
-                          int mode, uint32_t nb_total, cudaStream_t s)
+                          int mode, double c, uint32_t nb_total, cudaStream_t s)
 {
     const uint32_t ntiles = (nb_total + kSelTile - 1) / kSelTile;
-    select_count_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, mode, nb_total);
-    select_scatter_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, table, mode, nb_total, ntiles);
+    select_count_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, mode, c, nb_total);
+    select_scatter_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, table, mode, c, nb_total, ntiles);
     return cudaGetLastError();
 }
 

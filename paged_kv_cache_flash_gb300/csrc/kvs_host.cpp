@@ -1015,13 +1015,15 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
     const bool mirror = args->flags & KVS_GATHER_MIRROR, demote = args->flags & KVS_GATHER_DEMOTE;
     if (mirror && demote)
         return fail(ctx, KVS_EINVAL, "DEMOTE works in list mode only");
-    if (args->mode != KVS_SELECT_THRESH && args->mode != KVS_SELECT_LOWFRAC)
+    if (args->mode != KVS_SELECT_THRESH && args->mode != KVS_SELECT_LOWFRAC && args->mode != KVS_SELECT_LRFU)
         return fail(ctx, KVS_EINVAL, "unknown selection mode %d", args->mode);
     const size_t pb = ctx->sz.page_bytes;
     if (mirror && (!args->host_dst || args->host_dst_bytes < pb * ctx->cfg.pool_blocks))
         return fail(ctx, KVS_EINVAL, "MIRROR needs host_dst of pool_blocks pages");
-    if (args->mode == KVS_SELECT_LOWFRAC && !(args->frac >= 0.0 && args->frac <= 1.0))
+    if (args->mode != KVS_SELECT_THRESH && !(args->frac >= 0.0 && args->frac <= 1.0))
         return fail(ctx, KVS_EINVAL, "frac must be in [0, 1]");
+    if (args->mode == KVS_SELECT_LRFU && !(ctx->cfg.alpha < 1.0))
+        return fail(ctx, KVS_EINVAL, "LRFU needs alpha < 1 (the key slope -ln(1-alpha) is infinite)");
     cudaStream_t s = S(args->stream);
     cudaStream_t side = args->side_stream ? S(args->side_stream) : s;
     const uint32_t N = ctx->dset->nb_total;
@@ -1041,13 +1043,15 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         ctx->refcnt_dirty = false;
     }
     bool run = true;
-    if (args->mode == KVS_SELECT_LOWFRAC) {
+    // LRFU key slope: -ln(1 - alpha)
+    const double lrfu_c = -std::log1p(-ctx->cfg.alpha);
+    if (args->mode != KVS_SELECT_THRESH) {
         const uint32_t k = static_cast<uint32_t>(std::floor(args->frac * static_cast<double>(N)));
         if (k == 0)
             run = false;
         else if ((rc = launch_rc(ctx,
                                  launch_radix_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
-                                                     N, k, s),
+                                                     N, k, args->mode, lrfu_c, s),
                                  "radix select")))
             return rc;
     }
@@ -1056,7 +1060,8 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
     if (run) {
         if ((rc = launch_rc(ctx,
                             launch_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
-                                          static_cast<const int32_t *>(ctx->buf.block_table), args->mode, N, s),
+                                          static_cast<const int32_t *>(ctx->buf.block_table), args->mode, lrfu_c,
+                                          N, s),
                             "select", 2)))
             return rc;
         if ((rc = launch_rc(ctx, launch_plan(w, mirror ? 1u : 0u, s), "plan")))

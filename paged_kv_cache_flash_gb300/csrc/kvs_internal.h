@@ -165,10 +165,9 @@ cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const flo
                          double alpha, uint32_t W, double wR, double wE, double wN,
                          double lo, double hi, uint32_t nb_total, cudaStream_t s);
 cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *rec,
-                                uint32_t nb_total, uint32_t k, cudaStream_t s);
-cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec,
-                          const int32_t *table, int mode, uint32_t nb_total,
-                          cudaStream_t s);
+                                uint32_t nb_total, uint32_t k, int mode, double c, cudaStream_t s);
+cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table,
+                          int mode, double c, uint32_t nb_total, cudaStream_t s);
 cudaError_t launch_plan(const Work &w, uint32_t mirror, cudaStream_t s);
 cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *pages, uint32_t npages,
                            uint16_t *pool, cudaStream_t s);

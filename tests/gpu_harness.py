@@ -213,6 +213,7 @@ class Run:
             assert np.array_equal(g["tier"][keep], o["tier"][keep]), f"tier mismatch seq {sid}"
             assert np.array_equal(g["count"][keep], o["count"][keep]), f"count mismatch seq {sid}"
             assert np.array_equal(g["last_touch"][keep], o["last_touch"][keep])
+            assert np.array_equal(g["lrfu"][keep], o["lrfu"][keep]), f"lrfu mismatch seq {sid}"
         assert summ["out_max_abs"] <= OUT_TOL, summ
         assert summ["mass_max_abs"] <= MASS_TOL, summ
         if check_records:

@@ -38,10 +38,10 @@ def test_struct_layouts_match_header(tmp_path):
     src = tmp_path / "sz.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "kvs.h"\n'
-        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu %zu\\n\","
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\\n\","
         "sizeof(kvs_config), sizeof(kvs_sizes), sizeof(kvs_buffers), sizeof(kvs_key),"
         "sizeof(kvs_record), sizeof(kvs_gather_args), sizeof(kvs_gather_result),"
-        "offsetof(kvs_record, prio), offsetof(kvs_record, mass));return 0;}\n")
+        "offsetof(kvs_record, prio), offsetof(kvs_record, mass), offsetof(kvs_record, lrfu));return 0;}\n")
     exe = tmp_path / "sz"
     subprocess.run(["gcc", "-I", str(ROOT / "include"), str(src), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
@@ -49,7 +49,7 @@ def test_struct_layouts_match_header(tmp_path):
     exp = [ctypes.sizeof(K.kvs_config), ctypes.sizeof(K.kvs_sizes), ctypes.sizeof(K.kvs_buffers),
            ctypes.sizeof(K.kvs_key), K.RECORD_DTYPE.itemsize, ctypes.sizeof(K.kvs_gather_args),
            ctypes.sizeof(K.kvs_gather_result), K.RECORD_DTYPE.fields["prio"][1],
-           K.RECORD_DTYPE.fields["mass"][1]]
+           K.RECORD_DTYPE.fields["mass"][1], K.RECORD_DTYPE.fields["lrfu"][1]]
     assert got == exp
 
 
@@ -57,7 +57,7 @@ def test_record_layout_agrees_with_oracle_restatement():
     import oracle as O
     for name, ofield in [("seq_id", "seq_id"), ("block_idx", "block_idx"), ("score", "score"),
                          ("last_touch", "last_touch"), ("count", "count"), ("tier", "tier"),
-                         ("flags", "flags"), ("prio", "prio"), ("mass", "mass")]:
+                         ("flags", "flags"), ("prio", "prio"), ("mass", "mass"), ("lrfu", "lrfu")]:
         assert K.RECORD_DTYPE.fields[name][1] == O.REC_DTYPE.fields[ofield][1]
         assert K.RECORD_DTYPE.fields[name][0] == O.REC_DTYPE.fields[ofield][0]
 

@@ -203,6 +203,11 @@ def test_scoring_bit_exact_on_injected_mass(alpha, cuts):
             _, r = run.ctx.select_and_gather(K.KVS_SELECT_LOWFRAC, frac=0.25, ids=ids)
             got = [tuple(x) for x in ids.view(-1, 2)[: r.n_selected].cpu().tolist()]
             assert got == O.select_lowfrac(recs, 0.25)
+            if alpha < 1.0:     # LRFU victims: key order and the brute-force audit
+                _, r = run.ctx.select_and_gather(K.KVS_SELECT_LRFU, frac=0.25, ids=ids)
+                got = [tuple(x) for x in ids.view(-1, 2)[: r.n_selected].cpu().tolist()]
+                assert got == O.select_lrfu(recs, 0.25, alpha)
+                assert got == O.lrfu_victims_brute_force(recs, 0.25, t, alpha)
     if alpha == 0.0:     # blocks sat exactly on both cuts at some step
         assert {0, 1, 2} <= seen
     run.close()
