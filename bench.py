@@ -452,7 +452,7 @@ def run_kvs(args):
     algo = kv_bytes / K_ + wl.nseq * wl.L * wl.Hq * wl.d * 2 + sum(nb) * 4
     achieved = algo / (dec_avg / 1e3) / 1e9
     peak, peak_src = read_peaks()
-    traffic = read_traffic(args.workload) if args.kv_dtype == "bf16" else None
+    traffic = read_traffic(args.workload + ("" if args.kv_dtype == "bf16" else "_fp8"))
 
     # ---- end to end through host buffers --------------------------------
     e2e = None
