@@ -25,6 +25,9 @@ Sources (page titles and sections):
         (anchor zone, recent window, high EMA); s.12 notes beside the P
         formula: prefetch priority 1/(1 + distance/100) and the fetch-order
         blend 0.6 rope_factor + 0.4 ema_factor.
+  [KIVI] "Fitting a Million Tokens" s.02 "Quantize the cache": E4M3 pages;
+        2-bit keys per channel in 32-token groups, values per token, fp16
+        scale and zero per group, an unquantised residual window.
   [RETR] "RETRACTIONS": s.3 brute-force argmin audit of victim selection;
         the lazily decayed EMA and its order-preserving key
         K = ln S_touch + t_touch*(-ln(1-alpha)).
@@ -76,6 +79,10 @@ def _load():
             P, P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, P, P, P]
         lib.orc_decode_heads_u8.restype = ctypes.c_int
+        lib.orc_decode_heads_f32.argtypes = [
+            P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, P, P, P]
+        lib.orc_decode_heads_f32.restype = ctypes.c_int
         lib.orc_aggregate_mass.argtypes = [P, ctypes.c_int64, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, P]
         lib.orc_aggregate_mass.restype = None
@@ -114,15 +121,20 @@ def decode(q, K, V, *, L, Hq, Hkv, d, block_tokens=16, heads=None,
            threads=None, want_out=True, want_head_mass=True, k_lut=None, v_lut=None):
     """Decode attention of one sequence.
 
-    q: [L][Hq][d] bf16; K, V: [n][L][Hkv][d] bf16 in logical token order, or
-    uint8 codes with k_lut / v_lut (256 values each, e.g. e4m3_lut(scale)).
+    q: [L][Hq][d] bf16; K, V: [n][L][Hkv][d] bf16 in logical token order,
+    float32 numpy arrays (values), or uint8 codes with k_lut / v_lut (256
+    values each, e.g. e4m3_lut(scale)).
     heads: iterable of flat l*Hq+h indices (None = all, in order).
     Returns dict(out [nh][d], lse [nh], head_mass [nh][nb] or None).
     """
     lib = _load()
     coded = k_lut is not None
+    f32 = isinstance(K, np.ndarray) and K.dtype == np.float32
     qb = _u16(q)
-    if coded:
+    if f32:
+        kb = np.ascontiguousarray(K)
+        vb = np.ascontiguousarray(np.asarray(V, np.float32))
+    elif coded:
         kb = np.ascontiguousarray(np.asarray(K, np.uint8))
         vb = np.ascontiguousarray(np.asarray(V, np.uint8))
         lk = np.ascontiguousarray(np.asarray(k_lut, np.float64))
@@ -140,7 +152,10 @@ def decode(q, K, V, *, L, Hq, Hkv, d, block_tokens=16, heads=None,
     hm = np.zeros((nh, nb), np.float64) if want_head_mass else None
     hp = _ptr(hl) if hl is not None else None
     nt = int(threads or os.cpu_count() or 1)
-    if coded:
+    if f32:
+        rc = lib.orc_decode_heads_f32(_ptr(qb), _ptr(kb), _ptr(vb), n, L, Hq, Hkv, d,
+                                      block_tokens, hp, nh, nt, _ptr(out), _ptr(lse), _ptr(hm))
+    elif coded:
         rc = lib.orc_decode_heads_u8(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(lk), _ptr(lv), n, L, Hq,
                                      Hkv, d, block_tokens, hp, nh, nt, _ptr(out), _ptr(lse), _ptr(hm))
     else:
@@ -227,6 +242,165 @@ def quantize_e4m3(x, scale: float) -> np.ndarray:
 def quantize_bf16_e4m3(bits, scale: float) -> np.ndarray:
     """quantize_e4m3 of bf16 bit patterns (a torch bf16 tensor or uint16)."""
     return quantize_e4m3(bf16_to_f64(_u16(bits)).astype(np.float32), scale)
+
+
+# ---------------------------------------------------------------------------
+# KIVI-style 2-bit groups ([KIVI] s.02 "Quantize the cache": keys per channel
+# in groups of 32 tokens, two 16-token blocks; values per token in groups of
+# 32 channels; asymmetric, an fp16 scale and zero per group; the newest ~128
+# tokens stay unquantised, the boundary snapped down to a whole group)
+# ---------------------------------------------------------------------------
+
+KIVI_GROUP = 32
+KIVI_RESIDUAL = 128
+KIVI_TILE_BYTES = 3072      # one (layer, KV head) of a 32-token group, d = 128
+
+
+def kivi_quantized_tokens(n: int, residual: int = KIVI_RESIDUAL, group: int = KIVI_GROUP) -> int:
+    """Tokens in whole quantised groups: every group of 32 that ends at least
+    `residual` tokens before the end, group * floor(max(0, n - residual) / group)."""
+    return group * (max(0, n - residual) // group)
+
+
+def kivi_quant(x):
+    """Asymmetric 2-bit quantisation along the last axis (one group).
+
+    x: float32 (bf16 values widened exactly).  In fp32, rounded as written:
+    mn, mx = min, max; scale = fp16(fp32(mx - mn) / 3); zero = fp16(mn);
+    code = clamp(rint(fp32(x - zero) / scale), 0, 3) (ties to even), 0 where
+    scale is 0.  Returns (codes uint8, scale f16, zero f16)."""
+    x = np.asarray(x, np.float32)
+    mn = x.min(axis=-1)
+    mx = x.max(axis=-1)
+    scale = ((mx - mn) / np.float32(3.0)).astype(np.float16)
+    zero = mn.astype(np.float16)
+    sf = scale.astype(np.float32)[..., None]
+    zf = zero.astype(np.float32)[..., None]
+    t = x - zf
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = np.where(sf > 0, t / np.where(sf > 0, sf, np.float32(1.0)), np.float32(0.0))
+    codes = np.clip(np.rint(u), 0, 3).astype(np.uint8)
+    return codes, scale, zero
+
+
+def kivi_dequant(codes, scale, zero) -> np.ndarray:
+    """fp16(code * scale + zero), one rounding (the product and sum are exact
+    in fp64).  scale and zero broadcast over the group axis (last)."""
+    v = (np.asarray(codes, np.float64) * np.asarray(scale, np.float64)[..., None]
+         + np.asarray(zero, np.float64)[..., None])
+    return v.astype(np.float16)
+
+
+def kivi_quant_k(Kg):
+    """Keys of one group, [32][L][Hkv][d] (bf16 bits or float32): per
+    channel over the 32 tokens.  Returns codes [32][L][Hkv][d], scale and
+    zero [L][Hkv][d]."""
+    x = _as_f32(Kg)
+    c, s, z = kivi_quant(np.moveaxis(x, 0, -1))
+    return np.moveaxis(c, -1, 0), s, z
+
+
+def kivi_quant_v(Vg):
+    """Values of one group, [32][L][Hkv][d]: per token over groups of 32
+    channels.  Returns codes [32][L][Hkv][d], scale and zero
+    [32][L][Hkv][d/32]."""
+    x = _as_f32(Vg)
+    n, L, H, d = x.shape
+    c, s, z = kivi_quant(x.reshape(n, L, H, d // KIVI_GROUP, KIVI_GROUP))
+    return c.reshape(n, L, H, d), s, z
+
+
+def _as_f32(x) -> np.ndarray:
+    if isinstance(x, np.ndarray) and x.dtype == np.float32:
+        return x
+    return bf16_to_f64(_u16(x)).astype(np.float32)
+
+
+def kivi_effective(K, V):
+    """K, V of one sequence ([n][L][Hkv][d] bf16) as attention sees them
+    under the 2-bit scheme: tokens before kivi_quantized_tokens(n)
+    dequantised from their groups, the rest as stored.  float32 arrays."""
+    Kf, Vf = _as_f32(K).copy(), _as_f32(V).copy()
+    n = Kf.shape[0]
+    for a in range(0, kivi_quantized_tokens(n), KIVI_GROUP):
+        b = a + KIVI_GROUP
+        ck, sk, zk = kivi_quant_k(Kf[a:b])
+        Kf[a:b] = np.moveaxis(kivi_dequant(np.moveaxis(ck, 0, -1), sk, zk), -1, 0).astype(np.float32)
+        cv, sv, zv = kivi_quant_v(Vf[a:b])
+        n_, L, H, d = cv.shape
+        Vf[a:b] = kivi_dequant(cv.reshape(n_, L, H, d // KIVI_GROUP, KIVI_GROUP), sv, zv) \
+            .reshape(n_, L, H, d).astype(np.float32)
+    return Kf, Vf
+
+
+def kivi_group_tile(ck, sk, zk, cv, sv, zv) -> bytes:
+    """Bytes of one (layer, KV head) of a group page (d = 128), the layout a
+    warp of the decode kernel reads (lane = 4*g + t, g = lane // 4, t = lane % 4):
+
+      K codes  [0, 1024)   : [block j][lane][word w in 0..3]; word w holds the
+                             16 codes of token 16j + g + 8*(w // 2), dims
+                             32t + 16*(w % 2) + i, code i at bits 2i.
+      V codes  [1024, 2048): [block j][lane][word w]; pair i (0..7) of word w
+                             is m = 2w + i // 4, e = i % 4: dim 16m + g +
+                             8*(e % 2), token 16j + 2t + 8*(e // 2) at bits 2i
+                             and the next token at bits 16 + 2i.
+      K meta   [2048, 2560): [t][half h in 0..1][i in 0..7] of (scale pair,
+                             zero pair), each pair two fp16: channel
+                             32t + 16h + i (low), that channel + 8 (high).
+      V meta   [2560, 3072): [block j][token pair p in 0..7][channel group
+                             c in 0..3] of (scale pair, zero pair): tokens
+                             16j + 2p (low) and 16j + 2p + 1 (high).
+
+    ck, cv: codes [32][d]; sk, zk: [d]; sv, zv: [32][d/32]."""
+    ck = np.asarray(ck, np.uint32)
+    cv = np.asarray(cv, np.uint32)
+    kc = np.zeros((2, 32, 4), np.uint32)
+    vc = np.zeros((2, 32, 4), np.uint32)
+    for j in range(2):
+        for lane in range(32):
+            g, t = lane // 4, lane % 4
+            for w in range(4):
+                tok = 16 * j + g + 8 * (w // 2)
+                base = 32 * t + 16 * (w % 2)
+                kc[j, lane, w] = sum(int(ck[tok, base + i]) << (2 * i) for i in range(16))
+                word = 0
+                for i in range(8):
+                    m, e = 2 * w + i // 4, i % 4
+                    dim = 16 * m + g + 8 * (e % 2)
+                    tok0 = 16 * j + 2 * t + 8 * (e // 2)
+                    word |= int(cv[tok0, dim]) << (2 * i)
+                    word |= int(cv[tok0 + 1, dim]) << (16 + 2 * i)
+                vc[j, lane, w] = word
+    f16 = lambda a: np.asarray(a, np.float16).view(np.uint16).astype(np.uint32)
+    skb, zkb = f16(sk), f16(zk)
+    km = np.zeros((4, 2, 8, 2), np.uint32)
+    for t in range(4):
+        for h in range(2):
+            for i in range(8):
+                ch = 32 * t + 16 * h + i
+                km[t, h, i, 0] = skb[ch] | (skb[ch + 8] << 16)
+                km[t, h, i, 1] = zkb[ch] | (zkb[ch + 8] << 16)
+    svb, zvb = f16(sv), f16(zv)
+    vm = np.zeros((2, 8, 4, 2), np.uint32)
+    for j in range(2):
+        for p_ in range(8):
+            for c in range(4):
+                a = 16 * j + 2 * p_
+                vm[j, p_, c, 0] = svb[a, c] | (svb[a + 1, c] << 16)
+                vm[j, p_, c, 1] = zvb[a, c] | (zvb[a + 1, c] << 16)
+    out = b"".join(x.astype("<u4").tobytes() for x in (kc, vc, km, vm))
+    assert len(out) == KIVI_TILE_BYTES
+    return out
+
+
+def kivi_group_page(Kg, Vg) -> bytes:
+    """Bytes of one group page: the tiles of all (layer, KV head), layer
+    outermost, for the 32 tokens Kg, Vg ([32][L][Hkv][128])."""
+    ck, sk, zk = kivi_quant_k(Kg)
+    cv, sv, zv = kivi_quant_v(Vg)
+    L, H = ck.shape[1], ck.shape[2]
+    return b"".join(kivi_group_tile(ck[:, l, h], sk[l, h], zk[l, h], cv[:, l, h], sv[:, l, h], zv[:, l, h])
+                    for l in range(L) for h in range(H))
 
 
 # ---------------------------------------------------------------------------

@@ -56,17 +56,23 @@ double orc_bf16_to_f64(uint16_t h) { return bf16_to_f64(h); }
  *   bmass    : ceil(n / block_tokens) doubles, mu(b) (may be NULL)
  *   sbuf     : n doubles of scratch
  */
-/* K and V elements: bf16 bit patterns, or 8-bit codes read through a
+/* K and V elements: bf16 bit patterns, float32 values (e.g. dequantised
+ * 2-bit groups beside unquantised tokens), or 8-bit codes read through a
  * 256-entry table of values (code value x scale), e.g. for FP8 pages. */
 typedef struct {
-    const uint16_t *p16;      /* bf16 elements, or NULL */
-    const uint8_t *p8;        /* 8-bit codes, or NULL   */
-    const double *lut;        /* value of each code     */
+    const uint16_t *p16;      /* bf16 elements, or NULL    */
+    const uint8_t *p8;        /* 8-bit codes, or NULL      */
+    const double *lut;        /* value of each code        */
+    const float *p32;         /* float32 elements, or NULL */
 } elems_t;
 
 static double elem_at(const elems_t *e, int64_t idx)
 {
-    return e->p16 ? bf16_to_f64(e->p16[idx]) : e->lut[e->p8[idx]];
+    if (e->p16)
+        return bf16_to_f64(e->p16[idx]);
+    if (e->p32)
+        return (double)e->p32[idx];
+    return e->lut[e->p8[idx]];
 }
 
 static void attend_head(const uint16_t *q, const elems_t *k, const elems_t *v, int64_t off,
@@ -229,7 +235,7 @@ int orc_decode_heads(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      const int32_t *heads, int nheads, int nthreads,
                      double *out, double *lse, double *head_mass)
 {
-    elems_t ek = {k, NULL, NULL}, ev = {v, NULL, NULL};
+    elems_t ek = {k, NULL, NULL, NULL}, ev = {v, NULL, NULL, NULL};
     return decode_heads(q, ek, ev, n, L, Hq, Hkv, d, block_tokens, heads, nheads, nthreads,
                         out, lse, head_mass);
 }
@@ -246,7 +252,22 @@ int orc_decode_heads_u8(const uint16_t *q, const uint8_t *k, const uint8_t *v,
 {
     if (!lut_k || !lut_v)
         return -1;
-    elems_t ek = {NULL, k, lut_k}, ev = {NULL, v, lut_v};
+    elems_t ek = {NULL, k, lut_k, NULL}, ev = {NULL, v, lut_v, NULL};
+    return decode_heads(q, ek, ev, n, L, Hq, Hkv, d, block_tokens, heads, nheads, nthreads,
+                        out, lse, head_mass);
+}
+
+/*
+ * Same, with K and V as float32 values [n][L][Hkv][d].
+ */
+int orc_decode_heads_f32(const uint16_t *q, const float *k, const float *v,
+                         int64_t n, int L, int Hq, int Hkv, int d, int block_tokens,
+                         const int32_t *heads, int nheads, int nthreads,
+                         double *out, double *lse, double *head_mass)
+{
+    if (!k || !v)
+        return -1;
+    elems_t ek = {NULL, NULL, NULL, k}, ev = {NULL, NULL, NULL, v};
     return decode_heads(q, ek, ev, n, L, Hq, Hkv, d, block_tokens, heads, nheads, nthreads,
                         out, lse, head_mass);
 }

@@ -620,3 +620,122 @@ def test_brute_force_audit_catches_the_stale_high_heap():
     tt = rng.integers(0, 400, 300)
     assert _evict_all(S, tt, 400, 0.15, _heap_order_key) == 0
     assert _evict_all(S, tt, 400, 0.15, _heap_stale_high) > 100
+
+
+# ------------------------------------------------------------- KIVI 2-bit
+# [KIVI] s.02: keys per channel in 32-token groups (two blocks), values per
+# token in 32-channel groups, asymmetric 2-bit with an fp16 scale and zero
+# per group (1 extra bit per element: ~3 bits), newest ~128 tokens unquantised.
+
+
+def test_kivi_quant_closed_forms():
+    # a 4-level ramp along the group axis is reproduced exactly
+    x = np.tile(np.array([1.0, 1.5, 2.0, 2.5], np.float32), 8)[None]
+    c, s, z = O.kivi_quant(x)
+    assert c.tolist() == [[0, 1, 2, 3] * 8] and s[0] == 0.5 and z[0] == 1.0
+    assert np.array_equal(O.kivi_dequant(c, s, z).astype(np.float32), x)
+    # a constant group has scale 0, codes 0 and dequantises to fp16(x)
+    c, s, z = O.kivi_quant(np.full((1, 32), 0.3, np.float32))
+    assert s[0] == 0 and not c.any() and O.kivi_dequant(c, s, z)[0, 0] == np.float16(0.3)
+
+
+def test_kivi_error_bound():
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal((500, 32)) * rng.uniform(0.1, 10, (500, 1))).astype(np.float32)
+    c, s, z = O.kivi_quant(x)
+    xh = O.kivi_dequant(c, s, z).astype(np.float64)
+    sf = s.astype(np.float64)[:, None]
+    # half a step from rounding, plus what fp16 scale/zero and the final fp16 rounding add
+    bound = 0.5 * sf + 3 * np.abs(sf) * 2.0 ** -10 + np.abs(xh) * 2.0 ** -11 + np.abs(x.min(1))[:, None] * 2.0 ** -11
+    assert np.all(np.abs(xh - x) <= bound + 1e-12)
+
+
+def test_kivi_keys_per_channel_values_per_token():
+    # one outlier channel: per-channel key groups keep the other channels exact
+    x = np.zeros((32, 1, 1, 128), np.float32)
+    x[:, 0, 0, :] = np.tile(np.array([0.0, 0.25, 0.5, 0.75], np.float32), 8)[:, None]
+    x[:, 0, 0, 7] *= 1000.0
+    ck, sk, zk = O.kivi_quant_k(x)
+    assert sk[0, 0, 0] == np.float16(0.25) and sk[0, 0, 7] == np.float16(250.0)
+    assert np.array_equal(ck[:, 0, 0, 0], np.tile([0, 1, 2, 3], 8))
+    cv, sv, zv = O.kivi_quant_v(x)
+    assert sv.shape == (32, 1, 1, 4) and zv.shape == (32, 1, 1, 4)
+
+
+def test_kivi_residual_window_snaps_to_whole_groups():
+    Q = O.kivi_quantized_tokens
+    assert [Q(n) for n in (0, 31, 127, 128, 159, 160, 191, 192, 8192)] == [0, 0, 0, 0, 0, 32, 32, 64, 8064]
+    for n in range(128, 2000):
+        assert Q(n) % 32 == 0 and 128 <= n - Q(n) < 160
+    # a group is never cut: quantising fewer than 32 tokens would be the
+    # one-element "group" whose scale collapses and round-trips exactly
+    x = np.array([[3.14159]], np.float32)
+    c, s, z = O.kivi_quant(x)
+    assert s[0] == 0
+
+
+def test_kivi_effective_bits():
+    # 2 bits of code + 32 bits of fp16 scale/zero per 32 elements = 3 bits:
+    # 3 KiB per (layer, KV head) and 32 tokens of K and V, 16/3 = 5.3x below fp16
+    assert O.KIVI_TILE_BYTES * 8 == 3 * (2 * 32 * 128)
+    assert abs(2 * 32 * 128 * 2 / O.KIVI_TILE_BYTES - 16 / 3) < 1e-12
+
+
+def test_kivi_tile_layout_hand_offsets():
+    rng = np.random.default_rng(32)
+    ck = rng.integers(0, 4, (32, 128)).astype(np.uint8)
+    cv = rng.integers(0, 4, (32, 128)).astype(np.uint8)
+    sk = rng.uniform(0.1, 1, 128).astype(np.float16)
+    zk = rng.uniform(-1, 1, 128).astype(np.float16)
+    sv = rng.uniform(0.1, 1, (32, 4)).astype(np.float16)
+    zv = rng.uniform(-1, 1, (32, 4)).astype(np.float16)
+    tile = np.frombuffer(O.kivi_group_tile(ck, sk, zk, cv, sv, zv), "<u4")
+    # K: token 9 = block 0, g = 1, word 2 (row g+8); dim 37 = t 1, half 0, i 5
+    lane, w = 4 * 1 + 1, 2
+    assert (tile[(0 * 32 + lane) * 4 + w] >> 10) & 3 == ck[9, 37]
+    # K: token 24 = block 1, g = 0, word 3 (row 8, half 1); dim 90 = t 2, 16 + 10 -> i 10;
+    # lane = 4g + t = 2
+    assert (tile[(1 * 32 + 2) * 4 + 3] >> 20) & 3 == ck[24, 90]
+    # V: block 1, lane (g 3, t 2), word 1, pair 6 -> m 3, e 2: dim 51, tokens 16+4+8 = 28, 29
+    v = tile[256 + (1 * 32 + 14) * 4 + 1]
+    assert (v >> 12) & 3 == cv[28, 51] and (v >> 28) & 3 == cv[29, 51]
+    # K meta: t 3, half 1, i 2 -> channels 114 and 122
+    km = tile[512 + ((3 * 2 + 1) * 8 + 2) * 2]
+    assert km & 0xFFFF == sk.view(np.uint16)[114] and km >> 16 == sk.view(np.uint16)[122]
+    # V meta: block 1, token pair 5, channel group 2 -> zero of tokens 26, 27
+    vm = tile[640 + ((1 * 8 + 5) * 4 + 2) * 2 + 1]
+    assert vm & 0xFFFF == zv.view(np.uint16)[26, 2] and vm >> 16 == zv.view(np.uint16)[27, 2]
+
+
+def test_attention_on_kivi_effective_values_matches_library_sdpa():
+    wl, q, K, V = _case("l70b_8k", 300, L=2, prefill_lens=(300,))
+    Kf, Vf = O.kivi_effective(K, V)
+    Q = O.kivi_quantized_tokens(300)
+    assert Q == 160
+    # unquantised tail is the stored bf16, the quantised head differs
+    assert np.array_equal(Kf[Q:], O.bf16_to_f64(O._u16(K[Q:])).astype(np.float32))
+    assert not np.array_equal(Kf[:Q], O.bf16_to_f64(O._u16(K[:Q])).astype(np.float32))
+    r = O.decode(q, Kf, Vf, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d)
+    G = wl.Hq // wl.Hkv
+    qd = torch.from_numpy(O.bf16_to_f64(O._u16(q))).unsqueeze(2)
+    Kd = torch.from_numpy(Kf.astype(np.float64))
+    Vd = torch.from_numpy(Vf.astype(np.float64))
+    Kr = Kd.permute(1, 2, 0, 3).repeat_interleave(G, dim=1)
+    Vr = Vd.permute(1, 2, 0, 3).repeat_interleave(G, dim=1)
+    out = F.scaled_dot_product_attention(qd, Kr, Vr).squeeze(2)
+    np.testing.assert_allclose(r["out"].reshape(out.shape), out.numpy(), rtol=0, atol=1e-12)
+
+
+def test_kivi_pin_catches_per_token_keys(monkeypatch):
+    good = O.kivi_quant_k
+
+    def per_token(Kg):
+        x = O._as_f32(Kg)
+        n, L, H, d = x.shape
+        c, s, z = O.kivi_quant(x.reshape(n, L, H, d // 32, 32))
+        return c.reshape(n, L, H, d), s, z
+
+    monkeypatch.setattr(O, "kivi_quant_k", per_token)
+    with pytest.raises(Exception):
+        test_kivi_keys_per_channel_values_per_token()
+    monkeypatch.setattr(O, "kivi_quant_k", good)
