@@ -87,11 +87,34 @@ typedef enum kvs_status {
 
 typedef enum kvs_kv_dtype {
     KVS_KV_BF16 = 0,       /* pages hold bf16 K and V                          */
-    KVS_KV_FP8_E4M3 = 1    /* pages hold FP8 E4M3 codes: value = code * scale,
+    KVS_KV_FP8_E4M3 = 1,   /* pages hold FP8 E4M3 codes: value = code * scale,
                               appended bf16 values quantised as
                               code = e4m3(x / scale) ("Fitting a Million
                               Tokens", s.02: FP8 E4M3 KV halves the bytes)    */
+    KVS_KV_KIVI2 = 2       /* 2-bit groups behind a bf16 residual window
+                              ("Fitting a Million Tokens", s.02, KIVI): see
+                              KVS_KIVI_* below                               */
 } kvs_kv_dtype;
+
+/* KIVI-style 2-bit KV (kv_dtype KVS_KV_KIVI2, head_dim 128).  Pages are
+ * written in bf16 as usual; once a sequence holds n tokens, every whole group
+ * of 32 tokens (two blocks) that ends at least 128 tokens before the end --
+ * the first 32*floor(max(0, n-128)/32) tokens -- is quantised into a group
+ * page and its two bf16 pages go back to the free list.  Keys: per channel
+ * over the group's 32 tokens; values: per token over groups of 32 channels;
+ * asymmetric 2-bit, in fp32: mn, mx = min, max; scale = fp16((mx-mn)/3);
+ * zero = fp16(mn); code = clamp(rint((x - zero)/scale), 0, 3) (ties to even;
+ * 0 when scale is 0).  Attention reads fp16(code*scale + zero) (one
+ * rounding).  A group page holds, per (layer, KV head), 3072 bytes: K codes,
+ * V codes, K (scale, zero) per channel, V (scale, zero) per token and channel
+ * group -- 3 bits per element.  The table entry of a quantised block is
+ * KVS_TABLE_GROUP(g) for its group page g (both blocks of the group).
+ * KIVI contexts share no blocks between sequences and gather no pages
+ * (kvs_select_and_gather returns the id list only, flags 0, no host_dst). */
+#define KVS_KIVI_GROUP_TOKENS 32u
+#define KVS_KIVI_RESIDUAL 128u
+#define KVS_KIVI_TILE_BYTES 3072u
+#define KVS_TABLE_GROUP(g) (-2 - (int32_t)(g))
 
 typedef enum kvs_select_mode {
     KVS_SELECT_THRESH = 0,   /* every record with P < cut_lo (tier 2) */
@@ -126,6 +149,8 @@ typedef struct kvs_config {
                                      quotient x / scale is an IEEE fp32
                                      division, rounded to the nearest code
                                      (ties to even), saturating at +-448   */
+    uint32_t kivi_groups;         /* KIVI only: group pages in the group pool */
+    uint32_t reserved1;           /* 0                                        */
 } kvs_config;
 
 /* Byte sizes of the caller-allocated device buffers.  Every buffer must be
@@ -138,10 +163,13 @@ typedef struct kvs_sizes {
     size_t mass_bytes;        /* float [max_seqs][max_blocks_per_seq]         */
     size_t workspace_bytes;   /* decode partials, per-block LSE, select state */
     size_t staging_bytes;     /* staging_pages * page_bytes                   */
+    size_t group_page_bytes;  /* KIVI: L * Hkv * KVS_KIVI_TILE_BYTES, else 0  */
+    size_t group_pool_bytes;  /* KIVI: kivi_groups * group_page_bytes, else 0 */
 } kvs_sizes;
 
 typedef struct kvs_buffers {
     void *pool, *block_table, *records, *mass, *workspace, *staging;
+    void *group_pool;         /* KIVI only (group_pool_bytes), else NULL      */
 } kvs_buffers;
 
 /* Identity key of a block [GQA]: the sequence it belongs to and its logical

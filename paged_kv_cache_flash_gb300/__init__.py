@@ -26,7 +26,8 @@ STATUS_NAMES = ["OK", "EINVAL", "ENOMEM", "ECUDA", "ENOTFOUND", "EEXIST", "ETRUN
                 "ETIMEOUT", "EDEVICE"]
 KVS_SELECT_THRESH, KVS_SELECT_LOWFRAC = 0, 1
 KVS_SELECT_LRFU = 2
-KVS_KV_BF16, KVS_KV_FP8_E4M3 = 0, 1
+KVS_KV_BF16, KVS_KV_FP8_E4M3, KVS_KV_KIVI2 = 0, 1, 2
+KVS_KIVI_GROUP_TOKENS, KVS_KIVI_RESIDUAL = 32, 128
 KVS_GATHER_DEMOTE, KVS_GATHER_MIRROR = 1, 2
 KVS_MAX_CALL_SEQS = 256
 KVS_PREFETCH_MAX = 4096
@@ -44,18 +45,19 @@ class kvs_config(ctypes.Structure):
                 ("staging_pages", c_u32), ("alpha", c_dbl), ("recency_window", c_u32),
                 ("kv_dtype", c_u32), ("w_recency", c_dbl), ("w_ema", c_dbl), ("w_anchor", c_dbl),
                 ("cut_lo", c_dbl), ("cut_hi", c_dbl), ("pool_seed", c_u64),
-                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float), ("kivi_groups", c_u32),
+                ("reserved1", c_u32)]
 
 
 class kvs_sizes(ctypes.Structure):
     _fields_ = [("page_bytes", c_sz), ("pool_bytes", c_sz), ("table_bytes", c_sz),
                 ("records_bytes", c_sz), ("mass_bytes", c_sz), ("workspace_bytes", c_sz),
-                ("staging_bytes", c_sz)]
+                ("staging_bytes", c_sz), ("group_page_bytes", c_sz), ("group_pool_bytes", c_sz)]
 
 
 class kvs_buffers(ctypes.Structure):
     _fields_ = [("pool", c_vp), ("block_table", c_vp), ("records", c_vp), ("mass", c_vp),
-                ("workspace", c_vp), ("staging", c_vp)]
+                ("workspace", c_vp), ("staging", c_vp), ("group_pool", c_vp)]
 
 
 class kvs_key(ctypes.Structure):
@@ -161,14 +163,14 @@ def _check(ctx, rc):
 def make_config(L, Hq, Hkv, d, pool_blocks, max_seqs, max_blocks_per_seq, *, alpha=0.15,
                 recency_window=64, weights=(0.25, 0.55, 0.20), cuts=(0.3, 0.6), pool_seed=0,
                 staging_pages=16, max_call_blocks=0, kv_dtype=KVS_KV_BF16, k_scale=1.0,
-                v_scale=1.0) -> kvs_config:
+                v_scale=1.0, kivi_groups=0) -> kvs_config:
     return kvs_config(num_layers=L, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
                       block_tokens=BLOCK_TOKENS, pool_blocks=pool_blocks, max_seqs=max_seqs,
                       max_blocks_per_seq=max_blocks_per_seq, max_call_blocks=max_call_blocks,
                       staging_pages=staging_pages, alpha=alpha, recency_window=recency_window,
                       kv_dtype=kv_dtype, w_recency=weights[0], w_ema=weights[1],
                       w_anchor=weights[2], cut_lo=cuts[0], cut_hi=cuts[1], pool_seed=pool_seed,
-                      k_scale=k_scale, v_scale=v_scale)
+                      k_scale=k_scale, v_scale=v_scale, kivi_groups=kivi_groups)
 
 
 def kvs_required_sizes(cfg: kvs_config) -> kvs_sizes:
@@ -205,9 +207,11 @@ class Context:
         self.mass_buf = alloc(sz.mass_bytes)
         self.workspace = alloc(sz.workspace_bytes)
         self.staging = alloc(sz.staging_bytes)
+        self.group_pool = alloc(sz.group_pool_bytes) if sz.group_pool_bytes else None
         bufs = kvs_buffers(self.pool.data_ptr(), self.table.data_ptr(), self.records.data_ptr(),
                            self.mass_buf.data_ptr(), self.workspace.data_ptr(),
-                           self.staging.data_ptr())
+                           self.staging.data_ptr(),
+                           self.group_pool.data_ptr() if self.group_pool is not None else None)
         h = c_vp()
         with torch.cuda.device(self.device):
             _check(None, lib().kvs_create(ctypes.byref(cfg), ctypes.byref(bufs), ctypes.byref(h)))
@@ -387,6 +391,11 @@ class Context:
         (row = sequence slot, see seq_info)."""
         return self.mass_buf[: self.sizes.mass_bytes].view(self.torch.float32).view(
             self.cfg.max_seqs, self.cfg.max_blocks_per_seq)
+
+    def group_bytes_of(self, group_page: int):
+        """Bytes of a 2-bit group page (a CUDA uint8 view)."""
+        gb = self.sizes.group_page_bytes
+        return self.group_pool[group_page * gb:(group_page + 1) * gb]
 
     def page_bytes_of(self, page: int):
         """Bytes of a physical page (a CUDA uint8 view)."""

@@ -17,7 +17,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 OUT_DIR = PKG / "_build"
 LIB = OUT_DIR / "libkvs.so"
-SOURCES = ["kvs_decode.cu", "kvs_combine.cu", "kvs_blocks.cu", "kvs_host.cpp", "kvs_noalloc.cu"]
+SOURCES = ["kvs_decode.cu", "kvs_combine.cu", "kvs_blocks.cu", "kvs_kivi.cu", "kvs_host.cpp", "kvs_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -31,8 +31,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w,
     const uint32_t ci = blockIdx.x / (g.L * g.Hkv);
     const uint32_t rest = blockIdx.x % (g.L * g.Hkv);
     const uint32_t l = rest / g.Hkv, kvh = rest % g.Hkv;
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-        *w.counter = 0;            // ready for the next decode launch
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        w.counter[0] = 0;          // ready for the next decode launches
+        w.counter[1] = 0;
+    }
     const DSeq sq = ds->seq[ci];
     const uint32_t r0 = blockIdx.y * kMassRange;
     if (r0 >= sq.nb)

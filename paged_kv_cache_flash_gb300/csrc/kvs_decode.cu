@@ -109,12 +109,15 @@ __device__ __forceinline__ Prep prepare_item(const DecodeArgs &a, uint32_t id, u
     const DSeq &sq = ds->seq[ci];
     // KV head fastest: warps that claim consecutive items read adjacent
     // sub-pages of the same pages at about the same time (DRAM locality)
+    // (KIVI: the page items cover the blocks after the qb quantised ones,
+    // and their partials follow the nchunk_q group-page chunks)
     uint32_t local = id - sq.item_off;
     const uint32_t kvh = local % g.Hkv;
     local /= g.Hkv;
-    const uint32_t chunk = local % sq.nchunk;
-    const uint32_t l = local / sq.nchunk;
-    const uint32_t b0 = chunk * ds->chunk;
+    const uint32_t nch = sq.nchunk - sq.nchunk_q;
+    const uint32_t chunk = local % nch;
+    const uint32_t l = local / nch;
+    const uint32_t b0 = sq.qb + chunk * ds->chunk;
     const uint32_t nblk = min(ds->chunk, sq.nb - b0);
     p.it.valid = 1;
     p.it.ci = ci;
@@ -123,7 +126,7 @@ __device__ __forceinline__ Prep prepare_item(const DecodeArgs &a, uint32_t id, u
     p.it.b0 = b0;
     p.it.nblk = nblk;
     p.it.ntok = sq.ntok;
-    p.it.part = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk + chunk;
+    p.it.part = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk + sq.nchunk_q + chunk;
     p.it.lse0 = sq.blk_off + b0;
     const int32_t *trow = a.table + static_cast<size_t>(sq.slot) * g.mb + b0;
 #pragma unroll

@@ -48,7 +48,8 @@ struct SeqState {
     bool live = false;
     uint32_t ntok = 0;
     uint32_t shared_blocks = 0;      // leading blocks shared read-only
-    std::vector<int32_t> table;      // page per block, -1 = demoted
+    uint32_t qtok = 0;               // KIVI: tokens held in 2-bit group pages
+    std::vector<int32_t> table;      // page per block, -1 = demoted, KVS_TABLE_GROUP(g) = in group page g
 };
 
 struct Demoted {
@@ -98,6 +99,8 @@ struct kvs_ctx {
     bool side_pending = false, release_pending = false;
 
     uint64_t kernel_launches = 0;                   // kernels launched by this context
+    std::deque<uint32_t> free_groups;               // KIVI: free group pages
+    int kivi_grid = 0;                              // KIVI: persistent decode grid
     std::string err;
 };
 
@@ -227,8 +230,12 @@ int check_cfg(const kvs_config *c, kvs_ctx *ctx)
         return fail(ctx, KVS_EINVAL, "alpha must be in [0, 1] and recency_window > 0");
     if (!(c->cut_lo <= c->cut_hi))
         return fail(ctx, KVS_EINVAL, "cut_lo must not exceed cut_hi");
-    if (c->kv_dtype != KVS_KV_BF16 && c->kv_dtype != KVS_KV_FP8_E4M3)
+    if (c->kv_dtype != KVS_KV_BF16 && c->kv_dtype != KVS_KV_FP8_E4M3 && c->kv_dtype != KVS_KV_KIVI2)
         return fail(ctx, KVS_EINVAL, "unknown kv_dtype %u", c->kv_dtype);
+    if (c->kv_dtype == KVS_KV_KIVI2) {
+        if (c->head_dim != 128)
+            return fail(ctx, KVS_EINVAL, "2-bit groups need head_dim 128");
+    }
     if (c->kv_dtype == KVS_KV_FP8_E4M3) {
         if (c->head_dim != 128)
             return fail(ctx, KVS_EINVAL, "FP8 pages need head_dim 128");
@@ -244,6 +251,15 @@ uint32_t pick_wg(uint32_t hkv)
         if (hkv % w == 0)
             return w;
     return 1;
+}
+
+// KIVI: tokens in whole groups that end at least KVS_KIVI_RESIDUAL tokens
+// before the end of an n-token sequence.
+uint32_t kivi_q(uint64_t n)
+{
+    return n > KVS_KIVI_RESIDUAL
+               ? static_cast<uint32_t>((n - KVS_KIVI_RESIDUAL) / KVS_KIVI_GROUP_TOKENS * KVS_KIVI_GROUP_TOKENS)
+               : 0u;
 }
 
 SeqState *find_seq(kvs_ctx *ctx, uint64_t id, uint32_t *slot = nullptr)
@@ -263,15 +279,17 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
         return fail(ctx, KVS_EINVAL, "nseq must be in [1, %u]", kMaxCallSeqs);
     std::memset(ds, 0, sizeof(DSet));
     const Geo &g = ctx->geo;
-    uint32_t blk = 0, items = 0, parts = 0;
+    uint32_t blk = 0, items = 0, items_q = 0, parts = 0;
     std::vector<std::pair<uint64_t, uint32_t>> order;
     order.reserve(nseq);
-    uint32_t nbs[kMaxCallSeqs];
+    uint32_t nbs[kMaxCallSeqs], qbs[kMaxCallSeqs];
     for (uint32_t i = 0; i < nseq; ++i) {
         SeqState *s = find_seq(ctx, ids[i]);
         nbs[i] = s ? (s->ntok + kBlockTokens - 1) / kBlockTokens : 1;
+        qbs[i] = s && g.kivi ? s->qtok / kBlockTokens : 0;
     }
-    const uint32_t chunk = pick_chunk(nbs, nseq, g.L, g.Hkv, ctx->decode_grid * ctx->wg, ctx->lay.parts_max);
+    const uint32_t chunk = pick_chunk(nbs, nseq, g.L, g.Hkv, ctx->decode_grid * ctx->wg, ctx->lay.parts_max,
+                                      g.kivi ? qbs : nullptr);
     if (chunk == 0)
         return fail(ctx, KVS_EINVAL, "too many blocks in one call for the workspace partials");
     for (uint32_t i = 0; i < nseq; ++i) {
@@ -282,20 +300,27 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
         if (s->ntok == 0)
             return fail(ctx, KVS_EINVAL, "sequence %llu has no tokens", (unsigned long long)ids[i]);
         for (int32_t p : s->table)
-            if (p < 0)
+            if (p == -1)
                 return fail(ctx, KVS_EINVAL, "sequence %llu has a demoted block; re-admit it first",
                             (unsigned long long)ids[i]);
         DSeq &q = ds->seq[i];
         q.slot = slot;
         q.ntok = s->ntok;
         q.nb = (s->ntok + kBlockTokens - 1) / kBlockTokens;
-        q.nchunk = (q.nb + chunk - 1) / chunk;
+        // KIVI: the leading qb blocks (group pages) and the rest (pages) are
+        // chunked apart: group-page chunks first, then page chunks
+        q.qb = g.kivi ? s->qtok / kBlockTokens : 0;
+        q.nchunk_q = (q.qb + chunk - 1) / chunk;
+        const uint32_t nchunk_p = (q.nb - q.qb + chunk - 1) / chunk;
+        q.nchunk = q.nchunk_q + nchunk_p;
         q.blk_off = blk;
         q.item_off = items;
+        q.item_off_q = items_q;
         q.part_off = parts;
         q.seq_id = ids[i];
         blk += q.nb;
-        items += g.L * g.Hkv * q.nchunk;      // one item per KV head and chunk
+        items += g.L * g.Hkv * nchunk_p;      // one item per KV head and chunk
+        items_q += g.L * g.Hkv * q.nchunk_q;
         parts += g.L * g.Hkv * q.nchunk;
         order.emplace_back(ids[i], i);
     }
@@ -319,6 +344,7 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
     ds->nseq = nseq;
     ds->nb_total = blk;
     ds->n_items = items;
+    ds->n_items_q = items_q;
     ds->n_parts = parts;
     ds->wg = ctx->wg;
     ds->chunk = chunk;
@@ -369,6 +395,79 @@ int apply_patches(kvs_ctx *ctx, const std::vector<Patch> &p, cudaStream_t s)
             return rc;
     }
     return KVS_OK;
+}
+
+// KIVI: quantises, on stream s, every group of the listed sequences (slot,
+// state) that has fallen behind the residual window, then returns the
+// groups' bf16 pages to the free list (later writers run after the kernel
+// on the same stream).  The caller checked that enough group pages are free.
+int kivi_compress(kvs_ctx *ctx, const std::vector<std::pair<uint32_t, SeqState *>> &seqs, cudaStream_t s)
+{
+    std::vector<KiviJob> jobs;
+    for (const auto &e : seqs) {
+        SeqState *sq = e.second;
+        const uint32_t qn = kivi_q(sq->ntok);
+        for (uint32_t t0 = sq->qtok; t0 < qn; t0 += KVS_KIVI_GROUP_TOKENS) {
+            const uint32_t gi = t0 / KVS_KIVI_GROUP_TOKENS;
+            KiviJob j{};
+            j.slot = e.first;
+            j.group = gi;
+            j.page0 = sq->table[2 * gi];
+            j.page1 = sq->table[2 * gi + 1];
+            j.gpage = ctx->free_groups.front();
+            ctx->free_groups.pop_front();
+            jobs.push_back(j);
+        }
+    }
+    if (jobs.empty())
+        return KVS_OK;
+    int rc = order_pool_writes(ctx, s);
+    if (rc)
+        return rc;
+    const uint32_t per_slot = static_cast<uint32_t>(kRingSlotBytes / sizeof(KiviJob));
+    for (size_t off = 0; off < jobs.size(); off += per_slot) {
+        const uint32_t n = static_cast<uint32_t>(std::min<size_t>(per_slot, jobs.size() - off));
+        RingSlot r;
+        if ((rc = ring_acquire(ctx, n * sizeof(KiviJob), &r)))
+            return rc;
+        std::memcpy(r.host, jobs.data() + off, n * sizeof(KiviJob));
+        if ((rc = ring_push(ctx, r, n * sizeof(KiviJob), s)))
+            return rc;
+        if ((rc = launch_rc(ctx,
+                            launch_kivi_compress(ctx->geo, reinterpret_cast<const KiviJob *>(r.dev), n,
+                                                 static_cast<const uint8_t *>(ctx->buf.pool),
+                                                 static_cast<uint8_t *>(ctx->buf.group_pool),
+                                                 static_cast<int32_t *>(ctx->buf.block_table), s),
+                            "2-bit compress")))
+            return rc;
+        if ((rc = ring_release(ctx, r, s)))
+            return rc;
+    }
+    for (const KiviJob &j : jobs) {
+        for (int32_t p : {j.page0, j.page1})
+            if (--ctx->refcnt[p] == 0)
+                ctx->free_pages.push_back(p);
+    }
+    size_t k = 0;
+    for (const auto &e : seqs) {
+        SeqState *sq = e.second;
+        const uint32_t qn = kivi_q(sq->ntok);
+        for (uint32_t t0 = sq->qtok; t0 < qn; t0 += KVS_KIVI_GROUP_TOKENS, ++k) {
+            const uint32_t gi = t0 / KVS_KIVI_GROUP_TOKENS;
+            sq->table[2 * gi] = KVS_TABLE_GROUP(jobs[k].gpage);
+            sq->table[2 * gi + 1] = KVS_TABLE_GROUP(jobs[k].gpage);
+        }
+        sq->qtok = qn;
+    }
+    ctx->refcnt_dirty = true;
+    return KVS_OK;
+}
+
+// KIVI: group pages a sequence of ntok_after tokens would take beyond what it holds.
+uint32_t kivi_groups_needed(const SeqState *sq, uint64_t ntok_after)
+{
+    const uint32_t qn = kivi_q(ntok_after);
+    return qn > sq->qtok ? (qn - sq->qtok) / KVS_KIVI_GROUP_TOKENS : 0u;
 }
 
 // The staging ring: with 4 pages or more, the gather double-buffers through
@@ -512,6 +611,9 @@ int kvs_required_sizes(const kvs_config *cfg, kvs_sizes *out)
     out->mass_bytes = rows * sizeof(float);
     out->workspace_bytes = workspace_layout(c).total;
     out->staging_bytes = out->page_bytes * c.staging_pages;
+    const bool kivi = c.kv_dtype == KVS_KV_KIVI2;
+    out->group_page_bytes = kivi ? static_cast<size_t>(c.num_layers) * c.num_kv_heads * KVS_KIVI_TILE_BYTES : 0;
+    out->group_pool_bytes = out->group_page_bytes * (kivi ? c.kivi_groups : 0);
     return KVS_OK;
 }
 
@@ -531,6 +633,9 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
     for (void *p : {buf->pool, buf->block_table, buf->records, buf->mass, buf->workspace, buf->staging})
         if (reinterpret_cast<uintptr_t>(p) % 256)
             return fail(ctx, KVS_EINVAL, "device buffers must be 256-byte aligned");
+    if (cfg->kv_dtype == KVS_KV_KIVI2 && cfg->kivi_groups &&
+        (!buf->group_pool || reinterpret_cast<uintptr_t>(buf->group_pool) % 256))
+        return fail(ctx, KVS_EINVAL, "2-bit groups need a 256-byte aligned group_pool");
     static_assert(sizeof(kvs_record) == KVS_RECORD_BYTES, "record must be 64 bytes");
     static_assert(sizeof(kvs_key) == 16, "key must be 16 bytes");
     ctx->cfg = *cfg;
@@ -551,6 +656,11 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
     g.fp8 = cfg->kv_dtype == KVS_KV_FP8_E4M3 ? 1 : 0;
     g.k_scale = g.fp8 ? cfg->k_scale : 1.f;
     g.v_scale = g.fp8 ? cfg->v_scale : 1.f;
+    g.kivi = cfg->kv_dtype == KVS_KV_KIVI2 ? 1 : 0;
+    g.kivi_groups = g.kivi ? cfg->kivi_groups : 0;
+    g.group_page_bytes = ctx->sz.group_page_bytes;
+    for (uint32_t i = 0; i < g.kivi_groups; ++i)
+        ctx->free_groups.push_back(i);
     ctx->wg = pick_wg(g.Hkv);
     ctx->dset.reset(new DSet());
 
@@ -561,6 +671,12 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
         return fail(ctx, KVS_ECUDA, "decode kernel does not fit on an SM (%zu B shared memory)",
                     decode_smem_bytes(g, ctx->wg));
     ctx->decode_grid = per_sm * ctx->sm_count;
+    if (g.kivi) {
+        const int kper = decode_kivi_blocks_per_sm(g);
+        if (kper < 1)
+            return fail(ctx, KVS_ECUDA, "2-bit group decode kernel does not fit on an SM");
+        ctx->kivi_grid = kper * ctx->sm_count;
+    }
 
     // TMA descriptor of the pool: dims (d, token slot, KV head, K/V, layer*page)
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -672,6 +788,8 @@ int kvs_seq_add(kvs_ctx_t *ctx, uint64_t seq_id, int64_t parent, uint32_t shared
     } else if (shared_blocks) {
         return fail(ctx, KVS_EINVAL, "shared blocks need a parent");
     }
+    if (shared_blocks && ctx->geo.kivi)
+        return fail(ctx, KVS_EINVAL, "2-bit group contexts share no blocks");
     if (shared_blocks > ctx->cfg.max_blocks_per_seq)
         return fail(ctx, KVS_EINVAL, "shared prefix longer than a table row");
     const uint32_t slot = ctx->free_slots.back();
@@ -716,7 +834,13 @@ int kvs_seq_remove(kvs_ctx_t *ctx, uint64_t seq_id, void *stream)
         return fail(ctx, KVS_ENOTFOUND, "unknown sequence %llu", (unsigned long long)seq_id);
     CU(cudaEventRecord(ctx->ev_pool_release, S(stream)));
     ctx->release_pending = true;
-    for (int32_t p : s->table) {
+    for (size_t b = 0; b < s->table.size(); ++b) {
+        const int32_t p = s->table[b];
+        if (p <= KVS_TABLE_GROUP(0)) {
+            if (b % 2 == 0)                     // both blocks name the group page
+                ctx->free_groups.push_back(static_cast<uint32_t>(KVS_TABLE_GROUP(0) - p));
+            continue;
+        }
         if (p < 0)
             continue;
         if (--ctx->refcnt[p] == 0)
@@ -766,6 +890,9 @@ int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n, const void *k
     if (pages_available(ctx) < need)
         return fail(ctx, KVS_ENOMEM, "pool exhausted: %u pages needed, %zu free", need,
                     pages_available(ctx));
+    if (ctx->geo.kivi && kivi_groups_needed(s, p1) > ctx->free_groups.size())
+        return fail(ctx, KVS_ENOMEM, "group pool exhausted: %u group pages needed, %zu free",
+                    kivi_groups_needed(s, p1), ctx->free_groups.size());
     int rc = order_pool_writes(ctx, S(stream));
     if (rc || (rc = reclaim_pages(ctx, S(stream), need)))
         return rc;
@@ -822,6 +949,8 @@ int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n, const void *k
         }
     }
     s->ntok = static_cast<uint32_t>(p1);
+    if (ctx->geo.kivi)
+        return kivi_compress(ctx, {{slot, s}}, S(stream));
     return KVS_OK;
 }
 
@@ -875,6 +1004,14 @@ int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
     }
     if (pages_available(ctx) < fresh)
         return fail(ctx, KVS_ENOMEM, "pool exhausted: %u pages needed, %zu free", fresh, pages_available(ctx));
+    if (ctx->geo.kivi) {
+        size_t groups = 0;
+        for (uint32_t i = 0; i < nseq; ++i)
+            groups += kivi_groups_needed(seqs[i], seqs[i]->ntok + 1ull);
+        if (groups > ctx->free_groups.size())
+            return fail(ctx, KVS_ENOMEM, "group pool exhausted: %zu group pages needed, %zu free", groups,
+                        ctx->free_groups.size());
+    }
     int rc = order_pool_writes(ctx, S(stream));
     if (rc || (rc = reclaim_pages(ctx, S(stream), fresh)))
         return rc;
@@ -932,6 +1069,13 @@ int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
         }
         seqs[i]->ntok += 1;
     }
+    if (ctx->geo.kivi) {
+        std::vector<std::pair<uint32_t, SeqState *>> due;
+        for (uint32_t i = 0; i < nseq; ++i)
+            if (kivi_groups_needed(seqs[i], seqs[i]->ntok))
+                due.emplace_back(sa[i].slot, seqs[i]);
+        return kivi_compress(ctx, due, S(stream));
+    }
     return KVS_OK;
 }
 
@@ -960,7 +1104,16 @@ int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
                                                          ctx->decode_grid));
     if (ctx->ev_dec_start)
         CU(cudaEventRecord(ctx->ev_dec_start, s));
-    if ((rc = launch_rc(ctx,
+    if (ds->n_items_q &&
+        (rc = launch_rc(ctx,
+                        launch_decode_kivi(ctx->geo, ctx->work, static_cast<const uint16_t *>(q_dev),
+                                           static_cast<const int32_t *>(ctx->buf.block_table),
+                                           static_cast<const uint8_t *>(ctx->buf.group_pool), ds->n_items_q,
+                                           ctx->kivi_grid, s),
+                        "2-bit decode")))
+        return rc;
+    if (ds->n_items &&
+        (rc = launch_rc(ctx,
                         launch_decode(ctx->geo, ctx->tmap, ctx->work, static_cast<const uint16_t *>(q_dev),
                                       static_cast<const int32_t *>(ctx->buf.block_table), ds->n_items,
                                       ctx->wg, grid, s),
@@ -1015,6 +1168,8 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
     const bool mirror = args->flags & KVS_GATHER_MIRROR, demote = args->flags & KVS_GATHER_DEMOTE;
     if (mirror && demote)
         return fail(ctx, KVS_EINVAL, "DEMOTE works in list mode only");
+    if (ctx->geo.kivi && (args->flags || args->host_dst))
+        return fail(ctx, KVS_EINVAL, "2-bit group contexts return the selection only (no flags, no host_dst)");
     if (args->mode != KVS_SELECT_THRESH && args->mode != KVS_SELECT_LOWFRAC && args->mode != KVS_SELECT_LRFU)
         return fail(ctx, KVS_EINVAL, "unknown selection mode %d", args->mode);
     const size_t pb = ctx->sz.page_bytes;
@@ -1064,6 +1219,17 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
                                           N, s),
                             "select", 2)))
             return rc;
+        if (ctx->geo.kivi) {
+            // the id list only: quantised blocks have no page to plan
+            CU(cudaMemcpyAsync(ctx->pinned_small, w.sel_count, 4, cudaMemcpyDeviceToHost, s));
+            CU(cudaStreamSynchronize(s));
+            nsel = ctx->pinned_small[0];
+            res->n_selected = nsel;
+            if (nsel && args->ids_dev)
+                CU(cudaMemcpyAsync(args->ids_dev, w.sel_ids, std::min(nsel, args->ids_capacity) * sizeof(kvs_key),
+                                   cudaMemcpyDeviceToDevice, s));
+            return KVS_OK;
+        }
         if ((rc = launch_rc(ctx, launch_plan(w, mirror ? 1u : 0u, s), "plan")))
             return rc;
         // one readback: counts and the head of the copy list

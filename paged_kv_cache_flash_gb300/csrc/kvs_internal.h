@@ -34,7 +34,10 @@ struct DSeq {
     uint32_t blk_off;   // prefix of nb over call order (per-block LSE index)
     uint32_t item_off;  // prefix of CTA work items over call order
     uint32_t part_off;  // prefix of per-warp partials over call order
-    uint32_t nchunk;    // ceil(nb / chunk)
+    uint32_t nchunk;    // chunks (work items per (layer, KV head)): nchunk_q + residual chunks
+    uint32_t qb;        // KIVI: leading blocks held in 2-bit group pages (even), else 0
+    uint32_t nchunk_q;  // KIVI: chunks over those blocks (partials 0 .. nchunk_q-1), else 0
+    uint32_t item_off_q;  // KIVI: prefix of group-page work items over call order
     uint32_t pad;
     uint64_t seq_id;
 };
@@ -43,7 +46,8 @@ struct DSeq {
 struct DSet {
     uint32_t nseq;
     uint32_t nb_total;
-    uint32_t n_items;
+    uint32_t n_items;                 // bf16 (or FP8) page items
+    uint32_t n_items_q;               // KIVI group-page items
     uint32_t n_parts;
     uint64_t t;                       // step counter after the decode
     uint32_t wg;                      // KV heads (warps) per work item
@@ -60,12 +64,16 @@ struct Geo {
     uint64_t page_bytes;
     uint32_t fp8;                        // pages hold E4M3 codes (1 byte per element)
     float k_scale, v_scale;              // FP8: value = code * scale
+    uint32_t kivi;                       // 2-bit group pages behind a bf16 residual window
+    uint32_t kivi_groups;                // group pages in the group pool
+    uint64_t group_page_bytes;           // L * Hkv * KVS_KIVI_TILE_BYTES
 };
 
 struct Work {             // carved out of the caller's workspace buffer
     uint32_t *err;        // error word
     uint32_t *err_info;   // first offending value
-    uint32_t *counter;    // decode work counter (reset by the combine kernel)
+    uint32_t *counter;    // decode work counters: [0] page items, [1] group-page items
+                          // (reset by the combine kernel)
     uint32_t *sel_count;  // selected records
     uint64_t *sel_thr;    // LOWFRAC threshold key: [0] prio bits, [1] record index
     DSet *dset;
@@ -97,6 +105,15 @@ struct Layout {           // byte offsets inside the workspace
     size_t ring_slot_bytes;
     uint32_t ring_slots;
     uint32_t nb_max, parts_max, tiles_max;
+};
+
+// One 32-token group of one sequence to quantise into a group page.
+struct KiviJob {
+    uint32_t slot;      // sequence slot (table row)
+    uint32_t group;     // group index: blocks 2*group, 2*group+1
+    int32_t page0, page1;  // bf16 pages of the two blocks
+    uint32_t gpage;     // destination group page
+    uint32_t pad;
 };
 
 // One demoted block as the prefetch plan sees it.
@@ -175,6 +192,11 @@ cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pag
                           uint32_t npages, uint8_t *staging, cudaStream_t s);
 cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, uint8_t *page_clean,
                          const Patch *p, uint32_t n, cudaStream_t s);
+cudaError_t launch_kivi_compress(const Geo &g, const KiviJob *jobs, uint32_t njobs, const uint8_t *pool,
+                                 uint8_t *gpool, int32_t *table, cudaStream_t s);
+cudaError_t launch_decode_kivi(const Geo &g, const Work &w, const uint16_t *q, const int32_t *table,
+                               const uint8_t *gpool, uint32_t n_items, int grid, cudaStream_t s);
+int decode_kivi_blocks_per_sm(const Geo &g);
 cudaError_t launch_prefetch_plan(const PrefCand *cand, uint32_t n, uint32_t k, uint64_t *keys,
                                  uint64_t *out_key, uint32_t *out_idx, cudaStream_t s);
 cudaError_t launch_copy_mass(const Geo &g, const Work &w, const float *src, float *mass,
@@ -188,13 +210,16 @@ int decode_blocks_per_sm(const Geo &g, uint32_t wg);
 // as long as the chunk partials fit in parts_cap; if no size gives that many
 // items, the smallest that fits.  0 if not even 128 fits.
 inline uint32_t pick_chunk(const uint32_t *nb, uint32_t n, uint32_t L, uint32_t Hkv,
-                           uint32_t workers, uint64_t parts_cap)
+                           uint32_t workers, uint64_t parts_cap, const uint32_t *qb = nullptr)
 {
+    // qb (KIVI): leading group-page blocks, chunked apart from the rest
     uint32_t best = 0;
     for (uint32_t c = kMaxChunk; c >= kMinChunk; c >>= 1) {
         uint64_t parts = 0;
-        for (uint32_t i = 0; i < n; ++i)
-            parts += static_cast<uint64_t>(L) * Hkv * ((nb[i] + c - 1) / c);
+        for (uint32_t i = 0; i < n; ++i) {
+            const uint32_t q = qb ? qb[i] : 0;
+            parts += static_cast<uint64_t>(L) * Hkv * ((q + c - 1) / c + (nb[i] - q + c - 1) / c);
+        }
         if (parts > parts_cap)
             break;
         best = c;

@@ -1,0 +1,562 @@
+// KIVI-style 2-bit KV (sm_103a): group quantisation and the decode kernel
+// over group pages.
+//
+// Source: "Fitting a Million Tokens", s.02 "Quantize the cache" (KIVI): keys
+// per channel over groups of 32 tokens -- two 16-token blocks, so the group
+// is dequantised at block granularity inside the attention kernel -- values
+// per token over groups of 32 channels, asymmetric 2-bit codes with an fp16
+// scale and zero per group, the newest ~128 tokens kept unquantised.
+//
+//   kivi_compress_kernel -- one CTA of 128 threads per (group, layer, KV
+//                           head): reads the group's 32 bf16 tokens from its
+//                           two pages, quantises K per channel and V per
+//                           (token, 32-channel group) in fp32 with explicit
+//                           rounding, and writes the 3072-byte tile in the
+//                           layout the decode warps read.
+//   decode_kivi_kernel   -- persistent, independent warps as in the page
+//                           decode: each claims (sequence, layer, KV head,
+//                           chunk of groups) items, streams 3 KiB group tiles
+//                           through a bulk-copy ring, dequantises codes in
+//                           registers straight into f16 MMA fragments
+//                           (code pair -> f16 pair by a mask and the 1024
+//                           bias, then one fused multiply-add with the pair's
+//                           scale and zero) and writes the same split-K
+//                           partials and per-block log2-sum-exps.
+//
+// Tile layout (per (layer, KV head) of a group page; lane = 4g + t):
+//   [0, 1024)    K codes [block j][lane][word w]: word w = 16 codes of token
+//                16j + g + 8(w/2), channels 32t + 16(w%2) + i at bits 2i.
+//   [1024, 2048) V codes [block j][lane][word w]: pair i (0..7) of word w is
+//                m-tile m = 2w + i/4, register e = i%4: channel 16m + g +
+//                8(e%2), tokens 16j + 2t + 8(e/2) (bits 2i) and the next one
+//                (bits 16 + 2i).
+//   [2048, 2560) K (scale pair, zero pair) [t][h][i]: channels 32t + 16h + i
+//                (low half) and + 8 (high half).
+//   [2560, 3072) V (scale pair, zero pair) [block j][token pair p][channel
+//                group c]: tokens 16j + 2p (low) and 16j + 2p + 1 (high).
+// Pair i of a code word is (word >> 2i) & 0x00030003: two codes, one per
+// 16-bit half -- the operand pair of an f16 MMA register.
+#include <cuda_fp16.h>
+
+#include "kvs_internal.h"
+#include "kvs_ptx.h"
+
+namespace kvs {
+namespace {
+
+using namespace ptx;
+
+constexpr uint32_t kTile = KVS_KIVI_TILE_BYTES;
+constexpr int kKRing = 6;           // group tiles in flight per warp
+constexpr int kKWarps = 4;          // warps per CTA
+constexpr int kKMinCtas = 3;        // CTAs per SM (12 warps: dequantisation is ALU work)
+constexpr int kKD = 128;            // head dimension of the scheme
+
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+__device__ __forceinline__ uint16_t h_bits(__half h) { return __half_as_ushort(h); }
+
+// ------------------------------------------------------------------ compress
+__global__ void __launch_bounds__(128)
+    kivi_compress_kernel(const Geo g, const KiviJob *jobs, const uint8_t *pool, uint8_t *gpool,
+                         int32_t *table)
+{
+    __shared__ uint8_t kc[32][kKD];
+    __shared__ uint8_t vc[32][kKD];
+    __shared__ uint16_t sk[kKD], zk[kKD];
+    __shared__ uint16_t sv[32][4], zv[32][4];
+    __shared__ uint32_t tile[kTile / 4];
+    const uint32_t LH = g.L * g.Hkv;
+    const KiviJob job = jobs[blockIdx.x / LH];
+    const uint32_t lh = blockIdx.x % LH;
+    const uint32_t l = lh / g.Hkv, h = lh % g.Hkv;
+    const uint32_t tid = threadIdx.x;
+    // token t of the group: page of block t / 16, slot t % 16
+    auto row = [&](uint32_t t, uint32_t kv) -> const uint16_t * {
+        const int32_t page = t < 16 ? job.page0 : job.page1;
+        return reinterpret_cast<const uint16_t *>(
+            pool + static_cast<uint64_t>(page) * g.page_bytes +
+            ((((static_cast<uint64_t>(l) * 2 + kv) * g.Hkv + h) * kBlockTokens + (t & 15)) * kKD) * 2);
+    };
+    // keys: thread = channel, over the 32 tokens
+    {
+        float x[32];
+        float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+        for (uint32_t t = 0; t < 32; ++t) {
+            x[t] = bf16f(row(t, 0)[tid]);
+            mn = fminf(mn, x[t]);
+            mx = fmaxf(mx, x[t]);
+        }
+        const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+        const __half z16 = __float2half_rn(mn);
+        const float sf = __half2float(s16), zf = __half2float(z16);
+#pragma unroll
+        for (uint32_t t = 0; t < 32; ++t) {
+            int c = 0;
+            if (sf > 0.f)
+                c = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(x[t], zf), sf)), 0), 3);
+            kc[t][tid] = static_cast<uint8_t>(c);
+        }
+        sk[tid] = h_bits(s16);
+        zk[tid] = h_bits(z16);
+    }
+    // values: thread = (token, channel group), over 32 channels
+    {
+        const uint32_t t = tid >> 2, cg = tid & 3;
+        const uint4 *src = reinterpret_cast<const uint4 *>(row(t, 1) + 32 * cg);
+        float x[32];
+        float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = src[q];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[8 * q + 2 * e] = __uint_as_float(w[e] << 16);
+                x[8 * q + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            mn = fminf(mn, x[e]);
+            mx = fmaxf(mx, x[e]);
+        }
+        const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+        const __half z16 = __float2half_rn(mn);
+        const float sf = __half2float(s16), zf = __half2float(z16);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            int c = 0;
+            if (sf > 0.f)
+                c = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(x[e], zf), sf)), 0), 3);
+            vc[t][32 * cg + e] = static_cast<uint8_t>(c);
+        }
+        sv[t][cg] = h_bits(s16);
+        zv[t][cg] = h_bits(z16);
+    }
+    __syncthreads();
+    // code words: 256 K words and 256 V words, index (j * 32 + lane) * 4 + w
+    for (uint32_t wi = tid; wi < 256; wi += blockDim.x) {
+        const uint32_t j = wi >> 7, lane = (wi >> 2) & 31, w = wi & 3;
+        const uint32_t gq = lane >> 2, tq = lane & 3;
+        const uint32_t tok = 16 * j + gq + 8 * (w >> 1), base = 32 * tq + 16 * (w & 1);
+        uint32_t kw = 0, vw = 0;
+#pragma unroll
+        for (uint32_t i = 0; i < 16; ++i)
+            kw |= static_cast<uint32_t>(kc[tok][base + i]) << (2 * i);
+#pragma unroll
+        for (uint32_t i = 0; i < 8; ++i) {
+            const uint32_t m = 2 * w + (i >> 2), e = i & 3;
+            const uint32_t dim = 16 * m + gq + 8 * (e & 1);
+            const uint32_t tok0 = 16 * j + 2 * tq + 8 * (e >> 1);
+            vw |= static_cast<uint32_t>(vc[tok0][dim]) << (2 * i);
+            vw |= static_cast<uint32_t>(vc[tok0 + 1][dim]) << (16 + 2 * i);
+        }
+        tile[wi] = kw;
+        tile[256 + wi] = vw;
+    }
+    {
+        // K meta: ((t * 2 + h) * 8 + i) * 2 + which
+        const uint32_t which = tid & 1, i = (tid >> 1) & 7, hh = (tid >> 4) & 1, tq = tid >> 5;
+        const uint32_t ch = 32 * tq + 16 * hh + i;
+        const uint16_t *src = which ? zk : sk;
+        tile[512 + tid] = static_cast<uint32_t>(src[ch]) | (static_cast<uint32_t>(src[ch + 8]) << 16);
+        // V meta: ((j * 8 + p) * 4 + c) * 2 + which
+        const uint32_t cg = (tid >> 1) & 3, p = (tid >> 3) & 7, j = tid >> 6;
+        const uint32_t tok = 16 * j + 2 * p;
+        const uint16_t(*vsrc)[4] = which ? zv : sv;
+        tile[640 + tid] = static_cast<uint32_t>(vsrc[tok][cg]) | (static_cast<uint32_t>(vsrc[tok + 1][cg]) << 16);
+    }
+    __syncthreads();
+    uint32_t *dst = reinterpret_cast<uint32_t *>(gpool + static_cast<uint64_t>(job.gpage) * g.group_page_bytes +
+                                                 static_cast<uint64_t>(lh) * kTile);
+    for (uint32_t i = tid; i < kTile / 4; i += blockDim.x)
+        dst[i] = tile[i];
+    if (lh == 0 && tid == 0) {
+        int32_t *trow = table + static_cast<size_t>(job.slot) * g.mb;
+        trow[2 * job.group] = KVS_TABLE_GROUP(job.gpage);
+        trow[2 * job.group + 1] = KVS_TABLE_GROUP(job.gpage);
+    }
+}
+
+// -------------------------------------------------------------------- decode
+struct KArgs {
+    Geo g;
+    Work w;
+    const uint16_t *q;
+    const int32_t *table;
+    const uint8_t *gpool;
+    uint32_t n_items;
+};
+
+struct KItem {
+    uint32_t valid;
+    uint32_t ci, l, kvh;
+    uint32_t g0;        // first group
+    uint32_t ng;        // groups in the item
+    uint32_t part, lse0;
+};
+
+struct KPrep {
+    KItem it;
+    int32_t gp[2];      // group pages: lane j holds groups j and j + 32
+};
+
+__device__ __forceinline__ KPrep prepare_kitem(const KArgs &a, uint32_t id, uint32_t lane)
+{
+    KPrep p;
+    p.it.valid = 0;
+    p.it.ng = 0;
+    if (id >= a.n_items)
+        return p;
+    const DSet *ds = a.w.dset;
+    const Geo &g = a.g;
+    const uint32_t ci = find_seq(&ds->seq[0].item_off_q, sizeof(DSeq) / 4, ds->nseq, id);
+    const DSeq &sq = ds->seq[ci];
+    uint32_t local = id - sq.item_off_q;
+    const uint32_t kvh = local % g.Hkv;
+    local /= g.Hkv;
+    const uint32_t chunk = local % sq.nchunk_q;
+    const uint32_t l = local / sq.nchunk_q;
+    const uint32_t b0 = chunk * ds->chunk;
+    const uint32_t nblk = min(ds->chunk, sq.qb - b0);
+    p.it.valid = 1;
+    p.it.ci = ci;
+    p.it.l = l;
+    p.it.kvh = kvh;
+    p.it.g0 = b0 / 2;
+    p.it.ng = nblk / 2;
+    p.it.part = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk + chunk;
+    p.it.lse0 = sq.blk_off + b0;
+    const int32_t *trow = a.table + static_cast<size_t>(sq.slot) * g.mb + b0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const uint32_t j = lane + 32 * q;
+        int32_t gp = 0;
+        if (j < p.it.ng) {
+            const int32_t v = __ldg(trow + 2 * j);
+            gp = -2 - v;
+            if (v > -2 || gp >= static_cast<int32_t>(g.kivi_groups)) {
+                atomicOr(a.w.err, kErrBadPage);
+                atomicCAS(a.w.err_info, 0u, static_cast<uint32_t>(v) | 0x80000000u);
+                gp = 0;
+            }
+        }
+        p.gp[q] = gp;
+    }
+    return p;
+}
+
+struct KRing {
+    uint32_t inflight, st_issue, st_cons, ph_cons;
+};
+
+// Issues the next group tile of the warp's stream (items cur, then nxt).
+__device__ __forceinline__ bool kissue_next(const KArgs &a, const KPrep &cur, const KPrep &nxt, bool have_nxt,
+                                            bool &c_in_nxt, uint32_t &c_grp, KRing &rg, uint32_t ring_u32,
+                                            uint64_t *bars, uint32_t lane)
+{
+    if (!c_in_nxt && c_grp >= cur.it.ng) {
+        if (!have_nxt || !nxt.it.valid)
+            return false;
+        c_in_nxt = true;
+        c_grp = 0;
+    }
+    if (c_in_nxt && c_grp >= nxt.it.ng)
+        return false;
+    const KPrep &pp = c_in_nxt ? nxt : cur;
+    const int32_t gsel = c_grp < 32 ? pp.gp[0] : pp.gp[1];
+    const int32_t gp = __shfl_sync(0xffffffffu, gsel, c_grp & 31);
+    if (lane == 0) {
+        const uint32_t st = rg.st_issue;
+        const uint32_t bar = smem_u32(&bars[st]);
+        mbar_expect_tx(bar, kTile);
+        const uint8_t *src = a.gpool + static_cast<uint64_t>(gp) * a.g.group_page_bytes +
+                             (static_cast<uint64_t>(pp.it.l) * a.g.Hkv + pp.it.kvh) * kTile;
+        bulk_load(ring_u32 + st * kTile, src, kTile, bar);
+    }
+    ++c_grp;
+    ++rg.inflight;
+    rg.st_issue = rg.st_issue + 1 == kKRing ? 0 : rg.st_issue + 1;
+    return true;
+}
+
+// Pair i of code word w -> f16 pair (code * scale + zero), one rounding.
+__device__ __forceinline__ uint32_t kdq(uint32_t w, int i, uint32_t s2, uint32_t z2)
+{
+    const uint32_t x = ((w >> (2 * i)) & 0x00030003u) | 0x64006400u;       // f16 1024 + code
+    const __half2 c = __hsub2(*reinterpret_cast<const __half2 *>(&x), __halves2half2(__ushort_as_half(0x6400),
+                                                                                     __ushort_as_half(0x6400)));
+    const __half2 r = __hfma2(c, *reinterpret_cast<const __half2 *>(&s2), *reinterpret_cast<const __half2 *>(&z2));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t lo_bits, uint32_t hi_bits)
+{
+    return pack_f16(__uint_as_float(lo_bits << 16), __uint_as_float(hi_bits << 16));
+}
+
+__global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(const KArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t ksm_raw[];
+    __shared__ __align__(8) uint64_t bars[kKWarps][kKRing];
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ksm_raw) + 127) & ~uintptr_t(127));
+    const uint32_t ring_u32 = smem_u32(smem + warp * kKRing * kTile);
+    if (lane == 0) {
+        for (int s = 0; s < kKRing; ++s)
+            mbar_init(smem_u32(&bars[warp][s]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+
+    const Geo &g = a.g;
+    const uint32_t G = g.G;
+    const uint32_t gq = lane >> 2, tq = lane & 3;
+    const uint32_t h0 = 2 * tq, h1 = 2 * tq + 1;
+    const float scale_log2 = rsqrtf(static_cast<float>(kKD)) * kLog2e;
+    const uint32_t nb_total = a.w.dset->nb_total;
+    uint32_t *counter = a.w.counter + 1;
+
+    uint32_t claimed = 0;
+    if (lane == 0)
+        claimed = atomicAdd(counter, 1u);
+    KPrep cur = prepare_kitem(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+    if (lane == 0)
+        claimed = atomicAdd(counter, 1u);
+    KPrep nxt;
+    nxt.it.valid = 0;
+    nxt.it.ng = 0;
+    bool have_nxt = false;
+    KRing rg{0, 0, 0, 0};
+    bool c_in_nxt = false;
+    uint32_t c_grp = 0;
+    if (cur.it.valid)
+        while (rg.inflight < kKRing &&
+               kissue_next(a, cur, nxt, have_nxt, c_in_nxt, c_grp, rg, ring_u32, bars[warp], lane)) {
+        }
+
+    while (cur.it.valid) {
+        const KItem it = cur.it;
+        const uint32_t kvh = it.kvh;
+        // query fragments for the lane's head gq: channels 32tq + 16(ks/4) +
+        // {i0, i0+8} (b0) and {i0+1, i0+9} (b1), i0 = 2(ks%4) -- the pairs
+        // the K code words hold
+        uint32_t qf[8][2];
+        {
+            const bool valid = gq < G;
+            const uint16_t *qh = a.q + ((static_cast<size_t>(it.ci) * g.L + it.l) * g.Hq + kvh * G +
+                                        (valid ? gq : 0)) * kKD + 32 * tq;
+            uint32_t qw[16];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint4 x = valid ? __ldg(reinterpret_cast<const uint4 *>(qh) + v) : make_uint4(0, 0, 0, 0);
+                qw[4 * v] = x.x;
+                qw[4 * v + 1] = x.y;
+                qw[4 * v + 2] = x.z;
+                qw[4 * v + 3] = x.w;
+            }
+            auto qel = [&](int c) -> uint32_t {     // bf16 bits of channel 32tq + c
+                return (qw[c >> 1] >> (16 * (c & 1))) & 0xffffu;
+            };
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int b = 16 * (ks >> 2), i0 = 2 * (ks & 3);
+                qf[ks][0] = bf16x2_to_f16x2(qel(b + i0), qel(b + i0 + 8));
+                qf[ks][1] = bf16x2_to_f16x2(qel(b + i0 + 1), qel(b + i0 + 9));
+            }
+        }
+        float o[8][4];
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+            o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float *lse_row0 = a.w.lse_blk + (static_cast<size_t>(it.l) * g.Hq + kvh * G + h0) * nb_total + it.lse0;
+
+        for (uint32_t gi = 0; gi < it.ng; ++gi) {
+            mbar_wait(smem_u32(&bars[warp][rg.st_cons]), rg.ph_cons, a.w.err);
+            const uint32_t base = ring_u32 + rg.st_cons * kTile;
+            // K (scale, zero) pairs of the lane's channels: [h][i][scale, zero]
+            uint32_t km[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint4 x = lds128(base + 2048 + tq * 128 + 16 * v);
+                km[4 * v] = x.x;
+                km[4 * v + 1] = x.y;
+                km[4 * v + 2] = x.z;
+                km[4 * v + 3] = x.w;
+            }
+#pragma unroll
+            for (uint32_t j = 0; j < 2; ++j) {
+                const uint4 kw4 = lds128(base + (j * 32 + lane) * 16);
+                const uint4 vw4 = lds128(base + 1024 + (j * 32 + lane) * 16);
+                // V (scale, zero) pairs: token pairs tq and tq + 4, channel groups 0..3
+                uint32_t vm[2][8];
+#pragma unroll
+                for (int hp = 0; hp < 2; ++hp) {
+                    const uint32_t a0 = base + 2560 + ((j * 8 + tq + 4 * hp) * 4) * 8;
+                    const uint4 x = lds128(a0), y = lds128(a0 + 16);
+                    vm[hp][0] = x.x; vm[hp][1] = x.y; vm[hp][2] = x.z; vm[hp][3] = x.w;
+                    vm[hp][4] = y.x; vm[hp][5] = y.y; vm[hp][6] = y.z; vm[hp][7] = y.w;
+                }
+                if (j == 1) {
+                    // every lane has read the tile: refill the stage
+                    __syncwarp();
+                    --rg.inflight;
+                    if (++rg.st_cons == kKRing) {
+                        rg.st_cons = 0;
+                        rg.ph_cons ^= 1u;
+                    }
+                    if (rg.inflight < kKRing)
+                        kissue_next(a, cur, nxt, have_nxt, c_in_nxt, c_grp, rg, ring_u32, bars[warp], lane);
+                }
+                const uint32_t kw[4] = {kw4.x, kw4.y, kw4.z, kw4.w};
+                const uint32_t vw[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
+
+                // S^T = K . Q^T (16 tokens x 8 heads)
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int w = ks >> 2, i0 = 2 * (ks & 3);
+                    const uint32_t sa = km[(w * 8 + i0) * 2], za = km[(w * 8 + i0) * 2 + 1];
+                    const uint32_t sb = km[(w * 8 + i0 + 1) * 2], zb = km[(w * 8 + i0 + 1) * 2 + 1];
+                    mma_f16(s, kdq(kw[w], i0, sa, za), kdq(kw[2 + w], i0, sa, za), kdq(kw[w], i0 + 1, sb, zb),
+                            kdq(kw[2 + w], i0 + 1, sb, zb), qf[ks][0], qf[ks][1]);
+                }
+                s[0] *= scale_log2;
+                s[1] *= scale_log2;
+                s[2] *= scale_log2;
+                s[3] *= scale_log2;
+
+                float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                for (int x = 4; x < 32; x <<= 1) {
+                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+                }
+                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+                const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
+                const float p0 = fast_exp2(s[0] - mn0), p1 = fast_exp2(s[1] - mn1);
+                const float p2 = fast_exp2(s[2] - mn0), p3 = fast_exp2(s[3] - mn1);
+                float w0 = p0 + p2, w1 = p1 + p3;
+#pragma unroll
+                for (int x = 4; x < 32; x <<= 1) {
+                    w0 += __shfl_xor_sync(0xffffffffu, w0, x);
+                    w1 += __shfl_xor_sync(0xffffffffu, w1, x);
+                }
+                l0 = l0 * sc0 + w0;
+                l1 = l1 * sc1 + w1;
+                m0 = mn0;
+                m1 = mn1;
+                const uint32_t bi = 2 * gi + j;
+                if (gq == 0) {
+                    if (h0 < G)
+                        lse_row0[bi] = mn0 + fast_log2(w0);
+                    if (h1 < G)
+                        lse_row0[nb_total + bi] = mn1 + fast_log2(w1);
+                }
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    o[mt][0] *= sc0;
+                    o[mt][1] *= sc1;
+                    o[mt][2] *= sc0;
+                    o[mt][3] *= sc1;
+                }
+                const uint32_t pb0 = movmatrix_t(pack_f16(p0, p1));
+                const uint32_t pb1 = movmatrix_t(pack_f16(p2, p3));
+                // O^T += V^T . P^T; m-tile m: channels 16m .. 16m+15, channel group m/2
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    const int w = mt >> 1, cg = mt >> 1, i = 4 * (mt & 1);
+                    mma_f16(o[mt], kdq(vw[w], i, vm[0][2 * cg], vm[0][2 * cg + 1]),
+                            kdq(vw[w], i + 1, vm[0][2 * cg], vm[0][2 * cg + 1]),
+                            kdq(vw[w], i + 2, vm[1][2 * cg], vm[1][2 * cg + 1]),
+                            kdq(vw[w], i + 3, vm[1][2 * cg], vm[1][2 * cg + 1]), pb0, pb1);
+                }
+            }
+            if (gi == 0 && !have_nxt) {
+                nxt = prepare_kitem(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+                have_nxt = true;
+                if (lane == 0 && nxt.it.valid)
+                    claimed = atomicAdd(counter, 1u);
+                while (rg.inflight < kKRing &&
+                       kissue_next(a, cur, nxt, have_nxt, c_in_nxt, c_grp, rg, ring_u32, bars[warp], lane)) {
+                }
+            }
+        }
+
+        const uint32_t part = it.part;
+        if (gq == 0) {
+            a.w.part_ml[part * kMaxGroup + h0] = make_float2(m0, l0);
+            a.w.part_ml[part * kMaxGroup + h1] = make_float2(m1, l1);
+        }
+        float *po = a.w.part_o + static_cast<size_t>(part) * kMaxGroup * kKD;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            po[h0 * kKD + mt * 16 + gq] = o[mt][0];
+            po[h1 * kKD + mt * 16 + gq] = o[mt][1];
+            po[h0 * kKD + mt * 16 + gq + 8] = o[mt][2];
+            po[h1 * kKD + mt * 16 + gq + 8] = o[mt][3];
+        }
+        if (!have_nxt) {
+            nxt = prepare_kitem(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+            if (lane == 0 && nxt.it.valid)
+                claimed = atomicAdd(counter, 1u);
+        }
+        if (c_in_nxt)
+            c_in_nxt = false;
+        else
+            c_grp = 0;
+        cur = nxt;
+        have_nxt = false;
+        nxt.it.valid = 0;
+        nxt.it.ng = 0;
+        while (cur.it.valid && rg.inflight < kKRing &&
+               kissue_next(a, cur, nxt, have_nxt, c_in_nxt, c_grp, rg, ring_u32, bars[warp], lane)) {
+        }
+    }
+}
+
+constexpr size_t kKSmem = static_cast<size_t>(kKWarps) * kKRing * kTile + 128;
+
+}  // namespace
+
+cudaError_t launch_kivi_compress(const Geo &g, const KiviJob *jobs, uint32_t njobs, const uint8_t *pool,
+                                 uint8_t *gpool, int32_t *table, cudaStream_t s)
+{
+    if (njobs == 0)
+        return cudaSuccess;
+    kivi_compress_kernel<<<njobs * g.L * g.Hkv, 128, 0, s>>>(g, jobs, pool, gpool, table);
+    return cudaGetLastError();
+}
+
+int decode_kivi_blocks_per_sm(const Geo &)
+{
+    int n = 0;
+    cudaFuncSetAttribute(decode_kivi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kKSmem));
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kivi_kernel, 32 * kKWarps, kKSmem);
+    return n;
+}
+
+cudaError_t launch_decode_kivi(const Geo &g, const Work &w, const uint16_t *q, const int32_t *table,
+                               const uint8_t *gpool, uint32_t n_items, int grid, cudaStream_t s)
+{
+    if (n_items == 0)
+        return cudaSuccess;
+    KArgs a{g, w, q, table, gpool, n_items};
+    const int need = static_cast<int>((n_items + kKWarps - 1) / kKWarps);
+    decode_kivi_kernel<<<need < grid ? need : grid, 32 * kKWarps, kKSmem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kvs

@@ -50,18 +50,19 @@ class Run:
 
     def __init__(self, wl, alpha, *, staging_pages=8, chunk=4096, oracle_on=True,
                  oracle_seqs=None, pool_pages=None, extra_steps=0, device="cuda",
-                 kv_dtype=K.KVS_KV_BF16, k_scale=1.0, v_scale=1.0):
+                 kv_dtype=K.KVS_KV_BF16, k_scale=1.0, v_scale=1.0, kivi_groups=0):
         self.wl, self.alpha = wl, alpha
         self.dev = device
         self.ids = seq_ids_for(wl)
         self.mb = wl.max_blocks_per_seq() + (extra_steps + 15) // 16
         self.fp8 = kv_dtype == K.KVS_KV_FP8_E4M3
+        self.kivi = kv_dtype == K.KVS_KV_KIVI2
         self.k_scale, self.v_scale = k_scale, v_scale
         cfg = K.make_config(wl.L, wl.Hq, wl.Hkv, wl.d, pool_pages or wl.pool_pages, max_seqs=wl.nseq,
                             max_blocks_per_seq=self.mb, alpha=alpha,
                             recency_window=wl.recency_window, weights=wl.weights, cuts=wl.cuts,
                             pool_seed=wl.seed, staging_pages=staging_pages, kv_dtype=kv_dtype,
-                            k_scale=k_scale, v_scale=v_scale)
+                            k_scale=k_scale, v_scale=v_scale, kivi_groups=kivi_groups)
         self.ctx = K.Context(cfg)
         self.oracle_on = oracle_on
         track = set(range(wl.nseq)) if oracle_seqs is None else set(oracle_seqs)
@@ -162,7 +163,10 @@ class Run:
             if sid not in self.orc:
                 continue
             o = self.orc[sid]
-            if self.fp8:       # the pages hold codes of the bf16 inputs
+            if self.kivi:      # whole groups behind the residual window are 2-bit
+                Kf, Vf = O.kivi_effective(o.K, o.V)
+                r = O.decode_with_mass(q[s], Kf, Vf, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d)
+            elif self.fp8:     # the pages hold codes of the bf16 inputs
                 kc, vc = self.codes(o.K, o.V)
                 r = O.decode_with_mass(q[s], kc, vc, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d,
                                        k_lut=O.e4m3_lut(self.k_scale), v_lut=O.e4m3_lut(self.v_scale))
@@ -238,6 +242,11 @@ class Run:
         if self.fp8:
             return O.assemble_page(*self.codes(Kb, Vb), B)
         return O.assemble_page(Kb, Vb, B)
+
+    def oracle_group_page(self, sid, grp):
+        o = self.orc[sid]
+        a = grp * O.KIVI_GROUP
+        return O.kivi_group_page(o.K[a:a + O.KIVI_GROUP], o.V[a:a + O.KIVI_GROUP])
 
     def close(self):
         self.ctx.close()

@@ -156,6 +156,83 @@ def test_fp8_config_checks():
                                            k_scale=0.0))
 
 
+# ------------------------------------------------------------ KIVI 2-bit
+
+
+def _check_kivi_groups(run):
+    """Every quantised group: both blocks name one group page whose bytes are
+    the oracle's quantisation in the tile layout; the rest are bf16 pages."""
+    n_groups = 0
+    for sid in run.tracked:
+        _, ntok, nb, table = run.ctx.seq_info(sid)
+        q = O.kivi_quantized_tokens(ntok)
+        for b, p in enumerate(table):
+            if b < q // 16:
+                assert p <= -2 and table[b ^ 1] == p, (sid, b, p)
+            else:
+                assert p >= 0, (sid, b, p)
+        for grp in range(q // 32):
+            gp = -2 - table[2 * grp]
+            got = run.ctx.group_bytes_of(gp).cpu().numpy().tobytes()
+            assert got == run.oracle_group_page(sid, grp), (sid, grp)
+            n_groups += 1
+    return n_groups
+
+
+def test_kivi_parity():
+    """2-bit groups behind a 128-token residual window: group pages equal the
+    oracle's quantisation byte for byte; decode over groups + residual pages
+    matches the oracle on the effective values while sequences cross group
+    boundaries, through both append paths; selection returns ids only."""
+    wl = W.workload("l70b_8k", L=3, prefill_lens=(300, 1000, 17, 477), pool_pages=140, steps=40)
+    run = Run(wl, 0.15, kv_dtype=K.KVS_KV_KIVI2, kivi_groups=64)
+    assert _check_kivi_groups(run) == (160 + 864 + 0 + 320) // 32
+    for i in range(wl.steps):
+        res = run.step(None, batched_append=bool(i % 2))
+        summ = run.compare(res)
+        if i % 13 == 0:         # the THRESH list (ids only in 2-bit contexts)
+            excl = run.excluded_keys()
+            got = [k for k in res["ids"] if k not in excl]
+            assert got == [k for k in O.select_thresh({s: run.orc[s].rec for s in run.ids}) if k not in excl]
+            assert res["gather"].n_pages == 0
+    n = _check_kivi_groups(run)
+    assert n == (192 + 896 + 0 + 384) // 32
+    run.ctx.check_device()
+    print("kivi", summ, n, "groups")
+    run.close()
+
+
+def test_kivi_error_paths():
+    wl = W.workload("l70b_8k", L=2, prefill_lens=(300,), pool_pages=40, steps=2)
+    cfg = K.make_config(wl.L, wl.Hq, wl.Hkv, wl.d, 40, 2, 40, kv_dtype=K.KVS_KV_KIVI2, kivi_groups=4)
+    ctx = K.Context(cfg)
+    Kt, Vt = W.kv_tokens(wl, 0, 0, 300, "cuda")
+    ctx.seq_add(1)
+    with pytest.raises(K.KvsError) as e:          # 300 tokens need 5 groups: nothing appended
+        ctx.append_tokens(1, Kt, Vt)
+    assert e.value.code == K.KVS_ENOMEM and ctx.seq_info(1)[1] == 0
+    ctx.append_tokens(1, Kt[:200].contiguous(), Vt[:200].contiguous())    # 2 groups
+    _, ntok, nb, t = ctx.seq_info(1)
+    assert ntok == 200 and nb == 13
+    assert t[0] == t[1] <= -2 and t[2] == t[3] <= -2 and t[0] != t[2] and min(t[4:]) >= 0
+    with pytest.raises(K.KvsError) as e:          # no shared blocks in 2-bit contexts
+        ctx.seq_add(2, 1, 2)
+    assert e.value.code == K.KVS_EINVAL
+    q = torch.zeros((1, wl.L, wl.Hq, wl.d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((1, wl.L, wl.Hq, wl.d), device="cuda")
+    ctx.decode_step([1], q, out)
+    ctx.score_update()
+    host = _pinned(4 * ctx.page_bytes)
+    with pytest.raises(K.KvsError) as e:          # no gathers of group pages
+        ctx.select_and_gather(K.KVS_SELECT_THRESH, host)
+    assert e.value.code == K.KVS_EINVAL
+    free = ctx.free_pages()
+    ctx.seq_remove(1)
+    assert ctx.free_pages() == free + (200 - 64 + 15) // 16
+    ctx.check_device()
+    ctx.close()
+
+
 # --------------------------------------------------------------- scoring
 
 
