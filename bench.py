@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--impl", choices=["kvs", "reference"], default="kvs")
     ap.add_argument("--workload", default="l70b_128k")
     ap.add_argument("--alpha", type=float, default=None)
-    ap.add_argument("--gather", choices=["auto", "mirror", "list", "demote", "prefetch", "none"],
+    ap.add_argument("--gather", choices=["auto", "mirror", "list", "demote", "prefetch", "ids", "none"],
                     default="auto",
                     help="auto: demote for workloads with periodic demotion, else mirror; prefetch: "
                          "demoted blocks come back in fetch order, a budget per step, while the "
@@ -54,8 +54,9 @@ def parse():
     ap.add_argument("--victims", choices=["lowfrac", "lrfu"], default="lowfrac",
                     help="demotion victims: smallest P, or smallest LRFU key (lazily decayed "
                          "EMA of touches)")
-    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
-                    help="page element type: bf16, or FP8 E4M3 codes (per-tensor scale 1.0)")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8", "kivi2"], default="bf16",
+                    help="page element type: bf16, FP8 E4M3 codes (per-tensor scale 1.0), or 2-bit "
+                         "groups behind a 128-token bf16 residual window")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-literal", action="store_true")
@@ -200,12 +201,21 @@ class Pipeline:
         need = sum((n + steps_total + B - 1) // B for n in wl.prefill_lens)
         need -= (wl.shared_prefix_tokens // B) * (wl.nseq - 1)
         self.pool_pages = max(wl.pool_pages, need + 8)
+        self.kivi = kv_dtype == "kivi2"
+        groups = 0
+        if self.kivi:
+            # bf16 pages hold the residual windows (at most 160 + 15 tokens each)
+            # and one prefill chunk in flight; group pages hold the rest
+            self.pool_pages = wl.nseq * 12 + self.PREFILL_CHUNK // B + 16
+            groups = sum((n + steps_total) // K.KVS_KIVI_GROUP_TOKENS for n in wl.prefill_lens) + wl.nseq
+        dt = {"bf16": K.KVS_KV_BF16, "fp8": K.KVS_KV_FP8_E4M3, "kivi2": K.KVS_KV_KIVI2}[kv_dtype]
         cfg = K.make_config(wl.L, wl.Hq, wl.Hkv, wl.d, self.pool_pages, wl.nseq, mb, alpha=alpha,
                             recency_window=wl.recency_window, weights=wl.weights, cuts=wl.cuts,
-                            pool_seed=wl.seed, staging_pages=32,
-                            kv_dtype=K.KVS_KV_FP8_E4M3 if kv_dtype == "fp8" else K.KVS_KV_BF16)
+                            pool_seed=wl.seed, staging_pages=32, kv_dtype=dt, kivi_groups=groups)
         self.ctx = K.Context(cfg, device)
         self.token_bytes = wl.token_bytes // (2 if kv_dtype == "fp8" else 1)
+        # 2-bit groups: 3 KiB per (layer, KV head) and 32 tokens
+        self.group_token_bytes = wl.L * wl.Hkv * 3072 // 32
         self.side = torch.cuda.Stream(device)
         self.out = torch.empty((wl.nseq, wl.L, wl.Hq, wl.d), dtype=torch.float32, device=device)
         self.host = None
@@ -236,9 +246,12 @@ class Pipeline:
             torch.cuda.synchronize()
             del z
 
-    def prefill(self, chunk=4096):
+    PREFILL_CHUNK = 4096
+
+    def prefill(self, chunk=PREFILL_CHUNK):
         wl, W = self.wl, self.W
-        pre = wl.shared_prefix_tokens // wl.block_tokens
+        # 2-bit group contexts share no pages: each sequence holds its own prefix
+        pre = 0 if self.kivi else wl.shared_prefix_tokens // wl.block_tokens
         for s, sid in enumerate(self.ids):
             if s > 0 and pre:
                 self.ctx.seq_add(sid, self.ids[0], pre)
@@ -271,7 +284,14 @@ class Pipeline:
         return kv, qs
 
     def kv_bytes_this_step(self):
-        # tokens attended (after append) by the sequences decoded this step
+        # bytes of the tokens attended (after append) by the sequences decoded this step
+        if self.kivi:
+            tot = 0
+            for i in self.active:
+                n = self.ntok[i]
+                q = 32 * (max(0, n - 128) // 32)
+                tot += q * self.group_token_bytes + (n - q) * self.token_bytes
+            return tot
         return sum(self.ntok[i] for i in self.active) * self.token_bytes
 
     def _rows(self, x, active):
@@ -320,7 +340,9 @@ class Pipeline:
             ev[3].record(main)
         r = None
         self.steps_done += 1
-        if self.gather in ("mirror", "list"):
+        if self.gather == "ids":            # the THRESH list only, no page copies
+            rc, r = ctx.select_and_gather(K.KVS_SELECT_THRESH, None)
+        elif self.gather in ("mirror", "list"):
             flags = K.KVS_GATHER_MIRROR if self.gather == "mirror" else 0
             if mode_flags is not None:
                 flags = mode_flags
@@ -383,7 +405,7 @@ def run_kvs(args):
     wl = W.workload(args.workload)
     alpha = args.alpha if args.alpha is not None else wl.alphas[-1]
     if args.gather == "auto":
-        args.gather = "demote" if wl.demote_every else "mirror"
+        args.gather = "ids" if args.kv_dtype == "kivi2" else ("demote" if wl.demote_every else "mirror")
     K_, W_ = args.steps, args.warmup
     e2e_steps = 0 if args.no_e2e else K_
     lit_steps = 0 if (args.no_literal or args.gather not in ("mirror", "list")) else 2
@@ -408,7 +430,7 @@ def run_kvs(args):
     decoded = 0                     # sequence-steps decoded (all, unless prefetch pauses some)
     uniq_bytes = 0
     staged = 0
-    shared_extra = wl.shared_prefix_tokens * (wl.nseq - 1) * pipe.token_bytes
+    shared_extra = 0 if pipe.kivi else wl.shared_prefix_tokens * (wl.nseq - 1) * pipe.token_bytes
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -452,7 +474,7 @@ def run_kvs(args):
     algo = kv_bytes / K_ + wl.nseq * wl.L * wl.Hq * wl.d * 2 + sum(nb) * 4
     achieved = algo / (dec_avg / 1e3) / 1e9
     peak, peak_src = read_peaks()
-    traffic = read_traffic(args.workload + ("" if args.kv_dtype == "bf16" else "_fp8"))
+    traffic = read_traffic(args.workload + ("" if args.kv_dtype == "bf16" else "_" + args.kv_dtype))
 
     # ---- end to end through host buffers --------------------------------
     e2e = None
@@ -523,7 +545,9 @@ def run_kvs(args):
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
             "steps": K_, "warmup": W_, "ms_per_step": round(ms_max / K_, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if args.kv_dtype == "bf16" else "e4m3 KV, f16 MMA, fp32 accumulate",
+            "dtype": {"bf16": "bf16", "fp8": "e4m3 KV, f16 MMA, fp32 accumulate",
+                      "kivi2": "2-bit KV groups (fp16 scale/zero) + bf16 residual window, f16 MMA, "
+                               "fp32 accumulate"}[args.kv_dtype],
             "data": "synthetic (seeded generator; recency-skewed K/V)",
             "config": {"workload": f"{wl.name}: {wl.nseq} seq x "
                                    f"{wl.prefill_lens[0] if wl.nseq == 1 else f'{min(wl.prefill_lens)}..{max(wl.prefill_lens)}'} "

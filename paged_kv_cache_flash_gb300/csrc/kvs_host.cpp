@@ -775,6 +775,8 @@ int kvs_seq_add(kvs_ctx_t *ctx, uint64_t seq_id, int64_t parent, uint32_t shared
     if (ctx->free_slots.empty())
         return fail(ctx, KVS_ENOMEM, "no free sequence slot (max_seqs %u)", ctx->cfg.max_seqs);
     SeqState *par = nullptr;
+    if (shared_blocks && ctx->geo.kivi)
+        return fail(ctx, KVS_EINVAL, "2-bit group contexts share no blocks");
     if (parent >= 0) {
         par = find_seq(ctx, static_cast<uint64_t>(parent));
         if (!par)
@@ -788,8 +790,6 @@ int kvs_seq_add(kvs_ctx_t *ctx, uint64_t seq_id, int64_t parent, uint32_t shared
     } else if (shared_blocks) {
         return fail(ctx, KVS_EINVAL, "shared blocks need a parent");
     }
-    if (shared_blocks && ctx->geo.kivi)
-        return fail(ctx, KVS_EINVAL, "2-bit group contexts share no blocks");
     if (shared_blocks > ctx->cfg.max_blocks_per_seq)
         return fail(ctx, KVS_EINVAL, "shared prefix longer than a table row");
     const uint32_t slot = ctx->free_slots.back();

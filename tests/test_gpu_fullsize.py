@@ -61,6 +61,19 @@ def test_fp8_8k_full_size():
     run.close()
 
 
+def test_kivi_8k_full_size():
+    """The 8K workload with 2-bit groups behind the residual window, 2 steps,
+    full oracle on the effective values; 3 group pages byte for byte."""
+    from test_gpu_parity import _check_kivi_groups
+    wl = W.workload("l70b_8k", steps=2)
+    run = Run(wl, 0.15, kv_dtype=K.KVS_KV_KIVI2, kivi_groups=8192 // 32 + 4)
+    for _ in range(wl.steps):
+        summ = run.compare(run.step(None))
+    assert _check_kivi_groups(run, sample=3) == O.kivi_quantized_tokens(8194) // 32
+    print("kivi 8k", summ)
+    run.close()
+
+
 def test_128k_full_size():
     """1 sequence of 131,072 tokens (8,192 blocks, 40 GiB), 2 steps: outputs,
     masses and records against the full oracle; the P < 0.3 list in full and
