@@ -344,9 +344,10 @@ def kivi_group_tile(ck, sk, zk, cv, sv, zv) -> bytes:
                              is m = 2w + i // 4, e = i % 4: dim 16m + g +
                              8*(e % 2), token 16j + 2t + 8*(e // 2) at bits 2i
                              and the next token at bits 16 + 2i.
-      K meta   [2048, 2560): [t][half h in 0..1][i in 0..7] of (scale pair,
-                             zero pair), each pair two fp16: channel
-                             32t + 16h + i (low), that channel + 8 (high).
+      K meta   [2048, 2560): [half h in 0..1][ip in 0..3][t] of (scale pair,
+                             zero pair) for i = 2ip, then for i = 2ip + 1;
+                             each pair two fp16: channel 32t + 16h + i
+                             (low), that channel + 8 (high).
       V meta   [2560, 3072): [block j][token pair p in 0..7][channel group
                              c in 0..3] of (scale pair, zero pair): tokens
                              16j + 2p (low) and 16j + 2p + 1 (high).
@@ -373,13 +374,14 @@ def kivi_group_tile(ck, sk, zk, cv, sv, zv) -> bytes:
                 vc[j, lane, w] = word
     f16 = lambda a: np.asarray(a, np.float16).view(np.uint16).astype(np.uint32)
     skb, zkb = f16(sk), f16(zk)
-    km = np.zeros((4, 2, 8, 2), np.uint32)
-    for t in range(4):
-        for h in range(2):
-            for i in range(8):
-                ch = 32 * t + 16 * h + i
-                km[t, h, i, 0] = skb[ch] | (skb[ch + 8] << 16)
-                km[t, h, i, 1] = zkb[ch] | (zkb[ch + 8] << 16)
+    km = np.zeros((2, 4, 4, 2, 2), np.uint32)
+    for h in range(2):
+        for ip in range(4):
+            for t in range(4):
+                for di in range(2):
+                    ch = 32 * t + 16 * h + 2 * ip + di
+                    km[h, ip, t, di, 0] = skb[ch] | (skb[ch + 8] << 16)
+                    km[h, ip, t, di, 1] = zkb[ch] | (zkb[ch + 8] << 16)
     svb, zvb = f16(sv), f16(zv)
     vm = np.zeros((2, 8, 4, 2), np.uint32)
     for j in range(2):

@@ -18,9 +18,10 @@
 //                           chunk of groups) items, streams 3 KiB group tiles
 //                           through a bulk-copy ring, dequantises codes in
 //                           registers straight into f16 MMA fragments
-//                           (code pair -> f16 pair by a mask and the 1024
-//                           bias, then one fused multiply-add with the pair's
-//                           scale and zero) and writes the same split-K
+//                           (code pair -> biased f16 pair by one mask-and-or,
+//                           the bias subtracted exactly, then one fused
+//                           multiply-add with the pair's scale and zero) and
+//                           writes the same split-K
 //                           partials and per-block log2-sum-exps.
 //
 // Tile layout (per (layer, KV head) of a group page; lane = 4g + t):
@@ -30,12 +31,16 @@
 //                m-tile m = 2w + i/4, register e = i%4: channel 16m + g +
 //                8(e%2), tokens 16j + 2t + 8(e/2) (bits 2i) and the next one
 //                (bits 16 + 2i).
-//   [2048, 2560) K (scale pair, zero pair) [t][h][i]: channels 32t + 16h + i
-//                (low half) and + 8 (high half).
+//   [2048, 2560) K (scale pair, zero pair) [h][ip][t][i = 2ip, 2ip+1]:
+//                channels 32t + 16h + i (low half) and + 8 (high half); the
+//                four t of one (h, ip) are 64 contiguous bytes, so the 16-byte
+//                loads of the lanes t = 0..3 fall in different banks.
 //   [2560, 3072) V (scale pair, zero pair) [block j][token pair p][channel
 //                group c]: tokens 16j + 2p (low) and 16j + 2p + 1 (high).
-// Pair i of a code word is (word >> 2i) & 0x00030003: two codes, one per
-// 16-bit half -- the operand pair of an f16 MMA register.
+// Pair i of a code word is the two codes at bits 2i and 16 + 2i: the operand
+// pair of an f16 MMA register.  Pair i = p (p < 5) of a word w, or of
+// w >> 10 (p = i - 5), is taken by one mask-and-or into the mantissa of an
+// f16 pair with exponent 25 - 2p: value B_p + code, B_p = 2^(10-2p), exact.
 #include <cuda_fp16.h>
 
 #include "kvs_internal.h"
@@ -157,9 +162,10 @@ __global__ void __launch_bounds__(128)
         tile[256 + wi] = vw;
     }
     {
-        // K meta: ((t * 2 + h) * 8 + i) * 2 + which
-        const uint32_t which = tid & 1, i = (tid >> 1) & 7, hh = (tid >> 4) & 1, tq = tid >> 5;
-        const uint32_t ch = 32 * tq + 16 * hh + i;
+        // K meta: (((h * 4 + ip) * 4 + t) * 2 + di) * 2 + which, i = 2ip + di
+        const uint32_t which = tid & 1, di = (tid >> 1) & 1, tq = (tid >> 2) & 3, ip = (tid >> 4) & 3,
+                       hh = tid >> 6;
+        const uint32_t ch = 32 * tq + 16 * hh + 2 * ip + di;
         const uint16_t *src = which ? zk : sk;
         tile[512 + tid] = static_cast<uint32_t>(src[ch]) | (static_cast<uint32_t>(src[ch + 8]) << 16);
         // V meta: ((j * 8 + p) * 4 + c) * 2 + which
@@ -282,14 +288,34 @@ __device__ __forceinline__ bool kissue_next(const KArgs &a, const KPrep &cur, co
     return true;
 }
 
-// Pair i of code word w -> f16 pair (code * scale + zero), one rounding.
-__device__ __forceinline__ uint32_t kdq(uint32_t w, int i, uint32_t s2, uint32_t z2)
+// Pair I of code word w (w10 = w >> 10) -> f16 pair code * scale + zero,
+// one rounding: the biased pair B_p + code, minus B_p (exact), then one fma.
+template <int I>
+__device__ __forceinline__ uint32_t kdq_at(uint32_t w, uint32_t w10, uint32_t s2, uint32_t z2)
 {
-    const uint32_t x = ((w >> (2 * i)) & 0x00030003u) | 0x64006400u;       // f16 1024 + code
-    const __half2 c = __hsub2(*reinterpret_cast<const __half2 *>(&x), __halves2half2(__ushort_as_half(0x6400),
-                                                                                     __ushort_as_half(0x6400)));
+    constexpr int P = I < 5 ? I : I - 5;
+    constexpr uint32_t M = (3u << (2 * P)) | (3u << (2 * P + 16));
+    constexpr uint32_t E = 25u - 2u * P;
+    constexpr uint32_t C = (E << 10) | (E << 26);         // f16 pair (B_p, B_p)
+    const uint32_t x = ((I < 5 ? w : w10) & M) | C;
+    const uint32_t b = C;
+    const __half2 c = __hsub2(*reinterpret_cast<const __half2 *>(&x), *reinterpret_cast<const __half2 *>(&b));
     const __half2 r = __hfma2(c, *reinterpret_cast<const __half2 *>(&s2), *reinterpret_cast<const __half2 *>(&z2));
     return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint32_t kdq(uint32_t w, uint32_t w10, int i, uint32_t s2, uint32_t z2)
+{
+    switch (i) {    // i is a constant after unrolling
+    case 0: return kdq_at<0>(w, w10, s2, z2);
+    case 1: return kdq_at<1>(w, w10, s2, z2);
+    case 2: return kdq_at<2>(w, w10, s2, z2);
+    case 3: return kdq_at<3>(w, w10, s2, z2);
+    case 4: return kdq_at<4>(w, w10, s2, z2);
+    case 5: return kdq_at<5>(w, w10, s2, z2);
+    case 6: return kdq_at<6>(w, w10, s2, z2);
+    default: return kdq_at<7>(w, w10, s2, z2);
+    }
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
@@ -386,11 +412,11 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
         for (uint32_t gi = 0; gi < it.ng; ++gi) {
             mbar_wait(smem_u32(&bars[warp][rg.st_cons]), rg.ph_cons, a.w.err);
             const uint32_t base = ring_u32 + rg.st_cons * kTile;
-            // K (scale, zero) pairs of the lane's channels: [h][i][scale, zero]
+            // K (scale, zero) pairs of the lane's channels, as km[(h * 8 + i) * 2 + {scale, zero}]
             uint32_t km[32];
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const uint4 x = lds128(base + 2048 + tq * 128 + 16 * v);
+            for (int v = 0; v < 8; ++v) {       // v = h * 4 + ip
+                const uint4 x = lds128(base + 2048 + (v * 4 + tq) * 16);
                 km[4 * v] = x.x;
                 km[4 * v + 1] = x.y;
                 km[4 * v + 2] = x.z;
@@ -422,6 +448,8 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                 }
                 const uint32_t kw[4] = {kw4.x, kw4.y, kw4.z, kw4.w};
                 const uint32_t vw[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
+                const uint32_t kx[4] = {kw4.x >> 10, kw4.y >> 10, kw4.z >> 10, kw4.w >> 10};
+                const uint32_t vx[4] = {vw4.x >> 10, vw4.y >> 10, vw4.z >> 10, vw4.w >> 10};
 
                 // S^T = K . Q^T (16 tokens x 8 heads)
                 float s[4] = {0.f, 0.f, 0.f, 0.f};
@@ -430,8 +458,9 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                     const int w = ks >> 2, i0 = 2 * (ks & 3);
                     const uint32_t sa = km[(w * 8 + i0) * 2], za = km[(w * 8 + i0) * 2 + 1];
                     const uint32_t sb = km[(w * 8 + i0 + 1) * 2], zb = km[(w * 8 + i0 + 1) * 2 + 1];
-                    mma_f16(s, kdq(kw[w], i0, sa, za), kdq(kw[2 + w], i0, sa, za), kdq(kw[w], i0 + 1, sb, zb),
-                            kdq(kw[2 + w], i0 + 1, sb, zb), qf[ks][0], qf[ks][1]);
+                    mma_f16(s, kdq(kw[w], kx[w], i0, sa, za), kdq(kw[2 + w], kx[2 + w], i0, sa, za),
+                            kdq(kw[w], kx[w], i0 + 1, sb, zb), kdq(kw[2 + w], kx[2 + w], i0 + 1, sb, zb),
+                            qf[ks][0], qf[ks][1]);
                 }
                 s[0] *= scale_log2;
                 s[1] *= scale_log2;
@@ -478,10 +507,10 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     const int w = mt >> 1, cg = mt >> 1, i = 4 * (mt & 1);
-                    mma_f16(o[mt], kdq(vw[w], i, vm[0][2 * cg], vm[0][2 * cg + 1]),
-                            kdq(vw[w], i + 1, vm[0][2 * cg], vm[0][2 * cg + 1]),
-                            kdq(vw[w], i + 2, vm[1][2 * cg], vm[1][2 * cg + 1]),
-                            kdq(vw[w], i + 3, vm[1][2 * cg], vm[1][2 * cg + 1]), pb0, pb1);
+                    mma_f16(o[mt], kdq(vw[w], vx[w], i, vm[0][2 * cg], vm[0][2 * cg + 1]),
+                            kdq(vw[w], vx[w], i + 1, vm[0][2 * cg], vm[0][2 * cg + 1]),
+                            kdq(vw[w], vx[w], i + 2, vm[1][2 * cg], vm[1][2 * cg + 1]),
+                            kdq(vw[w], vx[w], i + 3, vm[1][2 * cg], vm[1][2 * cg + 1]), pb0, pb1);
                 }
             }
             if (gi == 0 && !have_nxt) {

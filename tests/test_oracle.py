@@ -699,8 +699,8 @@ def test_kivi_tile_layout_hand_offsets():
     # V: block 1, lane (g 3, t 2), word 1, pair 6 -> m 3, e 2: dim 51, tokens 16+4+8 = 28, 29
     v = tile[256 + (1 * 32 + 14) * 4 + 1]
     assert (v >> 12) & 3 == cv[28, 51] and (v >> 28) & 3 == cv[29, 51]
-    # K meta: t 3, half 1, i 2 -> channels 114 and 122
-    km = tile[512 + ((3 * 2 + 1) * 8 + 2) * 2]
+    # K meta: t 3, half 1, i 2 (ip 1, first of the two) -> channels 114 and 122
+    km = tile[512 + ((1 * 4 + 1) * 4 + 3) * 4]
     assert km & 0xFFFF == sk.view(np.uint16)[114] and km >> 16 == sk.view(np.uint16)[122]
     # V meta: block 1, token pair 5, channel group 2 -> zero of tokens 26, 27
     vm = tile[640 + ((1 * 8 + 5) * 4 + 2) * 2 + 1]
