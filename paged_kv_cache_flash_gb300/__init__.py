@@ -217,6 +217,23 @@ class Context:
             _check(None, lib().kvs_create(ctypes.byref(cfg), ctypes.byref(bufs), ctypes.byref(h)))
         self.h = h
         self.page_bytes = sz.page_bytes
+        self._id_arrays = {}        # ctypes id arrays of recurring sequence lists
+        self._pinned = {}           # data_ptr -> pinned check of host buffers
+
+    def _ids(self, seq_ids):
+        key = tuple(seq_ids)
+        arr = self._id_arrays.get(key)
+        if arr is None:
+            if len(self._id_arrays) > 64:
+                self._id_arrays.clear()
+            arr = self._id_arrays[key] = (c_u64 * len(key))(*key)
+        return arr
+
+    def _host_ok(self, t):
+        ok = self._pinned.get(t.data_ptr())
+        if ok is None:
+            ok = self._pinned[t.data_ptr()] = bool(t.is_pinned())
+        return ok
 
     # -- lifetime --
     def close(self):
@@ -257,16 +274,14 @@ class Context:
         assert k.dtype == t.bfloat16 and v.dtype == t.bfloat16 and k.is_cuda and v.is_cuda
         assert k.is_contiguous() and v.is_contiguous() and k.shape == v.shape
         assert k.shape[0] == len(seq_ids)
-        ids = (c_u64 * len(seq_ids))(*seq_ids)
-        _check(self.h, lib().kvs_append_step(self.h, ids, len(seq_ids), k.data_ptr(), v.data_ptr(),
-                                             _stream_handle(stream)))
+        _check(self.h, lib().kvs_append_step(self.h, self._ids(seq_ids), len(seq_ids), k.data_ptr(),
+                                             v.data_ptr(), _stream_handle(stream)))
 
     def decode_step(self, seq_ids, q, out, stream=None):
         t = self.torch
         assert q.dtype == t.bfloat16 and out.dtype == t.float32
         assert q.is_contiguous() and out.is_contiguous() and q.is_cuda and out.is_cuda
-        ids = (c_u64 * len(seq_ids))(*seq_ids)
-        _check(self.h, lib().kvs_decode_step(self.h, ids, len(seq_ids), q.data_ptr(),
+        _check(self.h, lib().kvs_decode_step(self.h, self._ids(seq_ids), len(seq_ids), q.data_ptr(),
                                              out.data_ptr(), _stream_handle(stream)))
 
     def score_update(self, stream=None):
@@ -285,7 +300,7 @@ class Context:
         a.flags = flags
         a.frac = frac
         if host_dst is not None:
-            assert host_dst.is_pinned()
+            assert self._host_ok(host_dst)
             a.host_dst = host_dst.data_ptr()
             a.host_dst_bytes = host_dst.numel() * host_dst.element_size()
         cap = None
