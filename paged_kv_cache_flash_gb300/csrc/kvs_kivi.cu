@@ -412,19 +412,107 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
         for (uint32_t gi = 0; gi < it.ng; ++gi) {
             mbar_wait(smem_u32(&bars[warp][rg.st_cons]), rg.ph_cons, a.w.err);
             const uint32_t base = ring_u32 + rg.st_cons * kTile;
-            // K (scale, zero) pairs of the lane's channels, as km[(h * 8 + i) * 2 + {scale, zero}]
-            uint32_t km[32];
+            // S^T = K . Q^T for both blocks of the group (16 tokens x 8 heads
+            // each): two independent MMA chains
+            float sj[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                // K (scale, zero) pairs of the lane's channels, km[(h * 8 + i) * 2 + {scale, zero}]
+                uint32_t km[32];
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {       // v = h * 4 + ip
-                const uint4 x = lds128(base + 2048 + (v * 4 + tq) * 16);
-                km[4 * v] = x.x;
-                km[4 * v + 1] = x.y;
-                km[4 * v + 2] = x.z;
-                km[4 * v + 3] = x.w;
+                for (int v = 0; v < 8; ++v) {   // v = h * 4 + ip
+                    const uint4 x = lds128(base + 2048 + (v * 4 + tq) * 16);
+                    km[4 * v] = x.x;
+                    km[4 * v + 1] = x.y;
+                    km[4 * v + 2] = x.z;
+                    km[4 * v + 3] = x.w;
+                }
+                uint32_t kw[2][4], kx[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint4 kw4 = lds128(base + (j * 32 + lane) * 16);
+                    kw[j][0] = kw4.x; kw[j][1] = kw4.y; kw[j][2] = kw4.z; kw[j][3] = kw4.w;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        kx[j][e] = kw[j][e] >> 10;
+                }
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int w = ks >> 2, i0 = 2 * (ks & 3);
+                    const uint32_t sa = km[(w * 8 + i0) * 2], za = km[(w * 8 + i0) * 2 + 1];
+                    const uint32_t sb = km[(w * 8 + i0 + 1) * 2], zb = km[(w * 8 + i0 + 1) * 2 + 1];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        mma_f16(sj[j], kdq(kw[j][w], kx[j][w], i0, sa, za),
+                                kdq(kw[j][2 + w], kx[j][2 + w], i0, sa, za),
+                                kdq(kw[j][w], kx[j][w], i0 + 1, sb, zb),
+                                kdq(kw[j][2 + w], kx[j][2 + w], i0 + 1, sb, zb), qf[ks][0], qf[ks][1]);
+                }
             }
 #pragma unroll
-            for (uint32_t j = 0; j < 2; ++j) {
-                const uint4 kw4 = lds128(base + (j * 32 + lane) * 16);
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    sj[j][e] *= scale_log2;
+
+            // one online-softmax update for the 32 tokens; the per-block
+            // log2-sum-exps are taken against the same running max
+            float bm0 = fmaxf(fmaxf(sj[0][0], sj[0][2]), fmaxf(sj[1][0], sj[1][2]));
+            float bm1 = fmaxf(fmaxf(sj[0][1], sj[0][3]), fmaxf(sj[1][1], sj[1][3]));
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
+            float pj[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                pj[j][0] = fast_exp2(sj[j][0] - mn0);
+                pj[j][1] = fast_exp2(sj[j][1] - mn1);
+                pj[j][2] = fast_exp2(sj[j][2] - mn0);
+                pj[j][3] = fast_exp2(sj[j][3] - mn1);
+            }
+            float w00 = pj[0][0] + pj[0][2], w01 = pj[0][1] + pj[0][3];   // block 0: heads h0, h1
+            float w10 = pj[1][0] + pj[1][2], w11 = pj[1][1] + pj[1][3];   // block 1
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                w00 += __shfl_xor_sync(0xffffffffu, w00, x);
+                w01 += __shfl_xor_sync(0xffffffffu, w01, x);
+                w10 += __shfl_xor_sync(0xffffffffu, w10, x);
+                w11 += __shfl_xor_sync(0xffffffffu, w11, x);
+            }
+            l0 = l0 * sc0 + (w00 + w10);
+            l1 = l1 * sc1 + (w01 + w11);
+            m0 = mn0;
+            m1 = mn1;
+            if (gq == 0) {
+                if (h0 < G) {
+                    lse_row0[2 * gi] = mn0 + fast_log2(w00);
+                    lse_row0[2 * gi + 1] = mn0 + fast_log2(w10);
+                }
+                if (h1 < G) {
+                    lse_row0[nb_total + 2 * gi] = mn1 + fast_log2(w01);
+                    lse_row0[nb_total + 2 * gi + 1] = mn1 + fast_log2(w11);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                o[mt][0] *= sc0;
+                o[mt][1] *= sc1;
+                o[mt][2] *= sc0;
+                o[mt][3] *= sc1;
+            }
+            uint32_t pb[2][2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                pb[j][0] = movmatrix_t(pack_f16(pj[j][0], pj[j][1]));
+                pb[j][1] = movmatrix_t(pack_f16(pj[j][2], pj[j][3]));
+            }
+            // O^T += V^T . P^T per block; m-tile m: channels 16m .. 16m+15,
+            // channel group m/2
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
                 const uint4 vw4 = lds128(base + 1024 + (j * 32 + lane) * 16);
                 // V (scale, zero) pairs: token pairs tq and tq + 4, channel groups 0..3
                 uint32_t vm[2][8];
@@ -446,71 +534,15 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                     if (rg.inflight < kKRing)
                         kissue_next(a, cur, nxt, have_nxt, c_in_nxt, c_grp, rg, ring_u32, bars[warp], lane);
                 }
-                const uint32_t kw[4] = {kw4.x, kw4.y, kw4.z, kw4.w};
                 const uint32_t vw[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
-                const uint32_t kx[4] = {kw4.x >> 10, kw4.y >> 10, kw4.z >> 10, kw4.w >> 10};
                 const uint32_t vx[4] = {vw4.x >> 10, vw4.y >> 10, vw4.z >> 10, vw4.w >> 10};
-
-                // S^T = K . Q^T (16 tokens x 8 heads)
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int w = ks >> 2, i0 = 2 * (ks & 3);
-                    const uint32_t sa = km[(w * 8 + i0) * 2], za = km[(w * 8 + i0) * 2 + 1];
-                    const uint32_t sb = km[(w * 8 + i0 + 1) * 2], zb = km[(w * 8 + i0 + 1) * 2 + 1];
-                    mma_f16(s, kdq(kw[w], kx[w], i0, sa, za), kdq(kw[2 + w], kx[2 + w], i0, sa, za),
-                            kdq(kw[w], kx[w], i0 + 1, sb, zb), kdq(kw[2 + w], kx[2 + w], i0 + 1, sb, zb),
-                            qf[ks][0], qf[ks][1]);
-                }
-                s[0] *= scale_log2;
-                s[1] *= scale_log2;
-                s[2] *= scale_log2;
-                s[3] *= scale_log2;
-
-                float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
-#pragma unroll
-                for (int x = 4; x < 32; x <<= 1) {
-                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
-                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
-                }
-                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-                const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
-                const float p0 = fast_exp2(s[0] - mn0), p1 = fast_exp2(s[1] - mn1);
-                const float p2 = fast_exp2(s[2] - mn0), p3 = fast_exp2(s[3] - mn1);
-                float w0 = p0 + p2, w1 = p1 + p3;
-#pragma unroll
-                for (int x = 4; x < 32; x <<= 1) {
-                    w0 += __shfl_xor_sync(0xffffffffu, w0, x);
-                    w1 += __shfl_xor_sync(0xffffffffu, w1, x);
-                }
-                l0 = l0 * sc0 + w0;
-                l1 = l1 * sc1 + w1;
-                m0 = mn0;
-                m1 = mn1;
-                const uint32_t bi = 2 * gi + j;
-                if (gq == 0) {
-                    if (h0 < G)
-                        lse_row0[bi] = mn0 + fast_log2(w0);
-                    if (h1 < G)
-                        lse_row0[nb_total + bi] = mn1 + fast_log2(w1);
-                }
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    o[mt][0] *= sc0;
-                    o[mt][1] *= sc1;
-                    o[mt][2] *= sc0;
-                    o[mt][3] *= sc1;
-                }
-                const uint32_t pb0 = movmatrix_t(pack_f16(p0, p1));
-                const uint32_t pb1 = movmatrix_t(pack_f16(p2, p3));
-                // O^T += V^T . P^T; m-tile m: channels 16m .. 16m+15, channel group m/2
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     const int w = mt >> 1, cg = mt >> 1, i = 4 * (mt & 1);
                     mma_f16(o[mt], kdq(vw[w], vx[w], i, vm[0][2 * cg], vm[0][2 * cg + 1]),
                             kdq(vw[w], vx[w], i + 1, vm[0][2 * cg], vm[0][2 * cg + 1]),
                             kdq(vw[w], vx[w], i + 2, vm[1][2 * cg], vm[1][2 * cg + 1]),
-                            kdq(vw[w], vx[w], i + 3, vm[1][2 * cg], vm[1][2 * cg + 1]), pb0, pb1);
+                            kdq(vw[w], vx[w], i + 3, vm[1][2 * cg], vm[1][2 * cg + 1]), pb[j][0], pb[j][1]);
                 }
             }
             if (gi == 0 && !have_nxt) {
