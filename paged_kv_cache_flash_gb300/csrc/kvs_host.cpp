@@ -421,27 +421,33 @@ int kivi_compress(kvs_ctx *ctx, const std::vector<std::pair<uint32_t, SeqState *
     }
     if (jobs.empty())
         return KVS_OK;
+    // on a failure the group pages go back; the bf16 pages stay in use
+    auto undo = [&](int rc) {
+        for (auto it = jobs.rbegin(); it != jobs.rend(); ++it)
+            ctx->free_groups.push_front(it->gpage);
+        return rc;
+    };
     int rc = order_pool_writes(ctx, s);
     if (rc)
-        return rc;
+        return undo(rc);
     const uint32_t per_slot = static_cast<uint32_t>(kRingSlotBytes / sizeof(KiviJob));
     for (size_t off = 0; off < jobs.size(); off += per_slot) {
         const uint32_t n = static_cast<uint32_t>(std::min<size_t>(per_slot, jobs.size() - off));
         RingSlot r;
         if ((rc = ring_acquire(ctx, n * sizeof(KiviJob), &r)))
-            return rc;
+            return undo(rc);
         std::memcpy(r.host, jobs.data() + off, n * sizeof(KiviJob));
         if ((rc = ring_push(ctx, r, n * sizeof(KiviJob), s)))
-            return rc;
+            return undo(rc);
         if ((rc = launch_rc(ctx,
                             launch_kivi_compress(ctx->geo, reinterpret_cast<const KiviJob *>(r.dev), n,
                                                  static_cast<const uint8_t *>(ctx->buf.pool),
                                                  static_cast<uint8_t *>(ctx->buf.group_pool),
                                                  static_cast<int32_t *>(ctx->buf.block_table), s),
                             "2-bit compress")))
-            return rc;
+            return undo(rc);
         if ((rc = ring_release(ctx, r, s)))
-            return rc;
+            return undo(rc);
     }
     for (const KiviJob &j : jobs) {
         for (int32_t p : {j.page0, j.page1})
