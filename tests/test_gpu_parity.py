@@ -148,6 +148,41 @@ def test_fp8_pages_parity(scales):
     run.close()
 
 
+def test_fp8_demote_prefetch_round_trip():
+    """FP8 pages (half size) through demotion to pinned host and back by a
+    budgeted prefetch: code pages byte-equal, records restored, decoding
+    resumes in parity."""
+    wl = W.workload("l70b_8k", L=2, prefill_lens=(400, 700), pool_pages=90, steps=4)
+    run = Run(wl, 0.05, kv_dtype=K.KVS_KV_FP8_E4M3, k_scale=0.5, v_scale=0.5)
+    for _ in range(2):
+        run.compare(run.step(None))
+    before = {sid: run.ctx.export_records(sid) for sid in run.ids}
+    pages = {(sid, b): run.ctx.page_bytes_of(p).cpu().numpy().tobytes()
+             for sid in run.ids for b, p in enumerate(run.ctx.seq_info(sid)[3])}
+    nrec = sum(len(v) for v in before.values())
+    host = _pinned(nrec * run.ctx.page_bytes)
+    ids = torch.zeros(2 * nrec, dtype=torch.int64, device="cuda")
+    rc, r = run.ctx.select_and_gather(K.KVS_SELECT_LOWFRAC, host, frac=0.3,
+                                      flags=K.KVS_GATHER_DEMOTE, ids=ids)
+    torch.cuda.synchronize()
+    assert rc == K.KVS_OK and r.n_demoted == r.n_selected == O.lowfrac_k(nrec, 0.3)
+    got = [tuple(x) for x in ids.view(-1, 2)[: r.n_demoted].cpu().tolist()]
+    pb = run.ctx.page_bytes
+    for i, key in enumerate(got):
+        assert host.numpy()[i * pb:(i + 1) * pb].tobytes() == pages[key] == run.oracle_page(*key)
+    side = torch.cuda.Stream()
+    while run.ctx.prefetch_plan(1):
+        run.ctx.prefetch(10, host, stream=side)
+    side.synchronize()
+    for sid in run.ids:
+        assert run.ctx.export_records(sid).tobytes() == before[sid].tobytes()
+        for b, p in enumerate(run.ctx.seq_info(sid)[3]):
+            assert run.ctx.page_bytes_of(p).cpu().numpy().tobytes() == pages[(sid, b)]
+    for _ in range(2):
+        run.compare(run.step(None))
+    run.close()
+
+
 def test_fp8_config_checks():
     with pytest.raises(K.KvsError):
         K.kvs_required_sizes(K.make_config(2, 8, 2, 64, 17, 1, 18, kv_dtype=K.KVS_KV_FP8_E4M3))
