@@ -87,7 +87,7 @@ def read_peaks():
 
 def decode_source_hash():
     h = hashlib.sha256()
-    for f in ("kvs_decode.cu", "kvs_ptx.h", "kvs_internal.h"):
+    for f in ("kvs_decode.cu", "kvs_kivi.cu", "kvs_ptx.h", "kvs_internal.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_flash_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
