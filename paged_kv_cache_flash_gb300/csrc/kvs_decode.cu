@@ -7,16 +7,25 @@
 // (sequence, 16-token block)).
 //
 // Structure of one step:
-//   decode_kernel  -- persistent CTAs pull work items (sequence, layer, group
-//                     of KV heads, chunk of 64 blocks).  Each warp owns one KV
-//                     head: a TMA ring streams the head's 4 KiB K and V
-//                     sub-pages of each block into shared memory (128-byte
-//                     swizzle), and warp-level tensor-core MMAs compute
+//   decode_kernel  -- persistent grid of independent warps.  Each warp claims
+//                     work items (sequence, layer, KV head, chunk of 16..128
+//                     blocks) from a global counter, prepares the next item
+//                     while computing the current one, and keeps its own TMA
+//                     ring of the head's K and V sub-pages streaming across
+//                     item boundaries (128-byte swizzle, bounded mbarrier
+//                     waits).  Warp-level tensor-core MMAs compute
 //                       S^T[16 tokens][8 heads] = K . Q^T
 //                       O^T[d][8 heads]        += V^T . P^T
 //                     with an online softmax in registers.  Per block it writes
-//                     the block's log2-sum-exp for each query head; per chunk
+//                     the block's log2-sum-exp for each query head; per item
 //                     the running max, sum and unnormalised output.
+//                     bf16 pages: bf16 MMAs, 6-stage rings, 4 warps per SM.
+//                     FP8 E4M3 pages ("Fitting a Million Tokens", s.02): S by
+//                     e4m3 MMAs over the stored codes with Q as two exact
+//                     E4M3 terms, O by f16 MMAs over codes converted in
+//                     registers; 4-stage rings, 12 warps per SM.
+//                     (2-bit KIVI group pages are decoded by kvs_kivi.cu; the
+//                     page items of such a sequence cover its residual blocks.)
 //   combine_kernel -- merges a stream's chunks: per head log2-sum-exp LSE_h and
 //                     the normalised output.
 //   mass_kernel    -- M(b) = 1/(L*Hq) * sum_{l,h} 2^(lse_blk(l,h,b) - LSE_h),
