@@ -225,6 +225,7 @@ class Pipeline:
         self.prefetched_pages = 0
         self.holes = {}                     # prefetch: seq_id -> blocks still demoted
         self.budget = prefetch_budget
+        self.last_round = 0                 # pages demoted by the last step (0: none)
         self.victim_mode = K.KVS_SELECT_LRFU if victims == "lrfu" else K.KVS_SELECT_LOWFRAC
         self.pf_stream = torch.cuda.Stream(device) if gather == "prefetch" else None
         self.pf_done = None
@@ -356,6 +357,7 @@ class Pipeline:
                                           side_stream=self.side)
             keys = [tuple(x) for x in self.ids_dev.view(-1, 2)[: r.n_demoted].cpu().tolist()]
             self.demoted_pages += r.n_demoted
+            self.last_round = r.n_demoted
             if self.gather == "demote":
                 ctx.readmit(keys, self.host)        # overlaps the demotion's copies
                 main.wait_stream(self.side)
@@ -440,9 +442,13 @@ def run_kvs(args):
     demoted0 = pipe.demoted_pages
     wall0 = time.perf_counter()
     t_start.record()
+    rounds = []                     # (timed step, pages) of demote + readmit round trips
     for i in range(K_):
         pipe.ctx.set_decode_events(dec[i][0], dec[i][1])
+        pipe.last_round = 0
         r = pipe.step(kv[W_ + i], qs[W_ + i], ev[i])
+        if pipe.last_round and args.gather == "demote":
+            rounds.append((i, pipe.last_round))
         kv_bytes += pipe.kv_bytes_this_step()
         decoded += len(pipe.active)
         uniq_bytes += pipe.kv_bytes_this_step() - shared_extra
@@ -465,6 +471,15 @@ def run_kvs(args):
     tok_s = decoded * ws / (ms_max / 1e3)
 
     dec_ms = [dec[i][0].elapsed_time(dec[i][1]) for i in range(K_)]
+    round_info = None
+    if rounds:
+        # selection + demotion (D2H) + re-admission (H2D) region of those steps
+        r_ms = [ev[i][3].elapsed_time(ev[i][4]) for i, _ in rounds]
+        r_bytes = [2 * n * pipe.ctx.page_bytes for _, n in rounds]
+        round_info = {"rounds": len(rounds), "pages_per_round": int(statistics.median(n for _, n in rounds)),
+                      "ms_per_round": round(statistics.median(r_ms), 3),
+                      "link_GBps": round(sum(r_bytes) / (sum(r_ms) / 1e3) / 1e9, 2),
+                      "note": "2 x page bytes per demoted page (to host and back) over the region"}
     part = {name: statistics.median(ev[i][a].elapsed_time(ev[i][b]) for i in range(K_))
             for name, a, b in [("append", 0, 1), ("decode_step", 1, 2), ("score", 2, 3),
                                ("select_gather", 3, 4)]}
@@ -565,6 +580,7 @@ def run_kvs(args):
                 "logical_exceeds_measured_peak": bool(value > peak),
                 "note": "logical bytes count a shared prefix once per sequence; unique bytes once"},
             "kv_gbps_pct_of_hbm": round(100 * value / peak, 2),
+            "kv_gbps_pct_of_8tbs": round(100 * value / 8000.0, 2),
             "roofline": {"bound": "hbm", "kernel": "decode_kernel (split-K paged GQA)",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -577,6 +593,7 @@ def run_kvs(args):
                                           max(part["decode_step"], 1e-9), 2),
             "gathered_pages_timed": staged,
             "demoted_and_readmitted_pages_timed": demoted,
+            "demote_readmit_rounds": round_info,
             "prefetched_pages_timed": prefetched if args.gather == "prefetch" else None,
             "e2e": e2e,
             "literal_gather": literal,
