@@ -237,6 +237,16 @@ def test_kivi_parity():
             assert res["gather"].n_pages == 0
     n = _check_kivi_groups(run)
     assert n == (192 + 896 + 0 + 384) // 32
+    # LOWFRAC and LRFU victims as id lists (ids only in 2-bit contexts): the
+    # oracle's selection over the device's records (compared above)
+    recs = {s: run.ctx.export_records(s) for s in run.ids}
+    nrec = sum(len(v) for v in recs.values())
+    ids = torch.zeros(2 * nrec, dtype=torch.int64, device="cuda")
+    for mode, ref in ((K.KVS_SELECT_LOWFRAC, O.select_lowfrac(recs, 0.2)),
+                      (K.KVS_SELECT_LRFU, O.select_lrfu(recs, 0.2, 0.15))):
+        rc, r = run.ctx.select_and_gather(mode, frac=0.2, ids=ids)
+        assert rc == K.KVS_OK and r.n_pages == 0
+        assert [tuple(x) for x in ids.view(-1, 2)[: r.n_selected].cpu().tolist()] == ref
     run.ctx.check_device()
     print("kivi", summ, n, "groups")
     run.close()
