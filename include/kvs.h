@@ -246,22 +246,26 @@ const char *kvs_last_error(const kvs_ctx_t *ctx);
  * count 0, last_touch = current step), written on `stream`.  Appending
  * never writes a shared page.  KVS_EEXIST if seq_id is
  * present, KVS_ENOTFOUND if the parent is not, KVS_ENOMEM if no slot is
- * free, KVS_EINVAL if the parent has fewer full blocks. */
+ * free, KVS_EINVAL if the parent has fewer full blocks or, in a 2-bit
+ * (KVS_KV_KIVI2) context, if any block is to be shared. */
 int kvs_seq_add(kvs_ctx_t *ctx, uint64_t seq_id, int64_t parent_seq_id,
                 uint32_t shared_prefix_blocks, void *stream);
 
 /* Removes a sequence: its pages lose one reference each and return to the
- * free list at zero; its demoted keys are dropped.  Stream-ordered after
- * `stream` (page reuse waits for work enqueued before). */
+ * free list at zero; its 2-bit group pages return to the group free list;
+ * its demoted keys are dropped.  Stream-ordered after `stream` (page reuse
+ * waits for work enqueued before). */
 int kvs_seq_remove(kvs_ctx_t *ctx, uint64_t seq_id, void *stream);
 
 /* Appends n tokens to a sequence [ARCH]: K and V are device, token-major
  * [n][L][Hkv][d] bf16.  A page is taken from the free list whenever a token
  * opens a new block; the page's later slots are zero-filled and the block's
  * record is created with score 0, count 0, last_touch = the current step
- * counter (decode steps completed so far), tier 255.  KVS_ENOMEM if the free
- * list runs out (nothing appended), KVS_EINVAL for n == 0 or a table row
- * overflow. */
+ * counter (decode steps completed so far), tier 255.  In a 2-bit context the
+ * groups that fall behind the residual window are then quantised into group
+ * pages on `stream` and their bf16 pages freed (KVS_KV_KIVI2 above).
+ * KVS_ENOMEM if the free list (or the group pool) runs out (nothing
+ * appended), KVS_EINVAL for n == 0 or a table row overflow. */
 int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n,
                       const void *k_dev, const void *v_dev, void *stream);
 int kvs_append_token(kvs_ctx_t *ctx, uint64_t seq_id, const void *k_dev,
@@ -271,9 +275,11 @@ int kvs_append_token(kvs_ctx_t *ctx, uint64_t seq_id, const void *k_dev,
  * of a decode step) [ARCH]: k, v device [nseq][L][Hkv][d] bf16, row i for
  * seq_ids[i].  Same effect as kvs_append_token for each sequence in turn:
  * a token that opens a block takes a page from the free list (tail slots
- * zeroed, record created with the current step counter).  KVS_ENOMEM if the
- * free list cannot cover every new block (nothing appended); KVS_EINVAL for
- * duplicates, a full table row, or a last block that is shared or demoted. */
+ * zeroed, record created with the current step counter), and in a 2-bit
+ * context the groups that become due are quantised in one launch.
+ * KVS_ENOMEM if the free list (or the group pool) cannot cover every new
+ * block (nothing appended); KVS_EINVAL for duplicates, a full table row, or
+ * a last block that is shared or demoted. */
 int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
                     const void *k_dev, const void *v_dev, void *stream);
 
@@ -285,7 +291,9 @@ int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
  *   M(b) = 1/(L*Hq) * sum_{l,h} sum_{t in b} softmax weight,
  * written to mass[slot][b].  q [nseq][L][Hq][d] bf16 and out [nseq][L][Hq][d]
  * float32 are device, in the order of seq_ids.  The set of sequences becomes
- * the one kvs_score_update and kvs_select_and_gather work on.
+ * the one kvs_score_update and kvs_select_and_gather work on.  In a 2-bit
+ * context the blocks in group pages are read through one kernel and the
+ * residual pages through the page kernel; both feed the same merge.
  * KVS_EINVAL: nseq == 0 or > KVS_MAX_CALL_SEQS, duplicates, an empty
  * sequence or one with a demoted block; KVS_ENOTFOUND: unknown id. */
 int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
@@ -396,15 +404,16 @@ int kvs_export_records(kvs_ctx_t *ctx, uint64_t seq_id, void *host_dst,
 
 /* Host view of a sequence: its slot (row of the table, records and mass
  * buffers), token count, block count, and (if table_out is not NULL) up to
- * table_cap page ids (-1 = demoted).  Any output pointer may be NULL. */
+ * table_cap page ids (-1 = demoted, KVS_TABLE_GROUP(g) = held in 2-bit group
+ * page g).  Any output pointer may be NULL. */
 int kvs_seq_info(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t *slot,
                  uint32_t *n_tokens, uint32_t *n_blocks, int32_t *table_out,
                  uint32_t table_cap);
 
 /* Measurement hook: when ev_start/ev_stop (cudaEvent_t as void*) are not
  * NULL, every later kvs_decode_step records ev_start on its stream right
- * before the split-K decode kernel and ev_stop right after it, so the kernel
- * can be timed on the stream it runs on.  NULL, NULL turns it off.  The
+ * before the split-K decode kernel(s) and ev_stop right after, so they can
+ * be timed on the stream they run on (2-bit contexts: both launches).  NULL, NULL turns it off.  The
  * events stay owned by the caller. */
 int kvs_set_decode_events(kvs_ctx_t *ctx, void *ev_start, void *ev_stop);
 
