@@ -229,7 +229,8 @@ class Pipeline:
         self.victim_mode = K.KVS_SELECT_LRFU if victims == "lrfu" else K.KVS_SELECT_LOWFRAC
         self.pf_stream = torch.cuda.Stream(device) if gather == "prefetch" else None
         self.pf_done = None
-        self.active = list(range(wl.nseq))  # sequences decoded by the last step
+        self.all_idx = list(range(wl.nseq))
+        self.active = self.all_idx          # sequences decoded by the last step
         self._idx = {}
         if gather in ("mirror", "list"):
             self.host = torch.empty(self.pool_pages * self.ctx.page_bytes, dtype=torch.uint8,
@@ -306,6 +307,7 @@ class Pipeline:
     def step(self, kv_row, q, ev=None, mode_flags=None):
         K, ctx, torch = self.K, self.ctx, self.torch
         main = torch.cuda.current_stream()
+        sh, side = main.cuda_stream, self.side.cuda_stream    # raw handles: no lookups per call
         if ev:
             ev[0].record(main)
         paused = set()
@@ -325,30 +327,34 @@ class Pipeline:
                     self.holes[sid] -= 1
                 self.holes = {k: v for k, v in self.holes.items() if v > 0}
                 self.prefetched_pages += len(plan)
-        active = [i for i, sid in enumerate(self.ids) if sid not in paused]
+        if paused:
+            active = [i for i, sid in enumerate(self.ids) if sid not in paused]
+            ids = [self.ids[i] for i in active]
+            out = self.out[:len(active)]
+        else:
+            active, ids, out = self.all_idx, self.ids, self.out
         self.active = active
-        ids = [self.ids[i] for i in active]
-        ctx.append_step(ids, self._rows(kv_row[0], active), self._rows(kv_row[1], active))
+        ctx.append_step(ids, self._rows(kv_row[0], active), self._rows(kv_row[1], active), stream=sh)
         for i in active:
             self.ntok[i] += 1
         if ev:
             ev[1].record(main)
-        ctx.decode_step(ids, self._rows(q, active), self.out[:len(active)])
+        ctx.decode_step(ids, self._rows(q, active), out, stream=sh)
         if ev:
             ev[2].record(main)
-        ctx.score_update()
+        ctx.score_update(stream=sh)
         if ev:
             ev[3].record(main)
         r = None
         self.steps_done += 1
         if self.gather == "ids":            # the THRESH list only, no page copies
-            rc, r = ctx.select_and_gather(K.KVS_SELECT_THRESH, None)
+            rc, r = ctx.select_and_gather(K.KVS_SELECT_THRESH, None, stream=sh)
         elif self.gather in ("mirror", "list"):
             flags = K.KVS_GATHER_MIRROR if self.gather == "mirror" else 0
             if mode_flags is not None:
                 flags = mode_flags
-            rc, r = ctx.select_and_gather(K.KVS_SELECT_THRESH, self.host, flags=flags,
-                                          side_stream=self.side)
+            rc, r = ctx.select_and_gather(K.KVS_SELECT_THRESH, self.host, flags=flags, stream=sh,
+                                          side_stream=side)
             main.wait_stream(self.side)
         elif self.demote_every and self.steps_done % self.demote_every == 0 and not self.holes:
             # the lowest-P fraction goes to pinned host and comes back with its record
