@@ -236,7 +236,9 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out);
  * work the context enqueued. */
 void kvs_destroy(kvs_ctx_t *ctx);
 
-/* Text of the last failure on this context (owned by the context). */
+/* Text of the last failure on this context (owned by the context).  With
+ * ctx NULL: the last failure of a call made without a context
+ * (kvs_required_sizes, a failed kvs_create) on the calling thread. */
 const char *kvs_last_error(const kvs_ctx_t *ctx);
 
 /* Adds a sequence with no tokens.  With parent_seq_id >= 0, the first
@@ -445,6 +447,21 @@ int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads,
                        const int32_t *block_table, uint32_t n_tokens,
                        const void *q, float *out, float *mass, void *stream,
                        char *msg, size_t msg_bytes);
+
+/* Test hook, process-wide (the pages have no counterpart): injects host-side
+ * failures so that error paths can be exercised without a GPU fault.
+ *   KVS_FAULT_HOSTALLOC: the pinned host allocation of the next kvs_create
+ *                        fails (KVS_ENOMEM; one shot; nothing leaks);
+ *   KVS_FAULT_WAIT:      every host wait of the library (read-backs, upload
+ *                        ring, kvs_check_device) sees its event as not yet
+ *                        complete, so it ends with KVS_ETIMEOUT after
+ *                        wait_limit_ms (the device work stays enqueued).
+ * wait_limit_ms also sets the limit of real waits (0 = 600,000 ms, the
+ * default).  kvs_debug_inject(0, 0) clears everything.  KVS_EINVAL for
+ * unknown bits. */
+#define KVS_FAULT_HOSTALLOC 1u
+#define KVS_FAULT_WAIT 2u
+int kvs_debug_inject(uint32_t faults, uint32_t wait_limit_ms);
 
 /* Kernels this context has launched so far (every kernel of the library,
  * counted at launch). */

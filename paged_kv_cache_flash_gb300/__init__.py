@@ -116,6 +116,7 @@ _SIGS = {
                                           c_vp, c_vp, c_vp, c_vp, ctypes.c_char_p, c_sz]),
     "kvs_step_count": (c_u64, [c_vp]),
     "kvs_kernel_launches": (c_u64, [c_vp]),
+    "kvs_debug_inject": (ctypes.c_int, [c_u32, c_u32]),
     "kvs_free_pages": (c_u32, [c_vp]),
     "kvs_check_device": (ctypes.c_int, [c_vp, c_vp]),
 }
@@ -152,7 +153,7 @@ class KvsError(RuntimeError):
 
 def _check(ctx, rc):
     if rc != KVS_OK:
-        msg = lib().kvs_last_error(ctx).decode(errors="replace") if ctx else ""
+        msg = lib().kvs_last_error(ctx).decode(errors="replace")
         raise KvsError(rc, msg)
     return rc
 
@@ -171,6 +172,14 @@ def make_config(L, Hq, Hkv, d, pool_blocks, max_seqs, max_blocks_per_seq, *, alp
                       kv_dtype=kv_dtype, w_recency=weights[0], w_ema=weights[1],
                       w_anchor=weights[2], cut_lo=cuts[0], cut_hi=cuts[1], pool_seed=pool_seed,
                       k_scale=k_scale, v_scale=v_scale, kivi_groups=kivi_groups)
+
+
+KVS_FAULT_HOSTALLOC, KVS_FAULT_WAIT = 1, 2
+
+
+def debug_inject(faults: int = 0, wait_limit_ms: int = 0) -> None:
+    """Test hook (process-wide): injected host-side failures; (0, 0) clears."""
+    _check(None, lib().kvs_debug_inject(faults, wait_limit_ms))
 
 
 def kvs_required_sizes(cfg: kvs_config) -> kvs_sizes:

@@ -9,7 +9,12 @@
 // scoring streams" (identity key and score persist across eviction and are
 // restored on re-admission); "RETRACTIONS" s.2 (blocks are write-once).
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
+#include <thread>
+
+#include <nvtx3/nvToolsExt.h>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -26,6 +31,13 @@
 #include "kvs_internal.h"
 
 using namespace kvs;
+
+// NVTX range around a public call (visible in Nsight Systems / Compute).
+struct KvsRange {
+    explicit KvsRange(const char *name) { nvtxRangePushA(name); }
+    ~KvsRange() { nvtxRangePop(); }
+};
+#define KVS_RANGE() const KvsRange kvs_range_(__func__)
 
 namespace {
 
@@ -101,10 +113,37 @@ struct kvs_ctx {
     uint64_t kernel_launches = 0;                   // kernels launched by this context
     std::deque<uint32_t> free_groups;               // KIVI: free group pages
     int kivi_grid = 0;                              // KIVI: persistent decode grid
+    cudaEvent_t ev_wait{};                          // bounded host waits
     std::string err;
+
+    // Releases what the context holds, also after a failed kvs_create.
+    ~kvs_ctx()
+    {
+        for (auto &e : ring_ev)
+            if (e)
+                cudaEventDestroy(e);
+        for (auto e : {ev_ready[0], ev_ready[1], ev_side_done, ev_pool_release, ev_quarantine, ev_wait})
+            if (e)
+                cudaEventDestroy(e);
+        for (auto e : chunk_ev)
+            cudaEventDestroy(e);
+        if (ring_host)
+            cudaFreeHost(ring_host);
+        if (pinned_small)
+            cudaFreeHost(pinned_small);
+    }
 };
 
 namespace {
+
+// Process-wide test hooks (kvs_debug_inject): a failing pinned allocation in
+// the next kvs_create, and host waits that never see their event complete.
+std::atomic<uint32_t> g_faults{0};
+std::atomic<uint32_t> g_wait_limit_ms{600000};
+
+// Text of the last failure of a call without a context (kvs_required_sizes,
+// kvs_create) on this thread; kvs_last_error(NULL) returns it.
+thread_local std::string t_err;
 
 int fail(kvs_ctx *c, int code, const char *fmt, ...)
 {
@@ -115,6 +154,8 @@ int fail(kvs_ctx *c, int code, const char *fmt, ...)
     va_end(ap);
     if (c)
         c->err = buf;
+    else
+        t_err = buf;
     return code;
 }
 
@@ -124,6 +165,38 @@ int fail(kvs_ctx *c, int code, const char *fmt, ...)
         if (e_ != cudaSuccess)                                                           \
             return fail(ctx, KVS_ECUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(e_), \
                         __FILE__, __LINE__);                                             \
+    } while (0)
+
+// Waits on the host until `ev` has completed, polling with a limit:
+// KVS_ETIMEOUT when the limit passes first (the device work stays enqueued),
+// KVS_ECUDA for an error reported by the event.
+int event_wait(kvs_ctx *ctx, cudaEvent_t ev, const char *what)
+{
+    const auto t0 = std::chrono::steady_clock::now();
+    const auto limit = std::chrono::milliseconds(g_wait_limit_ms.load());
+    for (uint32_t spin = 0;; ++spin) {
+        cudaError_t e = (g_faults.load() & KVS_FAULT_WAIT) ? cudaErrorNotReady : cudaEventQuery(ev);
+        if (e == cudaSuccess)
+            return KVS_OK;
+        if (e != cudaErrorNotReady)
+            return fail(ctx, KVS_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+        if (std::chrono::steady_clock::now() - t0 > limit)
+            return fail(ctx, KVS_ETIMEOUT, "%s: no completion within %u ms", what, g_wait_limit_ms.load());
+        if (spin > 256)
+            std::this_thread::yield();
+    }
+}
+
+// Waits for the work enqueued on `s` so far (event_wait on a fresh record).
+int stream_wait(kvs_ctx *ctx, cudaStream_t s, const char *what)
+{
+    CU(cudaEventRecord(ctx->ev_wait, s));
+    return event_wait(ctx, ctx->ev_wait, what);
+}
+#define WAIT(s)                                                  \
+    do {                                                         \
+        if (int rc_ = stream_wait(ctx, (s), __func__))           \
+            return rc_;                                          \
     } while (0)
 
 cudaStream_t S(void *s) { return static_cast<cudaStream_t>(s); }
@@ -151,7 +224,8 @@ int ring_acquire(kvs_ctx *ctx, size_t bytes, RingSlot *out)
     }
     ctx->ring_next = (i + 1) % kRingSlots;
     if (ctx->ring_used[i])
-        CU(cudaEventSynchronize(ctx->ring_ev[i]));
+        if (int rc = event_wait(ctx, ctx->ring_ev[i], "upload ring slot"))
+            return rc;
     out->idx = i;
     out->host = ctx->ring_host + i * kRingSlotBytes;
     out->dev = ctx->work.ring + i * kRingSlotBytes;
@@ -600,6 +674,7 @@ extern "C" {
 
 int kvs_required_sizes(const kvs_config *cfg, kvs_sizes *out)
 {
+    KVS_RANGE();
     kvs_ctx *ctx = nullptr;
     int rc = check_cfg(cfg, ctx);
     if (rc)
@@ -625,11 +700,20 @@ int kvs_required_sizes(const kvs_config *cfg, kvs_sizes *out)
 
 int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
 {
+    KVS_RANGE();
     if (!out)
         return KVS_EINVAL;
     *out = nullptr;
     std::unique_ptr<kvs_ctx> holder(new kvs_ctx());
     kvs_ctx *ctx = holder.get();
+    struct KeepErr {            // a failed create leaves its text for kvs_last_error(NULL)
+        std::unique_ptr<kvs_ctx> &h;
+        ~KeepErr()
+        {
+            if (h)
+                t_err = h->err;
+        }
+    } keep{holder};
     int rc = check_cfg(cfg, ctx);
     if (rc)
         return rc;
@@ -713,8 +797,11 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
     CU(cudaMemset(ctx->work.page_first, 0xff, static_cast<size_t>(cfg->pool_blocks) * 4));
     CU(cudaMemset(ctx->work.page_clean, 0, cfg->pool_blocks));
     CU(cudaMemset(ctx->work.dev_refcnt, 0, static_cast<size_t>(cfg->pool_blocks) * 4));
+    if (g_faults.fetch_and(~KVS_FAULT_HOSTALLOC) & KVS_FAULT_HOSTALLOC)
+        return fail(ctx, KVS_ENOMEM, "pinned host allocation failed (injected)");
     CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->ring_host), kRingSlots * kRingSlotBytes,
                      cudaHostAllocDefault));
+    CU(cudaEventCreateWithFlags(&ctx->ev_wait, cudaEventDisableTiming));
     CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->pinned_small), kReadbackBytes, cudaHostAllocDefault));
     for (auto &e : ctx->ring_ev)
         CU(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
@@ -745,35 +832,18 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
 
 void kvs_destroy(kvs_ctx_t *ctx)
 {
+    KVS_RANGE();
     if (!ctx)
         return;
     cudaDeviceSynchronize();
-    for (auto &e : ctx->ring_ev)
-        if (e)
-            cudaEventDestroy(e);
-    for (int i = 0; i < 2; ++i) {
-        if (ctx->ev_ready[i])
-            cudaEventDestroy(ctx->ev_ready[i]);
-    }
-    if (ctx->ev_side_done)
-        cudaEventDestroy(ctx->ev_side_done);
-    if (ctx->ev_pool_release)
-        cudaEventDestroy(ctx->ev_pool_release);
-    if (ctx->ev_quarantine)
-        cudaEventDestroy(ctx->ev_quarantine);
-    for (auto e : ctx->chunk_ev)
-        cudaEventDestroy(e);
-    if (ctx->ring_host)
-        cudaFreeHost(ctx->ring_host);
-    if (ctx->pinned_small)
-        cudaFreeHost(ctx->pinned_small);
     delete ctx;
 }
 
-const char *kvs_last_error(const kvs_ctx_t *ctx) { return ctx ? ctx->err.c_str() : "null context"; }
+const char *kvs_last_error(const kvs_ctx_t *ctx) { return ctx ? ctx->err.c_str() : t_err.c_str(); }
 
 int kvs_seq_add(kvs_ctx_t *ctx, uint64_t seq_id, int64_t parent, uint32_t shared_blocks, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if (ctx->slot_of.count(seq_id))
@@ -832,6 +902,7 @@ int kvs_seq_add(kvs_ctx_t *ctx, uint64_t seq_id, int64_t parent, uint32_t shared
 
 int kvs_seq_remove(kvs_ctx_t *ctx, uint64_t seq_id, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     uint32_t slot;
@@ -868,6 +939,7 @@ int kvs_seq_remove(kvs_ctx_t *ctx, uint64_t seq_id, void *stream)
 int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n, const void *k_dev,
                       const void *v_dev, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     uint32_t slot;
@@ -963,12 +1035,14 @@ int kvs_append_tokens(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t n, const void *k
 int kvs_append_token(kvs_ctx_t *ctx, uint64_t seq_id, const void *k_dev, const void *v_dev,
                      void *stream)
 {
+    KVS_RANGE();
     return kvs_append_tokens(ctx, seq_id, 1, k_dev, v_dev, stream);
 }
 
 int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const void *k_dev,
                     const void *v_dev, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if (!seq_ids || nseq == 0 || nseq > kMaxCallSeqs || !k_dev || !v_dev)
@@ -1088,6 +1162,7 @@ int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
 int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const void *q_dev,
                     float *out_dev, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if (!q_dev || !out_dev)
@@ -1139,6 +1214,7 @@ int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
 
 int kvs_score_update(kvs_ctx_t *ctx, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if (!ctx->have_set)
@@ -1154,6 +1230,7 @@ int kvs_score_update(kvs_ctx_t *ctx, void *stream)
 
 int kvs_set_alpha(kvs_ctx_t *ctx, double alpha)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if (!(alpha >= 0.0 && alpha <= 1.0))
@@ -1164,6 +1241,7 @@ int kvs_set_alpha(kvs_ctx_t *ctx, double alpha)
 
 int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gather_result *res)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if (!args || !res)
@@ -1228,7 +1306,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         if (ctx->geo.kivi) {
             // the id list only: quantised blocks have no page to plan
             CU(cudaMemcpyAsync(ctx->pinned_small, w.sel_count, 4, cudaMemcpyDeviceToHost, s));
-            CU(cudaStreamSynchronize(s));
+            WAIT(s);
             nsel = ctx->pinned_small[0];
             res->n_selected = nsel;
             if (nsel && args->ids_dev)
@@ -1240,7 +1318,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             return rc;
         // one readback: counts and the head of the copy list
         CU(cudaMemcpyAsync(ctx->pinned_small, w.readback, kReadbackBytes, cudaMemcpyDeviceToHost, s));
-        CU(cudaStreamSynchronize(s));
+        WAIT(s);
         nsel = ctx->pinned_small[0];
         npages = ctx->pinned_small[1];
         ncopy = ctx->pinned_small[2];
@@ -1250,7 +1328,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             copy_list.resize(ncopy);
             CU(cudaMemcpyAsync(copy_list.data() + head, w.readback + 4 + head, (ncopy - head) * 4,
                                cudaMemcpyDeviceToHost, s));
-            CU(cudaStreamSynchronize(s));
+            WAIT(s);
         }
     }
     res->n_selected = nsel;
@@ -1305,7 +1383,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             CU(cudaMemcpyAsync(dpages.data(), w.sel_pages, nsel * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
             CU(cudaMemcpyAsync(drecs.data(), w.sel_recs, nsel * sizeof(kvs_record), cudaMemcpyDeviceToHost, s));
         }
-        CU(cudaStreamSynchronize(s));
+        WAIT(s);
         if (trunc)
             for (auto &x : slots)
                 if (x >= static_cast<int32_t>(nstage))
@@ -1609,7 +1687,7 @@ int prefetch_plan(kvs_ctx_t *ctx, uint32_t budget, std::vector<std::pair<uint64_
     pkeys.resize(k);
     CU(cudaMemcpyAsync(pkeys.data(), dout_key, k * sizeof(uint64_t), cudaMemcpyDeviceToHost, s));
     CU(cudaMemcpyAsync(idx.data(), dout_idx, k * sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
-    CU(cudaStreamSynchronize(s));
+    WAIT(s);
     plan.resize(k);
     for (uint32_t i = 0; i < k; ++i) {
         if (idx[i] >= n)
@@ -1644,6 +1722,7 @@ extern "C" {
 int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n, const void *host_src,
                 size_t host_src_bytes, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if (n == 0)
@@ -1659,6 +1738,7 @@ int kvs_readmit(kvs_ctx_t *ctx, const kvs_key *keys, uint32_t n, const void *hos
 int kvs_prefetch_plan(kvs_ctx_t *ctx, uint32_t budget, kvs_key *keys_out, double *blend_out,
                       uint8_t *class_out, uint32_t *n_out, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if (!keys_out || !n_out)
@@ -1677,6 +1757,7 @@ int kvs_prefetch_plan(kvs_ctx_t *ctx, uint32_t budget, kvs_key *keys_out, double
 int kvs_prefetch(kvs_ctx_t *ctx, uint32_t budget, const void *host_src, size_t host_src_bytes,
                  kvs_key *keys_out, double *blend_out, uint8_t *class_out, uint32_t *n_out, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if (!keys_out || !n_out || !host_src)
@@ -1698,6 +1779,7 @@ int kvs_prefetch(kvs_ctx_t *ctx, uint32_t budget, const void *host_src, size_t h
 int kvs_debug_set_mass(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const float *mass_dev,
                        void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if (!mass_dev)
@@ -1721,6 +1803,7 @@ int kvs_debug_set_mass(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, c
 
 int kvs_debug_advance(kvs_ctx_t *ctx, uint64_t steps)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     ctx->t += steps;
@@ -1729,6 +1812,7 @@ int kvs_debug_advance(kvs_ctx_t *ctx, uint64_t steps)
 
 int kvs_export_records(kvs_ctx_t *ctx, uint64_t seq_id, void *host_dst, size_t host_bytes, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     uint32_t slot;
@@ -1741,7 +1825,7 @@ int kvs_export_records(kvs_ctx_t *ctx, uint64_t seq_id, void *host_dst, size_t h
     if (n) {
         CU(cudaMemcpyAsync(host_dst, static_cast<kvs_record *>(ctx->buf.records) + static_cast<size_t>(slot) * ctx->cfg.max_blocks_per_seq,
                            n, cudaMemcpyDeviceToHost, S(stream)));
-        CU(cudaStreamSynchronize(S(stream)));
+        WAIT(S(stream));
     }
     if (n < want)
         return fail(ctx, KVS_ETRUNC, "host buffer holds %zu of %zu records", n / 64, nb);
@@ -1751,6 +1835,7 @@ int kvs_export_records(kvs_ctx_t *ctx, uint64_t seq_id, void *host_dst, size_t h
 int kvs_seq_info(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t *slot, uint32_t *n_tokens,
                  uint32_t *n_blocks, int32_t *table_out, uint32_t table_cap)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     uint32_t sl;
@@ -1771,6 +1856,7 @@ int kvs_seq_info(kvs_ctx_t *ctx, uint64_t seq_id, uint32_t *slot, uint32_t *n_to
 
 int kvs_set_decode_events(kvs_ctx_t *ctx, void *ev_start, void *ev_stop)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     if ((ev_start == nullptr) != (ev_stop == nullptr))
@@ -1780,8 +1866,19 @@ int kvs_set_decode_events(kvs_ctx_t *ctx, void *ev_start, void *ev_stop)
     return KVS_OK;
 }
 
+int kvs_debug_inject(uint32_t faults, uint32_t wait_limit_ms)
+{
+    KVS_RANGE();
+    if (faults & ~(KVS_FAULT_HOSTALLOC | KVS_FAULT_WAIT))
+        return KVS_EINVAL;
+    g_faults.store(faults);
+    g_wait_limit_ms.store(wait_limit_ms ? wait_limit_ms : 600000u);
+    return KVS_OK;
+}
+
 uint64_t kvs_kernel_launches(const kvs_ctx_t *ctx)
 {
+    KVS_RANGE();
     return ctx ? ctx->kernel_launches : 0;
 }
 
@@ -1789,21 +1886,23 @@ uint64_t kvs_step_count(const kvs_ctx_t *ctx) { return ctx ? ctx->t : 0; }
 
 uint32_t kvs_free_pages(const kvs_ctx_t *ctx)
 {
+    KVS_RANGE();
     return ctx ? static_cast<uint32_t>(pages_available(ctx)) : 0;
 }
 
 int kvs_check_device(kvs_ctx_t *ctx, void *stream)
 {
+    KVS_RANGE();
     if (!ctx)
         return KVS_EINVAL;
     cudaStream_t s = S(stream);
     CU(cudaMemcpyAsync(ctx->pinned_small, ctx->work.err, 8, cudaMemcpyDeviceToHost, s));
-    CU(cudaStreamSynchronize(s));
+    WAIT(s);
     const uint32_t e = ctx->pinned_small[0], info = ctx->pinned_small[1];
     if (!e)
         return KVS_OK;
     CU(cudaMemsetAsync(ctx->work.err, 0, 8, s));
-    CU(cudaStreamSynchronize(s));
+    WAIT(s);
     if (e & kErrTmaTimeout)
         return fail(ctx, KVS_ETIMEOUT, "a decode kernel gave up waiting for a TMA copy (error word 0x%x)", e);
     return fail(ctx, KVS_EDEVICE, "device error word 0x%x (bad page %d, bad record %d), info 0x%x", e,
