@@ -5,13 +5,15 @@
 // Offloading for LLM Inference -- Visual Reference" s.4 (the decode output
 // over every cached token).
 //
-//   combine_kernel -- per (sequence, layer, KV head) and range of blocks: each
-//                     head's log2-sum-exp LSE_h from the chunk partials; the
-//                     first range's CTA also merges the output; every CTA
-//                     turns the per-block log2-sum-exps of its range into the
-//                     stream's block masses  sum_h 2^(lse_blk(h, b) - LSE_h).
+//   combine_kernel -- per (sequence, layer, KV head): each CTA recomputes the
+//                     heads' log2-sum-exp LSE_h from the chunk partials; CTA
+//                     y = 0 merges the output, CTAs y >= 1 turn the per-block
+//                     log2-sum-exps of block range y - 1 into the stream's
+//                     block masses  sum_h 2^(lse_blk(h, b) - LSE_h).
 //   mass_kernel    -- M(b) = 1/(L*Hq) * sum over the L*Hkv streams, in a fixed
 //                     order (deterministic).
+#include <type_traits>
+
 #include "kvs_internal.h"
 #include "kvs_ptx.h"
 
@@ -36,8 +38,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w,
         w.counter[1] = 0;
     }
     const DSeq sq = ds->seq[ci];
-    const uint32_t r0 = blockIdx.y * kMassRange;
-    if (r0 >= sq.nb)
+    // y == 0: the output merge; y >= 1: the block masses of range y - 1
+    const bool merge = blockIdx.y == 0;
+    const uint32_t r0 = merge ? 0u : (blockIdx.y - 1) * kMassRange;
+    if (!merge && r0 >= sq.nb)
         return;                    // uniform over the CTA
     const uint32_t pb = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk;
     if (h < g.G) {
@@ -55,7 +59,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w,
 #pragma unroll
         for (int x = 16; x > 0; x >>= 1)
             lsum += __shfl_xor_sync(0xffffffffu, lsum, x);
-        if (blockIdx.y == 0) {
+        if (merge) {
+            // D / 32 consecutive floats per lane: one 16-byte (D = 128) or
+            // 8-byte (D = 64) load per chunk
+            using Vec = typename std::conditional<D == 128, float4, float2>::type;
             constexpr int E = D / 32;
             float acc[E];
 #pragma unroll
@@ -64,21 +71,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w,
 #pragma unroll 4
             for (uint32_t c = 0; c < sq.nchunk; ++c) {
                 const float f = fast_exp2(w.part_ml[(pb + c) * kMaxGroup + h].x - mmax);
-                const float *po = w.part_o + (static_cast<size_t>(pb + c) * kMaxGroup + h) * D + lane * E;
+                const Vec v = *reinterpret_cast<const Vec *>(
+                    w.part_o + (static_cast<size_t>(pb + c) * kMaxGroup + h) * D + lane * E);
+                const float *pv = reinterpret_cast<const float *>(&v);
 #pragma unroll
                 for (int e = 0; e < E; ++e)
-                    acc[e] += po[e] * f;
+                    acc[e] += pv[e] * f;
             }
             const float inv = 1.f / lsum;
             const uint32_t hq = kvh * g.G + h;
-            float *dst = out + ((static_cast<size_t>(ci) * g.L + l) * g.Hq + hq) * D + lane * E;
+            Vec o;
+            float *po = reinterpret_cast<float *>(&o);
 #pragma unroll
             for (int e = 0; e < E; ++e)
-                dst[e] = acc[e] * inv;
+                po[e] = acc[e] * inv;
+            *reinterpret_cast<Vec *>(out + ((static_cast<size_t>(ci) * g.L + l) * g.Hq + hq) * D + lane * E) = o;
         }
         if (lane == 0)
             lse_sh[h] = mmax + fast_log2(lsum);
     }
+    if (merge)
+        return;                    // uniform over the CTA
     __syncthreads();
     const uint32_t nbt = ds->nb_total;
     const float *lb = w.lse_blk + (static_cast<size_t>(l) * g.Hq + kvh * g.G) * nbt + sq.blk_off;
@@ -126,7 +139,7 @@ __global__ void __launch_bounds__(256) mass_kernel(const Geo g, const Work w, fl
 cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq, uint32_t max_nb,
                            cudaStream_t s)
 {
-    const dim3 grid(nseq * g.L * g.Hkv, (max_nb + kMassRange - 1) / kMassRange);
+    const dim3 grid(nseq * g.L * g.Hkv, 1 + (max_nb + kMassRange - 1) / kMassRange);
     if (g.d == 128)
         combine_kernel<128><<<grid, 32 * kMaxGroup, 0, s>>>(g, w, out);
     else

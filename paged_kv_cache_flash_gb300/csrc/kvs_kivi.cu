@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                 bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
             }
             const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const bool moved = mn0 != m0 || mn1 != m1;
             const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
             float pj[2][4];
 #pragma unroll
@@ -496,12 +497,16 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                     lse_row0[nb_total + 2 * gi + 1] = mn1 + fast_log2(w11);
                 }
             }
+            // the rescale only where a running max moved in some lane
+            // (otherwise every factor is 2^0)
+            if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                o[mt][0] *= sc0;
-                o[mt][1] *= sc1;
-                o[mt][2] *= sc0;
-                o[mt][3] *= sc1;
+                for (int mt = 0; mt < 8; ++mt) {
+                    o[mt][0] *= sc0;
+                    o[mt][1] *= sc1;
+                    o[mt][2] *= sc0;
+                    o[mt][3] *= sc1;
+                }
             }
             uint32_t pb[2][2];
 #pragma unroll

@@ -113,6 +113,34 @@ def test_llama70b_shape_cut():
     run.close()
 
 
+@pytest.mark.parametrize("fmt,Hq,Hkv,d", [
+    ("bf16", 4, 4, 64), ("bf16", 6, 2, 128), ("bf16", 16, 2, 64), ("bf16", 8, 4, 128),
+    ("fp8", 4, 4, 128), ("fp8", 6, 2, 128), ("kivi2", 8, 4, 128), ("kivi2", 3, 3, 128)])
+def test_geometry_matrix(fmt, Hq, Hkv, d):
+    """GQA groups of 1, 2, 3 and 8 query heads at head dims 64 and 128 in
+    every page format the geometry allows: 3 layers, a one-token sequence, a
+    mid-block tail and a multi-chunk sequence, both append paths."""
+    wl = W.workload("l70b_8k", L=3, Hq=Hq, Hkv=Hkv, d=d, prefill_lens=(1, 200, 777),
+                    pool_pages=80, steps=3)
+    kw = {}
+    if fmt == "fp8":
+        kw = dict(kv_dtype=K.KVS_KV_FP8_E4M3, k_scale=0.5, v_scale=2.0)
+    elif fmt == "kivi2":
+        kw = dict(kv_dtype=K.KVS_KV_KIVI2, kivi_groups=40)
+    run = Run(wl, 0.15, **kw)
+    host = None if fmt == "kivi2" else _pinned(wl.pool_pages * run.ctx.page_bytes)
+    if fmt == "kivi2":
+        assert _check_kivi_groups(run) == (64 + 640) // 32
+    for i in range(wl.steps):
+        res = run.step(host, batched_append=bool(i % 2))
+        summ = run.compare(res)
+        if host is not None:
+            _check_gather(run, res, host)
+    run.ctx.check_device()
+    print(fmt, Hq, Hkv, d, summ)
+    run.close()
+
+
 @pytest.mark.slow
 def test_llama70b_8k_full_size():
     """The 8K single-sequence workload at full size (512 blocks, 2.50 GiB), 2 steps."""
