@@ -85,25 +85,35 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_source_hash():
+# kernel sources whose code decides the DRAM traffic of each page format's decode
+TRAFFIC_SOURCES = {
+    "bf16": ("kvs_decode.cu", "kvs_ptx.h", "kvs_internal.h"),
+    "fp8": ("kvs_decode.cu", "kvs_ptx.h", "kvs_internal.h"),
+    "kivi2": ("kvs_decode.cu", "kvs_kivi.cu", "kvs_ptx.h", "kvs_internal.h"),
+}
+
+
+def decode_source_hash(kv_dtype):
     h = hashlib.sha256()
-    for f in ("kvs_decode.cu", "kvs_kivi.cu", "kvs_ptx.h", "kvs_internal.h"):
+    for f in TRAFFIC_SOURCES[kv_dtype]:
         with open(os.path.join(ROOT, "paged_kv_cache_flash_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def read_traffic(workload):
+def read_traffic(workload, kv_dtype):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu
-    summary, if it was taken on the current kernel source for this workload."""
+    summary, if it was taken on the current kernel source for this workload
+    and page format."""
     try:
         txt = open(TRAFFIC_FILE).read()
     except OSError:
         return None
-    src = re.search(r"source_hash:\s*(\S+)", txt)
-    if not src or src.group(1) != decode_source_hash():
+    src = re.search(rf"source_hash\[{re.escape(kv_dtype)}\]:\s*(\S+)", txt)
+    if not src or src.group(1) != decode_source_hash(kv_dtype):
         return None
-    m = re.search(rf"traffic_bytes_per_launch\[{re.escape(workload)}\]:\s*([0-9.eE+]+)", txt)
+    key = workload + ("" if kv_dtype == "bf16" else "_" + kv_dtype)
+    m = re.search(rf"traffic_bytes_per_launch\[{re.escape(key)}\]:\s*([0-9.eE+]+)", txt)
     return float(m.group(1)) if m else None
 
 
@@ -495,7 +505,7 @@ def run_kvs(args):
     algo = kv_bytes / K_ + wl.nseq * wl.L * wl.Hq * wl.d * 2 + sum(nb) * 4
     achieved = algo / (dec_avg / 1e3) / 1e9
     peak, peak_src = read_peaks()
-    traffic = read_traffic(args.workload + ("" if args.kv_dtype == "bf16" else "_" + args.kv_dtype))
+    traffic = read_traffic(args.workload, args.kv_dtype)
 
     # ---- end to end through host buffers --------------------------------
     e2e = None
