@@ -44,11 +44,14 @@ def parse():
     ap.add_argument("--impl", choices=["kvs", "reference"], default="kvs")
     ap.add_argument("--workload", default="l70b_128k")
     ap.add_argument("--alpha", type=float, default=None)
-    ap.add_argument("--gather", choices=["auto", "mirror", "list", "demote", "prefetch", "ids", "none"],
+    ap.add_argument("--gather", choices=["auto", "mirror", "mirror-sync", "list", "demote", "prefetch", "ids",
+                                         "ids-sync", "none"],
                     default="auto",
-                    help="auto: demote for workloads with periodic demotion, else mirror; prefetch: "
-                         "demoted blocks come back in fetch order, a budget per step, while the "
-                         "sequences without holes decode")
+                    help="auto: demote for workloads with periodic demotion, else mirror (ids in 2-bit "
+                         "contexts); mirror / ids: the asynchronous select (no host wait per step), "
+                         "mirror-sync / ids-sync: the synchronising one; prefetch: demoted blocks "
+                         "come back in fetch order, a budget per step, while the sequences without "
+                         "holes decode")
     ap.add_argument("--prefetch-budget", type=int, default=512,
                     help="blocks re-admitted per step in prefetch mode")
     ap.add_argument("--victims", choices=["lowfrac", "lrfu"], default="lowfrac",
@@ -239,10 +242,12 @@ class Pipeline:
         self.victim_mode = K.KVS_SELECT_LRFU if victims == "lrfu" else K.KVS_SELECT_LOWFRAC
         self.pf_stream = torch.cuda.Stream(device) if gather == "prefetch" else None
         self.pf_done = None
+        self.async_pending = False          # an asynchronous select's counts are due
+        self.async_staged = 0
         self.all_idx = list(range(wl.nseq))
         self.active = self.all_idx          # sequences decoded by the last step
         self._idx = {}
-        if gather in ("mirror", "list"):
+        if gather in ("mirror", "mirror-sync", "list"):
             self.host = torch.empty(self.pool_pages * self.ctx.page_bytes, dtype=torch.uint8,
                                     pin_memory=True)
         elif gather in ("demote", "prefetch"):
@@ -314,7 +319,7 @@ class Pipeline:
             self._idx[key] = self.torch.tensor(active, dtype=self.torch.int64, device=self.dev)
         return x.index_select(0, self._idx[key])
 
-    def step(self, kv_row, q, ev=None, mode_flags=None):
+    def step(self, kv_row, q, ev=None, mode_flags=None, after_decode=None):
         K, ctx, torch = self.K, self.ctx, self.torch
         main = torch.cuda.current_stream()
         sh, side = main.cuda_stream, self.side.cuda_stream    # raw handles: no lookups per call
@@ -352,20 +357,24 @@ class Pipeline:
         ctx.decode_step(ids, self._rows(q, active), out, stream=sh)
         if ev:
             ev[2].record(main)
+        if after_decode is not None:
+            after_decode()          # host work that overlaps the rest of the step
         ctx.score_update(stream=sh)
         if ev:
             ev[3].record(main)
         r = None
         self.steps_done += 1
-        if self.gather == "ids":            # the THRESH list only, no page copies
-            rc, r = ctx.select_and_gather(K.KVS_SELECT_THRESH, None, stream=sh)
-        elif self.gather in ("mirror", "list"):
-            flags = K.KVS_GATHER_MIRROR if self.gather == "mirror" else 0
+        if self.gather in ("ids", "ids-sync"):      # the THRESH list only, no page copies
+            flags = K.KVS_GATHER_ASYNC if self.gather == "ids" else 0
+            r = self._select(K.KVS_SELECT_THRESH, None, flags, sh, sh)
+        elif self.gather in ("mirror", "mirror-sync", "list"):
+            flags = {"mirror": K.KVS_GATHER_MIRROR | K.KVS_GATHER_ASYNC,
+                     "mirror-sync": K.KVS_GATHER_MIRROR, "list": 0}[self.gather]
             if mode_flags is not None:
                 flags = mode_flags
-            rc, r = ctx.select_and_gather(K.KVS_SELECT_THRESH, self.host, flags=flags, stream=sh,
-                                          side_stream=side)
-            main.wait_stream(self.side)
+            r = self._select(K.KVS_SELECT_THRESH, self.host, flags, sh, side)
+            if not flags & K.KVS_GATHER_ASYNC:
+                main.wait_stream(self.side)
         elif self.demote_every and self.steps_done % self.demote_every == 0 and not self.holes:
             # the lowest-P fraction goes to pinned host and comes back with its record
             rc, r = ctx.select_and_gather(self.victim_mode, self.host, frac=self.wl.demote_frac,
@@ -383,6 +392,29 @@ class Pipeline:
         if ev:
             ev[4].record(main)
         return r
+
+
+    def _select(self, mode, host, flags, stream, side):
+        """THRESH select; an asynchronous call returns None and its counts are
+        collected at the next select (or by flush_counts), so the host never
+        waits for the step it has just enqueued."""
+        K, ctx = self.K, self.ctx
+        if self.async_pending:
+            self.async_staged += ctx.gather_counts().n_staged
+            self.async_pending = False
+        rc, r = ctx.select_and_gather(mode, host, flags=flags, stream=stream, side_stream=side)
+        if flags & K.KVS_GATHER_ASYNC:
+            self.async_pending = True
+            return None
+        return r
+
+    def flush_counts(self):
+        """Pages staged by asynchronous selects whose counts are not yet in."""
+        if self.async_pending:
+            self.async_staged += self.ctx.gather_counts().n_staged
+            self.async_pending = False
+        n, self.async_staged = self.async_staged, 0
+        return n
 
 
 def cpu_sample(wl, n_tokens, layers, device):
@@ -426,7 +458,7 @@ def run_kvs(args):
         args.gather = "ids" if args.kv_dtype == "kivi2" else ("demote" if wl.demote_every else "mirror")
     K_, W_ = args.steps, args.warmup
     e2e_steps = 0 if args.no_e2e else K_
-    lit_steps = 0 if (args.no_literal or args.gather not in ("mirror", "list")) else 2
+    lit_steps = 0 if (args.no_literal or args.gather not in ("mirror", "mirror-sync", "list")) else 2
     total = W_ + K_ + e2e_steps + lit_steps
     pipe = Pipeline(wl, alpha, total, dev, args.gather, args.kv_dtype, args.prefetch_budget, args.victims)
     pipe.prefill()
@@ -434,6 +466,7 @@ def run_kvs(args):
 
     for i in range(W_):
         pipe.step(kv[i], qs[i])
+    pipe.flush_counts()
     torch.cuda.synchronize()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K_)]
@@ -472,6 +505,7 @@ def run_kvs(args):
     demoted = pipe.demoted_pages - demoted0
     t_stop.record()
     torch.cuda.synchronize()
+    staged += pipe.flush_counts()
     wall = time.perf_counter() - wall0
     launches = pipe.ctx.kernel_launches() - launches0
     prefetched = pipe.prefetched_pages - prefetched0
@@ -510,32 +544,72 @@ def run_kvs(args):
     # ---- end to end through host buffers --------------------------------
     e2e = None
     if e2e_steps:
+        pipe.flush_counts()
         kvh, qh = pipe.inputs(W_ + K_ + 1, e2e_steps)
         kvh = [(k.cpu().pin_memory(), v.cpu().pin_memory()) for k, v in kvh]
         qh = [q.cpu().pin_memory() for q in qh]
-        dkv = (torch.empty_like(kv[0][0]), torch.empty_like(kv[0][1]))
-        dq = torch.empty_like(qs[0])
+        # double-buffered: the inputs of step i + 1 go up on one copy stream and
+        # the output of step i comes down on another while step i + 1 computes;
+        # every copy is inside the timed region
+        dkv = [(torch.empty_like(kv[0][0]), torch.empty_like(kv[0][1])) for _ in range(2)]
+        dq = [torch.empty_like(qs[0]) for _ in range(2)]
+        outs = [pipe.out, torch.empty_like(pipe.out)]
         out_h = torch.empty(pipe.out.shape, dtype=torch.float32, pin_memory=True)
         h2d = kvh[0][0].numel() * 2 + kvh[0][1].numel() * 2 + qh[0].numel() * 2
         d2h = out_h.numel() * 4
+        main = torch.cuda.current_stream()
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        out_free = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+
+        def upload(i):
+            b = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(done[b])      # step i - 2 has read this buffer
+                dkv[b][0].copy_(kvh[i][0], non_blocking=True)
+                dkv[b][1].copy_(kvh[i][1], non_blocking=True)
+                dq[b].copy_(qh[i], non_blocking=True)
+                in_ready[b].record(up)
+
+        def after_decode(i):
+            # runs once step i's decode is enqueued, while the device works: its
+            # inputs are consumed and its output final on the stream from here
+            b = i % 2
+            done[b].record(main)
+            with torch.cuda.stream(down):
+                down.wait_event(done[b])
+                out_h.copy_(outs[b], non_blocking=True)
+                out_free[b].record(down)
+            if i + 1 < e2e_steps:
+                upload(i + 1)
+
         torch.cuda.synchronize()
         e_b = 0
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record()
+        up.wait_event(s0)
+        upload(0)
         for i in range(e2e_steps):
-            dkv[0].copy_(kvh[i][0], non_blocking=True)
-            dkv[1].copy_(kvh[i][1], non_blocking=True)
-            dq.copy_(qh[i], non_blocking=True)
-            pipe.step(dkv, dq)
-            out_h.copy_(pipe.out, non_blocking=True)
+            b = i % 2
+            main.wait_event(in_ready[b])
+            if i >= 2:
+                main.wait_event(out_free[b])
+            pipe.out = outs[b]
+            pipe.step(dkv[b], dq[b], after_decode=lambda i=i: after_decode(i))
             e_b += pipe.kv_bytes_this_step()
+        main.wait_stream(down)
+        main.wait_stream(up)
         s1.record()
         torch.cuda.synchronize()
+        pipe.out = outs[0]
         e_ms = s0.elapsed_time(s1)
         e_ms_max, e_b_all = reduce_over_ranks(e_ms, e_b, dev)
         e_val = e_b_all / (e_ms_max / 1e3) / 1e9
         e2e = {"value": round(e_val, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e_ms / e2e_steps, 4)}
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e_ms / e2e_steps, 4),
+               "copies": "pinned host, double-buffered on two copy streams beside the steps"}
 
     # ---- literal per-step gather of every P < 0.3 page (list mode) -------
     literal = None
@@ -586,6 +660,8 @@ def run_kvs(args):
                                    + (f", {wl.shared_prefix_tokens}-token shared prefix" if wl.shared_prefix_tokens else ""),
                        "global_batch": wl.nseq, "seq_len": max(wl.prefill_lens),
                        "alpha": alpha, "gather": args.gather,
+                       "select_call": ("KVS_GATHER_ASYNC: no host wait; counts read one step later"
+                                       if args.gather in ("mirror", "ids") else "synchronising"),
                        **({"prefetch_budget": args.prefetch_budget} if args.gather == "prefetch" else {}),
                        **({"victims": args.victims} if args.gather in ("demote", "prefetch") else {}),
                        "l2": "inputs larger than L2 (KV per step >> 129 MB), no flush",

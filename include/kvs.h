@@ -110,7 +110,8 @@ typedef enum kvs_kv_dtype {
  * group -- 3 bits per element.  The table entry of a quantised block is
  * KVS_TABLE_GROUP(g) for its group page g (both blocks of the group).
  * KIVI contexts share no blocks between sequences and gather no pages
- * (kvs_select_and_gather returns the id list only, flags 0, no host_dst). */
+ * (kvs_select_and_gather returns the id list only: no host_dst, flags 0 or
+ * KVS_GATHER_ASYNC). */
 #define KVS_KIVI_GROUP_TOKENS 32u
 #define KVS_KIVI_RESIDUAL 128u
 #define KVS_KIVI_TILE_BYTES 3072u
@@ -126,6 +127,8 @@ typedef enum kvs_select_mode {
 #define KVS_GATHER_DEMOTE 1u  /* free the gathered pages, keep records by key */
 #define KVS_GATHER_MIRROR 2u  /* host_dst mirrors the pool (page p at p*page_bytes);
                                  pages whose host copy is current are not re-sent */
+#define KVS_GATHER_ASYNC 4u   /* with MIRROR, or alone in a 2-bit context: no host
+                                 wait; counts later from kvs_gather_counts */
 
 typedef struct kvs_config {
     uint32_t num_layers;          /* L                                        */
@@ -343,9 +346,25 @@ int kvs_set_alpha(kvs_ctx_t *ctx, double alpha);
  * again.  KVS_GATHER_DEMOTE (list mode only): eligible records are demoted:
  * their 64-byte record and the offset of their page in host_dst are kept
  * under their key, the table entry is cleared and the page freed.  The
- * caller keeps host_dst alive until kvs_readmit. */
+ * caller keeps host_dst alive until kvs_readmit.
+ * KVS_GATHER_ASYNC (with KVS_GATHER_MIRROR, or as the only flag of a 2-bit
+ * context): the call enqueues its work on `stream` and returns without
+ * waiting for the device; *res is zeroed.  The stale pages are written into
+ * host_dst by a device kernel on `stream` through the buffer's device
+ * mapping, so host_dst must be page-locked memory the device can address
+ * (cudaHostAlloc / cudaMallocHost, or cudaHostRegister'ed): KVS_EINVAL
+ * otherwise.  ids_dev and slot_dev receive min(ids_capacity, N) entries;
+ * those past the list's length are unspecified.  The counts of the latest
+ * such call come from kvs_gather_counts.  KVS_EINVAL with DEMOTE or in list
+ * mode. */
 int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args,
                           kvs_gather_result *res);
+
+/* Counts of the latest KVS_GATHER_ASYNC select: waits (bounded, KVS_ETIMEOUT)
+ * until that call's work on its stream has reached them, then fills *res as
+ * a synchronous call would have (n_demoted = 0).  KVS_EINVAL if no
+ * asynchronous select was made on this context. */
+int kvs_gather_counts(kvs_ctx_t *ctx, kvs_gather_result *res);
 
 /* Re-admits demoted blocks [GQA]: for each key, takes a page from the free
  * list, copies the page bytes from host_src (the buffer given to the demoting

@@ -28,7 +28,7 @@ KVS_SELECT_THRESH, KVS_SELECT_LOWFRAC = 0, 1
 KVS_SELECT_LRFU = 2
 KVS_KV_BF16, KVS_KV_FP8_E4M3, KVS_KV_KIVI2 = 0, 1, 2
 KVS_KIVI_GROUP_TOKENS, KVS_KIVI_RESIDUAL = 32, 128
-KVS_GATHER_DEMOTE, KVS_GATHER_MIRROR = 1, 2
+KVS_GATHER_DEMOTE, KVS_GATHER_MIRROR, KVS_GATHER_ASYNC = 1, 2, 4
 KVS_MAX_CALL_SEQS = 256
 KVS_PREFETCH_MAX = 4096
 BLOCK_TOKENS = 16
@@ -101,6 +101,7 @@ _SIGS = {
     "kvs_set_alpha": (ctypes.c_int, [c_vp, c_dbl]),
     "kvs_select_and_gather": (ctypes.c_int, [c_vp, ctypes.POINTER(kvs_gather_args),
                                              ctypes.POINTER(kvs_gather_result)]),
+    "kvs_gather_counts": (ctypes.c_int, [c_vp, ctypes.POINTER(kvs_gather_result)]),
     "kvs_readmit": (ctypes.c_int, [c_vp, ctypes.POINTER(kvs_key), c_u32, c_vp, c_sz, c_vp]),
     "kvs_prefetch_plan": (ctypes.c_int, [c_vp, c_u32, ctypes.POINTER(kvs_key), ctypes.POINTER(c_dbl),
                                          ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(c_u32), c_vp]),
@@ -327,6 +328,12 @@ class Context:
         if rc not in (KVS_OK, KVS_ETRUNC):
             _check(self.h, rc)
         return rc, r
+
+    def gather_counts(self):
+        """Counts of the latest KVS_GATHER_ASYNC select (waits for them)."""
+        r = kvs_gather_result()
+        _check(self.h, lib().kvs_gather_counts(self.h, ctypes.byref(r)))
+        return r
 
     def readmit(self, keys, host_src, stream=None):
         n = len(keys)

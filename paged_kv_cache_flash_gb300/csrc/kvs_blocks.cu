@@ -724,6 +724,42 @@ __global__ void __launch_bounds__(256)
         dst[i] = __ldcs(src + i);
 }
 
+// The plan's stale pages (plan[2] of them, page ids from plan + 4) straight
+// into the host mirror through its device mapping: pool page p to host page
+// p.  Every CTA takes its slice of every page (no division per element); an
+// id outside the pool is flagged and skipped.
+__global__ void __launch_bounds__(256)
+    mirror_copy_kernel(const uint4 *pool, const uint32_t *plan, uint4 *host, uint64_t page_vec,
+                       uint32_t pool_blocks, uint32_t *err, uint32_t *err_info)
+{
+    const uint32_t n = plan[2];
+    const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+    const uint64_t i0 = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (uint32_t k = 0; k < n; ++k) {
+        const uint32_t p = plan[4 + k];
+        if (p >= pool_blocks) {
+            if (i0 == 0) {
+                atomicOr(err, kErrBadPage);
+                atomicCAS(err_info, 0u, p | 0x80000000u);
+            }
+            continue;
+        }
+        const uint4 *src = pool + p * page_vec;
+        uint4 *dst = host + p * page_vec;
+        uint64_t i = i0;
+        for (; i + 3 * stride < page_vec; i += 4 * stride) {
+            const uint4 a = __ldcs(src + i), b = __ldcs(src + i + stride);
+            const uint4 c = __ldcs(src + i + 2 * stride), d = __ldcs(src + i + 3 * stride);
+            dst[i] = a;
+            dst[i + stride] = b;
+            dst[i + 2 * stride] = c;
+            dst[i + 3 * stride] = d;
+        }
+        for (; i < page_vec; i += stride)
+            dst[i] = __ldcs(src + i);
+    }
+}
+
 // staging page i -> pool page pages[i] (re-admission); grid.y = parts of a page
 __global__ void __launch_bounds__(256)
     scatter_kernel(const uint4 *staging, const int32_t *pages, uint4 *pool, uint64_t page_vec)
@@ -837,6 +873,15 @@ cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pag
     const uint32_t parts = static_cast<uint32_t>(std::max<uint64_t>(1, std::min<uint64_t>(64, page_vec / 4096)));
     gather_kernel<<<dim3(npages, parts), 256, 0, s>>>(reinterpret_cast<const uint4 *>(pool), pages,
                                                      reinterpret_cast<uint4 *>(staging), page_vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mirror_copy(const Geo &g, const Work &w, const uint16_t *pool, void *host_dev,
+                               uint32_t pool_blocks, int grid, cudaStream_t s)
+{
+    mirror_copy_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4 *>(pool), w.readback,
+                                            reinterpret_cast<uint4 *>(host_dev), g.page_bytes / 16,
+                                            pool_blocks, w.err, w.err_info);
     return cudaGetLastError();
 }
 

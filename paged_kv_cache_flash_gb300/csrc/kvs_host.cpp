@@ -102,6 +102,9 @@ struct kvs_ctx {
     bool ring_used[kRingSlots]{};
     uint32_t ring_next = 0;
     uint32_t *pinned_small = nullptr;               // readbacks
+    uint32_t *async_hdr = nullptr;                  // counts of the latest ASYNC select
+    cudaEvent_t ev_async{};                         // ... on the host after this event
+    int async_kind = 0;                             // 0 none yet, 1 mirror, 2 ids only
 
     cudaEvent_t ev_ready[2]{}, ev_side_done{}, ev_pool_release{};
     cudaEvent_t ev_dec_start = nullptr, ev_dec_stop = nullptr;   // caller's timing events
@@ -122,7 +125,7 @@ struct kvs_ctx {
         for (auto &e : ring_ev)
             if (e)
                 cudaEventDestroy(e);
-        for (auto e : {ev_ready[0], ev_ready[1], ev_side_done, ev_pool_release, ev_quarantine, ev_wait})
+        for (auto e : {ev_ready[0], ev_ready[1], ev_side_done, ev_pool_release, ev_quarantine, ev_wait, ev_async})
             if (e)
                 cudaEventDestroy(e);
         for (auto e : chunk_ev)
@@ -131,6 +134,8 @@ struct kvs_ctx {
             cudaFreeHost(ring_host);
         if (pinned_small)
             cudaFreeHost(pinned_small);
+        if (async_hdr)
+            cudaFreeHost(async_hdr);
     }
 };
 
@@ -803,6 +808,8 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
                      cudaHostAllocDefault));
     CU(cudaEventCreateWithFlags(&ctx->ev_wait, cudaEventDisableTiming));
     CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->pinned_small), kReadbackBytes, cudaHostAllocDefault));
+    CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->async_hdr), 64, cudaHostAllocDefault));
+    CU(cudaEventCreateWithFlags(&ctx->ev_async, cudaEventDisableTiming));
     for (auto &e : ctx->ring_ev)
         CU(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     for (int i = 0; i < 2; ++i) {
@@ -1250,10 +1257,16 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
     if (!ctx->have_set)
         return fail(ctx, KVS_EINVAL, "no decode set: call kvs_decode_step first");
     const bool mirror = args->flags & KVS_GATHER_MIRROR, demote = args->flags & KVS_GATHER_DEMOTE;
+    const bool async = args->flags & KVS_GATHER_ASYNC;
+    if (args->flags & ~(KVS_GATHER_MIRROR | KVS_GATHER_DEMOTE | KVS_GATHER_ASYNC))
+        return fail(ctx, KVS_EINVAL, "unknown flags 0x%x", args->flags);
     if (mirror && demote)
         return fail(ctx, KVS_EINVAL, "DEMOTE works in list mode only");
-    if (ctx->geo.kivi && (args->flags || args->host_dst))
-        return fail(ctx, KVS_EINVAL, "2-bit group contexts return the selection only (no flags, no host_dst)");
+    if (ctx->geo.kivi && ((args->flags & ~KVS_GATHER_ASYNC) || args->host_dst))
+        return fail(ctx, KVS_EINVAL,
+                    "2-bit group contexts return the selection only (no host_dst, flags 0 or ASYNC)");
+    if (async && !mirror && !ctx->geo.kivi)
+        return fail(ctx, KVS_EINVAL, "ASYNC works with MIRROR (or in a 2-bit context) only");
     if (args->mode != KVS_SELECT_THRESH && args->mode != KVS_SELECT_LOWFRAC && args->mode != KVS_SELECT_LRFU)
         return fail(ctx, KVS_EINVAL, "unknown selection mode %d", args->mode);
     const size_t pb = ctx->sz.page_bytes;
@@ -1263,6 +1276,17 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         return fail(ctx, KVS_EINVAL, "frac must be in [0, 1]");
     if (args->mode == KVS_SELECT_LRFU && !(ctx->cfg.alpha < 1.0))
         return fail(ctx, KVS_EINVAL, "LRFU needs alpha < 1 (the key slope -ln(1-alpha) is infinite)");
+    // ASYNC mirror: the device address of host_dst (page-locked and mapped)
+    void *host_dev = nullptr;
+    if (async && mirror) {
+        cudaPointerAttributes pa{};
+        if (cudaPointerGetAttributes(&pa, args->host_dst) != cudaSuccess || pa.type != cudaMemoryTypeHost ||
+            !pa.devicePointer) {
+            cudaGetLastError();
+            return fail(ctx, KVS_EINVAL, "ASYNC needs host_dst in page-locked memory the device can address");
+        }
+        host_dev = pa.devicePointer;
+    }
     cudaStream_t s = S(args->stream);
     cudaStream_t side = args->side_stream ? S(args->side_stream) : s;
     const uint32_t N = ctx->dset->nb_total;
@@ -1303,6 +1327,15 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
                                           N, s),
                             "select", 2)))
             return rc;
+        if (ctx->geo.kivi && async) {
+            CU(cudaMemcpyAsync(ctx->async_hdr, w.sel_count, 4, cudaMemcpyDeviceToHost, s));
+            CU(cudaEventRecord(ctx->ev_async, s));
+            ctx->async_kind = 2;
+            const uint32_t n = std::min(N, args->ids_capacity);
+            if (n && args->ids_dev)
+                CU(cudaMemcpyAsync(args->ids_dev, w.sel_ids, n * sizeof(kvs_key), cudaMemcpyDeviceToDevice, s));
+            return KVS_OK;
+        }
         if (ctx->geo.kivi) {
             // the id list only: quantised blocks have no page to plan
             CU(cudaMemcpyAsync(ctx->pinned_small, w.sel_count, 4, cudaMemcpyDeviceToHost, s));
@@ -1316,6 +1349,26 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         }
         if ((rc = launch_rc(ctx, launch_plan(w, mirror ? 1u : 0u, s), "plan")))
             return rc;
+        if (async) {
+            // the stale pages go to the host mirror by a device kernel in
+            // stream order (writers after it need no wait); the counts follow
+            // into pinned memory, read by kvs_gather_counts
+            if ((rc = launch_rc(ctx,
+                                launch_mirror_copy(ctx->geo, w, static_cast<const uint16_t *>(ctx->buf.pool),
+                                                   host_dev, ctx->cfg.pool_blocks, 2 * ctx->sm_count, s),
+                                "mirror copy")))
+                return rc;
+            CU(cudaMemcpyAsync(ctx->async_hdr, w.readback, 16, cudaMemcpyDeviceToHost, s));
+            CU(cudaEventRecord(ctx->ev_async, s));
+            ctx->async_kind = 1;
+            const uint32_t n = std::min(N, args->ids_capacity);
+            if (n && args->ids_dev)
+                CU(cudaMemcpyAsync(args->ids_dev, w.sel_ids, n * sizeof(kvs_key), cudaMemcpyDeviceToDevice, s));
+            if (n && args->slot_dev)
+                CU(cudaMemcpyAsync(args->slot_dev, w.plan_slot, n * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                                   s));
+            return KVS_OK;
+        }
         // one readback: counts and the head of the copy list
         CU(cudaMemcpyAsync(ctx->pinned_small, w.readback, kReadbackBytes, cudaMemcpyDeviceToHost, s));
         WAIT(s);
@@ -1330,6 +1383,14 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
                                cudaMemcpyDeviceToHost, s));
             WAIT(s);
         }
+    }
+    if (async) {
+        // nothing to select (k = 0): zero counts, in stream order
+        CU(cudaMemsetAsync(w.readback, 0, 16, s));
+        CU(cudaMemcpyAsync(ctx->async_hdr, w.readback, 16, cudaMemcpyDeviceToHost, s));
+        CU(cudaEventRecord(ctx->ev_async, s));
+        ctx->async_kind = ctx->geo.kivi ? 2 : 1;
+        return KVS_OK;
     }
     res->n_selected = nsel;
     res->n_pages = npages;
@@ -1478,6 +1539,27 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
     }
     if (trunc)
         return fail(ctx, KVS_ETRUNC, "host_dst holds %u of %u pages", nstage, npages);
+    return KVS_OK;
+}
+
+int kvs_gather_counts(kvs_ctx_t *ctx, kvs_gather_result *res)
+{
+    KVS_RANGE();
+    if (!ctx)
+        return KVS_EINVAL;
+    if (!res)
+        return fail(ctx, KVS_EINVAL, "res must be given");
+    std::memset(res, 0, sizeof *res);
+    if (!ctx->async_kind)
+        return fail(ctx, KVS_EINVAL, "no asynchronous select on this context");
+    if (int rc = event_wait(ctx, ctx->ev_async, "kvs_gather_counts"))
+        return rc;
+    res->n_selected = ctx->async_hdr[0];
+    if (ctx->async_kind == 1) {
+        res->n_pages = ctx->async_hdr[1];
+        res->n_staged = ctx->async_hdr[2];
+        res->bytes_to_host = static_cast<uint64_t>(res->n_staged) * ctx->sz.page_bytes;
+    }
     return KVS_OK;
 }
 

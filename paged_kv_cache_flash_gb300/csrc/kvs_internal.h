@@ -188,6 +188,8 @@ cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, co
 cudaError_t launch_plan(const Work &w, uint32_t mirror, cudaStream_t s);
 cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *pages, uint32_t npages,
                            uint16_t *pool, cudaStream_t s);
+cudaError_t launch_mirror_copy(const Geo &g, const Work &w, const uint16_t *pool, void *host_dev,
+                               uint32_t pool_blocks, int grid, cudaStream_t s);
 cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pages,
                           uint32_t npages, uint8_t *staging, cudaStream_t s);
 cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, uint8_t *page_clean,

@@ -145,6 +145,8 @@ class Run:
         side = torch.cuda.Stream()
         rc, r = self.ctx.select_and_gather(mode, gather_host, frac=frac, flags=flags, ids=ids,
                                            slots=slots, side_stream=side)
+        if flags & K.KVS_GATHER_ASYNC:
+            r = self.ctx.gather_counts()
         side.synchronize()
         torch.cuda.synchronize()
         res["rc"], res["gather"] = rc, r

@@ -1,4 +1,6 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -541,4 +543,99 @@ def test_mirror_mode_sends_each_full_page_once():
         for (sid, b), slot in zip(res["ids"], res["slots"]):
             assert hb[slot * pb:(slot + 1) * pb].tobytes() == run.oracle_page(sid, b)
     assert staged[0] > 0 and max(staged[1:]) <= 2
+    run.close()
+
+
+# ------------------------------------------------- asynchronous mirror mode
+
+
+def _counts(r):
+    return (r.n_selected, r.n_pages, r.n_staged, r.n_demoted, r.bytes_to_host)
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", dict(prefill_lens=(100, 64), pool_pages=20, steps=6, skew=True)),
+    ("l70b_8k", dict(L=4, prefill_lens=(1000, 300, 17), pool_pages=100, steps=5))])
+def test_async_mirror_matches_sync(name, kw):
+    """KVS_GATHER_MIRROR | KVS_GATHER_ASYNC (stale pages written by a device
+    kernel through the mirror's mapping, counts from kvs_gather_counts)
+    against the synchronous mirror on a second context fed the same steps:
+    same ids, slots and counts every step, byte-equal host mirrors, and the
+    mirrored pages equal the oracle's page assembly."""
+    wl = W.workload(name, **kw)
+    sync_run, async_run = Run(wl, 0.15), Run(wl, 0.15, oracle_on=False)
+    pb = sync_run.ctx.page_bytes
+    m_sync, m_async = _pinned(wl.pool_pages * pb), _pinned(wl.pool_pages * pb)
+    m_sync.zero_()
+    m_async.zero_()      # pages neither context writes compare equal too
+    staged = 0
+    for _ in range(wl.steps):
+        a = sync_run.step(m_sync, flags=K.KVS_GATHER_MIRROR)
+        b = async_run.step(m_async, flags=K.KVS_GATHER_MIRROR | K.KVS_GATHER_ASYNC)
+        sync_run.compare(a)
+        assert a["ids"] == b["ids"] and a["slots"] == b["slots"]
+        assert _counts(a["gather"]) == _counts(b["gather"])
+        assert torch.equal(a["out"], b["out"])
+        assert m_sync.numpy().tobytes() == m_async.numpy().tobytes()
+        hb = m_async.numpy()
+        for (sid, blk), slot in zip(b["ids"], b["slots"]):
+            if slot >= 0:
+                assert hb[slot * pb:(slot + 1) * pb].tobytes() == sync_run.oracle_page(sid, blk)
+        staged += b["gather"].n_staged
+    assert staged > 0
+    async_run.ctx.check_device()
+    sync_run.close()
+    async_run.close()
+
+
+def test_async_ids_only_in_2bit_context():
+    """2-bit context: KVS_GATHER_ASYNC returns the same THRESH and LOWFRAC
+    lists as the synchronous call, counts through kvs_gather_counts."""
+    wl = W.workload("l70b_8k", L=2, prefill_lens=(300, 500), pool_pages=60, steps=3)
+    run = Run(wl, 0.15, kv_dtype=K.KVS_KV_KIVI2, kivi_groups=32)
+    for _ in range(wl.steps):
+        run.compare(run.step(None))
+    nrec = sum(len(run.ctx.export_records(s)) for s in run.ids)
+    for mode, frac in ((K.KVS_SELECT_THRESH, 0.0), (K.KVS_SELECT_LOWFRAC, 0.25)):
+        i1 = torch.zeros(2 * nrec, dtype=torch.int64, device="cuda")
+        i2 = torch.zeros(2 * nrec, dtype=torch.int64, device="cuda")
+        rc, r1 = run.ctx.select_and_gather(mode, frac=frac, ids=i1)
+        rc2, r0 = run.ctx.select_and_gather(mode, frac=frac, flags=K.KVS_GATHER_ASYNC, ids=i2)
+        assert rc == rc2 == K.KVS_OK and _counts(r0) == (0, 0, 0, 0, 0)
+        r2 = run.ctx.gather_counts()
+        torch.cuda.synchronize()
+        assert _counts(r1) == _counts(r2) and r1.n_selected > 0
+        n = r1.n_selected
+        assert torch.equal(i1[:2 * n], i2[:2 * n])
+    run.close()
+
+
+def test_async_error_paths():
+    wl = W.workload("tiny", prefill_lens=(100,), pool_pages=20, steps=1)
+    run = Run(wl, 0.15, oracle_on=False)
+    run.step(None)
+    pb = run.ctx.page_bytes
+    mirror = _pinned(wl.pool_pages * pb)
+    with pytest.raises(K.KvsError) as e:        # no asynchronous select yet
+        run.ctx.gather_counts()
+    assert e.value.code == K.KVS_EINVAL
+    for flags in (K.KVS_GATHER_ASYNC, K.KVS_GATHER_ASYNC | K.KVS_GATHER_DEMOTE, 64):
+        with pytest.raises(K.KvsError) as e:
+            run.ctx.select_and_gather(K.KVS_SELECT_THRESH, mirror, flags=flags)
+        assert e.value.code == K.KVS_EINVAL
+    # pageable host memory cannot take device writes: refused before any work
+    page = np.zeros(wl.pool_pages * pb, dtype=np.uint8)
+    a = K.kvs_gather_args()
+    a.mode = K.KVS_SELECT_THRESH
+    a.flags = K.KVS_GATHER_MIRROR | K.KVS_GATHER_ASYNC
+    a.host_dst = page.ctypes.data
+    a.host_dst_bytes = page.nbytes
+    r = K.kvs_gather_result()
+    rc = K.lib().kvs_select_and_gather(run.ctx.h, ctypes.byref(a), ctypes.byref(r))
+    assert rc == K.KVS_EINVAL and b"page-locked" in K.lib().kvs_last_error(run.ctx.h)
+    # a valid asynchronous call after the refusals
+    rc, _ = run.ctx.select_and_gather(K.KVS_SELECT_THRESH, mirror,
+                                      flags=K.KVS_GATHER_MIRROR | K.KVS_GATHER_ASYNC)
+    assert rc == K.KVS_OK and run.ctx.gather_counts().n_selected >= 0
+    run.ctx.check_device()
     run.close()
