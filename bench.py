@@ -254,8 +254,10 @@ class Pipeline:
             k_max = int(math.floor(wl.demote_frac * (need + wl.nseq))) + 1
             self.host = torch.empty(k_max * self.ctx.page_bytes, dtype=torch.uint8, pin_memory=True)
             self.ids_dev = torch.zeros(2 * (need + wl.nseq), dtype=torch.int64, device=device)
-            # set-up: the first device->host copy into fresh pinned memory maps it;
-            # do that once here rather than inside the first timed demotion
+        if self.host is not None:
+            # set-up: the first copy-engine transfer into fresh pinned memory maps
+            # it (about 2/3 of the warm rate); do that once here rather than inside
+            # the first timed gather or demotion
             z = torch.zeros(1 << 30, dtype=torch.uint8, device=device)
             for a in range(0, self.host.numel(), z.numel()):
                 n = min(z.numel(), self.host.numel() - a)
