@@ -639,3 +639,61 @@ def test_async_error_paths():
     assert rc == K.KVS_OK and run.ctx.gather_counts().n_selected >= 0
     run.ctx.check_device()
     run.close()
+
+
+def test_async_steps_enqueued_back_to_back():
+    """The pipelined use of KVS_GATHER_ASYNC: 24 steps (append, decode, score,
+    asynchronous mirror select) enqueued with no host wait between them, the
+    counts of each select read one step later; against a synchronising
+    context fed the same inputs: every step's output, the final records and
+    the host mirrors are bit-equal, and the staged-page totals agree."""
+    wl = W.workload("l70b_8k", L=4, prefill_lens=(700, 300, 33), pool_pages=80, steps=24)
+    sync_run, async_run = Run(wl, 0.15, oracle_on=False), Run(wl, 0.15, oracle_on=False)
+    pb = sync_run.ctx.page_bytes
+    m_sync, m_async = _pinned(wl.pool_pages * pb), _pinned(wl.pool_pages * pb)
+    m_sync.zero_()
+    m_async.zero_()
+    ids = sync_run.ids
+    ntok = list(wl.prefill_lens)
+    rows, qs = [], []
+    for t in range(1, wl.steps + 1):
+        new = [W.kv_tokens(wl, s, ntok[s] + t - 1, ntok[s] + t, "cuda") for s in range(wl.nseq)]
+        rows.append((torch.cat([k for k, _ in new]).contiguous(), torch.cat([v for _, v in new]).contiguous()))
+        qs.append(torch.stack([W.queries(wl, s, t, "cuda") for s in range(wl.nseq)]).contiguous())
+    torch.cuda.synchronize()
+    shape = (wl.nseq, wl.L, wl.Hq, wl.d)
+    outs_s = [torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(wl.steps)]
+    outs_a = [torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(wl.steps)]
+    side = torch.cuda.Stream()
+    staged_s = staged_a = 0
+    pending = False
+    for t in range(wl.steps):
+        a = async_run.ctx
+        a.append_step(ids, *rows[t])
+        a.decode_step(ids, qs[t], outs_a[t])
+        a.score_update()
+        if pending:                      # the previous step's counts, read one step late
+            staged_a += a.gather_counts().n_staged
+        rc, r0 = a.select_and_gather(K.KVS_SELECT_THRESH, m_async,
+                                     flags=K.KVS_GATHER_MIRROR | K.KVS_GATHER_ASYNC)
+        assert rc == K.KVS_OK and r0.n_selected == 0
+        pending = True
+        s = sync_run.ctx
+        s.append_step(ids, *rows[t])
+        s.decode_step(ids, qs[t], outs_s[t])
+        s.score_update()
+        rc, r = s.select_and_gather(K.KVS_SELECT_THRESH, m_sync, flags=K.KVS_GATHER_MIRROR,
+                                    side_stream=side)
+        staged_s += r.n_staged
+    staged_a += async_run.ctx.gather_counts().n_staged
+    side.synchronize()
+    torch.cuda.synchronize()
+    for t in range(wl.steps):
+        assert torch.equal(outs_s[t], outs_a[t]), t
+    for sid in ids:
+        assert sync_run.ctx.export_records(sid).tobytes() == async_run.ctx.export_records(sid).tobytes()
+    assert m_sync.numpy().tobytes() == m_async.numpy().tobytes()
+    assert staged_a == staged_s > 0
+    async_run.ctx.check_device()
+    sync_run.close()
+    async_run.close()
