@@ -40,7 +40,7 @@ def _stale() -> bool:
     if not LIB.exists():
         return True
     t = LIB.stat().st_mtime
-    deps = [CSRC / s for s in SOURCES] + [CSRC / "kvs_internal.h", CSRC / "kvs_ptx.h",
+    deps = [CSRC / s for s in SOURCES] + [CSRC / "kvs_internal.h", CSRC / "kvs_launch.h", CSRC / "kvs_ptx.h",
                                          ROOT / "include" / "kvs.h", Path(__file__)]
     return any(p.stat().st_mtime > t for p in deps)
 

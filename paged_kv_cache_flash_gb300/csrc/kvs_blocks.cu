@@ -13,6 +13,7 @@
 #include <cuda_fp8.h>
 
 #include "kvs_internal.h"
+#include "kvs_launch.h"
 
 namespace kvs {
 namespace {
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kSelThreads)
 // Writes picked records in record order: key, page and record index.
 __global__ void __launch_bounds__(kSelThreads)
     select_scatter_kernel(const Geo g, const Work w, const kvs_record *recs, const int32_t *table,
-                          int mode, double lrfu_c, uint32_t nb_total, uint32_t ntiles)
+                          int mode, double lrfu_c, uint32_t nb_total, uint32_t ntiles, uint32_t count_pages)
 {
     __shared__ uint32_t wpre[kSelThreads / 32];
     __shared__ uint32_t base_sh;
@@ -373,11 +374,17 @@ __global__ void __launch_bounds__(kSelThreads)
         if (!pk[q])
             continue;
         const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
+        const int32_t page = table[static_cast<size_t>(slots[q]) * g.mb + bs[q]];
         w.sel_ids[pos] = keys[q];
         w.sel_recs[pos] = recs[static_cast<size_t>(slots[q]) * g.mb + bs[q]];
-        w.sel_pages[pos] = table[static_cast<size_t>(slots[q]) * g.mb + bs[q]];
+        w.sel_pages[pos] = page;
         w.sel_recidx[pos] = r;
         w.sel_full[pos] = (bs[q] + 1) * kBlockTokens <= nts[q] ? 1 : 0;
+        if (count_pages && page >= 0) {
+            // for the gather plan: listed references and first list position per page
+            atomicAdd(&w.page_cnt[page], 1u);
+            atomicMin(&w.page_first[page], pos);
+        }
         ++pos;
     }
 }
@@ -631,7 +638,9 @@ __global__ void __launch_bounds__(1024)
     }
 }
 
-// Gather plan of the selected list, one block of 1024 threads:
+// Gather plan of the selected list, one block of 1024 threads, from the
+// per-page counts select_scatter_kernel made (listed references page_cnt,
+// first list position page_first):
 //  - a page is eligible when every reference to it is selected (selected
 //    references == reference count), and is planned once, at its first
 //    selected position;
@@ -645,13 +654,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Work w, uint32_t mirro
 {
     __shared__ uint32_t wsum[33];
     const uint32_t n = *w.sel_count;
-    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
-        const int32_t p = w.sel_pages[i];
-        atomicAdd(&w.page_cnt[p], 1u);
-        atomicMin(&w.page_first[p], i);
-    }
-    __syncthreads();
-    // leaders in list order: 4 consecutive entries per thread per tile
+    // leaders in list order: 4 consecutive entries per thread per tile; one
+    // block scan of the packed counts (leaders low 16 bits, stale pages high:
+    // at most 4,096 of each per tile)
     uint32_t npages = 0, ncopy = 0;
     for (uint32_t t0 = 0; t0 < n; t0 += 4 * blockDim.x) {
         const uint32_t i0 = t0 + 4 * threadIdx.x;
@@ -671,10 +676,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Work w, uint32_t mirro
             nd += dirty[q];
         }
         uint32_t tot;
-        uint32_t pos = npages + block_scan_1024(nl, wsum, &tot);
-        npages += tot;
-        uint32_t cpos = ncopy + block_scan_1024(nd, wsum, &tot);
-        ncopy += tot;
+        const uint32_t ex = block_scan_1024(nl | (nd << 16), wsum, &tot);
+        uint32_t pos = npages + (ex & 0xffffu), cpos = ncopy + (ex >> 16);
+        npages += tot & 0xffffu;
+        ncopy += tot >> 16;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             if (lead[q]) {
@@ -690,16 +695,50 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Work w, uint32_t mirro
         }
     }
     __syncthreads();
-    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
-        const int32_t p = w.sel_pages[i];
-        const bool elig = w.page_cnt[p] == w.dev_refcnt[p];
-        w.plan_slot[i] = elig ? (mirror ? p : w.page_pos[p]) : -1;
+    // slots: 8 entries per thread per pass, every load of a pass issued
+    // before its stores
+    constexpr int R = 8;
+    for (uint32_t t0 = 0; t0 < n; t0 += R * blockDim.x) {
+        int32_t p[R];
+        uint32_t cnt[R], ref[R];
+        int32_t pos[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const uint32_t i = t0 + q * blockDim.x + threadIdx.x;
+            p[q] = i < n ? w.sel_pages[i] : -1;
+        }
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            cnt[q] = ref[q] = 0;
+            pos[q] = -1;
+            if (p[q] >= 0) {
+                cnt[q] = w.page_cnt[p[q]];
+                ref[q] = w.dev_refcnt[p[q]];
+                pos[q] = mirror ? p[q] : w.page_pos[p[q]];
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const uint32_t i = t0 + q * blockDim.x + threadIdx.x;
+            if (i < n)
+                w.plan_slot[i] = (p[q] >= 0 && cnt[q] == ref[q]) ? pos[q] : -1;
+        }
     }
     __syncthreads();
-    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
-        const int32_t p = w.sel_pages[i];
-        w.page_cnt[p] = 0;
-        w.page_first[p] = 0xffffffffu;
+    // page_cnt / page_first back to 0 / ~0 for the next plan
+    for (uint32_t t0 = 0; t0 < n; t0 += R * blockDim.x) {
+        int32_t p[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const uint32_t i = t0 + q * blockDim.x + threadIdx.x;
+            p[q] = i < n ? w.sel_pages[i] : -1;
+        }
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+            if (p[q] >= 0) {
+                w.page_cnt[p[q]] = 0;
+                w.page_first[p[q]] = 0xffffffffu;
+            }
     }
     if (threadIdx.x == 0) {
         w.readback[0] = n;
@@ -845,11 +884,12 @@ cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *r
 }
 
 cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table,
-                          int mode, double c, uint32_t nb_total, cudaStream_t s)
+                          int mode, double c, uint32_t nb_total, bool count_pages, cudaStream_t s)
 {
     const uint32_t ntiles = (nb_total + kSelTile - 1) / kSelTile;
     select_count_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, mode, c, nb_total);
-    select_scatter_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, table, mode, c, nb_total, ntiles);
+    select_scatter_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, table, mode, c, nb_total, ntiles,
+                                                        count_pages ? 1u : 0u);
     return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@
 #include <type_traits>
 
 #include "kvs_internal.h"
+#include "kvs_launch.h"
 #include "kvs_ptx.h"
 
 namespace kvs {

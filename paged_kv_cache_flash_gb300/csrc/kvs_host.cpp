@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 
 #include "kvs_internal.h"
+#include "kvs_launch.h"
 
 using namespace kvs;
 
@@ -1324,7 +1325,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         if ((rc = launch_rc(ctx,
                             launch_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
                                           static_cast<const int32_t *>(ctx->buf.block_table), args->mode, lrfu_c,
-                                          N, s),
+                                          N, !ctx->geo.kivi, s),
                             "select", 2)))
             return rc;
         if (ctx->geo.kivi && async) {

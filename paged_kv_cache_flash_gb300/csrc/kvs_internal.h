@@ -165,47 +165,6 @@ struct StepAppend {
     uint64_t seq_id;
 };
 
-// ---- launchers (each returns the cudaGetLastError() of its launch) -------
-cudaError_t launch_append_step(const Geo &g, const uint16_t *k, const uint16_t *v, uint16_t *pool,
-                               int32_t *table, kvs_record *records, uint8_t *page_clean,
-                               const StepAppend *sa, uint32_t nseq, uint32_t rows_total,
-                               uint64_t t_create, cudaStream_t s);
-cudaError_t launch_append(const Geo &g, const AppendArgs &a, cudaStream_t s);
-cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w,
-                          const uint16_t *q, const int32_t *table,
-                          uint32_t n_items, uint32_t wg, int grid, cudaStream_t s);
-cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq,
-                           uint32_t max_nb, cudaStream_t s);
-cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total,
-                        cudaStream_t s);
-cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const float *mass,
-                         double alpha, uint32_t W, double wR, double wE, double wN,
-                         double lo, double hi, uint32_t nb_total, cudaStream_t s);
-cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *rec,
-                                uint32_t nb_total, uint32_t k, int mode, double c, cudaStream_t s);
-cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table,
-                          int mode, double c, uint32_t nb_total, cudaStream_t s);
-cudaError_t launch_plan(const Work &w, uint32_t mirror, cudaStream_t s);
-cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *pages, uint32_t npages,
-                           uint16_t *pool, cudaStream_t s);
-cudaError_t launch_mirror_copy(const Geo &g, const Work &w, const uint16_t *pool, void *host_dev,
-                               uint32_t pool_blocks, int grid, cudaStream_t s);
-cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pages,
-                          uint32_t npages, uint8_t *staging, cudaStream_t s);
-cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, uint8_t *page_clean,
-                         const Patch *p, uint32_t n, cudaStream_t s);
-cudaError_t launch_kivi_compress(const Geo &g, const KiviJob *jobs, uint32_t njobs, const uint8_t *pool,
-                                 uint8_t *gpool, int32_t *table, cudaStream_t s);
-cudaError_t launch_decode_kivi(const Geo &g, const Work &w, const uint16_t *q, const int32_t *table,
-                               const uint8_t *gpool, uint32_t n_items, int grid, cudaStream_t s);
-int decode_kivi_blocks_per_sm(const Geo &g);
-cudaError_t launch_prefetch_plan(const PrefCand *cand, uint32_t n, uint32_t k, uint64_t *keys,
-                                 uint64_t *out_key, uint32_t *out_idx, cudaStream_t s);
-cudaError_t launch_copy_mass(const Geo &g, const Work &w, const float *src, float *mass,
-                             uint32_t nseq, cudaStream_t s);
-
-int decode_blocks_per_sm(const Geo &g, uint32_t wg);
-
 // Blocks per decode work item (one KV-head stream chunk) for one call: the
 // largest of 128, 64, 32, 16 that still gives each of the `workers` warps of
 // the persistent grid at least 8 items (a short tail without many partials),
@@ -230,6 +189,5 @@ inline uint32_t pick_chunk(const uint32_t *nb, uint32_t n, uint32_t L, uint32_t 
     }
     return best;
 }
-size_t decode_smem_bytes(const Geo &g, uint32_t wg);
 
 }  // namespace kvs

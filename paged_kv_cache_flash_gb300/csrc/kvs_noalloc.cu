@@ -24,6 +24,7 @@
 #include <cudaTypedefs.h>
 
 #include "kvs_internal.h"
+#include "kvs_launch.h"
 
 namespace {
 
