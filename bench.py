@@ -321,7 +321,11 @@ class Pipeline:
             self._idx[key] = self.torch.tensor(active, dtype=self.torch.int64, device=self.dev)
         return x.index_select(0, self._idx[key])
 
-    def step(self, kv_row, q, ev=None, mode_flags=None, after_decode=None):
+    def step(self, kv_row, q, ev=None, mode_flags=None, after_decode=None, phases=True):
+        """One decode step.  ev: 5 timing events (step start, after append,
+        after decode, after score, step end); with phases=False only the step
+        boundaries (and, on a demote round, the after-score event) are
+        recorded, so that nothing sits between the step's kernels."""
         K, ctx, torch = self.K, self.ctx, self.torch
         main = torch.cuda.current_stream()
         sh, side = main.cuda_stream, self.side.cuda_stream    # raw handles: no lookups per call
@@ -354,18 +358,19 @@ class Pipeline:
         ctx.append_step(ids, self._rows(kv_row[0], active), self._rows(kv_row[1], active), stream=sh)
         for i in active:
             self.ntok[i] += 1
-        if ev:
+        if ev and phases:
             ev[1].record(main)
         ctx.decode_step(ids, self._rows(q, active), out, stream=sh)
-        if ev:
+        if ev and phases:
             ev[2].record(main)
         if after_decode is not None:
             after_decode()          # host work that overlaps the rest of the step
         ctx.score_update(stream=sh)
-        if ev:
-            ev[3].record(main)
         r = None
         self.steps_done += 1
+        demoting = self.demote_every and self.steps_done % self.demote_every == 0 and not self.holes
+        if ev and (phases or demoting):
+            ev[3].record(main)
         if self.gather in ("ids", "ids-sync"):      # the THRESH list only, no page copies
             flags = K.KVS_GATHER_ASYNC if self.gather == "ids" else 0
             r = self._select(K.KVS_SELECT_THRESH, None, flags, sh, sh)
@@ -461,7 +466,8 @@ def run_kvs(args):
     K_, W_ = args.steps, args.warmup
     e2e_steps = 0 if args.no_e2e else K_
     lit_steps = 0 if (args.no_literal or args.gather not in ("mirror", "mirror-sync", "list")) else 2
-    total = W_ + K_ + e2e_steps + lit_steps
+    bd_steps = min(8, K_)
+    total = W_ + K_ + bd_steps + e2e_steps + lit_steps
     pipe = Pipeline(wl, alpha, total, dev, args.gather, args.kv_dtype, args.prefetch_budget, args.victims)
     pipe.prefill()
     kv, qs = pipe.inputs(1, W_ + K_)
@@ -497,7 +503,7 @@ def run_kvs(args):
     for i in range(K_):
         pipe.ctx.set_decode_events(dec[i][0], dec[i][1])
         pipe.last_round = 0
-        r = pipe.step(kv[W_ + i], qs[W_ + i], ev[i])
+        r = pipe.step(kv[W_ + i], qs[W_ + i], ev[i], phases=False)
         if pipe.last_round and args.gather == "demote":
             rounds.append((i, pipe.last_round))
         kv_bytes += pipe.kv_bytes_this_step()
@@ -507,6 +513,7 @@ def run_kvs(args):
     demoted = pipe.demoted_pages - demoted0
     t_stop.record()
     torch.cuda.synchronize()
+    ntok_timed = list(pipe.ntok)
     staged += pipe.flush_counts()
     wall = time.perf_counter() - wall0
     launches = pipe.ctx.kernel_launches() - launches0
@@ -532,12 +539,22 @@ def run_kvs(args):
                       "ms_per_round": round(statistics.median(r_ms), 3),
                       "link_GBps": round(sum(r_bytes) / (sum(r_ms) / 1e3) / 1e9, 2),
                       "note": "2 x page bytes per demoted page (to host and back) over the region"}
-    part = {name: statistics.median(ev[i][a].elapsed_time(ev[i][b]) for i in range(K_))
+    # ---- per-phase breakdown: a few more steps with an event between calls
+    # (kept out of the timed steps, where the calls' kernels follow each
+    # other with nothing in between)
+    kvb, qb = pipe.inputs(W_ + K_ + 1, bd_steps)
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(bd_steps)]
+    for i in range(bd_steps):
+        pipe.step(kvb[i], qb[i], evb[i])
+    pipe.flush_counts()
+    torch.cuda.synchronize()
+    del kvb, qb
+    part = {name: statistics.median(evb[i][a].elapsed_time(evb[i][b]) for i in range(bd_steps))
             for name, a, b in [("append", 0, 1), ("decode_step", 1, 2), ("score", 2, 3),
                                ("select_gather", 3, 4)]}
     dec_avg = sum(dec_ms) / len(dec_ms)
     B = wl.block_tokens
-    nb = [(n + B - 1) // B for n in pipe.ntok]
+    nb = [(n + B - 1) // B for n in ntok_timed]
     algo = kv_bytes / K_ + wl.nseq * wl.L * wl.Hq * wl.d * 2 + sum(nb) * 4
     achieved = algo / (dec_avg / 1e3) / 1e9
     peak, peak_src = read_peaks()
@@ -547,7 +564,7 @@ def run_kvs(args):
     e2e = None
     if e2e_steps:
         pipe.flush_counts()
-        kvh, qh = pipe.inputs(W_ + K_ + 1, e2e_steps)
+        kvh, qh = pipe.inputs(W_ + K_ + bd_steps + 1, e2e_steps)
         kvh = [(k.cpu().pin_memory(), v.cpu().pin_memory()) for k, v in kvh]
         qh = [q.cpu().pin_memory() for q in qh]
         # double-buffered: the inputs of step i + 1 go up on one copy stream and
@@ -616,7 +633,7 @@ def run_kvs(args):
     # ---- literal per-step gather of every P < 0.3 page (list mode) -------
     literal = None
     if lit_steps:
-        kvl, ql = pipe.inputs(W_ + K_ + e2e_steps + 1, lit_steps)
+        kvl, ql = pipe.inputs(W_ + K_ + bd_steps + e2e_steps + 1, lit_steps)
         torch.cuda.synchronize()
         l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         pages = moved = 0

@@ -41,7 +41,7 @@ def _stale() -> bool:
         return True
     t = LIB.stat().st_mtime
     deps = [CSRC / s for s in SOURCES] + [CSRC / "kvs_internal.h", CSRC / "kvs_launch.h", CSRC / "kvs_ptx.h",
-                                         ROOT / "include" / "kvs.h", Path(__file__)]
+                                         CSRC / "kvs_pdl.cuh", ROOT / "include" / "kvs.h", Path(__file__)]
     return any(p.stat().st_mtime > t for p in deps)
 
 

@@ -14,6 +14,7 @@
 
 #include "kvs_internal.h"
 #include "kvs_launch.h"
+#include "kvs_pdl.cuh"
 
 namespace kvs {
 namespace {
@@ -219,15 +220,24 @@ __global__ void score_kernel(const Geo g, const Work w, kvs_record *recs, const 
                              const ScoreArgs sa, uint32_t nb_total)
 {
     const uint32_t r = blockIdx.x * blockDim.x + threadIdx.x;
+    const DSet *ds = w.dset;
+    // the decode set was uploaded before the decode kernel: read it while the
+    // mass kernel finishes
+    DSeq sq{};
+    uint32_t b = 0;
+    uint64_t t = 0;
+    if (r < nb_total) {
+        const uint32_t si = find_sorted(ds, r);
+        sq = ds->seq[ds->sorted[si]];
+        b = r - ds->srt_off[si];
+        t = ds->t;
+    }
+    pdl_wait();
+    pdl_trigger();
     if (r >= nb_total)
         return;
-    const DSet *ds = w.dset;
-    const uint32_t si = find_sorted(ds, r);
-    const DSeq sq = ds->seq[ds->sorted[si]];
-    const uint32_t b = r - ds->srt_off[si];
     const size_t idx = static_cast<size_t>(sq.slot) * g.mb + b;
     kvs_record rec = recs[idx];
-    const uint64_t t = ds->t;
     if (rec.key.block_idx != b || rec.key.seq_id != sq.seq_id || rec.last_touch > t) {
         atomicOr(w.err, kErrBadRecord);
         return;
@@ -258,6 +268,24 @@ __global__ void score_kernel(const Geo g, const Work w, kvs_record *recs, const 
 constexpr int kSelThreads = 256;
 constexpr int kSelPerThread = 4;
 constexpr int kSelTile = kSelThreads * kSelPerThread;
+
+// Record-array index of record r of the decode set (record order), with its
+// sequence slot, block and token count (each optional).  Reads the decode set
+// only.
+__device__ __forceinline__ size_t rec_index(const Geo &g, const DSet *ds, uint32_t r, uint32_t *slot_out,
+                                            uint32_t *b_out, uint32_t *ntok_out)
+{
+    const uint32_t si = find_sorted(ds, r);
+    const DSeq &sq = ds->seq[ds->sorted[si]];
+    const uint32_t b = r - ds->srt_off[si];
+    if (slot_out)
+        *slot_out = sq.slot;
+    if (b_out)
+        *b_out = b;
+    if (ntok_out)
+        *ntok_out = sq.ntok;
+    return static_cast<size_t>(sq.slot) * g.mb + b;
+}
 
 __device__ __forceinline__ const kvs_record &rec_at(const Geo &g, const DSet *ds,
                                                     const kvs_record *recs, uint32_t r,
@@ -304,13 +332,18 @@ __global__ void __launch_bounds__(kSelThreads)
 {
     __shared__ uint32_t wsum[kSelThreads / 32];
     const DSet *ds = w.dset;
+    size_t idx[kSelPerThread];
+    for (int q = 0; q < kSelPerThread; ++q) {
+        const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
+        idx[q] = r < nb_total ? rec_index(g, ds, r, nullptr, nullptr, nullptr) : 0;
+    }
+    pdl_wait();                 // records and the threshold come from earlier kernels
+    pdl_trigger();
     uint32_t c = 0;
     for (int q = 0; q < kSelPerThread; ++q) {
         const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
-        if (r < nb_total) {
-            uint32_t slot, b;
-            c += picked(mode, rec_at(g, ds, recs, r, &slot, &b), r, w.sel_thr, lrfu_c) ? 1u : 0u;
-        }
+        if (r < nb_total)
+            c += picked(mode, recs[idx[q]], r, w.sel_thr, lrfu_c) ? 1u : 0u;
     }
     for (int x = 16; x > 0; x >>= 1)
         c += __shfl_xor_sync(0xffffffffu, c, x);
@@ -326,30 +359,43 @@ __global__ void __launch_bounds__(kSelThreads)
 }
 
 // Writes picked records in record order: key, page and record index.
+// out: optional direct outputs -- the caller's key list (ids, first ids_cap
+// entries) and, through its device mapping, a host word for the count.
 __global__ void __launch_bounds__(kSelThreads)
     select_scatter_kernel(const Geo g, const Work w, const kvs_record *recs, const int32_t *table,
-                          int mode, double lrfu_c, uint32_t nb_total, uint32_t ntiles, uint32_t count_pages)
+                          int mode, double lrfu_c, uint32_t nb_total, uint32_t ntiles, uint32_t count_pages,
+                          const SelectOut out)
 {
     __shared__ uint32_t wpre[kSelThreads / 32];
     __shared__ uint32_t base_sh;
     const DSet *ds = w.dset;
+    uint32_t slots[kSelPerThread], bs[kSelPerThread], nts[kSelPerThread];
+    size_t idx[kSelPerThread];
+    for (int q = 0; q < kSelPerThread; ++q) {
+        const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
+        idx[q] = r < nb_total ? rec_index(g, ds, r, &slots[q], &bs[q], &nts[q]) : 0;
+    }
+    pdl_wait();                 // tile counts and records come from earlier kernels
+    pdl_trigger();
     if (threadIdx.x == 0) {
         uint32_t base = 0;
         for (uint32_t q = 0; q < blockIdx.x; ++q)
             base += w.tile_cnt[q];
         base_sh = base;
-        if (blockIdx.x == ntiles - 1)
+        if (blockIdx.x == ntiles - 1) {
             *w.sel_count = base + w.tile_cnt[blockIdx.x];
+            if (out.count_host)
+                *out.count_host = base + w.tile_cnt[blockIdx.x];
+        }
     }
     bool pk[kSelPerThread];
-    uint32_t slots[kSelPerThread], bs[kSelPerThread], nts[kSelPerThread];
     kvs_key keys[kSelPerThread];
     uint32_t c = 0;
     for (int q = 0; q < kSelPerThread; ++q) {
         const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
         pk[q] = false;
         if (r < nb_total) {
-            const kvs_record &rec = rec_at(g, ds, recs, r, &slots[q], &bs[q], &nts[q]);
+            const kvs_record &rec = recs[idx[q]];
             pk[q] = picked(mode, rec, r, w.sel_thr, lrfu_c);
             keys[q] = rec.key;
         }
@@ -376,7 +422,9 @@ __global__ void __launch_bounds__(kSelThreads)
         const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
         const int32_t page = table[static_cast<size_t>(slots[q]) * g.mb + bs[q]];
         w.sel_ids[pos] = keys[q];
-        w.sel_recs[pos] = recs[static_cast<size_t>(slots[q]) * g.mb + bs[q]];
+        if (out.ids && pos < out.ids_cap)
+            out.ids[pos] = keys[q];
+        w.sel_recs[pos] = recs[idx[q]];
         w.sel_pages[pos] = page;
         w.sel_recidx[pos] = r;
         w.sel_full[pos] = (bs[q] + 1) * kBlockTokens <= nts[q] ? 1 : 0;
@@ -400,6 +448,8 @@ __global__ void __launch_bounds__(1024)
     __shared__ uint32_t pre_r;
     __shared__ uint32_t remaining;
     const DSet *ds = w.dset;
+    pdl_wait();                 // records come from the scoring kernel
+    pdl_trigger();
     if (threadIdx.x == 0) {
         pre_p = 0;
         pre_r = 0;
@@ -650,9 +700,11 @@ __global__ void __launch_bounds__(1024)
 //  - per selected key: its slot (plan position, or page id in mirror mode),
 //    -1 when its page is not eligible.
 // page_cnt / page_first are restored to 0 / ~0 before returning.
-__global__ void __launch_bounds__(1024) plan_kernel(const Work w, uint32_t mirror)
+__global__ void __launch_bounds__(1024) plan_kernel(const Work w, uint32_t mirror, const SelectOut out)
 {
     __shared__ uint32_t wsum[33];
+    pdl_wait();                 // the list and page counts come from the selection
+    pdl_trigger();
     const uint32_t n = *w.sel_count;
     // leaders in list order: 4 consecutive entries per thread per tile; one
     // block scan of the packed counts (leaders low 16 bits, stale pages high:
@@ -720,8 +772,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Work w, uint32_t mirro
 #pragma unroll
         for (int q = 0; q < R; ++q) {
             const uint32_t i = t0 + q * blockDim.x + threadIdx.x;
-            if (i < n)
-                w.plan_slot[i] = (p[q] >= 0 && cnt[q] == ref[q]) ? pos[q] : -1;
+            if (i < n) {
+                const int32_t v = (p[q] >= 0 && cnt[q] == ref[q]) ? pos[q] : -1;
+                w.plan_slot[i] = v;
+                if (out.slots && i < out.ids_cap)
+                    out.slots[i] = v;
+            }
         }
     }
     __syncthreads();
@@ -745,6 +801,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Work w, uint32_t mirro
         w.readback[1] = npages;
         w.readback[2] = ncopy;
         w.readback[3] = 0;
+        if (out.count_host) {
+            out.count_host[0] = n;
+            out.count_host[1] = npages;
+            out.count_host[2] = ncopy;
+            out.count_host[3] = 0;
+        }
     }
 }
 
@@ -771,6 +833,8 @@ __global__ void __launch_bounds__(256)
     mirror_copy_kernel(const uint4 *pool, const uint32_t *plan, uint4 *host, uint64_t page_vec,
                        uint32_t pool_blocks, uint32_t *err, uint32_t *err_info)
 {
+    pdl_wait();                 // the copy list comes from the plan kernel
+    pdl_trigger();
     const uint32_t n = plan[2];
     const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
     const uint64_t i0 = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -872,25 +936,26 @@ cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const flo
                          double hi, uint32_t nb_total, cudaStream_t s)
 {
     ScoreArgs sa{alpha, wR, wE, wN, lo, hi, W};
-    score_kernel<<<(nb_total + 127) / 128, 128, 0, s>>>(g, w, rec, mass, sa, nb_total);
-    return cudaGetLastError();
+    return launch_pdl(score_kernel, dim3((nb_total + 127) / 128), dim3(128), 0, s, g, w, rec, mass, sa, nb_total);
 }
 
 cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *rec,
                                 uint32_t nb_total, uint32_t k, int mode, double c, cudaStream_t s)
 {
-    radix_select_kernel<<<1, 1024, 0, s>>>(g, w, rec, nb_total, k, mode, c);
-    return cudaGetLastError();
+    return launch_pdl(radix_select_kernel, dim3(1), dim3(1024), 0, s, g, w, rec, nb_total, k, mode, c);
 }
 
 cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table,
-                          int mode, double c, uint32_t nb_total, bool count_pages, cudaStream_t s)
+                          int mode, double c, uint32_t nb_total, bool count_pages, const SelectOut &out,
+                          cudaStream_t s)
 {
     const uint32_t ntiles = (nb_total + kSelTile - 1) / kSelTile;
-    select_count_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, mode, c, nb_total);
-    select_scatter_kernel<<<ntiles, kSelThreads, 0, s>>>(g, w, rec, table, mode, c, nb_total, ntiles,
-                                                        count_pages ? 1u : 0u);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(select_count_kernel, dim3(ntiles), dim3(kSelThreads), 0, s, g, w, rec, mode, c,
+                               nb_total);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(select_scatter_kernel, dim3(ntiles), dim3(kSelThreads), 0, s, g, w, rec, table, mode, c,
+                      nb_total, ntiles, count_pages ? 1u : 0u, out);
 }
 
 cudaError_t launch_prefetch_plan(const PrefCand *cand, uint32_t n, uint32_t k, uint64_t *keys,
@@ -919,10 +984,9 @@ cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pag
 cudaError_t launch_mirror_copy(const Geo &g, const Work &w, const uint16_t *pool, void *host_dev,
                                uint32_t pool_blocks, int grid, cudaStream_t s)
 {
-    mirror_copy_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4 *>(pool), w.readback,
-                                            reinterpret_cast<uint4 *>(host_dev), g.page_bytes / 16,
-                                            pool_blocks, w.err, w.err_info);
-    return cudaGetLastError();
+    return launch_pdl(mirror_copy_kernel, dim3(grid), dim3(256), 0, s, reinterpret_cast<const uint4 *>(pool),
+                      static_cast<const uint32_t *>(w.readback), reinterpret_cast<uint4 *>(host_dev),
+                      static_cast<uint64_t>(g.page_bytes / 16), pool_blocks, w.err, w.err_info);
 }
 
 cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *pages, uint32_t npages,
@@ -942,10 +1006,9 @@ cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, uint8_t 
     return cudaGetLastError();
 }
 
-cudaError_t launch_plan(const Work &w, uint32_t mirror, cudaStream_t s)
+cudaError_t launch_plan(const Work &w, uint32_t mirror, const SelectOut &out, cudaStream_t s)
 {
-    plan_kernel<<<1, 1024, 0, s>>>(w, mirror);
-    return cudaGetLastError();
+    return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, w, mirror, out);
 }
 
 cudaError_t launch_copy_mass(const Geo &g, const Work &w, const float *src, float *mass,

@@ -7,15 +7,20 @@
 //
 //   combine_kernel -- per (sequence, layer, KV head): each CTA recomputes the
 //                     heads' log2-sum-exp LSE_h from the chunk partials; CTA
-//                     y = 0 merges the output, CTAs y >= 1 turn the per-block
-//                     log2-sum-exps of block range y - 1 into the stream's
-//                     block masses  sum_h 2^(lse_blk(h, b) - LSE_h).
+//                     y = 0 merges the output, and the CTAs of the block
+//                     ranges turn the per-block log2-sum-exps of their range
+//                     into the stream's block masses
+//                     sum_h 2^(lse_blk(h, b) - LSE_h).  Streams of many
+//                     chunks give the merge a CTA of its own; with few
+//                     chunks CTA 0 also takes the first block range.
 //   mass_kernel    -- M(b) = 1/(L*Hq) * sum over the L*Hkv streams, in a fixed
 //                     order (deterministic).
+// Both are launched as programmatic dependents (kvs_pdl.cuh).
 #include <type_traits>
 
 #include "kvs_internal.h"
 #include "kvs_launch.h"
+#include "kvs_pdl.cuh"
 #include "kvs_ptx.h"
 
 namespace kvs {
@@ -25,8 +30,10 @@ using namespace ptx;
 
 constexpr uint32_t kMassRange = 1024;   // blocks per combine CTA (stream-mass part)
 
+// split: 1 -> CTA y = 0 merges only and CTA y >= 1 takes block range y - 1;
+// 0 -> CTA y takes block range y, and CTA 0 also merges.
 template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w, float *out)
+__global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w, float *out, uint32_t split)
 {
     __shared__ float lse_sh[kMaxGroup];
     const DSet *ds = w.dset;
@@ -34,14 +41,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w,
     const uint32_t ci = blockIdx.x / (g.L * g.Hkv);
     const uint32_t rest = blockIdx.x % (g.L * g.Hkv);
     const uint32_t l = rest / g.Hkv, kvh = rest % g.Hkv;
+    const DSeq sq = ds->seq[ci];        // the decode set: uploaded before the decode kernel
+    pdl_wait();
+    pdl_trigger();
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
         w.counter[0] = 0;          // ready for the next decode launches
         w.counter[1] = 0;
     }
-    const DSeq sq = ds->seq[ci];
-    // y == 0: the output merge; y >= 1: the block masses of range y - 1
     const bool merge = blockIdx.y == 0;
-    const uint32_t r0 = merge ? 0u : (blockIdx.y - 1) * kMassRange;
+    const bool has_range = !split || blockIdx.y > 0;
+    const uint32_t r0 = (blockIdx.y - split) * kMassRange;     // unused without a range
     if (!merge && r0 >= sq.nb)
         return;                    // uniform over the CTA
     const uint32_t pb = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk;
@@ -91,7 +100,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w,
         if (lane == 0)
             lse_sh[h] = mmax + fast_log2(lsum);
     }
-    if (merge)
+    if (!has_range || r0 >= sq.nb)
         return;                    // uniform over the CTA
     __syncthreads();
     const uint32_t nbt = ds->nb_total;
@@ -106,52 +115,63 @@ __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w,
     }
 }
 
-// M(b) = 1/(L*Hq) * sum over the L*Hkv streams of stream_mass(b): 32
-// consecutive blocks per CTA x 8 interleaved partial sums, added in a fixed
-// order (deterministic).
-__global__ void __launch_bounds__(256) mass_kernel(const Geo g, const Work w, float *mass,
-                                                   uint32_t nb_total)
+// M(b) = 1/(L*Hq) * sum over the L*Hkv streams of stream_mass(b).  A CTA of
+// 1024 threads takes 16 consecutive blocks; thread (i, j) adds the streams
+// j, j + 64, ... of block i, and the 64 partial sums of a block are added by
+// a fixed tree (deterministic).
+constexpr uint32_t kMassBlocks = 16, kMassGroups = 64;
+
+__global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, float *mass,
+                                                    uint32_t nb_total)
 {
-    __shared__ float part[8][33];
+    __shared__ float part[kMassGroups][kMassBlocks + 1];
     const DSet *ds = w.dset;
-    const uint32_t i = threadIdx.x & 31, j = threadIdx.x >> 5;
-    const uint32_t r = blockIdx.x * 32 + i;
+    const uint32_t i = threadIdx.x % kMassBlocks, j = threadIdx.x / kMassBlocks;
+    const uint32_t r = blockIdx.x * kMassBlocks + i;
+    uint32_t slot = 0, b = 0;
+    if (r < nb_total && j == 0) {       // the decode set: uploaded before the decode kernel
+        const uint32_t ci = find_seq(&ds->seq[0].blk_off, sizeof(DSeq) / 4, ds->nseq, r);
+        slot = ds->seq[ci].slot;
+        b = r - ds->seq[ci].blk_off;
+    }
+    pdl_wait();
+    pdl_trigger();
     const uint32_t LS = g.L * g.Hkv;
     float acc = 0.f;
     if (r < nb_total)
-        for (uint32_t s = j; s < LS; s += 8)
+#pragma unroll 4
+        for (uint32_t s = j; s < LS; s += kMassGroups)
             acc += w.stream_mass[static_cast<size_t>(s) * nb_total + r];
     part[j][i] = acc;
     __syncthreads();
-    if (j == 0 && r < nb_total) {
-        float t = part[0][i];
 #pragma unroll
-        for (int q = 1; q < 8; ++q)
-            t += part[q][i];
-        const uint32_t ci = find_seq(&ds->seq[0].blk_off, sizeof(DSeq) / 4, ds->nseq, r);
-        const DSeq sq = ds->seq[ci];
-        mass[static_cast<size_t>(sq.slot) * g.mb + (r - sq.blk_off)] =
-            t / static_cast<float>(g.L * g.Hq);
+    for (uint32_t half = kMassGroups / 2; half > 0; half >>= 1) {
+        if (j < half)
+            part[j][i] += part[j + half][i];
+        __syncthreads();
     }
+    if (j == 0 && r < nb_total)
+        mass[static_cast<size_t>(slot) * g.mb + b] = part[0][i] / static_cast<float>(g.L * g.Hq);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq, uint32_t max_nb,
-                           cudaStream_t s)
+                           uint32_t max_nchunk, cudaStream_t s)
 {
-    const dim3 grid(nseq * g.L * g.Hkv, 1 + (max_nb + kMassRange - 1) / kMassRange);
+    // a merge of many chunks gets a CTA of its own; a short one shares CTA 0
+    // with the first block range
+    const uint32_t split = max_nchunk > 16 ? 1u : 0u;
+    const dim3 grid(nseq * g.L * g.Hkv, split + (max_nb + kMassRange - 1) / kMassRange);
     if (g.d == 128)
-        combine_kernel<128><<<grid, 32 * kMaxGroup, 0, s>>>(g, w, out);
-    else
-        combine_kernel<64><<<grid, 32 * kMaxGroup, 0, s>>>(g, w, out);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<128>, grid, dim3(32 * kMaxGroup), 0, s, g, w, out, split);
+    return launch_pdl(combine_kernel<64>, grid, dim3(32 * kMaxGroup), 0, s, g, w, out, split);
 }
 
 cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total, cudaStream_t s)
 {
-    mass_kernel<<<(nb_total + 31) / 32, 256, 0, s>>>(g, w, mass, nb_total);
-    return cudaGetLastError();
+    return launch_pdl(mass_kernel, dim3((nb_total + kMassBlocks - 1) / kMassBlocks), dim3(1024), 0, s, g, w,
+                      mass, nb_total);
 }
 
 }  // namespace kvs

@@ -104,6 +104,7 @@ struct kvs_ctx {
     uint32_t ring_next = 0;
     uint32_t *pinned_small = nullptr;               // readbacks
     uint32_t *async_hdr = nullptr;                  // counts of the latest ASYNC select
+    uint32_t *async_hdr_dev = nullptr;              // ... its device mapping (kernels write it)
     cudaEvent_t ev_async{};                         // ... on the host after this event
     int async_kind = 0;                             // 0 none yet, 1 mirror, 2 ids only
 
@@ -809,7 +810,8 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
                      cudaHostAllocDefault));
     CU(cudaEventCreateWithFlags(&ctx->ev_wait, cudaEventDisableTiming));
     CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->pinned_small), kReadbackBytes, cudaHostAllocDefault));
-    CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->async_hdr), 64, cudaHostAllocDefault));
+    CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->async_hdr), 64, cudaHostAllocMapped));
+    CU(cudaHostGetDevicePointer(reinterpret_cast<void **>(&ctx->async_hdr_dev), ctx->async_hdr, 0));
     CU(cudaEventCreateWithFlags(&ctx->ev_async, cudaEventDisableTiming));
     for (auto &e : ctx->ring_ev)
         CU(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
@@ -1210,10 +1212,13 @@ int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
         return rc;
     if (ctx->ev_dec_stop)
         CU(cudaEventRecord(ctx->ev_dec_stop, s));
-    uint32_t max_nb = 0;
-    for (uint32_t i = 0; i < ds->nseq; ++i)
+    uint32_t max_nb = 0, max_nchunk = 0;
+    for (uint32_t i = 0; i < ds->nseq; ++i) {
         max_nb = std::max(max_nb, ds->seq[i].nb);
-    if ((rc = launch_rc(ctx, launch_combine(ctx->geo, ctx->work, out_dev, ds->nseq, max_nb, s), "combine")))
+        max_nchunk = std::max(max_nchunk, ds->seq[i].nchunk);
+    }
+    if ((rc = launch_rc(ctx, launch_combine(ctx->geo, ctx->work, out_dev, ds->nseq, max_nb, max_nchunk, s),
+                        "combine")))
         return rc;
     return launch_rc(ctx, launch_mass(ctx->geo, ctx->work, static_cast<float *>(ctx->buf.mass),
                                       ds->nb_total, s),
@@ -1322,19 +1327,26 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
     uint32_t nsel = 0, npages = 0, ncopy = 0;
     std::vector<uint32_t> copy_list;
     if (run) {
+        // asynchronous calls: the kernels write the caller's lists and the
+        // counts (through the pinned header's device mapping) themselves, so
+        // no copy follows them
+        const uint32_t cap = std::min(N, args->ids_capacity);
+        SelectOut sel_out{};
+        if (async && args->ids_dev) {
+            sel_out.ids = args->ids_dev;
+            sel_out.ids_cap = cap;
+        }
+        if (async && ctx->geo.kivi)
+            sel_out.count_host = ctx->async_hdr_dev;
         if ((rc = launch_rc(ctx,
                             launch_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
                                           static_cast<const int32_t *>(ctx->buf.block_table), args->mode, lrfu_c,
-                                          N, !ctx->geo.kivi, s),
+                                          N, !ctx->geo.kivi, sel_out, s),
                             "select", 2)))
             return rc;
         if (ctx->geo.kivi && async) {
-            CU(cudaMemcpyAsync(ctx->async_hdr, w.sel_count, 4, cudaMemcpyDeviceToHost, s));
             CU(cudaEventRecord(ctx->ev_async, s));
             ctx->async_kind = 2;
-            const uint32_t n = std::min(N, args->ids_capacity);
-            if (n && args->ids_dev)
-                CU(cudaMemcpyAsync(args->ids_dev, w.sel_ids, n * sizeof(kvs_key), cudaMemcpyDeviceToDevice, s));
             return KVS_OK;
         }
         if (ctx->geo.kivi) {
@@ -1348,26 +1360,27 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
                                    cudaMemcpyDeviceToDevice, s));
             return KVS_OK;
         }
-        if ((rc = launch_rc(ctx, launch_plan(w, mirror ? 1u : 0u, s), "plan")))
+        SelectOut plan_out{};
+        if (async) {
+            if (args->slot_dev) {
+                plan_out.slots = args->slot_dev;
+                plan_out.ids_cap = cap;
+            }
+            plan_out.count_host = ctx->async_hdr_dev;
+        }
+        if ((rc = launch_rc(ctx, launch_plan(w, mirror ? 1u : 0u, plan_out, s), "plan")))
             return rc;
         if (async) {
             // the stale pages go to the host mirror by a device kernel in
-            // stream order (writers after it need no wait); the counts follow
-            // into pinned memory, read by kvs_gather_counts
+            // stream order (writers after it need no wait); the plan kernel
+            // wrote the counts into pinned memory, read by kvs_gather_counts
             if ((rc = launch_rc(ctx,
                                 launch_mirror_copy(ctx->geo, w, static_cast<const uint16_t *>(ctx->buf.pool),
                                                    host_dev, ctx->cfg.pool_blocks, 2 * ctx->sm_count, s),
                                 "mirror copy")))
                 return rc;
-            CU(cudaMemcpyAsync(ctx->async_hdr, w.readback, 16, cudaMemcpyDeviceToHost, s));
             CU(cudaEventRecord(ctx->ev_async, s));
             ctx->async_kind = 1;
-            const uint32_t n = std::min(N, args->ids_capacity);
-            if (n && args->ids_dev)
-                CU(cudaMemcpyAsync(args->ids_dev, w.sel_ids, n * sizeof(kvs_key), cudaMemcpyDeviceToDevice, s));
-            if (n && args->slot_dev)
-                CU(cudaMemcpyAsync(args->slot_dev, w.plan_slot, n * sizeof(int32_t), cudaMemcpyDeviceToDevice,
-                                   s));
             return KVS_OK;
         }
         // one readback: counts and the head of the copy list

@@ -98,6 +98,17 @@ struct Work {             // carved out of the caller's workspace buffer
     uint8_t *ring;        // device side of the upload ring
 };
 
+// Optional direct outputs of a selection (null / 0 when unused): the caller's
+// key and slot lists (their first ids_cap entries), and a host buffer, through
+// its device mapping, for the counts (select_scatter_kernel writes one word,
+// the selected count; plan_kernel four: selected, pages, pages copied, 0).
+struct SelectOut {
+    kvs_key *ids;
+    int32_t *slots;
+    uint32_t ids_cap;
+    uint32_t *count_host;
+};
+
 struct Layout {           // byte offsets inside the workspace
     size_t err, counter, sel_count, sel_thr, dset, part_ml, part_o, lse_blk,
         stream_mass, tile_cnt, sel_ids, sel_pages, sel_recidx, sel_recs, sel_full, dev_refcnt,

@@ -16,7 +16,7 @@ cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w,
                           const uint16_t *q, const int32_t *table,
                           uint32_t n_items, uint32_t wg, int grid, cudaStream_t s);
 cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq,
-                           uint32_t max_nb, cudaStream_t s);
+                           uint32_t max_nb, uint32_t max_nchunk, cudaStream_t s);
 cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total,
                         cudaStream_t s);
 cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const float *mass,
@@ -25,8 +25,9 @@ cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const flo
 cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *rec,
                                 uint32_t nb_total, uint32_t k, int mode, double c, cudaStream_t s);
 cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table,
-                          int mode, double c, uint32_t nb_total, bool count_pages, cudaStream_t s);
-cudaError_t launch_plan(const Work &w, uint32_t mirror, cudaStream_t s);
+                          int mode, double c, uint32_t nb_total, bool count_pages, const SelectOut &out,
+                          cudaStream_t s);
+cudaError_t launch_plan(const Work &w, uint32_t mirror, const SelectOut &out, cudaStream_t s);
 cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *pages, uint32_t npages,
                            uint16_t *pool, cudaStream_t s);
 cudaError_t launch_mirror_copy(const Geo &g, const Work &w, const uint16_t *pool, void *host_dev,

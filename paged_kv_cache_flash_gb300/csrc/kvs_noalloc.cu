@@ -195,7 +195,7 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
                                                          static_cast<uint32_t>(grid_per_sm)));
     NA_CHECK(launch_decode(g, tmap, w, static_cast<const uint16_t *>(q), block_table, ds.n_items, wg,
                            grid, s));
-    NA_CHECK(launch_combine(g, w, out, 1, nb, s));
+    NA_CHECK(launch_combine(g, w, out, 1, nb, nchunk, s));
     NA_CHECK(launch_mass(g, w, mass, nb, s));
 #undef NA_CHECK
     return KVS_OK;
