@@ -118,11 +118,14 @@ __global__ void append_kernel(const Geo g, const AppendArgs a, uint64_t rows_tot
 // row, 16-byte vector).  Row 0 of a sequence's rows holds the token; rows of
 // later slots (a freshly opened block) are zero-filled.  The first threads
 // past the row range write the records and table entries of fresh blocks.
+// sa: the per-sequence entries in device memory, or null when they come in
+// the parameters (inl, at most kStepInline of them).
 __global__ void append_step_kernel(const Geo g, const uint16_t *k, const uint16_t *v, uint16_t *pool,
                                    int32_t *table, kvs_record *records, uint8_t *page_clean,
-                                   const StepAppend *sa, uint32_t nseq, uint32_t rows_total,
-                                   uint32_t vec_per_row, uint64_t t_create)
+                                   const StepAppend *sa_dev, const __grid_constant__ StepAppendInline inl,
+                                   uint32_t nseq, uint32_t rows_total, uint32_t vec_per_row, uint64_t t_create)
 {
+    const StepAppend *sa = sa_dev ? sa_dev : inl.e;
     const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const uint64_t nvec = static_cast<uint64_t>(rows_total) * vec_per_row;
     if (tid < nvec) {
@@ -378,11 +381,12 @@ __global__ void __launch_bounds__(kSelThreads)
     pdl_wait();                 // tile counts and records come from earlier kernels
     pdl_trigger();
     if (threadIdx.x == 0) {
+        // one tile: no count kernel ran; the count is this CTA's own total
         uint32_t base = 0;
         for (uint32_t q = 0; q < blockIdx.x; ++q)
             base += w.tile_cnt[q];
         base_sh = base;
-        if (blockIdx.x == ntiles - 1) {
+        if (ntiles > 1 && blockIdx.x == ntiles - 1) {
             *w.sel_count = base + w.tile_cnt[blockIdx.x];
             if (out.count_host)
                 *out.count_host = base + w.tile_cnt[blockIdx.x];
@@ -415,6 +419,14 @@ __global__ void __launch_bounds__(kSelThreads)
     uint32_t wbase = 0;
     for (uint32_t q = 0; q < wid; ++q)
         wbase += wpre[q];
+    if (ntiles == 1 && threadIdx.x == 0) {
+        uint32_t total = 0;
+        for (uint32_t q = 0; q < kSelThreads / 32; ++q)
+            total += wpre[q];
+        *w.sel_count = total;
+        if (out.count_host)
+            *out.count_host = total;
+    }
     uint32_t pos = base_sh + wbase + inc - c;
     for (int q = 0; q < kSelPerThread; ++q) {
         if (!pk[q])
@@ -920,14 +932,21 @@ cudaError_t launch_append(const Geo &g, const AppendArgs &a, cudaStream_t s)
 
 cudaError_t launch_append_step(const Geo &g, const uint16_t *k, const uint16_t *v, uint16_t *pool,
                                int32_t *table, kvs_record *records, uint8_t *page_clean,
-                               const StepAppend *sa, uint32_t nseq, uint32_t rows_total,
-                               uint64_t t_create, cudaStream_t s)
+                               const StepAppend *sa_dev, const StepAppend *sa_host, uint32_t nseq,
+                               uint32_t rows_total, uint64_t t_create, cudaStream_t s)
 {
     const uint32_t vec_per_row = g.d * (g.fp8 ? 1 : 2) / 16;   // 16-byte page vectors per row
     const uint64_t threads = static_cast<uint64_t>(rows_total) * vec_per_row + nseq;
     const uint32_t bs = 256;
+    StepAppendInline inl{};
+    if (!sa_dev) {
+        if (nseq > kStepInline)
+            return cudaErrorInvalidValue;
+        for (uint32_t i = 0; i < nseq; ++i)
+            inl.e[i] = sa_host[i];
+    }
     append_step_kernel<<<static_cast<uint32_t>((threads + bs - 1) / bs), bs, 0, s>>>(
-        g, k, v, pool, table, records, page_clean, sa, nseq, rows_total, vec_per_row, t_create);
+        g, k, v, pool, table, records, page_clean, sa_dev, inl, nseq, rows_total, vec_per_row, t_create);
     return cudaGetLastError();
 }
 
@@ -950,12 +969,19 @@ cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, co
                           cudaStream_t s)
 {
     const uint32_t ntiles = (nb_total + kSelTile - 1) / kSelTile;
-    cudaError_t e = launch_pdl(select_count_kernel, dim3(ntiles), dim3(kSelThreads), 0, s, g, w, rec, mode, c,
-                               nb_total);
-    if (e != cudaSuccess)
-        return e;
+    if (ntiles > 1) {           // one tile counts itself in the scatter kernel
+        cudaError_t e = launch_pdl(select_count_kernel, dim3(ntiles), dim3(kSelThreads), 0, s, g, w, rec, mode,
+                                   c, nb_total);
+        if (e != cudaSuccess)
+            return e;
+    }
     return launch_pdl(select_scatter_kernel, dim3(ntiles), dim3(kSelThreads), 0, s, g, w, rec, table, mode, c,
                       nb_total, ntiles, count_pages ? 1u : 0u, out);
+}
+
+uint32_t select_launches(uint32_t nb_total)
+{
+    return nb_total > static_cast<uint32_t>(kSelTile) ? 2u : 1u;
 }
 
 cudaError_t launch_prefetch_plan(const PrefCand *cand, uint32_t n, uint32_t k, uint64_t *keys,

@@ -1127,15 +1127,20 @@ int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
         for (auto it = taken.rbegin(); it != taken.rend(); ++it)
             ctx->free_pages.push_front(*it);
     };
-    RingSlot r;
-    if ((rc = ring_acquire(ctx, nseq * sizeof(StepAppend), &r))) {
-        undo();
-        return rc;
-    }
-    std::memcpy(r.host, sa.data(), nseq * sizeof(StepAppend));
-    if ((rc = ring_push(ctx, r, nseq * sizeof(StepAppend), S(stream)))) {
-        undo();
-        return rc;
+    // a few sequences: the entries go in the kernel's parameters; more go
+    // through the upload ring
+    const bool inline_args = nseq <= kStepInline;
+    RingSlot r{};
+    if (!inline_args) {
+        if ((rc = ring_acquire(ctx, nseq * sizeof(StepAppend), &r))) {
+            undo();
+            return rc;
+        }
+        std::memcpy(r.host, sa.data(), nseq * sizeof(StepAppend));
+        if ((rc = ring_push(ctx, r, nseq * sizeof(StepAppend), S(stream)))) {
+            undo();
+            return rc;
+        }
     }
     if ((rc = launch_rc(ctx,
                         launch_append_step(g, static_cast<const uint16_t *>(k_dev),
@@ -1143,13 +1148,13 @@ int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
                                            static_cast<uint16_t *>(ctx->buf.pool),
                                            static_cast<int32_t *>(ctx->buf.block_table),
                                            static_cast<kvs_record *>(ctx->buf.records), ctx->work.page_clean,
-                                           reinterpret_cast<const StepAppend *>(r.dev), nseq, rows, ctx->t,
-                                           S(stream)),
+                                           inline_args ? nullptr : reinterpret_cast<const StepAppend *>(r.dev),
+                                           sa.data(), nseq, rows, ctx->t, S(stream)),
                         "append_step"))) {
         undo();
         return rc;
     }
-    if ((rc = ring_release(ctx, r, S(stream))))
+    if (!inline_args && (rc = ring_release(ctx, r, S(stream))))
         return rc;
     for (uint32_t i = 0; i < nseq; ++i) {
         if (sa[i].fresh) {
@@ -1342,7 +1347,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
                             launch_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
                                           static_cast<const int32_t *>(ctx->buf.block_table), args->mode, lrfu_c,
                                           N, !ctx->geo.kivi, sel_out, s),
-                            "select", 2)))
+                            "select", select_launches(N))))
             return rc;
         if (ctx->geo.kivi && async) {
             CU(cudaEventRecord(ctx->ev_async, s));

@@ -176,6 +176,13 @@ struct StepAppend {
     uint64_t seq_id;
 };
 
+// A step append of at most kStepInline sequences travels in the kernel's
+// parameters (no upload copy ahead of the kernel).
+constexpr uint32_t kStepInline = 16;
+struct StepAppendInline {
+    StepAppend e[kStepInline];
+};
+
 // Blocks per decode work item (one KV-head stream chunk) for one call: the
 // largest of 128, 64, 32, 16 that still gives each of the `workers` warps of
 // the persistent grid at least 8 items (a short tail without many partials),

@@ -7,10 +7,12 @@
 namespace kvs {
 
 // ---- launchers (each returns the cudaGetLastError() of its launch) -------
+// sa_dev: the entries in device memory; null -> taken from sa_host into the
+// kernel's parameters (nseq <= kStepInline)
 cudaError_t launch_append_step(const Geo &g, const uint16_t *k, const uint16_t *v, uint16_t *pool,
                                int32_t *table, kvs_record *records, uint8_t *page_clean,
-                               const StepAppend *sa, uint32_t nseq, uint32_t rows_total,
-                               uint64_t t_create, cudaStream_t s);
+                               const StepAppend *sa_dev, const StepAppend *sa_host, uint32_t nseq,
+                               uint32_t rows_total, uint64_t t_create, cudaStream_t s);
 cudaError_t launch_append(const Geo &g, const AppendArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w,
                           const uint16_t *q, const int32_t *table,
@@ -27,6 +29,7 @@ cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *r
 cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table,
                           int mode, double c, uint32_t nb_total, bool count_pages, const SelectOut &out,
                           cudaStream_t s);
+uint32_t select_launches(uint32_t nb_total);   // kernels launch_select issues
 cudaError_t launch_plan(const Work &w, uint32_t mirror, const SelectOut &out, cudaStream_t s);
 cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *pages, uint32_t npages,
                            uint16_t *pool, cudaStream_t s);
