@@ -8,6 +8,7 @@
 // across eviction); "LLM KV cache offload" (block tables, pinned-host
 // staging); "RETRACTIONS" s.3 (exact victim selection, audited by brute force).
 #include <algorithm>
+#include <cstring>
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -190,7 +191,7 @@ __device__ __forceinline__ uint32_t find_sorted(const DSet *ds, uint32_t r)
     uint32_t lo = 0, hi = ds->nseq;
     while (hi - lo > 1) {
         const uint32_t mid = (lo + hi) >> 1;
-        if (ds->srt_off[mid] <= r)
+        if (ds->seq[mid].srt_off <= r)
             lo = mid;
         else
             hi = mid;
@@ -231,8 +232,8 @@ __global__ void score_kernel(const Geo g, const Work w, kvs_record *recs, const 
     uint64_t t = 0;
     if (r < nb_total) {
         const uint32_t si = find_sorted(ds, r);
-        sq = ds->seq[ds->sorted[si]];
-        b = r - ds->srt_off[si];
+        sq = ds->seq[ds->seq[si].srt_ci];
+        b = r - ds->seq[si].srt_off;
         t = ds->t;
     }
     pdl_wait();
@@ -279,8 +280,8 @@ __device__ __forceinline__ size_t rec_index(const Geo &g, const DSet *ds, uint32
                                             uint32_t *b_out, uint32_t *ntok_out)
 {
     const uint32_t si = find_sorted(ds, r);
-    const DSeq &sq = ds->seq[ds->sorted[si]];
-    const uint32_t b = r - ds->srt_off[si];
+    const DSeq &sq = ds->seq[ds->seq[si].srt_ci];
+    const uint32_t b = r - ds->seq[si].srt_off;
     if (slot_out)
         *slot_out = sq.slot;
     if (b_out)
@@ -296,8 +297,8 @@ __device__ __forceinline__ const kvs_record &rec_at(const Geo &g, const DSet *ds
                                                     uint32_t *ntok_out = nullptr)
 {
     const uint32_t si = find_sorted(ds, r);
-    const DSeq &sq = ds->seq[ds->sorted[si]];
-    const uint32_t b = r - ds->srt_off[si];
+    const DSeq &sq = ds->seq[ds->seq[si].srt_ci];
+    const uint32_t b = r - ds->seq[si].srt_off;
     *slot_out = sq.slot;
     *b_out = b;
     if (ntok_out)
@@ -392,17 +393,23 @@ __global__ void __launch_bounds__(kSelThreads)
                 *out.count_host = base + w.tile_cnt[blockIdx.x];
         }
     }
+    // records and their table entries (same [slot][block] index) in one round
     bool pk[kSelPerThread];
-    kvs_key keys[kSelPerThread];
-    uint32_t c = 0;
+    kvs_record rv[kSelPerThread];
+    int32_t pages[kSelPerThread];
+#pragma unroll
     for (int q = 0; q < kSelPerThread; ++q) {
         const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
-        pk[q] = false;
         if (r < nb_total) {
-            const kvs_record &rec = recs[idx[q]];
-            pk[q] = picked(mode, rec, r, w.sel_thr, lrfu_c);
-            keys[q] = rec.key;
+            rv[q] = recs[idx[q]];
+            pages[q] = table[idx[q]];
         }
+    }
+    uint32_t c = 0;
+#pragma unroll
+    for (int q = 0; q < kSelPerThread; ++q) {
+        const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
+        pk[q] = r < nb_total && picked(mode, rv[q], r, w.sel_thr, lrfu_c);
         c += pk[q] ? 1u : 0u;
     }
     // exclusive scan of c over the block
@@ -428,15 +435,16 @@ __global__ void __launch_bounds__(kSelThreads)
             *out.count_host = total;
     }
     uint32_t pos = base_sh + wbase + inc - c;
+#pragma unroll
     for (int q = 0; q < kSelPerThread; ++q) {
         if (!pk[q])
             continue;
         const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
-        const int32_t page = table[static_cast<size_t>(slots[q]) * g.mb + bs[q]];
-        w.sel_ids[pos] = keys[q];
+        const int32_t page = pages[q];
+        w.sel_ids[pos] = rv[q].key;
         if (out.ids && pos < out.ids_cap)
-            out.ids[pos] = keys[q];
-        w.sel_recs[pos] = recs[idx[q]];
+            out.ids[pos] = rv[q].key;
+        w.sel_recs[pos] = rv[q];
         w.sel_pages[pos] = page;
         w.sel_recidx[pos] = r;
         w.sel_full[pos] = (bs[q] + 1) * kBlockTokens <= nts[q] ? 1 : 0;
@@ -718,6 +726,72 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Work w, uint32_t mirro
     pdl_wait();                 // the list and page counts come from the selection
     pdl_trigger();
     const uint32_t n = *w.sel_count;
+    if (n <= 4 * blockDim.x) {
+        // one pass with every entry's loads in registers: 4 consecutive
+        // entries per thread
+        const uint32_t i0 = 4 * threadIdx.x;
+        int32_t p[4];
+        uint32_t cnt[4], ref[4], lead[4], dirty[4], nl = 0, nd = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            p[q] = i0 + q < n ? w.sel_pages[i0 + q] : -1;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            cnt[q] = ref[q] = lead[q] = dirty[q] = 0;
+            if (p[q] >= 0) {
+                cnt[q] = w.page_cnt[p[q]];
+                ref[q] = w.dev_refcnt[p[q]];
+                lead[q] = (cnt[q] == ref[q] && w.page_first[p[q]] == i0 + q) ? 1u : 0u;
+                dirty[q] = (lead[q] && mirror && !w.page_clean[p[q]]) ? 1u : 0u;
+            }
+            nl += lead[q];
+            nd += dirty[q];
+        }
+        uint32_t tot;
+        const uint32_t ex = block_scan_1024(nl | (nd << 16), wsum, &tot);
+        uint32_t pos = ex & 0xffffu, cpos = ex >> 16;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (lead[q]) {
+                w.plan_pages[pos] = p[q];
+                w.page_pos[p[q]] = static_cast<int32_t>(pos);
+                ++pos;
+            }
+            if (dirty[q]) {
+                w.readback[4 + cpos] = static_cast<uint32_t>(p[q]);
+                w.page_clean[p[q]] = w.sel_full[i0 + q];
+                ++cpos;
+            }
+        }
+        __syncthreads();        // page_pos of every leader is written
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t i = i0 + q;
+            if (i < n) {
+                const int32_t v = (p[q] >= 0 && cnt[q] == ref[q]) ? (mirror ? p[q] : w.page_pos[p[q]]) : -1;
+                w.plan_slot[i] = v;
+                if (out.slots && i < out.ids_cap)
+                    out.slots[i] = v;
+            }
+            if (p[q] >= 0) {    // every read of the counts was before the scan's barriers
+                w.page_cnt[p[q]] = 0;
+                w.page_first[p[q]] = 0xffffffffu;
+            }
+        }
+        if (threadIdx.x == 0) {
+            w.readback[0] = n;
+            w.readback[1] = tot & 0xffffu;
+            w.readback[2] = tot >> 16;
+            w.readback[3] = 0;
+            if (out.count_host) {
+                out.count_host[0] = n;
+                out.count_host[1] = tot & 0xffffu;
+                out.count_host[2] = tot >> 16;
+                out.count_host[3] = 0;
+            }
+        }
+        return;
+    }
     // leaders in list order: 4 consecutive entries per thread per tile; one
     // block scan of the packed counts (leaders low 16 bits, stale pages high:
     // at most 4,096 of each per tile)
@@ -889,6 +963,17 @@ __global__ void __launch_bounds__(256)
         dst[i] = __ldcs(src + i);
 }
 
+// The decode set from the kernel's parameters into device memory.
+struct SetBlob {
+    uint4 v[kSetInlineBytes / 16];
+};
+
+__global__ void __launch_bounds__(256) set_kernel(const __grid_constant__ SetBlob b, uint32_t nvec, uint4 *dst)
+{
+    for (uint32_t i = threadIdx.x; i < nvec; i += blockDim.x)
+        dst[i] = b.v[i];
+}
+
 __global__ void patch_kernel(const Geo g, int32_t *table, kvs_record *recs, uint8_t *page_clean,
                              const Patch *p, uint32_t n)
 {
@@ -1022,6 +1107,18 @@ cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *
     const uint32_t parts = static_cast<uint32_t>(std::max<uint64_t>(1, std::min<uint64_t>(64, page_vec / 4096)));
     scatter_kernel<<<dim3(npages, parts), 256, 0, s>>>(reinterpret_cast<const uint4 *>(staging), pages,
                                                       reinterpret_cast<uint4 *>(pool), page_vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set(const void *src, size_t bytes, void *dst, cudaStream_t s)
+{
+    if (bytes > kSetInlineBytes)
+        return cudaErrorInvalidValue;
+    SetBlob b;
+    std::memset(&b, 0, sizeof b);
+    std::memcpy(&b, src, bytes);
+    const uint32_t nvec = static_cast<uint32_t>((bytes + 15) / 16);
+    set_kernel<<<1, 256, 0, s>>>(b, nvec, static_cast<uint4 *>(dst));
     return cudaGetLastError();
 }
 

@@ -33,7 +33,7 @@ constexpr uint32_t kMassRange = 1024;   // blocks per combine CTA (stream-mass p
 // split: 1 -> CTA y = 0 merges only and CTA y >= 1 takes block range y - 1;
 // 0 -> CTA y takes block range y, and CTA 0 also merges.
 template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w, float *out, uint32_t split)
+__global__ void __launch_bounds__(256, 5) combine_kernel(const Geo g, const Work w, float *out, uint32_t split)
 {
     __shared__ float lse_sh[kMaxGroup];
     const DSet *ds = w.dset;
@@ -54,33 +54,44 @@ __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w,
     if (!merge && r0 >= sq.nb)
         return;                    // uniform over the CTA
     const uint32_t pb = sq.part_off + (l * g.Hkv + kvh) * sq.nchunk;
+    const uint32_t nch = sq.nchunk;
     if (h < g.G) {
-        float mmax = -INFINITY;
-        for (uint32_t c = lane; c < sq.nchunk; c += 32)
-            mmax = fmaxf(mmax, w.part_ml[(pb + c) * kMaxGroup + h].x);
-#pragma unroll
-        for (int x = 16; x > 0; x >>= 1)
-            mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, x));
-        float lsum = 0.f;
-        for (uint32_t c = lane; c < sq.nchunk; c += 32) {
+        // LSE_h in one pass: each lane keeps a running (max, rescaled sum)
+        // over its chunks, then the lanes' pairs are merged
+        float m = -INFINITY, sum = 0.f, m_first = -INFINITY;
+        for (uint32_t c = lane; c < nch; c += 32) {
             const float2 ml = w.part_ml[(pb + c) * kMaxGroup + h];
-            lsum += ml.y * fast_exp2(ml.x - mmax);
+            if (c == lane)
+                m_first = ml.x;
+            const float mn = fmaxf(m, ml.x);
+            sum = sum * fast_exp2(m - mn) + ml.y * fast_exp2(ml.x - mn);
+            m = mn;
         }
+        sum = m == -INFINITY ? 0.f : sum;
 #pragma unroll
-        for (int x = 16; x > 0; x >>= 1)
-            lsum += __shfl_xor_sync(0xffffffffu, lsum, x);
+        for (int x = 16; x > 0; x >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m, x);
+            const float so = __shfl_xor_sync(0xffffffffu, sum, x);
+            const float mn = fmaxf(m, mo);
+            sum = mn == -INFINITY ? 0.f : sum * fast_exp2(m - mn) + so * fast_exp2(mo - mn);
+            m = mn;
+        }
+        const float mmax = m, lsum = sum;
         if (merge) {
             // D / 32 consecutive floats per lane: one 16-byte (D = 128) or
-            // 8-byte (D = 64) load per chunk
+            // 8-byte (D = 64) load per chunk; the chunk maxima of the first
+            // 32 chunks come from the lanes that read them above
             using Vec = typename std::conditional<D == 128, float4, float2>::type;
             constexpr int E = D / 32;
             float acc[E];
 #pragma unroll
             for (int e = 0; e < E; ++e)
                 acc[e] = 0.f;
-#pragma unroll 4
-            for (uint32_t c = 0; c < sq.nchunk; ++c) {
-                const float f = fast_exp2(w.part_ml[(pb + c) * kMaxGroup + h].x - mmax);
+#pragma unroll 8
+            for (uint32_t c = 0; c < nch; ++c) {
+                const float mc = c < 32 ? __shfl_sync(0xffffffffu, m_first, c)
+                                        : w.part_ml[(pb + c) * kMaxGroup + h].x;
+                const float f = fast_exp2(mc - mmax);
                 const Vec v = *reinterpret_cast<const Vec *>(
                     w.part_o + (static_cast<size_t>(pb + c) * kMaxGroup + h) * D + lane * E);
                 const float *pv = reinterpret_cast<const float *>(&v);
@@ -107,6 +118,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const Geo g, const Work w,
     const float *lb = w.lse_blk + (static_cast<size_t>(l) * g.Hq + kvh * g.G) * nbt + sq.blk_off;
     float *sm = w.stream_mass + (static_cast<size_t>(l) * g.Hkv + kvh) * nbt + sq.blk_off;
     const uint32_t r1 = min(sq.nb, r0 + kMassRange);
+#pragma unroll 2
     for (uint32_t b = r0 + threadIdx.x; b < r1; b += blockDim.x) {
         float acc = 0.f;
         for (uint32_t j = 0; j < g.G; ++j)

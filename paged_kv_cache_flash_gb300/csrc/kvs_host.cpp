@@ -358,7 +358,7 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
 {
     if (!ids || nseq == 0 || nseq > kMaxCallSeqs)
         return fail(ctx, KVS_EINVAL, "nseq must be in [1, %u]", kMaxCallSeqs);
-    std::memset(ds, 0, sizeof(DSet));
+    std::memset(ds, 0, dset_bytes(nseq));
     const Geo &g = ctx->geo;
     uint32_t blk = 0, items = 0, items_q = 0, parts = 0;
     std::vector<std::pair<uint64_t, uint32_t>> order;
@@ -417,11 +417,10 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
         return fail(ctx, KVS_EINVAL, "too many decode partials (%u > %u)", parts, ctx->lay.parts_max);
     uint32_t off = 0;
     for (uint32_t i = 0; i < nseq; ++i) {
-        ds->sorted[i] = order[i].second;
-        ds->srt_off[i] = off;
+        ds->seq[i].srt_ci = order[i].second;
+        ds->seq[i].srt_off = off;
         off += ds->seq[order[i].second].nb;
     }
-    ds->srt_off[nseq] = off;
     ds->nseq = nseq;
     ds->nb_total = blk;
     ds->n_items = items;
@@ -433,18 +432,25 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
     return KVS_OK;
 }
 
+int launch_rc(kvs_ctx *ctx, cudaError_t e, const char *what, uint32_t kernels = 1);
+
+// The header and the call's entries: a small set in a kernel's parameters,
+// a larger one through the upload ring.
 int upload_set(kvs_ctx *ctx, const DSet &ds, cudaStream_t s)
 {
+    const size_t bytes = dset_bytes(ds.nseq);
+    if (bytes <= kSetInlineBytes)
+        return launch_rc(ctx, launch_set(&ds, bytes, ctx->work.dset, s), "decode set");
     RingSlot r;
-    int rc = ring_acquire(ctx, sizeof(DSet), &r);
+    int rc = ring_acquire(ctx, bytes, &r);
     if (rc)
         return rc;
-    std::memcpy(r.host, &ds, sizeof(DSet));
-    CU(cudaMemcpyAsync(ctx->work.dset, r.host, sizeof(DSet), cudaMemcpyHostToDevice, s));
+    std::memcpy(r.host, &ds, bytes);
+    CU(cudaMemcpyAsync(ctx->work.dset, r.host, bytes, cudaMemcpyHostToDevice, s));
     return ring_release(ctx, r, s);
 }
 
-int launch_rc(kvs_ctx *ctx, cudaError_t e, const char *what, uint32_t kernels = 1)
+int launch_rc(kvs_ctx *ctx, cudaError_t e, const char *what, uint32_t kernels)
 {
     if (e != cudaSuccess)
         return fail(ctx, KVS_ECUDA, "%s launch failed: %s", what, cudaGetErrorString(e));

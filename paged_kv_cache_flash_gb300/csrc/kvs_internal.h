@@ -38,11 +38,16 @@ struct DSeq {
     uint32_t qb;        // KIVI: leading blocks held in 2-bit group pages (even), else 0
     uint32_t nchunk_q;  // KIVI: chunks over those blocks (partials 0 .. nchunk_q-1), else 0
     uint32_t item_off_q;  // KIVI: prefix of group-page work items over call order
-    uint32_t pad;
+    // record order (ascending seq_id) -- these two describe the sequence at
+    // POSITION i of that order, not the sequence of this entry:
+    uint32_t srt_ci;      // its call index
+    uint32_t srt_off;     // prefix of nb over the positions before it
     uint64_t seq_id;
 };
 
-// The decode set, uploaded once per decode call (or debug_set_mass).
+// The decode set, uploaded once per decode call (or debug_set_mass).  The
+// entries come last, so that a call uploads only the header and its nseq
+// entries (dset_bytes).
 struct DSet {
     uint32_t nseq;
     uint32_t nb_total;
@@ -53,9 +58,16 @@ struct DSet {
     uint32_t wg;                      // KV heads (warps) per work item
     uint32_t chunk;                   // blocks per work item in this call
     DSeq seq[kMaxCallSeqs];
-    uint32_t sorted[kMaxCallSeqs];    // call indices, ascending seq_id
-    uint32_t srt_off[kMaxCallSeqs + 1];  // record-order prefix of nb over `sorted`
 };
+
+inline size_t dset_bytes(uint32_t nseq)
+{
+    return offsetof(DSet, seq) + static_cast<size_t>(nseq) * sizeof(DSeq);
+}
+
+// A decode set of at most this many bytes travels in a kernel's parameters
+// (no upload copy).
+constexpr size_t kSetInlineBytes = 4096;
 
 // Geometry and device pointers every kernel may need.
 struct Geo {

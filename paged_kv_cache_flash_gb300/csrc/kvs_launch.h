@@ -37,6 +37,9 @@ cudaError_t launch_mirror_copy(const Geo &g, const Work &w, const uint16_t *pool
                                uint32_t pool_blocks, int grid, cudaStream_t s);
 cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pages,
                           uint32_t npages, uint8_t *staging, cudaStream_t s);
+// bytes (<= kSetInlineBytes) from host memory src to device memory dst, in
+// a kernel's parameters (no copy engine operation)
+cudaError_t launch_set(const void *src, size_t bytes, void *dst, cudaStream_t s);
 cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, uint8_t *page_clean,
                          const Patch *p, uint32_t n, cudaStream_t s);
 cudaError_t launch_kivi_compress(const Geo &g, const KiviJob *jobs, uint32_t njobs, const uint8_t *pool,

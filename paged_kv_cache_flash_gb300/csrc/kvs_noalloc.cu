@@ -159,7 +159,8 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
     ds.seq[0].ntok = n_tokens;
     ds.seq[0].nb = nb;
     ds.seq[0].nchunk = nchunk;
-    ds.srt_off[1] = nb;
+    ds.seq[0].srt_ci = 0;       // record order: the one sequence, from block 0
+    ds.seq[0].srt_off = 0;
 
     // TMA descriptor of the caller's pool (host-side encoding only)
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
