@@ -234,10 +234,27 @@ __global__ void __launch_bounds__(FP8 ? 128 : 256, Tile<D, FP8>::kMinCtas)
     const uint32_t nb_total = a.w.dset->nb_total;
     const uint32_t jm = lane >> 3, i8 = lane & 7;
 
+    // bf16 query fragments (B operand of S^T = K Q^T) of head gq of an item:
+    // loaded when the item is prepared, one item ahead, so that no item
+    // starts with a wait on them
+    auto load_q = [&](const Item &itm, uint32_t (&dst)[D / 16][2]) {
+        const bool valid = itm.valid && gq < G;
+        const uint16_t *qh = a.q + ((static_cast<size_t>(valid ? itm.ci : 0) * g.L + (valid ? itm.l : 0)) * g.Hq +
+                                    (valid ? itm.kvh * G + gq : 0)) * D;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            dst[ks][0] = valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 2 * tq)) : 0u;
+            dst[ks][1] = valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 8 + 2 * tq)) : 0u;
+        }
+    };
+    uint32_t qc[D / 16][2], qn[D / 16][2];   // bf16: current and next item
+
     uint32_t claimed = 0;
     if (lane == 0)
         claimed = atomicAdd(a.w.counter, 1u);
     Prep cur = prepare_item(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+    if constexpr (!FP8)
+        load_q(cur.it, qc);
     if (lane == 0)
         claimed = atomicAdd(a.w.counter, 1u);   // id of the item after cur
     Prep nxt;
@@ -315,9 +332,8 @@ __global__ void __launch_bounds__(FP8 ? 128 : 256, Tile<D, FP8>::kMinCtas)
             } else {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    qf[ks][0] = valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 2 * tq)) : 0u;
-                    qf[ks][1] =
-                        valid ? __ldg(reinterpret_cast<const uint32_t *>(qh + ks * 16 + 8 + 2 * tq)) : 0u;
+                    qf[ks][0] = qc[ks][0];
+                    qf[ks][1] = qc[ks][1];
                 }
             }
         }
@@ -467,6 +483,8 @@ __global__ void __launch_bounds__(FP8 ? 128 : 256, Tile<D, FP8>::kMinCtas)
             if (i == 0 && !have_nxt) {
                 // while the ring streams: the next item and the claim after it
                 nxt = prepare_item(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+                if constexpr (!FP8)
+                    load_q(nxt.it, qn);
                 have_nxt = true;
                 if (lane == 0 && nxt.it.valid)
                     claimed = atomicAdd(a.w.counter, 1u);
@@ -495,6 +513,8 @@ __global__ void __launch_bounds__(FP8 ? 128 : 256, Tile<D, FP8>::kMinCtas)
         // ---- the next item becomes current ----------------------------------
         if (!have_nxt) {                    // a one-block item: prepare now
             nxt = prepare_item(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+            if constexpr (!FP8)
+                load_q(nxt.it, qn);
             if (lane == 0 && nxt.it.valid)
                 claimed = atomicAdd(a.w.counter, 1u);
         }
@@ -504,6 +524,13 @@ __global__ void __launch_bounds__(FP8 ? 128 : 256, Tile<D, FP8>::kMinCtas)
             c_blk = 0;
         }
         cur = nxt;
+        if constexpr (!FP8) {
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                qc[ks][0] = qn[ks][0];
+                qc[ks][1] = qn[ks][1];
+            }
+        }
         have_nxt = false;
         nxt.it.valid = 0;
         nxt.it.nblk = 0;
