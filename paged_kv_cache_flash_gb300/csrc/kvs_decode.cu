@@ -57,10 +57,13 @@ struct Tile {
     static constexpr int kBoxBytes = 2 * 16 * 64 * 2;    // 4 KiB either way
     static constexpr int kStageBytes = kHalf * kBoxBytes;
     static constexpr int kBoxElems = FP8 ? 128 : 64;     // box width in elements
-    // FP8: a shallower ring (the same bytes in flight per SM) so that three
-    // CTAs of 4 warps fit on an SM, with registers capped to match
-    static constexpr int kRing = FP8 ? 4 : kStages;
-    static constexpr int kMinCtas = FP8 ? 3 : 1;
+    // Shallow rings so that several CTAs of 4 warps share an SM (the same
+    // bytes in flight per SM): a lone warp per SM sub-partition streams only
+    // as fast as its own instruction latencies allow, so two or three warps
+    // per sub-partition keep HBM busy when some have run out of items.
+    // bf16: two CTAs, 3 x 8 KiB per warp; FP8: three CTAs, 4 x 4 KiB.
+    static constexpr int kRing = FP8 ? 4 : 3;
+    static constexpr int kMinCtas = FP8 ? 3 : 2;
     static constexpr int kWarpBytes = kRing * kStageBytes;
 };
 
@@ -206,7 +209,7 @@ __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g
 // item while it computes the current one, and keeps its own TMA ring of
 // kStages blocks in flight across item boundaries.  No CTA-wide barrier.
 template <int D, bool FP8>
-__global__ void __launch_bounds__(FP8 ? 128 : 256, Tile<D, FP8>::kMinCtas)
+__global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
     decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a)
 {
     using T = Tile<D, FP8>;
