@@ -51,6 +51,8 @@ struct DecodeArgs {
 
 // Bytes of one block's K and V sub-pages for one KV head.  bf16: boxes of
 // [K,V][16 tok][64 dims]; FP8 codes: one box of [K,V][16 tok][128 dims].
+constexpr uint32_t kClaimLead = 4;   // blocks between claiming an item and needing its pages
+
 template <int D, bool FP8>
 struct Tile {
     static constexpr int kHalf = FP8 ? 1 : D / 64;       // TMA boxes per stage
@@ -120,17 +122,22 @@ __device__ __forceinline__ Prep prepare_item(const DecodeArgs &a, uint32_t id, u
     const uint32_t ci = find_seq(&ds->seq[0].item_off, sizeof(DSeq) / 4, ds->nseq, id);
     const DSeq &sq = ds->seq[ci];
     // KV head fastest: warps that claim consecutive items read adjacent
-    // sub-pages of the same pages at about the same time (DRAM locality)
+    // sub-pages of the same pages at about the same time (DRAM locality);
+    // then layer, then chunk
     // (KIVI: the page items cover the blocks after the qb quantised ones,
     // and their partials follow the nchunk_q group-page chunks)
+    // chunk-major: every stream's chunk c before any stream's chunk c + 1, so
+    // the small last chunks are claimed last
     uint32_t local = id - sq.item_off;
     const uint32_t kvh = local % g.Hkv;
     local /= g.Hkv;
-    const uint32_t nch = sq.nchunk - sq.nchunk_q;
-    const uint32_t chunk = local % nch;
-    const uint32_t l = local / nch;
-    const uint32_t b0 = sq.qb + chunk * ds->chunk;
-    const uint32_t nblk = min(ds->chunk, sq.nb - b0);
+    const uint32_t l = local % g.L;
+    const uint32_t chunk = local / g.L;
+    const uint32_t r0 = chunk < sq.nbig ? chunk * ds->chunk_big
+                                        : sq.nbig * ds->chunk_big + (chunk - sq.nbig) * ds->chunk_small;
+    const uint32_t size = chunk < sq.nbig ? ds->chunk_big : ds->chunk_small;
+    const uint32_t b0 = sq.qb + r0;
+    const uint32_t nblk = min(size, sq.nb - b0);
     p.it.valid = 1;
     p.it.ci = ci;
     p.it.l = l;
@@ -252,14 +259,18 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
     };
     uint32_t qc[D / 16][2], qn[D / 16][2];   // bf16: current and next item
 
-    uint32_t claimed = 0;
-    if (lane == 0)
-        claimed = atomicAdd(a.w.counter, 1u);
-    Prep cur = prepare_item(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+    // items are claimed one at a time, each shortly before the ring needs its
+    // first block (kClaimLead blocks of compute hide the claim and the page-id
+    // loads), so that a warp never holds work it has not nearly reached
+    auto claim = [&]() -> uint32_t {
+        uint32_t id = 0;
+        if (lane == 0)
+            id = atomicAdd(a.w.counter, 1u);
+        return __shfl_sync(0xffffffffu, id, 0);
+    };
+    Prep cur = prepare_item(a, claim(), lane);
     if constexpr (!FP8)
         load_q(cur.it, qc);
-    if (lane == 0)
-        claimed = atomicAdd(a.w.counter, 1u);   // id of the item after cur
     Prep nxt;
     nxt.it.valid = 0;
     nxt.it.nblk = 0;
@@ -275,6 +286,7 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
     while (cur.it.valid) {
         const Item it = cur.it;
         const uint32_t kvh = it.kvh;
+        const uint32_t claim_at = it.nblk > T::kRing + kClaimLead ? it.nblk - T::kRing - kClaimLead : 0;
 
         // query fragments (B operand of S^T = K Q^T), head gq, and the scale
         // of the logits of this lane's heads h0, h1 (log2 domain)
@@ -483,14 +495,12 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
                     mma_bf16(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pb0, pb1);
             }
 
-            if (i == 0 && !have_nxt) {
-                // while the ring streams: the next item and the claim after it
-                nxt = prepare_item(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+            if (i == claim_at && !have_nxt) {
+                // while the ring streams the current item's last blocks
+                nxt = prepare_item(a, claim(), lane);
                 if constexpr (!FP8)
                     load_q(nxt.it, qn);
                 have_nxt = true;
-                if (lane == 0 && nxt.it.valid)
-                    claimed = atomicAdd(a.w.counter, 1u);
                 while (rg.inflight < T::kRing && issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane)) {
                 }
             }
@@ -514,12 +524,10 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
         }
 
         // ---- the next item becomes current ----------------------------------
-        if (!have_nxt) {                    // a one-block item: prepare now
-            nxt = prepare_item(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+        if (!have_nxt) {                    // not claimed in the loop: claim now
+            nxt = prepare_item(a, claim(), lane);
             if constexpr (!FP8)
                 load_q(nxt.it, qn);
-            if (lane == 0 && nxt.it.valid)
-                claimed = atomicAdd(a.w.counter, 1u);
         }
         if (c_in_nxt) {
             c_in_nxt = false;               // cursor already inside the new item

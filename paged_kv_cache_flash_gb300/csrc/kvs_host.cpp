@@ -363,15 +363,27 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
     uint32_t blk = 0, items = 0, items_q = 0, parts = 0;
     std::vector<std::pair<uint64_t, uint32_t>> order;
     order.reserve(nseq);
-    uint32_t nbs[kMaxCallSeqs], qbs[kMaxCallSeqs];
+    uint32_t nres[kMaxCallSeqs], qbs[kMaxCallSeqs];
     for (uint32_t i = 0; i < nseq; ++i) {
         SeqState *s = find_seq(ctx, ids[i]);
-        nbs[i] = s ? (s->ntok + kBlockTokens - 1) / kBlockTokens : 1;
+        const uint32_t nb = s ? (s->ntok + kBlockTokens - 1) / kBlockTokens : 1;
         qbs[i] = s && g.kivi ? s->qtok / kBlockTokens : 0;
+        nres[i] = nb - qbs[i];
     }
-    const uint32_t chunk = pick_chunk(nbs, nseq, g.L, g.Hkv, ctx->decode_grid * ctx->wg, ctx->lay.parts_max,
-                                      g.kivi ? qbs : nullptr);
-    if (chunk == 0)
+    // 2-bit group-page chunks (uniform, for the 2-bit decode kernel's warps),
+    // then the page chunks with whatever partials are left
+    uint32_t chunk = kMinChunk;
+    uint64_t parts_q = 0;
+    if (g.kivi) {
+        chunk = pick_chunk(qbs, nseq, g.L, g.Hkv, static_cast<uint32_t>(ctx->kivi_grid) * 4, ctx->lay.parts_max);
+        if (chunk == 0)
+            return fail(ctx, KVS_EINVAL, "too many blocks in one call for the workspace partials");
+        for (uint32_t i = 0; i < nseq; ++i)
+            parts_q += static_cast<uint64_t>(g.L) * g.Hkv * ((qbs[i] + chunk - 1) / chunk);
+    }
+    const PageChunks pc = pick_page_chunks(nres, nseq, g.L, g.Hkv, ctx->decode_grid * ctx->wg,
+                                           ctx->lay.parts_max, parts_q);
+    if (pc.big == 0)
         return fail(ctx, KVS_EINVAL, "too many blocks in one call for the workspace partials");
     for (uint32_t i = 0; i < nseq; ++i) {
         uint32_t slot;
@@ -392,7 +404,8 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
         // chunked apart: group-page chunks first, then page chunks
         q.qb = g.kivi ? s->qtok / kBlockTokens : 0;
         q.nchunk_q = (q.qb + chunk - 1) / chunk;
-        const uint32_t nchunk_p = (q.nb - q.qb + chunk - 1) / chunk;
+        const uint32_t nchunk_p = pc.nchunk(q.nb - q.qb);
+        q.nbig = pc.nbig(q.nb - q.qb);
         q.nchunk = q.nchunk_q + nchunk_p;
         q.blk_off = blk;
         q.item_off = items;
@@ -428,6 +441,8 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
     ds->n_parts = parts;
     ds->wg = ctx->wg;
     ds->chunk = chunk;
+    ds->chunk_big = pc.big;
+    ds->chunk_small = pc.small;
     ds->t = ctx->t;
     return KVS_OK;
 }
@@ -607,9 +622,13 @@ Layout workspace_layout(const kvs_config &c)
     const size_t seqs = std::min<size_t>(c.max_seqs, kMaxCallSeqs);
     const size_t LH = static_cast<size_t>(c.num_layers) * c.num_q_heads;
     L.nb_max = static_cast<uint32_t>(nb_max);
-    // partials for chunks of 32 blocks (the decode picks 16 only when they fit)
+    // partials for chunks of 32 blocks, plus the short chunks at the end of
+    // each stream: their blocks cover about one large chunk (at most 128
+    // blocks) per decode warp (at most 2,048 warps), in chunks of 16, plus a
+    // short remainder per stream
     L.parts_max = static_cast<uint32_t>(static_cast<size_t>(c.num_layers) * c.num_kv_heads *
-                                        ((nb_max + 31) / 32 + seqs));
+                                            ((nb_max + 31) / 32 + 3 * seqs) +
+                                        2048 * 128 / 16);
     L.tiles_max = static_cast<uint32_t>((nb_max + 1023) / 1024 + 1);
     L.ring_slots = kRingSlots;
     L.ring_slot_bytes = kRingSlotBytes;

@@ -34,7 +34,8 @@ struct DSeq {
     uint32_t blk_off;   // prefix of nb over call order (per-block LSE index)
     uint32_t item_off;  // prefix of CTA work items over call order
     uint32_t part_off;  // prefix of per-warp partials over call order
-    uint32_t nchunk;    // chunks (work items per (layer, KV head)): nchunk_q + residual chunks
+    uint32_t nchunk;    // chunks (work items per (layer, KV head)): nchunk_q + page chunks
+    uint32_t nbig;      // page chunks of chunk_big blocks; the rest are of chunk_small
     uint32_t qb;        // KIVI: leading blocks held in 2-bit group pages (even), else 0
     uint32_t nchunk_q;  // KIVI: chunks over those blocks (partials 0 .. nchunk_q-1), else 0
     uint32_t item_off_q;  // KIVI: prefix of group-page work items over call order
@@ -56,7 +57,9 @@ struct DSet {
     uint32_t n_parts;
     uint64_t t;                       // step counter after the decode
     uint32_t wg;                      // KV heads (warps) per work item
-    uint32_t chunk;                   // blocks per work item in this call
+    uint32_t chunk;                   // blocks per 2-bit group-page work item
+    uint32_t chunk_big;               // blocks per page work item: the first nbig chunks
+    uint32_t chunk_small;             //   ... and the rest of each stream
     DSeq seq[kMaxCallSeqs];
 };
 
@@ -195,26 +198,76 @@ struct StepAppendInline {
     StepAppend e[kStepInline];
 };
 
-// Blocks per decode work item (one KV-head stream chunk) for one call: the
-// largest of 128, 64, 32, 16 that still gives each of the `workers` warps of
-// the persistent grid at least 8 items (a short tail without many partials),
-// as long as the chunk partials fit in parts_cap; if no size gives that many
-// items, the smallest that fits.  0 if not even 128 fits.
+// Blocks per 2-bit group-page work item for one call (uniform chunks of
+// the nb[i] group-page blocks): the largest of 128, 64, 32, 16 that still
+// gives each of the `workers` warps at least 8 items (a short tail without
+// many partials), as long as the chunk partials fit in parts_cap; if no size
+// gives that many items, the smallest that fits.  0 if not even 128 fits.
 inline uint32_t pick_chunk(const uint32_t *nb, uint32_t n, uint32_t L, uint32_t Hkv,
-                           uint32_t workers, uint64_t parts_cap, const uint32_t *qb = nullptr)
+                           uint32_t workers, uint64_t parts_cap)
 {
-    // qb (KIVI): leading group-page blocks, chunked apart from the rest
     uint32_t best = 0;
     for (uint32_t c = kMaxChunk; c >= kMinChunk; c >>= 1) {
         uint64_t parts = 0;
-        for (uint32_t i = 0; i < n; ++i) {
-            const uint32_t q = qb ? qb[i] : 0;
-            parts += static_cast<uint64_t>(L) * Hkv * ((q + c - 1) / c + (nb[i] - q + c - 1) / c);
-        }
+        for (uint32_t i = 0; i < n; ++i)
+            parts += static_cast<uint64_t>(L) * Hkv * ((nb[i] + c - 1) / c);
         if (parts > parts_cap)
             break;
         best = c;
         if (parts >= 8ull * workers)        // one item per partial
+            break;
+    }
+    return best;
+}
+
+// Page work items of one call.  Each (layer, KV head) stream of n blocks is
+// cut into nbig(n) chunks of `big` blocks followed by chunks of `small`
+// blocks over its last blocks (at least `tail` of them), and a sequence's
+// items are claimed chunk by chunk (every stream's chunk 0, then chunk 1, ...):
+// the small chunks come last, so that when the large ones run out every warp
+// still finds short work and the launch ends evenly.  `tail` makes the small
+// chunks of all streams at least one large chunk per warp.
+struct PageChunks {
+    uint32_t big, small, tail;
+    uint32_t nbig(uint32_t n) const { return n > tail ? (n - tail) / big : 0; }
+    uint32_t nchunk(uint32_t n) const
+    {
+        const uint32_t nb = nbig(n);
+        return nb + (n - nb * big + small - 1) / small;
+    }
+};
+
+// The largest big chunk (128, 64, 32, 16) whose large items alone give every
+// one of the `workers` warps one to start with; small chunks of 16 blocks
+// (or 32, 64, ... when the partials of 16 would not fit parts_cap with
+// extra_parts).  If no big chunk gives every warp a large item, the smallest
+// that fits.  big = 0 if nothing fits.
+inline PageChunks pick_page_chunks(const uint32_t *nres, uint32_t n, uint32_t L, uint32_t Hkv,
+                                   uint32_t workers, uint64_t parts_cap, uint64_t extra_parts)
+{
+    PageChunks best{0, 0, 0};
+    const uint64_t streams = static_cast<uint64_t>(n) * L * Hkv;
+    for (uint32_t c = kMaxChunk; c >= kMinChunk; c >>= 1) {
+        bool fits = false;
+        uint64_t big_items = 0;
+        for (uint32_t sm = kMinChunk; sm <= c && !fits; sm <<= 1) {
+            PageChunks pc;
+            pc.big = c;
+            pc.small = sm;
+            const uint64_t t = (static_cast<uint64_t>(workers) * c + streams - 1) / streams;
+            pc.tail = static_cast<uint32_t>((t + sm - 1) / sm * sm);
+            uint64_t parts = extra_parts;
+            big_items = 0;
+            for (uint32_t i = 0; i < n; ++i) {
+                parts += static_cast<uint64_t>(L) * Hkv * pc.nchunk(nres[i]);
+                big_items += static_cast<uint64_t>(L) * Hkv * pc.nbig(nres[i]);
+            }
+            if (parts <= parts_cap) {
+                fits = true;
+                best = pc;
+            }
+        }
+        if (!fits || big_items >= workers)
             break;
     }
     return best;

@@ -156,6 +156,9 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
     ds.n_parts = static_cast<uint32_t>(parts);
     ds.wg = wg;
     ds.chunk = chunk;
+    ds.chunk_big = chunk;       // uniform chunks: every chunk "big", the last one short
+    ds.chunk_small = chunk;
+    ds.seq[0].nbig = nchunk;
     ds.seq[0].ntok = n_tokens;
     ds.seq[0].nb = nb;
     ds.seq[0].nchunk = nchunk;
