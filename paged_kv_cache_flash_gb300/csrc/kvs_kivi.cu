@@ -55,6 +55,7 @@ constexpr uint32_t kTile = KVS_KIVI_TILE_BYTES;
 constexpr int kKRing = 6;           // group tiles in flight per warp
 constexpr int kKWarps = 4;          // warps per CTA
 constexpr int kKMinCtas = 3;        // CTAs per SM (12 warps: dequantisation is ALU work)
+constexpr uint32_t kKClaimLead = 2; // groups between claiming an item and needing its tiles
 constexpr int kKD = 128;            // head dimension of the scheme
 
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
@@ -354,12 +355,15 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
     const uint32_t nb_total = a.w.dset->nb_total;
     uint32_t *counter = a.w.counter + 1;
 
-    uint32_t claimed = 0;
-    if (lane == 0)
-        claimed = atomicAdd(counter, 1u);
-    KPrep cur = prepare_kitem(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
-    if (lane == 0)
-        claimed = atomicAdd(counter, 1u);
+    // one item claimed at a time, shortly before the ring needs its first
+    // tile (as in the page decode kernel)
+    auto claim = [&]() -> uint32_t {
+        uint32_t id = 0;
+        if (lane == 0)
+            id = atomicAdd(counter, 1u);
+        return __shfl_sync(0xffffffffu, id, 0);
+    };
+    KPrep cur = prepare_kitem(a, claim(), lane);
     KPrep nxt;
     nxt.it.valid = 0;
     nxt.it.ng = 0;
@@ -375,6 +379,7 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
     while (cur.it.valid) {
         const KItem it = cur.it;
         const uint32_t kvh = it.kvh;
+        const uint32_t claim_at = it.ng > kKRing + kKClaimLead ? it.ng - kKRing - kKClaimLead : 0;
         // query fragments for the lane's head gq: channels 32tq + 16(ks/4) +
         // {i0, i0+8} (b0) and {i0+1, i0+9} (b1), i0 = 2(ks%4) -- the pairs
         // the K code words hold
@@ -550,11 +555,9 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                             kdq(vw[w], vx[w], i + 3, vm[1][2 * cg], vm[1][2 * cg + 1]), pb[j][0], pb[j][1]);
                 }
             }
-            if (gi == 0 && !have_nxt) {
-                nxt = prepare_kitem(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
+            if (gi == claim_at && !have_nxt) {
+                nxt = prepare_kitem(a, claim(), lane);
                 have_nxt = true;
-                if (lane == 0 && nxt.it.valid)
-                    claimed = atomicAdd(counter, 1u);
                 while (rg.inflight < kKRing &&
                        kissue_next(a, cur, nxt, have_nxt, c_in_nxt, c_grp, rg, ring_u32, bars[warp], lane)) {
                 }
@@ -574,11 +577,8 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
             po[h0 * kKD + mt * 16 + gq + 8] = o[mt][2];
             po[h1 * kKD + mt * 16 + gq + 8] = o[mt][3];
         }
-        if (!have_nxt) {
-            nxt = prepare_kitem(a, __shfl_sync(0xffffffffu, claimed, 0), lane);
-            if (lane == 0 && nxt.it.valid)
-                claimed = atomicAdd(counter, 1u);
-        }
+        if (!have_nxt)                      // not claimed in the loop: claim now
+            nxt = prepare_kitem(a, claim(), lane);
         if (c_in_nxt)
             c_in_nxt = false;
         else
