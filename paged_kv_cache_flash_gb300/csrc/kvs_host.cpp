@@ -370,16 +370,17 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
         qbs[i] = s && g.kivi ? s->qtok / kBlockTokens : 0;
         nres[i] = nb - qbs[i];
     }
-    // 2-bit group-page chunks (uniform, for the 2-bit decode kernel's warps),
-    // then the page chunks with whatever partials are left
-    uint32_t chunk = kMinChunk;
+    // 2-bit group-page chunks (for the 2-bit decode kernel's warps), then the
+    // page chunks with whatever partials are left
+    PageChunks qc{kMinChunk, kMinChunk, 0};
     uint64_t parts_q = 0;
     if (g.kivi) {
-        chunk = pick_chunk(qbs, nseq, g.L, g.Hkv, static_cast<uint32_t>(ctx->kivi_grid) * 4, ctx->lay.parts_max);
-        if (chunk == 0)
+        qc = pick_page_chunks(qbs, nseq, g.L, g.Hkv, static_cast<uint32_t>(ctx->kivi_grid) * 4,
+                              ctx->lay.parts_max, 0);
+        if (qc.big == 0)
             return fail(ctx, KVS_EINVAL, "too many blocks in one call for the workspace partials");
         for (uint32_t i = 0; i < nseq; ++i)
-            parts_q += static_cast<uint64_t>(g.L) * g.Hkv * ((qbs[i] + chunk - 1) / chunk);
+            parts_q += static_cast<uint64_t>(g.L) * g.Hkv * qc.nchunk(qbs[i]);
     }
     const PageChunks pc = pick_page_chunks(nres, nseq, g.L, g.Hkv, ctx->decode_grid * ctx->wg,
                                            ctx->lay.parts_max, parts_q);
@@ -403,7 +404,8 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
         // KIVI: the leading qb blocks (group pages) and the rest (pages) are
         // chunked apart: group-page chunks first, then page chunks
         q.qb = g.kivi ? s->qtok / kBlockTokens : 0;
-        q.nchunk_q = (q.qb + chunk - 1) / chunk;
+        q.nchunk_q = qc.nchunk(q.qb);
+        q.nbig_q = qc.nbig(q.qb);
         const uint32_t nchunk_p = pc.nchunk(q.nb - q.qb);
         q.nbig = pc.nbig(q.nb - q.qb);
         q.nchunk = q.nchunk_q + nchunk_p;
@@ -440,7 +442,8 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
     ds->n_items_q = items_q;
     ds->n_parts = parts;
     ds->wg = ctx->wg;
-    ds->chunk = chunk;
+    ds->chunk = qc.big;
+    ds->chunk_q_small = qc.small;
     ds->chunk_big = pc.big;
     ds->chunk_small = pc.small;
     ds->t = ctx->t;

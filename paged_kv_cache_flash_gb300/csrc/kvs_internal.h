@@ -38,6 +38,7 @@ struct DSeq {
     uint32_t nbig;      // page chunks of chunk_big blocks; the rest are of chunk_small
     uint32_t qb;        // KIVI: leading blocks held in 2-bit group pages (even), else 0
     uint32_t nchunk_q;  // KIVI: chunks over those blocks (partials 0 .. nchunk_q-1), else 0
+    uint32_t nbig_q;    // KIVI: group-page chunks of `chunk` blocks; the rest of chunk_q_small
     uint32_t item_off_q;  // KIVI: prefix of group-page work items over call order
     // record order (ascending seq_id) -- these two describe the sequence at
     // POSITION i of that order, not the sequence of this entry:
@@ -57,7 +58,8 @@ struct DSet {
     uint32_t n_parts;
     uint64_t t;                       // step counter after the decode
     uint32_t wg;                      // KV heads (warps) per work item
-    uint32_t chunk;                   // blocks per 2-bit group-page work item
+    uint32_t chunk;                   // blocks per 2-bit group-page work item: the first nbig_q
+    uint32_t chunk_q_small;           //   ... and the rest of each stream
     uint32_t chunk_big;               // blocks per page work item: the first nbig chunks
     uint32_t chunk_small;             //   ... and the rest of each stream
     DSeq seq[kMaxCallSeqs];
@@ -198,29 +200,8 @@ struct StepAppendInline {
     StepAppend e[kStepInline];
 };
 
-// Blocks per 2-bit group-page work item for one call (uniform chunks of
-// the nb[i] group-page blocks): the largest of 128, 64, 32, 16 that still
-// gives each of the `workers` warps at least 8 items (a short tail without
-// many partials), as long as the chunk partials fit in parts_cap; if no size
-// gives that many items, the smallest that fits.  0 if not even 128 fits.
-inline uint32_t pick_chunk(const uint32_t *nb, uint32_t n, uint32_t L, uint32_t Hkv,
-                           uint32_t workers, uint64_t parts_cap)
-{
-    uint32_t best = 0;
-    for (uint32_t c = kMaxChunk; c >= kMinChunk; c >>= 1) {
-        uint64_t parts = 0;
-        for (uint32_t i = 0; i < n; ++i)
-            parts += static_cast<uint64_t>(L) * Hkv * ((nb[i] + c - 1) / c);
-        if (parts > parts_cap)
-            break;
-        best = c;
-        if (parts >= 8ull * workers)        // one item per partial
-            break;
-    }
-    return best;
-}
-
-// Page work items of one call.  Each (layer, KV head) stream of n blocks is
+// Work items of one call (page items, and separately the 2-bit group-page
+// items of a KIVI context).  Each (layer, KV head) stream of n blocks is
 // cut into nbig(n) chunks of `big` blocks followed by chunks of `small`
 // blocks over its last blocks (at least `tail` of them), and a sequence's
 // items are claimed chunk by chunk (every stream's chunk 0, then chunk 1, ...):

@@ -221,13 +221,17 @@ __device__ __forceinline__ KPrep prepare_kitem(const KArgs &a, uint32_t id, uint
     const Geo &g = a.g;
     const uint32_t ci = find_seq(&ds->seq[0].item_off_q, sizeof(DSeq) / 4, ds->nseq, id);
     const DSeq &sq = ds->seq[ci];
+    // chunk-major, KV head fastest, as the page items: large chunks first,
+    // the short ones last (all chunk sizes even: whole groups)
     uint32_t local = id - sq.item_off_q;
     const uint32_t kvh = local % g.Hkv;
     local /= g.Hkv;
-    const uint32_t chunk = local % sq.nchunk_q;
-    const uint32_t l = local / sq.nchunk_q;
-    const uint32_t b0 = chunk * ds->chunk;
-    const uint32_t nblk = min(ds->chunk, sq.qb - b0);
+    const uint32_t l = local % g.L;
+    const uint32_t chunk = local / g.L;
+    const uint32_t b0 = chunk < sq.nbig_q ? chunk * ds->chunk
+                                          : sq.nbig_q * ds->chunk + (chunk - sq.nbig_q) * ds->chunk_q_small;
+    const uint32_t size = chunk < sq.nbig_q ? ds->chunk : ds->chunk_q_small;
+    const uint32_t nblk = min(size, sq.qb - b0);
     p.it.valid = 1;
     p.it.ci = ci;
     p.it.l = l;
