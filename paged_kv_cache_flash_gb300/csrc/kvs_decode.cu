@@ -8,26 +8,29 @@
 //
 // Structure of one step:
 //   decode_kernel  -- persistent grid of independent warps.  Each warp claims
-//                     work items (sequence, layer, KV head, chunk of 16..128
-//                     blocks) from a global counter, prepares the next item
-//                     while computing the current one, and keeps its own TMA
-//                     ring of the head's K and V sub-pages streaming across
-//                     item boundaries (128-byte swizzle, bounded mbarrier
-//                     waits).  Warp-level tensor-core MMAs compute
+//                     work items (sequence, layer, KV head, chunk: 128-block
+//                     chunks first, 16-block chunks over the end of each
+//                     stream, claimed chunk by chunk) from a global counter,
+//                     each shortly before its ring needs the item's first
+//                     block, and keeps its own TMA ring of the head's K and V
+//                     sub-pages streaming across item boundaries (128-byte
+//                     swizzle, bounded mbarrier waits).  Warp-level
+//                     tensor-core MMAs compute
 //                       S^T[16 tokens][8 heads] = K . Q^T
 //                       O^T[d][8 heads]        += V^T . P^T
 //                     with an online softmax in registers.  Per block it writes
 //                     the block's log2-sum-exp for each query head; per item
 //                     the running max, sum and unnormalised output.
-//                     bf16 pages: bf16 MMAs, 6-stage rings, 4 warps per SM.
+//                     bf16 pages: bf16 MMAs, 3-stage rings, 8 warps per SM.
 //                     FP8 E4M3 pages ("Fitting a Million Tokens", s.02): S by
 //                     e4m3 MMAs over the stored codes with Q as two exact
 //                     E4M3 terms, O by f16 MMAs over codes converted in
 //                     registers; 4-stage rings, 12 warps per SM.
 //                     (2-bit KIVI group pages are decoded by kvs_kivi.cu; the
 //                     page items of such a sequence cover its residual blocks.)
-//   combine_kernel -- merges a stream's chunks: per head log2-sum-exp LSE_h and
-//                     the normalised output.
+//   combine_kernel -- merges a stream's chunks: per head log2-sum-exp LSE_h,
+//                     the normalised output and the stream's block masses
+//                     (kvs_combine.cu).
 //   mass_kernel    -- M(b) = 1/(L*Hq) * sum_{l,h} 2^(lse_blk(l,h,b) - LSE_h),
 //                     summed in a fixed order (deterministic).
 #include <cuda_bf16.h>
@@ -213,8 +216,9 @@ __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g
 
 // Persistent kernel of fully independent warps.  Each warp claims work items
 // (one KV-head stream chunk each) from a global counter, prepares the next
-// item while it computes the current one, and keeps its own TMA ring of
-// kStages blocks in flight across item boundaries.  No CTA-wide barrier.
+// one while it computes the last blocks of the current one, and keeps its own
+// TMA ring of T::kRing blocks in flight across item boundaries.  No CTA-wide
+// barrier.
 template <int D, bool FP8>
 __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
     decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a)
@@ -245,8 +249,8 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
     const uint32_t jm = lane >> 3, i8 = lane & 7;
 
     // bf16 query fragments (B operand of S^T = K Q^T) of head gq of an item:
-    // loaded when the item is prepared, one item ahead, so that no item
-    // starts with a wait on them
+    // loaded when the item is prepared, before the current item ends, so
+    // that no item starts with a wait on them
     auto load_q = [&](const Item &itm, uint32_t (&dst)[D / 16][2]) {
         const bool valid = itm.valid && gq < G;
         const uint16_t *qh = a.q + ((static_cast<size_t>(valid ? itm.ci : 0) * g.L + (valid ? itm.l : 0)) * g.Hq +
