@@ -33,7 +33,7 @@ constexpr uint32_t kMassRange = 1024;   // blocks per combine CTA (stream-mass p
 // split: 1 -> CTA y = 0 merges only and CTA y >= 1 takes block range y - 1;
 // 0 -> CTA y takes block range y, and CTA 0 also merges.
 template <int D>
-__global__ void __launch_bounds__(256, 5) combine_kernel(const Geo g, const Work w, float *out, uint32_t split)
+__global__ void __launch_bounds__(256, 8) combine_kernel(const Geo g, const Work w, float *out, uint32_t split)
 {
     __shared__ float lse_sh[kMaxGroup];
     const DSet *ds = w.dset;
