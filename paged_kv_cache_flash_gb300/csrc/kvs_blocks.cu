@@ -373,11 +373,11 @@ __global__ void __launch_bounds__(kSelThreads)
     __shared__ uint32_t wpre[kSelThreads / 32];
     __shared__ uint32_t base_sh;
     const DSet *ds = w.dset;
-    uint32_t slots[kSelPerThread], bs[kSelPerThread], nts[kSelPerThread];
+    uint32_t bs[kSelPerThread], nts[kSelPerThread];
     size_t idx[kSelPerThread];
     for (int q = 0; q < kSelPerThread; ++q) {
         const uint32_t r = blockIdx.x * kSelTile + threadIdx.x * kSelPerThread + q;
-        idx[q] = r < nb_total ? rec_index(g, ds, r, &slots[q], &bs[q], &nts[q]) : 0;
+        idx[q] = r < nb_total ? rec_index(g, ds, r, nullptr, &bs[q], &nts[q]) : 0;
     }
     pdl_wait();                 // tile counts and records come from earlier kernels
     pdl_trigger();

@@ -450,7 +450,13 @@ int build_set(kvs_ctx *ctx, const uint64_t *ids, uint32_t nseq, DSet *ds)
     return KVS_OK;
 }
 
-int launch_rc(kvs_ctx *ctx, cudaError_t e, const char *what, uint32_t kernels = 1);
+int launch_rc(kvs_ctx *ctx, cudaError_t e, const char *what, uint32_t kernels = 1)
+{
+    if (e != cudaSuccess)
+        return fail(ctx, KVS_ECUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+    ctx->kernel_launches += kernels;
+    return KVS_OK;
+}
 
 // The header and the call's entries: a small set in a kernel's parameters,
 // a larger one through the upload ring.
@@ -468,13 +474,6 @@ int upload_set(kvs_ctx *ctx, const DSet &ds, cudaStream_t s)
     return ring_release(ctx, r, s);
 }
 
-int launch_rc(kvs_ctx *ctx, cudaError_t e, const char *what, uint32_t kernels)
-{
-    if (e != cudaSuccess)
-        return fail(ctx, KVS_ECUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
-    ctx->kernel_launches += kernels;
-    return KVS_OK;
-}
 
 // Patch list upload + kernel (table entries and records).
 int apply_patches(kvs_ctx *ctx, const std::vector<Patch> &p, cudaStream_t s)
