@@ -92,6 +92,28 @@ def test_ragged_multi_sequence_and_shared_prefix():
     run.close()
 
 
+def test_many_sequences_ring_uploads_and_multi_tile_selection():
+    """80 sequences of 1..499 tokens in every call: the decode set (more than
+    63 entries) and the step append (more than 16) travel through the upload
+    ring instead of kernel parameters, and the ~1,300 records take the
+    two-kernel (count, then scatter) selection; 3 steps against the full
+    oracle, listed ids and gathered pages checked."""
+    rng = np.random.default_rng(0x6B76 + 80)
+    lens = tuple(int(x) for x in rng.integers(1, 500, size=80))
+    pool = sum((n + 4 + 15) // 16 for n in lens) + 8
+    wl = W.workload("tiny", prefill_lens=lens, pool_pages=pool, steps=3, skew=True)
+    assert sum((n + wl.steps + 15) // 16 for n in lens) > 1024
+    run = Run(wl, 0.15)
+    host = _pinned(pool * wl.page_bytes)
+    for _ in range(wl.steps):
+        res = run.step(host)
+        summ = run.compare(res)
+        _check_gather(run, res, host)
+    run.ctx.check_device()
+    print("80 sequences", summ)
+    run.close()
+
+
 def test_single_token_sequence_and_large_group():
     """One-token sequences (nothing but block 0) and the full 8:1 group at d=128."""
     wl = W.workload("l70b_8k", L=3, prefill_lens=(1, 17), pool_pages=8, steps=3)
