@@ -78,6 +78,28 @@ def dist_info():
     return ws, rank, local
 
 
+def session_copy_rate(torch, dev, gib=4, reps=20):
+    """The box's streaming copy rate in this session ([VA] method for its copy
+    figure: large buffers, median of repeated runs): a device-to-device copy
+    of `gib` GiB, read + write bytes, the median of `reps` runs timed with
+    CUDA events."""
+    n = (gib << 30) // 2
+    a = torch.empty(n, dtype=torch.bfloat16, device=dev).normal_()
+    b = torch.empty_like(a)
+    b.copy_(a)
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    del a, b
+    torch.cuda.empty_cache()
+    return 2 * n * 2 / (statistics.median(ts) / 1e3) / 1e9
+
+
 def read_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -649,6 +671,14 @@ def run_kvs(args):
                    "select_gather_ms": round(literal_ms, 3),
                    "host_link_GBps": round(moved / (literal_ms / 1e3) / 1e9, 2) if literal_ms else None}
 
+    # ---- the box's streaming copy rate in this session (context for the
+    # roofline: MEASURED_PEAKS.json is the denominator; this shows what this
+    # box moved today with a plain copy)
+    s_copy = session_copy_rate(torch, dev)
+    stream = {"copy_GBps": round(s_copy, 1), "decode_kernel_vs_copy": round(achieved / s_copy, 4),
+              "method": "torch copy_ of 4 GiB bf16 buffers, read + write bytes, median of 20 runs, "
+                        "CUDA events"}
+
     # ---- CPU baseline: the oracle on a bounded sample --------------------
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -710,6 +740,7 @@ def run_kvs(args):
             "literal_gather": literal,
             "cpu_baseline": cpu,
             "clocks": clk,
+            "copy_rate_session": stream,
             "gpu_launches": launches,
             "wall_s_timed": round(wall, 3),
         }
