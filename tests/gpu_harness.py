@@ -169,7 +169,7 @@ class Run:
                 Kf, Vf = O.kivi_effective(o.K, o.V)
                 r = O.decode_with_mass(q[s], Kf, Vf, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d)
             elif self.fp8:     # the pages hold codes of the bf16 inputs
-                kc, vc = self.codes(o.K, o.V)
+                kc, vc = self.seq_codes(sid, o)
                 r = O.decode_with_mass(q[s], kc, vc, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d,
                                        k_lut=O.e4m3_lut(self.k_scale), v_lut=O.e4m3_lut(self.v_scale))
             else:
@@ -236,6 +236,19 @@ class Run:
 
     def codes(self, Kb, Vb):
         return (O.quantize_bf16_e4m3(Kb, self.k_scale), O.quantize_bf16_e4m3(Vb, self.v_scale))
+
+    def seq_codes(self, sid, o):
+        """Codes of a sequence's tokens so far: tokens are write-once, so the
+        codes of earlier steps are kept and only the new tokens quantised."""
+        cache = self.__dict__.setdefault("_codes", {})
+        kc, vc = cache.get(sid, (None, None))
+        done = 0 if kc is None else kc.shape[0]
+        if done < o.n:
+            k_new, v_new = self.codes(o.K[done:], o.V[done:])
+            kc = k_new if kc is None else np.concatenate([kc, k_new])
+            vc = v_new if vc is None else np.concatenate([vc, v_new])
+            cache[sid] = (kc, vc)
+        return kc[:o.n], vc[:o.n]
 
     def oracle_page(self, sid, b):
         o = self.orc[sid]
