@@ -28,7 +28,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr uint32_t kMassRange = 1024;   // blocks per combine CTA (stream-mass part)
+constexpr uint32_t kMassRange = 2048;   // blocks per combine CTA (stream-mass part)
 
 // split: 1 -> CTA y = 0 merges only and CTA y >= 1 takes block range y - 1;
 // 0 -> CTA y takes block range y, and CTA 0 also merges.
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(256, 8) combine_kernel(const Geo g, const Work
     const float *lb = w.lse_blk + (static_cast<size_t>(l) * g.Hq + kvh * g.G) * nbt + sq.blk_off;
     float *sm = w.stream_mass + (static_cast<size_t>(l) * g.Hkv + kvh) * nbt + sq.blk_off;
     const uint32_t r1 = min(sq.nb, r0 + kMassRange);
-#pragma unroll 2
+#pragma unroll 4
     for (uint32_t b = r0 + threadIdx.x; b < r1; b += blockDim.x) {
         float acc = 0.f;
         for (uint32_t j = 0; j < g.G; ++j)
