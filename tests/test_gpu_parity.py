@@ -92,14 +92,16 @@ def test_ragged_multi_sequence_and_shared_prefix():
     run.close()
 
 
-def test_many_sequences_ring_uploads_and_multi_tile_selection():
-    """80 sequences of 1..499 tokens in every call: the decode set (more than
-    63 entries) and the step append (more than 16) travel through the upload
-    ring instead of kernel parameters, and the ~1,300 records take the
-    two-kernel (count, then scatter) selection; 3 steps against the full
-    oracle, listed ids and gathered pages checked."""
-    rng = np.random.default_rng(0x6B76 + 80)
-    lens = tuple(int(x) for x in rng.integers(1, 500, size=80))
+@pytest.mark.parametrize("nseq,max_len", [(80, 500), (K.KVS_MAX_CALL_SEQS, 140)])
+def test_many_sequences_ring_uploads_and_multi_tile_selection(nseq, max_len):
+    """80 sequences of 1..499 tokens, and the most one call takes (256) of
+    1..139 tokens, in every call: the decode set (more than 63 entries) and the
+    step append (more than 16) travel through the upload ring instead of
+    kernel parameters, and the 1,000+ records take the two-kernel (count,
+    then scatter) selection; 3 steps against the full oracle, listed ids and
+    gathered pages checked."""
+    rng = np.random.default_rng(0x6B76 + nseq)
+    lens = tuple(int(x) for x in rng.integers(1, max_len, size=nseq))
     pool = sum((n + 4 + 15) // 16 for n in lens) + 8
     wl = W.workload("tiny", prefill_lens=lens, pool_pages=pool, steps=3, skew=True)
     assert sum((n + wl.steps + 15) // 16 for n in lens) > 1024
@@ -110,7 +112,7 @@ def test_many_sequences_ring_uploads_and_multi_tile_selection():
         summ = run.compare(res)
         _check_gather(run, res, host)
     run.ctx.check_device()
-    print("80 sequences", summ)
+    print(nseq, "sequences", summ)
     run.close()
 
 
