@@ -482,6 +482,20 @@ int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads,
 #define KVS_FAULT_WAIT 2u
 int kvs_debug_inject(uint32_t faults, uint32_t wait_limit_ms);
 
+/* Test hook, process-wide, no GPU needed (the pages have no counterpart): the
+ * decode work-item plan the library uses for one call.  Sequence i of the n
+ * has nres[i] blocks in each of its num_layers x num_kv_heads streams;
+ * `workers` decode warps claim the items; at most parts_cap chunk partials
+ * may be used, extra_parts of them already taken.  A stream of m blocks is
+ * cut into nbig = (m > tail ? (m - tail) / big : 0) chunks of `big` blocks
+ * followed by chunks of `small` blocks (the last one shorter), claimed
+ * chunk by chunk.  *big = 0 when no plan fits parts_cap.  KVS_EINVAL for
+ * null pointers, n == 0, or zero layers, heads or workers. */
+int kvs_debug_chunk_plan(const uint32_t *nres, uint32_t n, uint32_t num_layers,
+                         uint32_t num_kv_heads, uint32_t workers, uint64_t parts_cap,
+                         uint64_t extra_parts, uint32_t *big, uint32_t *small,
+                         uint32_t *tail);
+
 /* Kernels this context has launched so far (every kernel of the library,
  * counted at launch). */
 uint64_t kvs_kernel_launches(const kvs_ctx_t *ctx);

@@ -118,6 +118,9 @@ _SIGS = {
     "kvs_step_count": (c_u64, [c_vp]),
     "kvs_kernel_launches": (c_u64, [c_vp]),
     "kvs_debug_inject": (ctypes.c_int, [c_u32, c_u32]),
+    "kvs_debug_chunk_plan": (ctypes.c_int, [ctypes.POINTER(c_u32), c_u32, c_u32, c_u32, c_u32, c_u64, c_u64,
+                                            ctypes.POINTER(c_u32), ctypes.POINTER(c_u32),
+                                            ctypes.POINTER(c_u32)]),
     "kvs_free_pages": (c_u32, [c_vp]),
     "kvs_check_device": (ctypes.c_int, [c_vp, c_vp]),
 }
@@ -181,6 +184,18 @@ KVS_FAULT_HOSTALLOC, KVS_FAULT_WAIT = 1, 2
 def debug_inject(faults: int = 0, wait_limit_ms: int = 0) -> None:
     """Test hook (process-wide): injected host-side failures; (0, 0) clears."""
     _check(None, lib().kvs_debug_inject(faults, wait_limit_ms))
+
+
+def debug_chunk_plan(nres, num_layers: int, num_kv_heads: int, workers: int, parts_cap: int,
+                     extra_parts: int = 0):
+    """Test hook: the decode work-item plan (big, small, tail) of a call whose
+    sequences have nres[i] blocks per stream (see kvs_debug_chunk_plan)."""
+    arr = (c_u32 * len(nres))(*nres)
+    big, small, tail = c_u32(), c_u32(), c_u32()
+    _check(None, lib().kvs_debug_chunk_plan(arr, len(nres), num_layers, num_kv_heads, workers, parts_cap,
+                                            extra_parts, ctypes.byref(big), ctypes.byref(small),
+                                            ctypes.byref(tail)))
+    return big.value, small.value, tail.value
 
 
 def kvs_required_sizes(cfg: kvs_config) -> kvs_sizes:

@@ -1929,6 +1929,19 @@ int kvs_debug_set_mass(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, c
                      "copy mass");
 }
 
+int kvs_debug_chunk_plan(const uint32_t *nres, uint32_t n, uint32_t num_layers, uint32_t num_kv_heads,
+                         uint32_t workers, uint64_t parts_cap, uint64_t extra_parts, uint32_t *big,
+                         uint32_t *small, uint32_t *tail)
+{
+    if (!nres || !big || !small || !tail || n == 0 || !num_layers || !num_kv_heads || !workers)
+        return KVS_EINVAL;
+    const PageChunks pc = pick_page_chunks(nres, n, num_layers, num_kv_heads, workers, parts_cap, extra_parts);
+    *big = pc.big;
+    *small = pc.small;
+    *tail = pc.tail;
+    return KVS_OK;
+}
+
 int kvs_debug_advance(kvs_ctx_t *ctx, uint64_t steps)
 {
     KVS_RANGE();
