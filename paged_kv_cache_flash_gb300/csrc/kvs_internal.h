@@ -16,7 +16,7 @@ constexpr int kBlockTokens = 16;
 constexpr uint32_t kMaxChunk = 128;   // blocks per decode work item (split-K chunk): at most
 constexpr uint32_t kMinChunk = 16;    //   ... and at least
 constexpr int kMaxGroup = 8;          // query heads per KV head handled by one warp
-constexpr int kStages = 6;            // deepest TMA ring per warp (bf16: 6 x 8 KiB)
+constexpr int kStages = 6;            // mbarriers reserved per warp (rings use 3 (bf16) or 4 (FP8))
 constexpr int kMaxCallSeqs = KVS_MAX_CALL_SEQS;
 
 // Device error word bits (set by kernels, read by kvs_check_device).
