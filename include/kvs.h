@@ -332,9 +332,13 @@ int kvs_set_alpha(kvs_ctx_t *ctx, double alpha);
  *   LRFU   : as LOWFRAC with the order-preserving key of [RETR] s.3,
  *            K = ln(lrfu) + last_touch * (-ln(1 - alpha)) (-inf when lrfu
  *            is 0), in place of P: the records whose lazily decayed LRFU
- *            score is smallest at any step (the device's log, so keys equal
- *            to within an ulp may order either way).  KVS_EINVAL if
- *            alpha >= 1.
+ *            score is smallest at any step.  Both logarithms come from the
+ *            series ln x = e ln2 + 2 artanh(s), x = m 2^e with m in
+ *            [sqrt(1/2), sqrt(2)), s = (m-1)/(m+1), the odd powers of s up
+ *            to s^23 by Horner's rule, each step one round-to-nearest fp64
+ *            operation in that order (no fused multiply-add), so that keys
+ *            and their order are reproducible bit for bit off the device.
+ *            KVS_EINVAL if alpha >= 1.
  * A page is eligible when every record that references it is in the list
  * (a shared page is released only by its last user); each eligible page is
  * gathered once, at the position of its first record.  Default: eligible
@@ -423,6 +427,14 @@ int kvs_debug_advance(kvs_ctx_t *ctx, uint64_t steps);
 int kvs_export_records(kvs_ctx_t *ctx, uint64_t seq_id, void *host_dst,
                        size_t host_bytes, void *stream);
 
+/* Test hook (the pages have no counterpart): overwrites the records of one
+ * sequence with host_src (block order, 64 B each, exactly all its blocks),
+ * so that selection can be driven from planted records.  Every record must
+ * carry the sequence's key (seq_id, block index): KVS_EINVAL otherwise, and
+ * for a size other than 64 * blocks.  Synchronising. */
+int kvs_debug_import_records(kvs_ctx_t *ctx, uint64_t seq_id, const void *host_src,
+                             size_t host_bytes, void *stream);
+
 /* Host view of a sequence: its slot (row of the table, records and mass
  * buffers), token count, block count, and (if table_out is not NULL) up to
  * table_cap page ids (-1 = demoted, KVS_TABLE_GROUP(g) = held in 2-bit group
@@ -454,6 +466,16 @@ int kvs_set_decode_events(kvs_ctx_t *ctx, void *ev_start, void *ev_stop);
  * 8-KV-head, d=128 shape the limit is 12,288 tokens).  Nothing is allocated:
  * no cudaMalloc, cudaFree or allocating library routine.
  *
+ * status (optional, device, 2 x uint32, 4-byte aligned, caller-owned):
+ * written in stream order after the outputs with the kernels' error word
+ * (bit 0: a block-table entry outside [0, pool_blocks) -- demoted or 2-bit
+ * entries included -- was read; the kernel used page 0 in its place, so out
+ * and mass are not valid; bit 1: a wait for a TMA copy ran out) and the
+ * first offending table value or-ed with 0x80000000 (0: none).  {0, 0}:
+ * out and mass are valid.  With
+ * status NULL such a problem goes unreported (the call still returns KVS_OK
+ * once its work is enqueued).
+ *
  * The first call on a device (with that device current) looks up the array's
  * device address and the decode kernel's occupancy; make that first call
  * before any stream capture.  Every call shares the array: calls that overlap
@@ -464,8 +486,8 @@ int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads,
                        uint32_t num_kv_heads, uint32_t head_dim,
                        const void *pool, uint32_t pool_blocks,
                        const int32_t *block_table, uint32_t n_tokens,
-                       const void *q, float *out, float *mass, void *stream,
-                       char *msg, size_t msg_bytes);
+                       const void *q, float *out, float *mass, uint32_t *status,
+                       void *stream, char *msg, size_t msg_bytes);
 
 /* Test hook, process-wide (the pages have no counterpart): injects host-side
  * failures so that error paths can be exercised without a GPU fault.

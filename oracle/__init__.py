@@ -473,14 +473,51 @@ def lrfu_decayed(S_touch, t_touch, t: int, alpha: float) -> np.ndarray:
     return np.asarray(S_touch, np.float64) * lrfu_decay(alpha, np.int64(t) - np.asarray(t_touch, np.int64))
 
 
+# the double nearest ln 2, and the double nearest sqrt(1/2)
+LN2 = float.fromhex("0x1.62e42fefa39efp-1")
+SQRT_HALF = float.fromhex("0x1.6a09e667f3bcdp-1")
+LN_SERIES_TERMS = 12      # odd powers s^1 .. s^23
+
+
+def ln_series(x) -> np.ndarray:
+    """Natural logarithm of positive normal fp64 values from its series
+    definition: x = m * 2^e with m in [sqrt(1/2), sqrt(2)) (m from frexp,
+    doubled below sqrt(1/2)); s = (m - 1)/(m + 1), z = s*s;
+    ln m = 2 artanh(s) = 2 s (1 + z/3 + z^2/5 + ... + z^11/23), the
+    bracket by Horner's rule from the 1/23 term down (h = 1/d + z*h);
+    ln x = e*ln2 + ln m.  |s| < 0.172, so the series is cut where its next
+    term is below 1e-20 of the first.  Every step is one IEEE fp64 operation
+    (no fused multiply-add), so any program taking the same steps gets the
+    same bits: the logarithm in the LRFU key must order near-equal keys the
+    same way wherever it is evaluated.  (The series: Abramowitz and Stegun,
+    Handbook of Mathematical Functions, 4.1.27.)"""
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)
+    low = m < SQRT_HALF
+    m = np.where(low, m * 2.0, m)
+    e = np.where(low, e - 1, e).astype(np.float64)
+    s = (m - 1.0) / (m + 1.0)
+    z = s * s
+    h = np.full(x.shape, 1.0 / (2 * LN_SERIES_TERMS - 1))
+    for d in range(2 * LN_SERIES_TERMS - 3, 0, -2):
+        h = (1.0 / d) + z * h
+    return e * LN2 + 2.0 * (s * h)
+
+
+def lrfu_slope(alpha: float) -> float:
+    """-ln(1 - alpha), by ln_series: the key's growth per step of t_touch."""
+    return float(-ln_series(np.float64(1.0) - np.float64(alpha)))
+
+
 def lrfu_key(S_touch, t_touch, alpha: float) -> np.ndarray:
     """[RETR] s.3 order-preserving key K = ln S_touch + t_touch*(-ln(1-alpha)):
     ln of the decayed score at any t is K + t*ln(1-alpha), so K orders the
-    blocks as the decayed score does, at every t (-inf for S_touch = 0)."""
+    blocks as the decayed score does, at every t (-inf for S_touch = 0).
+    Both logarithms by ln_series; the sum and product in fp64 as written."""
     S = np.asarray(S_touch, np.float64)
-    with np.errstate(divide="ignore"):
-        lnS = np.log(S)
-    return lnS + np.asarray(t_touch, np.float64) * -np.log1p(-np.float64(alpha))
+    pos = S > 0
+    lnS = np.where(pos, ln_series(np.where(pos, S, 1.0)), -np.inf)
+    return lnS + np.asarray(t_touch, np.float64) * lrfu_slope(alpha)
 
 
 def recency(t: int, last_touch: np.ndarray, W: int) -> np.ndarray:

@@ -110,11 +110,12 @@ _SIGS = {
     "kvs_debug_set_mass": (ctypes.c_int, [c_vp, ctypes.POINTER(c_u64), c_u32, c_vp, c_vp]),
     "kvs_debug_advance": (ctypes.c_int, [c_vp, c_u64]),
     "kvs_export_records": (ctypes.c_int, [c_vp, c_u64, c_vp, c_sz, c_vp]),
+    "kvs_debug_import_records": (ctypes.c_int, [c_vp, c_u64, c_vp, c_sz, c_vp]),
     "kvs_seq_info": (ctypes.c_int, [c_vp, c_u64, ctypes.POINTER(c_u32), ctypes.POINTER(c_u32),
                                     ctypes.POINTER(c_u32), ctypes.POINTER(c_i32), c_u32]),
     "kvs_set_decode_events": (ctypes.c_int, [c_vp, c_vp, c_vp]),
     "kvs_decode_noalloc": (ctypes.c_int, [c_u32, c_u32, c_u32, c_u32, c_vp, c_u32, c_vp, c_u32,
-                                          c_vp, c_vp, c_vp, c_vp, ctypes.c_char_p, c_sz]),
+                                          c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_char_p, c_sz]),
     "kvs_step_count": (c_u64, [c_vp]),
     "kvs_kernel_launches": (c_u64, [c_vp]),
     "kvs_debug_inject": (ctypes.c_int, [c_u32, c_u32]),
@@ -404,6 +405,13 @@ class Context:
         _check(self.h, lib().kvs_export_records(self.h, seq_id, out.ctypes.data, nb * 64,
                                                 _stream_handle(stream)))
         return out[:nb]
+
+    def debug_import_records(self, seq_id, recs: np.ndarray, stream=None):
+        """Test hook: overwrites the sequence's records (RECORD_DTYPE, block order)."""
+        recs = np.ascontiguousarray(recs)
+        assert recs.dtype.itemsize == 64
+        _check(self.h, lib().kvs_debug_import_records(self.h, seq_id, recs.ctypes.data, recs.nbytes,
+                                                      _stream_handle(stream)))
 
     def seq_info(self, seq_id):
         """(slot, n_tokens, n_blocks, table)"""

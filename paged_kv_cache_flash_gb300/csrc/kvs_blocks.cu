@@ -306,15 +306,60 @@ __device__ __forceinline__ const kvs_record &rec_at(const Geo &g, const DSet *ds
     return recs[static_cast<size_t>(sq.slot) * g.mb + b];
 }
 
+// Natural logarithm of a positive normal double from its series definition
+// (Abramowitz and Stegun, Handbook of Mathematical Functions, 4.1.27):
+// x = m 2^e with m in [sqrt(1/2), sqrt(2)); s = (m - 1)/(m + 1), z = s*s;
+// ln m = 2 artanh(s) = 2 s (1 + z/3 + z^2/5 + ... + z^11/23), the bracket by
+// Horner's rule from the 1/23 term down; ln x = e ln2 + ln m.  |s| < 0.172,
+// so the cut-off term is below 1e-20 of the first.  Each step is one
+// correctly rounded fp64 operation in a fixed order (explicit round-to-nearest
+// intrinsics, no fused multiply-add), so the same steps give the same bits on
+// any IEEE machine: near-equal LRFU keys then order the same way everywhere.
+__device__ __forceinline__ double ln_series(double x)
+{
+    constexpr double kLn2 = 0x1.62e42fefa39efp-1;        // the double nearest ln 2
+    constexpr double kSqrtHalf = 0x1.6a09e667f3bcdp-1;   // the double nearest sqrt(1/2)
+    const long long bits = __double_as_longlong(x);
+    int e = static_cast<int>((bits >> 52) & 0x7ff) - 1022;              // x = m 2^e, m in [1/2, 1)
+    double m = __longlong_as_double((bits & 0x000fffffffffffffLL) | 0x3fe0000000000000LL);
+    if (m < kSqrtHalf) {
+        m = __dmul_rn(m, 2.0);
+        e -= 1;
+    }
+    const double s = __ddiv_rn(__dsub_rn(m, 1.0), __dadd_rn(m, 1.0));
+    const double z = __dmul_rn(s, s);
+    double h = 1.0 / 23.0;
+    h = __dadd_rn(1.0 / 21.0, __dmul_rn(z, h));
+    h = __dadd_rn(1.0 / 19.0, __dmul_rn(z, h));
+    h = __dadd_rn(1.0 / 17.0, __dmul_rn(z, h));
+    h = __dadd_rn(1.0 / 15.0, __dmul_rn(z, h));
+    h = __dadd_rn(1.0 / 13.0, __dmul_rn(z, h));
+    h = __dadd_rn(1.0 / 11.0, __dmul_rn(z, h));
+    h = __dadd_rn(1.0 / 9.0, __dmul_rn(z, h));
+    h = __dadd_rn(1.0 / 7.0, __dmul_rn(z, h));
+    h = __dadd_rn(1.0 / 5.0, __dmul_rn(z, h));
+    h = __dadd_rn(1.0 / 3.0, __dmul_rn(z, h));
+    h = __dadd_rn(1.0, __dmul_rn(z, h));
+    return __dadd_rn(__dmul_rn(static_cast<double>(e), kLn2), __dmul_rn(2.0, __dmul_rn(s, h)));
+}
+
+// Slope of the LRFU key per step of the touch time: -ln(1 - alpha).
+__device__ __forceinline__ double lrfu_slope(double alpha)
+{
+    return -ln_series(__dsub_rn(1.0, alpha));
+}
+
 // 64-bit order key of a record for LOWFRAC (P >= 0: its bits order like P)
-// and LRFU (K = ln lrfu + last_touch * c with c = -ln(1 - alpha), mapped to
-// bits that order like K: negative values complemented, others with the
-// top bit set).
+// and LRFU (K = ln lrfu + last_touch * c with c = lrfu_slope(alpha), -inf
+// for a block never touched, mapped to bits that order like K: negative
+// values complemented, others with the top bit set).
 __device__ __forceinline__ uint64_t sel_key(int mode, const kvs_record &rec, double c)
 {
     if (mode != KVS_SELECT_LRFU)
         return static_cast<uint64_t>(__double_as_longlong(rec.prio));
-    const double K = __dadd_rn(log(rec.lrfu), __dmul_rn(static_cast<double>(rec.last_touch), c));
+    const double K = rec.lrfu > 0.0
+                         ? __dadd_rn(ln_series(rec.lrfu), __dmul_rn(static_cast<double>(rec.last_touch), c))
+                         : -__longlong_as_double(0x7ff0000000000000LL);
     const uint64_t u = static_cast<uint64_t>(__double_as_longlong(K));
     return (u >> 63) ? ~u : (u | (uint64_t(1) << 63));
 }
@@ -331,9 +376,10 @@ __device__ __forceinline__ bool picked(int mode, const kvs_record &rec, uint32_t
 
 // Counts picked records per tile of kSelTile records.
 __global__ void __launch_bounds__(kSelThreads)
-    select_count_kernel(const Geo g, const Work w, const kvs_record *recs, int mode, double lrfu_c,
+    select_count_kernel(const Geo g, const Work w, const kvs_record *recs, int mode, double alpha,
                         uint32_t nb_total)
 {
+    const double lrfu_c = mode == KVS_SELECT_LRFU ? lrfu_slope(alpha) : 0.0;
     __shared__ uint32_t wsum[kSelThreads / 32];
     const DSet *ds = w.dset;
     size_t idx[kSelPerThread];
@@ -367,9 +413,10 @@ __global__ void __launch_bounds__(kSelThreads)
 // entries) and, through its device mapping, a host word for the count.
 __global__ void __launch_bounds__(kSelThreads)
     select_scatter_kernel(const Geo g, const Work w, const kvs_record *recs, const int32_t *table,
-                          int mode, double lrfu_c, uint32_t nb_total, uint32_t ntiles, uint32_t count_pages,
+                          int mode, double alpha, uint32_t nb_total, uint32_t ntiles, uint32_t count_pages,
                           const SelectOut out)
 {
+    const double lrfu_c = mode == KVS_SELECT_LRFU ? lrfu_slope(alpha) : 0.0;
     __shared__ uint32_t wpre[kSelThreads / 32];
     __shared__ uint32_t base_sh;
     const DSet *ds = w.dset;
@@ -461,8 +508,9 @@ __global__ void __launch_bounds__(kSelThreads)
 // by an 8-bit radix descent over the 96-bit key.  One block of 1024 threads.
 __global__ void __launch_bounds__(1024)
     radix_select_kernel(const Geo g, const Work w, const kvs_record *recs, uint32_t nb_total,
-                        uint32_t k, int mode, double c)
+                        uint32_t k, int mode, double alpha)
 {
+    const double c = mode == KVS_SELECT_LRFU ? lrfu_slope(alpha) : 0.0;
     __shared__ uint32_t hist[256];
     __shared__ uint64_t pre_p;
     __shared__ uint32_t pre_r;
@@ -1044,23 +1092,23 @@ cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const flo
 }
 
 cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *rec,
-                                uint32_t nb_total, uint32_t k, int mode, double c, cudaStream_t s)
+                                uint32_t nb_total, uint32_t k, int mode, double alpha, cudaStream_t s)
 {
-    return launch_pdl(radix_select_kernel, dim3(1), dim3(1024), 0, s, g, w, rec, nb_total, k, mode, c);
+    return launch_pdl(radix_select_kernel, dim3(1), dim3(1024), 0, s, g, w, rec, nb_total, k, mode, alpha);
 }
 
 cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table,
-                          int mode, double c, uint32_t nb_total, bool count_pages, const SelectOut &out,
+                          int mode, double alpha, uint32_t nb_total, bool count_pages, const SelectOut &out,
                           cudaStream_t s)
 {
     const uint32_t ntiles = (nb_total + kSelTile - 1) / kSelTile;
     if (ntiles > 1) {           // one tile counts itself in the scatter kernel
         cudaError_t e = launch_pdl(select_count_kernel, dim3(ntiles), dim3(kSelThreads), 0, s, g, w, rec, mode,
-                                   c, nb_total);
+                                   alpha, nb_total);
         if (e != cudaSuccess)
             return e;
     }
-    return launch_pdl(select_scatter_kernel, dim3(ntiles), dim3(kSelThreads), 0, s, g, w, rec, table, mode, c,
+    return launch_pdl(select_scatter_kernel, dim3(ntiles), dim3(kSelThreads), 0, s, g, w, rec, table, mode, alpha,
                       nb_total, ntiles, count_pages ? 1u : 0u, out);
 }
 

@@ -1344,15 +1344,14 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         ctx->refcnt_dirty = false;
     }
     bool run = true;
-    // LRFU key slope: -ln(1 - alpha)
-    const double lrfu_c = -std::log1p(-ctx->cfg.alpha);
+    const double alpha = ctx->cfg.alpha;     // LRFU: the kernels take the key's slope from it
     if (args->mode != KVS_SELECT_THRESH) {
         const uint32_t k = static_cast<uint32_t>(std::floor(args->frac * static_cast<double>(N)));
         if (k == 0)
             run = false;
         else if ((rc = launch_rc(ctx,
                                  launch_radix_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
-                                                     N, k, args->mode, lrfu_c, s),
+                                                     N, k, args->mode, alpha, s),
                                  "radix select")))
             return rc;
     }
@@ -1372,7 +1371,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             sel_out.count_host = ctx->async_hdr_dev;
         if ((rc = launch_rc(ctx,
                             launch_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
-                                          static_cast<const int32_t *>(ctx->buf.block_table), args->mode, lrfu_c,
+                                          static_cast<const int32_t *>(ctx->buf.block_table), args->mode, alpha,
                                           N, !ctx->geo.kivi, sel_out, s),
                             "select", select_launches(N))))
             return rc;
@@ -1970,6 +1969,33 @@ int kvs_export_records(kvs_ctx_t *ctx, uint64_t seq_id, void *host_dst, size_t h
     }
     if (n < want)
         return fail(ctx, KVS_ETRUNC, "host buffer holds %zu of %zu records", n / 64, nb);
+    return KVS_OK;
+}
+
+int kvs_debug_import_records(kvs_ctx_t *ctx, uint64_t seq_id, const void *host_src, size_t host_bytes,
+                             void *stream)
+{
+    KVS_RANGE();
+    if (!ctx || !host_src)
+        return KVS_EINVAL;
+    uint32_t slot;
+    SeqState *s = find_seq(ctx, seq_id, &slot);
+    if (!s)
+        return fail(ctx, KVS_ENOTFOUND, "unknown sequence %llu", (unsigned long long)seq_id);
+    const size_t nb = s->table.size();
+    if (host_bytes != nb * sizeof(kvs_record))
+        return fail(ctx, KVS_EINVAL, "expected %zu records (%zu bytes), got %zu bytes", nb,
+                    nb * sizeof(kvs_record), host_bytes);
+    const kvs_record *src = static_cast<const kvs_record *>(host_src);
+    for (size_t b = 0; b < nb; ++b)
+        if (src[b].key.seq_id != seq_id || src[b].key.block_idx != b)
+            return fail(ctx, KVS_EINVAL, "record %zu carries key (%llu, %llu)", b,
+                        (unsigned long long)src[b].key.seq_id, (unsigned long long)src[b].key.block_idx);
+    if (nb) {
+        CU(cudaMemcpyAsync(static_cast<kvs_record *>(ctx->buf.records) + static_cast<size_t>(slot) * ctx->cfg.max_blocks_per_seq,
+                           host_src, host_bytes, cudaMemcpyHostToDevice, S(stream)));
+        WAIT(S(stream));
+    }
     return KVS_OK;
 }
 

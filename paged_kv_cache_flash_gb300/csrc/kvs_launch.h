@@ -24,10 +24,12 @@ cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_to
 cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const float *mass,
                          double alpha, uint32_t W, double wR, double wE, double wN,
                          double lo, double hi, uint32_t nb_total, cudaStream_t s);
+// alpha: the EMA weight (LRFU mode: the key's slope -ln(1 - alpha) is taken
+// on the device, by the same fixed sequence of fp64 operations as the key)
 cudaError_t launch_radix_select(const Geo &g, const Work &w, const kvs_record *rec,
-                                uint32_t nb_total, uint32_t k, int mode, double c, cudaStream_t s);
+                                uint32_t nb_total, uint32_t k, int mode, double alpha, cudaStream_t s);
 cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table,
-                          int mode, double c, uint32_t nb_total, bool count_pages, const SelectOut &out,
+                          int mode, double alpha, uint32_t nb_total, bool count_pages, const SelectOut &out,
                           cudaStream_t s);
 uint32_t select_launches(uint32_t nb_total);   // kernels launch_select issues
 cudaError_t launch_plan(const Work &w, uint32_t mirror, const SelectOut &out, cudaStream_t s);

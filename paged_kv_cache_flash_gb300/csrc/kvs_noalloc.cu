@@ -16,6 +16,11 @@
 // is cleared at the start of each call; the rest is fully written before it
 // is read.  Two calls whose work overlaps on the GPU (different streams, no
 // ordering between them) race on the array: order them.
+//
+// The kernels' error word (a block-table entry outside the pool, replaced by
+// page 0 before any access; a TMA wait that ran out) lives in the array too;
+// a caller that passes `status` gets it, with the first offending value,
+// copied there in stream order after the outputs.
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
@@ -54,7 +59,7 @@ int say(char *msg, size_t n, int code, const char *text)
 extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uint32_t num_kv_heads,
                                   uint32_t head_dim, const void *pool, uint32_t pool_blocks,
                                   const int32_t *block_table, uint32_t n_tokens, const void *q,
-                                  float *out, float *mass, void *stream, char *msg,
+                                  float *out, float *mass, uint32_t *status, void *stream, char *msg,
                                   size_t msg_bytes)
 {
     using namespace kvs;
@@ -147,9 +152,12 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
     w.lse_blk = reinterpret_cast<float *>(base + off_lb);
     w.stream_mass = reinterpret_cast<float *>(base + off_sm);
 
-    // the one-sequence decode set
-    DSet ds;
-    std::memset(&ds, 0, sizeof ds);
+    // the one-sequence decode set: header and one entry, sent in a kernel's
+    // parameters (no copy-engine operation, no host buffer to keep alive)
+    alignas(16) uint8_t set_bytes[kSetInlineBytes];
+    static_assert(offsetof(DSet, seq) + sizeof(DSeq) <= kSetInlineBytes, "one-entry set fits the parameters");
+    std::memset(set_bytes, 0, sizeof set_bytes);
+    DSet &ds = *reinterpret_cast<DSet *>(set_bytes);
     ds.nseq = 1;
     ds.nb_total = nb;
     ds.n_items = g.L * g.Hkv * nchunk;
@@ -194,13 +202,15 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
         }                                                                     \
     } while (0)
     NA_CHECK(cudaMemsetAsync(base + off_hdr, 0, 256, s));
-    NA_CHECK(cudaMemcpyAsync(w.dset, &ds, sizeof ds, cudaMemcpyHostToDevice, s));
+    NA_CHECK(launch_set(&ds, dset_bytes(1), w.dset, s));
     const int grid = static_cast<int>(std::min<uint32_t>((ds.n_items + wg - 1) / wg,
                                                          static_cast<uint32_t>(grid_per_sm)));
     NA_CHECK(launch_decode(g, tmap, w, static_cast<const uint16_t *>(q), block_table, ds.n_items, wg,
                            grid, s));
     NA_CHECK(launch_combine(g, w, out, 1, nb, nchunk, s));
     NA_CHECK(launch_mass(g, w, mass, nb, s));
+    if (status)     // error word and its first offending value, after the outputs
+        NA_CHECK(cudaMemcpyAsync(status, w.err, 2 * sizeof(uint32_t), cudaMemcpyDeviceToDevice, s));
 #undef NA_CHECK
     return KVS_OK;
 }

@@ -547,6 +547,67 @@ def test_lrfu_key_orders_like_decayed_score_at_every_time():
     assert O.lrfu_key(np.array([0.0]), np.array([5]), alpha)[0] == -np.inf
 
 
+def _ulps(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return np.abs(a - b) / np.spacing(np.maximum(np.abs(a), np.abs(b)))
+
+
+def test_ln_series_closed_forms_and_library_log():
+    # the constants are the doubles nearest ln 2 and sqrt(1/2)
+    assert O.LN2 == 0.6931471805599453 and abs(O.LN2 - math.log(2.0)) == 0.0
+    assert O.SQRT_HALF == math.sqrt(0.5)
+    # m = 1 leaves the series out: ln 2^k = k * ln2, one rounding
+    for k in (-60, -7, -1, 0, 1, 3, 52, 300):
+        assert O.ln_series(np.float64(2.0) ** k)[()] == np.float64(k) * O.LN2
+    assert O.ln_series(1.0)[()] == 0.0
+    # within a few ulps of the library logarithm over many decades, and on
+    # [alpha, 1], where LRFU scores live
+    rng = np.random.default_rng(40)
+    x = np.exp(rng.uniform(-700.0, 700.0, 100000))
+    assert _ulps(O.ln_series(x), np.log(x)).max() <= 4
+    x = rng.uniform(0.01, 1.0, 100000)
+    assert _ulps(O.ln_series(x), np.log(x)).max() <= 4
+    # the split at sqrt(1/2): both sides of it, and values next to 1
+    for v in (O.SQRT_HALF, np.nextafter(O.SQRT_HALF, 0), np.nextafter(1.0, 0), np.nextafter(1.0, 2)):
+        assert _ulps(O.ln_series(v), np.log(v)) <= 4
+    # the slope is ln of 1 - alpha rounded to fp64: that rounding (half an
+    # ulp of 1) grows by 1/alpha in the logarithm, so small alpha loses a few
+    # more ulps against log1p, which never forms 1 - alpha
+    for a in (0.01, 0.05, 0.15, 0.5):
+        assert _ulps(O.lrfu_slope(a), -np.log1p(-a)) <= 8
+
+
+def test_ln_series_catches_a_short_series(monkeypatch):
+    # a series cut after four terms is off by far more than the bound above
+    monkeypatch.setattr(O, "LN_SERIES_TERMS", 4)
+    x = np.random.default_rng(41).uniform(0.01, 1.0, 1000)
+    assert _ulps(O.ln_series(x), np.log(x)).max() > 100
+
+
+def test_lrfu_keys_of_equal_decayed_scores_agree_to_a_few_ulps():
+    # [RETR] s.3: K is order-preserving because ln S_touch + t_touch*c does
+    # not change along a decay path: a block touched at t with score S and
+    # one touched at t + d with score S*(1-alpha)^d have the same key up to
+    # rounding (a wrong slope sign or a dropped term moves it by ~d*c)
+    rng = np.random.default_rng(42)
+    for alpha in (0.01, 0.05, 0.15):
+        S = rng.uniform(0.3, 1.0, 2000)
+        t = rng.integers(0, 100, 2000)
+        d = rng.integers(1, 60, 2000)
+        K1 = O.lrfu_key(S, t, alpha)
+        K2 = O.lrfu_key(S * O.lrfu_decay(alpha, d), t + d, alpha)
+        # absolute: K sums terms of opposite sign (ln S < 0, t*c > 0), so its
+        # own ulp says nothing; 1e-12 is a few ulps of the terms (|t*c| < 20)
+        assert np.abs(K1 - K2).max() < 1e-12 and np.count_nonzero(K1 != K2) > 0
+    # near-equal keys order by (key, record order) in the selection
+    recs = O.new_records(7, 0, 6, 0)
+    recs["last_touch"] = [10, 11, 12, 13, 14, 15]
+    recs["lrfu"] = 0.9 * O.lrfu_decay(0.15, recs["last_touch"].astype(np.int64) - 10)
+    K = O.lrfu_key(recs["lrfu"], recs["last_touch"], 0.15)
+    want = sorted(range(6), key=lambda i: (float(K[i]), i))[:3]
+    assert O.select_lrfu({7: recs}, 0.5, 0.15) == [(7, i) for i in sorted(want)]
+
+
 def _lrfu_recs(rng, nseq=3, nb=60, T=120, alpha=0.15):
     out = {}
     for s in range(nseq):
