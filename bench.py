@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-literal", action="store_true")
+    ap.add_argument("--no-batched", action="store_true",
+                    help="128K workload only: skip the batched workload's line under \"batched\"")
     ap.add_argument("--cpu-layers", type=int, default=8,
                     help="layers of the workload in the CPU-baseline sample")
     return ap.parse_args()
@@ -470,27 +472,91 @@ def time_oracle(wl, q, K, V, layers, threads):
     return time.perf_counter() - t0
 
 
-def run_kvs(args):
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline_leg(wl, dev, layers, alpha, kv_bytes_step, pages_step):
+    """The oracle, as it stands, timed on this host's cores on bounded samples
+    of one step of the workload, and the whole step estimated from them:
+    attention + block mass (fp64, the C oracle) of sequence 0 on `layers` of
+    its layers with every core and on one layer with one thread, scaled to
+    all layers and sequences by tokens; then the scoring, THRESH selection
+    and gather plan of every record of the workload (numpy, one thread), and
+    the page assembly of 8 pages (scaled to the pages the path sends to the
+    host per step)."""
+    import numpy as np
+    import oracle as O
+    import workloads as W
+    n = wl.prefill_lens[0] + 1
+    q, Kc, Vc = cpu_sample(wl, n, layers, dev)
+    allc = os.cpu_count() or 1
+    t_all = time_oracle(wl, q, Kc, Vc, layers, allc) / layers
+    K1, V1 = Kc[:, :1].contiguous(), Vc[:, :1].contiguous()
+    t_one = time_oracle(wl, q[:1].contiguous(), K1, V1, 1, 1)
+    tok_total = sum(x + 1 for x in wl.prefill_lens)
+    attn_all = t_all * wl.L * tok_total / n
+    attn_one = t_one * wl.L * tok_total / n
+    B = wl.block_tokens
+    recs = {5000 - 17 * s: O.new_records(5000 - 17 * s, 0, (x + B) // B, 0)
+            for s, x in enumerate(wl.prefill_lens)}
+    masses = {sid: W.synthetic_masses(sid, len(r)).astype(np.float64) for sid, r in recs.items()}
+    t0 = time.perf_counter()
+    recs = {sid: O.score_update(r, masses[sid], 1, alpha, wl.recency_window, wl.weights, wl.cuts)
+            for sid, r in recs.items()}
+    t_score = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    ids = O.select_thresh(recs)
+    page_of = {k: k for k in ids}
+    O.gather_plan(ids, page_of, {k: {k} for k in ids})
+    t_select = time.perf_counter() - t0
+    npg = min(8, n // B)
+    t0 = time.perf_counter()
+    for b in range(npg):
+        O.assemble_page(Kc[b * B:(b + 1) * B], Vc[b * B:(b + 1) * B], B)
+    t_page = (time.perf_counter() - t0) / max(npg, 1) * wl.L / layers
+    rest = t_score + t_select + t_page * pages_step
+    step_all, step_one = attn_all + rest, attn_one + rest
+    return {"value": round(kv_bytes_step / step_all / 1e9, 4), "unit": UNIT, "cores": allc, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "single_thread": {"value": round(kv_bytes_step / step_one / 1e9, 4), "unit": UNIT, "cores": 1},
+            "step_estimate_s": {"all_cores": round(step_all, 3), "one_thread": round(step_one, 3)},
+            "parts_s": {"attention_per_layer_seq0_all_cores": round(t_all, 4),
+                        "attention_per_layer_seq0_one_thread": round(t_one, 4),
+                        "score_all_records": round(t_score, 4), "select_and_plan": round(t_select, 4),
+                        "page_assembly_per_page": round(t_page, 5), "pages_per_step": round(pages_step, 2)},
+            "sample": f"sequence 0 ({n} tokens): fp64 attention + block mass of layers 0..{layers - 1} "
+                      f"of {wl.L} on {allc} threads and of layer 0 on 1 thread, scaled by layers and "
+                      f"tokens to the step ({tok_total} tokens); scoring, THRESH selection and gather "
+                      f"plan of all {sum(len(r) for r in recs.values())} records; page assembly of "
+                      f"{npg} pages x the {pages_step:.1f} pages the path sends to host per step"}
+
+
+def measure(args, wname, dev, ws, rank, local, sub=False):
+    """Times K steps of one workload after W warm-up steps and returns the
+    JSON fields of its line (rank 0; None elsewhere).  sub: a second workload
+    of the same run -- no literal-gather, copy-rate or CPU-baseline legs."""
     import torch
     import workloads as W
-    from paged_kv_cache_flash_gb300 import build
-    build.build()
-    ws, rank, local = dist_info()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    wl = W.workload(args.workload)
+    wl = W.workload(wname)
     alpha = args.alpha if args.alpha is not None else wl.alphas[-1]
-    if args.gather == "auto":
-        args.gather = "ids" if args.kv_dtype == "kivi2" else ("demote" if wl.demote_every else "mirror")
+    gather = args.gather
+    if gather == "auto":
+        gather = "ids" if args.kv_dtype == "kivi2" else ("demote" if wl.demote_every else "mirror")
     K_, W_ = args.steps, args.warmup
     e2e_steps = 0 if args.no_e2e else K_
-    lit_steps = 0 if (args.no_literal or args.gather not in ("mirror", "mirror-sync", "list")) else 2
+    lit_steps = 0 if (sub or args.no_literal or gather not in ("mirror", "mirror-sync", "list")) else 2
     bd_steps = min(8, K_)
     total = W_ + K_ + bd_steps + e2e_steps + lit_steps
-    pipe = Pipeline(wl, alpha, total, dev, args.gather, args.kv_dtype, args.prefetch_budget, args.victims)
+    pipe = Pipeline(wl, alpha, total, dev, gather, args.kv_dtype, args.prefetch_budget, args.victims)
     pipe.prefill()
     kv, qs = pipe.inputs(1, W_ + K_)
 
@@ -526,7 +592,7 @@ def run_kvs(args):
         pipe.ctx.set_decode_events(dec[i][0], dec[i][1])
         pipe.last_round = 0
         r = pipe.step(kv[W_ + i], qs[W_ + i], ev[i], phases=False)
-        if pipe.last_round and args.gather == "demote":
+        if pipe.last_round and gather == "demote":
             rounds.append((i, pipe.last_round))
         kv_bytes += pipe.kv_bytes_this_step()
         decoded += len(pipe.active)
@@ -580,7 +646,7 @@ def run_kvs(args):
     algo = kv_bytes / K_ + wl.nseq * wl.L * wl.Hq * wl.d * 2 + sum(nb) * 4
     achieved = algo / (dec_avg / 1e3) / 1e9
     peak, peak_src = read_peaks()
-    traffic = read_traffic(args.workload, args.kv_dtype)
+    traffic = read_traffic(wname, args.kv_dtype)
 
     # ---- end to end through host buffers --------------------------------
     e2e = None
@@ -674,25 +740,18 @@ def run_kvs(args):
     # ---- the box's streaming copy rate in this session (context for the
     # roofline: MEASURED_PEAKS.json is the denominator; this shows what this
     # box moved today with a plain copy)
-    s_copy = session_copy_rate(torch, dev)
-    stream = {"copy_GBps": round(s_copy, 1), "decode_kernel_vs_copy": round(achieved / s_copy, 4),
-              "method": "torch copy_ of 4 GiB bf16 buffers, read + write bytes, median of 20 runs, "
-                        "CUDA events"}
+    stream = None
+    if not sub:
+        s_copy = session_copy_rate(torch, dev)
+        stream = {"copy_GBps": round(s_copy, 1), "decode_kernel_vs_copy": round(achieved / s_copy, 4),
+                  "method": "torch copy_ of 4 GiB bf16 buffers, read + write bytes, median of 20 runs, "
+                            "CUDA events"}
 
     # ---- CPU baseline: the oracle on a bounded sample --------------------
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        layers = min(args.cpu_layers, wl.L)
-        n = wl.prefill_lens[0] + 1
-        q, Kc, Vc = cpu_sample(wl, n, layers, dev)
-        threads = os.cpu_count() or 1
-        secs = time_oracle(wl, q, Kc, Vc, layers, threads)
-        sample_bytes = n * layers * wl.Hkv * wl.d * 2 * 2
-        cpu = {"value": round(sample_bytes / secs / 1e9, 4), "unit": UNIT, "cores": threads,
-               "kind": "oracle",
-               "sample": f"one decode step of sequence 0 ({n} tokens), layers 0..{layers - 1} "
-                         f"of {wl.L}, all {wl.Hq} query heads: fp64 attention + block mass, "
-                         f"{secs:.1f} s wall"}
+    if rank == 0 and ws == 1 and not sub and not args.no_cpu_baseline:
+        per_step_pages = staged / K_ if K_ else 0.0
+        cpu = cpu_baseline_leg(wl, dev, min(args.cpu_layers, wl.L), alpha, kv_bytes / K_, per_step_pages)
 
     if rank == 0:
         line = {
@@ -708,11 +767,11 @@ def run_kvs(args):
                                    f"tokens (+1 per step), L={wl.L} Hq={wl.Hq} Hkv={wl.Hkv} d={wl.d}, 16-token pages"
                                    + (f", {wl.shared_prefix_tokens}-token shared prefix" if wl.shared_prefix_tokens else ""),
                        "global_batch": wl.nseq, "seq_len": max(wl.prefill_lens),
-                       "alpha": alpha, "gather": args.gather,
+                       "alpha": alpha, "gather": gather,
                        "select_call": ("KVS_GATHER_ASYNC: no host wait; counts read one step later"
-                                       if args.gather in ("mirror", "ids") else "synchronising"),
-                       **({"prefetch_budget": args.prefetch_budget} if args.gather == "prefetch" else {}),
-                       **({"victims": args.victims} if args.gather in ("demote", "prefetch") else {}),
+                                       if gather in ("mirror", "ids") else "synchronising"),
+                       **({"prefetch_budget": args.prefetch_budget} if gather == "prefetch" else {}),
+                       **({"victims": args.victims} if gather in ("demote", "prefetch") else {}),
                        "l2": "inputs larger than L2 (KV per step >> 129 MB), no flush",
                        "parallelism": f"replicas x{ws}"},
             "decode_tok_per_s": round(tok_s, 2),
@@ -735,7 +794,7 @@ def run_kvs(args):
             "gathered_pages_timed": staged,
             "demoted_and_readmitted_pages_timed": demoted,
             "demote_readmit_rounds": round_info,
-            "prefetched_pages_timed": prefetched if args.gather == "prefetch" else None,
+            "prefetched_pages_timed": prefetched if gather == "prefetch" else None,
             "e2e": e2e,
             "literal_gather": literal,
             "cpu_baseline": cpu,
@@ -744,6 +803,39 @@ def run_kvs(args):
             "gpu_launches": launches,
             "wall_s_timed": round(wall, 3),
         }
+        if sub:
+            for k in ("literal_gather", "cpu_baseline", "copy_rate_session", "n_gpus", "metric", "unit",
+                      "higher_is_better", "scaling", "vs_baseline", "data", "dtype"):
+                line.pop(k, None)
+        pipe.ctx.close()
+        return line
+    pipe.ctx.close()
+    return None
+
+
+def run_kvs(args):
+    import torch
+    from paged_kv_cache_flash_gb300 import build
+    build.build()
+    ws, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    line = measure(args, args.workload, dev, ws, rank, local)
+    if args.workload == "l70b_128k" and not args.no_batched:
+        # the other workload the target names: the batched one, same steps,
+        # warm-up and page format, its own line under "batched"
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        if hasattr(torch._C, "_host_emptyCache"):
+            torch._C._host_emptyCache()     # the 128K run's pinned host mirror
+        sub = measure(args, "l70b_batch16", dev, ws, rank, local, sub=True)
+        if line is not None:
+            line["batched"] = sub
+    if rank == 0:
         print(json.dumps(line))
     if ws > 1:
         torch.distributed.destroy_process_group()
