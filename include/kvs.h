@@ -230,7 +230,10 @@ typedef struct kvs_gather_result {
 int kvs_required_sizes(const kvs_config *cfg, kvs_sizes *out);
 
 /* Creates a context over caller-allocated device buffers (sizes from
- * kvs_required_sizes, all on the current device).  Zeroes the block table,
+ * kvs_required_sizes, all on the current device): the block manager of
+ * [ARCH] -- a pool of fixed-size blocks handed out from a free list, a
+ * block table per sequence, reference counts for shared blocks -- whose
+ * bookkeeping the context holds on the host.  Zeroes the block table,
  * records and mass (synchronously) and builds the pool's TMA descriptor.
  * The free list holds every pool page in an order seeded by cfg->pool_seed. */
 int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out);

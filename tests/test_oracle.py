@@ -135,12 +135,17 @@ def test_single_token_and_partial_block():
 
 
 def test_skewed_inputs_put_most_mass_on_recent_tenth():
-    """The generator's recency boost (input shaping) does what it says."""
-    wl, q, K, V = _case("l70b_8k", 2048, L=2, prefill_lens=(2048,))
+    """The generator's recency boost (input shaping only) does what it says:
+    with the analytic c = ln 36 (0.1*36 / (0.1*36 + 0.9) = 80 %), the
+    step-1 block mass of the 8K workload's recent tenth is 0.780 on this
+    8-layer cut (0.782 over all 80 layers), its block 0 above the uniform
+    share."""
+    wl, q, K, V = _case("l70b_8k", 8192, L=8, prefill_lens=(8192,))
     r = O.decode_with_mass(q, K, V, L=wl.L, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, want_out=False)
     nb = len(r["mass"])
     recent = r["mass"][int(0.9 * nb):].sum()
-    assert 0.65 < recent < 0.92
+    assert abs(recent - 0.78) < 0.01
+    assert r["mass"][0] * nb > 1.0
 
 
 # ----------------------------------------------------------------- scoring
