@@ -63,6 +63,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-literal", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="decode and score in two calls (kvs_decode_step + kvs_score_update) instead of "
+                         "kvs_decode_score_step")
     ap.add_argument("--no-batched", action="store_true",
                     help="128K workload only: skip the batched workload's line under \"batched\"")
     ap.add_argument("--cpu-layers", type=int, default=8,
@@ -225,12 +228,13 @@ class Pipeline:
     """The hot path, driven through the public C ABI for a set of sequences."""
 
     def __init__(self, wl, alpha, steps_total, device, gather, kv_dtype="bf16", prefetch_budget=512,
-                 victims="lowfrac"):
+                 victims="lowfrac", fused=True):
         import torch
         import paged_kv_cache_flash_gb300 as K
         import workloads as W
         self.torch, self.K, self.W = torch, K, W
         self.wl, self.dev, self.gather = wl, device, gather
+        self.fused = fused
         B = wl.block_tokens
         self.ids = [5000 - 17 * s for s in range(wl.nseq)]
         self.ntok = list(wl.prefill_lens)
@@ -384,12 +388,16 @@ class Pipeline:
             self.ntok[i] += 1
         if ev and phases:
             ev[1].record(main)
-        ctx.decode_step(ids, self._rows(q, active), out, stream=sh)
+        if self.fused:      # scoring in the decode epilogue
+            ctx.decode_score_step(ids, self._rows(q, active), out, stream=sh)
+        else:
+            ctx.decode_step(ids, self._rows(q, active), out, stream=sh)
         if ev and phases:
             ev[2].record(main)
         if after_decode is not None:
             after_decode()          # host work that overlaps the rest of the step
-        ctx.score_update(stream=sh)
+        if not self.fused:
+            ctx.score_update(stream=sh)
         r = None
         self.steps_done += 1
         demoting = self.demote_every and self.steps_done % self.demote_every == 0 and not self.holes
@@ -556,7 +564,8 @@ def measure(args, wname, dev, ws, rank, local, sub=False):
     lit_steps = 0 if (sub or args.no_literal or gather not in ("mirror", "mirror-sync", "list")) else 2
     bd_steps = min(8, K_)
     total = W_ + K_ + bd_steps + e2e_steps + lit_steps
-    pipe = Pipeline(wl, alpha, total, dev, gather, args.kv_dtype, args.prefetch_budget, args.victims)
+    pipe = Pipeline(wl, alpha, total, dev, gather, args.kv_dtype, args.prefetch_budget, args.victims,
+                    fused=not args.unfused)
     pipe.prefill()
     kv, qs = pipe.inputs(1, W_ + K_)
 
@@ -768,6 +777,9 @@ def measure(args, wname, dev, ws, rank, local, sub=False):
                                    + (f", {wl.shared_prefix_tokens}-token shared prefix" if wl.shared_prefix_tokens else ""),
                        "global_batch": wl.nseq, "seq_len": max(wl.prefill_lens),
                        "alpha": alpha, "gather": gather,
+                       "score_call": ("kvs_decode_step + kvs_score_update" if args.unfused else
+                                      "kvs_decode_score_step: records scored in the decode epilogue "
+                                      "(breakdown 'score' is then empty)"),
                        "select_call": ("KVS_GATHER_ASYNC: no host wait; counts read one step later"
                                        if gather in ("mirror", "ids") else "synchronising"),
                        **({"prefetch_budget": args.prefetch_budget} if gather == "prefetch" else {}),
@@ -791,6 +803,7 @@ def measure(args, wname, dev, ws, rank, local, sub=False):
             "breakdown_ms": {k: round(v, 4) for k, v in part.items()},
             "scoring_overhead_pct": round(100 * (part["score"] + part["select_gather"]) /
                                           max(part["decode_step"], 1e-9), 2),
+            "outside_decode_kernel_pct": round(100 * (ms_max / K_ - dec_avg) / dec_avg, 2),
             "gathered_pages_timed": staged,
             "demoted_and_readmitted_pages_timed": demoted,
             "demote_readmit_rounds": round_info,

@@ -307,6 +307,15 @@ int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
 int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
                     const void *q_dev, float *out_dev, void *stream);
 
+/* kvs_decode_step followed by kvs_score_update, in fewer launches: the
+ * epilogue that writes each block's mass scores the block's record in the
+ * same kernel ([GQA]: the aggregated mass lands in the 64-byte record).
+ * Results are bit-identical to the two calls.  kvs_score_update must not be
+ * called for a set this call scored (KVS_EINVAL).  Errors as
+ * kvs_decode_step. */
+int kvs_decode_score_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
+                          const void *q_dev, float *out_dev, void *stream);
+
 /* Scores every block of the last decode set [VA] s.11, s.12, [GQA]:
  *   E <- alpha*M + (1-alpha)*E;  if M*num_blocks >= 1 (a touch):
  *   count += 1, lrfu <- alpha + (1-alpha)^(t - last_touch) * lrfu,
@@ -320,6 +329,7 @@ int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq,
  * exponentiation (result = 1, base = 1-alpha; per bit of the exponent from
  * the lowest: if set result *= base; base *= base). */
 int kvs_score_update(kvs_ctx_t *ctx, void *stream);
+/* (KVS_EINVAL if the last set was already scored by kvs_decode_score_step.) */
 
 /* Changes alpha for later score updates. */
 int kvs_set_alpha(kvs_ctx_t *ctx, double alpha);

@@ -97,6 +97,7 @@ _SIGS = {
     "kvs_append_token": (ctypes.c_int, [c_vp, c_u64, c_vp, c_vp, c_vp]),
     "kvs_append_step": (ctypes.c_int, [c_vp, ctypes.POINTER(c_u64), c_u32, c_vp, c_vp, c_vp]),
     "kvs_decode_step": (ctypes.c_int, [c_vp, ctypes.POINTER(c_u64), c_u32, c_vp, c_vp, c_vp]),
+    "kvs_decode_score_step": (ctypes.c_int, [c_vp, ctypes.POINTER(c_u64), c_u32, c_vp, c_vp, c_vp]),
     "kvs_score_update": (ctypes.c_int, [c_vp, c_vp]),
     "kvs_set_alpha": (ctypes.c_int, [c_vp, c_dbl]),
     "kvs_select_and_gather": (ctypes.c_int, [c_vp, ctypes.POINTER(kvs_gather_args),
@@ -309,6 +310,14 @@ class Context:
         assert q.is_contiguous() and out.is_contiguous() and q.is_cuda and out.is_cuda
         _check(self.h, lib().kvs_decode_step(self.h, self._ids(seq_ids), len(seq_ids), q.data_ptr(),
                                              out.data_ptr(), _stream_handle(stream)))
+
+    def decode_score_step(self, seq_ids, q, out, stream=None):
+        """decode_step + score_update, the scoring in the decode epilogue."""
+        t = self.torch
+        assert q.dtype == t.bfloat16 and out.dtype == t.float32
+        assert q.is_contiguous() and out.is_contiguous() and q.is_cuda and out.is_cuda
+        _check(self.h, lib().kvs_decode_score_step(self.h, self._ids(seq_ids), len(seq_ids), q.data_ptr(),
+                                                   out.data_ptr(), _stream_handle(stream)))
 
     def score_update(self, stream=None):
         _check(self.h, lib().kvs_score_update(self.h, _stream_handle(stream)))

@@ -16,6 +16,7 @@
 #include "kvs_internal.h"
 #include "kvs_launch.h"
 #include "kvs_pdl.cuh"
+#include "kvs_score.cuh"
 
 namespace kvs {
 namespace {
@@ -107,8 +108,9 @@ __global__ void append_kernel(const Geo g, const AppendArgs a, uint64_t rows_tot
             r.pad0 = 0;
             r.prio = 0.0;
             r.mass = 0.f;
-            for (int q = 0; q < 12; ++q)
+            for (int q = 0; q < 4; ++q)
                 r.reserved[q] = 0;
+            r.lrfu = 0.0;
             a.records[idx] = r;
             a.table[idx] = a.pages[b - a.first_blk];
         }
@@ -176,8 +178,9 @@ __global__ void append_step_kernel(const Geo g, const uint16_t *k, const uint16_
                 rec.pad0 = 0;
                 rec.prio = 0.0;
                 rec.mass = 0.f;
-                for (int q = 0; q < 12; ++q)
+                for (int q = 0; q < 4; ++q)
                     rec.reserved[q] = 0;
+                rec.lrfu = 0.0;
                 records[idx] = rec;
                 table[idx] = a.page;
             }
@@ -199,34 +202,15 @@ __device__ __forceinline__ uint32_t find_sorted(const DSet *ds, uint32_t r)
     return lo;
 }
 
-struct ScoreArgs {
-    double alpha, wR, wE, wN, lo, hi;
-    uint32_t W;
-};
-
-// (1 - alpha)^dt by binary exponentiation: result = 1, base = 1 - alpha; per
-// bit of dt from the lowest, if set result *= base; then base *= base.
-__device__ __forceinline__ double lrfu_decay(double alpha, uint64_t dt)
-{
-    double base = __dsub_rn(1.0, alpha), res = 1.0;
-    for (; dt; dt >>= 1) {
-        if (dt & 1u)
-            res = __dmul_rn(res, base);
-        base = __dmul_rn(base, base);
-    }
-    return res;
-}
-
 // One thread per record of the decode set (record order: ascending seq_id,
-// then block).  fp64, every operation rounded on its own (no fused
-// multiply-add), in the order: EMA, touch, recency, anchor, P, tier.
+// then block); the scoring itself is score_record (kvs_score.cuh).
 __global__ void score_kernel(const Geo g, const Work w, kvs_record *recs, const float *mass,
                              const ScoreArgs sa, uint32_t nb_total)
 {
     const uint32_t r = blockIdx.x * blockDim.x + threadIdx.x;
     const DSet *ds = w.dset;
     // the decode set was uploaded before the decode kernel: read it while the
-    // mass kernel finishes
+    // mass is being finished
     DSeq sq{};
     uint32_t b = 0;
     uint64_t t = 0;
@@ -241,31 +225,7 @@ __global__ void score_kernel(const Geo g, const Work w, kvs_record *recs, const 
     if (r >= nb_total)
         return;
     const size_t idx = static_cast<size_t>(sq.slot) * g.mb + b;
-    kvs_record rec = recs[idx];
-    if (rec.key.block_idx != b || rec.key.seq_id != sq.seq_id || rec.last_touch > t) {
-        atomicOr(w.err, kErrBadRecord);
-        return;
-    }
-    const double M = static_cast<double>(mass[idx]);
-    // E <- alpha*M + (1 - alpha)*E
-    const double E = __dadd_rn(__dmul_rn(sa.alpha, M), __dmul_rn(__dsub_rn(1.0, sa.alpha), rec.score));
-    // touch: mass at or above the uniform share 1/num_blocks; the
-    // event-driven score decays lazily from the previous touch
-    if (__dmul_rn(M, static_cast<double>(sq.nb)) >= 1.0) {
-        rec.count += 1;
-        rec.lrfu = __dadd_rn(sa.alpha, __dmul_rn(lrfu_decay(sa.alpha, t - rec.last_touch), rec.lrfu));
-        rec.last_touch = t;
-    }
-    const double age = static_cast<double>(t - rec.last_touch);
-    double R = __dsub_rn(1.0, __ddiv_rn(age, static_cast<double>(sa.W)));
-    R = fmin(fmax(R, 0.0), 1.0);
-    const double N = (b == 0 || b + 1 == sq.nb) ? 1.0 : 0.0;
-    const double P = __dadd_rn(__dadd_rn(__dmul_rn(sa.wR, R), __dmul_rn(sa.wE, E)), __dmul_rn(sa.wN, N));
-    rec.score = E;
-    rec.prio = P;
-    rec.tier = P >= sa.hi ? 0 : (P >= sa.lo ? 1 : 2);
-    rec.mass = static_cast<float>(M);
-    recs[idx] = rec;
+    score_record(sa, recs, idx, sq.seq_id, b, sq.nb, t, mass[idx], w.err);
 }
 
 // ---------------------------------------------------------------- selection
@@ -605,6 +565,101 @@ __device__ __forceinline__ uint32_t block_scan_1024(uint32_t f, uint32_t *wsum, 
     *total = wsum[32];
     __syncthreads();
     return pos;
+}
+
+// Selection and gather plan of a set of at most one tile (kSelOneTile
+// records) in one CTA: thread r takes record r (record order), the picks are
+// placed by a block scan (list order = record order among the picks), and
+// each picking thread then plans its own list entry -- a page is gathered at
+// its first entry once every record that references it is listed -- as
+// plan_kernel does.  Outputs as select_scatter_kernel + plan_kernel: the
+// list, its records and pages, the plan, the slots, the counts (readback and,
+// through its device mapping, out.count_host), the per-page counters back at
+// 0 / ~0.
+constexpr uint32_t kSelOneTile = 1024;
+
+__global__ void __launch_bounds__(kSelOneTile)
+    select_plan_kernel(const Geo g, const Work w, const kvs_record *recs, const int32_t *table, int mode,
+                       double alpha, uint32_t nb_total, uint32_t mirror, const SelectOut out)
+{
+    __shared__ uint32_t wsum[33];
+    const double lrfu_c = mode == KVS_SELECT_LRFU ? lrfu_slope(alpha) : 0.0;
+    const DSet *ds = w.dset;
+    const uint32_t r = threadIdx.x;
+    uint32_t b = 0, nt = 0;
+    size_t idx = 0;
+    if (r < nb_total)
+        idx = rec_index(g, ds, r, nullptr, &b, &nt);
+    pdl_wait();                 // records (and the LOWFRAC threshold) come from earlier kernels
+    pdl_trigger();
+    kvs_record rec;
+    int32_t page = -1;
+    bool pk = false;
+    if (r < nb_total) {
+        rec = recs[idx];
+        page = table[idx];
+        pk = picked(mode, rec, r, w.sel_thr, lrfu_c);
+    }
+    uint32_t nsel;
+    const uint32_t pos = block_scan_1024(pk ? 1u : 0u, wsum, &nsel);
+    if (pk) {
+        w.sel_ids[pos] = rec.key;
+        if (out.ids && pos < out.ids_cap)
+            out.ids[pos] = rec.key;
+        w.sel_recs[pos] = rec;
+        w.sel_pages[pos] = page;
+        w.sel_recidx[pos] = r;
+        w.sel_full[pos] = (b + 1) * kBlockTokens <= nt ? 1 : 0;
+        if (page >= 0) {
+            atomicAdd(&w.page_cnt[page], 1u);
+            atomicMin(&w.page_first[page], pos);
+        }
+    }
+    if (threadIdx.x == 0)
+        *w.sel_count = nsel;
+    __syncthreads();            // every listed reference of this call is counted
+    // ---- plan: each picking thread decides for its own list entry ----
+    uint32_t cnt = 0, ref = 0, lead = 0, dirty = 0;
+    if (pk && page >= 0) {
+        cnt = __ldcg(&w.page_cnt[page]);
+        ref = w.dev_refcnt[page];
+        lead = (cnt == ref && __ldcg(&w.page_first[page]) == pos) ? 1u : 0u;
+        dirty = (lead && mirror && !w.page_clean[page]) ? 1u : 0u;
+    }
+    uint32_t tot;
+    const uint32_t ex = block_scan_1024(lead | (dirty << 16), wsum, &tot);
+    if (lead) {
+        const uint32_t ppos = ex & 0xffffu;
+        w.plan_pages[ppos] = page;
+        w.page_pos[page] = static_cast<int32_t>(ppos);
+    }
+    if (dirty) {
+        w.readback[4 + (ex >> 16)] = static_cast<uint32_t>(page);
+        w.page_clean[page] = (b + 1) * kBlockTokens <= nt ? 1 : 0;
+    }
+    __syncthreads();            // page_pos of every leader is written
+    if (pk) {
+        const int32_t v = (page >= 0 && cnt == ref) ? (mirror ? page : __ldcg(&w.page_pos[page])) : -1;
+        w.plan_slot[pos] = v;
+        if (out.slots && pos < out.ids_cap)
+            out.slots[pos] = v;
+        if (page >= 0) {        // every read of the counters was before the scans' barriers
+            w.page_cnt[page] = 0;
+            w.page_first[page] = 0xffffffffu;
+        }
+    }
+    if (threadIdx.x == 0) {
+        w.readback[0] = nsel;
+        w.readback[1] = tot & 0xffffu;
+        w.readback[2] = tot >> 16;
+        w.readback[3] = 0;
+        if (out.count_host) {
+            out.count_host[0] = nsel;
+            out.count_host[1] = tot & 0xffffu;
+            out.count_host[2] = tot >> 16;
+            out.count_host[3] = 0;
+        }
+    }
 }
 
 // ------------------------------------------------------------- prefetch plan
@@ -1110,6 +1165,18 @@ cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, co
     }
     return launch_pdl(select_scatter_kernel, dim3(ntiles), dim3(kSelThreads), 0, s, g, w, rec, table, mode, alpha,
                       nb_total, ntiles, count_pages ? 1u : 0u, out);
+}
+
+bool select_plan_fits(uint32_t nb_total) { return nb_total <= kSelOneTile; }
+
+cudaError_t launch_select_plan(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table, int mode,
+                               double alpha, uint32_t nb_total, uint32_t mirror, const SelectOut &out,
+                               cudaStream_t s)
+{
+    if (nb_total > kSelOneTile)
+        return cudaErrorInvalidValue;
+    return launch_pdl(select_plan_kernel, dim3(1), dim3(kSelOneTile), 0, s, g, w, rec, table, mode, alpha,
+                      nb_total, mirror, out);
 }
 
 uint32_t select_launches(uint32_t nb_total)

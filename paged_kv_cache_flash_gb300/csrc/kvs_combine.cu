@@ -14,7 +14,9 @@
 //                     chunks give the merge a CTA of its own; with few
 //                     chunks CTA 0 also takes the first block range.
 //   mass_kernel    -- M(b) = 1/(L*Hq) * sum over the L*Hkv streams, in a fixed
-//                     order (deterministic).
+//                     order (deterministic); when asked, the thread that
+//                     writes M(b) also scores block b's record (score_record:
+//                     the aggregated mass lands in the 64-byte record).
 // Both are launched as programmatic dependents (kvs_pdl.cuh).
 #include <type_traits>
 
@@ -22,6 +24,7 @@
 #include "kvs_launch.h"
 #include "kvs_pdl.cuh"
 #include "kvs_ptx.h"
+#include "kvs_score.cuh"
 
 namespace kvs {
 namespace {
@@ -134,17 +137,22 @@ __global__ void __launch_bounds__(256, 8) combine_kernel(const Geo g, const Work
 constexpr uint32_t kMassBlocks = 16, kMassGroups = 64;
 
 __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, float *mass,
-                                                    uint32_t nb_total)
+                                                    uint32_t nb_total, kvs_record *recs, const ScoreArgs sa,
+                                                    uint32_t score)
 {
     __shared__ float part[kMassGroups][kMassBlocks + 1];
     const DSet *ds = w.dset;
     const uint32_t i = threadIdx.x % kMassBlocks, j = threadIdx.x / kMassBlocks;
     const uint32_t r = blockIdx.x * kMassBlocks + i;
-    uint32_t slot = 0, b = 0;
+    uint32_t slot = 0, b = 0, nb = 0;
+    uint64_t seq_id = 0, t = 0;
     if (r < nb_total && j == 0) {       // the decode set: uploaded before the decode kernel
         const uint32_t ci = find_seq(&ds->seq[0].blk_off, sizeof(DSeq) / 4, ds->nseq, r);
         slot = ds->seq[ci].slot;
         b = r - ds->seq[ci].blk_off;
+        nb = ds->seq[ci].nb;
+        seq_id = ds->seq[ci].seq_id;
+        t = ds->t;
     }
     pdl_wait();
     pdl_trigger();
@@ -162,8 +170,13 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
             part[j][i] += part[j + half][i];
         __syncthreads();
     }
-    if (j == 0 && r < nb_total)
-        mass[static_cast<size_t>(slot) * g.mb + b] = part[0][i] / static_cast<float>(g.L * g.Hq);
+    if (j == 0 && r < nb_total) {
+        const size_t idx = static_cast<size_t>(slot) * g.mb + b;
+        const float M = part[0][i] / static_cast<float>(g.L * g.Hq);
+        mass[idx] = M;
+        if (score)
+            score_record(sa, recs, idx, seq_id, b, nb, t, M, w.err);
+    }
 }
 
 }  // namespace
@@ -180,10 +193,12 @@ cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nse
     return launch_pdl(combine_kernel<64>, grid, dim3(32 * kMaxGroup), 0, s, g, w, out, split);
 }
 
-cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total, cudaStream_t s)
+cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total, kvs_record *recs,
+                        const ScoreArgs *score, cudaStream_t s)
 {
+    const ScoreArgs sa = score ? *score : ScoreArgs{};
     return launch_pdl(mass_kernel, dim3((nb_total + kMassBlocks - 1) / kMassBlocks), dim3(1024), 0, s, g, w,
-                      mass, nb_total);
+                      mass, nb_total, recs, sa, score ? 1u : 0u);
 }
 
 }  // namespace kvs

@@ -32,7 +32,8 @@
 //                     the normalised output and the stream's block masses
 //                     (kvs_combine.cu).
 //   mass_kernel    -- M(b) = 1/(L*Hq) * sum_{l,h} 2^(lse_blk(l,h,b) - LSE_h),
-//                     summed in a fixed order (deterministic).
+//                     summed in a fixed order (deterministic); scores the
+//                     records when asked.
 #include <cuda_bf16.h>
 
 #include "kvs_internal.h"

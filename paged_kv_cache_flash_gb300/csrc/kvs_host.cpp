@@ -97,6 +97,7 @@ struct kvs_ctx {
 
     std::unique_ptr<DSet> dset;                     // host copy of the current set
     bool have_set = false;
+    bool set_scored = false;     // the current set was scored by kvs_decode_score_step
 
     uint8_t *ring_host = nullptr;                   // pinned upload ring
     cudaEvent_t ring_ev[kRingSlots]{};
@@ -1201,12 +1202,20 @@ int kvs_append_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
     return KVS_OK;
 }
 
-int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const void *q_dev,
-                    float *out_dev, void *stream)
+}  // extern "C"
+
+namespace {
+
+ScoreArgs score_args(const kvs_ctx *ctx)
 {
-    KVS_RANGE();
-    if (!ctx)
-        return KVS_EINVAL;
+    const kvs_config &c = ctx->cfg;
+    return ScoreArgs{c.alpha, c.w_recency, c.w_ema, c.w_anchor, c.cut_lo, c.cut_hi, c.recency_window};
+}
+
+// decode + combine + masses; with score, the epilogue also scores the set
+int decode_impl(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const void *q_dev, float *out_dev,
+                void *stream, bool score)
+{
     if (!q_dev || !out_dev)
         return fail(ctx, KVS_EINVAL, "q and out must be given");
     if ((reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(out_dev)) % 16)
@@ -1252,9 +1261,36 @@ int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, cons
     if ((rc = launch_rc(ctx, launch_combine(ctx->geo, ctx->work, out_dev, ds->nseq, max_nb, max_nchunk, s),
                         "combine")))
         return rc;
-    return launch_rc(ctx, launch_mass(ctx->geo, ctx->work, static_cast<float *>(ctx->buf.mass),
-                                      ds->nb_total, s),
-                     "mass");
+    const ScoreArgs sa = score_args(ctx);
+    if ((rc = launch_rc(ctx,
+                        launch_mass(ctx->geo, ctx->work, static_cast<float *>(ctx->buf.mass), ds->nb_total,
+                                    static_cast<kvs_record *>(ctx->buf.records), score ? &sa : nullptr, s),
+                        "mass")))
+        return rc;
+    ctx->set_scored = score;
+    return KVS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvs_decode_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const void *q_dev,
+                    float *out_dev, void *stream)
+{
+    KVS_RANGE();
+    if (!ctx)
+        return KVS_EINVAL;
+    return decode_impl(ctx, seq_ids, nseq, q_dev, out_dev, stream, false);
+}
+
+int kvs_decode_score_step(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const void *q_dev,
+                          float *out_dev, void *stream)
+{
+    KVS_RANGE();
+    if (!ctx)
+        return KVS_EINVAL;
+    return decode_impl(ctx, seq_ids, nseq, q_dev, out_dev, stream, true);
 }
 
 int kvs_score_update(kvs_ctx_t *ctx, void *stream)
@@ -1264,6 +1300,8 @@ int kvs_score_update(kvs_ctx_t *ctx, void *stream)
         return KVS_EINVAL;
     if (!ctx->have_set)
         return fail(ctx, KVS_EINVAL, "no decode set: call kvs_decode_step first");
+    if (ctx->set_scored)
+        return fail(ctx, KVS_EINVAL, "the last decode set was scored by kvs_decode_score_step");
     const kvs_config &c = ctx->cfg;
     return launch_rc(ctx,
                      launch_score(ctx->geo, ctx->work, static_cast<kvs_record *>(ctx->buf.records),
@@ -1369,11 +1407,28 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         }
         if (async && ctx->geo.kivi)
             sel_out.count_host = ctx->async_hdr_dev;
-        if ((rc = launch_rc(ctx,
-                            launch_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
-                                          static_cast<const int32_t *>(ctx->buf.block_table), args->mode, alpha,
-                                          N, !ctx->geo.kivi, sel_out, s),
-                            "select", select_launches(N))))
+        const bool one_kernel = !ctx->geo.kivi && select_plan_fits(N);
+        if (one_kernel) {
+            // selection and plan in one launch
+            SelectOut o = sel_out;
+            if (async) {
+                if (args->slot_dev) {
+                    o.slots = args->slot_dev;
+                    o.ids_cap = cap;
+                }
+                o.count_host = ctx->async_hdr_dev;
+            }
+            if ((rc = launch_rc(ctx,
+                                launch_select_plan(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
+                                                   static_cast<const int32_t *>(ctx->buf.block_table), args->mode,
+                                                   alpha, N, mirror ? 1u : 0u, o, s),
+                                "select and plan")))
+                return rc;
+        } else if ((rc = launch_rc(ctx,
+                                   launch_select(ctx->geo, w, static_cast<const kvs_record *>(ctx->buf.records),
+                                                 static_cast<const int32_t *>(ctx->buf.block_table), args->mode,
+                                                 alpha, N, !ctx->geo.kivi, sel_out, s),
+                                   "select", select_launches(N))))
             return rc;
         if (ctx->geo.kivi && async) {
             CU(cudaEventRecord(ctx->ev_async, s));
@@ -1399,7 +1454,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             }
             plan_out.count_host = ctx->async_hdr_dev;
         }
-        if ((rc = launch_rc(ctx, launch_plan(w, mirror ? 1u : 0u, plan_out, s), "plan")))
+        if (!one_kernel && (rc = launch_rc(ctx, launch_plan(w, mirror ? 1u : 0u, plan_out, s), "plan")))
             return rc;
         if (async) {
             // the stale pages go to the host mirror by a device kernel in
@@ -1922,6 +1977,7 @@ int kvs_debug_set_mass(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, c
     if ((rc = upload_set(ctx, *ds, s)))
         return rc;
     ctx->have_set = true;
+    ctx->set_scored = false;
     return launch_rc(ctx,
                      launch_copy_mass(ctx->geo, ctx->work, mass_dev, static_cast<float *>(ctx->buf.mass),
                                       nseq, s),

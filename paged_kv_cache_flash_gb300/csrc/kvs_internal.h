@@ -74,6 +74,14 @@ inline size_t dset_bytes(uint32_t nseq)
 // (no upload copy).
 constexpr size_t kSetInlineBytes = 4096;
 
+// Parameters of the per-block scoring ("KV-Cache Offloading for LLM
+// Inference -- Visual Reference" s.11-12): EMA weight, priority weights,
+// tier cuts, recency window.
+struct ScoreArgs {
+    double alpha, wR, wE, wN, lo, hi;
+    uint32_t W;
+};
+
 // Geometry and device pointers every kernel may need.
 struct Geo {
     uint32_t L, Hq, Hkv, d, G;

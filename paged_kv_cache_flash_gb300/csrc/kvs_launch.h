@@ -19,8 +19,10 @@ cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w,
                           uint32_t n_items, uint32_t wg, int grid, cudaStream_t s);
 cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq,
                            uint32_t max_nb, uint32_t max_nchunk, cudaStream_t s);
-cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total,
-                        cudaStream_t s);
+// Block masses into mass ([slot][mb]); with score != nullptr the kernel also
+// scores every block of the set (records updated as by launch_score).
+cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total, kvs_record *recs,
+                        const ScoreArgs *score, cudaStream_t s);
 cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const float *mass,
                          double alpha, uint32_t W, double wR, double wE, double wN,
                          double lo, double hi, uint32_t nb_total, cudaStream_t s);
@@ -32,6 +34,12 @@ cudaError_t launch_select(const Geo &g, const Work &w, const kvs_record *rec, co
                           int mode, double alpha, uint32_t nb_total, bool count_pages, const SelectOut &out,
                           cudaStream_t s);
 uint32_t select_launches(uint32_t nb_total);   // kernels launch_select issues
+// Selection and gather plan in one kernel (launch_select + launch_plan), for
+// sets of at most select_plan_fits records; out: ids (cap), slots, counts.
+bool select_plan_fits(uint32_t nb_total);
+cudaError_t launch_select_plan(const Geo &g, const Work &w, const kvs_record *rec, const int32_t *table, int mode,
+                               double alpha, uint32_t nb_total, uint32_t mirror, const SelectOut &out,
+                               cudaStream_t s);
 cudaError_t launch_plan(const Work &w, uint32_t mirror, const SelectOut &out, cudaStream_t s);
 cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *pages, uint32_t npages,
                            uint16_t *pool, cudaStream_t s);

@@ -208,7 +208,7 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
     NA_CHECK(launch_decode(g, tmap, w, static_cast<const uint16_t *>(q), block_table, ds.n_items, wg,
                            grid, s));
     NA_CHECK(launch_combine(g, w, out, 1, nb, nchunk, s));
-    NA_CHECK(launch_mass(g, w, mass, nb, s));
+    NA_CHECK(launch_mass(g, w, mass, nb, nullptr, nullptr, s));
     if (status)     // error word and its first offending value, after the outputs
         NA_CHECK(cudaMemcpyAsync(status, w.err, 2 * sizeof(uint32_t), cudaMemcpyDeviceToDevice, s));
 #undef NA_CHECK

@@ -88,12 +88,15 @@ class Run:
     each sequence's attention, mass and records depend on it alone.
     attn_steps: the steps at which mode (i) attention runs (None = every
     step); mode (i) records are kept only when it runs at every step.
-    alpha: one EMA weight, or a tuple of them (one context each)."""
+    alpha: one EMA weight, or a tuple of them (one context each).
+    fused: each step decodes and scores in one call (kvs_decode_score_step)
+    instead of kvs_decode_step + kvs_score_update."""
 
     def __init__(self, wl, alpha, *, staging_pages=8, chunk=4096, oracle_on=True,
                  oracle_seqs=None, attn_steps=None, pool_pages=None, extra_steps=0, device="cuda",
-                 kv_dtype=K.KVS_KV_BF16, k_scale=1.0, v_scale=1.0, kivi_groups=0):
+                 kv_dtype=K.KVS_KV_BF16, k_scale=1.0, v_scale=1.0, kivi_groups=0, fused=False):
         self.wl = wl
+        self.fused = fused
         alphas = tuple(alpha) if isinstance(alpha, (tuple, list)) else (alpha,)
         self.alpha = alphas[0]
         self.dev = device
@@ -210,8 +213,11 @@ class Run:
         for ln, host in zip(self.lanes, hosts):
             ctx = ln.ctx
             out = torch.empty((wl.nseq, wl.L, wl.Hq, wl.d), dtype=torch.float32, device=self.dev)
-            ctx.decode_step(self.ids, q, out)
-            ctx.score_update()
+            if self.fused:
+                ctx.decode_score_step(self.ids, q, out)
+            else:
+                ctx.decode_step(self.ids, q, out)
+                ctx.score_update()
             ids = torch.zeros(nrec * 2, dtype=torch.int64, device=self.dev)
             slots = torch.full((nrec,), -2, dtype=torch.int32, device=self.dev)
             side = torch.cuda.Stream()

@@ -16,7 +16,8 @@ cudaError_t launch_decode(const Geo &, const CUtensorMap &, const Work &, const 
                           uint32_t, uint32_t, int, cudaStream_t) { return cudaErrorNoDevice; }
 cudaError_t launch_combine(const Geo &, const Work &, float *, uint32_t, uint32_t, uint32_t, cudaStream_t)
 { return cudaErrorNoDevice; }
-cudaError_t launch_mass(const Geo &, const Work &, float *, uint32_t, cudaStream_t) { return cudaErrorNoDevice; }
+cudaError_t launch_mass(const Geo &, const Work &, float *, uint32_t, kvs_record *, const ScoreArgs *, cudaStream_t)
+{ return cudaErrorNoDevice; }
 cudaError_t launch_score(const Geo &, const Work &, kvs_record *, const float *, double, uint32_t, double,
                          double, double, double, double, uint32_t, cudaStream_t) { return cudaErrorNoDevice; }
 cudaError_t launch_radix_select(const Geo &, const Work &, const kvs_record *, uint32_t, uint32_t, int, double,
@@ -24,6 +25,9 @@ cudaError_t launch_radix_select(const Geo &, const Work &, const kvs_record *, u
 cudaError_t launch_select(const Geo &, const Work &, const kvs_record *, const int32_t *, int, double, uint32_t,
                           bool, const SelectOut &, cudaStream_t) { return cudaErrorNoDevice; }
 uint32_t select_launches(uint32_t) { return 0; }
+bool select_plan_fits(uint32_t) { return false; }
+cudaError_t launch_select_plan(const Geo &, const Work &, const kvs_record *, const int32_t *, int, double, uint32_t,
+                               uint32_t, const SelectOut &, cudaStream_t) { return cudaErrorNoDevice; }
 cudaError_t launch_plan(const Work &, uint32_t, const SelectOut &, cudaStream_t) { return cudaErrorNoDevice; }
 cudaError_t launch_scatter(const Geo &, const uint8_t *, const int32_t *, uint32_t, uint16_t *, cudaStream_t)
 { return cudaErrorNoDevice; }

@@ -43,7 +43,7 @@ def test_llama70b_8k_full_size():
     to a host buffer of the whole pool every step."""
     wl = W.workload("l70b_8k")
     assert wl.steps == 32 and wl.alphas == (0.15,)
-    run = Run(wl, 0.15)
+    run = Run(wl, 0.15, fused=True)
     host = _pinned(wl.pool_pages * wl.page_bytes)
     acc = {}
     for _ in range(wl.steps):
@@ -64,7 +64,7 @@ def test_batch16_shared_prefix_full_size():
     (checked through the conditioned gather plan, slot by slot)."""
     wl = W.workload("l70b_batch16")
     assert wl.steps == 16 and wl.alphas == (0.01, 0.15)
-    run = Run(wl, wl.alphas)
+    run = Run(wl, wl.alphas, fused=True)
     hosts = [_pinned(wl.pool_pages * wl.page_bytes), _pinned(256 * wl.page_bytes)]
     acc = {}
     for _ in range(wl.steps):
@@ -99,7 +99,7 @@ def test_128k_full_size():
     assert wl.steps == 64 and wl.alphas == (0.01, 0.05, 0.15)
     extra = 2
     attn = {1, 2, 32, 64}
-    run = Run(wl, wl.alphas, attn_steps=attn, extra_steps=extra)
+    run = Run(wl, wl.alphas, attn_steps=attn, extra_steps=extra, fused=True)
     hosts = [_pinned(64 * wl.page_bytes) for _ in run.lanes]
     acc = {}
     for _ in range(wl.steps + extra):
@@ -132,7 +132,7 @@ def test_mixed32_demote_readmit_full_size():
     wl = W.workload("l70b_mixed32")
     assert wl.steps == 32 and wl.alphas == (0.05,) and wl.demote_every == 8
     follow = [0, 13, 31]
-    run = Run(wl, 0.05, oracle_seqs=follow, extra_steps=1)
+    run = Run(wl, 0.05, oracle_seqs=follow, extra_steps=1, fused=True)
     ctx = run.ctx
     acc = {}
     rounds = 0

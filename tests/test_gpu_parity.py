@@ -104,6 +104,32 @@ def test_many_sequences_ring_uploads_and_multi_tile_selection(nseq, max_len):
     run.close()
 
 
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", dict(prefill_lens=(40, 33, 150), shared_prefix_tokens=32, pool_pages=40, steps=6, skew=True)),
+    ("l70b_8k", dict(L=6, prefill_lens=(3000, 1, 700), pool_pages=300, steps=4))])
+def test_fused_decode_score_matches_two_calls(name, kw):
+    """kvs_decode_score_step (scores in the decode epilogue) against
+    kvs_decode_step + kvs_score_update on a second context fed the same
+    steps: outputs, masses, all record bytes and the lists bit for bit, the
+    fused side also against the oracle; a score update after a fused step is
+    refused."""
+    wl = W.workload(name, **kw)
+    two, one = Run(wl, 0.15, oracle_on=False), Run(wl, 0.15, fused=True)
+    for _ in range(wl.steps):
+        a, b = two.step(None), one.step(None)
+        one.compare(b)
+        assert torch.equal(a["out"], b["out"])
+        assert all(np.array_equal(a["mass"][s], b["mass"][s]) for s in two.ids)
+        assert all(a["records"][s].tobytes() == b["records"][s].tobytes() for s in two.ids)
+        assert a["ids"] == b["ids"]
+    with pytest.raises(K.KvsError) as e:
+        one.ctx.score_update()
+    assert e.value.code == K.KVS_EINVAL
+    one.ctx.check_device()
+    two.close()
+    one.close()
+
+
 def test_single_token_sequence_and_large_group():
     """One-token sequences (nothing but block 0) and the full 8:1 group at d=128."""
     wl = W.workload("l70b_8k", L=3, prefill_lens=(1, 17), pool_pages=8, steps=3)
