@@ -335,15 +335,21 @@ def kivi_effective(K, V):
 
 def kivi_group_tile(ck, sk, zk, cv, sv, zv) -> bytes:
     """Bytes of one (layer, KV head) of a group page (d = 128), the layout a
-    warp of the decode kernel reads (lane = 4*g + t, g = lane // 4, t = lane % 4):
+    warp of the decode kernel reads (lane = 4*g + t, g = lane // 4, t = lane % 4).
 
-      K codes  [0, 1024)   : [block j][lane][word w in 0..3]; word w holds the
-                             16 codes of token 16j + g + 8*(w // 2), dims
-                             32t + 16*(w % 2) + i, code i at bits 2i.
-      V codes  [1024, 2048): [block j][lane][word w]; pair i (0..7) of word w
-                             is m = 2w + i // 4, e = i % 4: dim 16m + g +
-                             8*(e % 2), token 16j + 2t + 8*(e // 2) at bits 2i
-                             and the next token at bits 16 + 2i.
+    Code words hold operand pairs as the two 2-bit fields of a byte's two
+    nibbles: in byte k (k = 0..3) of word w, the pair (bits 0-1, bits 4-5)
+    belongs to operand register k of step 2w and the pair (bits 2-3,
+    bits 6-7) to register k of step 2w + 1 (first element in the low field).
+
+      K codes  [0, 1024)   : [block j][lane][word w in 0..3]; step s = k-step
+                             (16 channels) s, register r: token 16j + g +
+                             8*(r % 2), channels (c, c + 8) for r < 2 and
+                             (c + 1, c + 9) for r >= 2, c = 32t + 16*(s // 4)
+                             + 2*(s % 4).
+      V codes  [1024, 2048): [block j][lane][word w]; step s = m-tile
+                             (16 channels) s, register r: channel 16s + g +
+                             8*(r % 2), tokens (16j + 2t + 8*(r // 2), the next).
       K meta   [2048, 2560): [half h in 0..1][ip in 0..3][t] of (scale pair,
                              zero pair) for i = 2ip, then for i = 2ip + 1;
                              each pair two fp16: channel 32t + 16h + i
@@ -355,23 +361,33 @@ def kivi_group_tile(ck, sk, zk, cv, sv, zv) -> bytes:
     ck, cv: codes [32][d]; sk, zk: [d]; sv, zv: [32][d/32]."""
     ck = np.asarray(ck, np.uint32)
     cv = np.asarray(cv, np.uint32)
-    kc = np.zeros((2, 32, 4), np.uint32)
-    vc = np.zeros((2, 32, 4), np.uint32)
-    for j in range(2):
-        for lane in range(32):
-            g, t = lane // 4, lane % 4
-            for w in range(4):
-                tok = 16 * j + g + 8 * (w // 2)
-                base = 32 * t + 16 * (w % 2)
-                kc[j, lane, w] = sum(int(ck[tok, base + i]) << (2 * i) for i in range(16))
-                word = 0
-                for i in range(8):
-                    m, e = 2 * w + i // 4, i % 4
-                    dim = 16 * m + g + 8 * (e % 2)
-                    tok0 = 16 * j + 2 * t + 8 * (e // 2)
-                    word |= int(cv[tok0, dim]) << (2 * i)
-                    word |= int(cv[tok0 + 1, dim]) << (16 + 2 * i)
-                vc[j, lane, w] = word
+
+    def k_pair(j, g, t, s, r):
+        tok = 16 * j + g + 8 * (r % 2)
+        c = 32 * t + 16 * (s // 4) + 2 * (s % 4) + (r // 2)
+        return ck[tok, c], ck[tok, c + 8]
+
+    def v_pair(j, g, t, s, r):
+        ch = 16 * s + g + 8 * (r % 2)
+        tok = 16 * j + 2 * t + 8 * (r // 2)
+        return cv[tok, ch], cv[tok + 1, ch]
+
+    def words(pair):
+        out = np.zeros((2, 32, 4), np.uint32)
+        for j in range(2):
+            for lane in range(32):
+                g, t = lane // 4, lane % 4
+                for w in range(4):
+                    word = 0
+                    for k in range(4):
+                        for half, s in ((0, 2 * w), (1, 2 * w + 1)):
+                            lo, hi = pair(j, g, t, s, k)
+                            word |= int(lo) << (8 * k + 2 * half)
+                            word |= int(hi) << (8 * k + 4 + 2 * half)
+                    out[j, lane, w] = word
+        return out
+
+    kc, vc = words(k_pair), words(v_pair)
     f16 = lambda a: np.asarray(a, np.float16).view(np.uint16).astype(np.uint32)
     skb, zkb = f16(sk), f16(zk)
     km = np.zeros((2, 4, 4, 2, 2), np.uint32)

@@ -15,32 +15,40 @@
 //                           layout the decode warps read.
 //   decode_kivi_kernel   -- persistent, independent warps as in the page
 //                           decode: each claims (sequence, layer, KV head,
-//                           chunk of groups) items, streams 3 KiB group tiles
-//                           through a bulk-copy ring, dequantises codes in
-//                           registers straight into f16 MMA fragments
-//                           (code pair -> biased f16 pair by one mask-and-or,
-//                           the bias subtracted exactly, then one fused
-//                           multiply-add with the pair's scale and zero) and
-//                           writes the same split-K
-//                           partials and per-block log2-sum-exps.
+//                           chunk of groups) items and streams 3 KiB group
+//                           tiles through a bulk-copy ring.  Codes become
+//                           f16 pairs code/2 by the FP4 (e2m1) pair
+//                           conversion (exact).  Keys: fp16(code*s + z) by one
+//                           f16 fused multiply-add per pair, (code/2)(2s) + z
+//                           -- the quantiser's dequantised value, one
+//                           rounding -- into the S MMAs.  Values are s_t*code +
+//                           z_t per token and channel group, and never formed:
+//                           O^T += (codes/2) . (2 s_t P^T) per m-tile, and the
+//                           zero term, one value per (channel group, head), by
+//                           one MMA per block whose rows are the four channel
+//                           groups, added to O at the end of the item.  It
+//                           writes the
+//                           same split-K partials and per-block log2-sum-exps
+//                           as the page decode.
 //
-// Tile layout (per (layer, KV head) of a group page; lane = 4g + t):
-//   [0, 1024)    K codes [block j][lane][word w]: word w = 16 codes of token
-//                16j + g + 8(w/2), channels 32t + 16(w%2) + i at bits 2i.
-//   [1024, 2048) V codes [block j][lane][word w]: pair i (0..7) of word w is
-//                m-tile m = 2w + i/4, register e = i%4: channel 16m + g +
-//                8(e%2), tokens 16j + 2t + 8(e/2) (bits 2i) and the next one
-//                (bits 16 + 2i).
+// Tile layout (per (layer, KV head) of a group page; lane = 4g + t).  A code
+// word holds operand pairs as the 2-bit low fields of a byte's two nibbles:
+// byte k of word w carries register k of step 2w (fields 0-1 and 4-5, first
+// element low) and register k of step 2w + 1 (fields 2-3 and 6-7), so
+// (w & 0x33333333) and ((w >> 2) & 0x33333333) are each four FP4 pairs.
+//   [0, 1024)    K codes [block j][lane][word w]: step s = k-step s (16
+//                channels), register r: token 16j + g + 8(r%2), channels
+//                (c, c+8) for r < 2 and (c+1, c+9) for r >= 2,
+//                c = 32t + 16(s/4) + 2(s%4).
+//   [1024, 2048) V codes [block j][lane][word w]: step s = m-tile s,
+//                register r: channel 16s + g + 8(r%2), tokens 16j + 2t +
+//                8(r/2) and the next one.
 //   [2048, 2560) K (scale pair, zero pair) [h][ip][t][i = 2ip, 2ip+1]:
 //                channels 32t + 16h + i (low half) and + 8 (high half); the
 //                four t of one (h, ip) are 64 contiguous bytes, so the 16-byte
 //                loads of the lanes t = 0..3 fall in different banks.
 //   [2560, 3072) V (scale pair, zero pair) [block j][token pair p][channel
 //                group c]: tokens 16j + 2p (low) and 16j + 2p + 1 (high).
-// Pair i of a code word is the two codes at bits 2i and 16 + 2i: the operand
-// pair of an f16 MMA register.  Pair i = p (p < 5) of a word w, or of
-// w >> 10 (p = i - 5), is taken by one mask-and-or into the mantissa of an
-// f16 pair with exponent 25 - 2p: value B_p + code, B_p = 2^(10-2p), exact.
 #include <cuda_fp16.h>
 
 #include "kvs_internal.h"
@@ -142,22 +150,27 @@ __global__ void __launch_bounds__(128)
         zv[t][cg] = h_bits(z16);
     }
     __syncthreads();
-    // code words: 256 K words and 256 V words, index (j * 32 + lane) * 4 + w
+    // code words: 256 K words and 256 V words, index (j * 32 + lane) * 4 + w;
+    // byte k of word w: register k of step 2w (fields 0-1 and 4-5) and of
+    // step 2w + 1 (fields 2-3 and 6-7), first element in the low field
     for (uint32_t wi = tid; wi < 256; wi += blockDim.x) {
         const uint32_t j = wi >> 7, lane = (wi >> 2) & 31, w = wi & 3;
         const uint32_t gq = lane >> 2, tq = lane & 3;
-        const uint32_t tok = 16 * j + gq + 8 * (w >> 1), base = 32 * tq + 16 * (w & 1);
         uint32_t kw = 0, vw = 0;
 #pragma unroll
-        for (uint32_t i = 0; i < 16; ++i)
-            kw |= static_cast<uint32_t>(kc[tok][base + i]) << (2 * i);
+        for (uint32_t k = 0; k < 4; ++k) {
 #pragma unroll
-        for (uint32_t i = 0; i < 8; ++i) {
-            const uint32_t m = 2 * w + (i >> 2), e = i & 3;
-            const uint32_t dim = 16 * m + gq + 8 * (e & 1);
-            const uint32_t tok0 = 16 * j + 2 * tq + 8 * (e >> 1);
-            vw |= static_cast<uint32_t>(vc[tok0][dim]) << (2 * i);
-            vw |= static_cast<uint32_t>(vc[tok0 + 1][dim]) << (16 + 2 * i);
+            for (uint32_t half = 0; half < 2; ++half) {
+                const uint32_t st = 2 * w + half, lo = 8 * k + 2 * half, hi = lo + 4;
+                // K step st: token 16j + g + 8(k % 2), channels (c, c + 8)
+                const uint32_t tok = 16 * j + gq + 8 * (k & 1);
+                const uint32_t c = 32 * tq + 16 * (st >> 2) + 2 * (st & 3) + (k >> 1);
+                kw |= (static_cast<uint32_t>(kc[tok][c]) << lo) | (static_cast<uint32_t>(kc[tok][c + 8]) << hi);
+                // V m-tile st: channel 16 st + g + 8(k % 2), tokens t0 and t0 + 1
+                const uint32_t ch = 16 * st + gq + 8 * (k & 1);
+                const uint32_t t0 = 16 * j + 2 * tq + 8 * (k >> 1);
+                vw |= (static_cast<uint32_t>(vc[t0][ch]) << lo) | (static_cast<uint32_t>(vc[t0 + 1][ch]) << hi);
+            }
         }
         tile[wi] = kw;
         tile[256 + wi] = vw;
@@ -293,35 +306,40 @@ __device__ __forceinline__ bool kissue_next(const KArgs &a, const KPrep &cur, co
     return true;
 }
 
-// Pair I of code word w (w10 = w >> 10) -> f16 pair code * scale + zero,
-// one rounding: the biased pair B_p + code, minus B_p (exact), then one fma.
-template <int I>
-__device__ __forceinline__ uint32_t kdq_at(uint32_t w, uint32_t w10, uint32_t s2, uint32_t z2)
+// The four bytes of a masked code word (each byte two 2-bit codes in the low
+// fields of its nibbles) as four f16 pairs code/2: a 2-bit field in the low
+// bits of an FP4 (e2m1) nibble is the value code/2 exactly (0, 0.5, 1, 1.5),
+// and the hardware conversion takes a byte of two nibbles to an f16 pair
+// (low nibble to the low half).
+__device__ __forceinline__ void e2m1x4(uint32_t m, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
 {
-    constexpr int P = I < 5 ? I : I - 5;
-    constexpr uint32_t M = (3u << (2 * P)) | (3u << (2 * P + 16));
-    constexpr uint32_t E = 25u - 2u * P;
-    constexpr uint32_t C = (E << 10) | (E << 26);         // f16 pair (B_p, B_p)
-    const uint32_t x = ((I < 5 ? w : w10) & M) | C;
-    const uint32_t b = C;
-    const __half2 c = __hsub2(*reinterpret_cast<const __half2 *>(&x), *reinterpret_cast<const __half2 *>(&b));
-    const __half2 r = __hfma2(c, *reinterpret_cast<const __half2 *>(&s2), *reinterpret_cast<const __half2 *>(&z2));
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+        : "r"(m));
+}
+
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b)
+{
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-__device__ __forceinline__ uint32_t kdq(uint32_t w, uint32_t w10, int i, uint32_t s2, uint32_t z2)
+__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c)
 {
-    switch (i) {    // i is a constant after unrolling
-    case 0: return kdq_at<0>(w, w10, s2, z2);
-    case 1: return kdq_at<1>(w, w10, s2, z2);
-    case 2: return kdq_at<2>(w, w10, s2, z2);
-    case 3: return kdq_at<3>(w, w10, s2, z2);
-    case 4: return kdq_at<4>(w, w10, s2, z2);
-    case 5: return kdq_at<5>(w, w10, s2, z2);
-    case 6: return kdq_at<6>(w, w10, s2, z2);
-    default: return kdq_at<7>(w, w10, s2, z2);
-    }
+    const __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b),
+                              *reinterpret_cast<const __half2 *>(&c));
+    return *reinterpret_cast<const uint32_t *>(&r);
 }
+
+__device__ __forceinline__ uint32_t hadd2u(uint32_t a, uint32_t b)
+{
+    const __half2 r = __hadd2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+constexpr uint32_t kCodeMask = 0x33333333u;    // the low fields of both nibbles of every byte
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
@@ -415,74 +433,73 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
             o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        float zp[4] = {0.f, 0.f, 0.f, 0.f};      // zero term of the values: [channel group gq][heads h0, h1]
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         float *lse_row0 = a.w.lse_blk + (static_cast<size_t>(it.l) * g.Hq + kvh * G + h0) * nb_total + it.lse0;
 
         for (uint32_t gi = 0; gi < it.ng; ++gi) {
             mbar_wait(smem_u32(&bars[warp][rg.st_cons]), rg.ph_cons, a.w.err);
             const uint32_t base = ring_u32 + rg.st_cons * kTile;
-            // S^T = K . Q^T for both blocks of the group (16 tokens x 8 heads
-            // each): two independent MMA chains
+            // ---- S^T = K . Q^T for both blocks of the group (16 tokens x 8
+            // heads each), two independent MMA chains.  A key is
+            // fp16(code * s_c + z_c): the code, exact as code/2, times 2 s_c
+            // plus z_c in one f16 fused multiply-add (one rounding)
             float sj[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             {
-                // K (scale, zero) pairs of the lane's channels, km[(h * 8 + i) * 2 + {scale, zero}]
-                uint32_t km[32];
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {   // v = h * 4 + ip
-                    const uint4 x = lds128(base + 2048 + (v * 4 + tq) * 16);
-                    km[4 * v] = x.x;
-                    km[4 * v + 1] = x.y;
-                    km[4 * v + 2] = x.z;
-                    km[4 * v + 3] = x.w;
-                }
-                uint32_t kw[2][4], kx[2][4];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint4 kw4 = lds128(base + (j * 32 + lane) * 16);
-                    kw[j][0] = kw4.x; kw[j][1] = kw4.y; kw[j][2] = kw4.z; kw[j][3] = kw4.w;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        kx[j][e] = kw[j][e] >> 10;
-                }
+                const uint4 kw0 = lds128(base + lane * 16), kw1 = lds128(base + (32 + lane) * 16);
+                const uint32_t kw[2][4] = {{kw0.x, kw0.y, kw0.z, kw0.w}, {kw1.x, kw1.y, kw1.z, kw1.w}};
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const int w = ks >> 2, i0 = 2 * (ks & 3);
-                    const uint32_t sa = km[(w * 8 + i0) * 2], za = km[(w * 8 + i0) * 2 + 1];
-                    const uint32_t sb = km[(w * 8 + i0 + 1) * 2], zb = km[(w * 8 + i0 + 1) * 2 + 1];
+                    // (scale, zero) pairs of the k-step's channels (c, c+8) and (c+1, c+9)
+                    const uint4 m = lds128(base + 2048 + (ks * 4 + tq) * 16);
+                    const uint32_t sa = hadd2u(m.x, m.x), sb = hadd2u(m.z, m.z);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        mma_f16(sj[j], kdq(kw[j][w], kx[j][w], i0, sa, za),
-                                kdq(kw[j][2 + w], kx[j][2 + w], i0, sa, za),
-                                kdq(kw[j][w], kx[j][w], i0 + 1, sb, zb),
-                                kdq(kw[j][2 + w], kx[j][2 + w], i0 + 1, sb, zb), qf[ks][0], qf[ks][1]);
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t wd = kw[j][ks >> 1];
+                        uint32_t a0, a1, a2, a3;
+                        e2m1x4((ks & 1) ? ((wd >> 2) & kCodeMask) : (wd & kCodeMask), a0, a1, a2, a3);
+                        mma_f16(sj[j], hfma2u(a0, sa, m.y), hfma2u(a1, sa, m.y), hfma2u(a2, sb, m.w),
+                                hfma2u(a3, sb, m.w), qf[ks][0], qf[ks][1]);
+                    }
                 }
             }
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    sj[j][e] *= scale_log2;
-
             // one online-softmax update for the 32 tokens; the per-block
-            // log2-sum-exps are taken against the same running max
-            float bm0 = fmaxf(fmaxf(sj[0][0], sj[0][2]), fmaxf(sj[1][0], sj[1][2]));
-            float bm1 = fmaxf(fmaxf(sj[0][1], sj[0][3]), fmaxf(sj[1][1], sj[1][3]));
+            // log2-sum-exps are taken against the same running max.  The
+            // lanes' maxima are merged only when one of them exceeds the
+            // running max (otherwise the running max stands)
+            const float lm0 = fmaxf(fmaxf(sj[0][0], sj[0][2]), fmaxf(sj[1][0], sj[1][2]));
+            const float lm1 = fmaxf(fmaxf(sj[0][1], sj[0][3]), fmaxf(sj[1][1], sj[1][3]));
+            float bm0 = lm0 * scale_log2, bm1 = lm1 * scale_log2;     // scores in log2 units
+            float mn0 = m0, mn1 = m1;
+            bool moved = false;
+            if (__any_sync(0xffffffffu, bm0 > m0 || bm1 > m1)) {
 #pragma unroll
-            for (int x = 4; x < 32; x <<= 1) {
-                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
-                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+                for (int x = 4; x < 32; x <<= 1) {
+                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+                }
+                mn0 = fmaxf(m0, bm0);
+                mn1 = fmaxf(m1, bm1);
+                moved = true;
             }
-            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-            const bool moved = mn0 != m0 || mn1 != m1;
             const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
+            const float ad0 = -mn0, ad1 = -mn1;
             float pj[2][4];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                pj[j][0] = fast_exp2(sj[j][0] - mn0);
-                pj[j][1] = fast_exp2(sj[j][1] - mn1);
-                pj[j][2] = fast_exp2(sj[j][2] - mn0);
-                pj[j][3] = fast_exp2(sj[j][3] - mn1);
+                pj[j][0] = fast_exp2(fmaf(sj[j][0], scale_log2, ad0));
+                pj[j][1] = fast_exp2(fmaf(sj[j][1], scale_log2, ad1));
+                pj[j][2] = fast_exp2(fmaf(sj[j][2], scale_log2, ad0));
+                pj[j][3] = fast_exp2(fmaf(sj[j][3], scale_log2, ad1));
             }
+            uint32_t pb[2][2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                pb[j][0] = movmatrix_t(pack_f16(pj[j][0], pj[j][1]));
+                pb[j][1] = movmatrix_t(pack_f16(pj[j][2], pj[j][3]));
+            }
+            // per-block sums of the (fp32) weights, per head, over the 8 lanes
+            // of the head's column
             float w00 = pj[0][0] + pj[0][2], w01 = pj[0][1] + pj[0][3];   // block 0: heads h0, h1
             float w10 = pj[1][0] + pj[1][2], w11 = pj[1][1] + pj[1][3];   // block 1
 #pragma unroll
@@ -506,9 +523,9 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                     lse_row0[nb_total + 2 * gi + 1] = mn1 + fast_log2(w11);
                 }
             }
-            // the rescale only where a running max moved in some lane
-            // (otherwise every factor is 2^0)
-            if (__any_sync(0xffffffffu, moved)) {
+            // the rescale only after a merge of the maxima (otherwise every
+            // factor is 2^0); `moved` is the same in every lane
+            if (moved) {
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     o[mt][0] *= sc0;
@@ -516,19 +533,20 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                     o[mt][2] *= sc0;
                     o[mt][3] *= sc1;
                 }
+                zp[0] *= sc0;
+                zp[1] *= sc1;
+                zp[2] *= sc0;
+                zp[3] *= sc1;
             }
-            uint32_t pb[2][2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                pb[j][0] = movmatrix_t(pack_f16(pj[j][0], pj[j][1]));
-                pb[j][1] = movmatrix_t(pack_f16(pj[j][2], pj[j][3]));
-            }
-            // O^T += V^T . P^T per block; m-tile m: channels 16m .. 16m+15,
-            // channel group m/2
+            // ---- O^T += V^T . P^T per block.  Values are s_t * code + z_t per
+            // token and 32-channel group: the codes (as code/2) against P^T
+            // scaled by 2 s_t of the m-tile's channel group; the zero term,
+            // one value per (channel group, head), by one MMA whose rows are
+            // the four channel groups, into zp (added to O at the item's end)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const uint4 vw4 = lds128(base + 1024 + (j * 32 + lane) * 16);
-                // V (scale, zero) pairs: token pairs tq and tq + 4, channel groups 0..3
+                // (scale, zero) pairs: token pairs tq and tq + 4, channel groups 0..3
                 uint32_t vm[2][8];
 #pragma unroll
                 for (int hp = 0; hp < 2; ++hp) {
@@ -549,15 +567,24 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                         kissue_next(a, cur, nxt, have_nxt, c_in_nxt, c_grp, rg, ring_u32, bars[warp], lane);
                 }
                 const uint32_t vw[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
-                const uint32_t vx[4] = {vw4.x >> 10, vw4.y >> 10, vw4.z >> 10, vw4.w >> 10};
+                const uint32_t p20 = hadd2u(pb[j][0], pb[j][0]), p21 = hadd2u(pb[j][1], pb[j][1]);
+                uint32_t z0 = 0, z2 = 0;    // row gq = channel group gq (rows 4..15 zero)
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    const int w = mt >> 1, cg = mt >> 1, i = 4 * (mt & 1);
-                    mma_f16(o[mt], kdq(vw[w], vx[w], i, vm[0][2 * cg], vm[0][2 * cg + 1]),
-                            kdq(vw[w], vx[w], i + 1, vm[0][2 * cg], vm[0][2 * cg + 1]),
-                            kdq(vw[w], vx[w], i + 2, vm[1][2 * cg], vm[1][2 * cg + 1]),
-                            kdq(vw[w], vx[w], i + 3, vm[1][2 * cg], vm[1][2 * cg + 1]), pb[j][0], pb[j][1]);
+                for (int cg = 0; cg < 4; ++cg) {
+                    const uint32_t b0 = hmul2u(p20, vm[0][2 * cg]), b1 = hmul2u(p21, vm[1][2 * cg]);
+                    if (gq == static_cast<uint32_t>(cg)) {
+                        z0 = vm[0][2 * cg + 1];
+                        z2 = vm[1][2 * cg + 1];
+                    }
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int mt = 2 * cg + half;
+                        uint32_t a0, a1, a2, a3;
+                        e2m1x4(half ? ((vw[cg] >> 2) & kCodeMask) : (vw[cg] & kCodeMask), a0, a1, a2, a3);
+                        mma_f16(o[mt], a0, a1, a2, a3, b0, b1);
+                    }
                 }
+                mma_f16(zp, z0, 0u, z2, 0u, pb[j][0], pb[j][1]);
             }
             if (gi == claim_at && !have_nxt) {
                 nxt = prepare_kitem(a, claim(), lane);
@@ -568,6 +595,20 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
             }
         }
 
+        // the values' zero term: channel group cg's (head h0, h1) sums sit in
+        // lane 4 cg + tq; every channel of the group receives them
+#pragma unroll
+        for (int cg = 0; cg < 4; ++cg) {
+            const float v0 = __shfl_sync(0xffffffffu, zp[0], 4 * cg + tq);
+            const float v1 = __shfl_sync(0xffffffffu, zp[1], 4 * cg + tq);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                o[2 * cg + half][0] += v0;
+                o[2 * cg + half][1] += v1;
+                o[2 * cg + half][2] += v0;
+                o[2 * cg + half][3] += v1;
+            }
+        }
         const uint32_t part = it.part;
         if (gq == 0) {
             a.w.part_ml[part * kMaxGroup + h0] = make_float2(m0, l0);

@@ -756,15 +756,16 @@ def test_kivi_tile_layout_hand_offsets():
     sv = rng.uniform(0.1, 1, (32, 4)).astype(np.float16)
     zv = rng.uniform(-1, 1, (32, 4)).astype(np.float16)
     tile = np.frombuffer(O.kivi_group_tile(ck, sk, zk, cv, sv, zv), "<u4")
-    # K: token 9 = block 0, g = 1, word 2 (row g+8); dim 37 = t 1, half 0, i 5
-    lane, w = 4 * 1 + 1, 2
-    assert (tile[(0 * 32 + lane) * 4 + w] >> 10) & 3 == ck[9, 37]
-    # K: token 24 = block 1, g = 0, word 3 (row 8, half 1); dim 90 = t 2, 16 + 10 -> i 10;
-    # lane = 4g + t = 2
-    assert (tile[(1 * 32 + 2) * 4 + 3] >> 20) & 3 == ck[24, 90]
-    # V: block 1, lane (g 3, t 2), word 1, pair 6 -> m 3, e 2: dim 51, tokens 16+4+8 = 28, 29
+    # K: token 9 = block 0, g = 1, row g + 8 (r odd); channel 37 = 32*1 + 2*2 + 1: t 1,
+    # step 2, r = 3 (channels 37, 45), first element -> lane 5, word 1, byte 3, bits 24-25
+    assert (tile[(0 * 32 + 5) * 4 + 1] >> 24) & 3 == ck[9, 37]
+    # K: token 24 = block 1, g = 0, row 8 (r odd); channel 90 = 64 + 16 + 2*1 + 8: t 2,
+    # step 5, r = 1, second element -> lane 2, word 2, byte 1, bits 8 + 4 + 2 = 14
+    assert (tile[(1 * 32 + 2) * 4 + 2] >> 14) & 3 == ck[24, 90]
+    # V: block 1, lane 14 (g 3, t 2), m-tile 3, r = 2: channel 51, tokens 28 and 29 ->
+    # word 1, byte 2, second half of the byte's pairs: bits 18-19 and 22-23
     v = tile[256 + (1 * 32 + 14) * 4 + 1]
-    assert (v >> 12) & 3 == cv[28, 51] and (v >> 28) & 3 == cv[29, 51]
+    assert (v >> 18) & 3 == cv[28, 51] and (v >> 22) & 3 == cv[29, 51]
     # K meta: t 3, half 1, i 2 (ip 1, first of the two) -> channels 114 and 122
     km = tile[512 + ((1 * 4 + 1) * 4 + 3) * 4]
     assert km & 0xFFFF == sk.view(np.uint16)[114] and km >> 16 == sk.view(np.uint16)[122]
