@@ -351,13 +351,15 @@ class Pipeline:
 
     def step(self, kv_row, q, ev=None, mode_flags=None, after_decode=None, phases=True):
         """One decode step.  ev: 5 timing events (step start, after append,
-        after decode, after score, step end); with phases=False only the step
-        boundaries (and, on a demote round, the after-score event) are
-        recorded, so that nothing sits between the step's kernels."""
+        after decode, after score, step end); with phases=False only a demote
+        round records two of them (after score, step end), so that nothing
+        sits between the kernels of the other steps or between steps (an
+        event in the stream stops the next kernel's programmatic early
+        launch)."""
         K, ctx, torch = self.K, self.ctx, self.torch
         main = torch.cuda.current_stream()
         sh, side = main.cuda_stream, self.side.cuda_stream    # raw handles: no lookups per call
-        if ev:
+        if ev and phases:
             ev[0].record(main)
         paused = set()
         if self.gather == "prefetch":
@@ -428,7 +430,7 @@ class Pipeline:
             else:
                 for sid, _ in keys:
                     self.holes[sid] = self.holes.get(sid, 0) + 1
-        if ev:
+        if ev and (phases or demoting):
             ev[4].record(main)
         return r
 

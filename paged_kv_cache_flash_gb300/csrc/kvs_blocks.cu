@@ -128,6 +128,8 @@ __global__ void append_step_kernel(const Geo g, const uint16_t *k, const uint16_
                                    const StepAppend *sa_dev, const __grid_constant__ StepAppendInline inl,
                                    uint32_t nseq, uint32_t rows_total, uint32_t vec_per_row, uint64_t t_create)
 {
+    pdl_wait();                 // the pages, table and records may still be read by earlier kernels
+    pdl_trigger();
     const StepAppend *sa = sa_dev ? sa_dev : inl.e;
     const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const uint64_t nvec = static_cast<uint64_t>(rows_total) * vec_per_row;
@@ -572,10 +574,14 @@ __device__ __forceinline__ uint32_t block_scan_1024(uint32_t f, uint32_t *wsum, 
 // placed by a block scan (list order = record order among the picks), and
 // each picking thread then plans its own list entry -- a page is gathered at
 // its first entry once every record that references it is listed -- as
-// plan_kernel does.  Outputs as select_scatter_kernel + plan_kernel: the
-// list, its records and pages, the plan, the slots, the counts (readback and,
-// through its device mapping, out.count_host), the per-page counters back at
-// 0 / ~0.
+// plan_kernel does.  A page referenced once (the common case: no shared
+// prefix) needs no counting: its one entry leads.  Pages of several
+// references are counted with atomics before the first scan, whose barriers
+// order them before the counts are read; the first entry is the one of the
+// smallest record index, which is the smallest list position.  Outputs as
+// select_scatter_kernel + plan_kernel: the list, its records and pages, the
+// plan, the slots, the counts (readback and, through its device mapping,
+// out.count_host), the per-page counters back at 0 / ~0.
 constexpr uint32_t kSelOneTile = 1024;
 
 __global__ void __launch_bounds__(kSelOneTile)
@@ -594,14 +600,24 @@ __global__ void __launch_bounds__(kSelOneTile)
     pdl_trigger();
     kvs_record rec;
     int32_t page = -1;
+    uint32_t ref = 0, clean = 1;
     bool pk = false;
     if (r < nb_total) {
         rec = recs[idx];
         page = table[idx];
+        if (page >= 0) {
+            ref = w.dev_refcnt[page];
+            clean = w.page_clean[page];
+        }
         pk = picked(mode, rec, r, w.sel_thr, lrfu_c);
     }
+    const bool shared = pk && page >= 0 && ref != 1;
+    if (shared) {
+        atomicAdd(&w.page_cnt[page], 1u);
+        atomicMin(&w.page_first[page], r);
+    }
     uint32_t nsel;
-    const uint32_t pos = block_scan_1024(pk ? 1u : 0u, wsum, &nsel);
+    const uint32_t pos = block_scan_1024(pk ? 1u : 0u, wsum, &nsel);   // its barriers order the atomics
     if (pk) {
         w.sel_ids[pos] = rec.key;
         if (out.ids && pos < out.ids_cap)
@@ -610,43 +626,41 @@ __global__ void __launch_bounds__(kSelOneTile)
         w.sel_pages[pos] = page;
         w.sel_recidx[pos] = r;
         w.sel_full[pos] = (b + 1) * kBlockTokens <= nt ? 1 : 0;
-        if (page >= 0) {
-            atomicAdd(&w.page_cnt[page], 1u);
-            atomicMin(&w.page_first[page], pos);
-        }
     }
     if (threadIdx.x == 0)
         *w.sel_count = nsel;
-    __syncthreads();            // every listed reference of this call is counted
     // ---- plan: each picking thread decides for its own list entry ----
-    uint32_t cnt = 0, ref = 0, lead = 0, dirty = 0;
-    if (pk && page >= 0) {
-        cnt = __ldcg(&w.page_cnt[page]);
-        ref = w.dev_refcnt[page];
-        lead = (cnt == ref && __ldcg(&w.page_first[page]) == pos) ? 1u : 0u;
-        dirty = (lead && mirror && !w.page_clean[page]) ? 1u : 0u;
+    bool whole = pk && page >= 0;            // every reference of the page is listed
+    uint32_t lead = whole ? 1u : 0u;
+    if (shared) {
+        const uint32_t cnt = __ldcg(&w.page_cnt[page]);
+        whole = cnt == ref;
+        lead = (whole && __ldcg(&w.page_first[page]) == r) ? 1u : 0u;
     }
+    const uint32_t dirty = (lead && mirror && !clean) ? 1u : 0u;
     uint32_t tot;
     const uint32_t ex = block_scan_1024(lead | (dirty << 16), wsum, &tot);
     if (lead) {
         const uint32_t ppos = ex & 0xffffu;
         w.plan_pages[ppos] = page;
-        w.page_pos[page] = static_cast<int32_t>(ppos);
+        if (!mirror)
+            w.page_pos[page] = static_cast<int32_t>(ppos);
     }
     if (dirty) {
         w.readback[4 + (ex >> 16)] = static_cast<uint32_t>(page);
         w.page_clean[page] = (b + 1) * kBlockTokens <= nt ? 1 : 0;
     }
-    __syncthreads();            // page_pos of every leader is written
+    if (!mirror)
+        __syncthreads();        // page_pos of every leader is written
     if (pk) {
-        const int32_t v = (page >= 0 && cnt == ref) ? (mirror ? page : __ldcg(&w.page_pos[page])) : -1;
+        const int32_t v = whole ? (mirror ? page : __ldcg(&w.page_pos[page])) : -1;
         w.plan_slot[pos] = v;
         if (out.slots && pos < out.ids_cap)
             out.slots[pos] = v;
-        if (page >= 0) {        // every read of the counters was before the scans' barriers
-            w.page_cnt[page] = 0;
-            w.page_first[page] = 0xffffffffu;
-        }
+    }
+    if (shared) {               // every read of the counters was before the second scan's barriers
+        w.page_cnt[page] = 0;
+        w.page_first[page] = 0xffffffffu;
     }
     if (threadIdx.x == 0) {
         w.readback[0] = nsel;
@@ -1073,6 +1087,8 @@ struct SetBlob {
 
 __global__ void __launch_bounds__(256) set_kernel(const __grid_constant__ SetBlob b, uint32_t nvec, uint4 *dst)
 {
+    pdl_trigger();
+    pdl_wait();                 // earlier kernels of the stream may still read the old set
     for (uint32_t i = threadIdx.x; i < nvec; i += blockDim.x)
         dst[i] = b.v[i];
 }
@@ -1133,9 +1149,9 @@ cudaError_t launch_append_step(const Geo &g, const uint16_t *k, const uint16_t *
         for (uint32_t i = 0; i < nseq; ++i)
             inl.e[i] = sa_host[i];
     }
-    append_step_kernel<<<static_cast<uint32_t>((threads + bs - 1) / bs), bs, 0, s>>>(
-        g, k, v, pool, table, records, page_clean, sa_dev, inl, nseq, rows_total, vec_per_row, t_create);
-    return cudaGetLastError();
+    return launch_pdl(append_step_kernel, dim3(static_cast<uint32_t>((threads + bs - 1) / bs)), dim3(bs), 0, s,
+                      g, k, v, pool, table, records, page_clean, sa_dev, inl, nseq, rows_total, vec_per_row,
+                      t_create);
 }
 
 cudaError_t launch_score(const Geo &g, const Work &w, kvs_record *rec, const float *mass,
@@ -1233,8 +1249,7 @@ cudaError_t launch_set(const void *src, size_t bytes, void *dst, cudaStream_t s)
     std::memset(&b, 0, sizeof b);
     std::memcpy(&b, src, bytes);
     const uint32_t nvec = static_cast<uint32_t>((bytes + 15) / 16);
-    set_kernel<<<1, 256, 0, s>>>(b, nvec, static_cast<uint4 *>(dst));
-    return cudaGetLastError();
+    return launch_pdl(set_kernel, dim3(1), dim3(256), 0, s, b, nvec, static_cast<uint4 *>(dst));
 }
 
 cudaError_t launch_patch(const Geo &g, int32_t *table, kvs_record *rec, uint8_t *page_clean,

@@ -124,8 +124,10 @@ __global__ void __launch_bounds__(256, 8) combine_kernel(const Geo g, const Work
 #pragma unroll 4
     for (uint32_t b = r0 + threadIdx.x; b < r1; b += blockDim.x) {
         float acc = 0.f;
-        for (uint32_t j = 0; j < g.G; ++j)
-            acc += fast_exp2(lb[static_cast<size_t>(j) * nbt + b] - lse_sh[j]);
+#pragma unroll
+        for (uint32_t j = 0; j < kMaxGroup; ++j)
+            if (j < g.G)
+                acc += fast_exp2(lb[static_cast<size_t>(j) * nbt + b] - lse_sh[j]);
         sm[b] = acc;
     }
 }
@@ -146,6 +148,7 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
     const uint32_t r = blockIdx.x * kMassBlocks + i;
     uint32_t slot = 0, b = 0, nb = 0;
     uint64_t seq_id = 0, t = 0;
+    kvs_record rec;
     if (r < nb_total && j == 0) {       // the decode set: uploaded before the decode kernel
         const uint32_t ci = find_seq(&ds->seq[0].blk_off, sizeof(DSeq) / 4, ds->nseq, r);
         slot = ds->seq[ci].slot;
@@ -153,6 +156,10 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
         nb = ds->seq[ci].nb;
         seq_id = ds->seq[ci].seq_id;
         t = ds->t;
+        // the record: final before the decode kernel started (nothing between
+        // it and this kernel writes records)
+        if (score)
+            rec = recs[static_cast<size_t>(slot) * g.mb + b];
     }
     pdl_wait();
     pdl_trigger();
@@ -175,7 +182,7 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
         const float M = part[0][i] / static_cast<float>(g.L * g.Hq);
         mass[idx] = M;
         if (score)
-            score_record(sa, recs, idx, seq_id, b, nb, t, M, w.err);
+            score_loaded(sa, rec, recs + idx, seq_id, b, nb, t, M, w.err);
     }
 }
 
@@ -185,8 +192,10 @@ cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nse
                            uint32_t max_nchunk, cudaStream_t s)
 {
     // a merge of many chunks gets a CTA of its own; a short one shares CTA 0
-    // with the first block range
-    const uint32_t split = max_nchunk > 16 ? 1u : 0u;
+    // with the first block range (one CTA per stream while a sequence has at
+    // most kMassRange blocks: 8 per SM at 32 registers a thread, so that 640
+    // streams run in one wave)
+    const uint32_t split = max_nchunk > 32 ? 1u : 0u;
     const dim3 grid(nseq * g.L * g.Hkv, split + (max_nb + kMassRange - 1) / kMassRange);
     if (g.d == 128)
         return launch_pdl(combine_kernel<128>, grid, dim3(32 * kMaxGroup), 0, s, g, w, out, split);

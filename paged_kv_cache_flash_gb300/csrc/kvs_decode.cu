@@ -37,6 +37,7 @@
 #include <cuda_bf16.h>
 
 #include "kvs_internal.h"
+#include "kvs_pdl.cuh"
 #include "kvs_ptx.h"
 
 namespace kvs {
@@ -204,10 +205,11 @@ __device__ __forceinline__ bool issue_next(const CUtensorMap *tmap, const Geo &g
         const uint32_t bar = smem_u32(&bars[st]);
         mbar_expect_tx(bar, T::kStageBytes);
         const int c4 = page * static_cast<int>(g.L) + static_cast<int>(l);
+        const uint64_t pol = l2_evict_first();      // pages are read once per step
 #pragma unroll
         for (int h = 0; h < T::kHalf; ++h)
             tma_load_5d(ring_u32 + st * T::kStageBytes + h * T::kBoxBytes, tmap, bar,
-                        h * T::kBoxElems, 0, static_cast<int>(kv), 0, c4);
+                        h * T::kBoxElems, 0, static_cast<int>(kv), 0, c4, pol);
     }
     ++c_blk;
     ++rg.inflight;
@@ -228,6 +230,10 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[8][kStages];
 
+    // the combine kernel (a programmatic dependent) may place its CTAs beside
+    // this persistent grid now: they wait for its completion, and start at
+    // once when it completes
+    pdl_trigger();
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -215,7 +215,9 @@ struct StepAppendInline {
 // items are claimed chunk by chunk (every stream's chunk 0, then chunk 1, ...):
 // the small chunks come last, so that when the large ones run out every warp
 // still finds short work and the launch ends evenly.  `tail` makes the small
-// chunks of all streams at least one large chunk per warp.
+// chunks of all streams at least half a large chunk per warp: when the large
+// items run out, a warp has on average half of one left, so that much short
+// work per warp evens the finish (a larger tail only adds partials and items).
 struct PageChunks {
     uint32_t big, small, tail;
     uint32_t nbig(uint32_t n) const { return n > tail ? (n - tail) / big : 0; }
@@ -243,7 +245,7 @@ inline PageChunks pick_page_chunks(const uint32_t *nres, uint32_t n, uint32_t L,
             PageChunks pc;
             pc.big = c;
             pc.small = sm;
-            const uint64_t t = (static_cast<uint64_t>(workers) * c + streams - 1) / streams;
+            const uint64_t t = (static_cast<uint64_t>(workers) * c / 2 + streams - 1) / streams;
             pc.tail = static_cast<uint32_t>((t + sm - 1) / sm * sm);
             uint64_t parts = extra_parts;
             big_items = 0;

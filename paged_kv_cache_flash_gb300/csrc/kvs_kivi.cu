@@ -52,6 +52,7 @@
 #include <cuda_fp16.h>
 
 #include "kvs_internal.h"
+#include "kvs_pdl.cuh"
 #include "kvs_ptx.h"
 
 namespace kvs {
@@ -298,7 +299,7 @@ __device__ __forceinline__ bool kissue_next(const KArgs &a, const KPrep &cur, co
         mbar_expect_tx(bar, kTile);
         const uint8_t *src = a.gpool + static_cast<uint64_t>(gp) * a.g.group_page_bytes +
                              (static_cast<uint64_t>(pp.it.l) * a.g.Hkv + pp.it.kvh) * kTile;
-        bulk_load(ring_u32 + st * kTile, src, kTile, bar);
+        bulk_load(ring_u32 + st * kTile, src, kTile, bar, l2_evict_first());
     }
     ++c_grp;
     ++rg.inflight;
@@ -358,6 +359,7 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
 {
     extern __shared__ __align__(1024) uint8_t ksm_raw[];
     __shared__ __align__(8) uint64_t bars[kKWarps][kKRing];
+    pdl_trigger();              // lets a programmatically dependent combine place its CTAs
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ksm_raw) + 127) & ~uintptr_t(127));
     const uint32_t ring_u32 = smem_u32(smem + warp * kKRing * kTile);

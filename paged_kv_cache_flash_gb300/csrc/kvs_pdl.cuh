@@ -1,6 +1,6 @@
-// Programmatic dependent launch for the short kernels that follow the decode
-// kernel in a step (block mass, scoring, selection, gather plan, mirror
-// copy).
+// Programmatic dependent launch for the short kernels of a step: the token
+// append and the decode-set upload ahead of the decode kernel, and block
+// mass, scoring, selection, gather plan and mirror copy after it.
 //
 // A kernel launched with launch_pdl() may be scheduled while the kernel
 // before it in the stream is still running: its CTAs start, do what depends
@@ -12,9 +12,15 @@
 //     earlier kernel of the stream may still write, and before it exits (so
 //     that the grid completes only after its predecessor has, which keeps
 //     the ordering transitive along the chain);
-//   - before pdl_wait() it reads only data that was complete before the
-//     chain's first normally-launched kernel started (the decode set, which
-//     a copy ahead of the decode kernel uploads).
+//   - before pdl_wait() it reads only data that was final before the last
+//     normally-launched kernel ahead of it started: the decode set and the
+//     block records, final before the decode kernel (a normal launch) starts.
+//     The set upload and the token append are launched this way too, but
+//     touch memory only after their own pdl_wait(), and a normally-launched
+//     kernel (the decode kernel, or the mass copy of a debug set) follows
+//     every set upload before anything reads the set.
+// The decode kernels trigger their dependents at their start, so that the
+// combine kernel's CTAs are in place when the decode completes.
 // After a copy or an event in the stream the attribute has no effect: the
 // kernel starts after everything before it, as a plain launch would.
 #pragma once

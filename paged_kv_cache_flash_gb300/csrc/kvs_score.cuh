@@ -26,15 +26,15 @@ __device__ __forceinline__ double lrfu_decay(double alpha, uint64_t dt)
     return res;
 }
 
-// Scores block b of a sequence (its record at `idx`) from its fp32 mass M at
-// step t: fp64, every operation rounded on its own (no fused multiply-add),
-// in the order EMA, touch, recency, anchor, P, tier.  nb: the sequence's
-// block count.  A record that does not carry (seq_id, b) or whose touch time
-// lies after t is left alone and flagged in the error word.
-__device__ __forceinline__ void score_record(const ScoreArgs &sa, kvs_record *recs, size_t idx, uint64_t seq_id,
+// Scores block b of a sequence from its fp32 mass M at step t: rec is its
+// record as loaded, dst where the scored record goes.  fp64, every operation
+// rounded on its own (no fused multiply-add), in the order EMA, touch,
+// recency, anchor, P, tier.  nb: the sequence's block count.  A record that
+// does not carry (seq_id, b) or whose touch time lies after t is left alone
+// and flagged in the error word.
+__device__ __forceinline__ void score_loaded(const ScoreArgs &sa, kvs_record rec, kvs_record *dst, uint64_t seq_id,
                                              uint32_t b, uint32_t nb, uint64_t t, float mass, uint32_t *err)
 {
-    kvs_record rec = recs[idx];
     if (rec.key.block_idx != b || rec.key.seq_id != seq_id || rec.last_touch > t) {
         atomicOr(err, kErrBadRecord);
         return;
@@ -58,7 +58,13 @@ __device__ __forceinline__ void score_record(const ScoreArgs &sa, kvs_record *re
     rec.prio = P;
     rec.tier = P >= sa.hi ? 0 : (P >= sa.lo ? 1 : 2);
     rec.mass = mass;
-    recs[idx] = rec;
+    *dst = rec;
+}
+
+__device__ __forceinline__ void score_record(const ScoreArgs &sa, kvs_record *recs, size_t idx, uint64_t seq_id,
+                                             uint32_t b, uint32_t nb, uint64_t t, float mass, uint32_t *err)
+{
+    score_loaded(sa, recs[idx], recs + idx, seq_id, b, nb, t, mass, err);
 }
 
 }  // namespace kvs

@@ -40,7 +40,7 @@ def rule(nres, L, H, workers, cap, extra):
         for sm in (16, 32, 64, 128):
             if sm > c:
                 break
-            t = -(-workers * c // streams)
+            t = -(-(workers * c // 2) // streams)
             tail = -(-t // sm) * sm
             parts = extra + sum(L * H * len(chunks(m, c, sm, tail)) for m in nres)
             if parts <= cap:
@@ -81,10 +81,10 @@ def test_plan_follows_rule_and_covers_every_stream(case):
         return
     assert big in SIZES and small >= MIN_SMALL and small <= big and small & (small - 1) == 0
     assert tail % small == 0
-    # the short chunks of every stream cover at least its share of one large
-    # chunk per warp
+    # the short chunks of every stream cover at least its share of half a
+    # large chunk per warp
     streams = len(nres) * L * H
-    assert tail * streams >= workers * big
+    assert 2 * tail * streams >= workers * big - 1
     parts = extra
     for m in nres:
         c = chunks(m, big, small, tail)
@@ -99,18 +99,20 @@ def test_plan_follows_rule_and_covers_every_stream(case):
 
 def test_bench_workloads():
     # 70B shape (80 layers x 8 KV heads): 1,216 bf16 decode warps, 1,824 FP8 / 2-bit
-    assert K.debug_chunk_plan([513], 80, 8, 1216, 10 ** 9) == (128, 16, 256)
-    assert K.debug_chunk_plan([8193], 80, 8, 1216, 10 ** 9) == (128, 16, 256)
-    assert K.debug_chunk_plan([513], 80, 8, 1824, 10 ** 9) == (64, 16, 192)
+    assert K.debug_chunk_plan([513], 80, 8, 1216, 10 ** 9) == (128, 16, 128)
+    assert K.debug_chunk_plan([8193], 80, 8, 1216, 10 ** 9) == (128, 16, 128)
+    assert K.debug_chunk_plan([513], 80, 8, 1824, 10 ** 9) == (64, 16, 96)
     # a small call gets short chunks only
     big, small, tail = K.debug_chunk_plan([17], 2, 2, 1216, 10 ** 9)
     assert chunks(17, big, small, tail) == [16, 1]
 
 
 def test_short_chunks_grow_when_partials_are_scarce():
-    # 8K: 11 x 640 partials with 32-block short chunks, 19 x 640 with 16
-    assert K.debug_chunk_plan([513], 80, 8, 1216, 640 * 19) == (128, 16, 256)
-    assert K.debug_chunk_plan([513], 80, 8, 1216, 640 * 12) == (128, 32, 256)
+    # 8K: 8 x 640 partials with 32-block short chunks (3 x 128 + 4 x 32 + 1),
+    # 12 x 640 with 16 (3 x 128 + 8 x 16 + 1)
+    assert K.debug_chunk_plan([513], 80, 8, 1216, 640 * 12) == (128, 16, 128)
+    assert K.debug_chunk_plan([513], 80, 8, 1216, 640 * 11) == (128, 32, 128)
+    assert K.debug_chunk_plan([513], 80, 8, 1216, 640 * 8) == (128, 32, 128)
     assert K.debug_chunk_plan([513], 80, 8, 1216, 100) == (0, 0, 0)
 
 
