@@ -70,6 +70,10 @@ def parse():
                     help="128K workload only: skip the batched workload's line under \"batched\"")
     ap.add_argument("--cpu-layers", type=int, default=8,
                     help="layers of the workload in the CPU-baseline sample")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling cut: the workload's first N layers only (same sequences; a "
+                         "decode launch's reads scale by L / N).  Not a bench figure of the named "
+                         "workload (its line carries no traffic figure)")
     return ap.parse_args()
 
 
@@ -557,6 +561,8 @@ def measure(args, wname, dev, ws, rank, local, sub=False):
     import torch
     import workloads as W
     wl = W.workload(wname)
+    if args.layers:
+        wl = wl.with_(L=args.layers)
     alpha = args.alpha if args.alpha is not None else wl.alphas[-1]
     gather = args.gather
     if gather == "auto":
@@ -657,7 +663,7 @@ def measure(args, wname, dev, ws, rank, local, sub=False):
     algo = kv_bytes / K_ + wl.nseq * wl.L * wl.Hq * wl.d * 2 + sum(nb) * 4
     achieved = algo / (dec_avg / 1e3) / 1e9
     peak, peak_src = read_peaks()
-    traffic = read_traffic(wname, args.kv_dtype)
+    traffic = None if args.layers else read_traffic(wname, args.kv_dtype)
 
     # ---- end to end through host buffers --------------------------------
     e2e = None
