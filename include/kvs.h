@@ -107,7 +107,7 @@ typedef enum kvs_kv_dtype {
  * 0 when scale is 0).  Attention reads fp16(code*scale + zero) (one
  * rounding).  A group page holds, per (layer, KV head), 3072 bytes: K codes,
  * V codes, K (scale, zero) per channel, V (scale, zero) per token and channel
- * group -- 3 bits per element.  The table entry of a quantised block is
+ * group, each scale stored doubled (exact in fp16) -- 3 bits per element.  The table entry of a quantised block is
  * KVS_TABLE_GROUP(g) for its group page g (both blocks of the group).
  * KIVI contexts share no blocks between sequences and gather no pages
  * (kvs_select_and_gather returns the id list only: no host_dst, flags 0 or

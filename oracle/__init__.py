@@ -357,6 +357,7 @@ def kivi_group_tile(ck, sk, zk, cv, sv, zv) -> bytes:
       V meta   [2560, 3072): [block j][token pair p in 0..7][channel group
                              c in 0..3] of (scale pair, zero pair): tokens
                              16j + 2p (low) and 16j + 2p + 1 (high).
+      Every scale is stored doubled, 2 * scale (exact in fp16).
 
     ck, cv: codes [32][d]; sk, zk: [d]; sv, zv: [32][d/32]."""
     ck = np.asarray(ck, np.uint32)
@@ -389,7 +390,8 @@ def kivi_group_tile(ck, sk, zk, cv, sv, zv) -> bytes:
 
     kc, vc = words(k_pair), words(v_pair)
     f16 = lambda a: np.asarray(a, np.float16).view(np.uint16).astype(np.uint32)
-    skb, zkb = f16(sk), f16(zk)
+    two = np.float16(2.0)
+    skb, zkb = f16(np.asarray(sk, np.float16) * two), f16(zk)
     km = np.zeros((2, 4, 4, 2, 2), np.uint32)
     for h in range(2):
         for ip in range(4):
@@ -398,7 +400,7 @@ def kivi_group_tile(ck, sk, zk, cv, sv, zv) -> bytes:
                     ch = 32 * t + 16 * h + 2 * ip + di
                     km[h, ip, t, di, 0] = skb[ch] | (skb[ch + 8] << 16)
                     km[h, ip, t, di, 1] = zkb[ch] | (zkb[ch + 8] << 16)
-    svb, zvb = f16(sv), f16(zv)
+    svb, zvb = f16(np.asarray(sv, np.float16) * two), f16(zv)
     vm = np.zeros((2, 8, 4, 2), np.uint32)
     for j in range(2):
         for p_ in range(8):

@@ -36,6 +36,8 @@
 // byte k of word w carries register k of step 2w (fields 0-1 and 4-5, first
 // element low) and register k of step 2w + 1 (fields 2-3 and 6-7), so
 // (w & 0x33333333) and ((w >> 2) & 0x33333333) are each four FP4 pairs.
+// Scales are held doubled (2s, exact in fp16), the factor the code/2 operands
+// need.
 //   [0, 1024)    K codes [block j][lane][word w]: step s = k-step s (16
 //                channels), register r: token 16j + g + 8(r%2), channels
 //                (c, c+8) for r < 2 and (c+1, c+9) for r >= 2,
@@ -43,11 +45,11 @@
 //   [1024, 2048) V codes [block j][lane][word w]: step s = m-tile s,
 //                register r: channel 16s + g + 8(r%2), tokens 16j + 2t +
 //                8(r/2) and the next one.
-//   [2048, 2560) K (scale pair, zero pair) [h][ip][t][i = 2ip, 2ip+1]:
+//   [2048, 2560) K (2 x scale pair, zero pair) [h][ip][t][i = 2ip, 2ip+1]:
 //                channels 32t + 16h + i (low half) and + 8 (high half); the
 //                four t of one (h, ip) are 64 contiguous bytes, so the 16-byte
 //                loads of the lanes t = 0..3 fall in different banks.
-//   [2560, 3072) V (scale pair, zero pair) [block j][token pair p][channel
+//   [2560, 3072) V (2 x scale pair, zero pair) [block j][token pair p][channel
 //                group c]: tokens 16j + 2p (low) and 16j + 2p + 1 (high).
 #include <cuda_fp16.h>
 
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(128)
                 c = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(x[t], zf), sf)), 0), 3);
             kc[t][tid] = static_cast<uint8_t>(c);
         }
-        sk[tid] = h_bits(s16);
+        sk[tid] = h_bits(__hadd(s16, s16));    // the tile holds 2s (exact)
         zk[tid] = h_bits(z16);
     }
     // values: thread = (token, channel group), over 32 channels
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(128)
                 c = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(x[e], zf), sf)), 0), 3);
             vc[t][32 * cg + e] = static_cast<uint8_t>(c);
         }
-        sv[t][cg] = h_bits(s16);
+        sv[t][cg] = h_bits(__hadd(s16, s16));
         zv[t][cg] = h_bits(z16);
     }
     __syncthreads();
@@ -334,13 +336,14 @@ __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c)
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-__device__ __forceinline__ uint32_t hadd2u(uint32_t a, uint32_t b)
-{
-    const __half2 r = __hadd2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
-    return *reinterpret_cast<const uint32_t *>(&r);
-}
-
 constexpr uint32_t kCodeMask = 0x33333333u;    // the low fields of both nibbles of every byte
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
@@ -454,7 +457,7 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                 for (int ks = 0; ks < 8; ++ks) {
                     // (scale, zero) pairs of the k-step's channels (c, c+8) and (c+1, c+9)
                     const uint4 m = lds128(base + 2048 + (ks * 4 + tq) * 16);
-                    const uint32_t sa = hadd2u(m.x, m.x), sb = hadd2u(m.z, m.z);
+                    const uint32_t sa = m.x, sb = m.z;        // 2 s (the tile holds 2s)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const uint32_t wd = kw[j][ks >> 1];
@@ -569,15 +572,16 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                         kissue_next(a, cur, nxt, have_nxt, c_in_nxt, c_grp, rg, ring_u32, bars[warp], lane);
                 }
                 const uint32_t vw[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
-                const uint32_t p20 = hadd2u(pb[j][0], pb[j][0]), p21 = hadd2u(pb[j][1], pb[j][1]);
-                uint32_t z0 = 0, z2 = 0;    // row gq = channel group gq (rows 4..15 zero)
+                // zero pairs of channel group gq (A row gq; rows 4..15 zero):
+                // token pairs tq and tq + 4
+                const uint32_t za = base + 2560 + ((j * 8 + tq) * 4 + (gq & 3)) * 8 + 4;
+                uint32_t z0 = lds32(za), z2 = lds32(za + 4 * 4 * 8);
+                if (gq >= 4)
+                    z0 = z2 = 0;
 #pragma unroll
                 for (int cg = 0; cg < 4; ++cg) {
-                    const uint32_t b0 = hmul2u(p20, vm[0][2 * cg]), b1 = hmul2u(p21, vm[1][2 * cg]);
-                    if (gq == static_cast<uint32_t>(cg)) {
-                        z0 = vm[0][2 * cg + 1];
-                        z2 = vm[1][2 * cg + 1];
-                    }
+                    // P^T times 2 s_t (the tile holds 2s) of the channel group
+                    const uint32_t b0 = hmul2u(pb[j][0], vm[0][2 * cg]), b1 = hmul2u(pb[j][1], vm[1][2 * cg]);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int mt = 2 * cg + half;

@@ -786,9 +786,16 @@ def test_kivi_tile_layout_hand_offsets():
     # word 1, byte 2, second half of the byte's pairs: bits 18-19 and 22-23
     v = tile[256 + (1 * 32 + 14) * 4 + 1]
     assert (v >> 18) & 3 == cv[28, 51] and (v >> 22) & 3 == cv[29, 51]
-    # K meta: t 3, half 1, i 2 (ip 1, first of the two) -> channels 114 and 122
+    # K meta: t 3, half 1, i 2 (ip 1, first of the two) -> channels 114 and 122,
+    # scales stored doubled (exact in fp16)
     km = tile[512 + ((1 * 4 + 1) * 4 + 3) * 4]
-    assert km & 0xFFFF == sk.view(np.uint16)[114] and km >> 16 == sk.view(np.uint16)[122]
+    s2 = (sk * np.float16(2)).view(np.uint16)
+    assert km & 0xFFFF == s2[114] and km >> 16 == s2[122]
+    assert np.array_equal(s2.view(np.float16).astype(np.float64), 2 * sk.astype(np.float64))
+    # V meta: block 0, token pair 3, channel group 1 -> doubled scales of tokens 6, 7
+    vs = tile[640 + ((0 * 8 + 3) * 4 + 1) * 2]
+    v2 = (sv * np.float16(2)).view(np.uint16)
+    assert vs & 0xFFFF == v2[6, 1] and vs >> 16 == v2[7, 1]
     # V meta: block 1, token pair 5, channel group 2 -> zero of tokens 26, 27
     vm = tile[640 + ((1 * 8 + 5) * 4 + 2) * 2 + 1]
     assert vm & 0xFFFF == zv.view(np.uint16)[26, 2] and vm >> 16 == zv.view(np.uint16)[27, 2]
