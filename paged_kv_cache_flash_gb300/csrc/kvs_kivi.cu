@@ -439,8 +439,16 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
         for (int mt = 0; mt < 8; ++mt)
             o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         float zp[4] = {0.f, 0.f, 0.f, 0.f};      // zero term of the values: [channel group gq][heads h0, h1]
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float *lse_row0 = a.w.lse_blk + (static_cast<size_t>(it.l) * g.Hq + kvh * G + h0) * nb_total + it.lse0;
+        float m0 = -INFINITY, m1 = -INFINITY;
+        // the weight sum of one block of one head per lane (see the reduction
+        // below): lanes gq = 0, 2, 4, 6 of each column write the per-block
+        // log2-sum-exp of block (gq & 4 ? 1 : 0) of head (gq & 2 ? h1 : h0)
+        const bool wb = gq & 4, wh = gq & 2;
+        float lpart = 0.f;
+        float *lse_w = nullptr;
+        if (!(gq & 1) && (wh ? h1 : h0) < G)
+            lse_w = a.w.lse_blk + (static_cast<size_t>(it.l) * g.Hq + kvh * G + (wh ? h1 : h0)) * nb_total +
+                    it.lse0 + (wb ? 1 : 0);
 
         for (uint32_t gi = 0; gi < it.ng; ++gi) {
             mbar_wait(smem_u32(&bars[warp][rg.st_cons]), rg.ph_cons, a.w.err);
@@ -503,31 +511,26 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                 pb[j][0] = movmatrix_t(pack_f16(pj[j][0], pj[j][1]));
                 pb[j][1] = movmatrix_t(pack_f16(pj[j][2], pj[j][3]));
             }
-            // per-block sums of the (fp32) weights, per head, over the 8 lanes
-            // of the head's column
-            float w00 = pj[0][0] + pj[0][2], w01 = pj[0][1] + pj[0][3];   // block 0: heads h0, h1
-            float w10 = pj[1][0] + pj[1][2], w11 = pj[1][1] + pj[1][3];   // block 1
-#pragma unroll
-            for (int x = 4; x < 32; x <<= 1) {
-                w00 += __shfl_xor_sync(0xffffffffu, w00, x);
-                w01 += __shfl_xor_sync(0xffffffffu, w01, x);
-                w10 += __shfl_xor_sync(0xffffffffu, w10, x);
-                w11 += __shfl_xor_sync(0xffffffffu, w11, x);
+            // per-block sums of the (fp32) weights over the 8 lanes of a head's
+            // column, reduced transposed: at each level a lane keeps half of
+            // its sums and passes the other half, so that lane gq ends with
+            // the sum of block (gq & 4) for head (gq & 2 ? h1 : h0)
+            {
+                const float w00 = pj[0][0] + pj[0][2], w01 = pj[0][1] + pj[0][3];   // block 0: h0, h1
+                const float w10 = pj[1][0] + pj[1][2], w11 = pj[1][1] + pj[1][3];   // block 1
+                float k0 = wb ? w10 : w00, k1 = wb ? w11 : w01;
+                k0 += __shfl_xor_sync(0xffffffffu, wb ? w00 : w10, 16);
+                k1 += __shfl_xor_sync(0xffffffffu, wb ? w01 : w11, 16);
+                float v = wh ? k1 : k0;
+                v += __shfl_xor_sync(0xffffffffu, wh ? k0 : k1, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                const float mnw = wh ? mn1 : mn0;
+                lpart = lpart * (wh ? sc1 : sc0) + v;      // this lane's block of its head
+                if (lse_w)
+                    lse_w[2 * gi] = mnw + fast_log2(v);
             }
-            l0 = l0 * sc0 + (w00 + w10);
-            l1 = l1 * sc1 + (w01 + w11);
             m0 = mn0;
             m1 = mn1;
-            if (gq == 0) {
-                if (h0 < G) {
-                    lse_row0[2 * gi] = mn0 + fast_log2(w00);
-                    lse_row0[2 * gi + 1] = mn0 + fast_log2(w10);
-                }
-                if (h1 < G) {
-                    lse_row0[nb_total + 2 * gi] = mn1 + fast_log2(w01);
-                    lse_row0[nb_total + 2 * gi + 1] = mn1 + fast_log2(w11);
-                }
-            }
             // the rescale only after a merge of the maxima (otherwise every
             // factor is 2^0); `moved` is the same in every lane
             if (moved) {
@@ -615,6 +618,10 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                 o[2 * cg + half][3] += v1;
             }
         }
+        // the heads' weight sums: both blocks' parts (lanes 16 apart), then
+        // head h1's from lane gq = 2 to lane gq = 0
+        const float lhead = lpart + __shfl_xor_sync(0xffffffffu, lpart, 16);
+        const float l1 = __shfl_xor_sync(0xffffffffu, lhead, 8), l0 = lhead;
         const uint32_t part = it.part;
         if (gq == 0) {
             a.w.part_ml[part * kMaxGroup + h0] = make_float2(m0, l0);
