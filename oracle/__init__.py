@@ -354,9 +354,10 @@ def kivi_group_tile(ck, sk, zk, cv, sv, zv) -> bytes:
                              zero pair) for i = 2ip, then for i = 2ip + 1;
                              each pair two fp16: channel 32t + 16h + i
                              (low), that channel + 8 (high).
-      V meta   [2560, 3072): [block j][token pair p in 0..7][channel group
-                             c in 0..3] of (scale pair, zero pair): tokens
-                             16j + 2p (low) and 16j + 2p + 1 (high).
+      V meta   [2560, 2816): scale pairs [block j][token pair p in 0..7]
+                             [channel group c in 0..3]: tokens 16j + 2p
+                             (low) and 16j + 2p + 1 (high);
+               [2816, 3072): zero pairs, the same order.
       Every scale is stored doubled, 2 * scale (exact in fp16).
 
     ck, cv: codes [32][d]; sk, zk: [d]; sv, zv: [32][d/32]."""
@@ -401,13 +402,13 @@ def kivi_group_tile(ck, sk, zk, cv, sv, zv) -> bytes:
                     km[h, ip, t, di, 0] = skb[ch] | (skb[ch + 8] << 16)
                     km[h, ip, t, di, 1] = zkb[ch] | (zkb[ch + 8] << 16)
     svb, zvb = f16(np.asarray(sv, np.float16) * two), f16(zv)
-    vm = np.zeros((2, 8, 4, 2), np.uint32)
+    vm = np.zeros((2, 2, 8, 4), np.uint32)        # [scales, zeros][j][p][c]
     for j in range(2):
         for p_ in range(8):
             for c in range(4):
                 a = 16 * j + 2 * p_
-                vm[j, p_, c, 0] = svb[a, c] | (svb[a + 1, c] << 16)
-                vm[j, p_, c, 1] = zvb[a, c] | (zvb[a + 1, c] << 16)
+                vm[0, j, p_, c] = svb[a, c] | (svb[a + 1, c] << 16)
+                vm[1, j, p_, c] = zvb[a, c] | (zvb[a + 1, c] << 16)
     out = b"".join(x.astype("<u4").tobytes() for x in (kc, vc, km, vm))
     assert len(out) == KIVI_TILE_BYTES
     return out

@@ -49,8 +49,9 @@
 //                channels 32t + 16h + i (low half) and + 8 (high half); the
 //                four t of one (h, ip) are 64 contiguous bytes, so the 16-byte
 //                loads of the lanes t = 0..3 fall in different banks.
-//   [2560, 3072) V (2 x scale pair, zero pair) [block j][token pair p][channel
-//                group c]: tokens 16j + 2p (low) and 16j + 2p + 1 (high).
+//   [2560, 2816) V 2 x scale pairs [block j][token pair p][channel group c]:
+//                tokens 16j + 2p (low) and 16j + 2p + 1 (high);
+//   [2816, 3072) V zero pairs, the same order.
 #include <cuda_fp16.h>
 
 #include "kvs_internal.h"
@@ -185,10 +186,11 @@ __global__ void __launch_bounds__(128)
         const uint32_t ch = 32 * tq + 16 * hh + 2 * ip + di;
         const uint16_t *src = which ? zk : sk;
         tile[512 + tid] = static_cast<uint32_t>(src[ch]) | (static_cast<uint32_t>(src[ch + 8]) << 16);
-        // V meta: ((j * 8 + p) * 4 + c) * 2 + which
-        const uint32_t cg = (tid >> 1) & 3, p = (tid >> 3) & 7, j = tid >> 6;
+        // V meta: the scales, then the zeros, each [j][p][c]: vwhich * 64 +
+        // (j * 8 + p) * 4 + c
+        const uint32_t vwhich = tid >> 6, cg = tid & 3, p = (tid >> 2) & 7, j = (tid >> 5) & 1;
         const uint32_t tok = 16 * j + 2 * p;
-        const uint16_t(*vsrc)[4] = which ? zv : sv;
+        const uint16_t(*vsrc)[4] = vwhich ? zv : sv;
         tile[640 + tid] = static_cast<uint32_t>(vsrc[tok][cg]) | (static_cast<uint32_t>(vsrc[tok + 1][cg]) << 16);
     }
     __syncthreads();
@@ -495,7 +497,8 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                 mn1 = fmaxf(m1, bm1);
                 moved = true;
             }
-            const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
+            // rescale factors: 2^0 unless the running max moved
+            const float sc0 = moved ? fast_exp2(m0 - mn0) : 1.f, sc1 = moved ? fast_exp2(m1 - mn1) : 1.f;
             const float ad0 = -mn0, ad1 = -mn1;
             float pj[2][4];
 #pragma unroll
@@ -554,15 +557,19 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const uint4 vw4 = lds128(base + 1024 + (j * 32 + lane) * 16);
-                // (scale, zero) pairs: token pairs tq and tq + 4, channel groups 0..3
-                uint32_t vm[2][8];
+                // 2 x scale pairs: token pairs tq and tq + 4, channel groups 0..3
+                uint32_t vs[2][4];
 #pragma unroll
                 for (int hp = 0; hp < 2; ++hp) {
-                    const uint32_t a0 = base + 2560 + ((j * 8 + tq + 4 * hp) * 4) * 8;
-                    const uint4 x = lds128(a0), y = lds128(a0 + 16);
-                    vm[hp][0] = x.x; vm[hp][1] = x.y; vm[hp][2] = x.z; vm[hp][3] = x.w;
-                    vm[hp][4] = y.x; vm[hp][5] = y.y; vm[hp][6] = y.z; vm[hp][7] = y.w;
+                    const uint4 x = lds128(base + 2560 + ((j * 8 + tq + 4 * hp) * 4) * 4);
+                    vs[hp][0] = x.x; vs[hp][1] = x.y; vs[hp][2] = x.z; vs[hp][3] = x.w;
                 }
+                // zero pairs of channel group gq (A row gq; rows 4..15 zero):
+                // token pairs tq and tq + 4
+                const uint32_t za = base + 2816 + ((j * 8 + tq) * 4 + (gq & 3)) * 4;
+                uint32_t z0 = lds32(za), z2 = lds32(za + 4 * 4 * 4);
+                if (gq >= 4)
+                    z0 = z2 = 0;
                 if (j == 1) {
                     // every lane has read the tile: refill the stage
                     __syncwarp();
@@ -575,16 +582,10 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                         kissue_next(a, cur, nxt, have_nxt, c_in_nxt, c_grp, rg, ring_u32, bars[warp], lane);
                 }
                 const uint32_t vw[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
-                // zero pairs of channel group gq (A row gq; rows 4..15 zero):
-                // token pairs tq and tq + 4
-                const uint32_t za = base + 2560 + ((j * 8 + tq) * 4 + (gq & 3)) * 8 + 4;
-                uint32_t z0 = lds32(za), z2 = lds32(za + 4 * 4 * 8);
-                if (gq >= 4)
-                    z0 = z2 = 0;
 #pragma unroll
                 for (int cg = 0; cg < 4; ++cg) {
                     // P^T times 2 s_t (the tile holds 2s) of the channel group
-                    const uint32_t b0 = hmul2u(pb[j][0], vm[0][2 * cg]), b1 = hmul2u(pb[j][1], vm[1][2 * cg]);
+                    const uint32_t b0 = hmul2u(pb[j][0], vs[0][cg]), b1 = hmul2u(pb[j][1], vs[1][cg]);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int mt = 2 * cg + half;

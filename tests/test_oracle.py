@@ -793,11 +793,12 @@ def test_kivi_tile_layout_hand_offsets():
     assert km & 0xFFFF == s2[114] and km >> 16 == s2[122]
     assert np.array_equal(s2.view(np.float16).astype(np.float64), 2 * sk.astype(np.float64))
     # V meta: block 0, token pair 3, channel group 1 -> doubled scales of tokens 6, 7
-    vs = tile[640 + ((0 * 8 + 3) * 4 + 1) * 2]
+    vs = tile[640 + (0 * 8 + 3) * 4 + 1]
     v2 = (sv * np.float16(2)).view(np.uint16)
     assert vs & 0xFFFF == v2[6, 1] and vs >> 16 == v2[7, 1]
-    # V meta: block 1, token pair 5, channel group 2 -> zero of tokens 26, 27
-    vm = tile[640 + ((1 * 8 + 5) * 4 + 2) * 2 + 1]
+    # V meta: block 1, token pair 5, channel group 2 -> zero of tokens 26, 27 (zeros
+    # after the 64 words of scales)
+    vm = tile[640 + 64 + (1 * 8 + 5) * 4 + 2]
     assert vm & 0xFFFF == zv.view(np.uint16)[26, 2] and vm >> 16 == zv.view(np.uint16)[27, 2]
 
 
