@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
         for (int mt = 0; mt < 8; ++mt)
             o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         float zp[4] = {0.f, 0.f, 0.f, 0.f};      // zero term of the values: [channel group gq][heads h0, h1]
-        float m0 = -INFINITY, m1 = -INFINITY;
+        float m0 = -INFINITY, m1 = -INFINITY, r0 = -INFINITY, r1 = -INFINITY;
         // the weight sum of one block of one head per lane (see the reduction
         // below): lanes gq = 0, 2, 4, 6 of each column write the per-block
         // log2-sum-exp of block (gq & 4 ? 1 : 0) of head (gq & 2 ? h1 : h0)
@@ -482,31 +482,37 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
             // log2-sum-exps are taken against the same running max.  The
             // lanes' maxima are merged only when one of them exceeds the
             // running max (otherwise the running max stands)
+            // The maxima are compared in raw score units (r0, r1; m0, m1 are the
+            // same maxima in log2 units, r * scale_log2): rounding is monotonic,
+            // so this moves exactly when the log2-unit comparison would, and
+            // a group that does not move the max needs no scaling of it.
             const float lm0 = fmaxf(fmaxf(sj[0][0], sj[0][2]), fmaxf(sj[1][0], sj[1][2]));
             const float lm1 = fmaxf(fmaxf(sj[0][1], sj[0][3]), fmaxf(sj[1][1], sj[1][3]));
-            float bm0 = lm0 * scale_log2, bm1 = lm1 * scale_log2;     // scores in log2 units
-            float mn0 = m0, mn1 = m1;
+            float sc0 = 1.f, sc1 = 1.f;     // rescale factors: 2^0 unless the running max moved
             bool moved = false;
-            if (__any_sync(0xffffffffu, bm0 > m0 || bm1 > m1)) {
+            if (__any_sync(0xffffffffu, lm0 > r0 || lm1 > r1)) {
+                float b0 = lm0, b1 = lm1;
 #pragma unroll
                 for (int x = 4; x < 32; x <<= 1) {
-                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
-                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+                    b0 = fmaxf(b0, __shfl_xor_sync(0xffffffffu, b0, x));
+                    b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, x));
                 }
-                mn0 = fmaxf(m0, bm0);
-                mn1 = fmaxf(m1, bm1);
+                r0 = fmaxf(r0, b0);
+                r1 = fmaxf(r1, b1);
+                const float mn0 = r0 * scale_log2, mn1 = r1 * scale_log2;
+                sc0 = fast_exp2(m0 - mn0);
+                sc1 = fast_exp2(m1 - mn1);
+                m0 = mn0;
+                m1 = mn1;
                 moved = true;
             }
-            // rescale factors: 2^0 unless the running max moved
-            const float sc0 = moved ? fast_exp2(m0 - mn0) : 1.f, sc1 = moved ? fast_exp2(m1 - mn1) : 1.f;
-            const float ad0 = -mn0, ad1 = -mn1;
             float pj[2][4];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                pj[j][0] = fast_exp2(fmaf(sj[j][0], scale_log2, ad0));
-                pj[j][1] = fast_exp2(fmaf(sj[j][1], scale_log2, ad1));
-                pj[j][2] = fast_exp2(fmaf(sj[j][2], scale_log2, ad0));
-                pj[j][3] = fast_exp2(fmaf(sj[j][3], scale_log2, ad1));
+                pj[j][0] = fast_exp2(fmaf(sj[j][0], scale_log2, -m0));
+                pj[j][1] = fast_exp2(fmaf(sj[j][1], scale_log2, -m1));
+                pj[j][2] = fast_exp2(fmaf(sj[j][2], scale_log2, -m0));
+                pj[j][3] = fast_exp2(fmaf(sj[j][3], scale_log2, -m1));
             }
             uint32_t pb[2][2];
 #pragma unroll
@@ -527,13 +533,11 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
                 float v = wh ? k1 : k0;
                 v += __shfl_xor_sync(0xffffffffu, wh ? k0 : k1, 8);
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
-                const float mnw = wh ? mn1 : mn0;
+                const float mnw = wh ? m1 : m0;
                 lpart = lpart * (wh ? sc1 : sc0) + v;      // this lane's block of its head
                 if (lse_w)
                     lse_w[2 * gi] = mnw + fast_log2(v);
             }
-            m0 = mn0;
-            m1 = mn1;
             // the rescale only after a merge of the maxima (otherwise every
             // factor is 2^0); `moved` is the same in every lane
             if (moved) {
