@@ -367,8 +367,15 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt)
             o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float *lse_row0 = a.w.lse_blk + (static_cast<size_t>(it.l) * g.Hq + kvh * G + h0) * nb_total + it.lse0;
+        float m0 = -INFINITY, m1 = -INFINITY;
+        // each lane keeps the weight sum of one head (gq & 4 ? h1 : h0; see
+        // the reduction below); lanes gq = 0 and 4 write the per-block
+        // log2-sum-exps of heads h0 and h1
+        const bool wh = gq & 4;
+        float lpart = 0.f;
+        float *lse_w = nullptr;
+        if ((gq & 3) == 0 && (wh ? h1 : h0) < G)
+            lse_w = a.w.lse_blk + (static_cast<size_t>(it.l) * g.Hq + kvh * G + (wh ? h1 : h0)) * nb_total + it.lse0;
 
         for (uint32_t i = 0; i < it.nblk; ++i) {
             mbar_wait(smem_u32(&bars[warp][rg.st_cons]), rg.ph_cons, a.w.err);
@@ -439,12 +446,11 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
                 s[3] = tok1 < it.ntok ? s[3] : -INFINITY;
             }
 
-            float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
-#pragma unroll
-            for (int x = 4; x < 32; x <<= 1) {
-                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
-                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
-            }
+            // the lanes' maxima are merged only when one of them exceeds the
+            // running max; otherwise the running max stands and every rescale
+            // factor is 2^0 (the same values as merging, with less work)
+            const float lm0 = fmaxf(s[0], s[2]), lm1 = fmaxf(s[1], s[3]);
+            const bool moved = __any_sync(0xffffffffu, lm0 > m0 || lm1 > m1);
             // every lane has its K and V fragments: refill the stage
             __syncwarp();
             --rg.inflight;
@@ -455,32 +461,41 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
             if (rg.inflight < T::kRing)
                 issue_next<D, FP8>(&tmap, g, cur, nxt, have_nxt, c_in_nxt, c_blk, rg, ring_u32, bars[warp], lane);
 
-            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-            const float sc0 = fast_exp2(m0 - mn0), sc1 = fast_exp2(m1 - mn1);
-            const float p0 = fast_exp2(s[0] - mn0), p1 = fast_exp2(s[1] - mn1);
-            const float p2 = fast_exp2(s[2] - mn0), p3 = fast_exp2(s[3] - mn1);
-            float w0 = p0 + p2, w1 = p1 + p3;
+            float sc0 = 1.f, sc1 = 1.f;
+            if (moved) {
+                float bm0 = lm0, bm1 = lm1;
 #pragma unroll
-            for (int x = 4; x < 32; x <<= 1) {
-                w0 += __shfl_xor_sync(0xffffffffu, w0, x);
-                w1 += __shfl_xor_sync(0xffffffffu, w1, x);
-            }
-            l0 = l0 * sc0 + w0;
-            l1 = l1 * sc1 + w1;
-            m0 = mn0;
-            m1 = mn1;
-            if (gq == 0) {
-                if (h0 < G)
-                    lse_row0[i] = mn0 + fast_log2(w0);
-                if (h1 < G)
-                    lse_row0[nb_total + i] = mn1 + fast_log2(w1);
-            }
+                for (int x = 4; x < 32; x <<= 1) {
+                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+                }
+                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+                sc0 = fast_exp2(m0 - mn0);
+                sc1 = fast_exp2(m1 - mn1);
+                m0 = mn0;
+                m1 = mn1;
 #pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                o[mt][0] *= sc0;
-                o[mt][1] *= sc1;
-                o[mt][2] *= sc0;
-                o[mt][3] *= sc1;
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    o[mt][0] *= sc0;
+                    o[mt][1] *= sc1;
+                    o[mt][2] *= sc0;
+                    o[mt][3] *= sc1;
+                }
+            }
+            const float p0 = fast_exp2(s[0] - m0), p1 = fast_exp2(s[1] - m1);
+            const float p2 = fast_exp2(s[2] - m0), p3 = fast_exp2(s[3] - m1);
+            // the block's weight sums over the 8 lanes of each head's column,
+            // reduced transposed: lanes gq < 4 end with head h0's, gq >= 4
+            // with head h1's
+            {
+                const float w0 = p0 + p2, w1 = p1 + p3;
+                float v = wh ? w1 : w0;
+                v += __shfl_xor_sync(0xffffffffu, wh ? w0 : w1, 16);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                lpart = lpart * (wh ? sc1 : sc0) + v;
+                if (lse_w)
+                    lse_w[i] = (wh ? m1 : m0) + fast_log2(v);
             }
             // P^T as the B operand: transpose the two 8x8 16-bit tiles in registers
             const uint32_t pb0 = movmatrix_t(FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1));
@@ -518,6 +533,7 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
         }
 
         // ---- chunk partials ----------------------------------------------
+        const float l0 = lpart, l1 = __shfl_xor_sync(0xffffffffu, lpart, 16);   // in lane gq = 0
         const uint32_t part = it.part;
         if (gq == 0) {
             a.w.part_ml[part * kMaxGroup + h0] = make_float2(m0, l0);
