@@ -10,9 +10,9 @@
 //                     y = 0 merges the output, and the CTAs of the block
 //                     ranges turn the per-block log2-sum-exps of their range
 //                     into the stream's block masses
-//                     sum_h 2^(lse_blk(h, b) - LSE_h).  Streams of many
-//                     chunks give the merge a CTA of its own; with few
-//                     chunks CTA 0 also takes the first block range.
+//                     sum_h 2^(lse_blk(h, b) - LSE_h).  The merge has a
+//                     CTA of its own (the kernel can also give it to the
+//                     first range's CTA: split = 0).
 //   mass_kernel    -- M(b) = 1/(L*Hq) * sum over the L*Hkv streams, in a fixed
 //                     order (deterministic); when asked, the thread that
 //                     writes M(b) also scores block b's record (score_record:
@@ -191,11 +191,12 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
 cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq, uint32_t max_nb,
                            uint32_t max_nchunk, cudaStream_t s)
 {
-    // a merge of many chunks gets a CTA of its own; a short one shares CTA 0
-    // with the first block range (one CTA per stream while a sequence has at
-    // most kMassRange blocks: 8 per SM at 32 registers a thread, so that 640
-    // streams run in one wave)
-    const uint32_t split = max_nchunk > 32 ? 1u : 0u;
+    // the merge gets a CTA of its own, beside the block ranges' CTAs, so that
+    // the two dependent-load chains run at once (measured at 8K, 12-15
+    // chunks per stream: ~3 us less than one CTA doing both; 8 CTAs per SM at
+    // 32 registers a thread keep 1,280 of them in about one wave)
+    (void)max_nchunk;
+    const uint32_t split = 1u;
     const dim3 grid(nseq * g.L * g.Hkv, split + (max_nb + kMassRange - 1) / kMassRange);
     if (g.d == 128)
         return launch_pdl(combine_kernel<128>, grid, dim3(32 * kMaxGroup), 0, s, g, w, out, split);
