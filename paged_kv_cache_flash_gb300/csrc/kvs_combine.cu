@@ -11,8 +11,8 @@
 //                     ranges turn the per-block log2-sum-exps of their range
 //                     into the stream's block masses
 //                     sum_h 2^(lse_blk(h, b) - LSE_h).  The merge has a
-//                     CTA of its own (the kernel can also give it to the
-//                     first range's CTA: split = 0).
+//                     CTA of its own, or with many short streams shares the
+//                     first range's CTA (launch_combine decides).
 //   mass_kernel    -- M(b) = 1/(L*Hq) * sum over the L*Hkv streams, in a fixed
 //                     order (deterministic); when asked, the thread that
 //                     writes M(b) also scores block b's record (score_record:
@@ -189,14 +189,17 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
 }  // namespace
 
 cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq, uint32_t max_nb,
-                           uint32_t max_nchunk, cudaStream_t s)
+                           uint32_t max_nchunk, uint32_t sm_count, cudaStream_t s)
 {
-    // the merge gets a CTA of its own, beside the block ranges' CTAs, so that
-    // the two dependent-load chains run at once (measured at 8K, 12-15
-    // chunks per stream: ~3 us less than one CTA doing both; 8 CTAs per SM at
-    // 32 registers a thread keep 1,280 of them in about one wave)
-    (void)max_nchunk;
-    const uint32_t split = 1u;
+    // The merge gets a CTA of its own, beside the block ranges' CTAs, so that
+    // the two dependent-load chains run at once, when a stream's merge is long
+    // (more than 32 chunks) or when there are no more streams than CTAs fit
+    // at once (8 per SM at 32 registers a thread): measured ~3 us less at 8K
+    // (640 streams of 12-15 chunks).  With many short streams (the batched
+    // workload: 10,240) the extra CTAs only add waves (~10 us more), so the
+    // first range's CTA merges too.
+    const uint32_t nstreams = nseq * g.L * g.Hkv;
+    const uint32_t split = (max_nchunk > 32 || nstreams <= 8 * sm_count) ? 1u : 0u;
     const dim3 grid(nseq * g.L * g.Hkv, split + (max_nb + kMassRange - 1) / kMassRange);
     if (g.d == 128)
         return launch_pdl(combine_kernel<128>, grid, dim3(32 * kMaxGroup), 0, s, g, w, out, split);

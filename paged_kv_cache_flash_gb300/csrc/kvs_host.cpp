@@ -1258,7 +1258,8 @@ int decode_impl(kvs_ctx_t *ctx, const uint64_t *seq_ids, uint32_t nseq, const vo
         max_nb = std::max(max_nb, ds->seq[i].nb);
         max_nchunk = std::max(max_nchunk, ds->seq[i].nchunk);
     }
-    if ((rc = launch_rc(ctx, launch_combine(ctx->geo, ctx->work, out_dev, ds->nseq, max_nb, max_nchunk, s),
+    if ((rc = launch_rc(ctx, launch_combine(ctx->geo, ctx->work, out_dev, ds->nseq, max_nb, max_nchunk,
+                                            static_cast<uint32_t>(ctx->sm_count), s),
                         "combine")))
         return rc;
     const ScoreArgs sa = score_args(ctx);

@@ -18,7 +18,7 @@ cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w,
                           const uint16_t *q, const int32_t *table,
                           uint32_t n_items, uint32_t wg, int grid, cudaStream_t s);
 cudaError_t launch_combine(const Geo &g, const Work &w, float *out, uint32_t nseq,
-                           uint32_t max_nb, uint32_t max_nchunk, cudaStream_t s);
+                           uint32_t max_nb, uint32_t max_nchunk, uint32_t sm_count, cudaStream_t s);
 // Block masses into mass ([slot][mb]); with score != nullptr the kernel also
 // scores every block of the set (records updated as by launch_score).
 cudaError_t launch_mass(const Geo &g, const Work &w, float *mass, uint32_t nb_total, kvs_record *recs,

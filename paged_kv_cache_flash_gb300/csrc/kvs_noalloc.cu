@@ -118,7 +118,7 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
     if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return say(msg, msg_bytes, KVS_ECUDA, "no usable current device");
     uint8_t *base;
-    int grid_per_sm;
+    int grid_per_sm, sm_count;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_scratch_dev[dev]) {
@@ -140,6 +140,7 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
             return say(msg, msg_bytes, KVS_ECUDA, "decode kernel does not fit on an SM");
         base = static_cast<uint8_t *>(g_scratch_dev[dev]);
         grid_per_sm = per * g_sm_count[dev];
+        sm_count = g_sm_count[dev];
     }
 
     Work w{};
@@ -207,7 +208,7 @@ extern "C" int kvs_decode_noalloc(uint32_t num_layers, uint32_t num_q_heads, uin
                                                          static_cast<uint32_t>(grid_per_sm)));
     NA_CHECK(launch_decode(g, tmap, w, static_cast<const uint16_t *>(q), block_table, ds.n_items, wg,
                            grid, s));
-    NA_CHECK(launch_combine(g, w, out, 1, nb, nchunk, s));
+    NA_CHECK(launch_combine(g, w, out, 1, nb, nchunk, static_cast<uint32_t>(sm_count), s));
     NA_CHECK(launch_mass(g, w, mass, nb, nullptr, nullptr, s));
     if (status)     // error word and its first offending value, after the outputs
         NA_CHECK(cudaMemcpyAsync(status, w.err, 2 * sizeof(uint32_t), cudaMemcpyDeviceToDevice, s));

@@ -14,7 +14,7 @@ cudaError_t launch_append_step(const Geo &, const uint16_t *, const uint16_t *, 
 cudaError_t launch_append(const Geo &, const AppendArgs &, cudaStream_t) { return cudaErrorNoDevice; }
 cudaError_t launch_decode(const Geo &, const CUtensorMap &, const Work &, const uint16_t *, const int32_t *,
                           uint32_t, uint32_t, int, cudaStream_t) { return cudaErrorNoDevice; }
-cudaError_t launch_combine(const Geo &, const Work &, float *, uint32_t, uint32_t, uint32_t, cudaStream_t)
+cudaError_t launch_combine(const Geo &, const Work &, float *, uint32_t, uint32_t, uint32_t, uint32_t, cudaStream_t)
 { return cudaErrorNoDevice; }
 cudaError_t launch_mass(const Geo &, const Work &, float *, uint32_t, kvs_record *, const ScoreArgs *, cudaStream_t)
 { return cudaErrorNoDevice; }
