@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
         nb = ds->seq[ci].nb;
         seq_id = ds->seq[ci].seq_id;
         t = ds->t;
-        // the record: final before the decode kernel started (nothing between
-        // it and this kernel writes records)
+        // the record: written two or more launches ahead (token append,
+        // scoring of earlier steps); the decode and combine kernels write none
         if (score)
             rec = recs[static_cast<size_t>(slot) * g.mb + b];
     }
@@ -165,10 +165,21 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
     pdl_trigger();
     const uint32_t LS = g.L * g.Hkv;
     float acc = 0.f;
-    if (r < nb_total)
-#pragma unroll 4
-        for (uint32_t s = j; s < LS; s += kMassGroups)
+    if (r < nb_total) {
+        // the thread's first 16 streams in one round of loads, added in
+        // stream order (as the plain loop would), then any further ones
+        float v[16];
+#pragma unroll
+        for (uint32_t k = 0; k < 16; ++k) {
+            const uint32_t s = j + k * kMassGroups;
+            v[k] = s < LS ? w.stream_mass[static_cast<size_t>(s) * nb_total + r] : 0.f;
+        }
+#pragma unroll
+        for (uint32_t k = 0; k < 16; ++k)
+            acc += v[k];
+        for (uint32_t s = j + 16 * kMassGroups; s < LS; s += kMassGroups)
             acc += w.stream_mass[static_cast<size_t>(s) * nb_total + r];
+    }
     part[j][i] = acc;
     __syncthreads();
 #pragma unroll

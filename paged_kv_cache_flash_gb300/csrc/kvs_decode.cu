@@ -230,10 +230,6 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[8][kStages];
 
-    // the combine kernel (a programmatic dependent) may place its CTAs beside
-    // this persistent grid now: they wait for its completion, and start at
-    // once when it completes
-    pdl_trigger();
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -245,6 +241,13 @@ __global__ void __launch_bounds__(128, Tile<D, FP8>::kMinCtas)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncwarp();
+    // launched as a programmatic dependent of the decode-set upload: the CTAs
+    // are placed while it runs, and nothing in global memory is touched
+    // before it has completed.  Then the combine kernel (the next dependent)
+    // may place its CTAs beside this persistent grid: they wait for its
+    // completion, and start at once when it completes
+    pdl_wait();
+    pdl_trigger();
 
     const Geo &g = a.g;
     const uint32_t G = g.G;
@@ -614,12 +617,10 @@ cudaError_t launch_decode(const Geo &g, const CUtensorMap &tmap, const Work &w, 
     DecodeArgs a{g, w, q, table, n_items, wg};
     const size_t smem = decode_smem_bytes(g, wg);
     if (g.fp8)
-        decode_kernel<128, true><<<grid, 32 * wg, smem, s>>>(tmap, a);
-    else if (g.d == 128)
-        decode_kernel<128, false><<<grid, 32 * wg, smem, s>>>(tmap, a);
-    else
-        decode_kernel<64, false><<<grid, 32 * wg, smem, s>>>(tmap, a);
-    return cudaGetLastError();
+        return launch_pdl(decode_kernel<128, true>, dim3(grid), dim3(32 * wg), smem, s, tmap, a);
+    if (g.d == 128)
+        return launch_pdl(decode_kernel<128, false>, dim3(grid), dim3(32 * wg), smem, s, tmap, a);
+    return launch_pdl(decode_kernel<64, false>, dim3(grid), dim3(32 * wg), smem, s, tmap, a);
 }
 
 }  // namespace kvs

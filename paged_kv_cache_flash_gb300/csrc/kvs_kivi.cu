@@ -364,7 +364,6 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
 {
     extern __shared__ __align__(1024) uint8_t ksm_raw[];
     __shared__ __align__(8) uint64_t bars[kKWarps][kKRing];
-    pdl_trigger();              // lets a programmatically dependent combine place its CTAs
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ksm_raw) + 127) & ~uintptr_t(127));
     const uint32_t ring_u32 = smem_u32(smem + warp * kKRing * kTile);
@@ -375,6 +374,11 @@ __global__ void __launch_bounds__(32 * kKWarps, kKMinCtas) decode_kivi_kernel(co
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncwarp();
+    // a programmatic dependent, as the page decode: nothing in global memory
+    // before the kernel ahead has completed; then the next kernel (the page
+    // decode of the residual, or the combine) may place its CTAs
+    pdl_wait();
+    pdl_trigger();
 
     const Geo &g = a.g;
     const uint32_t G = g.G;
@@ -684,8 +688,7 @@ cudaError_t launch_decode_kivi(const Geo &g, const Work &w, const uint16_t *q, c
         return cudaSuccess;
     KArgs a{g, w, q, table, gpool, n_items};
     const int need = static_cast<int>((n_items + kKWarps - 1) / kKWarps);
-    decode_kivi_kernel<<<need < grid ? need : grid, 32 * kKWarps, kKSmem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_kivi_kernel, dim3(need < grid ? need : grid), dim3(32 * kKWarps), kKSmem, s, a);
 }
 
 }  // namespace kvs

@@ -1,26 +1,29 @@
-// Programmatic dependent launch for the short kernels of a step: the token
-// append and the decode-set upload ahead of the decode kernel, and block
-// mass, scoring, selection, gather plan and mirror copy after it.
+// Programmatic dependent launch for the kernels of a step: the token append,
+// the decode-set upload, the decode kernels, and block mass, scoring,
+// selection, gather plan and mirror copy after them.
 //
 // A kernel launched with launch_pdl() may be scheduled while the kernel
 // before it in the stream is still running: its CTAs start, do what depends
 // on nothing that kernel writes, and block in pdl_wait() until that kernel
 // has completed and its memory is visible.  This hides the launch and ramp
-// of each short kernel behind the tail of the previous one.  Rules every
-// kernel launched this way follows:
+// of each kernel behind the tail of the previous one.  Rules every kernel
+// launched this way follows:
 //   - every thread calls pdl_wait() before it reads or writes memory that an
 //     earlier kernel of the stream may still write, and before it exits (so
 //     that the grid completes only after its predecessor has, which keeps
 //     the ordering transitive along the chain);
-//   - before pdl_wait() it reads only data that was final before the last
-//     normally-launched kernel ahead of it started: the decode set and the
-//     block records, final before the decode kernel (a normal launch) starts.
-//     The set upload and the token append are launched this way too, but
-//     touch memory only after their own pdl_wait(), and a normally-launched
-//     kernel (the decode kernel, or the mass copy of a debug set) follows
-//     every set upload before anything reads the set.
-// The decode kernels trigger their dependents at their start, so that the
-// combine kernel's CTAs are in place when the decode completes.
+//   - a kernel triggers its dependents (pdl_trigger) only after its own
+//     pdl_wait() has returned, so that when a kernel starts, every kernel two
+//     or more launches ahead of it has completed.  The one exception is the
+//     set upload, which triggers at its start; the kernel after it (a decode
+//     kernel, or a plain launch) touches no memory before its own wait;
+//   - before pdl_wait() a kernel reads only data written two or more launches
+//     ahead of it: the decode set and the block records, read early by the
+//     combine, mass and selection kernels, are written by the set upload, the
+//     token append, the scoring of earlier steps and plain launches (record
+//     patches), never by the decode kernels or the kernels after them.
+// The decode kernels trigger right after their wait, so that the combine
+// kernel's CTAs are in place when the decode completes.
 // After a copy or an event in the stream the attribute has no effect: the
 // kernel starts after everything before it, as a plain launch would.
 #pragma once
