@@ -378,9 +378,14 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args,
                           kvs_gather_result *res);
 
 /* Counts of the latest KVS_GATHER_ASYNC select: waits (bounded, KVS_ETIMEOUT)
- * until that call's work on its stream has reached them, then fills *res as
- * a synchronous call would have (n_demoted = 0).  KVS_EINVAL if no
- * asynchronous select was made on this context. */
+ * until that call's work on its stream has reached them -- with MIRROR, until
+ * its page copies are visible in the host mirror -- then fills *res as a
+ * synchronous call would have (n_demoted = 0).  A MIRROR call signals this
+ * through a pinned word its last kernel writes, not through a stream event,
+ * so that nothing in the stream separates it from the next kernels; the
+ * stream must stay alive until the counts are read.  KVS_ECUDA if the stream
+ * fails meanwhile, KVS_EDEVICE if it drains without the signal.  KVS_EINVAL
+ * if no asynchronous select was made on this context. */
 int kvs_gather_counts(kvs_ctx_t *ctx, kvs_gather_result *res);
 
 /* Re-admits demoted blocks [GQA]: for each key, takes a page from the free

@@ -1032,9 +1032,17 @@ __global__ void __launch_bounds__(256)
 // into the host mirror through its device mapping: pool page p to host page
 // p.  Every CTA takes its slice of every page (no division per element); an
 // id outside the pool is flagged and skipped.
+//
+// Completion goes to the host through pinned memory, not a stream event
+// (an event between this kernel and the next step's first kernel would make
+// that a plain launch): hdr[0..3] receive the counts plan[0..2] and 0, then
+// hdr[4] the call's sequence number, once every copy of the call is visible
+// to the host.  The copying threads fence at system scope and their CTAs
+// count themselves on plan[3] (0 from the plan kernel); the CTA that
+// arrives last publishes.  With nothing to copy CTA 0 publishes at once.
 __global__ void __launch_bounds__(256)
-    mirror_copy_kernel(const uint4 *pool, const uint32_t *plan, uint4 *host, uint64_t page_vec,
-                       uint32_t pool_blocks, uint32_t *err, uint32_t *err_info)
+    mirror_copy_kernel(const uint4 *pool, uint32_t *plan, uint4 *host, uint64_t page_vec,
+                       uint32_t pool_blocks, uint32_t *err, uint32_t *err_info, uint32_t *hdr, uint32_t seq)
 {
     pdl_wait();                 // the copy list comes from the plan kernel
     pdl_trigger();
@@ -1063,6 +1071,28 @@ __global__ void __launch_bounds__(256)
         }
         for (; i < page_vec; i += stride)
             dst[i] = __ldcs(src + i);
+    }
+    if (!hdr)
+        return;                 // uniform over the grid
+    if (n)
+        __threadfence_system(); // this thread's host writes, before its CTA arrives
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        bool last = blockIdx.x == 0;
+        if (n) {
+            __threadfence_system();
+            last = atomicAdd(plan + 3, 1u) == gridDim.x - 1;
+        }
+        if (last) {
+            __threadfence_system();     // every CTA's copies before the counts and the tag
+            volatile uint32_t *h = hdr;
+            h[0] = plan[0];
+            h[1] = plan[1];
+            h[2] = n;
+            h[3] = 0;
+            __threadfence_system();
+            h[4] = seq;
+        }
     }
 }
 
@@ -1224,11 +1254,11 @@ cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pag
 }
 
 cudaError_t launch_mirror_copy(const Geo &g, const Work &w, const uint16_t *pool, void *host_dev,
-                               uint32_t pool_blocks, int grid, cudaStream_t s)
+                               uint32_t pool_blocks, int grid, uint32_t *hdr_dev, uint32_t seq, cudaStream_t s)
 {
     return launch_pdl(mirror_copy_kernel, dim3(grid), dim3(256), 0, s, reinterpret_cast<const uint4 *>(pool),
-                      static_cast<const uint32_t *>(w.readback), reinterpret_cast<uint4 *>(host_dev),
-                      static_cast<uint64_t>(g.page_bytes / 16), pool_blocks, w.err, w.err_info);
+                      w.readback, reinterpret_cast<uint4 *>(host_dev), static_cast<uint64_t>(g.page_bytes / 16),
+                      pool_blocks, w.err, w.err_info, hdr_dev, seq);
 }
 
 cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *pages, uint32_t npages,

@@ -15,7 +15,8 @@
 //                     first range's CTA (launch_combine decides).
 //   mass_kernel    -- M(b) = 1/(L*Hq) * sum over the L*Hkv streams, in a fixed
 //                     order (deterministic); when asked, the thread that
-//                     writes M(b) also scores block b's record (score_record:
+//                     writes M(b) also scores block b's record (score_prep
+//                     before the kernel's wait, score_finish after it:
 //                     the aggregated mass lands in the 64-byte record).
 // Both are launched as programmatic dependents (kvs_pdl.cuh).
 #include <type_traits>
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
     uint32_t slot = 0, b = 0, nb = 0;
     uint64_t seq_id = 0, t = 0;
     kvs_record rec;
+    ScorePrep prep;
     if (r < nb_total && j == 0) {       // the decode set: uploaded before the decode kernel
         const uint32_t ci = find_seq(&ds->seq[0].blk_off, sizeof(DSeq) / 4, ds->nseq, r);
         slot = ds->seq[ci].slot;
@@ -157,9 +159,13 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
         seq_id = ds->seq[ci].seq_id;
         t = ds->t;
         // the record: written two or more launches ahead (token append,
-        // scoring of earlier steps); the decode and combine kernels write none
-        if (score)
+        // scoring of earlier steps); the decode and combine kernels write
+        // none.  Its mass-free scoring terms (fp64: the decay, the recency
+        // division) are taken here, while the combine still runs
+        if (score) {
             rec = recs[static_cast<size_t>(slot) * g.mb + b];
+            prep = score_prep(sa, rec, seq_id, b, nb, t);
+        }
     }
     pdl_wait();
     pdl_trigger();
@@ -193,7 +199,7 @@ __global__ void __launch_bounds__(1024) mass_kernel(const Geo g, const Work w, f
         const float M = part[0][i] / static_cast<float>(g.L * g.Hq);
         mass[idx] = M;
         if (score)
-            score_loaded(sa, rec, recs + idx, seq_id, b, nb, t, M, w.err);
+            score_finish(sa, prep, rec, recs + idx, nb, t, M, w.err);
     }
 }
 

@@ -104,9 +104,12 @@ struct kvs_ctx {
     bool ring_used[kRingSlots]{};
     uint32_t ring_next = 0;
     uint32_t *pinned_small = nullptr;               // readbacks
-    uint32_t *async_hdr = nullptr;                  // counts of the latest ASYNC select
+    uint32_t *async_hdr = nullptr;                  // counts of the latest ASYNC select, [4]: its tag
     uint32_t *async_hdr_dev = nullptr;              // ... its device mapping (kernels write it)
-    cudaEvent_t ev_async{};                         // ... on the host after this event
+    cudaEvent_t ev_async{};                         // ... on the host after this event, or
+    uint32_t async_seq = 0;                         // ... once async_hdr[4] holds this number
+    bool async_tagged = false;                      //     (mirror selects: no event in the stream)
+    cudaStream_t async_stream{};                    //     written by a kernel on this stream
     int async_kind = 0;                             // 0 none yet, 1 mirror, 2 ids only
 
     cudaEvent_t ev_ready[2]{}, ev_side_done{}, ev_pool_release{};
@@ -188,6 +191,33 @@ int event_wait(kvs_ctx *ctx, cudaEvent_t ev, const char *what)
             return KVS_OK;
         if (e != cudaErrorNotReady)
             return fail(ctx, KVS_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+        if (std::chrono::steady_clock::now() - t0 > limit)
+            return fail(ctx, KVS_ETIMEOUT, "%s: no completion within %u ms", what, g_wait_limit_ms.load());
+        if (spin > 256)
+            std::this_thread::yield();
+    }
+}
+
+// Waits, as event_wait does, until a kernel enqueued on stream s has written
+// `seq` into the pinned word *tag (acquire: what the kernel wrote before it is
+// visible after).  The stream is queried now and then (a query is not a
+// stream operation): an error on it ends the wait, and so does a stream that
+// has drained without the tag.
+int tag_wait(kvs_ctx *ctx, const uint32_t *tag, uint32_t seq, cudaStream_t s, const char *what)
+{
+    const auto t0 = std::chrono::steady_clock::now();
+    const auto limit = std::chrono::milliseconds(g_wait_limit_ms.load());
+    const bool faked = g_faults.load() & KVS_FAULT_WAIT;
+    for (uint32_t spin = 0;; ++spin) {
+        if (!faked && __atomic_load_n(tag, __ATOMIC_ACQUIRE) == seq)
+            return KVS_OK;
+        if (!faked && (spin & 255u) == 255u) {
+            const cudaError_t e = cudaStreamQuery(s);
+            if (e == cudaSuccess && __atomic_load_n(tag, __ATOMIC_ACQUIRE) != seq)
+                return fail(ctx, KVS_EDEVICE, "%s: the stream drained without the completion word", what);
+            if (e != cudaSuccess && e != cudaErrorNotReady)
+                return fail(ctx, KVS_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+        }
         if (std::chrono::steady_clock::now() - t0 > limit)
             return fail(ctx, KVS_ETIMEOUT, "%s: no completion within %u ms", what, g_wait_limit_ms.load());
         if (spin > 256)
@@ -839,6 +869,7 @@ int kvs_create(const kvs_config *cfg, const kvs_buffers *buf, kvs_ctx_t **out)
     CU(cudaEventCreateWithFlags(&ctx->ev_wait, cudaEventDisableTiming));
     CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->pinned_small), kReadbackBytes, cudaHostAllocDefault));
     CU(cudaHostAlloc(reinterpret_cast<void **>(&ctx->async_hdr), 64, cudaHostAllocMapped));
+    std::memset(ctx->async_hdr, 0, 64);
     CU(cudaHostGetDevicePointer(reinterpret_cast<void **>(&ctx->async_hdr_dev), ctx->async_hdr, 0));
     CU(cudaEventCreateWithFlags(&ctx->ev_async, cudaEventDisableTiming));
     for (auto &e : ctx->ring_ev)
@@ -1433,6 +1464,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             return rc;
         if (ctx->geo.kivi && async) {
             CU(cudaEventRecord(ctx->ev_async, s));
+            ctx->async_tagged = false;
             ctx->async_kind = 2;
             return KVS_OK;
         }
@@ -1461,12 +1493,19 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
             // the stale pages go to the host mirror by a device kernel in
             // stream order (writers after it need no wait); the plan kernel
             // wrote the counts into pinned memory, read by kvs_gather_counts
+            // ... and, once those copies are visible here, the counts and
+            // the call's number into async_hdr: no event in the stream, so
+            // the next step's first kernel still launches programmatically
+            const uint32_t seq = ctx->async_seq + 1;
             if ((rc = launch_rc(ctx,
                                 launch_mirror_copy(ctx->geo, w, static_cast<const uint16_t *>(ctx->buf.pool),
-                                                   host_dev, ctx->cfg.pool_blocks, 2 * ctx->sm_count, s),
+                                                   host_dev, ctx->cfg.pool_blocks, 2 * ctx->sm_count,
+                                                   ctx->async_hdr_dev, seq, s),
                                 "mirror copy")))
                 return rc;
-            CU(cudaEventRecord(ctx->ev_async, s));
+            ctx->async_seq = seq;
+            ctx->async_tagged = true;
+            ctx->async_stream = s;
             ctx->async_kind = 1;
             return KVS_OK;
         }
@@ -1490,6 +1529,7 @@ int kvs_select_and_gather(kvs_ctx_t *ctx, const kvs_gather_args *args, kvs_gathe
         CU(cudaMemsetAsync(w.readback, 0, 16, s));
         CU(cudaMemcpyAsync(ctx->async_hdr, w.readback, 16, cudaMemcpyDeviceToHost, s));
         CU(cudaEventRecord(ctx->ev_async, s));
+        ctx->async_tagged = false;
         ctx->async_kind = ctx->geo.kivi ? 2 : 1;
         return KVS_OK;
     }
@@ -1653,7 +1693,9 @@ int kvs_gather_counts(kvs_ctx_t *ctx, kvs_gather_result *res)
     std::memset(res, 0, sizeof *res);
     if (!ctx->async_kind)
         return fail(ctx, KVS_EINVAL, "no asynchronous select on this context");
-    if (int rc = event_wait(ctx, ctx->ev_async, "kvs_gather_counts"))
+    if (int rc = ctx->async_tagged ? tag_wait(ctx, ctx->async_hdr + 4, ctx->async_seq, ctx->async_stream,
+                                              "kvs_gather_counts")
+                                   : event_wait(ctx, ctx->ev_async, "kvs_gather_counts"))
         return rc;
     res->n_selected = ctx->async_hdr[0];
     if (ctx->async_kind == 1) {

@@ -43,8 +43,10 @@ cudaError_t launch_select_plan(const Geo &g, const Work &w, const kvs_record *re
 cudaError_t launch_plan(const Work &w, uint32_t mirror, const SelectOut &out, cudaStream_t s);
 cudaError_t launch_scatter(const Geo &g, const uint8_t *staging, const int32_t *pages, uint32_t npages,
                            uint16_t *pool, cudaStream_t s);
+// hdr_dev: pinned, mapped words [0..4] that receive the counts and then seq
+// once the copies are visible to the host (null: no completion word)
 cudaError_t launch_mirror_copy(const Geo &g, const Work &w, const uint16_t *pool, void *host_dev,
-                               uint32_t pool_blocks, int grid, cudaStream_t s);
+                               uint32_t pool_blocks, int grid, uint32_t *hdr_dev, uint32_t seq, cudaStream_t s);
 cudaError_t launch_gather(const Geo &g, const uint16_t *pool, const int32_t *pages,
                           uint32_t npages, uint8_t *staging, cudaStream_t s);
 // bytes (<= kSetInlineBytes) from host memory src to device memory dst, in

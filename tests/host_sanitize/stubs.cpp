@@ -31,7 +31,8 @@ cudaError_t launch_select_plan(const Geo &, const Work &, const kvs_record *, co
 cudaError_t launch_plan(const Work &, uint32_t, const SelectOut &, cudaStream_t) { return cudaErrorNoDevice; }
 cudaError_t launch_scatter(const Geo &, const uint8_t *, const int32_t *, uint32_t, uint16_t *, cudaStream_t)
 { return cudaErrorNoDevice; }
-cudaError_t launch_mirror_copy(const Geo &, const Work &, const uint16_t *, void *, uint32_t, int, cudaStream_t)
+cudaError_t launch_mirror_copy(const Geo &, const Work &, const uint16_t *, void *, uint32_t, int, uint32_t *, uint32_t,
+                               cudaStream_t)
 { return cudaErrorNoDevice; }
 cudaError_t launch_gather(const Geo &, const uint16_t *, const int32_t *, uint32_t, uint8_t *, cudaStream_t)
 { return cudaErrorNoDevice; }
