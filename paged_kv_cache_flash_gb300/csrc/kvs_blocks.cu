@@ -1084,7 +1084,8 @@ __global__ void __launch_bounds__(256)
             last = atomicAdd(plan + 3, 1u) == gridDim.x - 1;
         }
         if (last) {
-            __threadfence_system();     // every CTA's copies before the counts and the tag
+            if (n)
+                __threadfence_system(); // every CTA's copies before the counts and the tag
             volatile uint32_t *h = hdr;
             h[0] = plan[0];
             h[1] = plan[1];
